@@ -1,0 +1,249 @@
+"""ctypes wrapper around the single-threaded C++ oracle of the NVFP4 MoE layer.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this module; the product library never does, and the two share no code.
+Every function here only marshals numpy arrays into the C routines of ``moe_oracle.cpp``.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.cpp")
+_LIB_PATH = os.path.join(_HERE, "liboracle_moe.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with g++ (-ffp-contract=off: no fused multiply-add anywhere)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["g++", "-O2", "-std=c++17", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+               "-o", tmp, _SRC]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class Expert(C.Structure):
+    _fields_ = [("codes", C.c_void_p * 3), ("sf", C.c_void_p * 3), ("ts", C.c_float * 3)]
+
+
+class MoeArgs(C.Structure):
+    _fields_ = [("T", C.c_int64), ("H", C.c_int32), ("I", C.c_int32), ("E", C.c_int32),
+                ("k", C.c_int32), ("has_shared", C.c_int32), ("I_shared", C.c_int32),
+                ("ts_h", C.c_float), ("xq", C.c_void_p), ("xsf", C.c_void_p), ("ts_a", C.c_float),
+                ("logits", C.c_void_p), ("experts", C.c_void_p), ("y", C.c_void_p),
+                ("ids", C.c_void_p), ("w", C.c_void_p), ("counts", C.c_void_p),
+                ("offsets", C.c_void_p), ("perm_src", C.c_void_p), ("inv", C.c_void_p),
+                ("hq", C.c_void_p), ("hsf", C.c_void_p), ("shq", C.c_void_p), ("shsf", C.c_void_p)]
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = C.CDLL(_LIB_PATH)
+        L.orc_bf16_to_f32.restype = C.c_float
+        L.orc_bf16_to_f32.argtypes = [C.c_uint16]
+        L.orc_f32_to_bf16.restype = C.c_uint16
+        L.orc_f32_to_bf16.argtypes = [C.c_float]
+        L.orc_e2m1_decode.restype = C.c_float
+        L.orc_e2m1_decode.argtypes = [C.c_uint8]
+        L.orc_e2m1_encode.restype = C.c_uint8
+        L.orc_e2m1_encode.argtypes = [C.c_float]
+        L.orc_e4m3_decode.restype = C.c_float
+        L.orc_e4m3_decode.argtypes = [C.c_uint8]
+        L.orc_e4m3_encode.restype = C.c_uint8
+        L.orc_e4m3_encode.argtypes = [C.c_float]
+        L.orc_quantize_f32.restype = None
+        L.orc_quantize_f32.argtypes = [C.c_void_p, C.c_int64, C.c_int64, C.c_float, C.c_void_p, C.c_void_p]
+        L.orc_tensor_scale_bf16.restype = C.c_float
+        L.orc_tensor_scale_bf16.argtypes = [C.c_void_p, C.c_int64]
+        L.orc_quantize_bf16.restype = C.c_int
+        L.orc_quantize_bf16.argtypes = [C.c_void_p, C.c_int64, C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p]
+        L.orc_dequantize.restype = None
+        L.orc_dequantize.argtypes = [C.c_void_p, C.c_void_p, C.c_float, C.c_int64, C.c_int64, C.c_void_p]
+        L.orc_router.restype = None
+        L.orc_router.argtypes = [C.c_void_p, C.c_int64, C.c_int, C.c_int, C.c_void_p, C.c_void_p]
+        L.orc_plan.restype = None
+        L.orc_plan.argtypes = [C.c_void_p, C.c_int64, C.c_int, C.c_int] + [C.c_void_p] * 4
+        L.orc_moe_forward.restype = C.c_int
+        L.orc_moe_forward.argtypes = [C.POINTER(MoeArgs)]
+        L.orc_moe_forward_bruteforce.restype = C.c_int
+        L.orc_moe_forward_bruteforce.argtypes = [C.POINTER(MoeArgs)]
+        _lib = L
+    return _lib
+
+
+def _p(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+# ----------------------------------------------------------------------------- scalar codecs
+def e2m1_decode(code: int) -> float:
+    return float(lib().orc_e2m1_decode(code))
+
+
+def e2m1_encode(q: float) -> int:
+    return int(lib().orc_e2m1_encode(q))
+
+
+def e4m3_decode(code: int) -> float:
+    return float(lib().orc_e4m3_decode(code))
+
+
+def e4m3_encode(v: float) -> int:
+    return int(lib().orc_e4m3_encode(v))
+
+
+def f32_to_bf16_bits(v: float) -> int:
+    return int(lib().orc_f32_to_bf16(v))
+
+
+# ----------------------------------------------------------------------------- quantisation
+def as_bf16_bits(x) -> np.ndarray:
+    """A torch BF16 tensor or a uint16 array -> contiguous uint16 bit patterns."""
+    if hasattr(x, "view") and hasattr(x, "dtype") and str(x.dtype) == "torch.bfloat16":
+        import torch
+        return np.ascontiguousarray(x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+    return np.ascontiguousarray(np.asarray(x, dtype=np.uint16))
+
+
+def quantize_bf16(x):
+    """BF16 [rows, cols] -> (codes uint8 [rows, cols/2], sf uint8 [rows, cols/16], ts float, status)."""
+    xb = as_bf16_bits(x)
+    rows, cols = xb.shape
+    codes = np.zeros((rows, cols // 2), np.uint8)
+    sf = np.zeros((rows, cols // 16), np.uint8)
+    ts = C.c_float(0)
+    st = lib().orc_quantize_bf16(_p(xb), rows, cols, _p(codes), _p(sf), C.byref(ts))
+    return codes, sf, float(np.float32(ts.value)), st
+
+
+def quantize_f32(x: np.ndarray, ts: float):
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    rows, cols = x.shape
+    codes = np.zeros((rows, cols // 2), np.uint8)
+    sf = np.zeros((rows, cols // 16), np.uint8)
+    lib().orc_quantize_f32(_p(x), rows, cols, ts, _p(codes), _p(sf))
+    return codes, sf
+
+
+def tensor_scale_bf16(x) -> float:
+    xb = as_bf16_bits(x)
+    return float(np.float32(lib().orc_tensor_scale_bf16(_p(xb), xb.size)))
+
+
+def dequantize(codes: np.ndarray, sf: np.ndarray, ts: float) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, np.uint8)
+    sf = np.ascontiguousarray(sf, np.uint8)
+    rows, cols = codes.shape[0], codes.shape[1] * 2
+    out = np.zeros((rows, cols), np.float32)
+    lib().orc_dequantize(_p(codes), _p(sf), ts, rows, cols, _p(out))
+    return out
+
+
+# ----------------------------------------------------------------------------- routing
+def router(logits: np.ndarray, k: int):
+    logits = np.ascontiguousarray(logits, np.float32)
+    T, E = logits.shape
+    ids = np.zeros((T, k), np.int32)
+    w = np.zeros((T, k), np.float32)
+    lib().orc_router(_p(logits), T, E, k, _p(ids), _p(w))
+    return ids, w
+
+
+def plan(ids: np.ndarray, E: int):
+    ids = np.ascontiguousarray(ids, np.int32)
+    T, k = ids.shape
+    counts = np.zeros(E, np.int32)
+    offsets = np.zeros(E + 1, np.int32)
+    perm_src = np.zeros(T * k, np.int32)
+    inv = np.zeros(T * k, np.int32)
+    lib().orc_plan(_p(ids), T, E, k, _p(counts), _p(offsets), _p(perm_src), _p(inv))
+    return counts, offsets, perm_src, inv
+
+
+# ----------------------------------------------------------------------------- the layer
+class QuantExpert:
+    """Canonical NVFP4 weights of one expert: gate/up [I,H], down [H,I] codes + scales + ts."""
+
+    def __init__(self, codes, sf, ts):
+        self.codes = [np.ascontiguousarray(c, np.uint8) for c in codes]
+        self.sf = [np.ascontiguousarray(s, np.uint8) for s in sf]
+        self.ts = [float(t) for t in ts]
+
+    @classmethod
+    def from_bf16(cls, gate, up, down):
+        cs, ss, ts = [], [], []
+        for w in (gate, up, down):
+            c, s, t, st = quantize_bf16(w)
+            if st != 0:
+                raise ValueError("non-finite weight")
+            cs.append(c), ss.append(s), ts.append(t)
+        return cls(cs, ss, ts)
+
+
+def moe_forward(xq, xsf, ts_a, logits, experts, k, ts_h=1.0, shared=None, bruteforce=False,
+                want_debug=False):
+    """The layer on quantised activations.  ``experts`` is a list of length E whose entries are
+    QuantExpert or None (None only for experts no token routes to); ``shared`` a QuantExpert."""
+    xq = np.ascontiguousarray(xq, np.uint8)
+    xsf = np.ascontiguousarray(xsf, np.uint8)
+    logits = np.ascontiguousarray(logits, np.float32)
+    T, E = logits.shape
+    H = xq.shape[1] * 2
+    I = None
+    for ex in experts:
+        if ex is not None:
+            I = ex.codes[0].shape[0]
+            break
+    if I is None:
+        I = 16
+    Is = shared.codes[0].shape[0] if shared is not None else 0
+    table = (Expert * (E + (1 if shared is not None else 0)))()
+    keep = []
+    for i, ex in enumerate(list(experts) + ([shared] if shared is not None else [])):
+        if ex is None:
+            continue
+        for m in range(3):
+            table[i].codes[m] = _p(ex.codes[m])
+            table[i].sf[m] = _p(ex.sf[m])
+            table[i].ts[m] = ex.ts[m]
+        keep.append(ex)
+    y = np.zeros((T, H), np.uint16)
+    a = MoeArgs()
+    a.T, a.H, a.I, a.E, a.k = T, H, I, E, k
+    a.has_shared = 1 if shared is not None else 0
+    a.I_shared = Is
+    a.ts_h = ts_h
+    a.xq, a.xsf, a.ts_a = _p(xq), _p(xsf), ts_a
+    a.logits = _p(logits)
+    a.experts = C.cast(table, C.c_void_p)
+    a.y = _p(y)
+    dbg = {}
+    if want_debug and not bruteforce:
+        dbg = dict(ids=np.zeros((T, k), np.int32), w=np.zeros((T, k), np.float32),
+                   counts=np.zeros(E, np.int32), offsets=np.zeros(E + 1, np.int32),
+                   perm_src=np.zeros(T * k, np.int32), inv=np.zeros(T * k, np.int32),
+                   hq=np.zeros((T * k, I // 2), np.uint8), hsf=np.zeros((T * k, I // 16), np.uint8))
+        if shared is not None:
+            dbg["shq"] = np.zeros((T, Is // 2), np.uint8)
+            dbg["shsf"] = np.zeros((T, Is // 16), np.uint8)
+        for name, arr in dbg.items():
+            setattr(a, name, _p(arr))
+    fn = lib().orc_moe_forward_bruteforce if bruteforce else lib().orc_moe_forward
+    st = fn(C.byref(a))
+    if st != 0:
+        raise RuntimeError(f"oracle status {st}")
+    return (y, dbg) if want_debug else y
+
+
+def bf16_bits_to_f32(y: np.ndarray) -> np.ndarray:
+    return (np.asarray(y, np.uint32) << 16).view(np.float32)
