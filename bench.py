@@ -1,0 +1,445 @@
+#!/usr/bin/env python
+"""Throughput of the fused NVFP4 MoE layer on GB300.
+
+Workload (default "decode"): H=2048, E=128 experts, top-8, I=768, SwiGLU, x ~ N(0,1) BF16, router
+logits ~ N(0,1) ("uniform routing"), weights ~ N(0,0.02) NVFP4-quantised; the layer is run at
+T in {1, 8, 32, 64} tokens.  One step = one layer call (moe_run) at T = (1, 8, 32, 64)[step % 4];
+the L2 cache is flushed (a write of 2x its size) before every call, outside the timed events, so
+each call reads its weights from HBM as a layer of a real model does.  Inputs are resident in
+HBM before the timed region.  Metric: tokens/s (+ effective TFLOPS and %% of HBM bandwidth).
+
+Multi-GPU (torchrun): the layer does not shard across GPUs here, so each rank runs an
+independent replica on its own GPU (weak scaling); timing is the max over ranks.
+
+--impl reference times the CPU oracle (the plain single-threaded C++ implementation the tests
+check against) on the host cores, on a bounded token sample of every step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "NVFP4 MoE tokens/s & eff. TFLOPS; % of HBM BW (decode) / FP4 peak (prefill)"
+UNIT = "tokens/s"
+KERNELS_PER_CALL = 8   # act amax, act encode, router, plan scan, plan scatter, GEMM1, GEMM2, bf16 out
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode",
+                    choices=["decode", "tiny", "prefill", "large", "skewed"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-budget-s", type=float, default=150.0,
+                    help="wall-time budget of the reference arm's timed + warm-up steps")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------------------- peaks
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ----------------------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons, sampled while the GPU is under load."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0=None, t1=None):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, line in self.lines:
+            if t0 is not None and not (t0 <= ts <= t1):
+                continue
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------------------- helpers
+def workload(name):
+    import synth
+    cs = synth.CONFIGS[name]
+    return cs, list(cs.tokens)
+
+
+def expert_bytes(cs):
+    """NVFP4 bytes of one expert: codes (1/2 byte) + E4M3 scales (1/16 byte) per weight."""
+    per_matrix = cs.inter * cs.hidden
+    return 3 * per_matrix * 9 // 16
+
+
+def layer_counters(cs, T, touched, has_shared):
+    """Algorithmic bytes / FLOPs of one call (touched experts' weights counted once)."""
+    H, I, k = cs.hidden, cs.inter, cs.top_k
+    R = T * k
+    rows = R + (T if has_shared else 0)
+    n_exp = touched + (1 if has_shared else 0)
+    w13 = n_exp * 2 * I * H * 9 // 16
+    w2 = n_exp * H * I * 9 // 16
+    act_in = T * H * 2 + T * cs.experts * 4
+    out = T * H * 2
+    return dict(
+        flops=rows * 6 * H * I,
+        layer_bytes=w13 + w2 + act_in + out,
+        # GEMM1: gate/up weights + gathered activation codes/scales + requantised h out
+        gemm1_swiglu=w13 + rows * H * 9 // 16 + rows * I * 9 // 16,
+        # GEMM2: down weights + h codes/scales in + the FP32 token accumulator written
+        gemm2_combine=w2 + rows * I * 9 // 16 + T * H * 4,
+        act_quant=2 * T * H * 2 + T * H * 9 // 16 + T * H * 4,
+        router_plan=T * cs.experts * 4 + R * 16,
+        bf16_out=T * H * 4 + T * H * 2,
+    )
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(tokens_per_rank: float, seconds_per_rank: float, world: int):
+    """Whole-job throughput: all ranks' tokens over the slowest rank's time."""
+    tmax = max_over_ranks(seconds_per_rank, world)
+    return tokens_per_rank * world / tmax, tmax
+
+
+# ----------------------------------------------------------------------------------------- oracle
+def oracle_inputs(cs, wg, wu, wd, sh, need):
+    import numpy as np
+    import oracle
+    experts = [None] * cs.experts
+    for e in sorted(set(int(i) for i in need)):
+        experts[e] = oracle.QuantExpert.from_bf16(wg[e].cpu(), wu[e].cpu(), wd[e].cpu())
+    sho = oracle.QuantExpert.from_bf16(*[s.cpu() for s in sh]) if sh is not None else None
+    return experts, sho
+
+
+def oracle_call(cs, x_cpu, lg_np, experts, sho):
+    import oracle
+    xq, xsf, ts, st = oracle.quantize_bf16(x_cpu)
+    return oracle.moe_forward(xq, xsf, ts, lg_np, experts, cs.top_k, shared=sho)
+
+
+# ----------------------------------------------------------------------------------------- ours
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import synth
+    import nvfp4_mixture_experts_softmax_gb300 as moe
+    from nvfp4_mixture_experts_softmax_gb300 import _build
+
+    _build.build()
+    dev = torch.device("cuda", local)
+    cs, Ts = workload(args.workload)
+    has_shared = cs.has_shared
+    Tmax = max(Ts)
+    cfg = moe.make_config(cs.experts, cs.hidden, cs.inter, cs.top_k, shared_inter=cs.shared_inter,
+                          max_tokens=Tmax)
+    wg, wu, wd = synth.gen_all_experts(cs, device=dev)
+    sh = synth.gen_shared(cs, device=dev) if has_shared else None
+    wbuf = moe.quantize_weights(cfg, wg, wu, wd, shared=sh)
+    xs = {T: synth.gen_x(cs, T, device=dev, row0=1000 * i) for i, T in enumerate(Ts)}
+    lgs = {T: synth.gen_logits(cs, T, device=dev, row0=1000 * i) for i, T in enumerate(Ts)}
+    ws = torch.empty(moe.workspace_size(cfg, Tmax), dtype=torch.uint8, device=dev)
+    ys = {T: torch.empty(T, cs.hidden, dtype=torch.bfloat16, device=dev) for T in Ts}
+
+    # touched experts per call (from the device plan, read once before timing)
+    touched = {}
+    for T in Ts:
+        out = moe.plan(lgs[T], cs.top_k)
+        touched[T] = int((out["counts"] > 0).sum().item())
+    counters = {T: layer_counters(cs, T, touched[T], has_shared) for T in Ts}
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call(i, timer=None):
+        T = Ts[i % len(Ts)]
+        moe.run(cfg, wbuf, xs[T], lgs[T], y=ys[T], workspace=ws, timer=timer)
+        return T
+
+    for i in range(args.warmup):
+        flush.zero_()
+        call(i)
+    torch.cuda.synchronize()
+    assert moe.last_device_status(ws) == 0, "device status after warm-up"
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_settle = time.time()
+    while time.time() - t_settle < 0.4:      # hold the GPU busy so sampled clocks are under load
+        flush.zero_()
+        torch.cuda.synchronize()
+    timers = [moe.StageTimer() for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    w0 = time.time()
+    tokens = 0
+    Tseq = []
+    for i in range(args.steps):
+        flush.zero_()
+        T = call(i, timers[i])
+        tokens += T
+        Tseq.append(T)
+    torch.cuda.synchronize()
+    barrier(world)
+    w1 = time.time()
+    time.sleep(0.1)
+    sampler.stop()
+    st = moe.last_device_status(ws)
+    assert st == 0, f"device status {st}"
+
+    stage_ms = {n: 0.0 for n in moe.STAGES}
+    call_ms = []
+    per_T_ms = {T: [] for T in Ts}
+    for T, tm in zip(Tseq, timers):
+        s = tm.stage_ms()
+        for n, v in s.items():
+            stage_ms[n] += v
+        c = tm.events[0].elapsed_time(tm.events[-1])
+        call_ms.append(c)
+        per_T_ms[T].append(c)
+    dev_s = sum(call_ms) / 1e3
+    value, tmax = aggregate(tokens, dev_s, world)
+
+    hbm_peak, bf16_peak, peak_src = measured_peaks()
+    tot = {key: sum(counters[T][key] for T in Tseq) for key in counters[Ts[0]]}
+    dominant = max(stage_ms, key=stage_ms.get)
+    dom_s = stage_ms[dominant] / 1e3
+    achieved = tot[dominant] / dom_s / 1e9
+    eff_tflops = tot["flops"] / dev_s / 1e12
+    layer_gbs = tot["layer_bytes"] / dev_s / 1e9
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    hx = {T: xs[T].cpu().pin_memory() for T in Ts}
+    hl = {T: lgs[T].cpu().pin_memory() for T in Ts}
+    hy = {T: torch.empty(T, cs.hidden, dtype=torch.bfloat16).pin_memory() for T in Ts}
+    dx = {T: torch.empty_like(xs[T]) for T in Ts}
+    dl = {T: torch.empty_like(lgs[T]) for T in Ts}
+    e_ms, h2d, d2h = [], 0, 0
+    for i in range(args.warmup + args.steps):
+        T = Ts[i % len(Ts)]
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        dx[T].copy_(hx[T], non_blocking=True)
+        dl[T].copy_(hl[T], non_blocking=True)
+        moe.run(cfg, wbuf, dx[T], dl[T], y=ys[T], workspace=ws)
+        hy[T].copy_(ys[T], non_blocking=True)
+        e1.record(stream)
+        if i >= args.warmup:
+            e_ms.append((e0, e1, T))
+    torch.cuda.synchronize()
+    e2e_s = sum(a.elapsed_time(b) for a, b, _ in e_ms) / 1e3
+    e2e_tokens = sum(T for _, _, T in e_ms)
+    for _, _, T in e_ms:
+        h2d += T * cs.hidden * 2 + T * cs.experts * 4
+        d2h += T * cs.hidden * 2
+    e2e_value, _ = aggregate(e2e_tokens, e2e_s, world)
+
+    # ---- CPU baseline: the oracle, single thread, one pass over the workload's token counts
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        need = set()
+        for T in Ts:
+            out = moe.plan(lgs[T], cs.top_k)
+            need.update(out["topk_ids"].cpu().numpy().reshape(-1).tolist())
+        experts, sho = oracle_inputs(cs, wg, wu, wd, sh, need)
+        c_tok, c_s = 0, 0.0
+        for T in Ts:
+            xc, lc = xs[T].cpu(), lgs[T].cpu().numpy()
+            t0 = time.perf_counter()
+            oracle_call(cs, xc, lc, experts, sho)
+            c_s += time.perf_counter() - t0
+            c_tok += T
+        cpu = {"value": c_tok / c_s, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"one layer call at each T in {Ts} ({c_tok} tokens), single-threaded C++ "
+                         f"oracle incl. activation quantisation; weight quantisation untimed"}
+
+    clocks = sampler.summary(t_settle, w1 + 0.05)
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tmax * 1e3 / args.steps, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4(e2m1+e4m3) mma, f32 acc",
+        "data": "synthetic (seeded SplitMix64/Box-Muller), random-init weights",
+        "config": {"workload": f"{args.workload}: {cs.description}", "tokens_per_step": Ts,
+                   "step": f"one moe_run call at T = tokens_per_step[step mod {len(Ts)}]",
+                   "l2": "flushed (2x L2 write) before every call, outside the timed events",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "eff_tflops": round(eff_tflops, 3),
+        "layer_hbm_gbs": round(layer_gbs, 1),
+        "layer_hbm_frac": round(layer_gbs / hbm_peak, 4),
+        "per_T_us": {str(T): round(statistics.median(v) * 1e3, 2) for T, v in per_T_ms.items()},
+        "touched_experts": {str(T): touched[T] for T in Ts},
+        "stage_share": {n: round(v / sum(stage_ms.values()), 4) for n, v in stage_ms.items()},
+        "roofline": {"kernel": dominant, "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                     else "fallback", "traffic": None},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
+                "h2d_bytes_per_step": h2d // max(len(e_ms), 1),
+                "d2h_bytes_per_step": d2h // max(len(e_ms), 1)},
+        "gpu_launches": KERNELS_PER_CALL * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": round(w1 - w0, 4),
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------------------- reference
+def run_reference(args, world, rank, local):
+    if rank != 0:
+        return
+    import numpy as np
+    import synth
+    cs, Ts = workload(args.workload)
+    dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
+    wg, wu, wd = synth.gen_all_experts(cs, device=dev)
+    sh = synth.gen_shared(cs, device=dev) if cs.has_shared else None
+    xs = {T: synth.gen_x(cs, T, device=dev, row0=1000 * i).cpu() for i, T in enumerate(Ts)}
+    lgs = {T: synth.gen_logits(cs, T, device=dev, row0=1000 * i).cpu().numpy() for i, T in enumerate(Ts)}
+    import oracle
+    need = set()
+    for T in Ts:
+        ids, _ = oracle.router(lgs[T], cs.top_k)
+        need.update(ids.reshape(-1).tolist())
+    experts, sho = oracle_inputs(cs, wg, wu, wd, sh, need)
+    del wg, wu, wd
+    # per-step token sample: one token per call costs about one expert-set decode; size the
+    # sample so that warm-up + timed steps fit the budget
+    t0 = time.perf_counter()
+    oracle_call(cs, xs[Ts[0]][:1], lgs[Ts[0]][:1], experts, sho)
+    one = max(time.perf_counter() - t0, 1e-3)
+    nsteps = args.warmup + args.steps
+    per_step = args.ref_budget_s / max(nsteps, 1)
+    cap = max(1, int(per_step / one))
+    tok, secs = 0, 0.0
+    for i in range(nsteps):
+        T = Ts[i % len(Ts)]
+        n = min(T, cap)
+        t0 = time.perf_counter()
+        oracle_call(cs, xs[T][:n], lgs[T][:n], experts, sho)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            tok += n
+            secs += dt
+    value = tok / secs
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs * 1e3 / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32 (host oracle)",
+        "data": "synthetic (seeded SplitMix64/Box-Muller), random-init weights",
+        "config": {"workload": f"{args.workload}: {cs.description}", "tokens_per_step": Ts,
+                   "token_sample_cap": cap},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"per step the first min(T, {cap}) tokens of that step's call"},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank, local)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,164 @@
+/*
+ * nvfp4_moe.h - C ABI of the fused NVFP4 Mixture-of-Experts layer for GB300 (sm_103a).
+ *
+ * The layer (one call of moe_run):
+ *   1. router: softmax over E logits per token, top-k under the strict order (value descending,
+ *      lower expert index on ties), weights renormalised over the chosen k
+ *      ("vllm.cpp docs/STATUS.md", row "DeepSeek-V4-Flash decode ds4-gap - Lever 3");
+ *   2. activation quantiser: x [T,H] BF16 -> NVFP4 with one FP32 tensor scale max|x|/(6*448)
+ *      ("nvfp4-megamoe-kernel compare pre-b1...master", section "7. NVFP4 Quantization / Runtime
+ *      Activation Global Scale (gsa)"), E4M3 scales per 16 elements, E2M1 codes;
+ *   3. plan: per-expert counts, offsets and a stable token->expert permutation, built on the device
+ *      without any host read (same page, "CATEGORY 3: Data-dependent control flow" - bincount
+ *      replaced by a device scatter into a preallocated buffer - and "SECTION C - DSV4-specific
+ *      kernels that must be GPU-native", item 4: expert offsets stay GPU tensors);
+ *   4. GEMM1: block-scaled FP4 grouped GEMM of the gathered rows with each expert's gate and up
+ *      weights, epilogue SwiGLU silu(g)*u and NVFP4 requantisation of h (same page, section "MoE
+ *      kernel (FusedSwiGLUScaledGroupedGemmKernel)");
+ *   5. GEMM2: block-scaled FP4 grouped GEMM of h with the down weights, scaled by the router weight;
+ *   6. combine: y[t] = sum_j w_j * out_j (+ the shared expert, weight 1), rounded once to BF16
+ *      ("vllm.cpp docs/STATUS.md", row "Brick C part 1", MoeCombineKernel).
+ *
+ * Formats.  NVFP4 codes are E2M1, two per byte, element 2i in the low nibble; block scales are
+ * FP8 E4M3 (one byte per 16 consecutive elements along the reduction dimension); tensor scales
+ * are FP32.  Canonical layouts are row major: codes [rows, cols/2], scales [rows, cols/16].
+ *
+ * Conventions for every entry point.
+ *   - Tensor pointers are DEVICE pointers unless stated otherwise; tensors are contiguous and row
+ *     major; BF16 tensors are passed as void*.
+ *   - The caller owns every buffer: inputs, outputs, the packed-weight buffer and the workspace.
+ *     The library allocates no memory and keeps no state between calls.
+ *   - All work is enqueued on `stream`; no entry point synchronises except
+ *     moe_last_device_status.  moe_quantize_act, moe_plan and moe_run read nothing back to the
+ *     host and allocate nothing, so they can be recorded in a CUDA graph.
+ *   - Return value: MOE_OK (0) or a negative moe_status.  Argument errors are detected on the
+ *     host before anything is enqueued.  Errors found on the device (a non-finite activation
+ *     maximum, a pipeline wait that ran out) are written to a status word at the start of the
+ *     workspace; read it with moe_last_device_status.  Outputs of a call that raised a device
+ *     error are unspecified.
+ */
+#ifndef NVFP4_MOE_H
+#define NVFP4_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* the same type as cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,       /* null pointer, k < 1 or k > E, negative size ... */
+  MOE_ERR_UNSUPPORTED_SHAPE = -2, /* H or I not a multiple of 256, T > max_tokens, E > 1024 ... */
+  MOE_ERR_WORKSPACE_TOO_SMALL = -3,
+  MOE_ERR_CUDA = -4,              /* a CUDA runtime call failed (launch error ...) */
+  MOE_ERR_DEVICE_TIMEOUT = -5,    /* device status: a bounded pipeline wait ran out */
+  MOE_ERR_NONFINITE = -6,         /* device status: max|x| is not finite */
+  MOE_ERR_UNIMPLEMENTED = -7
+} moe_status;
+
+/* Shape of one MoE layer. */
+typedef struct {
+  int32_t num_experts;   /* E, routed experts, 1..1024 */
+  int32_t hidden;        /* H, multiple of 256 */
+  int32_t inter;         /* I, routed-expert intermediate size, multiple of 256 */
+  int32_t top_k;         /* k, 1..min(E, 32) */
+  int32_t shared_inter;  /* 0: no shared expert; otherwise its intermediate size (must equal I) */
+  float h_tensor_scale;  /* fixed FP32 tensor scale used to requantise h (1.0 by default) */
+  int32_t max_tokens;    /* largest T a workspace sized with moe_workspace_size must serve */
+  uint32_t flags;        /* reserved, must be 0 */
+} moe_config;
+
+/* Optional device buffers that receive the layer's intermediates (any field may be NULL). */
+typedef struct {
+  int32_t* topk_ids; /* [T,k] */
+  float* topk_w;     /* [T,k] */
+  int32_t* counts;   /* [E] */
+  int32_t* offsets;  /* [E+1] */
+  int32_t* perm_src; /* [T*k] permuted row -> token */
+  int32_t* inv;      /* [T*k] assignment t*k+j -> permuted row */
+  uint8_t* xq;       /* [T,H/2]  quantised activations */
+  uint8_t* xsf;      /* [T,H/16] */
+  float* ts_a;       /* [1]      activation tensor scale */
+  uint8_t* hq;       /* [T*k + T*shared, I/2]  requantised intermediate, permuted row order,
+                        shared-expert rows last (row T*k + t is token t) */
+  uint8_t* hsf;      /* [T*k + T*shared, I/16] */
+  void** stage_events; /* NULL, or an array of MOE_STAGE_EVENTS cudaEvent_t handles recorded on
+                          `stream`: [0] before the layer, then after the activation quantiser,
+                          the router + plan, GEMM1, GEMM2 and the BF16 output respectively */
+} moe_debug;
+
+#define MOE_STAGE_EVENTS 6
+
+/* Text for a status code (static storage). */
+const char* moe_status_string(int status);
+
+/* Checks a configuration; MOE_OK or the error moe_run would return for it. */
+int moe_config_check(const moe_config* cfg);
+
+/* ---------------------------------------------------------------------------------------------
+ * Weights.  moe_quantize_weights turns BF16 expert weights into NVFP4 (per expert and matrix: an
+ * FP32 tensor scale max|W|/(6*448), E4M3 block scales along the input dimension, E2M1 codes;
+ * "nvfp4-megamoe-kernel compare pre-b1...master", section "NVFP4 Weight Global Scale (gsb)", and
+ * "vllm.cpp docs/STATUS.md" row on NVFP4 weight_packed [N, K/2] / weight_scale [N, K/16]) and
+ * writes them into a caller-owned device buffer of moe_weights_size bytes, in the library's
+ * private GEMM-ready layout (gate/up rows interleaved by 16, scales pre-arranged for the tensor
+ * memory copy).  Off the hot path: run once per layer.
+ * ------------------------------------------------------------------------------------------- */
+size_t moe_weights_size(const moe_config* cfg);
+
+/* w_gate, w_up: [E, I, H] BF16; w_down: [E, H, I] BF16; s_gate, s_up: [I, H], s_down: [H, I]
+ * (NULL unless cfg->shared_inter > 0).  wbuf: 256-byte aligned device buffer of wbuf_bytes.
+ * Returns MOE_ERR_INVALID_ARG on null pointers, MOE_ERR_WORKSPACE_TOO_SMALL if wbuf_bytes is too
+ * small.  Non-finite weights give unspecified codes. */
+int moe_quantize_weights(const moe_config* cfg, const void* w_gate, const void* w_up,
+                         const void* w_down, const void* s_gate, const void* s_up,
+                         const void* s_down, void* wbuf, size_t wbuf_bytes, moe_stream_t stream);
+
+/* Copies one expert matrix back out of wbuf in canonical layout.  expert: 0..E-1, or -1 for the
+ * shared expert; matrix: 0 gate [I,H], 1 up [I,H], 2 down [H,I].  codes [N, K/2], sf [N, K/16]
+ * and ts [1] are device buffers. */
+int moe_weights_export(const moe_config* cfg, const void* wbuf, int32_t expert, int32_t matrix,
+                       uint8_t* codes, uint8_t* sf, float* ts, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Activation quantiser (one tensor scale for the whole [rows, cols] tensor, then per-16 blocks).
+ * x: [rows, cols] BF16, cols a multiple of 16 and x 16-byte aligned; codes [rows, cols/2];
+ * sf [rows, cols/16]; ts: device FP32 scalar.  rows == 0 is MOE_OK and does nothing.
+ * ------------------------------------------------------------------------------------------- */
+size_t moe_act_workspace_size(int64_t rows, int64_t cols);
+int moe_quantize_act(const void* x, int64_t rows, int64_t cols, uint8_t* codes, uint8_t* sf,
+                     float* ts, void* workspace, size_t ws_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Router + plan.  logits [T,E] FP32 -> topk_ids [T,k] (slot 0 the largest), topk_w [T,k],
+ * counts [E], offsets [E+1] (exclusive prefix sums, offsets[E] = T*k), perm_src [T*k]
+ * (permuted row -> token; rows of one expert ordered by ascending t*k+j), inv [T*k].
+ * ------------------------------------------------------------------------------------------- */
+size_t moe_plan_workspace_size(int32_t T, int32_t E, int32_t k);
+int moe_plan(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* topk_ids,
+             float* topk_w, int32_t* counts, int32_t* offsets, int32_t* perm_src, int32_t* inv,
+             void* workspace, size_t ws_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * The layer.  wbuf: written by moe_quantize_weights for the same cfg.  x [T,H] BF16 (16-byte
+ * aligned), logits [T,E] FP32, y [T,H] BF16 out.  k must equal cfg->top_k.  T == 0 is MOE_OK.
+ * workspace: >= moe_workspace_size(cfg, T) bytes, 256-byte aligned.  debug: NULL, or a host
+ * struct of device buffers that receive the intermediates.
+ * ------------------------------------------------------------------------------------------- */
+size_t moe_workspace_size(const moe_config* cfg, int32_t T);
+int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float* logits, int32_t T,
+            int32_t k, void* y, void* workspace, size_t ws_bytes, moe_stream_t stream,
+            const moe_debug* debug);
+
+/* Synchronises `stream`'s device and copies the device status word at the start of a workspace
+ * used by moe_quantize_act, moe_plan or moe_run into *host_status (MOE_OK or a device error). */
+int moe_last_device_status(const void* workspace, int32_t* host_status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NVFP4_MOE_H */

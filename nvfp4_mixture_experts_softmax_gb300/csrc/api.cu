@@ -1,0 +1,318 @@
+// C ABI of the NVFP4 MoE library: argument checks, workspace carving and the launch sequence.
+// Nothing here allocates device memory or reads device values back to the host (the single
+// exception is moe_last_device_status, which exists to do exactly that).
+#include <cmath>
+
+#include "internal.h"
+
+using namespace nvfp4moe;
+
+namespace {
+
+inline cudaStream_t to_cuda(moe_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_cfg(const moe_config* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->flags != 0u) return MOE_ERR_INVALID_ARG;
+  if (c->num_experts < 1 || c->top_k < 1 || c->hidden <= 0 || c->inter <= 0 || c->max_tokens < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (c->top_k > c->num_experts) return MOE_ERR_INVALID_ARG;
+  if (!(std::isfinite(c->h_tensor_scale) && c->h_tensor_scale > 0.0f)) return MOE_ERR_INVALID_ARG;
+  if (c->num_experts > 1024 || c->top_k > 32) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (c->hidden % kBK != 0 || c->inter % kBK != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (c->shared_inter != 0 && c->shared_inter != c->inter) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (c->shared_inter < 0) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(int s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace or buffer too small";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device pipeline wait timed out";
+    case MOE_ERR_NONFINITE: return "non-finite input maximum";
+    case MOE_ERR_UNIMPLEMENTED: return "not implemented";
+    default: return "unknown status";
+  }
+}
+
+int moe_config_check(const moe_config* cfg) { return check_cfg(cfg); }
+
+size_t moe_weights_size(const moe_config* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return 0;
+  return WeightLayout(*cfg).total;
+}
+
+int moe_quantize_weights(const moe_config* cfg, const void* w_gate, const void* w_up,
+                         const void* w_down, const void* s_gate, const void* s_up,
+                         const void* s_down, void* wbuf, size_t wbuf_bytes, moe_stream_t stream) {
+  int st = check_cfg(cfg);
+  if (st != MOE_OK) return st;
+  if (!w_gate || !w_up || !w_down || !wbuf) return MOE_ERR_INVALID_ARG;
+  if (cfg->shared_inter > 0 && (!s_gate || !s_up || !s_down)) return MOE_ERR_INVALID_ARG;
+  for (const void* p : {w_gate, w_up, w_down})
+    if (!aligned(p, 16)) return MOE_ERR_INVALID_ARG;
+  if (cfg->shared_inter > 0)
+    for (const void* p : {s_gate, s_up, s_down})
+      if (!aligned(p, 16)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(wbuf, kAlign)) return MOE_ERR_INVALID_ARG;
+  const WeightLayout L(*cfg);
+  if (wbuf_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return cuda_status(launch_weight_quant(*cfg, L, w_gate, w_up, w_down, s_gate, s_up, s_down,
+                                         static_cast<uint8_t*>(wbuf), to_cuda(stream)));
+}
+
+int moe_weights_export(const moe_config* cfg, const void* wbuf, int32_t expert, int32_t matrix,
+                       uint8_t* codes, uint8_t* sf, float* ts, moe_stream_t stream) {
+  int st = check_cfg(cfg);
+  if (st != MOE_OK) return st;
+  if (!wbuf || !codes || !sf || !ts) return MOE_ERR_INVALID_ARG;
+  if (matrix < 0 || matrix > 2) return MOE_ERR_INVALID_ARG;
+  int slot;
+  if (expert == -1) {
+    if (cfg->shared_inter <= 0) return MOE_ERR_INVALID_ARG;
+    slot = cfg->num_experts;
+  } else if (expert >= 0 && expert < cfg->num_experts) {
+    slot = expert;
+  } else {
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (!aligned(codes, 8)) return MOE_ERR_INVALID_ARG;
+  const WeightLayout L(*cfg);
+  return cuda_status(launch_weight_export(*cfg, L, static_cast<const uint8_t*>(wbuf), slot, matrix,
+                                          codes, sf, ts, to_cuda(stream)));
+}
+
+size_t moe_act_workspace_size(int64_t rows, int64_t cols) {
+  (void)rows;
+  (void)cols;
+  return 256 + 4 * 1024;
+}
+
+int moe_quantize_act(const void* x, int64_t rows, int64_t cols, uint8_t* codes, uint8_t* sf,
+                     float* ts, void* workspace, size_t ws_bytes, moe_stream_t stream) {
+  if (rows < 0 || cols <= 0 || cols % 16 != 0) return MOE_ERR_INVALID_ARG;
+  if (!workspace || ws_bytes < moe_act_workspace_size(rows, cols)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned(workspace, 16)) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!x || !codes || !sf || !ts) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(codes, 8) || !aligned(ts, 4)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = to_cuda(stream);
+  WsHeader* hdr = static_cast<WsHeader*>(workspace);
+  cudaError_t e = cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  uint32_t* partials = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + 256);
+  return cuda_status(launch_act_quant(x, rows, cols, codes, sf, ts, hdr, partials, nullptr, 0, s));
+}
+
+size_t moe_plan_workspace_size(int32_t T, int32_t E, int32_t k) {
+  if (T < 0 || E < 1 || k < 1) return 0;
+  const int tpc = plan_tokens_per_chunk(k);
+  const size_t nchunks = ((size_t)T + tpc - 1) / tpc;
+  return 256 + align_up(4 * nchunks * E) * 2;
+}
+
+int moe_plan(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* topk_ids,
+             float* topk_w, int32_t* counts, int32_t* offsets, int32_t* perm_src, int32_t* inv,
+             void* workspace, size_t ws_bytes, moe_stream_t stream) {
+  if (T < 0 || E < 1 || k < 1 || k > E) return MOE_ERR_INVALID_ARG;
+  if (E > 1024 || k > 32) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
+  if (!workspace || ws_bytes < moe_plan_workspace_size(T, E, k)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned(workspace, kAlign)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = to_cuda(stream);
+  if (cudaMemsetAsync(workspace, 0, 256, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (T == 0) {
+    if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  if (!logits || !topk_ids || !topk_w || !perm_src || !inv) return MOE_ERR_INVALID_ARG;
+  const int tpc = plan_tokens_per_chunk(k);
+  const size_t nchunks = ((size_t)T + tpc - 1) / tpc;
+  uint8_t* w8 = static_cast<uint8_t*>(workspace);
+  PlanArgs a{};
+  a.logits = logits;
+  a.T = T;
+  a.E = E;
+  a.k = k;
+  a.shared_rows = 0;
+  a.ids = topk_ids;
+  a.w = topk_w;
+  a.counts = counts;
+  a.offsets = offsets;
+  a.tile_start = nullptr;
+  a.perm_src = perm_src;
+  a.perm_w = nullptr;
+  a.inv = inv;
+  a.hist = reinterpret_cast<int32_t*>(w8 + 256);
+  a.base = reinterpret_cast<int32_t*>(w8 + 256 + align_up(4 * nchunks * E));
+  a.status = reinterpret_cast<int32_t*>(w8);
+  return cuda_status(launch_plan(a, s));
+}
+
+size_t moe_workspace_size(const moe_config* cfg, int32_t T) {
+  if (check_cfg(cfg) != MOE_OK || T < 0) return 0;
+  return RunLayout(*cfg, T).total;
+}
+
+int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float* logits, int32_t T,
+            int32_t k, void* y, void* workspace, size_t ws_bytes, moe_stream_t stream,
+            const moe_debug* debug) {
+  int st = check_cfg(cfg);
+  if (st != MOE_OK) return st;
+  if (T < 0 || k != cfg->top_k) return MOE_ERR_INVALID_ARG;
+  if (cfg->max_tokens > 0 && T > cfg->max_tokens) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if ((int64_t)T * (cfg->top_k + 1) > (int64_t)INT32_MAX / 2) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!workspace) return MOE_ERR_INVALID_ARG;
+  const RunLayout L(*cfg, T);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned(workspace, kAlign)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!wbuf || !x || !logits || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned(wbuf, kAlign) || !aligned(x, 16) || !aligned(y, 8)) return MOE_ERR_INVALID_ARG;
+
+  cudaStream_t s = to_cuda(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const uint8_t* wb = static_cast<const uint8_t*>(wbuf);
+  const WeightLayout W(*cfg);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws + L.hdr);
+  const int E = cfg->num_experts, H = cfg->hidden, I = cfg->inter;
+  const int shared = cfg->shared_inter > 0 ? 1 : 0;
+
+  auto i32 = [&](size_t off) { return reinterpret_cast<int32_t*>(ws + off); };
+  auto f32 = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
+
+  cudaEvent_t* ev = (debug && debug->stage_events) ? reinterpret_cast<cudaEvent_t*>(debug->stage_events)
+                                                    : nullptr;
+  auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], s) : cudaSuccess; };
+
+  cudaError_t e = mark(0);
+  if (e == cudaSuccess) e = cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  // 1. activation quantiser (and zero the FP32 output accumulator on the way)
+  e = launch_act_quant(x, T, H, ws + L.xq, ws + L.xsf, nullptr, hdr,
+                       reinterpret_cast<uint32_t*>(ws + L.amax_part), f32(L.yacc), (int64_t)T * H, s);
+  if (e == cudaSuccess) e = mark(1);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  // 2. router + plan
+  PlanArgs pa{};
+  pa.logits = logits;
+  pa.T = T;
+  pa.E = E;
+  pa.k = k;
+  pa.shared_rows = shared ? T : 0;
+  pa.ids = i32(L.ids);
+  pa.w = f32(L.w);
+  pa.counts = debug ? debug->counts : nullptr;
+  pa.offsets = i32(L.seg_off);
+  pa.tile_start = i32(L.tile_start);
+  pa.perm_src = i32(L.perm_src);
+  pa.perm_w = f32(L.perm_w);
+  pa.inv = i32(L.inv);
+  pa.hist = i32(L.hist);
+  pa.base = i32(L.base);
+  pa.status = &hdr->status;
+  e = launch_plan(pa, s);
+  if (e == cudaSuccess) e = mark(2);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  const int nseg = E + shared;
+  const int64_t max_mtiles = ((int64_t)L.Rt + (int64_t)nseg * (kBM - 1)) / kBM;
+  const float* w_ts = reinterpret_cast<const float*>(wb + W.ts);
+
+  // 3. GEMM1 + SwiGLU + requantisation
+  GemmArgs g{};
+  g.a_codes = ws + L.xq;
+  g.a_sf = ws + L.xsf;
+  g.a_gather = i32(L.perm_src);
+  g.b_sf = wb + W.w13_sf;
+  g.b_sf_per_seg = W.w13_sf_per_e;
+  g.w_ts = w_ts;
+  g.seg_off = i32(L.seg_off);
+  g.tile_start = i32(L.tile_start);
+  g.nseg = nseg;
+  g.N = 2 * I;
+  g.K = H;
+  g.mode = 0;
+  g.ts_a = &hdr->ts;
+  g.ts_h = cfg->h_tensor_scale;
+  g.hq = ws + L.hq;
+  g.hsf = ws + L.hsf;
+  g.status = &hdr->status;
+  g.max_items = (int)std::min<int64_t>(max_mtiles * (g.N / kBN), INT32_MAX);
+  g.max_ctas = g.max_items;
+  g.a_rows = T;
+  g.out_rows = L.Rt;
+  g.y_rows = T;
+  e = launch_grouped_gemm(g, wb + W.w13_codes, W.Et * 2 * I, s);
+  if (e == cudaSuccess) e = mark(3);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  // 4. GEMM2 (down projection) with the router-weighted accumulation into the token rows
+  GemmArgs g2 = g;
+  g2.a_codes = ws + L.hq;
+  g2.a_sf = ws + L.hsf;
+  g2.a_gather = nullptr;
+  g2.b_sf = wb + W.w2_sf;
+  g2.b_sf_per_seg = W.w2_sf_per_e;
+  g2.N = H;
+  g2.K = I;
+  g2.mode = 1;
+  g2.perm_src = i32(L.perm_src);
+  g2.perm_w = f32(L.perm_w);
+  g2.yacc = f32(L.yacc);
+  g2.max_items = (int)std::min<int64_t>(max_mtiles * (g2.N / kBN), INT32_MAX);
+  g2.max_ctas = g2.max_items;
+  g2.a_rows = L.Rt;
+  e = launch_grouped_gemm(g2, wb + W.w2_codes, W.Et * H, s);
+  if (e == cudaSuccess) e = mark(4);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  // 5. BF16 output
+  e = launch_finalize(f32(L.yacc), y, (int64_t)T * H, s);
+  if (e == cudaSuccess) e = mark(5);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  if (debug) {
+    auto cp = [&](void* dst, size_t off, size_t bytes) {
+      if (dst && e == cudaSuccess) e = cudaMemcpyAsync(dst, ws + off, bytes, cudaMemcpyDeviceToDevice, s);
+    };
+    const size_t R = (size_t)L.R, Rt = (size_t)L.Rt;
+    cp(debug->topk_ids, L.ids, 4 * R);
+    cp(debug->topk_w, L.w, 4 * R);
+    cp(debug->offsets, L.seg_off, 4 * (size_t)(E + 1));
+    cp(debug->perm_src, L.perm_src, 4 * R);
+    cp(debug->inv, L.inv, 4 * R);
+    cp(debug->xq, L.xq, (size_t)T * H / 2);
+    cp(debug->xsf, L.xsf, (size_t)T * H / 16);
+    cp(debug->ts_a, L.hdr + offsetof(WsHeader, ts), 4);
+    cp(debug->hq, L.hq, Rt * I / 2);
+    cp(debug->hsf, L.hsf, Rt * I / 16);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+int moe_last_device_status(const void* workspace, int32_t* host_status) {
+  if (!workspace || !host_status) return MOE_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpy(host_status, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,414 @@
+// Persistent grouped GEMM on the 5th-generation tensor cores with block-scaled FP4 operands
+// (tcgen05.mma kind::mxf4nvf4, E2M1 values, one E4M3 scale per 16 elements), used twice per layer:
+//   GEMM1: rows of the quantised activations gathered in expert order x the expert's interleaved
+//          gate/up weights; the epilogue applies the tensor scales, SwiGLU silu(g)*u, and
+//          requantises h to NVFP4 ("nvfp4-megamoe-kernel compare pre-b1...master", section "MoE
+//          kernel (FusedSwiGLUScaledGroupedGemmKernel)": epilogue with global scale + SwiGLU in
+//          registers between the tensor-memory load and the store);
+//   GEMM2: the requantised h x the expert's down weights; the epilogue scales by the tensor scales
+//          and the router weight and accumulates into the token's FP32 output row
+//          ("vllm.cpp docs/STATUS.md", row "Brick C part 1": y = sum_j w_j * expert_out_j).
+//
+// One CTA per SM, warp-specialised (the pages' design uses TMA / MMA / epilogue / scheduler warps;
+// here the scheduler is a static round robin over a device-built tile list):
+//   warps 0-3  epilogue: tensor memory -> registers -> global, one accumulator row per thread;
+//   warp  4    TMA: weight tile (2-D tensor map, 128B swizzle) + its pre-arranged scale block;
+//   warp  5    tensor-memory allocation and the single MMA-issuing thread;
+//   warps 6-9  activation rows gathered with cp.async into the same 128B-swizzled layout, and
+//              their scales into the 32x4x4 arrangement the scale-factor copy expects.
+// A 5-stage shared-memory ring (mbarrier full/empty pairs) feeds the MMA; two 128-column FP32
+// accumulators in tensor memory let the epilogue of one tile overlap the main loop of the next.
+// Every wait is bounded in time and reports MOE_ERR_DEVICE_TIMEOUT instead of hanging.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace nvfp4moe {
+
+namespace {
+
+constexpr int kStages = 5;
+constexpr int kEpiWarps = 4;
+constexpr int kTmaWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kProdWarp0 = 6;
+constexpr int kProdWarps = 4;
+constexpr int kProdThreads = kProdWarps * 32;
+constexpr int kThreads = (kProdWarp0 + kProdWarps) * 32;
+constexpr int kABytes = kBM * 128;
+constexpr int kBBytes = kBN * 128;
+constexpr int kSfBytes = 4 * 512;  // four 512-byte scale blocks (one per 64-wide MMA K step)
+constexpr int kStageBytes = kABytes + kBBytes + 2 * kSfBytes;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCols = kBN;
+constexpr uint32_t kSfCol0 = 2 * kAccCols;
+constexpr uint32_t kSfColsPerStage = 32;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "tensor memory budget");
+static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
+
+// Instruction descriptor of tcgen05.mma kind::mxf4nvf4: A and B E2M1 (format 1) at bits 7-9 and
+// 10-12, both K-major, N >> 3 at bits 17-22, UE4M3 scale type (bit 23 = 0), M >> 4 at bits 24-28,
+// scale-factor ids 0, dense K = 64.
+constexpr uint32_t make_idesc(int M, int N) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+struct TileInfo {
+  int seg, m0, rows, nt;
+};
+
+__device__ __forceinline__ TileInfo decode_tile(int item, int n_tiles, const int32_t* s_tile,
+                                                const int32_t* s_seg, int nseg) {
+  TileInfo t;
+  const int mt = item / n_tiles;
+  t.nt = item - mt * n_tiles;
+  int lo = 0, hi = nseg - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_tile[mid] <= mt) lo = mid;
+    else hi = mid - 1;
+  }
+  t.seg = lo;
+  t.m0 = s_seg[lo] + (mt - s_tile[lo]) * kBM;
+  t.rows = min(kBM, s_seg[lo + 1] - t.m0);
+  return t;
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* acc_full = bars + 2 * kStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int32_t* s_tile = reinterpret_cast<int32_t*>(smem + kStages * kStageBytes + 256);
+  int32_t* s_seg = s_tile + (p.nseg + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i <= p.nseg; i += blockDim.x) {
+    s_tile[i] = p.tile_start[i];
+    s_seg[i] = p.seg_off[i];
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(full + s), kProdThreads + 1);
+      mbar_init(smem_u32(empty + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(acc_full + b), 1);
+      mbar_init(smem_u32(acc_empty + b), kEpiWarps);
+    }
+    mbar_init(smem_u32(drain), 1);
+    fence_barrier_init();
+  }
+  if (warp == kTmaWarp && lane == 0)
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_b) : "memory");
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int n_tiles = p.N / kBN;
+  int total = s_tile[p.nseg] * n_tiles;
+  if (total < 0 || total > p.max_items) {  // malformed plan: do nothing, report it
+    if (threadIdx.x == 0) set_status(p.status, MOE_ERR_INVALID_ARG);
+    total = 0;
+  }
+  const int kst = p.K / kBK;
+  const uint32_t smem0 = smem_u32(smem);
+
+  if (warp == kTmaWarp) {
+    // ---------------- weight tiles (TMA) ----------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+        const TileInfo t = decode_tile(item, n_tiles, s_tile, s_seg, p.nseg);
+        const int brow = t.seg * p.N + t.nt * kBN;
+        const uint8_t* sfsrc = p.b_sf + (size_t)t.seg * p.b_sf_per_seg +
+                               (size_t)(t.nt * kBN / 128) * (p.K / 64) * 512;
+        for (int ks = 0; ks < kst; ++ks) {
+          if (!mbar_wait_bounded(smem_u32(empty + stage), phase ^ 1u, kWaitLimitNs, p.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sb = smem0 + stage * kStageBytes;
+          mbar_arrive_expect_tx(smem_u32(full + stage), kBBytes + kSfBytes);
+          tma_load_2d(sb + kABytes, &tmap_b, ks * 128, brow, smem_u32(full + stage));
+          bulk_load(sb + kABytes + kBBytes + kSfBytes, sfsrc + (size_t)ks * kSfBytes, kSfBytes,
+                    smem_u32(full + stage));
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // tail: wait until the MMA has released every stage, so no arrival is still in flight
+      for (int i = 0; i < kStages && ok; ++i) {
+        if (!mbar_wait_bounded(smem_u32(empty + stage), phase ^ 1u, kWaitLimitNs, p.status)) break;
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------- MMA issue (one thread) ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc(kBM, kBN);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t acc_phase[2] = {0u, 0u};
+      bool ok = true;
+      int it = 0;
+      for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++it) {
+        const int abuf = it & 1;
+        if (!mbar_wait_bounded(smem_u32(acc_empty + abuf), acc_phase[abuf] ^ 1u, kWaitLimitNs,
+                               p.status)) {
+          ok = false;
+          break;
+        }
+        acc_phase[abuf] ^= 1u;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + abuf * kAccCols;
+        for (int ks = 0; ks < kst; ++ks) {
+          if (!mbar_wait_bounded(smem_u32(full + stage), phase, kWaitLimitNs, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sb = smem0 + stage * kStageBytes;
+          const uint32_t sfa_s = sb + kABytes + kBBytes;
+          const uint32_t sfb_s = sfa_s + kSfBytes;
+          const uint32_t sf_t = tmem_base + kSfCol0 + stage * kSfColsPerStage;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            tc_cp_32x128b_warpx4(sf_t + kk * 4, smem_desc(sfa_s + kk * 512, 0, 128, kLayoutSwizzleNone));
+            tc_cp_32x128b_warpx4(sf_t + 16 + kk * 4,
+                                 smem_desc(sfb_s + kk * 512, 0, 128, kLayoutSwizzleNone));
+          }
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = smem_desc(sb + kk * 32, 16, 1024, kLayoutSwizzle128B);
+            const uint64_t bd = smem_desc(sb + kABytes + kk * 32, 16, 1024, kLayoutSwizzle128B);
+            tc_mma_mxf4nvf4(d_tmem, ad, bd, idesc, sf_t + kk * 4, sf_t + 16 + kk * 4,
+                            (ks | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(smem_u32(empty + stage));
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (ok) tc_commit(smem_u32(acc_full + abuf));
+      }
+      // make sure no tensor-core operation is still running before tensor memory is released
+      tc_commit(smem_u32(drain));
+      mbar_wait_bounded(smem_u32(drain), 0u, kWaitLimitNs, p.status);
+    }
+  } else if (warp >= kProdWarp0) {
+    // ---------------- activation rows (cp.async gather) ----------------
+    const int pt = threadIdx.x - kProdWarp0 * 32;  // 0..127
+    int stage = 0;
+    uint32_t phase = 0;
+    int pending = -1;
+    bool ok = true;
+    for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+      const TileInfo t = decode_tile(item, n_tiles, s_tile, s_seg, p.nseg);
+      // this thread copies 16-byte chunk (pt % 8) of rows pt/8 + 16*i, i = 0..7, and the four
+      // scale words of row pt
+      const uint8_t* crow[8];
+      uint32_t cbytes[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = (pt >> 3) + 16 * i;
+        const int pr = t.m0 + r;
+        const int src = (r < t.rows && pr >= 0 && pr < p.out_rows)
+                            ? (p.a_gather ? __ldg(p.a_gather + pr) : pr) : -1;
+        if (src >= 0 && src < p.a_rows) {
+          crow[i] = p.a_codes + (size_t)src * (p.K / 2) + (pt & 7) * 16;
+          cbytes[i] = 16;
+        } else {
+          if (r < t.rows) set_status(p.status, MOE_ERR_INVALID_ARG);
+          crow[i] = p.a_codes;
+          cbytes[i] = 0;
+        }
+      }
+      const uint8_t* srow;
+      uint32_t sbytes;
+      const int spr = t.m0 + pt;
+      const int ssrc = (pt < t.rows && spr >= 0 && spr < p.out_rows)
+                           ? (p.a_gather ? __ldg(p.a_gather + spr) : spr) : -1;
+      if (ssrc >= 0 && ssrc < p.a_rows) {
+        srow = p.a_sf + (size_t)ssrc * (p.K / 16);
+        sbytes = 4;
+      } else {
+        srow = p.a_sf;
+        sbytes = 0;
+      }
+      for (int ks = 0; ks < kst; ++ks) {
+        if (!mbar_wait_bounded(smem_u32(empty + stage), phase ^ 1u, kWaitLimitNs, p.status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sb = smem0 + stage * kStageBytes;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = (pt >> 3) + 16 * i;
+          const uint32_t dst = sb + r * 128 + ((((pt & 7) ^ (r & 7))) << 4);
+          cp_async_16(dst, crow[i] + (cbytes[i] ? ks * 128 : 0), cbytes[i]);
+        }
+        const uint32_t sfa_s = sb + kABytes + kBBytes + (pt & 31) * 16 + (pt >> 5) * 4;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          cp_async_4(sfa_s + kk * 512, srow + (sbytes ? ks * 16 + kk * 4 : 0), sbytes);
+        cp_async_commit();
+        if (pending >= 0) {
+          cp_async_wait<1>();
+          fence_proxy_async_smem();
+          mbar_arrive(smem_u32(full + pending));
+        }
+        pending = stage;
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+    }
+    cp_async_wait<0>();
+    if (pending >= 0 && ok) {
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(full + pending));
+    }
+  } else {
+    // ---------------- epilogue (warps 0-3) ----------------
+    uint32_t acc_phase[2] = {0u, 0u};
+    int it = 0;
+    const int r = warp * 32 + lane;
+    const float ts_a = p.mode == 0 ? *p.ts_a : 0.0f;
+    for (int item = blockIdx.x; item < total; item += gridDim.x, ++it) {
+      const TileInfo t = decode_tile(item, n_tiles, s_tile, s_seg, p.nseg);
+      const int abuf = it & 1;
+      if (!mbar_wait_bounded(smem_u32(acc_full + abuf), acc_phase[abuf], kWaitLimitNs, p.status))
+        break;
+      acc_phase[abuf] ^= 1u;
+      tc_fence_after();
+      const int prow = t.m0 + r;
+      const bool valid = r < t.rows && prow >= 0 && prow < p.out_rows;
+      const uint32_t tbase = tmem_base + abuf * kAccCols + ((uint32_t)(warp * 32) << 16);
+      if (p.mode == 0) {
+        const float ag = ts_a * p.w_ts[t.seg * 4 + 0];
+        const float au = ts_a * p.w_ts[t.seg * 4 + 1];
+        const int I = p.N / 2;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tbase + c * 32, v);
+          tmem_ld_wait();
+          if (valid) {
+            float h[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              h[i] = silu_mul(__uint_as_float(v[i]) * ag, __uint_as_float(v[16 + i]) * au);
+            uint32_t lo, hi, s;
+            quant_block16(h, p.ts_h, lo, hi, s);
+            const int f0 = t.nt * (kBN / 2) + c * 16;
+            *reinterpret_cast<uint2*>(p.hq + (size_t)prow * (I / 2) + f0 / 2) = make_uint2(lo, hi);
+            p.hsf[(size_t)prow * (I / 16) + f0 / 16] = (uint8_t)s;
+          }
+        }
+      } else {
+        const float alpha = p.ts_h * p.w_ts[t.seg * 4 + 2];
+        int tok = 0;
+        float wr = 0.0f;
+        bool ok_row = valid;
+        if (valid) {
+          tok = __ldg(p.perm_src + prow);
+          wr = __ldg(p.perm_w + prow);
+          if (tok < 0 || tok >= p.y_rows) {
+            set_status(p.status, MOE_ERR_INVALID_ARG);
+            ok_row = false;
+            tok = 0;
+          }
+        }
+        float* yrow = p.yacc + (size_t)tok * p.N + t.nt * kBN;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tbase + c * 32, v);
+          tmem_ld_wait();
+          if (ok_row) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              red_add_v4(yrow + c * 32 + 4 * i, (__uint_as_float(v[4 * i]) * alpha) * wr,
+                         (__uint_as_float(v[4 * i + 1]) * alpha) * wr,
+                         (__uint_as_float(v[4 * i + 2]) * alpha) * wr,
+                         (__uint_as_float(v[4 * i + 3]) * alpha) * wr);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(acc_empty + abuf));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+size_t gemm_smem_bytes(int nseg) {
+  return 1024 + (size_t)kStages * kStageBytes + 256 + sizeof(int32_t) * 2 * (nseg + 2);
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm(const GemmArgs& a, const uint8_t* b_codes, int b_rows_total,
+                                cudaStream_t s) {
+  auto encode = get_encode_fn();
+  if (!encode) return cudaErrorNotSupported;
+  CUtensorMap tmap;
+  const cuuint64_t dims[2] = {(cuuint64_t)(a.K / 2), (cuuint64_t)b_rows_total};
+  const cuuint64_t strides[1] = {(cuuint64_t)(a.K / 2)};
+  const cuuint32_t box[2] = {128, (cuuint32_t)kBN};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(b_codes), dims,
+                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  const size_t smem = gemm_smem_bytes(a.nseg);
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int grid = a.max_ctas;
+  if (grid > num_sms()) grid = num_sms();
+  if (grid < 1) grid = 1;
+  grouped_gemm_kernel<<<grid, kThreads, smem, s>>>(tmap, a);
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4moe

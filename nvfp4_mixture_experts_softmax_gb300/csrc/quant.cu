@@ -1,0 +1,328 @@
+// NVFP4 quantisers: activations (one tensor scale, then per-16 blocks), expert weights (per expert
+// and matrix, packed for the grouped GEMM), the export of packed weights back to the canonical
+// layout, and the FP32 -> BF16 output rounding.
+//
+// Quantisation rule ("nvfp4-megamoe-kernel compare pre-b1...master", section "7. NVFP4
+// Quantization": tensor scale max|x| / (6 * 448); block scales E4M3 over 16 elements, codes E2M1,
+// section "NVFP4 throughout"): ts = amax / 2688, sf = E4M3((block_max / 6) / ts), code =
+// E2M1(x / (decode(sf) * ts)), round to nearest even, IEEE FP32 division (no fast math).
+#include "common.cuh"
+#include "internal.h"
+
+namespace nvfp4moe {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kMaxAmaxBlocks = 1024;
+
+__device__ __forceinline__ uint32_t abs_bf16_max8(uint4 v) {
+  uint32_t a = max(v.x & 0x7FFFu, (v.x >> 16) & 0x7FFFu);
+  uint32_t b = max(v.y & 0x7FFFu, (v.y >> 16) & 0x7FFFu);
+  uint32_t c = max(v.z & 0x7FFFu, (v.z >> 16) & 0x7FFFu);
+  uint32_t d = max(v.w & 0x7FFFu, (v.w >> 16) & 0x7FFFu);
+  return max(max(a, b), max(c, d));
+}
+
+__device__ __forceinline__ uint32_t block_max_u32(uint32_t m, uint32_t* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  if (warp == 0) {
+    m = lane < (int)(blockDim.x >> 5) ? red[lane] : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+  }
+  return m;  // valid in warp 0
+}
+
+// Pass 1: max |x| over the whole tensor (BF16 magnitudes compare as their bit patterns), with a
+// last-block reduction that writes ts = amax / 2688 and re-arms the block counter.  Optionally
+// zero-fills `zero` (the FP32 output accumulator of the layer) on the way.
+__global__ void __launch_bounds__(kThreads) act_amax_kernel(const uint4* __restrict__ x,
+                                                           int64_t nvec, WsHeader* hdr,
+                                                           uint32_t* partials, float* ts_out,
+                                                           float4* zero, int64_t nzero4) {
+  __shared__ uint32_t red[32];
+  __shared__ bool is_last;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  uint32_t m = 0;
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+#pragma unroll 4
+  for (; i < nvec; i += stride) m = max(m, abs_bf16_max8(__ldg(x + i)));
+  for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < nzero4; j += stride)
+    zero[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  m = block_max_u32(m, red);
+  if (threadIdx.x == 0) {
+    partials[blockIdx.x] = m;
+    __threadfence();
+    const uint32_t prev = atomicAdd(&hdr->counter, 1u);
+    is_last = (prev == gridDim.x - 1);
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  uint32_t v = 0;
+  for (int b = threadIdx.x; b < (int)gridDim.x; b += blockDim.x)
+    v = max(v, __ldcg(partials + b));
+  __syncthreads();
+  v = block_max_u32(v, red);
+  if (threadIdx.x == 0) {
+    if (v >= 0x7F80u) set_status(&hdr->status, MOE_ERR_NONFINITE);
+    const float amax = bf16_bits_to_f32(v);
+    const float ts = __fdiv_rn(amax, 2688.0f);
+    hdr->ts = ts;
+    if (ts_out) *ts_out = ts;
+    hdr->counter = 0u;
+  }
+}
+
+// Pass 2: one thread per 16-element block: 32 bytes in, 8 code bytes and 1 scale byte out.
+__global__ void __launch_bounds__(kThreads) act_encode_kernel(const uint4* __restrict__ x,
+                                                             int64_t nblk,
+                                                             const float* __restrict__ ts_ptr,
+                                                             uint2* __restrict__ codes,
+                                                             uint8_t* __restrict__ sf) {
+  const float ts = *ts_ptr;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblk; b += stride) {
+    const uint4 v0 = __ldg(x + 2 * b), v1 = __ldg(x + 2 * b + 1);
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    float f[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      f[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
+      f[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+    }
+    uint32_t lo, hi, s;
+    quant_block16(f, ts, lo, hi, s);
+    codes[b] = make_uint2(lo, hi);
+    sf[b] = (uint8_t)s;
+  }
+}
+
+// ---- weights ----
+
+struct WeightSrc {
+  const uint16_t* routed[3];  // gate [E,I,H], up [E,I,H], down [E,H,I]
+  const uint16_t* shared[3];  // [I,H], [I,H], [H,I] or null
+  int E, H, I;
+};
+
+__device__ __forceinline__ const uint16_t* matrix_ptr(const WeightSrc& w, int slot, int m,
+                                                      int64_t per) {
+  return slot < w.E ? w.routed[m] + (int64_t)slot * per : w.shared[m];
+}
+
+// Byte offset of the scale of (row n, 16-block kb) inside a packed [N/128][K/64][512] block array.
+__host__ __device__ __forceinline__ int64_t packed_sf_offset(int64_t n, int64_t kb, int64_t K) {
+  return ((n >> 7) * (K >> 6) + (kb >> 2)) * 512 + (n & 31) * 16 + ((n & 127) >> 5) * 4 + (kb & 3);
+}
+
+// Row of the gate (m=0) or up (m=1) row n inside the 16-interleaved w13 layout.
+__host__ __device__ __forceinline__ int64_t w13_row(int64_t n, int m) {
+  return (n >> 4) * 32 + (m ? 16 : 0) + (n & 15);
+}
+
+// max |W| per (slot, matrix) as BF16 magnitude bits, atomically max-ed into amax_bits[slot*4+m].
+__global__ void __launch_bounds__(kThreads) weight_amax_kernel(WeightSrc w, uint32_t* amax_bits) {
+  __shared__ uint32_t red[32];
+  const int mi = blockIdx.y;
+  const int slot = mi / 3, m = mi % 3;
+  const int64_t per = (int64_t)w.I * w.H;
+  const uint4* src = reinterpret_cast<const uint4*>(matrix_ptr(w, slot, m, per));
+  const int64_t nvec = per / 8;
+  uint32_t v = 0;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec;
+       i += (int64_t)gridDim.x * blockDim.x)
+    v = max(v, abs_bf16_max8(__ldg(src + i)));
+  v = block_max_u32(v, red);
+  if (threadIdx.x == 0) atomicMax(amax_bits + slot * 4 + m, v);
+}
+
+__global__ void weight_ts_kernel(uint32_t* amax_bits_then_ts, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) {
+    const float amax = bf16_bits_to_f32(amax_bits_then_ts[i]);
+    reinterpret_cast<float*>(amax_bits_then_ts)[i] = __fdiv_rn(amax, 2688.0f);
+  }
+}
+
+struct WeightDst {
+  uint8_t* w13_codes;
+  uint8_t* w13_sf;
+  uint8_t* w2_codes;
+  uint8_t* w2_sf;
+  const float* ts;  // [Et][4]
+  int64_t w13_codes_per_e, w13_sf_per_e, w2_codes_per_e, w2_sf_per_e;
+};
+
+// One thread per 16-element block of one matrix row: quantise and store into the packed layout.
+__global__ void __launch_bounds__(kThreads) weight_encode_kernel(WeightSrc w, WeightDst d) {
+  const int mi = blockIdx.y;
+  const int slot = mi / 3, m = mi % 3;
+  const int64_t per = (int64_t)w.I * w.H;
+  const int64_t K = m < 2 ? w.H : w.I;
+  const int64_t nblk = per / 16;
+  const uint16_t* src = matrix_ptr(w, slot, m, per);
+  const float ts = d.ts[slot * 4 + m];
+  for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblk;
+       b += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t n = b / (K / 16), kb = b % (K / 16);
+    const uint4* p = reinterpret_cast<const uint4*>(src + n * K + kb * 16);
+    const uint4 v0 = __ldg(p), v1 = __ldg(p + 1);
+    const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    float f[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      f[2 * i] = bf16_bits_to_f32(wv[i] & 0xFFFFu);
+      f[2 * i + 1] = bf16_bits_to_f32(wv[i] >> 16);
+    }
+    uint32_t lo, hi, s;
+    quant_block16(f, ts, lo, hi, s);
+    if (m < 2) {
+      const int64_t r = w13_row(n, m);
+      *reinterpret_cast<uint2*>(d.w13_codes + slot * d.w13_codes_per_e + r * (K / 2) + kb * 8) =
+          make_uint2(lo, hi);
+      d.w13_sf[slot * d.w13_sf_per_e + packed_sf_offset(r, kb, K)] = (uint8_t)s;
+    } else {
+      *reinterpret_cast<uint2*>(d.w2_codes + slot * d.w2_codes_per_e + n * (K / 2) + kb * 8) =
+          make_uint2(lo, hi);
+      d.w2_sf[slot * d.w2_sf_per_e + packed_sf_offset(n, kb, K)] = (uint8_t)s;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) weight_export_kernel(WeightDst d, int slot, int m,
+                                                                int64_t N, int64_t K,
+                                                                uint8_t* codes, uint8_t* sf,
+                                                                float* ts) {
+  const int64_t nblk = N * K / 16;
+  for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblk;
+       b += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t n = b / (K / 16), kb = b % (K / 16);
+    uint2 c;
+    uint8_t s;
+    if (m < 2) {
+      const int64_t r = w13_row(n, m);
+      c = *reinterpret_cast<const uint2*>(d.w13_codes + slot * d.w13_codes_per_e + r * (K / 2) +
+                                          kb * 8);
+      s = d.w13_sf[slot * d.w13_sf_per_e + packed_sf_offset(r, kb, K)];
+    } else {
+      c = *reinterpret_cast<const uint2*>(d.w2_codes + slot * d.w2_codes_per_e + n * (K / 2) +
+                                          kb * 8);
+      s = d.w2_sf[slot * d.w2_sf_per_e + packed_sf_offset(n, kb, K)];
+    }
+    *reinterpret_cast<uint2*>(codes + n * (K / 2) + kb * 8) = c;
+    sf[n * (K / 16) + kb] = s;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) *ts = d.ts[slot * 4 + m];
+}
+
+__global__ void __launch_bounds__(kThreads) finalize_kernel(const float4* __restrict__ acc,
+                                                           uint2* __restrict__ y, int64_t n4) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const float4 v = __ldcs(acc + i);
+    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+    __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+    y[i] = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+  }
+}
+
+int grid_for(int64_t work, int per_block, int cap) {
+  int64_t g = (work + per_block - 1) / per_block;
+  if (g < 1) g = 1;
+  if (g > cap) g = cap;
+  return (int)g;
+}
+
+WeightDst make_dst(const WeightLayout& L, uint8_t* wbuf) {
+  WeightDst d;
+  d.w13_codes = wbuf + L.w13_codes;
+  d.w13_sf = wbuf + L.w13_sf;
+  d.w2_codes = wbuf + L.w2_codes;
+  d.w2_sf = wbuf + L.w2_sf;
+  d.ts = reinterpret_cast<const float*>(wbuf + L.ts);
+  d.w13_codes_per_e = (int64_t)L.w13_codes_per_e;
+  d.w13_sf_per_e = (int64_t)L.w13_sf_per_e;
+  d.w2_codes_per_e = (int64_t)L.w2_codes_per_e;
+  d.w2_sf_per_e = (int64_t)L.w2_sf_per_e;
+  return d;
+}
+
+}  // namespace
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+  }
+  return n;
+}
+
+cudaError_t launch_act_quant(const void* x, int64_t rows, int64_t cols, uint8_t* codes, uint8_t* sf,
+                             float* ts, WsHeader* hdr, uint32_t* partials, float* zero_buf,
+                             int64_t zero_floats, cudaStream_t s) {
+  const int64_t n = rows * cols;
+  const int64_t nvec = n / 8;
+  const int g1 = grid_for(nvec, kThreads * 8, kMaxAmaxBlocks);
+  act_amax_kernel<<<g1, kThreads, 0, s>>>(reinterpret_cast<const uint4*>(x), nvec, hdr, partials,
+                                          ts, reinterpret_cast<float4*>(zero_buf), zero_floats / 4);
+  const int64_t nblk = n / 16;
+  const int g2 = grid_for(nblk, kThreads, num_sms() * 16);
+  act_encode_kernel<<<g2, kThreads, 0, s>>>(reinterpret_cast<const uint4*>(x), nblk, &hdr->ts,
+                                            reinterpret_cast<uint2*>(codes), sf);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_weight_quant(const moe_config& c, const WeightLayout& L, const void* wg,
+                                const void* wu, const void* wd, const void* sg, const void* su,
+                                const void* sd, uint8_t* wbuf, cudaStream_t s) {
+  WeightSrc w;
+  w.routed[0] = static_cast<const uint16_t*>(wg);
+  w.routed[1] = static_cast<const uint16_t*>(wu);
+  w.routed[2] = static_cast<const uint16_t*>(wd);
+  w.shared[0] = static_cast<const uint16_t*>(sg);
+  w.shared[1] = static_cast<const uint16_t*>(su);
+  w.shared[2] = static_cast<const uint16_t*>(sd);
+  w.E = c.num_experts;
+  w.H = c.hidden;
+  w.I = c.inter;
+  uint32_t* amax = reinterpret_cast<uint32_t*>(wbuf + L.ts);
+  cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float) * 4 * L.Et, s);
+  if (e != cudaSuccess) return e;
+  const int64_t per = (int64_t)c.inter * c.hidden;
+  dim3 g1(grid_for(per / 8, kThreads * 8, 256), L.Et * 3);
+  weight_amax_kernel<<<g1, kThreads, 0, s>>>(w, amax);
+  weight_ts_kernel<<<(L.Et * 4 + 255) / 256, 256, 0, s>>>(amax, L.Et * 4);
+  WeightDst d = make_dst(L, wbuf);
+  dim3 g2(grid_for(per / 16, kThreads, 4096), L.Et * 3);
+  weight_encode_kernel<<<g2, kThreads, 0, s>>>(w, d);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_weight_export(const moe_config& c, const WeightLayout& L, const uint8_t* wbuf,
+                                 int slot, int m, uint8_t* codes, uint8_t* sf, float* ts,
+                                 cudaStream_t s) {
+  WeightDst d = make_dst(L, const_cast<uint8_t*>(wbuf));
+  const int64_t N = m < 2 ? c.inter : c.hidden;
+  const int64_t K = m < 2 ? c.hidden : c.inter;
+  weight_export_kernel<<<grid_for(N * K / 16, kThreads, 4096), kThreads, 0, s>>>(d, slot, m, N, K,
+                                                                                codes, sf, ts);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const float* yacc, void* y, int64_t n, cudaStream_t s) {
+  const int64_t n4 = n / 4;
+  finalize_kernel<<<grid_for(n4, kThreads, num_sms() * 8), kThreads, 0, s>>>(
+      reinterpret_cast<const float4*>(yacc), reinterpret_cast<uint2*>(y), n4);
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4moe

@@ -112,8 +112,9 @@ class MoeConfig:
 
 # Zipf-skewed routing: logits = N(0,1) + beta * ln p_e with p_e proportional to rank_e^-1.2.
 # beta was chosen by tests/golden/calibrate_zipf_beta.py (which routes with the oracle) so that
-# the most popular expert receives about 4000 of the 16384*4 assignments.
-ZIPF_BETA = 1.6
+# the most popular expert receives about 4000 of the 16384*4 assignments; observed loads with
+# seed 0 run from 532 to 4002 tokens per expert.
+ZIPF_BETA = 0.2373
 
 CONFIGS = {
     "tiny": MoeConfig(0, "tiny", (16,), 256, 8, 2, 512, 0.02,

@@ -1,0 +1,87 @@
+"""The C-ABI library loads without a GPU, exports every function include/*.h declares, and rejects
+bad arguments on the host before touching the device."""
+import ctypes as C
+import glob
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from nvfp4_mixture_experts_softmax_gb300 import _build
+    _build.build()
+    import nvfp4_mixture_experts_softmax_gb300 as m
+    m.lib()
+    return m
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b(moe_\w+)\s*\(", src, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_header_symbols_exported(moe):
+    names = declared_functions()
+    assert "moe_run" in names and len(names) >= 12
+    lib = C.CDLL(moe.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert names == set(moe.EXPORTED)
+
+
+def test_status_strings(moe):
+    for code in range(-7, 1):
+        assert moe.status_string(code)
+    assert moe.status_string(-99) == "unknown status"
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(num_experts=8, hidden=256, inter=512, top_k=2), 0),
+    (dict(num_experts=8, hidden=256, inter=512, top_k=9), -1),
+    (dict(num_experts=0, hidden=256, inter=512, top_k=1), -1),
+    (dict(num_experts=8, hidden=200, inter=512, top_k=2), -2),
+    (dict(num_experts=8, hidden=256, inter=100, top_k=2), -2),
+    (dict(num_experts=2048, hidden=256, inter=256, top_k=2), -2),
+    (dict(num_experts=64, hidden=256, inter=256, top_k=33), -2),
+    (dict(num_experts=8, hidden=256, inter=512, top_k=2, shared_inter=256), -2),
+    (dict(num_experts=8, hidden=256, inter=512, top_k=2, h_tensor_scale=0.0), -1),
+    (dict(num_experts=8, hidden=256, inter=512, top_k=2, h_tensor_scale=float("nan")), -1),
+])
+def test_config_check(moe, kw, want):
+    assert moe.config_check(moe.make_config(**kw)) == want
+
+
+def test_sizes(moe):
+    cfg = moe.make_config(128, 2048, 768, 8)
+    # weights: per expert 3 * H * I * (1/2 + 1/16) bytes, plus the tensor scales
+    assert moe.weights_size(cfg) >= 128 * 3 * 2048 * 768 * 9 // 16
+    assert moe.weights_size(cfg) < 128 * 3 * 2048 * 768 * 9 // 16 + 4096
+    assert moe.workspace_size(cfg, 64) > moe.workspace_size(cfg, 1) > 0
+    assert moe.workspace_size(moe.make_config(8, 200, 512, 2), 4) == 0
+    shared = moe.make_config(256, 7168, 2048, 8, shared_inter=2048)
+    assert moe.weights_size(shared) > moe.weights_size(moe.make_config(256, 7168, 2048, 8))
+
+
+def test_host_side_rejections(moe):
+    L = moe.lib()
+    cfg = moe.make_config(8, 256, 512, 2)
+    # null / undersized buffers are rejected before any device work
+    assert L.moe_quantize_act(None, 4, 256, None, None, None, None, 0, None) == -3
+    assert L.moe_quantize_act(None, 4, 250, None, None, None, None, 0, None) == -1
+    assert L.moe_plan(None, 4, 8, 9, None, None, None, None, None, None, None, 0, None) == -1
+    assert L.moe_plan(None, 4, 2048, 2, None, None, None, None, None, None, None, 0, None) == -2
+    assert L.moe_run(C.byref(cfg), None, None, None, 4, 2, None, None, 0, None, None) == -1
+    assert L.moe_run(C.byref(cfg), None, None, None, 4, 3, None, None, 0, None, None) == -1
+    assert L.moe_quantize_weights(C.byref(cfg), None, None, None, None, None, None, None, 0, None) == -1
+    assert L.moe_weights_export(C.byref(cfg), None, 0, 0, None, None, None, None) == -1
+    st = C.c_int32(0)
+    assert L.moe_last_device_status(None, C.byref(st)) == -1

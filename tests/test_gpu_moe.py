@@ -1,0 +1,131 @@
+"""GPU parity of the whole layer (moe_run through the C ABI) against the oracle.
+
+Bit-exact: activation codes / scales / tensor scale, router ids, counts, offsets, permutation.
+Within the layer's bounds: the requantised intermediate (<= 0.1% codes off by one step) and the
+output (relative L2 <= 5e-3, max |err| <= 3e-2 * RMS).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from parity import assert_h_close, assert_y_close, oracle_experts_from
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import nvfp4_mixture_experts_softmax_gb300 as m
+    m.lib()
+    return m
+
+
+def run_and_check(moe, cs, T, logits=None):
+    dev = "cuda"
+    k = cs.top_k
+    x = synth.gen_x(cs, T, device=dev)
+    if logits is None:
+        logits = synth.gen_logits(cs, T, device=dev)
+    wg, wu, wd = synth.gen_all_experts(cs, device=dev)
+    sh = synth.gen_shared(cs, device=dev) if cs.shared_inter else None
+    cfg = moe.make_config(cs.experts, cs.hidden, cs.inter, k, shared_inter=cs.shared_inter,
+                          max_tokens=T)
+    wbuf = moe.quantize_weights(cfg, wg, wu, wd, shared=sh)
+    ws = torch.empty(moe.workspace_size(cfg, T), dtype=torch.uint8, device=dev)
+    y, dbg = moe.run(cfg, wbuf, x, logits, workspace=ws, debug=True)
+    assert moe.last_device_status(ws) == 0
+
+    lg = logits.cpu().numpy()
+    xq, xsf, ts_a, st = oracle.quantize_bf16(x.cpu())
+    assert st == 0
+    ids_o, _ = oracle.router(lg, k)
+    experts = oracle_experts_from(wg, wu, wd, ids_o)
+    sho = oracle.QuantExpert.from_bf16(*[s.cpu() for s in sh]) if sh is not None else None
+    y_ref, od = oracle.moe_forward(xq, xsf, ts_a, lg, experts, k, shared=sho, want_debug=True)
+
+    g = {n: t.cpu().numpy() for n, t in dbg.items()}
+    assert g["ts_a"][0] == ts_a
+    assert np.array_equal(g["xq"], xq) and np.array_equal(g["xsf"], xsf)
+    assert np.array_equal(g["topk_ids"], od["ids"])
+    assert np.allclose(g["topk_w"], od["w"], rtol=4e-7, atol=1e-9)
+    assert np.array_equal(g["counts"], od["counts"])
+    assert np.array_equal(g["offsets"], od["offsets"])
+    assert np.array_equal(g["perm_src"], od["perm_src"])
+    assert np.array_equal(g["inv"], od["inv"])
+    R = T * k
+    assert_h_close(g["hq"][:R], g["hsf"][:R], od["hq"], od["hsf"])
+    if sh is not None:
+        assert_h_close(g["hq"][R:], g["hsf"][R:], od["shq"], od["shsf"])
+    rel, mx = assert_y_close(y.float().cpu().numpy(), oracle.bf16_bits_to_f32(y_ref))
+    return y, rel, mx
+
+
+@pytest.mark.parametrize("T", [16])
+def test_tiny(moe, T):
+    run_and_check(moe, synth.CONFIGS["tiny"], T)
+
+
+@pytest.mark.parametrize("T", [1, 8, 32, 64])
+def test_decode(moe, T):
+    run_and_check(moe, synth.CONFIGS["decode"], T)
+
+
+SMALL = [
+    # several 128-row tiles per expert with a ragged last tile
+    synth.custom_config("two_experts_many_rows", 300, 256, 2, 1, 256, config_id=120),
+    # more experts than tokens: several experts stay empty
+    synth.custom_config("empty_experts", 5, 256, 12, 1, 256, config_id=121),
+    # k = E
+    synth.custom_config("k_eq_e", 9, 256, 4, 4, 512, config_id=122),
+    # shared expert
+    synth.custom_config("shared", 20, 512, 6, 2, 256, shared_inter=256, config_id=123),
+    # a single expert, a single token
+    synth.custom_config("single", 1, 256, 1, 1, 256, config_id=124),
+    # wider K and N than the tiny layer, ragged rows
+    synth.custom_config("ragged_wide", 37, 1024, 16, 3, 768, config_id=125),
+]
+
+
+@pytest.mark.parametrize("cs", SMALL, ids=lambda c: c.name)
+def test_small_shapes(moe, cs):
+    run_and_check(moe, cs, cs.tokens[0])
+
+
+def test_popular_expert_many_tiles(moe):
+    cs = synth.custom_config("popular", 700, 512, 8, 2, 256, config_id=126)
+    lg = synth.gen_logits(cs, 700)
+    lg[:, 3] += 50.0      # expert 3 gets every token: 6 tiles of 128 rows
+    run_and_check(moe, cs, 700, logits=lg.cuda())
+
+
+def test_repeat_calls_consistent(moe):
+    cs = synth.CONFIGS["tiny"]
+    y1, _, _ = run_and_check(moe, cs, 16)
+    y2, _, _ = run_and_check(moe, cs, 16)
+    d = (y1.float() - y2.float()).abs().max().item()
+    assert d <= 1e-2 * y1.float().abs().max().item()
+
+
+def test_zero_tokens_and_errors(moe):
+    cs = synth.CONFIGS["tiny"]
+    cfg = moe.make_config(cs.experts, cs.hidden, cs.inter, cs.top_k)
+    wg, wu, wd = synth.gen_all_experts(cs, device="cuda")
+    wbuf = moe.quantize_weights(cfg, wg, wu, wd)
+    x = torch.zeros(0, cs.hidden, dtype=torch.bfloat16, device="cuda")
+    lg = torch.zeros(0, cs.experts, device="cuda")
+    y = moe.run(cfg, wbuf, x, lg)
+    assert y.shape == (0, cs.hidden)
+    x = synth.gen_x(cs, 4, device="cuda")
+    lg = synth.gen_logits(cs, 4, device="cuda")
+    with pytest.raises(RuntimeError, match="INVALID_ARG"):
+        moe.run(cfg, wbuf, x, lg, k=cs.top_k + 1)
+    small_ws = torch.empty(1024, dtype=torch.uint8, device="cuda")
+    with pytest.raises(RuntimeError, match="WORKSPACE_TOO_SMALL"):
+        moe.run(cfg, wbuf, x, lg, workspace=small_ws)
+    bad = moe.make_config(cs.experts, 200, cs.inter, cs.top_k)      # H not a multiple of 256
+    with pytest.raises(RuntimeError, match="UNSUPPORTED_SHAPE"):
+        moe.quantize_weights(bad, wg, wu, wd)
