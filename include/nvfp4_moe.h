@@ -144,6 +144,28 @@ int moe_plan(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* topk
              void* workspace, size_t ws_bytes, moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * moe_plan_static: moe_plan without a workspace argument.  It has no counterpart on the pages
+ * this library follows; it exists for callers that cannot allocate device memory (a plugin whose
+ * host framework owns every device allocation, code running while a memory pool is frozen or
+ * capped, a plain C caller without an allocator).  Its scratch is a file-scope static device
+ * array of MOE_PLAN_STATIC_SCRATCH_BYTES bytes that every GPU loading the library keeps until
+ * the process exits.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - Arguments and outputs are those of moe_plan; the caller still owns every output buffer.
+ *   - A problem whose moe_plan_workspace_size(T, E, k) exceeds MOE_PLAN_STATIC_SCRATCH_BYTES is
+ *     rejected with MOE_ERR_WORKSPACE_TOO_SMALL: ceil(T/64)*E must stay within 131,040 for
+ *     k <= 16 (ceil(T/32)*E for larger k), e.g. T = 8,192 tokens at E = 1,024 experts.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
+ *     that device current; make that first call before any stream capture.
+ *   - All calls share the one array per device, and it keeps the last call's contents: calls
+ *     that may overlap on the GPU (two streams, two threads) race and must be serialised by the
+ *     caller.  The device status word in the array is cleared at the start of every call.
+ * ------------------------------------------------------------------------------------------- */
+#define MOE_PLAN_STATIC_SCRATCH_BYTES (1u << 20)
+int moe_plan_static(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* topk_ids,
+                    float* topk_w, int32_t* counts, int32_t* offsets, int32_t* perm_src,
+                    int32_t* inv, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
  * The layer.  wbuf: written by moe_quantize_weights for the same cfg.  x [T,H] BF16 (16-byte
  * aligned), logits [T,E] FP32, y [T,H] BF16 out.  k must equal cfg->top_k.  T == 0 is MOE_OK.
  * workspace: >= moe_workspace_size(cfg, T) bytes, 256-byte aligned.  debug: NULL, or a host

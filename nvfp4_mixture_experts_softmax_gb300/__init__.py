@@ -23,7 +23,7 @@ STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED_SHAPE
 EXPORTED = ["moe_status_string", "moe_config_check", "moe_weights_size", "moe_quantize_weights",
             "moe_weights_export", "moe_act_workspace_size", "moe_quantize_act",
             "moe_plan_workspace_size", "moe_plan", "moe_workspace_size", "moe_run",
-            "moe_last_device_status"]
+            "moe_last_device_status", "moe_plan_static"]
 
 
 class MoeConfig(C.Structure):
@@ -70,6 +70,7 @@ def lib():
             "moe_workspace_size": (sz, [cfgp, i32]),
             "moe_run": (C.c_int, [cfgp, vp, vp, vp, i32, i32, vp, vp, sz, vp, C.POINTER(MoeDebug)]),
             "moe_last_device_status": (C.c_int, [vp, C.POINTER(C.c_int32)]),
+            "moe_plan_static": (C.c_int, [vp, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -169,6 +170,25 @@ def plan(logits, k: int, workspace=None, stream=None):
                           _ptr(out["counts"]), _ptr(out["offsets"]), _ptr(out["perm_src"]),
                           _ptr(out["inv"]), _ptr(workspace), workspace.numel(), _stream(stream)),
            "moe_plan")
+    return out
+
+
+def plan_static(logits, k: int, out=None, stream=None):
+    """moe_plan through moe_plan_static: no workspace argument, for callers that cannot
+    allocate device memory (the library's static per-device scratch is used; calls on several
+    streams at once race).  ``out`` may pass preallocated output tensors."""
+    T, E = logits.shape
+    dev = logits.device
+    if out is None:
+        out = dict(topk_ids=torch.empty(T, k, dtype=torch.int32, device=dev),
+                   topk_w=torch.empty(T, k, dtype=torch.float32, device=dev),
+                   counts=torch.empty(E, dtype=torch.int32, device=dev),
+                   offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                   perm_src=torch.empty(T * k, dtype=torch.int32, device=dev),
+                   inv=torch.empty(T * k, dtype=torch.int32, device=dev))
+    _check(lib().moe_plan_static(_ptr(logits), T, E, k, _ptr(out["topk_ids"]), _ptr(out["topk_w"]),
+                                 _ptr(out["counts"]), _ptr(out["offsets"]), _ptr(out["perm_src"]),
+                                 _ptr(out["inv"]), _stream(stream)), "moe_plan_static")
     return out
 
 

@@ -85,3 +85,5 @@ def test_host_side_rejections(moe):
     assert L.moe_weights_export(C.byref(cfg), None, 0, 0, None, None, None, None) == -1
     st = C.c_int32(0)
     assert L.moe_last_device_status(None, C.byref(st)) == -1
+    assert L.moe_plan_static(None, 4, 8, 9, None, None, None, None, None, None, None) == -1
+    assert L.moe_plan_static(None, 1 << 24, 1024, 8, None, None, None, None, None, None, None) == -3
