@@ -196,7 +196,15 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
 
   cudaEvent_t* ev = (debug && debug->stage_events) ? reinterpret_cast<cudaEvent_t*>(debug->stage_events)
                                                     : nullptr;
-  auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], s) : cudaSuccess; };
+  // inside a stream capture the events must become record nodes of the graph
+  cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+  if (ev && cudaStreamIsCapturing(s, &capture) != cudaSuccess) return MOE_ERR_CUDA;
+  auto mark = [&](int i) {
+    if (!ev) return cudaSuccess;
+    return capture == cudaStreamCaptureStatusActive
+               ? cudaEventRecordWithFlags(ev[i], s, cudaEventRecordExternal)
+               : cudaEventRecord(ev[i], s);
+  };
 
   cudaError_t e = mark(0);
   if (e == cudaSuccess) e = cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s);
@@ -239,8 +247,8 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
   g.a_codes = ws + L.xq;
   g.a_sf = ws + L.xsf;
   g.a_gather = i32(L.perm_src);
-  g.b_sf = wb + W.w13_sf;
-  g.b_sf_per_seg = W.w13_sf_per_e;
+  g.b_tiles = wb + W.w13;
+  g.b_per_seg = W.w13_per_e;
   g.w_ts = w_ts;
   g.seg_off = i32(L.seg_off);
   g.tile_start = i32(L.tile_start);
@@ -258,7 +266,7 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
   g.a_rows = T;
   g.out_rows = L.Rt;
   g.y_rows = T;
-  e = launch_grouped_gemm(g, wb + W.w13_codes, W.Et * 2 * I, s);
+  e = launch_grouped_gemm(g, s);
   if (e == cudaSuccess) e = mark(3);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
@@ -267,8 +275,8 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
   g2.a_codes = ws + L.hq;
   g2.a_sf = ws + L.hsf;
   g2.a_gather = nullptr;
-  g2.b_sf = wb + W.w2_sf;
-  g2.b_sf_per_seg = W.w2_sf_per_e;
+  g2.b_tiles = wb + W.w2;
+  g2.b_per_seg = W.w2_per_e;
   g2.N = H;
   g2.K = I;
   g2.mode = 1;
@@ -278,7 +286,7 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
   g2.max_items = (int)std::min<int64_t>(max_mtiles * (g2.N / kBN), INT32_MAX);
   g2.max_ctas = g2.max_items;
   g2.a_rows = L.Rt;
-  e = launch_grouped_gemm(g2, wb + W.w2_codes, W.Et * H, s);
+  e = launch_grouped_gemm(g2, s);
   if (e == cudaSuccess) e = mark(4);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 

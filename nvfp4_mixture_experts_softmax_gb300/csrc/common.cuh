@@ -74,6 +74,27 @@ __device__ __forceinline__ void quant_block16(const float* x, float ts, uint32_t
   hi = e2m1x8(q[8], q[9], q[10], q[11], q[12], q[13], q[14], q[15]);
 }
 
+// The same block quantisation with reciprocal multiplies instead of divisions, for the
+// intermediate h of the layer (whose codes are compared within one code step, not bit for bit):
+//   sf = E4M3(max|x| * (1/6) * inv_ts); code_i = E2M1(x_i * (1 / (decode(sf) * ts))).
+// It differs from quant_block16 only when a quotient lies within an ulp of a rounding boundary.
+__device__ __forceinline__ void quant_block16_fast(const float* x, float ts, float inv_ts,
+                                                   uint32_t& lo, uint32_t& hi, uint32_t& sf) {
+  float bamax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) bamax = fmaxf(bamax, fabsf(x[i]));
+  lo = hi = 0u;
+  sf = 0u;
+  if (bamax == 0.0f) return;
+  sf = f32_to_e4m3(bamax * (1.0f / 6.0f) * inv_ts);
+  const float S = e4m3_to_f32(sf) * ts;
+  if (S == 0.0f) return;
+  const float r = __frcp_rn(S);
+  lo = e2m1x8(x[0] * r, x[1] * r, x[2] * r, x[3] * r, x[4] * r, x[5] * r, x[6] * r, x[7] * r);
+  hi = e2m1x8(x[8] * r, x[9] * r, x[10] * r, x[11] * r, x[12] * r, x[13] * r, x[14] * r,
+              x[15] * r);
+}
+
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
 
 // ---------------------------------------------------------------------------------------------
@@ -118,16 +139,21 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 }
 
 // Waits for the phase with the given parity; gives up after `limit_ns` nanoseconds, records
-// MOE_ERR_DEVICE_TIMEOUT in the status word and returns false.
+// MOE_ERR_DEVICE_TIMEOUT in the status word and returns false.  The clock is read only every
+// 1024 polls so that a wait which is about to succeed costs no more than the poll itself.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                                   int32_t* status) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  while (true) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > limit_ns) {
-      set_status(status, MOE_ERR_DEVICE_TIMEOUT);
-      return false;
+    if ((i & 1023u) == 1023u) {
+      const uint64_t now = global_timer_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > limit_ns) {
+        set_status(status, MOE_ERR_DEVICE_TIMEOUT);
+        return false;
+      }
     }
   }
 }

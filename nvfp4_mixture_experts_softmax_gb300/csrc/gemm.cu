@@ -12,16 +12,13 @@
 // One CTA per SM, warp-specialised (the pages' design uses TMA / MMA / epilogue / scheduler warps;
 // here the scheduler is a static round robin over a device-built tile list):
 //   warps 0-3  epilogue: tensor memory -> registers -> global, one accumulator row per thread;
-//   warp  4    TMA: weight tile (2-D tensor map, 128B swizzle) + its pre-arranged scale block;
+//   warp  4    TMA: one bulk copy per stage of the pre-swizzled weight block and its scales;
 //   warp  5    tensor-memory allocation and the single MMA-issuing thread;
 //   warps 6-9  activation rows gathered with cp.async into the same 128B-swizzled layout, and
 //              their scales into the 32x4x4 arrangement the scale-factor copy expects.
 // A 5-stage shared-memory ring (mbarrier full/empty pairs) feeds the MMA; two 128-column FP32
 // accumulators in tensor memory let the epilogue of one tile overlap the main loop of the next.
 // Every wait is bounded in time and reports MOE_ERR_DEVICE_TIMEOUT instead of hanging.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include "common.cuh"
 #include "internal.h"
 
@@ -35,12 +32,15 @@ constexpr int kTmaWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kProdWarp0 = 6;
 constexpr int kProdWarps = 4;
-constexpr int kProdThreads = kProdWarps * 32;
 constexpr int kThreads = (kProdWarp0 + kProdWarps) * 32;
+// Stage layout: A codes | A scales | B codes | B scales.  B codes + scales are one packed weight
+// block (kTileBlockBytes contiguous bytes in global memory), loaded with a single bulk copy.
 constexpr int kABytes = kBM * 128;
-constexpr int kBBytes = kBN * 128;
-constexpr int kSfBytes = 4 * 512;  // four 512-byte scale blocks (one per 64-wide MMA K step)
-constexpr int kStageBytes = kABytes + kBBytes + 2 * kSfBytes;
+constexpr int kSfBytes = 4 * 512;  // four 512-byte scale groups (one per 64-wide MMA K step)
+constexpr int kBOff = kABytes + kSfBytes;
+constexpr int kStageBytes = kBOff + kTileBlockBytes;
+static_assert(kBN == 128 && kTileBlockBytes == kBN * 128 + kSfBytes, "packed block = B stage");
+static_assert(kBOff % 1024 == 0, "B tile stays 1024-byte aligned for the 128B swizzle");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = kBN;
 constexpr uint32_t kSfCol0 = 2 * kAccCols;
@@ -78,12 +78,19 @@ __device__ __forceinline__ TileInfo decode_tile(int item, int n_tiles, const int
   return t;
 }
 
+// silu(g) * u with the fast exponential and division (h is requantised to NVFP4 right after;
+// for g < -88 the denominator overflows to inf and the quotient is a signed zero).
 __device__ __forceinline__ float silu_mul(float g, float u) {
-  return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs p) {
+// Tile row r is placed at accumulator lane (r % 4) * 32 + r / 4, so that the valid rows of a
+// nearly empty tile (decode) are spread over the four epilogue warps instead of all landing in
+// the first one.  lane_of_row and row_of_lane are inverse bijections of [0, 128).
+__device__ __forceinline__ int lane_of_row(int r) { return (r & 3) * 32 + (r >> 2); }
+__device__ __forceinline__ int row_of_lane(int l) { return (l & 31) * 4 + (l >> 5); }
+
+__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -108,7 +115,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(full + s), kProdThreads + 1);
+      mbar_init(smem_u32(full + s), 2);  // one producer warp + the TMA thread
       mbar_init(smem_u32(empty + s), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -118,8 +125,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(drain), 1);
     fence_barrier_init();
   }
-  if (warp == kTmaWarp && lane == 0)
-    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_b) : "memory");
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -142,18 +147,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
         const TileInfo t = decode_tile(item, n_tiles, s_tile, s_seg, p.nseg);
-        const int brow = t.seg * p.N + t.nt * kBN;
-        const uint8_t* sfsrc = p.b_sf + (size_t)t.seg * p.b_sf_per_seg +
-                               (size_t)(t.nt * kBN / 128) * (p.K / 64) * 512;
+        const uint8_t* bsrc = p.b_tiles + (size_t)t.seg * p.b_per_seg +
+                              (size_t)t.nt * kst * kTileBlockBytes;
         for (int ks = 0; ks < kst; ++ks) {
           if (!mbar_wait_bounded(smem_u32(empty + stage), phase ^ 1u, kWaitLimitNs, p.status)) {
             ok = false;
             break;
           }
           const uint32_t sb = smem0 + stage * kStageBytes;
-          mbar_arrive_expect_tx(smem_u32(full + stage), kBBytes + kSfBytes);
-          tma_load_2d(sb + kABytes, &tmap_b, ks * 128, brow, smem_u32(full + stage));
-          bulk_load(sb + kABytes + kBBytes + kSfBytes, sfsrc + (size_t)ks * kSfBytes, kSfBytes,
+          mbar_arrive_expect_tx(smem_u32(full + stage), kTileBlockBytes);
+          bulk_load(sb + kBOff, bsrc + (size_t)ks * kTileBlockBytes, kTileBlockBytes,
                     smem_u32(full + stage));
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
@@ -190,8 +193,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t sb = smem0 + stage * kStageBytes;
-          const uint32_t sfa_s = sb + kABytes + kBBytes;
-          const uint32_t sfb_s = sfa_s + kSfBytes;
+          const uint32_t sfa_s = sb + kABytes;
+          const uint32_t sfb_s = sb + kBOff + kTileBytes;
           const uint32_t sf_t = tmem_base + kSfCol0 + stage * kSfColsPerStage;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
@@ -202,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t ad = smem_desc(sb + kk * 32, 16, 1024, kLayoutSwizzle128B);
-            const uint64_t bd = smem_desc(sb + kABytes + kk * 32, 16, 1024, kLayoutSwizzle128B);
+            const uint64_t bd = smem_desc(sb + kBOff + kk * 32, 16, 1024, kLayoutSwizzle128B);
             tc_mma_mxf4nvf4(d_tmem, ad, bd, idesc, sf_t + kk * 4, sf_t + 16 + kk * 4,
                             (ks | kk) != 0 ? 1u : 0u);
           }
@@ -217,81 +220,86 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kProdWarp0) {
     // ---------------- activation rows (cp.async gather) ----------------
-    const int pt = threadIdx.x - kProdWarp0 * 32;  // 0..127
+    // Producer warp wp owns every kProdWarps-th pipeline stage.  For a stage it owns it copies the
+    // valid rows' 128-byte K slices into the 128B-swizzled layout and their scale words into the
+    // 32x4x4 scale arrangement, waits for its own copies, fences them for the tensor core's async
+    // proxy and arrives on the stage's full barrier.  Stages owned by different warps are in
+    // flight together, so no stage waits on an earlier stage's copies.  Rows past the tile's last
+    // valid row are not written: their accumulator rows are never stored.
+    const int wp = warp - kProdWarp0;
     int stage = 0;
     uint32_t phase = 0;
-    int pending = -1;
+    int j = 0;  // pipeline stages issued so far by the CTA (all warps count them alike)
     bool ok = true;
     for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
       const TileInfo t = decode_tile(item, n_tiles, s_tile, s_seg, p.nseg);
-      // this thread copies 16-byte chunk (pt % 8) of rows pt/8 + 16*i, i = 0..7, and the four
-      // scale words of row pt
-      const uint8_t* crow[8];
-      uint32_t cbytes[8];
+      const int first_own = (wp - (j % kProdWarps) + kProdWarps) % kProdWarps;
+      int src[4] = {-1, -1, -1, -1};  // source row of tile rows lane + 32 i
+      if (first_own < kst) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int r = (pt >> 3) + 16 * i;
-        const int pr = t.m0 + r;
-        const int src = (r < t.rows && pr >= 0 && pr < p.out_rows)
-                            ? (p.a_gather ? __ldg(p.a_gather + pr) : pr) : -1;
-        if (src >= 0 && src < p.a_rows) {
-          crow[i] = p.a_codes + (size_t)src * (p.K / 2) + (pt & 7) * 16;
-          cbytes[i] = 16;
-        } else {
-          if (r < t.rows) set_status(p.status, MOE_ERR_INVALID_ARG);
-          crow[i] = p.a_codes;
-          cbytes[i] = 0;
+        for (int i = 0; i < 4; ++i) {
+          const int r = lane + 32 * i;
+          const int pr = t.m0 + r;
+          if (r < t.rows) {
+            int sr = -1;
+            if (pr >= 0 && pr < p.out_rows) sr = p.a_gather ? __ldg(p.a_gather + pr) : pr;
+            if (sr < 0 || sr >= p.a_rows) {
+              set_status(p.status, MOE_ERR_INVALID_ARG);
+              sr = -1;
+            }
+            src[i] = sr;
+          }
         }
       }
-      const uint8_t* srow;
-      uint32_t sbytes;
-      const int spr = t.m0 + pt;
-      const int ssrc = (pt < t.rows && spr >= 0 && spr < p.out_rows)
-                           ? (p.a_gather ? __ldg(p.a_gather + spr) : spr) : -1;
-      if (ssrc >= 0 && ssrc < p.a_rows) {
-        srow = p.a_sf + (size_t)ssrc * (p.K / 16);
-        sbytes = 4;
-      } else {
-        srow = p.a_sf;
-        sbytes = 0;
-      }
-      for (int ks = 0; ks < kst; ++ks) {
-        if (!mbar_wait_bounded(smem_u32(empty + stage), phase ^ 1u, kWaitLimitNs, p.status)) {
-          ok = false;
-          break;
-        }
-        const uint32_t sb = smem0 + stage * kStageBytes;
+      for (int ks = 0; ks < kst; ++ks, ++j) {
+        if (j % kProdWarps == wp) {
+          if (!mbar_wait_bounded(smem_u32(empty + stage), phase ^ 1u, kWaitLimitNs, p.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sb = smem0 + stage * kStageBytes;
+          // codes: 16-byte chunk (lane & 7) of rows (lane >> 3) + 4 i
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int r = (pt >> 3) + 16 * i;
-          const uint32_t dst = sb + r * 128 + ((((pt & 7) ^ (r & 7))) << 4);
-          cp_async_16(dst, crow[i] + (cbytes[i] ? ks * 128 : 0), cbytes[i]);
-        }
-        const uint32_t sfa_s = sb + kABytes + kBBytes + (pt & 31) * 16 + (pt >> 5) * 4;
+          for (int i = 0; i < 32; ++i) {
+            if (4 * i >= t.rows) break;
+            const int r = (lane >> 3) + 4 * i;
+            const int sr = __shfl_sync(0xffffffffu, src[i >> 3], r & 31);
+            if (r < t.rows && sr >= 0) {
+              const int c = lane & 7, L = lane_of_row(r);
+              cp_async_16(sb + L * 128 + ((c ^ (L & 7)) << 4),
+                          p.a_codes + (size_t)sr * (p.K / 2) + ks * 128 + c * 16, 16);
+            }
+          }
+          // scales: word (lane & 3) of rows (lane >> 2) + 8 i
+          const uint32_t sfa_s = sb + kABytes;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          cp_async_4(sfa_s + kk * 512, srow + (sbytes ? ks * 16 + kk * 4 : 0), sbytes);
-        cp_async_commit();
-        if (pending >= 0) {
-          cp_async_wait<1>();
+          for (int i = 0; i < 16; ++i) {
+            if (8 * i >= t.rows) break;
+            const int r = (lane >> 2) + 8 * i;
+            const int sr = __shfl_sync(0xffffffffu, src[i >> 2], r & 31);
+            if (r < t.rows && sr >= 0) {
+              const int kk = lane & 3, L = lane_of_row(r);
+              cp_async_4(sfa_s + kk * 512 + (L & 31) * 16 + (L >> 5) * 4,
+                         p.a_sf + (size_t)sr * (p.K / 16) + ks * 16 + kk * 4, 4);
+            }
+          }
+          cp_async_commit();
+          cp_async_wait<0>();
           fence_proxy_async_smem();
-          mbar_arrive(smem_u32(full + pending));
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(full + stage));
         }
-        pending = stage;
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
     }
     cp_async_wait<0>();
-    if (pending >= 0 && ok) {
-      fence_proxy_async_smem();
-      mbar_arrive(smem_u32(full + pending));
-    }
   } else {
     // ---------------- epilogue (warps 0-3) ----------------
     uint32_t acc_phase[2] = {0u, 0u};
     int it = 0;
-    const int r = warp * 32 + lane;
+    const int r = row_of_lane(warp * 32 + lane);   // this thread's accumulator lane -> tile row
     const float ts_a = p.mode == 0 ? *p.ts_a : 0.0f;
+    const float inv_ts_h = 1.0f / p.ts_h;
     for (int item = blockIdx.x; item < total; item += gridDim.x, ++it) {
       const TileInfo t = decode_tile(item, n_tiles, s_tile, s_seg, p.nseg);
       const int abuf = it & 1;
@@ -317,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 16; ++i)
               h[i] = silu_mul(__uint_as_float(v[i]) * ag, __uint_as_float(v[16 + i]) * au);
             uint32_t lo, hi, s;
-            quant_block16(h, p.ts_h, lo, hi, s);
+            quant_block16_fast(h, p.ts_h, inv_ts_h, lo, hi, s);
             const int f0 = t.nt * (kBN / 2) + c * 16;
             *reinterpret_cast<uint2*>(p.hq + (size_t)prow * (I / 2) + f0 / 2) = make_uint2(lo, hi);
             p.hsf[(size_t)prow * (I / 16) + f0 / 16] = (uint8_t)s;
@@ -367,39 +375,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
 size_t gemm_smem_bytes(int nseg) {
   return 1024 + (size_t)kStages * kStageBytes + 256 + sizeof(int32_t) * 2 * (nseg + 2);
 }
 
 }  // namespace
 
-cudaError_t launch_grouped_gemm(const GemmArgs& a, const uint8_t* b_codes, int b_rows_total,
-                                cudaStream_t s) {
-  auto encode = get_encode_fn();
-  if (!encode) return cudaErrorNotSupported;
-  CUtensorMap tmap;
-  const cuuint64_t dims[2] = {(cuuint64_t)(a.K / 2), (cuuint64_t)b_rows_total};
-  const cuuint64_t strides[1] = {(cuuint64_t)(a.K / 2)};
-  const cuuint32_t box[2] = {128, (cuuint32_t)kBN};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(b_codes), dims,
-                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s) {
   const size_t smem = gemm_smem_bytes(a.nseg);
   cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -407,7 +389,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, const uint8_t* b_codes, int b
   int grid = a.max_ctas;
   if (grid > num_sms()) grid = num_sms();
   if (grid < 1) grid = 1;
-  grouped_gemm_kernel<<<grid, kThreads, smem, s>>>(tmap, a);
+  grouped_gemm_kernel<<<grid, kThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -20,35 +20,56 @@ constexpr int kMmaK = 64;      // K of one block-scaled FP4 MMA
 // Router chunking: tokens per chunk (one router block and one scatter block each).
 inline int plan_tokens_per_chunk(int k) { return k <= 16 ? 64 : 32; }
 
-// Private layout of the packed-weight buffer.
-//   w13 codes [Et][2I][H/2]: row 32b+i is gate row 16b+i for i < 16, else up row 16b+i-16.
-//   w13 sf    [Et][2I/128][H/64][512 B]: per 128-row group and 64-wide K chunk, one 512-byte
-//             block with byte (n%32)*16 + ((n%128)/32)*4 + (k/16)%4 for row n, column k.
-//   w2 codes  [Et][H][I/2];  w2 sf [Et][H/128][I/64][512 B] (same arrangement).
-//   ts        [Et][4] FP32: gate, up, down tensor scales (the 4th is padding).
+// Private layout of the packed-weight buffer: every weight matrix is stored as GEMM-ready
+// blocks, one per (128-row N tile, 256-wide K stage), each block 18432 contiguous bytes:
+//   [0, 16384)      codes of the 128 rows x 128 bytes, row r at r*128, its 16-byte chunk c stored
+//                   at chunk position c ^ (r % 8) (the 128-byte swizzle the MMA descriptor uses);
+//   [16384, 18432)  E4M3 scales as four 512-byte groups (one per 64-wide MMA K step), row r's
+//                   scale word (4 scales) at (r % 32)*16 + (r / 32)*4 (the arrangement that the
+//                   tensor-memory scale copy expects).
+// A tile of the MMA's B operand for one pipeline stage is therefore one contiguous bulk copy.
+//   w13 [Et][2I/128][H/256][18432]: GEMM1 rows interleaved by 16 (rows 32b+i are gate rows
+//       16b+i for i < 16, up rows 16b+i-16 otherwise);
+//   w2  [Et][H/128][I/256][18432]: GEMM2 (down) rows;
+//   ts  [Et][4] FP32: gate, up, down tensor scales (the 4th is padding).
 // Et = E + 1 with a shared expert, which is stored last.
+constexpr int kTileBytes = 128 * 128;             // codes of one (N tile, K stage) block
+constexpr int kTileSfBytes = 4 * 512;             // its scales
+constexpr int kTileBlockBytes = kTileBytes + kTileSfBytes;
+
 struct WeightLayout {
   int E, Et, H, I;
-  size_t w13_codes, w13_sf, w2_codes, w2_sf, ts, total;
-  size_t w13_codes_per_e, w13_sf_per_e, w2_codes_per_e, w2_sf_per_e;
+  size_t w13, w2, ts, total;
+  size_t w13_per_e, w2_per_e;
   explicit WeightLayout(const moe_config& c) {
     E = c.num_experts;
     Et = E + (c.shared_inter > 0 ? 1 : 0);
     H = c.hidden;
     I = c.inter;
-    w13_codes_per_e = (size_t)2 * I * H / 2;
-    w13_sf_per_e = (size_t)2 * I * H / 16;
-    w2_codes_per_e = (size_t)H * I / 2;
-    w2_sf_per_e = (size_t)H * I / 16;
+    w13_per_e = (size_t)(2 * I / 128) * (H / 256) * kTileBlockBytes;
+    w2_per_e = (size_t)(H / 128) * (I / 256) * kTileBlockBytes;
     size_t o = 0;
-    w13_codes = o; o = align_up(o + w13_codes_per_e * Et);
-    w13_sf = o;    o = align_up(o + w13_sf_per_e * Et);
-    w2_codes = o;  o = align_up(o + w2_codes_per_e * Et);
-    w2_sf = o;     o = align_up(o + w2_sf_per_e * Et);
-    ts = o;        o = align_up(o + sizeof(float) * 4 * Et);
+    w13 = o; o = align_up(o + w13_per_e * Et);
+    w2 = o;  o = align_up(o + w2_per_e * Et);
+    ts = o;  o = align_up(o + sizeof(float) * 4 * Et);
     total = o;
   }
 };
+
+// Byte offsets of the code byte pair (row n, 16-block kb) and of its scale inside one packed
+// matrix with K columns (K a multiple of 256, rows a multiple of 128).
+__host__ __device__ __forceinline__ size_t packed_code_offset(int64_t n, int64_t kb, int64_t K) {
+  const int64_t kst = K / 256, r = n & 127;
+  const int64_t blk = (n >> 7) * kst + kb / 16;
+  const int64_t c = (kb % 16) >> 1;               // 16-byte chunk of the 128-byte row slice
+  return (size_t)(blk * kTileBlockBytes + r * 128 + ((c ^ (r & 7)) << 4) + (kb & 1) * 8);
+}
+__host__ __device__ __forceinline__ size_t packed_sf_offset(int64_t n, int64_t kb, int64_t K) {
+  const int64_t kst = K / 256, r = n & 127;
+  const int64_t blk = (n >> 7) * kst + kb / 16;
+  return (size_t)(blk * kTileBlockBytes + kTileBytes + ((kb % 16) >> 2) * 512 + (r & 31) * 16 +
+                  (r >> 5) * 4 + (kb & 3));
+}
 
 // Workspace of moe_run for T tokens.  Offset 0 holds the device status word.
 struct RunLayout {
@@ -130,10 +151,10 @@ struct GemmArgs {
   const uint8_t* a_codes;
   const uint8_t* a_sf;
   const int32_t* a_gather;
-  // B operand: expert s owns rows [s*N, (s+1)*N) of the codes tensor map and the packed scale
-  // block b_sf + s*b_sf_per_seg.
-  const uint8_t* b_sf;
-  size_t b_sf_per_seg;
+  // B operand: expert s's packed blocks start at b_tiles + s*b_per_seg ([N/128][K/256] blocks
+  // of kTileBlockBytes, see WeightLayout).
+  const uint8_t* b_tiles;
+  size_t b_per_seg;
   const float* w_ts;      // [nseg][4] tensor scales
   const int32_t* seg_off; // [nseg+1]
   const int32_t* tile_start;  // [nseg+1]
@@ -156,8 +177,7 @@ struct GemmArgs {
   int y_rows;             // rows of yacc (mode 1)
   int max_items;          // upper bound of m-tiles x n-tiles
 };
-cudaError_t launch_grouped_gemm(const GemmArgs& a, const uint8_t* b_codes, int b_rows_total,
-                                cudaStream_t s);
+cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s);
 
 cudaError_t launch_finalize(const float* yacc, void* y, int64_t n, cudaStream_t s);
 

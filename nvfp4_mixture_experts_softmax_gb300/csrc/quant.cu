@@ -116,11 +116,6 @@ __device__ __forceinline__ const uint16_t* matrix_ptr(const WeightSrc& w, int sl
   return slot < w.E ? w.routed[m] + (int64_t)slot * per : w.shared[m];
 }
 
-// Byte offset of the scale of (row n, 16-block kb) inside a packed [N/128][K/64][512] block array.
-__host__ __device__ __forceinline__ int64_t packed_sf_offset(int64_t n, int64_t kb, int64_t K) {
-  return ((n >> 7) * (K >> 6) + (kb >> 2)) * 512 + (n & 31) * 16 + ((n & 127) >> 5) * 4 + (kb & 3);
-}
-
 // Row of the gate (m=0) or up (m=1) row n inside the 16-interleaved w13 layout.
 __host__ __device__ __forceinline__ int64_t w13_row(int64_t n, int m) {
   return (n >> 4) * 32 + (m ? 16 : 0) + (n & 15);
@@ -151,12 +146,10 @@ __global__ void weight_ts_kernel(uint32_t* amax_bits_then_ts, int n) {
 }
 
 struct WeightDst {
-  uint8_t* w13_codes;
-  uint8_t* w13_sf;
-  uint8_t* w2_codes;
-  uint8_t* w2_sf;
+  uint8_t* w13;     // [Et][2I/128][H/256][block]
+  uint8_t* w2;      // [Et][H/128][I/256][block]
   const float* ts;  // [Et][4]
-  int64_t w13_codes_per_e, w13_sf_per_e, w2_codes_per_e, w2_sf_per_e;
+  int64_t w13_per_e, w2_per_e;
 };
 
 // One thread per 16-element block of one matrix row: quantise and store into the packed layout.
@@ -182,16 +175,10 @@ __global__ void __launch_bounds__(kThreads) weight_encode_kernel(WeightSrc w, We
     }
     uint32_t lo, hi, s;
     quant_block16(f, ts, lo, hi, s);
-    if (m < 2) {
-      const int64_t r = w13_row(n, m);
-      *reinterpret_cast<uint2*>(d.w13_codes + slot * d.w13_codes_per_e + r * (K / 2) + kb * 8) =
-          make_uint2(lo, hi);
-      d.w13_sf[slot * d.w13_sf_per_e + packed_sf_offset(r, kb, K)] = (uint8_t)s;
-    } else {
-      *reinterpret_cast<uint2*>(d.w2_codes + slot * d.w2_codes_per_e + n * (K / 2) + kb * 8) =
-          make_uint2(lo, hi);
-      d.w2_sf[slot * d.w2_sf_per_e + packed_sf_offset(n, kb, K)] = (uint8_t)s;
-    }
+    uint8_t* base = m < 2 ? d.w13 + slot * d.w13_per_e : d.w2 + slot * d.w2_per_e;
+    const int64_t r = m < 2 ? w13_row(n, m) : n;
+    *reinterpret_cast<uint2*>(base + packed_code_offset(r, kb, K)) = make_uint2(lo, hi);
+    base[packed_sf_offset(r, kb, K)] = (uint8_t)s;
   }
 }
 
@@ -203,18 +190,10 @@ __global__ void __launch_bounds__(kThreads) weight_export_kernel(WeightDst d, in
   for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblk;
        b += (int64_t)gridDim.x * blockDim.x) {
     const int64_t n = b / (K / 16), kb = b % (K / 16);
-    uint2 c;
-    uint8_t s;
-    if (m < 2) {
-      const int64_t r = w13_row(n, m);
-      c = *reinterpret_cast<const uint2*>(d.w13_codes + slot * d.w13_codes_per_e + r * (K / 2) +
-                                          kb * 8);
-      s = d.w13_sf[slot * d.w13_sf_per_e + packed_sf_offset(r, kb, K)];
-    } else {
-      c = *reinterpret_cast<const uint2*>(d.w2_codes + slot * d.w2_codes_per_e + n * (K / 2) +
-                                          kb * 8);
-      s = d.w2_sf[slot * d.w2_sf_per_e + packed_sf_offset(n, kb, K)];
-    }
+    const uint8_t* base = m < 2 ? d.w13 + slot * d.w13_per_e : d.w2 + slot * d.w2_per_e;
+    const int64_t r = m < 2 ? w13_row(n, m) : n;
+    const uint2 c = *reinterpret_cast<const uint2*>(base + packed_code_offset(r, kb, K));
+    const uint8_t s = base[packed_sf_offset(r, kb, K)];
     *reinterpret_cast<uint2*>(codes + n * (K / 2) + kb * 8) = c;
     sf[n * (K / 16) + kb] = s;
   }
@@ -241,15 +220,11 @@ int grid_for(int64_t work, int per_block, int cap) {
 
 WeightDst make_dst(const WeightLayout& L, uint8_t* wbuf) {
   WeightDst d;
-  d.w13_codes = wbuf + L.w13_codes;
-  d.w13_sf = wbuf + L.w13_sf;
-  d.w2_codes = wbuf + L.w2_codes;
-  d.w2_sf = wbuf + L.w2_sf;
+  d.w13 = wbuf + L.w13;
+  d.w2 = wbuf + L.w2;
   d.ts = reinterpret_cast<const float*>(wbuf + L.ts);
-  d.w13_codes_per_e = (int64_t)L.w13_codes_per_e;
-  d.w13_sf_per_e = (int64_t)L.w13_sf_per_e;
-  d.w2_codes_per_e = (int64_t)L.w2_codes_per_e;
-  d.w2_sf_per_e = (int64_t)L.w2_sf_per_e;
+  d.w13_per_e = (int64_t)L.w13_per_e;
+  d.w2_per_e = (int64_t)L.w2_per_e;
   return d;
 }
 

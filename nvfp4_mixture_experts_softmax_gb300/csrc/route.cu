@@ -1,8 +1,9 @@
 // Router top-k and the token -> expert plan (histogram, scan, stable scatter), all on the device.
 //
 // Router: one warp per token ("vllm.cpp docs/STATUS.md", row "DeepSeek-V4-Flash decode ds4-gap -
-// Lever 3 (route -> warp-topk)": experts spread over the lanes, per-lane arg-max, shuffle
-// reduction, mask and repeat).  Selection is on the raw logits under the strict order (value
+// Lever 3 (route -> warp-topk)": experts spread over the lanes, per-lane arg-max, warp
+// reduction, mask and repeat; here the reduction is two redux.sync instructions per round on an
+// order-preserving integer key).  Selection is on the raw logits under the strict order (value
 // descending, lower index on ties), which softmax preserves; the weights are
 // w_j = exp(l_j - l_0) / sum_{i<k} exp(l_i - l_0), summed in slot order (softmax restricted to
 // the chosen k and renormalised).
@@ -10,9 +11,10 @@
 // Plan: counts and offsets are built without any host read ("nvfp4-megamoe-kernel compare
 // pre-b1...master", "CATEGORY 3: Data-dependent control flow": device scatter into a preallocated
 // buffer instead of bincount).  Rows of one expert are ordered by ascending assignment index
-// t*k + j, so the permutation has exactly one correct value: each chunk of tokens counts its
-// assignments per expert, a scan turns the counts into per-(chunk, expert) bases, and the
-// scatter ranks assignments inside a chunk with warp match + per-warp counts.
+// t*k + j, so the permutation has exactly one correct value.  Small batches (T*k <= 2048) run
+// the whole plan in one block; larger ones count assignments per chunk of tokens, scan the
+// counts into per-(chunk, expert) bases, and rank assignments inside a chunk with warp match +
+// per-warp counts.
 #include <cfloat>
 
 #include "common.cuh"
@@ -24,60 +26,6 @@ namespace {
 
 constexpr int kRouterWarps = 8;
 constexpr int kMaxVpl = 32;  // experts per lane: E <= 1024
-
-template <int VPL>
-__global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(
-    const float* __restrict__ logits, int T, int E, int k, int tpc, int32_t* __restrict__ ids,
-    float* __restrict__ wout, int32_t* __restrict__ hist) {
-  extern __shared__ int32_t s_hist[];  // [E]
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
-  __syncthreads();
-  const int t_begin = blockIdx.x * tpc;
-  const int t_end = min(T, t_begin + tpc);
-  for (int t = t_begin + warp; t < t_end; t += kRouterWarps) {
-    const float* row = logits + (int64_t)t * E;
-    float v[VPL];
-    uint32_t taken = 0;
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E) v[i] = __ldg(row + e);
-      else { v[i] = -FLT_MAX; taken |= 1u << i; }
-    }
-    int my_id = 0;
-    float my_l = 0.0f;
-    for (int j = 0; j < k; ++j) {
-      int bi = -1;
-      float bv = 0.0f;
-#pragma unroll
-      for (int i = 0; i < VPL; ++i)
-        if (!((taken >> i) & 1u) && (bi < 0 || v[i] > bv)) { bv = v[i]; bi = i; }
-      int be = bi < 0 ? INT_MAX : lane + 32 * bi;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        const bool better = oe != INT_MAX &&
-                            (be == INT_MAX || ov > bv || (ov == bv && oe < be));
-        if (better) { bv = ov; be = oe; }
-      }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      if (lane == j) { my_id = be; my_l = bv; }
-    }
-    const float l0 = __shfl_sync(0xffffffffu, my_l, 0);
-    const float ex = lane < k ? expf(my_l - l0) : 0.0f;
-    float sum = 0.0f;
-    for (int j = 0; j < k; ++j) sum = sum + __shfl_sync(0xffffffffu, ex, j);
-    if (lane < k) {
-      ids[(int64_t)t * k + lane] = my_id;
-      wout[(int64_t)t * k + lane] = __fdiv_rn(ex, sum);
-      atomicAdd(&s_hist[my_id], 1);
-    }
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(int64_t)blockIdx.x * E + e] = s_hist[e];
-}
 
 // Exclusive scan of one value per thread over the block (blockDim.x <= 1024).
 __device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t* sw, int32_t& total) {
@@ -104,6 +52,152 @@ __device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t* sw, 
   const int32_t r = (warp ? sw[warp - 1] : 0) + x - v;
   __syncthreads();
   return r;
+}
+
+// Order-preserving map of a float to an unsigned key (larger float -> larger key); -0 is folded
+// into +0 so that the two compare equal, as floats do.
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t u = __float_as_uint(v == 0.0f ? 0.0f : v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Top-k of one token's logits by one warp: lane l holds experts l, l+32, ...  Each of the k
+// rounds takes the warp maximum of the lanes' best keys, then the lowest expert index among the
+// lanes holding it (hardware redux.sync), so ties go to the lower index.  Lane j < k ends with
+// the j-th choice (my_id, my_l).
+template <int VPL>
+__device__ __forceinline__ void warp_topk(const float* __restrict__ row, int E, int k, int lane,
+                                          int& my_id, float& my_l) {
+  float v[VPL];
+  uint32_t key[VPL];
+  uint32_t taken = 0;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      v[i] = __ldg(row + e);
+      key[i] = order_key(v[i]);
+    } else {
+      v[i] = 0.0f;
+      key[i] = 0u;
+      taken |= 1u << i;
+    }
+  }
+  my_id = 0;
+  my_l = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    int bi = -1;
+    uint32_t bk = 0u;
+    float bv = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)
+      if (!((taken >> i) & 1u) && (bi < 0 || key[i] > bk)) { bk = key[i]; bv = v[i]; bi = i; }
+    const uint32_t lane_key = bi < 0 ? 0u : bk;
+    const uint32_t mk = __reduce_max_sync(0xffffffffu, lane_key);
+    const uint32_t cand = (bi >= 0 && lane_key == mk) ? (uint32_t)(lane + 32 * bi) : 0xffffffffu;
+    const uint32_t be = __reduce_min_sync(0xffffffffu, cand);
+    const float wv = __shfl_sync(0xffffffffu, bv, (int)(be & 31u));
+    if ((int)(be & 31u) == lane) taken |= 1u << (be >> 5);
+    if (lane == j) { my_id = (int)be; my_l = wv; }
+  }
+}
+
+// Renormalised softmax weights of the k chosen logits, summed in slot order; lanes < k write.
+__device__ __forceinline__ float topk_weight(float my_l, int k, int lane) {
+  const float l0 = __shfl_sync(0xffffffffu, my_l, 0);
+  const float ex = lane < k ? expf(my_l - l0) : 0.0f;
+  float sum = 0.0f;
+  for (int j = 0; j < k; ++j) sum = sum + __shfl_sync(0xffffffffu, ex, j);
+  return __fdiv_rn(ex, sum);
+}
+
+// One warp per token; the per-chunk expert histogram (chunk = tpc tokens) is accumulated with
+// global atomics into `hist`, which the caller zeroes first.
+template <int VPL>
+__global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(
+    const float* __restrict__ logits, int T, int E, int k, int tpc, int32_t* __restrict__ ids,
+    float* __restrict__ wout, int32_t* __restrict__ hist) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kRouterWarps + warp;
+  if (t >= T) return;
+  int my_id;
+  float my_l;
+  warp_topk<VPL>(logits + (int64_t)t * E, E, k, lane, my_id, my_l);
+  const float w = topk_weight(my_l, k, lane);
+  if (lane < k) {
+    ids[(int64_t)t * k + lane] = my_id;
+    wout[(int64_t)t * k + lane] = w;
+    atomicAdd(hist + (int64_t)(t / tpc) * E + my_id, 1);
+  }
+}
+
+// The whole plan in one block for small batches (T*k <= kSmallPlanRows): route, count, scan,
+// and place every assignment at offsets[e] + #(earlier assignments to e).
+constexpr int kSmallPlanRows = 2048;
+constexpr int kSmallPlanThreads = 1024;
+
+template <int VPL>
+__global__ void __launch_bounds__(kSmallPlanThreads) plan_small_kernel(
+    const float* __restrict__ logits, int T, int E, int k, int shared_rows,
+    int32_t* __restrict__ ids, float* __restrict__ wout, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ tile_start,
+    int32_t* __restrict__ perm_src, float* __restrict__ perm_w, int32_t* __restrict__ inv) {
+  __shared__ int32_t s_cnt[1024];
+  __shared__ int32_t s_off[1024];
+  __shared__ int32_t s_ids[kSmallPlanRows];
+  __shared__ float s_w[kSmallPlanRows];
+  __shared__ int32_t sw[32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+  __syncthreads();
+  for (int t = warp; t < T; t += kSmallPlanThreads / 32) {
+    int my_id;
+    float my_l;
+    warp_topk<VPL>(logits + (int64_t)t * E, E, k, lane, my_id, my_l);
+    const float w = topk_weight(my_l, k, lane);
+    if (lane < k) {
+      ids[(int64_t)t * k + lane] = my_id;
+      wout[(int64_t)t * k + lane] = w;
+      s_ids[t * k + lane] = my_id;
+      s_w[t * k + lane] = w;
+      atomicAdd(&s_cnt[my_id], 1);
+    }
+  }
+  __syncthreads();
+  const int e = threadIdx.x;
+  const int32_t cnt = e < E ? s_cnt[e] : 0;
+  int32_t total, ttotal;
+  const int32_t off = block_exclusive_scan(cnt, sw, total);
+  const int32_t toff = block_exclusive_scan((cnt + kBM - 1) / kBM, sw, ttotal);
+  if (e < E) {
+    s_off[e] = off;
+    if (counts) counts[e] = cnt;
+    offsets[e] = off;
+    if (tile_start) tile_start[e] = toff;
+  }
+  if (threadIdx.x == 0) {
+    offsets[E] = total;
+    if (shared_rows > 0) offsets[E + 1] = total + shared_rows;
+    if (tile_start) {
+      tile_start[E] = ttotal;
+      if (shared_rows > 0) tile_start[E + 1] = ttotal + (shared_rows + kBM - 1) / kBM;
+    }
+  }
+  __syncthreads();
+  const int R = T * k;
+  for (int a = threadIdx.x; a < R; a += blockDim.x) {
+    const int ea = s_ids[a];
+    int rank = 0;
+    for (int b = 0; b < a; ++b) rank += (s_ids[b] == ea);
+    const int p = s_off[ea] + rank;
+    perm_src[p] = a / k;
+    if (perm_w) perm_w[p] = s_w[a];
+    inv[a] = p;
+  }
+  for (int t = threadIdx.x; t < shared_rows; t += blockDim.x) {
+    perm_src[R + t] = t;
+    if (perm_w) perm_w[R + t] = 1.0f;
+  }
 }
 
 // One block of 1024 threads: per-expert exclusive scan over chunks (base), counts, segment
@@ -199,11 +293,27 @@ __global__ void __launch_bounds__(1024) plan_scatter_kernel(
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s) {
   const int tpc = plan_tokens_per_chunk(a.k);
   const int nchunks = (a.T + tpc - 1) / tpc;
-  const size_t hist_smem = sizeof(int32_t) * a.E;
   const int vpl = (a.E + 31) / 32;
-#define NVFP4MOE_ROUTER(V)                                                                  \
-  router_kernel<V><<<nchunks, kRouterWarps * 32, hist_smem, s>>>(a.logits, a.T, a.E, a.k, tpc, \
-                                                               a.ids, a.w, a.hist)
+  if ((int64_t)a.T * a.k <= kSmallPlanRows) {
+#define NVFP4MOE_SMALL(V)                                                                     \
+  plan_small_kernel<V><<<1, kSmallPlanThreads, 0, s>>>(a.logits, a.T, a.E, a.k, a.shared_rows, \
+                                                       a.ids, a.w, a.counts, a.offsets,        \
+                                                       a.tile_start, a.perm_src, a.perm_w, a.inv)
+    if (vpl <= 1) NVFP4MOE_SMALL(1);
+    else if (vpl <= 2) NVFP4MOE_SMALL(2);
+    else if (vpl <= 4) NVFP4MOE_SMALL(4);
+    else if (vpl <= 8) NVFP4MOE_SMALL(8);
+    else if (vpl <= 16) NVFP4MOE_SMALL(16);
+    else NVFP4MOE_SMALL(kMaxVpl);
+#undef NVFP4MOE_SMALL
+    return cudaGetLastError();
+  }
+  cudaError_t err = cudaMemsetAsync(a.hist, 0, sizeof(int32_t) * (size_t)nchunks * a.E, s);
+  if (err != cudaSuccess) return err;
+  const int rblocks = (a.T + kRouterWarps - 1) / kRouterWarps;
+#define NVFP4MOE_ROUTER(V)                                                                 \
+  router_kernel<V><<<rblocks, kRouterWarps * 32, 0, s>>>(a.logits, a.T, a.E, a.k, tpc, a.ids, \
+                                                        a.w, a.hist)
   if (vpl <= 1) NVFP4MOE_ROUTER(1);
   else if (vpl <= 2) NVFP4MOE_ROUTER(2);
   else if (vpl <= 4) NVFP4MOE_ROUTER(4);
@@ -211,7 +321,7 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s) {
   else if (vpl <= 16) NVFP4MOE_ROUTER(16);
   else NVFP4MOE_ROUTER(kMaxVpl);
 #undef NVFP4MOE_ROUTER
-  cudaError_t err = cudaGetLastError();
+  err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const size_t scan_smem = sizeof(int32_t) * kScanRows * a.E;
   if (scan_smem > 48 * 1024) {

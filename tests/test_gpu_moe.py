@@ -129,3 +129,32 @@ def test_zero_tokens_and_errors(moe):
     bad = moe.make_config(cs.experts, 200, cs.inter, cs.top_k)      # H not a multiple of 256
     with pytest.raises(RuntimeError, match="UNSUPPORTED_SHAPE"):
         moe.quantize_weights(bad, wg, wu, wd)
+
+
+def test_cuda_graph_replay_matches_eager(moe):
+    """The layer is recorded into a CUDA graph (no allocation, no host read inside moe_run) and
+    the replays agree with an eager call; the pages check graph replay against eager the same
+    way ("b12x" README, DeepSeek V4.1 Flash MoE benchmark)."""
+    cs = synth.CONFIGS["decode"]
+    T = 8
+    x = synth.gen_x(cs, T, device="cuda")
+    lg = synth.gen_logits(cs, T, device="cuda")
+    wg, wu, wd = synth.gen_all_experts(cs, device="cuda")
+    cfg = moe.make_config(cs.experts, cs.hidden, cs.inter, cs.top_k, max_tokens=T)
+    wbuf = moe.quantize_weights(cfg, wg, wu, wd)
+    ws = torch.empty(moe.workspace_size(cfg, T), dtype=torch.uint8, device="cuda")
+    y_eager = moe.run(cfg, wbuf, x, lg, workspace=ws).clone()
+    y = torch.empty_like(y_eager)
+    timer = moe.StageTimer()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        moe.run(cfg, wbuf, x, lg, y=y, workspace=ws, timer=timer)
+    for _ in range(3):
+        y.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert moe.last_device_status(ws) == 0
+        d = (y.float() - y_eager.float()).abs().max().item()
+        assert d <= 1e-2 * y_eager.float().abs().max().item()
+        ms = timer.stage_ms()
+        assert all(v >= 0 for v in ms.values()) and sum(ms.values()) > 0
