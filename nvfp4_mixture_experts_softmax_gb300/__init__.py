@@ -37,6 +37,8 @@ class MoeConfig(C.Structure):
                 f"max_tokens={self.max_tokens})")
 
 
+# Stages between the library's stage events.  Small batches run the quantiser, router and plan
+# as one fused kernel: its time is reported under "act_quant" and "router_plan" is then empty.
 STAGES = ("act_quant", "router_plan", "gemm1_swiglu", "gemm2_combine", "bf16_out")
 N_STAGE_EVENTS = len(STAGES) + 1
 

@@ -207,7 +207,36 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
   };
 
   cudaError_t e = mark(0);
-  if (e == cudaSuccess) e = cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  if (L.small) {
+    // 1+2. one block: status reset, activation quantiser, router and plan
+    PrologueArgs pr{};
+    pr.x = x;
+    pr.T = T;
+    pr.H = H;
+    pr.status = &hdr->status;
+    pr.ts = &hdr->ts;
+    pr.xq = ws + L.xq;
+    pr.xsf = ws + L.xsf;
+    pr.logits = logits;
+    pr.E = E;
+    pr.k = k;
+    pr.shared_rows = shared ? T : 0;
+    pr.ids = i32(L.ids);
+    pr.w = f32(L.w);
+    pr.counts = debug ? debug->counts : nullptr;
+    pr.offsets = i32(L.seg_off);
+    pr.tile_start = i32(L.tile_start);
+    pr.perm_src = i32(L.perm_src);
+    pr.perm_w = f32(L.perm_w);
+    pr.inv = i32(L.inv);
+    e = launch_prologue_small(pr, s);
+    if (e == cudaSuccess) e = mark(1);
+    if (e == cudaSuccess) e = mark(2);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  } else {
+  e = cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
   // 1. activation quantiser (and zero the FP32 output accumulator on the way)
@@ -237,6 +266,7 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
   e = launch_plan(pa, s);
   if (e == cudaSuccess) e = mark(2);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
 
   const int nseg = E + shared;
   const int64_t max_mtiles = ((int64_t)L.Rt + (int64_t)nseg * (kBM - 1)) / kBM;
@@ -261,12 +291,15 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
   g.hq = ws + L.hq;
   g.hsf = ws + L.hsf;
   g.status = &hdr->status;
-  g.max_items = (int)std::min<int64_t>(max_mtiles * (g.N / kBN), INT32_MAX);
+  // decode-sized batches: every expert has at most T <= kDecodeMaxRows rows, one tile each
+  const bool decode = T <= kDecodeMaxRows;
+  const int64_t item_rows = decode ? std::min<int64_t>(nseg, L.Rt) : max_mtiles;
+  g.max_items = (int)std::min<int64_t>(item_rows * (g.N / kBN), INT32_MAX);
   g.max_ctas = g.max_items;
   g.a_rows = T;
   g.out_rows = L.Rt;
   g.y_rows = T;
-  e = launch_grouped_gemm(g, s);
+  e = decode ? launch_grouped_gemm_decode(g, s) : launch_grouped_gemm(g, s);
   if (e == cudaSuccess) e = mark(3);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
@@ -279,19 +312,21 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
   g2.b_per_seg = W.w2_per_e;
   g2.N = H;
   g2.K = I;
-  g2.mode = 1;
+  g2.mode = L.small ? 2 : 1;
   g2.perm_src = i32(L.perm_src);
   g2.perm_w = f32(L.perm_w);
   g2.yacc = f32(L.yacc);
-  g2.max_items = (int)std::min<int64_t>(max_mtiles * (g2.N / kBN), INT32_MAX);
+  g2.obuf = f32(L.obuf);
+  g2.max_items = (int)std::min<int64_t>(item_rows * (g2.N / kBN), INT32_MAX);
   g2.max_ctas = g2.max_items;
   g2.a_rows = L.Rt;
-  e = launch_grouped_gemm(g2, s);
+  e = decode ? launch_grouped_gemm_decode(g2, s) : launch_grouped_gemm(g2, s);
   if (e == cudaSuccess) e = mark(4);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
-  // 5. BF16 output
-  e = launch_finalize(f32(L.yacc), y, (int64_t)T * H, s);
+  // 5. BF16 output (small batches: sum each token's stored rows in slot order)
+  e = L.small ? launch_finalize_gather(f32(L.obuf), i32(L.inv), T, k, H, shared, y, s)
+              : launch_finalize(f32(L.yacc), y, (int64_t)T * H, s);
   if (e == cudaSuccess) e = mark(5);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 

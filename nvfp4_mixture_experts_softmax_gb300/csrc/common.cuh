@@ -10,6 +10,18 @@
 
 namespace nvfp4moe {
 
+// Programmatic dependent launch: a kernel launched with the programmatic-serialization attribute
+// may start while its predecessor in the stream is still running.  Each kernel of the layer
+// calls griddep_wait() before its first access to global memory (so every read sees the
+// predecessor's writes and no write races a read of the predecessor) and griddep_launch() to
+// let its own successor start launching.  Both are no-ops for an ordinary launch.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Device status word: the first error wins.
 __device__ __forceinline__ void set_status(int32_t* st, int32_t code) {
   if (st) atomicCAS(st, 0, code);
@@ -96,6 +108,48 @@ __device__ __forceinline__ void quant_block16_fast(const float* x, float ts, flo
 }
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
+
+// NVFP4 encode of BF16 block b (elements 16b .. 16b+15 of x): 8 code bytes and 1 scale byte.
+__device__ __forceinline__ void encode_bf16_block16(const uint4* __restrict__ x, int64_t b,
+                                                    float ts, uint2* __restrict__ codes,
+                                                    uint8_t* __restrict__ sf) {
+  const uint4 v0 = __ldg(x + 2 * b), v1 = __ldg(x + 2 * b + 1);
+  const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+  float f[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    f[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
+    f[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+  }
+  uint32_t lo, hi, s;
+  quant_block16(f, ts, lo, hi, s);
+  codes[b] = make_uint2(lo, hi);
+  sf[b] = (uint8_t)s;
+}
+
+__device__ __forceinline__ uint32_t abs_bf16_max8(uint4 v) {
+  uint32_t a = max(v.x & 0x7FFFu, (v.x >> 16) & 0x7FFFu);
+  uint32_t b = max(v.y & 0x7FFFu, (v.y >> 16) & 0x7FFFu);
+  uint32_t c = max(v.z & 0x7FFFu, (v.z >> 16) & 0x7FFFu);
+  uint32_t d = max(v.w & 0x7FFFu, (v.w >> 16) & 0x7FFFu);
+  return max(max(a, b), max(c, d));
+}
+
+__device__ __forceinline__ uint32_t block_max_u32(uint32_t m, uint32_t* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  if (warp == 0) {
+    m = lane < (int)(blockDim.x >> 5) ? red[lane] : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+  }
+  return m;  // valid in warp 0
+}
+
+
 
 // ---------------------------------------------------------------------------------------------
 // Shared-memory addresses, mbarriers, bounded waits.

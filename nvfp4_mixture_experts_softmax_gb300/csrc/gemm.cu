@@ -26,7 +26,7 @@ namespace nvfp4moe {
 
 namespace {
 
-constexpr int kStages = 5;
+constexpr int kStages = 6;
 constexpr int kEpiWarps = 4;
 constexpr int kTmaWarp = 4;
 constexpr int kMmaWarp = 5;
@@ -105,10 +105,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const GemmArg
   int32_t* s_seg = s_tile + (p.nseg + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = threadIdx.x; i <= p.nseg; i += blockDim.x) {
-    s_tile[i] = p.tile_start[i];
-    s_seg[i] = p.seg_off[i];
-  }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
@@ -124,6 +120,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const GemmArg
     }
     mbar_init(smem_u32(drain), 1);
     fence_barrier_init();
+  }
+  // everything above touched only shared and tensor memory; wait for the producer kernel now
+  griddep_wait();
+  griddep_launch();
+  for (int i = threadIdx.x; i <= p.nseg; i += blockDim.x) {
+    s_tile[i] = p.tile_start[i];
+    s_seg[i] = p.seg_off[i];
   }
   tc_fence_before();
   __syncthreads();
@@ -345,7 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const GemmArg
             tok = 0;
           }
         }
-        float* yrow = p.yacc + (size_t)tok * p.N + t.nt * kBN;
+        float* yrow = p.mode == 1 ? p.yacc + (size_t)tok * p.N + t.nt * kBN
+                                  : p.obuf + (size_t)(ok_row ? prow : 0) * p.N + t.nt * kBN;
 #pragma unroll 1
         for (int c = 0; c < kBN / 32; ++c) {
           uint32_t v[32];
@@ -353,11 +357,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const GemmArg
           tmem_ld_wait();
           if (ok_row) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              red_add_v4(yrow + c * 32 + 4 * i, (__uint_as_float(v[4 * i]) * alpha) * wr,
-                         (__uint_as_float(v[4 * i + 1]) * alpha) * wr,
-                         (__uint_as_float(v[4 * i + 2]) * alpha) * wr,
-                         (__uint_as_float(v[4 * i + 3]) * alpha) * wr);
+            for (int i = 0; i < 8; ++i) {
+              const float4 d = make_float4((__uint_as_float(v[4 * i]) * alpha) * wr,
+                                           (__uint_as_float(v[4 * i + 1]) * alpha) * wr,
+                                           (__uint_as_float(v[4 * i + 2]) * alpha) * wr,
+                                           (__uint_as_float(v[4 * i + 3]) * alpha) * wr);
+              if (p.mode == 1) red_add_v4(yrow + c * 32 + 4 * i, d.x, d.y, d.z, d.w);
+              else *reinterpret_cast<float4*>(yrow + c * 32 + 4 * i) = d;
+            }
           }
         }
       }
@@ -389,8 +396,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s) {
   int grid = a.max_ctas;
   if (grid > num_sms()) grid = num_sms();
   if (grid < 1) grid = 1;
-  grouped_gemm_kernel<<<grid, kThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(grouped_gemm_kernel, dim3(grid), dim3(kThreads), smem, s, a);
 }
 
 }  // namespace nvfp4moe

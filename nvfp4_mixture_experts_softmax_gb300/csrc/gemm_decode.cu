@@ -1,0 +1,405 @@
+// Grouped block-scaled FP4 GEMM for decode-sized batches (every expert receives at most 64 rows),
+// with the operands swapped: the expert's weights are the MMA's A operand (M = 128 weight rows of
+// one packed block per K stage, loaded by one bulk copy) and the expert's token rows are the
+// B operand (N = the rows rounded up to 16).  The tensor core then works on the real tokens
+// only, a pipeline stage is 28 KB instead of 36 KB (7 stages in flight), and the accumulator
+// holds one weight row per TMEM lane and one token per column:
+//   GEMM1 (mode 0): warp w of the epilogue holds the 16 gate rows and the 16 up rows of one
+//          16-feature NVFP4 block, so each half-warp computes silu(g)*u of one token and
+//          requantises the block with half-warp reductions;
+//   GEMM2 (mode 1 / 2): lanes hold consecutive output features, so a token's row is written (or
+//          reduced) 128 contiguous bytes per warp.
+// Warp roles and the pipeline are those of the general kernel in gemm.cu ("nvfp4-megamoe-kernel
+// compare pre-b1...master", section "MoE kernel": TMA, MMA and epilogue warps; the pages keep
+// decode on 1-CTA tiles).
+#include "common.cuh"
+#include "internal.h"
+
+namespace nvfp4moe {
+
+namespace {
+
+constexpr int kStages = 7;
+constexpr int kEpiWarps = 4;
+constexpr int kTmaWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kProdWarp0 = 6;
+constexpr int kProdWarps = 4;
+constexpr int kThreads = (kProdWarp0 + kProdWarps) * 32;
+constexpr int kNmax = kDecodeMaxRows;                 // token rows per expert tile
+constexpr int kXOff = kTileBlockBytes;                 // token codes after the weight block
+constexpr int kXSfOff = kXOff + kNmax * 128;           // token scales
+constexpr int kStageBytes = kXSfOff + 4 * 512;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCols = kNmax;
+constexpr uint32_t kSfCol0 = 2 * kAccCols;
+constexpr uint32_t kSfColsPerStage = 32;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "tensor memory budget");
+static_assert(kStageBytes % 1024 == 0 && kXOff % 1024 == 0, "1024-byte aligned swizzled tiles");
+static_assert(kNmax % 16 == 0 && kNmax <= 64, "token tile");
+
+constexpr uint32_t make_idesc(int M, int N) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+struct TileInfo {
+  int seg, m0, rows, nt;
+};
+
+// Items are (active expert, 128-row weight tile); an active expert owns exactly one m-tile here.
+__device__ __forceinline__ TileInfo decode_item(int item, int n_tiles, const int32_t* s_tile,
+                                                const int32_t* s_seg, int nseg) {
+  TileInfo t;
+  const int mt = item / n_tiles;
+  t.nt = item - mt * n_tiles;
+  int lo = 0, hi = nseg - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_tile[mid] <= mt) lo = mid;
+    else hi = mid - 1;
+  }
+  t.seg = lo;
+  t.m0 = s_seg[lo];
+  t.rows = min(kNmax, s_seg[lo + 1] - t.m0);
+  return t;
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
+
+__device__ __forceinline__ void red_add_f32(float* addr, float v) {
+  asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_decode_kernel(const GemmArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* acc_full = bars + 2 * kStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int32_t* s_tile = reinterpret_cast<int32_t*>(smem + kStages * kStageBytes + 256);
+  int32_t* s_seg = s_tile + (p.nseg + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(full + s), 2);  // one token-gather warp + the weight copy
+      mbar_init(smem_u32(empty + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(acc_full + b), 1);
+      mbar_init(smem_u32(acc_empty + b), kEpiWarps);
+    }
+    mbar_init(smem_u32(drain), 1);
+    fence_barrier_init();
+  }
+  griddep_wait();
+  griddep_launch();
+  for (int i = threadIdx.x; i <= p.nseg; i += blockDim.x) {
+    s_tile[i] = p.tile_start[i];
+    s_seg[i] = p.seg_off[i];
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int n_tiles = p.N / 128;
+  int total = s_tile[p.nseg] * n_tiles;
+  if (total < 0 || total > p.max_items) {
+    if (threadIdx.x == 0) set_status(p.status, MOE_ERR_INVALID_ARG);
+    total = 0;
+  }
+  const int kst = p.K / kBK;
+  const uint32_t smem0 = smem_u32(smem);
+
+  if (warp == kTmaWarp) {
+    // ---------------- weight blocks: one bulk copy per stage ----------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+        const TileInfo t = decode_item(item, n_tiles, s_tile, s_seg, p.nseg);
+        const uint8_t* src = p.b_tiles + (size_t)t.seg * p.b_per_seg +
+                             (size_t)t.nt * kst * kTileBlockBytes;
+        for (int ks = 0; ks < kst; ++ks) {
+          if (!mbar_wait_bounded(smem_u32(empty + stage), phase ^ 1u, kWaitLimitNs, p.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sb = smem0 + stage * kStageBytes;
+          mbar_arrive_expect_tx(smem_u32(full + stage), kTileBlockBytes);
+          bulk_load(sb, src + (size_t)ks * kTileBlockBytes, kTileBlockBytes, smem_u32(full + stage));
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      for (int i = 0; i < kStages && ok; ++i) {
+        if (!mbar_wait_bounded(smem_u32(empty + stage), phase ^ 1u, kWaitLimitNs, p.status)) break;
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------- MMA issue: D[weight row][token] ----------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t acc_phase[2] = {0u, 0u};
+      bool ok = true;
+      int it = 0;
+      for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++it) {
+        const TileInfo t = decode_item(item, n_tiles, s_tile, s_seg, p.nseg);
+        const int nmma = max(16, (t.rows + 15) & ~15);
+        const uint32_t idesc = make_idesc(128, nmma);
+        const int abuf = it & 1;
+        if (!mbar_wait_bounded(smem_u32(acc_empty + abuf), acc_phase[abuf] ^ 1u, kWaitLimitNs,
+                               p.status)) {
+          ok = false;
+          break;
+        }
+        acc_phase[abuf] ^= 1u;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + abuf * kAccCols;
+        for (int ks = 0; ks < kst; ++ks) {
+          if (!mbar_wait_bounded(smem_u32(full + stage), phase, kWaitLimitNs, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sb = smem0 + stage * kStageBytes;
+          const uint32_t sfw_s = sb + kTileBytes;
+          const uint32_t sfx_s = sb + kXSfOff;
+          const uint32_t sf_t = tmem_base + kSfCol0 + stage * kSfColsPerStage;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            tc_cp_32x128b_warpx4(sf_t + kk * 4, smem_desc(sfw_s + kk * 512, 0, 128, kLayoutSwizzleNone));
+            tc_cp_32x128b_warpx4(sf_t + 16 + kk * 4,
+                                 smem_desc(sfx_s + kk * 512, 0, 128, kLayoutSwizzleNone));
+          }
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = smem_desc(sb + kk * 32, 16, 1024, kLayoutSwizzle128B);
+            const uint64_t bd = smem_desc(sb + kXOff + kk * 32, 16, 1024, kLayoutSwizzle128B);
+            tc_mma_mxf4nvf4(d_tmem, ad, bd, idesc, sf_t + kk * 4, sf_t + 16 + kk * 4,
+                            (ks | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(smem_u32(empty + stage));
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (ok) tc_commit(smem_u32(acc_full + abuf));
+      }
+      tc_commit(smem_u32(drain));
+      mbar_wait_bounded(smem_u32(drain), 0u, kWaitLimitNs, p.status);
+    }
+  } else if (warp >= kProdWarp0) {
+    // ---------------- token rows (cp.async gather), stage ownership round robin ----------------
+    const int wp = warp - kProdWarp0;
+    int stage = 0;
+    uint32_t phase = 0;
+    int j = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+      const TileInfo t = decode_item(item, n_tiles, s_tile, s_seg, p.nseg);
+      const int first_own = (wp - (j % kProdWarps) + kProdWarps) % kProdWarps;
+      int src[2] = {-1, -1};   // source row of token rows lane and lane + 32
+      if (first_own < kst) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int r = lane + 32 * i;
+          const int pr = t.m0 + r;
+          if (r < t.rows) {
+            int sr = -1;
+            if (pr >= 0 && pr < p.out_rows) sr = p.a_gather ? __ldg(p.a_gather + pr) : pr;
+            if (sr < 0 || sr >= p.a_rows) {
+              set_status(p.status, MOE_ERR_INVALID_ARG);
+              sr = -1;
+            }
+            src[i] = sr;
+          }
+        }
+      }
+      for (int ks = 0; ks < kst; ++ks, ++j) {
+        if (j % kProdWarps == wp) {
+          if (!mbar_wait_bounded(smem_u32(empty + stage), phase ^ 1u, kWaitLimitNs, p.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sb = smem0 + stage * kStageBytes;
+#pragma unroll
+          for (int i = 0; i < kNmax / 4; ++i) {      // 16-byte chunk (lane & 7) of row (lane>>3)+4i
+            if (4 * i >= t.rows) break;
+            const int r = (lane >> 3) + 4 * i;
+            const int sr = __shfl_sync(0xffffffffu, src[i >> 3], r & 31);
+            if (r < t.rows && sr >= 0) {
+              const int c = lane & 7;
+              cp_async_16(sb + kXOff + r * 128 + ((c ^ (r & 7)) << 4),
+                          p.a_codes + (size_t)sr * (p.K / 2) + ks * 128 + c * 16, 16);
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < kNmax / 8; ++i) {      // scale word (lane & 3) of row (lane>>2)+8i
+            if (8 * i >= t.rows) break;
+            const int r = (lane >> 2) + 8 * i;
+            const int sr = __shfl_sync(0xffffffffu, src[i >> 2], r & 31);
+            if (r < t.rows && sr >= 0) {
+              const int kk = lane & 3;
+              cp_async_4(sb + kXSfOff + kk * 512 + (r & 31) * 16 + (r >> 5) * 4,
+                         p.a_sf + (size_t)sr * (p.K / 16) + ks * 16 + kk * 4, 4);
+            }
+          }
+          cp_async_commit();
+          cp_async_wait<0>();
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(full + stage));
+        }
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+    }
+    cp_async_wait<0>();
+  } else {
+    // ---------------- epilogue (warps 0-3): lane = weight row, column = token ----------------
+    uint32_t acc_phase[2] = {0u, 0u};
+    int it = 0;
+    const float ts_a = p.mode == 0 ? *p.ts_a : 0.0f;
+    const float inv_ts_h = 1.0f / p.ts_h;
+    const bool lo_half = lane < 16;
+    for (int item = blockIdx.x; item < total; item += gridDim.x, ++it) {
+      const TileInfo t = decode_item(item, n_tiles, s_tile, s_seg, p.nseg);
+      const int abuf = it & 1;
+      if (!mbar_wait_bounded(smem_u32(acc_full + abuf), acc_phase[abuf], kWaitLimitNs, p.status))
+        break;
+      acc_phase[abuf] ^= 1u;
+      tc_fence_after();
+      const int rows = (t.m0 >= 0 && t.m0 + t.rows <= p.out_rows) ? t.rows : 0;
+      const uint32_t tbase = tmem_base + abuf * kAccCols + ((uint32_t)(warp * 32) << 16);
+      if (p.mode == 0) {
+        // block b of h: 16 features; lanes < 16 hold gate rows, lanes >= 16 the up rows
+        const int I = p.N / 2;
+        const int b = t.nt * 4 + warp;
+        const float ag = ts_a * p.w_ts[t.seg * 4 + 0];
+        const float au = ts_a * p.w_ts[t.seg * 4 + 1];
+#pragma unroll 1
+        for (int cb = 0; cb < kNmax; cb += 32) {
+          if (cb >= rows) break;
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tbase + cb, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int n = 0; n < 32; n += 2) {
+            if (cb + n >= rows) break;
+            const float a0 = __uint_as_float(v[n]), a1 = __uint_as_float(v[n + 1]);
+            const float x0 = __shfl_xor_sync(0xffffffffu, a0, 16);
+            const float x1 = __shfl_xor_sync(0xffffffffu, a1, 16);
+            // the lower half-warp takes token cb+n, the upper half token cb+n+1
+            const float g = lo_half ? a0 : x1;
+            const float u = lo_half ? x0 : a1;
+            const int col = cb + n + (lo_half ? 0 : 1);
+            const float h = silu_mul(g * ag, u * au);
+            float bamax = fabsf(h);
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) bamax = fmaxf(bamax, __shfl_xor_sync(0xffffffffu, bamax, o));
+            uint32_t sf = 0u;
+            float q = 0.0f;
+            if (bamax != 0.0f) {
+              sf = f32_to_e4m3(bamax * (1.0f / 6.0f) * inv_ts_h);
+              const float S = e4m3_to_f32(sf) * p.ts_h;
+              if (S != 0.0f) q = h * __frcp_rn(S);
+            }
+            // gather the eight quotients of each quarter-warp into its first lane
+            const int g0 = lane & ~7;
+            float qq[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) qq[e] = __shfl_sync(0xffffffffu, q, g0 + e);
+            const uint32_t word = e2m1x8(qq[0], qq[1], qq[2], qq[3], qq[4], qq[5], qq[6], qq[7]);
+            const uint32_t word_hi = __shfl_down_sync(0xffffffffu, word, 8);
+            if ((lane & 15) == 0 && col < rows) {
+              const size_t prow = (size_t)(t.m0 + col);
+              *reinterpret_cast<uint2*>(p.hq + prow * (I / 2) + b * 8) = make_uint2(word, word_hi);
+              p.hsf[prow * (I / 16) + b] = (uint8_t)sf;
+            }
+          }
+        }
+      } else {
+        // output features m = nt*128 + warp*32 + lane; token column n -> permuted row m0 + n
+        const float alpha = p.ts_h * p.w_ts[t.seg * 4 + 2];
+        const int m = t.nt * 128 + warp * 32 + lane;
+        float wr[2] = {0.0f, 0.0f};
+        int tok[2] = {0, 0};
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int r = lane + 32 * i;
+          if (r < rows) {
+            wr[i] = __ldg(p.perm_w + t.m0 + r);
+            int tk = __ldg(p.perm_src + t.m0 + r);
+            if (tk < 0 || tk >= p.y_rows) {
+              set_status(p.status, MOE_ERR_INVALID_ARG);
+              tk = -1;
+            }
+            tok[i] = tk;
+          }
+        }
+#pragma unroll 1
+        for (int cb = 0; cb < kNmax; cb += 32) {
+          if (cb >= rows) break;
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tbase + cb, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int n = 0; n < 32; ++n) {
+            if (cb + n >= rows) break;
+            const float w = __shfl_sync(0xffffffffu, wr[cb >> 5], n);
+            const float d = (__uint_as_float(v[n]) * alpha) * w;
+            if (p.mode == 2) {
+              p.obuf[(size_t)(t.m0 + cb + n) * p.N + m] = d;
+            } else {
+              const int tk = __shfl_sync(0xffffffffu, tok[cb >> 5], n);
+              if (tk >= 0) red_add_f32(p.yacc + (size_t)tk * p.N + m, d);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(acc_empty + abuf));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+size_t smem_bytes(int nseg) {
+  return 1024 + (size_t)kStages * kStageBytes + 256 + sizeof(int32_t) * 2 * (nseg + 2);
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm_decode(const GemmArgs& a, cudaStream_t s) {
+  const size_t smem = smem_bytes(a.nseg);
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_decode_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int grid = a.max_ctas;
+  if (grid > num_sms()) grid = num_sms();
+  if (grid < 1) grid = 1;
+  return launch_pdl(grouped_gemm_decode_kernel, dim3(grid), dim3(kThreads), smem, s, a);
+}
+
+}  // namespace nvfp4moe

@@ -4,6 +4,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "nvfp4_moe.h"
 
 namespace nvfp4moe {
@@ -71,11 +73,18 @@ __host__ __device__ __forceinline__ size_t packed_sf_offset(int64_t n, int64_t k
                   (r >> 5) * 4 + (kb & 3));
 }
 
+// Small batches run a fused prologue (one block does the quantiser, router and plan) and combine
+// by storing every assignment's output row and summing a token's rows in slot order.
+constexpr int64_t kSmallPrologueElems = 512 * 1024;   // T*H handled by the one-block prologue
+constexpr int64_t kStoreCombineElems = 16 << 20;      // (T*k + shared T) * H stored in FP32
+bool prologue_small_fits(int T, int H, int k);
+
 // Workspace of moe_run for T tokens.  Offset 0 holds the device status word.
 struct RunLayout {
   size_t hdr, amax_part, ids, w, hist, base, seg_off, tile_start, perm_src, perm_w, inv, xq, xsf,
-      hq, hsf, yacc, total;
+      hq, hsf, yacc, obuf, total;
   int T, R, Rt, nseg, nchunks, tpc;
+  bool small;   // fused prologue + stored-row combine
   RunLayout(const moe_config& c, int T_) {
     T = T_;
     const int k = c.top_k, E = c.num_experts, H = c.hidden, I = c.inter;
@@ -101,7 +110,10 @@ struct RunLayout {
     xsf = o;        o = align_up(o + (size_t)T * H / 16);
     hq = o;         o = align_up(o + (size_t)Rt * I / 2);
     hsf = o;        o = align_up(o + (size_t)Rt * I / 16);
-    yacc = o;       o = align_up(o + 4 * (size_t)T * H);
+    small = (int64_t)R <= 2048 && (int64_t)T * H <= kSmallPrologueElems &&
+            (int64_t)Rt * H <= kStoreCombineElems;
+    yacc = o;       o = align_up(o + (small ? 0 : 4 * (size_t)T * H));
+    obuf = o;       o = align_up(o + (small ? 4 * (size_t)Rt * H : 0));
     total = o;
   }
 };
@@ -161,7 +173,9 @@ struct GemmArgs {
   int nseg;
   int N, K;
   // epilogue
-  int mode;               // 0: SwiGLU + requant (GEMM1), 1: down projection + weighted combine
+  int mode;               // 0: SwiGLU + requant (GEMM1); 1: down projection, router-weighted
+                          // reduction into yacc; 2: down projection, router-weighted row stored
+                          // to obuf (row = permuted row)
   const float* ts_a;      // device scalar (mode 0)
   float ts_h;
   uint8_t* hq;            // mode 0 out [rows, N/4]   (h has N/2 features)
@@ -169,6 +183,7 @@ struct GemmArgs {
   const int32_t* perm_src;  // mode 1
   const float* perm_w;      // mode 1
   float* yacc;              // mode 1 out [T, N]
+  float* obuf;              // mode 2 out [rows, N]
   int32_t* status;
   int max_ctas;
   // bounds used to reject malformed plan data instead of touching memory outside the buffers
@@ -179,8 +194,46 @@ struct GemmArgs {
 };
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s);
 
+// Decode-sized batches (T <= kDecodeMaxRows, so no expert receives more rows): weights as the
+// MMA's M operand, tokens as N (gemm_decode.cu).  Same arguments as launch_grouped_gemm.
+constexpr int kDecodeMaxRows = 64;
+cudaError_t launch_grouped_gemm_decode(const GemmArgs& a, cudaStream_t s);
+
 cudaError_t launch_finalize(const float* yacc, void* y, int64_t n, cudaStream_t s);
+cudaError_t launch_finalize_gather(const float* o, const int32_t* inv, int T, int k, int H,
+                                   int shared, void* y, cudaStream_t s);
+
+struct PrologueArgs {
+  const void* x;           // [T, H] BF16
+  int T, H;
+  int32_t* status;
+  float* ts;
+  uint8_t* xq;             // [T, H/2]
+  uint8_t* xsf;            // [T, H/16]
+  const float* logits;     // [T, E]
+  int E, k, shared_rows;
+  int32_t *ids, *counts, *offsets, *tile_start, *perm_src, *inv;
+  float *w, *perm_w;
+};
+cudaError_t launch_prologue_small(const PrologueArgs& a, cudaStream_t s);
 
 int num_sms();
+
+// Launches `kernel` with the programmatic-stream-serialization attribute (see griddep_wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace nvfp4moe

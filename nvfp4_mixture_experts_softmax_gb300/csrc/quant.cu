@@ -16,28 +16,6 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kMaxAmaxBlocks = 1024;
 
-__device__ __forceinline__ uint32_t abs_bf16_max8(uint4 v) {
-  uint32_t a = max(v.x & 0x7FFFu, (v.x >> 16) & 0x7FFFu);
-  uint32_t b = max(v.y & 0x7FFFu, (v.y >> 16) & 0x7FFFu);
-  uint32_t c = max(v.z & 0x7FFFu, (v.z >> 16) & 0x7FFFu);
-  uint32_t d = max(v.w & 0x7FFFu, (v.w >> 16) & 0x7FFFu);
-  return max(max(a, b), max(c, d));
-}
-
-__device__ __forceinline__ uint32_t block_max_u32(uint32_t m, uint32_t* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) red[warp] = m;
-  __syncthreads();
-  if (warp == 0) {
-    m = lane < (int)(blockDim.x >> 5) ? red[lane] : 0u;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-  }
-  return m;  // valid in warp 0
-}
-
 // Pass 1: max |x| over the whole tensor (BF16 magnitudes compare as their bit patterns), with a
 // last-block reduction that writes ts = amax / 2688 and re-arms the block counter.  Optionally
 // zero-fills `zero` (the FP32 output accumulator of the layer) on the way.
@@ -47,6 +25,8 @@ __global__ void __launch_bounds__(kThreads) act_amax_kernel(const uint4* __restr
                                                            float4* zero, int64_t nzero4) {
   __shared__ uint32_t red[32];
   __shared__ bool is_last;
+  griddep_wait();
+  griddep_launch();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   uint32_t m = 0;
   int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -85,21 +65,12 @@ __global__ void __launch_bounds__(kThreads) act_encode_kernel(const uint4* __res
                                                              const float* __restrict__ ts_ptr,
                                                              uint2* __restrict__ codes,
                                                              uint8_t* __restrict__ sf) {
+  griddep_wait();
+  griddep_launch();
   const float ts = *ts_ptr;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblk; b += stride) {
-    const uint4 v0 = __ldg(x + 2 * b), v1 = __ldg(x + 2 * b + 1);
-    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    float f[16];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      f[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
-      f[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
-    }
-    uint32_t lo, hi, s;
-    quant_block16(f, ts, lo, hi, s);
-    codes[b] = make_uint2(lo, hi);
-    sf[b] = (uint8_t)s;
+    encode_bf16_block16(x, b, ts, codes, sf);
   }
 }
 
@@ -202,11 +173,47 @@ __global__ void __launch_bounds__(kThreads) weight_export_kernel(WeightDst d, in
 
 __global__ void __launch_bounds__(kThreads) finalize_kernel(const float4* __restrict__ acc,
                                                            uint2* __restrict__ y, int64_t n4) {
+  griddep_wait();
+  griddep_launch();
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
        i += (int64_t)gridDim.x * blockDim.x) {
     const float4 v = __ldcs(acc + i);
     __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
     __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+    y[i] = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+  }
+}
+
+// y[t] = bf16( sum_{j<k} o[inv[t*k+j]] (+ o[T*k + t] for the shared expert) ), summed in slot
+// order; o holds each assignment's router-weighted expert output in FP32.
+__global__ void __launch_bounds__(kThreads) finalize_gather_kernel(const float4* __restrict__ o,
+                                                                  const int32_t* __restrict__ inv,
+                                                                  int T, int k, int H4,
+                                                                  int shared, uint2* __restrict__ y) {
+  griddep_wait();
+  griddep_launch();
+  const int64_t n = (int64_t)T * H4;
+  const int64_t R = (int64_t)T * k;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = i / H4, m = i - t * H4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < k; ++j) {
+      const float4 v = __ldcg(o + (int64_t)__ldg(inv + t * k + j) * H4 + m);
+      acc.x = __fadd_rn(acc.x, v.x);
+      acc.y = __fadd_rn(acc.y, v.y);
+      acc.z = __fadd_rn(acc.z, v.z);
+      acc.w = __fadd_rn(acc.w, v.w);
+    }
+    if (shared) {
+      const float4 v = __ldcg(o + (R + t) * H4 + m);
+      acc.x = __fadd_rn(acc.x, v.x);
+      acc.y = __fadd_rn(acc.y, v.y);
+      acc.z = __fadd_rn(acc.z, v.z);
+      acc.w = __fadd_rn(acc.w, v.w);
+    }
+    __nv_bfloat162 a = __floats2bfloat162_rn(acc.x, acc.y);
+    __nv_bfloat162 b = __floats2bfloat162_rn(acc.z, acc.w);
     y[i] = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
   }
 }
@@ -247,13 +254,15 @@ cudaError_t launch_act_quant(const void* x, int64_t rows, int64_t cols, uint8_t*
   const int64_t n = rows * cols;
   const int64_t nvec = n / 8;
   const int g1 = grid_for(nvec, kThreads * 8, kMaxAmaxBlocks);
-  act_amax_kernel<<<g1, kThreads, 0, s>>>(reinterpret_cast<const uint4*>(x), nvec, hdr, partials,
-                                          ts, reinterpret_cast<float4*>(zero_buf), zero_floats / 4);
+  cudaError_t e = launch_pdl(act_amax_kernel, dim3(g1), dim3(kThreads), 0, s,
+                             reinterpret_cast<const uint4*>(x), nvec, hdr, partials, ts,
+                             reinterpret_cast<float4*>(zero_buf), zero_floats / 4);
+  if (e != cudaSuccess) return e;
   const int64_t nblk = n / 16;
   const int g2 = grid_for(nblk, kThreads, num_sms() * 16);
-  act_encode_kernel<<<g2, kThreads, 0, s>>>(reinterpret_cast<const uint4*>(x), nblk, &hdr->ts,
-                                            reinterpret_cast<uint2*>(codes), sf);
-  return cudaGetLastError();
+  return launch_pdl(act_encode_kernel, dim3(g2), dim3(kThreads), 0, s,
+                    reinterpret_cast<const uint4*>(x), nblk, (const float*)&hdr->ts,
+                    reinterpret_cast<uint2*>(codes), sf);
 }
 
 cudaError_t launch_weight_quant(const moe_config& c, const WeightLayout& L, const void* wg,
@@ -293,11 +302,18 @@ cudaError_t launch_weight_export(const moe_config& c, const WeightLayout& L, con
   return cudaGetLastError();
 }
 
+cudaError_t launch_finalize_gather(const float* o, const int32_t* inv, int T, int k, int H,
+                                   int shared, void* y, cudaStream_t s) {
+  const int64_t n4 = (int64_t)T * (H / 4);
+  return launch_pdl(finalize_gather_kernel, dim3(grid_for(n4, kThreads, num_sms() * 8)),
+                    dim3(kThreads), 0, s, reinterpret_cast<const float4*>(o), inv, T, k, H / 4,
+                    shared, reinterpret_cast<uint2*>(y));
+}
+
 cudaError_t launch_finalize(const float* yacc, void* y, int64_t n, cudaStream_t s) {
   const int64_t n4 = n / 4;
-  finalize_kernel<<<grid_for(n4, kThreads, num_sms() * 8), kThreads, 0, s>>>(
-      reinterpret_cast<const float4*>(yacc), reinterpret_cast<uint2*>(y), n4);
-  return cudaGetLastError();
+  return launch_pdl(finalize_kernel, dim3(grid_for(n4, kThreads, num_sms() * 8)), dim3(kThreads),
+                    0, s, reinterpret_cast<const float4*>(yacc), reinterpret_cast<uint2*>(y), n4);
 }
 
 }  // namespace nvfp4moe

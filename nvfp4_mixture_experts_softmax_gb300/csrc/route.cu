@@ -19,97 +19,13 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "route.cuh"
 
 namespace nvfp4moe {
 
 namespace {
 
 constexpr int kRouterWarps = 8;
-constexpr int kMaxVpl = 32;  // experts per lane: E <= 1024
-
-// Exclusive scan of one value per thread over the block (blockDim.x <= 1024).
-__device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t* sw, int32_t& total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  int32_t x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) sw[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int32_t s = lane < nw ? sw[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int32_t y = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += y;
-    }
-    if (lane < nw) sw[lane] = s;  // inclusive warp prefix
-  }
-  __syncthreads();
-  total = sw[nw - 1];
-  const int32_t r = (warp ? sw[warp - 1] : 0) + x - v;
-  __syncthreads();
-  return r;
-}
-
-// Order-preserving map of a float to an unsigned key (larger float -> larger key); -0 is folded
-// into +0 so that the two compare equal, as floats do.
-__device__ __forceinline__ uint32_t order_key(float v) {
-  const uint32_t u = __float_as_uint(v == 0.0f ? 0.0f : v);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// Top-k of one token's logits by one warp: lane l holds experts l, l+32, ...  Each of the k
-// rounds takes the warp maximum of the lanes' best keys, then the lowest expert index among the
-// lanes holding it (hardware redux.sync), so ties go to the lower index.  Lane j < k ends with
-// the j-th choice (my_id, my_l).
-template <int VPL>
-__device__ __forceinline__ void warp_topk(const float* __restrict__ row, int E, int k, int lane,
-                                          int& my_id, float& my_l) {
-  float v[VPL];
-  uint32_t key[VPL];
-  uint32_t taken = 0;
-#pragma unroll
-  for (int i = 0; i < VPL; ++i) {
-    const int e = lane + 32 * i;
-    if (e < E) {
-      v[i] = __ldg(row + e);
-      key[i] = order_key(v[i]);
-    } else {
-      v[i] = 0.0f;
-      key[i] = 0u;
-      taken |= 1u << i;
-    }
-  }
-  my_id = 0;
-  my_l = 0.0f;
-  for (int j = 0; j < k; ++j) {
-    int bi = -1;
-    uint32_t bk = 0u;
-    float bv = 0.0f;
-#pragma unroll
-    for (int i = 0; i < VPL; ++i)
-      if (!((taken >> i) & 1u) && (bi < 0 || key[i] > bk)) { bk = key[i]; bv = v[i]; bi = i; }
-    const uint32_t lane_key = bi < 0 ? 0u : bk;
-    const uint32_t mk = __reduce_max_sync(0xffffffffu, lane_key);
-    const uint32_t cand = (bi >= 0 && lane_key == mk) ? (uint32_t)(lane + 32 * bi) : 0xffffffffu;
-    const uint32_t be = __reduce_min_sync(0xffffffffu, cand);
-    const float wv = __shfl_sync(0xffffffffu, bv, (int)(be & 31u));
-    if ((int)(be & 31u) == lane) taken |= 1u << (be >> 5);
-    if (lane == j) { my_id = (int)be; my_l = wv; }
-  }
-}
-
-// Renormalised softmax weights of the k chosen logits, summed in slot order; lanes < k write.
-__device__ __forceinline__ float topk_weight(float my_l, int k, int lane) {
-  const float l0 = __shfl_sync(0xffffffffu, my_l, 0);
-  const float ex = lane < k ? expf(my_l - l0) : 0.0f;
-  float sum = 0.0f;
-  for (int j = 0; j < k; ++j) sum = sum + __shfl_sync(0xffffffffu, ex, j);
-  return __fdiv_rn(ex, sum);
-}
 
 // One warp per token; the per-chunk expert histogram (chunk = tpc tokens) is accumulated with
 // global atomics into `hist`, which the caller zeroes first.
@@ -117,6 +33,8 @@ template <int VPL>
 __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(
     const float* __restrict__ logits, int T, int E, int k, int tpc, int32_t* __restrict__ ids,
     float* __restrict__ wout, int32_t* __restrict__ hist) {
+  griddep_wait();
+  griddep_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kRouterWarps + warp;
   if (t >= T) return;
@@ -131,73 +49,17 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(
   }
 }
 
-// The whole plan in one block for small batches (T*k <= kSmallPlanRows): route, count, scan,
-// and place every assignment at offsets[e] + #(earlier assignments to e).
-constexpr int kSmallPlanRows = 2048;
-constexpr int kSmallPlanThreads = 1024;
-
 template <int VPL>
 __global__ void __launch_bounds__(kSmallPlanThreads) plan_small_kernel(
     const float* __restrict__ logits, int T, int E, int k, int shared_rows,
     int32_t* __restrict__ ids, float* __restrict__ wout, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ tile_start,
     int32_t* __restrict__ perm_src, float* __restrict__ perm_w, int32_t* __restrict__ inv) {
-  __shared__ int32_t s_cnt[1024];
-  __shared__ int32_t s_off[1024];
-  __shared__ int32_t s_ids[kSmallPlanRows];
-  __shared__ float s_w[kSmallPlanRows];
-  __shared__ int32_t sw[32];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
-  __syncthreads();
-  for (int t = warp; t < T; t += kSmallPlanThreads / 32) {
-    int my_id;
-    float my_l;
-    warp_topk<VPL>(logits + (int64_t)t * E, E, k, lane, my_id, my_l);
-    const float w = topk_weight(my_l, k, lane);
-    if (lane < k) {
-      ids[(int64_t)t * k + lane] = my_id;
-      wout[(int64_t)t * k + lane] = w;
-      s_ids[t * k + lane] = my_id;
-      s_w[t * k + lane] = w;
-      atomicAdd(&s_cnt[my_id], 1);
-    }
-  }
-  __syncthreads();
-  const int e = threadIdx.x;
-  const int32_t cnt = e < E ? s_cnt[e] : 0;
-  int32_t total, ttotal;
-  const int32_t off = block_exclusive_scan(cnt, sw, total);
-  const int32_t toff = block_exclusive_scan((cnt + kBM - 1) / kBM, sw, ttotal);
-  if (e < E) {
-    s_off[e] = off;
-    if (counts) counts[e] = cnt;
-    offsets[e] = off;
-    if (tile_start) tile_start[e] = toff;
-  }
-  if (threadIdx.x == 0) {
-    offsets[E] = total;
-    if (shared_rows > 0) offsets[E + 1] = total + shared_rows;
-    if (tile_start) {
-      tile_start[E] = ttotal;
-      if (shared_rows > 0) tile_start[E + 1] = ttotal + (shared_rows + kBM - 1) / kBM;
-    }
-  }
-  __syncthreads();
-  const int R = T * k;
-  for (int a = threadIdx.x; a < R; a += blockDim.x) {
-    const int ea = s_ids[a];
-    int rank = 0;
-    for (int b = 0; b < a; ++b) rank += (s_ids[b] == ea);
-    const int p = s_off[ea] + rank;
-    perm_src[p] = a / k;
-    if (perm_w) perm_w[p] = s_w[a];
-    inv[a] = p;
-  }
-  for (int t = threadIdx.x; t < shared_rows; t += blockDim.x) {
-    perm_src[R + t] = t;
-    if (perm_w) perm_w[R + t] = 1.0f;
-  }
+  extern __shared__ __align__(16) uint8_t s_dyn[];
+  griddep_wait();
+  griddep_launch();
+  small_plan_body<VPL>(logits, T, E, k, shared_rows, ids, wout, counts, offsets, tile_start,
+                       perm_src, perm_w, inv, s_dyn);
 }
 
 // One block of 1024 threads: per-expert exclusive scan over chunks (base), counts, segment
@@ -213,6 +75,8 @@ __global__ void __launch_bounds__(1024) plan_scan_kernel(const int32_t* __restri
                                                         int32_t* __restrict__ tile_start) {
   extern __shared__ int32_t s_tile[];  // [kScanRows][E]
   __shared__ int32_t sw[32];
+  griddep_wait();
+  griddep_launch();
   const int e = threadIdx.x;
   int32_t run = 0;
   for (int c0 = 0; c0 < nchunks; c0 += kScanRows) {
@@ -258,6 +122,8 @@ __global__ void __launch_bounds__(1024) plan_scatter_kernel(
     int shared_rows, const int32_t* __restrict__ base, const int32_t* __restrict__ offsets,
     int32_t* __restrict__ perm_src, float* __restrict__ perm_w, int32_t* __restrict__ inv) {
   extern __shared__ int32_t s_wcnt[];  // [nwarps][E]
+  griddep_wait();
+  griddep_launch();
   const int nw = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < nw * E; i += blockDim.x) s_wcnt[i] = 0;
   __syncthreads();
@@ -295,10 +161,17 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s) {
   const int nchunks = (a.T + tpc - 1) / tpc;
   const int vpl = (a.E + 31) / 32;
   if ((int64_t)a.T * a.k <= kSmallPlanRows) {
-#define NVFP4MOE_SMALL(V)                                                                     \
-  plan_small_kernel<V><<<1, kSmallPlanThreads, 0, s>>>(a.logits, a.T, a.E, a.k, a.shared_rows, \
-                                                       a.ids, a.w, a.counts, a.offsets,        \
-                                                       a.tile_start, a.perm_src, a.perm_w, a.inv)
+    const size_t smem = small_plan_smem_bytes(a.E);
+#define NVFP4MOE_SMALL(V)                                                                       \
+  do {                                                                                          \
+    if (smem > 48 * 1024)                                                                       \
+      cudaFuncSetAttribute(plan_small_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
+                           (int)smem);                                                          \
+    cudaError_t le = launch_pdl(plan_small_kernel<V>, dim3(1), dim3(kSmallPlanThreads), smem, s,  \
+        a.logits, a.T, a.E, a.k, a.shared_rows, a.ids, a.w, a.counts, a.offsets, a.tile_start, \
+        a.perm_src, a.perm_w, a.inv);                                                           \
+    if (le != cudaSuccess) return le;                                                           \
+  } while (0)
     if (vpl <= 1) NVFP4MOE_SMALL(1);
     else if (vpl <= 2) NVFP4MOE_SMALL(2);
     else if (vpl <= 4) NVFP4MOE_SMALL(4);
@@ -312,8 +185,8 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s) {
   if (err != cudaSuccess) return err;
   const int rblocks = (a.T + kRouterWarps - 1) / kRouterWarps;
 #define NVFP4MOE_ROUTER(V)                                                                 \
-  router_kernel<V><<<rblocks, kRouterWarps * 32, 0, s>>>(a.logits, a.T, a.E, a.k, tpc, a.ids, \
-                                                        a.w, a.hist)
+  err = launch_pdl(router_kernel<V>, dim3(rblocks), dim3(kRouterWarps * 32), 0, s, a.logits, a.T, \
+                   a.E, a.k, tpc, a.ids, a.w, a.hist)
   if (vpl <= 1) NVFP4MOE_ROUTER(1);
   else if (vpl <= 2) NVFP4MOE_ROUTER(2);
   else if (vpl <= 4) NVFP4MOE_ROUTER(4);
@@ -329,9 +202,8 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s) {
                                (int)scan_smem);
     if (err != cudaSuccess) return err;
   }
-  plan_scan_kernel<<<1, 1024, scan_smem, s>>>(a.hist, nchunks, a.E, a.shared_rows, a.base,
-                                              a.counts, a.offsets, a.tile_start);
-  err = cudaGetLastError();
+  err = launch_pdl(plan_scan_kernel, dim3(1), dim3(1024), scan_smem, s, (const int32_t*)a.hist,
+                   nchunks, a.E, a.shared_rows, a.base, a.counts, a.offsets, a.tile_start);
   if (err != cudaSuccess) return err;
   const int threads = ((tpc * a.k + 31) / 32) * 32;
   const size_t sc_smem = sizeof(int32_t) * (threads / 32) * a.E;
@@ -340,10 +212,9 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s) {
                                (int)sc_smem);
     if (err != cudaSuccess) return err;
   }
-  plan_scatter_kernel<<<nchunks, threads, sc_smem, s>>>(a.ids, a.w, a.T, a.E, a.k, tpc,
-                                                        a.shared_rows, a.base, a.offsets,
-                                                        a.perm_src, a.perm_w, a.inv);
-  return cudaGetLastError();
+  return launch_pdl(plan_scatter_kernel, dim3(nchunks), dim3(threads), sc_smem, s,
+                    (const int32_t*)a.ids, (const float*)a.w, a.T, a.E, a.k, tpc, a.shared_rows,
+                    (const int32_t*)a.base, (const int32_t*)a.offsets, a.perm_src, a.perm_w, a.inv);
 }
 
 }  // namespace nvfp4moe

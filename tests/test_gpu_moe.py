@@ -87,6 +87,8 @@ SMALL = [
     synth.custom_config("single", 1, 256, 1, 1, 256, config_id=124),
     # wider K and N than the tiny layer, ragged rows
     synth.custom_config("ragged_wide", 37, 1024, 16, 3, 768, config_id=125),
+    # large enough for the multi-kernel path (chunked plan, reduction combine), with a shared expert
+    synth.custom_config("general_path", 640, 1024, 16, 4, 256, shared_inter=256, config_id=127),
 ]
 
 
