@@ -209,7 +209,36 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
   cudaError_t e = mark(0);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
-  if (L.small) {
+  if (L.decode) {
+    // 1+2. a cluster: status reset, router and plan, activation quantiser in expert order
+    DecodePrologueArgs pr{};
+    pr.x = x;
+    pr.T = T;
+    pr.H = H;
+    pr.status = &hdr->status;
+    pr.ts = &hdr->ts;
+    pr.xq = ws + L.xq;
+    pr.xsf = ws + L.xsf;
+    pr.xq_perm = ws + L.xq_perm;
+    pr.xsf_tiles = ws + L.xsf_tiles;
+    pr.logits = logits;
+    pr.E = E;
+    pr.k = k;
+    pr.shared_rows = shared ? T : 0;
+    pr.ids = i32(L.ids);
+    pr.w = f32(L.w);
+    pr.counts = debug ? debug->counts : nullptr;
+    pr.offsets = i32(L.seg_off);
+    pr.tile_start = i32(L.tile_start);
+    pr.perm_src = i32(L.perm_src);
+    pr.perm_w = f32(L.perm_w);
+    pr.inv = i32(L.inv);
+    pr.perm_seg = i32(L.perm_seg);
+    e = launch_decode_prologue(pr, s);
+    if (e == cudaSuccess) e = mark(1);
+    if (e == cudaSuccess) e = mark(2);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  } else if (L.small) {
     // 1+2. one block: status reset, activation quantiser, router and plan
     PrologueArgs pr{};
     pr.x = x;
@@ -231,6 +260,7 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
     pr.perm_src = i32(L.perm_src);
     pr.perm_w = f32(L.perm_w);
     pr.inv = i32(L.inv);
+    pr.perm_seg = i32(L.perm_seg);
     e = launch_prologue_small(pr, s);
     if (e == cudaSuccess) e = mark(1);
     if (e == cudaSuccess) e = mark(2);
@@ -260,6 +290,7 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
   pa.perm_src = i32(L.perm_src);
   pa.perm_w = f32(L.perm_w);
   pa.inv = i32(L.inv);
+  pa.perm_seg = i32(L.perm_seg);
   pa.hist = i32(L.hist);
   pa.base = i32(L.base);
   pa.status = &hdr->status;
@@ -270,6 +301,13 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
 
   const int nseg = E + shared;
   const int64_t max_mtiles = ((int64_t)L.Rt + (int64_t)nseg * (kBM - 1)) / kBM;
+  if (!L.decode) {
+    // activations into expert order (the decode prologue writes them there itself)
+    e = launch_permute_rows(ws + L.xq, ws + L.xsf, T, H, L.Rt, E, i32(L.perm_src),
+                            i32(L.perm_seg), i32(L.seg_off), i32(L.tile_start), ws + L.xq_perm,
+                            ws + L.xsf_tiles, &hdr->status, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
   const float* w_ts = reinterpret_cast<const float*>(wb + W.ts);
 
   // 3. GEMM1 + SwiGLU + requantisation
@@ -292,7 +330,10 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
   g.hsf = ws + L.hsf;
   g.status = &hdr->status;
   // decode-sized batches: every expert has at most T <= kDecodeMaxRows rows, one tile each
-  const bool decode = T <= kDecodeMaxRows;
+  const bool decode = L.decode;
+  g.a_codes = ws + L.xq_perm;            // expert-ordered activations, read by TMA boxes
+  g.a_sf_tiles = ws + L.xsf_tiles;
+  g.hsf_tiles = ws + L.hsf_tiles;
   const int64_t item_rows = decode ? std::min<int64_t>(nseg, L.Rt) : max_mtiles;
   g.max_items = (int)std::min<int64_t>(item_rows * (g.N / kBN), INT32_MAX);
   g.max_ctas = g.max_items;
@@ -308,6 +349,7 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
   g2.a_codes = ws + L.hq;
   g2.a_sf = ws + L.hsf;
   g2.a_gather = nullptr;
+  g2.a_sf_tiles = ws + L.hsf_tiles;
   g2.b_tiles = wb + W.w2;
   g2.b_per_seg = W.w2_per_e;
   g2.N = H;

@@ -109,6 +109,20 @@ __device__ __forceinline__ void quant_block16_fast(const float* x, float ts, flo
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
 
+// NVFP4 quantisation of BF16 block b (elements 16b .. 16b+15 of x) with tensor scale ts.
+__device__ __forceinline__ void quant_bf16_block16(const uint4* __restrict__ x, int64_t b, float ts,
+                                                   uint32_t& lo, uint32_t& hi, uint32_t& sf) {
+  const uint4 v0 = __ldg(x + 2 * b), v1 = __ldg(x + 2 * b + 1);
+  const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+  float f[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    f[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
+    f[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+  }
+  quant_block16(f, ts, lo, hi, sf);
+}
+
 // NVFP4 encode of BF16 block b (elements 16b .. 16b+15 of x): 8 code bytes and 1 scale byte.
 __device__ __forceinline__ void encode_bf16_block16(const uint4* __restrict__ x, int64_t b,
                                                     float ts, uint2* __restrict__ codes,
@@ -158,6 +172,26 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t m, uint32_t* red) {
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+
+// Thread-block clusters: rank of this CTA, a full cluster barrier (release / acquire, so global
+// and shared writes before it are visible to every CTA of the cluster after it) and a 32-bit
+// load from another CTA's shared memory.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+__device__ __forceinline__ uint32_t ld_dsmem_u32(const void* local_smem, uint32_t rank) {
+  uint32_t ra, v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local_smem)), "r"(rank));
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(ra) : "memory");
+  return v;
+}
+
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

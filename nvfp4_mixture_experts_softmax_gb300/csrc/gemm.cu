@@ -1,24 +1,29 @@
 // Persistent grouped GEMM on the 5th-generation tensor cores with block-scaled FP4 operands
-// (tcgen05.mma kind::mxf4nvf4, E2M1 values, one E4M3 scale per 16 elements), used twice per layer:
-//   GEMM1: rows of the quantised activations gathered in expert order x the expert's interleaved
-//          gate/up weights; the epilogue applies the tensor scales, SwiGLU silu(g)*u, and
-//          requantises h to NVFP4 ("nvfp4-megamoe-kernel compare pre-b1...master", section "MoE
-//          kernel (FusedSwiGLUScaledGroupedGemmKernel)": epilogue with global scale + SwiGLU in
+// (tcgen05.mma kind::mxf4nvf4, E2M1 values, one E4M3 scale per 16 elements), used twice per layer
+// for batches larger than the decode path's:
+//   GEMM1: the expert-ordered quantised activations x the expert's interleaved gate/up weights;
+//          the epilogue applies the tensor scales, SwiGLU silu(g)*u, and requantises h to NVFP4
+//          ("nvfp4-megamoe-kernel compare pre-b1...master", section "MoE kernel
+//          (FusedSwiGLUScaledGroupedGemmKernel)": epilogue with global scale + SwiGLU in
 //          registers between the tensor-memory load and the store);
-//   GEMM2: the requantised h x the expert's down weights; the epilogue scales by the tensor scales
-//          and the router weight and accumulates into the token's FP32 output row
+//   GEMM2: h x the expert's down weights; the epilogue scales by the tensor scales and the router
+//          weight and reduces into the token's FP32 output row (or stores the row)
 //          ("vllm.cpp docs/STATUS.md", row "Brick C part 1": y = sum_j w_j * expert_out_j).
 //
-// One CTA per SM, warp-specialised (the pages' design uses TMA / MMA / epilogue / scheduler warps;
-// here the scheduler is a static round robin over a device-built tile list):
+// Tiles are 128 expert-ordered rows (MMA M) x 128 weight rows (MMA N), K in stages of 256.  Every
+// operand arrives by the copy engine: per stage one 2-D TMA box of the 128 activation rows
+// (128-byte swizzle; an expert's rows are contiguous in the expert-ordered buffer), one bulk
+// copy of their pre-arranged scales, and one bulk copy of the packed weight block.  One CTA per
+// SM, warp-specialised (the pages' design uses TMA / MMA / epilogue warps and a scheduler warp;
+// here the schedule is a static round robin over the device-built tile list):
 //   warps 0-3  epilogue: tensor memory -> registers -> global, one accumulator row per thread;
-//   warp  4    TMA: one bulk copy per stage of the pre-swizzled weight block and its scales;
-//   warp  5    tensor-memory allocation and the single MMA-issuing thread;
-//   warps 6-9  activation rows gathered with cp.async into the same 128B-swizzled layout, and
-//              their scales into the 32x4x4 arrangement the scale-factor copy expects.
-// A 5-stage shared-memory ring (mbarrier full/empty pairs) feeds the MMA; two 128-column FP32
-// accumulators in tensor memory let the epilogue of one tile overlap the main loop of the next.
-// Every wait is bounded in time and reports MOE_ERR_DEVICE_TIMEOUT instead of hanging.
+//   warp  4    copy issue; warp 5 tensor-memory allocation and the single MMA-issuing thread.
+// A 6-stage shared-memory ring (mbarrier full/empty pairs) feeds the MMA; two 128-column FP32
+// accumulators let the epilogue of one tile overlap the main loop of the next.  Every wait is
+// bounded in time and reports MOE_ERR_DEVICE_TIMEOUT instead of hanging.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -30,25 +35,23 @@ constexpr int kStages = 6;
 constexpr int kEpiWarps = 4;
 constexpr int kTmaWarp = 4;
 constexpr int kMmaWarp = 5;
-constexpr int kProdWarp0 = 6;
-constexpr int kProdWarps = 4;
-constexpr int kThreads = (kProdWarp0 + kProdWarps) * 32;
-// Stage layout: A codes | A scales | B codes | B scales.  B codes + scales are one packed weight
-// block (kTileBlockBytes contiguous bytes in global memory), loaded with a single bulk copy.
+constexpr int kThreads = (kMmaWarp + 1) * 32;
+// Stage layout: A codes | A scales | B block (codes + scales, one packed weight block).
 constexpr int kABytes = kBM * 128;
 constexpr int kSfBytes = 4 * 512;  // four 512-byte scale groups (one per 64-wide MMA K step)
 constexpr int kBOff = kABytes + kSfBytes;
 constexpr int kStageBytes = kBOff + kTileBlockBytes;
-static_assert(kBN == 128 && kTileBlockBytes == kBN * 128 + kSfBytes, "packed block = B stage");
-static_assert(kBOff % 1024 == 0, "B tile stays 1024-byte aligned for the 128B swizzle");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = kBN;
 constexpr uint32_t kSfCol0 = 2 * kAccCols;
 constexpr uint32_t kSfColsPerStage = 32;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
+static_assert(kBN == 128 && kTileBlockBytes == kBN * 128 + kSfBytes, "packed block = B stage");
+static_assert(kBOff % 1024 == 0, "B tile stays 1024-byte aligned for the 128B swizzle");
 static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "tensor memory budget");
 static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
+static_assert(kStages * kStageBytes + 1024 + 256 + 8 * 1027 <= 232448, "shared memory");
 
 // Instruction descriptor of tcgen05.mma kind::mxf4nvf4: A and B E2M1 (format 1) at bits 7-9 and
 // 10-12, both K-major, N >> 3 at bits 17-22, UE4M3 scale type (bit 23 = 0), M >> 4 at bits 24-28,
@@ -84,13 +87,8 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
   return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
-// Tile row r is placed at accumulator lane (r % 4) * 32 + r / 4, so that the valid rows of a
-// nearly empty tile (decode) are spread over the four epilogue warps instead of all landing in
-// the first one.  lane_of_row and row_of_lane are inverse bijections of [0, 128).
-__device__ __forceinline__ int lane_of_row(int r) { return (r & 3) * 32 + (r >> 2); }
-__device__ __forceinline__ int row_of_lane(int l) { return (l & 31) * 4 + (l >> 5); }
-
-__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const GemmArgs p) {
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -111,7 +109,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const GemmArg
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(full + s), 2);  // one producer warp + the TMA thread
+      mbar_init(smem_u32(full + s), 1);  // the copy-issuing thread (expect_tx)
       mbar_init(smem_u32(empty + s), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -121,6 +119,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const GemmArg
     mbar_init(smem_u32(drain), 1);
     fence_barrier_init();
   }
+  if (warp == kTmaWarp && lane == 0)
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_a) : "memory");
   // everything above touched only shared and tensor memory; wait for the producer kernel now
   griddep_wait();
   griddep_launch();
@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const GemmArg
   const uint32_t smem0 = smem_u32(smem);
 
   if (warp == kTmaWarp) {
-    // ---------------- weight tiles (TMA) ----------------
+    // ---------------- all operands: TMA box of A rows + bulk copies ----------------
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
@@ -152,15 +152,19 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const GemmArg
         const TileInfo t = decode_tile(item, n_tiles, s_tile, s_seg, p.nseg);
         const uint8_t* bsrc = p.b_tiles + (size_t)t.seg * p.b_per_seg +
                               (size_t)t.nt * kst * kTileBlockBytes;
+        // the global m-tile index is also the tile of the pre-arranged activation scales
+        const uint8_t* asf = p.a_sf_tiles + (size_t)(item / n_tiles) * (p.K / 64) * 512;
         for (int ks = 0; ks < kst; ++ks) {
           if (!mbar_wait_bounded(smem_u32(empty + stage), phase ^ 1u, kWaitLimitNs, p.status)) {
             ok = false;
             break;
           }
           const uint32_t sb = smem0 + stage * kStageBytes;
-          mbar_arrive_expect_tx(smem_u32(full + stage), kTileBlockBytes);
-          bulk_load(sb + kBOff, bsrc + (size_t)ks * kTileBlockBytes, kTileBlockBytes,
-                    smem_u32(full + stage));
+          const uint32_t fb = smem_u32(full + stage);
+          mbar_arrive_expect_tx(fb, kStageBytes);
+          tma_load_2d(sb, &tmap_a, ks * 128, t.m0, fb);
+          bulk_load(sb + kABytes, asf + (size_t)ks * kSfBytes, kSfBytes, fb);
+          bulk_load(sb + kBOff, bsrc + (size_t)ks * kTileBlockBytes, kTileBlockBytes, fb);
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
@@ -221,86 +225,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const GemmArg
       tc_commit(smem_u32(drain));
       mbar_wait_bounded(smem_u32(drain), 0u, kWaitLimitNs, p.status);
     }
-  } else if (warp >= kProdWarp0) {
-    // ---------------- activation rows (cp.async gather) ----------------
-    // Producer warp wp owns every kProdWarps-th pipeline stage.  For a stage it owns it copies the
-    // valid rows' 128-byte K slices into the 128B-swizzled layout and their scale words into the
-    // 32x4x4 scale arrangement, waits for its own copies, fences them for the tensor core's async
-    // proxy and arrives on the stage's full barrier.  Stages owned by different warps are in
-    // flight together, so no stage waits on an earlier stage's copies.  Rows past the tile's last
-    // valid row are not written: their accumulator rows are never stored.
-    const int wp = warp - kProdWarp0;
-    int stage = 0;
-    uint32_t phase = 0;
-    int j = 0;  // pipeline stages issued so far by the CTA (all warps count them alike)
-    bool ok = true;
-    for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
-      const TileInfo t = decode_tile(item, n_tiles, s_tile, s_seg, p.nseg);
-      const int first_own = (wp - (j % kProdWarps) + kProdWarps) % kProdWarps;
-      int src[4] = {-1, -1, -1, -1};  // source row of tile rows lane + 32 i
-      if (first_own < kst) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = lane + 32 * i;
-          const int pr = t.m0 + r;
-          if (r < t.rows) {
-            int sr = -1;
-            if (pr >= 0 && pr < p.out_rows) sr = p.a_gather ? __ldg(p.a_gather + pr) : pr;
-            if (sr < 0 || sr >= p.a_rows) {
-              set_status(p.status, MOE_ERR_INVALID_ARG);
-              sr = -1;
-            }
-            src[i] = sr;
-          }
-        }
-      }
-      for (int ks = 0; ks < kst; ++ks, ++j) {
-        if (j % kProdWarps == wp) {
-          if (!mbar_wait_bounded(smem_u32(empty + stage), phase ^ 1u, kWaitLimitNs, p.status)) {
-            ok = false;
-            break;
-          }
-          const uint32_t sb = smem0 + stage * kStageBytes;
-          // codes: 16-byte chunk (lane & 7) of rows (lane >> 3) + 4 i
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            if (4 * i >= t.rows) break;
-            const int r = (lane >> 3) + 4 * i;
-            const int sr = __shfl_sync(0xffffffffu, src[i >> 3], r & 31);
-            if (r < t.rows && sr >= 0) {
-              const int c = lane & 7, L = lane_of_row(r);
-              cp_async_16(sb + L * 128 + ((c ^ (L & 7)) << 4),
-                          p.a_codes + (size_t)sr * (p.K / 2) + ks * 128 + c * 16, 16);
-            }
-          }
-          // scales: word (lane & 3) of rows (lane >> 2) + 8 i
-          const uint32_t sfa_s = sb + kABytes;
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            if (8 * i >= t.rows) break;
-            const int r = (lane >> 2) + 8 * i;
-            const int sr = __shfl_sync(0xffffffffu, src[i >> 2], r & 31);
-            if (r < t.rows && sr >= 0) {
-              const int kk = lane & 3, L = lane_of_row(r);
-              cp_async_4(sfa_s + kk * 512 + (L & 31) * 16 + (L >> 5) * 4,
-                         p.a_sf + (size_t)sr * (p.K / 16) + ks * 16 + kk * 4, 4);
-            }
-          }
-          cp_async_commit();
-          cp_async_wait<0>();
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(full + stage));
-        }
-        if (++stage == kStages) { stage = 0; phase ^= 1u; }
-      }
-    }
-    cp_async_wait<0>();
   } else {
     // ---------------- epilogue (warps 0-3) ----------------
     uint32_t acc_phase[2] = {0u, 0u};
     int it = 0;
-    const int r = row_of_lane(warp * 32 + lane);   // this thread's accumulator lane -> tile row
+    const int r = warp * 32 + lane;   // this thread's accumulator lane = tile row
     const float ts_a = p.mode == 0 ? *p.ts_a : 0.0f;
     const float inv_ts_h = 1.0f / p.ts_h;
     for (int item = blockIdx.x; item < total; item += gridDim.x, ++it) {
@@ -317,6 +246,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const GemmArg
         const float ag = ts_a * p.w_ts[t.seg * 4 + 0];
         const float au = ts_a * p.w_ts[t.seg * 4 + 1];
         const int I = p.N / 2;
+        const size_t mt = (size_t)(item / n_tiles);
+        const int rr = r & 127;
+        uint8_t* hsf_tile = p.hsf_tiles + mt * (I / 64) * 512 + (rr & 31) * 16 + (rr >> 5) * 4;
 #pragma unroll 1
         for (int c = 0; c < kBN / 32; ++c) {
           uint32_t v[32];
@@ -332,6 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const GemmArg
             const int f0 = t.nt * (kBN / 2) + c * 16;
             *reinterpret_cast<uint2*>(p.hq + (size_t)prow * (I / 2) + f0 / 2) = make_uint2(lo, hi);
             p.hsf[(size_t)prow * (I / 16) + f0 / 16] = (uint8_t)s;
+            hsf_tile[(size_t)(f0 / 64) * 512 + ((f0 / 16) & 3)] = (uint8_t)s;
           }
         }
       } else {
@@ -388,7 +321,32 @@ size_t gemm_smem_bytes(int nseg) {
 
 }  // namespace
 
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn_general() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s) {
+  auto encode = encode_fn_general();
+  if (!encode) return cudaErrorNotSupported;
+  // expert-ordered activation rows [out_rows, K/2] bytes; box = 128 bytes x 128 rows, 128B swizzle
+  CUtensorMap tmap;
+  const cuuint64_t dims[2] = {(cuuint64_t)(a.K / 2), (cuuint64_t)a.out_rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)(a.K / 2)};
+  const cuuint32_t box[2] = {128, (cuuint32_t)kBM};
+  const cuuint32_t estr[2] = {1, 1};
+  if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.a_codes), dims,
+             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
   const size_t smem = gemm_smem_bytes(a.nseg);
   cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -396,7 +354,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s) {
   int grid = a.max_ctas;
   if (grid > num_sms()) grid = num_sms();
   if (grid < 1) grid = 1;
-  return launch_pdl(grouped_gemm_kernel, dim3(grid), dim3(kThreads), smem, s, a);
+  return launch_pdl(grouped_gemm_kernel, dim3(grid), dim3(kThreads), smem, s, tmap, a);
 }
 
 }  // namespace nvfp4moe

@@ -9,9 +9,16 @@
 //          requantises the block with half-warp reductions;
 //   GEMM2 (mode 1 / 2): lanes hold consecutive output features, so a token's row is written (or
 //          reduced) 128 contiguous bytes per warp.
-// Warp roles and the pipeline are those of the general kernel in gemm.cu ("nvfp4-megamoe-kernel
-// compare pre-b1...master", section "MoE kernel": TMA, MMA and epilogue warps; the pages keep
-// decode on 1-CTA tiles).
+// Every operand arrives by the copy engine: per stage one bulk copy of the weight block, one
+// 2-D TMA tile (128-byte swizzle) of the expert's token rows - the activations (GEMM1) or h
+// (GEMM2) are stored in expert order, so an expert's rows are contiguous - and one bulk copy of
+// the tokens' scales, which the producer kernels write pre-arranged per expert tile.  Warps:
+// 0-3 epilogue, 4 copy issue, 5 MMA ("nvfp4-megamoe-kernel compare pre-b1...master", section
+// "MoE kernel": TMA, MMA and epilogue warps; the pages keep decode on 1-CTA tiles).  Four TMEM
+// accumulators let the epilogue trail the main loop by up to three tiles.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -20,25 +27,28 @@ namespace nvfp4moe {
 namespace {
 
 constexpr int kStages = 7;
+constexpr int kAccBufs = 3;
+constexpr int kXBoxRows = 16;                          // token rows per TMA box
 constexpr int kEpiWarps = 4;
 constexpr int kTmaWarp = 4;
 constexpr int kMmaWarp = 5;
-constexpr int kProdWarp0 = 6;
-constexpr int kProdWarps = 4;
-constexpr int kThreads = (kProdWarp0 + kProdWarps) * 32;
+constexpr int kThreads = (kMmaWarp + 1) * 32;
 constexpr int kNmax = kDecodeMaxRows;                 // token rows per expert tile
 constexpr int kXOff = kTileBlockBytes;                 // token codes after the weight block
-constexpr int kXSfOff = kXOff + kNmax * 128;           // token scales
-constexpr int kStageBytes = kXSfOff + 4 * 512;
+constexpr int kXBytes = kNmax * 128;
+constexpr int kXSfOff = kXOff + kXBytes;               // token scales
+constexpr int kXSfBytes = 4 * 512;
+constexpr int kStageBytes = kXSfOff + kXSfBytes;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = kNmax;
-constexpr uint32_t kSfCol0 = 2 * kAccCols;
+constexpr uint32_t kSfCol0 = kAccBufs * kAccCols;
 constexpr uint32_t kSfColsPerStage = 32;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "tensor memory budget");
 static_assert(kStageBytes % 1024 == 0 && kXOff % 1024 == 0, "1024-byte aligned swizzled tiles");
-static_assert(kNmax % 16 == 0 && kNmax <= 64, "token tile");
+static_assert(kStages * kStageBytes + 1024 + 256 + 8 * 1027 <= 232448, "shared memory");
+static_assert(kNmax % kXBoxRows == 0 && kNmax <= 64, "token tile");
 
 constexpr uint32_t make_idesc(int M, int N) {
   return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
@@ -74,7 +84,8 @@ __device__ __forceinline__ void red_add_f32(float* addr, float v) {
   asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
 }
 
-__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_decode_kernel(const GemmArgs p) {
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_decode_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -82,8 +93,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_decode_kernel(const 
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* acc_full = bars + 2 * kStages;
-  uint64_t* acc_empty = acc_full + 2;
-  uint64_t* drain = acc_empty + 2;
+  uint64_t* acc_empty = acc_full + kAccBufs;
+  uint64_t* drain = acc_empty + kAccBufs;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int32_t* s_tile = reinterpret_cast<int32_t*>(smem + kStages * kStageBytes + 256);
   int32_t* s_seg = s_tile + (p.nseg + 1);
@@ -95,16 +106,18 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_decode_kernel(const 
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(full + s), 2);  // one token-gather warp + the weight copy
+      mbar_init(smem_u32(full + s), 1);  // the copy-issuing thread (expect_tx)
       mbar_init(smem_u32(empty + s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kAccBufs; ++b) {
       mbar_init(smem_u32(acc_full + b), 1);
       mbar_init(smem_u32(acc_empty + b), kEpiWarps);
     }
     mbar_init(smem_u32(drain), 1);
     fence_barrier_init();
   }
+  if (warp == kTmaWarp && lane == 0)
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_x) : "memory");
   griddep_wait();
   griddep_launch();
   for (int i = threadIdx.x; i <= p.nseg; i += blockDim.x) {
@@ -126,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_decode_kernel(const 
   const uint32_t smem0 = smem_u32(smem);
 
   if (warp == kTmaWarp) {
-    // ---------------- weight blocks: one bulk copy per stage ----------------
+    // ---------------- all operands: bulk copies + one 2-D TMA tile per stage ----------------
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
@@ -135,14 +148,23 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_decode_kernel(const 
         const TileInfo t = decode_item(item, n_tiles, s_tile, s_seg, p.nseg);
         const uint8_t* src = p.b_tiles + (size_t)t.seg * p.b_per_seg +
                              (size_t)t.nt * kst * kTileBlockBytes;
+        const uint8_t* xsf = p.a_sf_tiles + (size_t)s_tile[t.seg] * (p.K / 64) * 512;
         for (int ks = 0; ks < kst; ++ks) {
           if (!mbar_wait_bounded(smem_u32(empty + stage), phase ^ 1u, kWaitLimitNs, p.status)) {
             ok = false;
             break;
           }
           const uint32_t sb = smem0 + stage * kStageBytes;
-          mbar_arrive_expect_tx(smem_u32(full + stage), kTileBlockBytes);
-          bulk_load(sb, src + (size_t)ks * kTileBlockBytes, kTileBlockBytes, smem_u32(full + stage));
+          const uint32_t fb = smem_u32(full + stage);
+          // only the boxes that hold the expert's rows (16 rows each); the rest of the token
+          // tile stays stale and only feeds accumulator columns that are never stored
+          const int nbox = (max(t.rows, 1) + kXBoxRows - 1) / kXBoxRows;
+          mbar_arrive_expect_tx(fb, kTileBlockBytes + nbox * kXBoxRows * 128 + kXSfBytes);
+          bulk_load(sb, src + (size_t)ks * kTileBlockBytes, kTileBlockBytes, fb);
+          for (int bx = 0; bx < nbox; ++bx)
+            tma_load_2d(sb + kXOff + bx * kXBoxRows * 128, &tmap_x, ks * 128,
+                        t.m0 + bx * kXBoxRows, fb);
+          bulk_load(sb + kXSfOff, xsf + (size_t)ks * kXSfBytes, kXSfBytes, fb);
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
@@ -156,14 +178,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_decode_kernel(const 
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t acc_phase[2] = {0u, 0u};
+      uint32_t acc_phase[kAccBufs] = {};
       bool ok = true;
       int it = 0;
       for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++it) {
         const TileInfo t = decode_item(item, n_tiles, s_tile, s_seg, p.nseg);
         const int nmma = max(16, (t.rows + 15) & ~15);
         const uint32_t idesc = make_idesc(128, nmma);
-        const int abuf = it & 1;
+        const int abuf = it % kAccBufs;
         if (!mbar_wait_bounded(smem_u32(acc_empty + abuf), acc_phase[abuf] ^ 1u, kWaitLimitNs,
                                p.status)) {
           ok = false;
@@ -203,82 +225,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_decode_kernel(const 
       tc_commit(smem_u32(drain));
       mbar_wait_bounded(smem_u32(drain), 0u, kWaitLimitNs, p.status);
     }
-  } else if (warp >= kProdWarp0) {
-    // ---------------- token rows (cp.async gather), stage ownership round robin ----------------
-    const int wp = warp - kProdWarp0;
-    int stage = 0;
-    uint32_t phase = 0;
-    int j = 0;
-    bool ok = true;
-    for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
-      const TileInfo t = decode_item(item, n_tiles, s_tile, s_seg, p.nseg);
-      const int first_own = (wp - (j % kProdWarps) + kProdWarps) % kProdWarps;
-      int src[2] = {-1, -1};   // source row of token rows lane and lane + 32
-      if (first_own < kst) {
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int r = lane + 32 * i;
-          const int pr = t.m0 + r;
-          if (r < t.rows) {
-            int sr = -1;
-            if (pr >= 0 && pr < p.out_rows) sr = p.a_gather ? __ldg(p.a_gather + pr) : pr;
-            if (sr < 0 || sr >= p.a_rows) {
-              set_status(p.status, MOE_ERR_INVALID_ARG);
-              sr = -1;
-            }
-            src[i] = sr;
-          }
-        }
-      }
-      for (int ks = 0; ks < kst; ++ks, ++j) {
-        if (j % kProdWarps == wp) {
-          if (!mbar_wait_bounded(smem_u32(empty + stage), phase ^ 1u, kWaitLimitNs, p.status)) {
-            ok = false;
-            break;
-          }
-          const uint32_t sb = smem0 + stage * kStageBytes;
-#pragma unroll
-          for (int i = 0; i < kNmax / 4; ++i) {      // 16-byte chunk (lane & 7) of row (lane>>3)+4i
-            if (4 * i >= t.rows) break;
-            const int r = (lane >> 3) + 4 * i;
-            const int sr = __shfl_sync(0xffffffffu, src[i >> 3], r & 31);
-            if (r < t.rows && sr >= 0) {
-              const int c = lane & 7;
-              cp_async_16(sb + kXOff + r * 128 + ((c ^ (r & 7)) << 4),
-                          p.a_codes + (size_t)sr * (p.K / 2) + ks * 128 + c * 16, 16);
-            }
-          }
-#pragma unroll
-          for (int i = 0; i < kNmax / 8; ++i) {      // scale word (lane & 3) of row (lane>>2)+8i
-            if (8 * i >= t.rows) break;
-            const int r = (lane >> 2) + 8 * i;
-            const int sr = __shfl_sync(0xffffffffu, src[i >> 2], r & 31);
-            if (r < t.rows && sr >= 0) {
-              const int kk = lane & 3;
-              cp_async_4(sb + kXSfOff + kk * 512 + (r & 31) * 16 + (r >> 5) * 4,
-                         p.a_sf + (size_t)sr * (p.K / 16) + ks * 16 + kk * 4, 4);
-            }
-          }
-          cp_async_commit();
-          cp_async_wait<0>();
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(full + stage));
-        }
-        if (++stage == kStages) { stage = 0; phase ^= 1u; }
-      }
-    }
-    cp_async_wait<0>();
   } else {
     // ---------------- epilogue (warps 0-3): lane = weight row, column = token ----------------
-    uint32_t acc_phase[2] = {0u, 0u};
+    uint32_t acc_phase[kAccBufs] = {};
     int it = 0;
     const float ts_a = p.mode == 0 ? *p.ts_a : 0.0f;
     const float inv_ts_h = 1.0f / p.ts_h;
     const bool lo_half = lane < 16;
     for (int item = blockIdx.x; item < total; item += gridDim.x, ++it) {
       const TileInfo t = decode_item(item, n_tiles, s_tile, s_seg, p.nseg);
-      const int abuf = it & 1;
+      const int abuf = it % kAccBufs;
       if (!mbar_wait_bounded(smem_u32(acc_full + abuf), acc_phase[abuf], kWaitLimitNs, p.status))
         break;
       acc_phase[abuf] ^= 1u;
@@ -289,6 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_decode_kernel(const 
         // block b of h: 16 features; lanes < 16 hold gate rows, lanes >= 16 the up rows
         const int I = p.N / 2;
         const int b = t.nt * 4 + warp;
+        uint8_t* hsf_tile = p.hsf_tiles + ((size_t)s_tile[t.seg] * (I / 64) + b / 4) * 512 + (b & 3);
         const float ag = ts_a * p.w_ts[t.seg * 4 + 0];
         const float au = ts_a * p.w_ts[t.seg * 4 + 1];
 #pragma unroll 1
@@ -329,6 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_decode_kernel(const 
               const size_t prow = (size_t)(t.m0 + col);
               *reinterpret_cast<uint2*>(p.hq + prow * (I / 2) + b * 8) = make_uint2(word, word_hi);
               p.hsf[prow * (I / 16) + b] = (uint8_t)sf;
+              hsf_tile[(col & 31) * 16 + (col >> 5) * 4] = (uint8_t)sf;
             }
           }
         }
@@ -389,9 +347,36 @@ size_t smem_bytes(int nseg) {
   return 1024 + (size_t)kStages * kStageBytes + 256 + sizeof(int32_t) * 2 * (nseg + 2);
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
 }  // namespace
 
+bool tensor_map_available() { return encode_fn() != nullptr; }
+
 cudaError_t launch_grouped_gemm_decode(const GemmArgs& a, cudaStream_t s) {
+  auto encode = encode_fn();
+  if (!encode) return cudaErrorNotSupported;
+  // token rows [out_rows, K/2] bytes in expert order; box = 128 bytes x 16 rows, 128B swizzle
+  CUtensorMap tmap;
+  const cuuint64_t dims[2] = {(cuuint64_t)(a.K / 2), (cuuint64_t)a.out_rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)(a.K / 2)};
+  const cuuint32_t box[2] = {128, (cuuint32_t)kXBoxRows};
+  const cuuint32_t estr[2] = {1, 1};
+  if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.a_codes), dims,
+             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
   const size_t smem = smem_bytes(a.nseg);
   cudaError_t e = cudaFuncSetAttribute(grouped_gemm_decode_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -399,7 +384,7 @@ cudaError_t launch_grouped_gemm_decode(const GemmArgs& a, cudaStream_t s) {
   int grid = a.max_ctas;
   if (grid > num_sms()) grid = num_sms();
   if (grid < 1) grid = 1;
-  return launch_pdl(grouped_gemm_decode_kernel, dim3(grid), dim3(kThreads), smem, s, a);
+  return launch_pdl(grouped_gemm_decode_kernel, dim3(grid), dim3(kThreads), smem, s, tmap, a);
 }
 
 }  // namespace nvfp4moe

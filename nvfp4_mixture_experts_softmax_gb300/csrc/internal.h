@@ -18,6 +18,7 @@ constexpr int kBM = 128;       // permuted rows per tile (MMA M)
 constexpr int kBN = 128;       // output columns per tile (MMA N)
 constexpr int kBK = 256;       // FP4 elements of K per pipeline stage (128 bytes per row)
 constexpr int kMmaK = 64;      // K of one block-scaled FP4 MMA
+constexpr int kDecodeMaxRows = 64;   // batches up to this many tokens take the decode path
 
 // Router chunking: tokens per chunk (one router block and one scatter block each).
 inline int plan_tokens_per_chunk(int k) { return k <= 16 ? 64 : 32; }
@@ -82,9 +83,10 @@ bool prologue_small_fits(int T, int H, int k);
 // Workspace of moe_run for T tokens.  Offset 0 holds the device status word.
 struct RunLayout {
   size_t hdr, amax_part, ids, w, hist, base, seg_off, tile_start, perm_src, perm_w, inv, xq, xsf,
-      hq, hsf, yacc, obuf, total;
-  int T, R, Rt, nseg, nchunks, tpc;
+      hq, hsf, yacc, obuf, perm_seg, xq_perm, xsf_tiles, hsf_tiles, total;
+  int T, R, Rt, nseg, nchunks, tpc, dtiles;
   bool small;   // fused prologue + stored-row combine
+  bool decode;  // T <= kDecodeMaxRows: cluster prologue and the swapped-operand decode GEMM
   RunLayout(const moe_config& c, int T_) {
     T = T_;
     const int k = c.top_k, E = c.num_experts, H = c.hidden, I = c.inter;
@@ -114,6 +116,13 @@ struct RunLayout {
             (int64_t)Rt * H <= kStoreCombineElems;
     yacc = o;       o = align_up(o + (small ? 0 : 4 * (size_t)T * H));
     obuf = o;       o = align_up(o + (small ? 4 * (size_t)Rt * H : 0));
+    decode = small && T <= kDecodeMaxRows;
+    // m-tiles of 128 expert-ordered rows (decode: one per active expert)
+    dtiles = decode ? (nseg < Rt ? nseg : Rt) : (int)(((int64_t)Rt + (int64_t)nseg * 127) / 128);
+    perm_seg = o;   o = align_up(o + 4 * (size_t)Rt);
+    xq_perm = o;    o = align_up(o + (size_t)Rt * H / 2);
+    xsf_tiles = o;  o = align_up(o + (size_t)dtiles * (H / 64) * 512);
+    hsf_tiles = o;  o = align_up(o + (size_t)dtiles * (I / 64) * 512);
     total = o;
   }
 };
@@ -151,6 +160,7 @@ struct PlanArgs {
   int32_t* perm_src;      // [R + shared_rows]
   float* perm_w;          // [R + shared_rows] (may be null)
   int32_t* inv;           // [T*k]
+  int32_t* perm_seg;      // [R + shared_rows] expert (segment) of each permuted row (may be null)
   int32_t* hist;          // [nchunks*E] scratch
   int32_t* base;          // [nchunks*E] scratch
   int32_t* status;
@@ -191,15 +201,30 @@ struct GemmArgs {
   int out_rows;           // rows of hq / hsf (mode 0) or of the permuted space (mode 1)
   int y_rows;             // rows of yacc (mode 1)
   int max_items;          // upper bound of m-tiles x n-tiles
+  // decode kernel only: token rows are contiguous per expert (a_codes in permuted order, read
+  // through a tensor map), their scales pre-arranged per expert tile, and GEMM1 also writes the
+  // scales of h in that arrangement for GEMM2
+  const uint8_t* a_sf_tiles;  // [tiles][K/64][512]
+  uint8_t* hsf_tiles;         // mode 0 out [tiles][(N/2)/64][512]
 };
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s);
 
 // Decode-sized batches (T <= kDecodeMaxRows, so no expert receives more rows): weights as the
 // MMA's M operand, tokens as N (gemm_decode.cu).  Same arguments as launch_grouped_gemm.
-constexpr int kDecodeMaxRows = 64;
 cudaError_t launch_grouped_gemm_decode(const GemmArgs& a, cudaStream_t s);
+// 2-D tensor map encoder of the driver, fetched through the runtime (no libcuda link).
+bool tensor_map_available();
 
 cudaError_t launch_finalize(const float* yacc, void* y, int64_t n, cudaStream_t s);
+
+// Copies quantised activation rows into expert (permuted) order and scatters their scale words
+// into the GEMM's tile arrangement: row p takes token perm_src[p]; its tile is
+// tile_start[e] + (p - offsets[e]) / 128 for its expert e = perm_seg[p].
+cudaError_t launch_permute_rows(const uint8_t* xq, const uint8_t* xsf, int T, int H, int Rt,
+                                int E, const int32_t* perm_src, const int32_t* perm_seg,
+                                const int32_t* offsets, const int32_t* tile_start,
+                                uint8_t* xq_perm, uint8_t* xsf_tiles, int32_t* status,
+                                cudaStream_t s);
 cudaError_t launch_finalize_gather(const float* o, const int32_t* inv, int T, int k, int H,
                                    int shared, void* y, cudaStream_t s);
 
@@ -212,10 +237,28 @@ struct PrologueArgs {
   uint8_t* xsf;            // [T, H/16]
   const float* logits;     // [T, E]
   int E, k, shared_rows;
-  int32_t *ids, *counts, *offsets, *tile_start, *perm_src, *inv;
+  int32_t *ids, *counts, *offsets, *tile_start, *perm_src, *inv, *perm_seg;
   float *w, *perm_w;
 };
 cudaError_t launch_prologue_small(const PrologueArgs& a, cudaStream_t s);
+
+// Decode batches: the prologue as a cluster that also writes the activations in expert order.
+constexpr int kDecodeProCtas = 8;
+struct DecodePrologueArgs {
+  const void* x;           // [T, H] BF16
+  int T, H;
+  int32_t* status;
+  float* ts;
+  uint8_t* xq;             // [T, H/2]  token order
+  uint8_t* xsf;            // [T, H/16]
+  uint8_t* xq_perm;        // [Rt, H/2] permuted (expert) order
+  uint8_t* xsf_tiles;      // [tiles][H/64][512] token-operand scale arrangement
+  const float* logits;     // [T, E]
+  int E, k, shared_rows;
+  int32_t *ids, *counts, *offsets, *tile_start, *perm_src, *inv, *perm_seg;
+  float *w, *perm_w;
+};
+cudaError_t launch_decode_prologue(const DecodePrologueArgs& a, cudaStream_t s);
 
 int num_sms();
 

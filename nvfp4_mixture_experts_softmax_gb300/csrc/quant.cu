@@ -218,6 +218,50 @@ __global__ void __launch_bounds__(kThreads) finalize_gather_kernel(const float4*
   }
 }
 
+// Expert-ordered copy of the quantised activations: 16-byte code vectors, then 4-scale words into
+// the 32x4x4 arrangement of the GEMM tiles (see launch_permute_rows).
+__global__ void __launch_bounds__(kThreads) permute_rows_kernel(
+    const uint4* __restrict__ xq, const uint32_t* __restrict__ xsf, int T, int H, int Rt, int E,
+    const int32_t* __restrict__ perm_src, const int32_t* __restrict__ perm_seg,
+    const int32_t* __restrict__ offsets, const int32_t* __restrict__ tile_start,
+    uint4* __restrict__ xq_perm, uint8_t* __restrict__ xsf_tiles, int32_t* status) {
+  griddep_wait();
+  griddep_launch();
+  const int vpr = H / 32, wpr = H / 64;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t nvec = (int64_t)Rt * vpr;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+    const int64_t p = i / vpr;
+    const int v = (int)(i - p * vpr);
+    const int t = __ldg(perm_src + p);
+    if (t < 0 || t >= T) {
+      set_status(status, MOE_ERR_INVALID_ARG);
+      continue;
+    }
+    xq_perm[p * vpr + v] = __ldg(xq + (int64_t)t * vpr + v);
+  }
+  const int64_t nw = (int64_t)Rt * wpr;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nw; i += stride) {
+    const int64_t p = i / wpr;
+    const int wd = (int)(i - p * wpr);
+    const int t = __ldg(perm_src + p);
+    const int e = __ldg(perm_seg + p);
+    if (t < 0 || t >= T || e < 0 || e > E) {
+      set_status(status, MOE_ERR_INVALID_ARG);
+      continue;
+    }
+    const int r = (int)(p - __ldg(offsets + e));
+    if (r < 0) {
+      set_status(status, MOE_ERR_INVALID_ARG);
+      continue;
+    }
+    const int64_t tile = __ldg(tile_start + e) + (r >> 7);
+    const int rr = r & 127;
+    *reinterpret_cast<uint32_t*>(xsf_tiles + (tile * wpr + wd) * 512 + (rr & 31) * 16 + (rr >> 5) * 4) =
+        __ldg(xsf + (int64_t)t * wpr + wd);
+  }
+}
+
 int grid_for(int64_t work, int per_block, int cap) {
   int64_t g = (work + per_block - 1) / per_block;
   if (g < 1) g = 1;
@@ -308,6 +352,18 @@ cudaError_t launch_finalize_gather(const float* o, const int32_t* inv, int T, in
   return launch_pdl(finalize_gather_kernel, dim3(grid_for(n4, kThreads, num_sms() * 8)),
                     dim3(kThreads), 0, s, reinterpret_cast<const float4*>(o), inv, T, k, H / 4,
                     shared, reinterpret_cast<uint2*>(y));
+}
+
+cudaError_t launch_permute_rows(const uint8_t* xq, const uint8_t* xsf, int T, int H, int Rt,
+                                int E, const int32_t* perm_src, const int32_t* perm_seg,
+                                const int32_t* offsets, const int32_t* tile_start,
+                                uint8_t* xq_perm, uint8_t* xsf_tiles, int32_t* status,
+                                cudaStream_t s) {
+  const int64_t work = (int64_t)Rt * (H / 32);
+  return launch_pdl(permute_rows_kernel, dim3(grid_for(work, kThreads, num_sms() * 8)),
+                    dim3(kThreads), 0, s, reinterpret_cast<const uint4*>(xq),
+                    reinterpret_cast<const uint32_t*>(xsf), T, H, Rt, E, perm_src, perm_seg,
+                    offsets, tile_start, reinterpret_cast<uint4*>(xq_perm), xsf_tiles, status);
 }
 
 cudaError_t launch_finalize(const float* yacc, void* y, int64_t n, cudaStream_t s) {

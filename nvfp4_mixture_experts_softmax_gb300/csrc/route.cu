@@ -54,12 +54,13 @@ __global__ void __launch_bounds__(kSmallPlanThreads) plan_small_kernel(
     const float* __restrict__ logits, int T, int E, int k, int shared_rows,
     int32_t* __restrict__ ids, float* __restrict__ wout, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ tile_start,
-    int32_t* __restrict__ perm_src, float* __restrict__ perm_w, int32_t* __restrict__ inv) {
+    int32_t* __restrict__ perm_src, float* __restrict__ perm_w, int32_t* __restrict__ inv,
+    int32_t* __restrict__ perm_seg) {
   extern __shared__ __align__(16) uint8_t s_dyn[];
   griddep_wait();
   griddep_launch();
   small_plan_body<VPL>(logits, T, E, k, shared_rows, ids, wout, counts, offsets, tile_start,
-                       perm_src, perm_w, inv, s_dyn);
+                       perm_src, perm_w, inv, s_dyn, perm_seg);
 }
 
 // One block of 1024 threads: per-expert exclusive scan over chunks (base), counts, segment
@@ -120,7 +121,8 @@ __global__ void __launch_bounds__(1024) plan_scan_kernel(const int32_t* __restri
 __global__ void __launch_bounds__(1024) plan_scatter_kernel(
     const int32_t* __restrict__ ids, const float* __restrict__ w, int T, int E, int k, int tpc,
     int shared_rows, const int32_t* __restrict__ base, const int32_t* __restrict__ offsets,
-    int32_t* __restrict__ perm_src, float* __restrict__ perm_w, int32_t* __restrict__ inv) {
+    int32_t* __restrict__ perm_src, float* __restrict__ perm_w, int32_t* __restrict__ inv,
+    int32_t* __restrict__ perm_seg) {
   extern __shared__ int32_t s_wcnt[];  // [nwarps][E]
   griddep_wait();
   griddep_launch();
@@ -143,6 +145,7 @@ __global__ void __launch_bounds__(1024) plan_scatter_kernel(
     const int32_t p = offsets[e] + base[(int64_t)blockIdx.x * E + e] + rank;
     perm_src[p] = (int32_t)(a / k);
     if (perm_w) perm_w[p] = w[a];
+    if (perm_seg) perm_seg[p] = e;
     inv[a] = p;
   }
   if (shared_rows > 0) {  // the shared expert's rows: token t at row R + t, weight 1
@@ -150,6 +153,7 @@ __global__ void __launch_bounds__(1024) plan_scatter_kernel(
     for (int t = t0 + threadIdx.x; t < min(T, t0 + tpc); t += blockDim.x) {
       perm_src[R + t] = t;
       if (perm_w) perm_w[R + t] = 1.0f;
+      if (perm_seg) perm_seg[R + t] = E;
     }
   }
 }
@@ -169,7 +173,7 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s) {
                            (int)smem);                                                          \
     cudaError_t le = launch_pdl(plan_small_kernel<V>, dim3(1), dim3(kSmallPlanThreads), smem, s,  \
         a.logits, a.T, a.E, a.k, a.shared_rows, a.ids, a.w, a.counts, a.offsets, a.tile_start, \
-        a.perm_src, a.perm_w, a.inv);                                                           \
+        a.perm_src, a.perm_w, a.inv, a.perm_seg);                                               \
     if (le != cudaSuccess) return le;                                                           \
   } while (0)
     if (vpl <= 1) NVFP4MOE_SMALL(1);
@@ -214,7 +218,8 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s) {
   }
   return launch_pdl(plan_scatter_kernel, dim3(nchunks), dim3(threads), sc_smem, s,
                     (const int32_t*)a.ids, (const float*)a.w, a.T, a.E, a.k, tpc, a.shared_rows,
-                    (const int32_t*)a.base, (const int32_t*)a.offsets, a.perm_src, a.perm_w, a.inv);
+                    (const int32_t*)a.base, (const int32_t*)a.offsets, a.perm_src, a.perm_w, a.inv,
+                    a.perm_seg);
 }
 
 }  // namespace nvfp4moe

@@ -101,18 +101,20 @@ inline size_t small_plan_smem_bytes(int E) {
          (size_t)(kSmallPlanThreads / 32) * E * sizeof(uint16_t);
 }
 
-// Route T tokens (T*k <= kSmallPlanRows), count per expert, scan, and place every assignment a
-// at offsets[e] + #(earlier assignments to e): assignments are taken 1024 at a time; inside a
-// group, a warp ranks equal experts with match_any and each warp adds the counts of the warps
-// before it; a per-expert cursor carries the counts of earlier groups.  Must be called by all
-// kSmallPlanThreads threads of the block.
-template <int VPL>
-__device__ __forceinline__ void small_plan_body(
-    const float* __restrict__ logits, int T, int E, int k, int shared_rows,
-    int32_t* __restrict__ ids, float* __restrict__ wout, int32_t* __restrict__ counts,
-    int32_t* __restrict__ offsets, int32_t* __restrict__ tile_start,
-    int32_t* __restrict__ perm_src, float* __restrict__ perm_w, int32_t* __restrict__ inv,
-    uint8_t* dyn) {
+// Place the T*k assignments of a small batch (T*k <= kSmallPlanRows) whose expert ids and router
+// weights sit in s_ids / s_w and whose per-expert counts sit in s_cnt: scan the counts into
+// offsets (and 128-row tile starts), then put assignment a at offsets[e] + #(earlier assignments
+// to e).  Assignments are taken 1024 at a time; inside a group a warp ranks equal experts with
+// match_any and each warp adds the counts of the warps before it; a per-expert cursor carries
+// the counts of earlier groups.  Must be called by all kSmallPlanThreads threads of the block;
+// `dyn` is the dynamic shared memory laid out as in small_plan_body.
+__device__ __forceinline__ void small_place(int T, int E, int k, int shared_rows,
+                                            int32_t* __restrict__ counts,
+                                            int32_t* __restrict__ offsets,
+                                            int32_t* __restrict__ tile_start,
+                                            int32_t* __restrict__ perm_src,
+                                            float* __restrict__ perm_w, int32_t* __restrict__ inv,
+                                            uint8_t* dyn, int32_t* __restrict__ perm_seg) {
   int32_t* s_cnt = reinterpret_cast<int32_t*>(dyn);
   int32_t* s_off = s_cnt + E;
   int32_t* s_cur = s_off + E;
@@ -122,25 +124,7 @@ __device__ __forceinline__ void small_plan_body(
   __shared__ int32_t sw[32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int nw = kSmallPlanThreads / 32;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    s_cnt[e] = 0;
-    s_cur[e] = 0;
-  }
-  __syncthreads();
-  for (int t = warp; t < T; t += nw) {
-    int my_id;
-    float my_l;
-    warp_topk<VPL>(logits + (int64_t)t * E, E, k, lane, my_id, my_l);
-    const float w = topk_weight(my_l, k, lane);
-    if (lane < k) {
-      ids[(int64_t)t * k + lane] = my_id;
-      wout[(int64_t)t * k + lane] = w;
-      s_ids[t * k + lane] = my_id;
-      s_w[t * k + lane] = w;
-      atomicAdd(&s_cnt[my_id], 1);
-    }
-  }
-  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cur[e] = 0;
   const int e = threadIdx.x;
   const int32_t cnt = e < E ? s_cnt[e] : 0;
   int32_t total, ttotal;
@@ -177,6 +161,7 @@ __device__ __forceinline__ void small_plan_body(
       const int p = s_off[ea] + rank;
       perm_src[p] = a / k;
       if (perm_w) perm_w[p] = s_w[a];
+      if (perm_seg) perm_seg[p] = ea;
       inv[a] = p;
     }
     __syncthreads();
@@ -190,7 +175,41 @@ __device__ __forceinline__ void small_plan_body(
   for (int t = threadIdx.x; t < shared_rows; t += blockDim.x) {
     perm_src[R + t] = t;
     if (perm_w) perm_w[R + t] = 1.0f;
+    if (perm_seg) perm_seg[R + t] = E;
   }
+}
+
+// Route T tokens (T*k <= kSmallPlanRows) inside one block, count per expert, then place (above).
+template <int VPL>
+__device__ __forceinline__ void small_plan_body(
+    const float* __restrict__ logits, int T, int E, int k, int shared_rows,
+    int32_t* __restrict__ ids, float* __restrict__ wout, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ tile_start,
+    int32_t* __restrict__ perm_src, float* __restrict__ perm_w, int32_t* __restrict__ inv,
+    uint8_t* dyn, int32_t* __restrict__ perm_seg = nullptr) {
+  int32_t* s_cnt = reinterpret_cast<int32_t*>(dyn);
+  int32_t* s_ids = s_cnt + 3 * E;
+  float* s_w = reinterpret_cast<float*>(s_ids + kSmallPlanRows);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int nw = kSmallPlanThreads / 32;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+  __syncthreads();
+  for (int t = warp; t < T; t += nw) {
+    int my_id;
+    float my_l;
+    warp_topk<VPL>(logits + (int64_t)t * E, E, k, lane, my_id, my_l);
+    const float w = topk_weight(my_l, k, lane);
+    if (lane < k) {
+      ids[(int64_t)t * k + lane] = my_id;
+      wout[(int64_t)t * k + lane] = w;
+      s_ids[t * k + lane] = my_id;
+      s_w[t * k + lane] = w;
+      atomicAdd(&s_cnt[my_id], 1);
+    }
+  }
+  __syncthreads();
+  small_place(T, E, k, shared_rows, counts, offsets, tile_start, perm_src, perm_w, inv, dyn,
+              perm_seg);
 }
 
 }  // namespace nvfp4moe
