@@ -32,7 +32,7 @@ import torch  # noqa: E402
 
 METRIC = "NVFP4 MoE tokens/s & eff. TFLOPS; % of HBM BW (decode) / FP4 peak (prefill)"
 UNIT = "tokens/s"
-KERNELS_PER_CALL = 8   # act amax, act encode, router, plan scan, plan scatter, GEMM1, GEMM2, bf16 out
+FP4_PER_BF16 = 6.0     # nominal dense FP4 / BF16 tensor rate of the part (13.5 / 2.25 PFLOP/s)
 
 
 def parse():
@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--workload", default="decode",
                     choices=["decode", "tiny", "prefill", "large", "skewed"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", default=None,
+                    help="comma-separated batch sizes replacing the workload's own list")
     ap.add_argument("--ref-budget-s", type=float, default=150.0,
                     help="wall-time budget of the reference arm's timed + warm-up steps")
     return ap.parse_args()
@@ -134,10 +136,11 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------------------- helpers
-def workload(name):
+def workload(name, tokens=None):
     import synth
     cs = synth.CONFIGS[name]
-    return cs, list(cs.tokens)
+    Ts = [int(t) for t in tokens.split(",")] if tokens else list(cs.tokens)
+    return cs, Ts
 
 
 def expert_bytes(cs):
@@ -158,6 +161,8 @@ def layer_counters(cs, T, touched, has_shared):
     out = T * H * 2
     return dict(
         flops=rows * 6 * H * I,
+        gemm1_swiglu_flops=rows * 4 * H * I,
+        gemm2_combine_flops=rows * 2 * H * I,
         layer_bytes=w13 + w2 + act_in + out,
         # GEMM1: gate/up weights + gathered activation codes/scales + requantised h out
         gemm1_swiglu=w13 + rows * H * 9 // 16 + rows * I * 9 // 16,
@@ -232,7 +237,7 @@ def run_ours(args, world, rank, local):
 
     _build.build()
     dev = torch.device("cuda", local)
-    cs, Ts = workload(args.workload)
+    cs, Ts = workload(args.workload, args.tokens)
     has_shared = cs.has_shared
     Tmax = max(Ts)
     cfg = moe.make_config(cs.experts, cs.hidden, cs.inter, cs.top_k, shared_inter=cs.shared_inter,
@@ -251,6 +256,7 @@ def run_ours(args, world, rank, local):
         out = moe.plan(lgs[T], cs.top_k)
         touched[T] = int((out["counts"] > 0).sum().item())
     counters = {T: layer_counters(cs, T, touched[T], has_shared) for T in Ts}
+    launches = {T: moe.run_kernel_count(cfg, T) for T in Ts}
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
@@ -353,10 +359,27 @@ def run_ours(args, world, rank, local):
     hbm_peak, bf16_peak, peak_src = measured_peaks()
     tot = {key: sum(counters[T][key] for T in Tseq) for key in counters[Ts[0]]}
     dominant = max(stage_ms, key=stage_ms.get)
-    # roofline of the dominant kernel on the launches of the largest batch of the workload
+    # roofline of the dominant kernel on the launches of the largest batch of the workload: the
+    # weight-streaming decode batches against HBM bandwidth, the large batches' GEMMs against the
+    # dense FP4 tensor peak (measured BF16 peak x the nominal FP4/BF16 ratio)
     Tr = max(Ts)
     dom_launch_s = statistics.mean(stage_ms_T[Tr][dominant]) / 1e3
-    achieved = counters[Tr][dominant] / dom_launch_s / 1e9
+    tensor_bound = Tr > 64 and dominant in ("gemm1_swiglu", "gemm2_combine")
+    if tensor_bound:
+        fp4_peak = bf16_peak * FP4_PER_BF16
+        achieved = counters[Tr][dominant + "_flops"] / dom_launch_s / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp4_peak, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / fp4_peak, 4),
+                "algorithmic_flops_per_launch": counters[Tr][dominant + "_flops"],
+                "peak_source": (f"{peak_src} bf16 {bf16_peak} TFLOP/s x {FP4_PER_BF16} nominal "
+                                f"FP4/BF16 ratio")}
+    else:
+        achieved = counters[Tr][dominant] / dom_launch_s / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(achieved / hbm_peak, 4),
+                "algorithmic_bytes_per_launch": counters[Tr][dominant],
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                else "fallback"}
     traffic = measured_traffic(f"{dominant}@{args.workload}_T{Tr}")
     eff_tflops = tot["flops"] / dev_s / 1e12
     layer_gbs = tot["layer_bytes"] / dev_s / 1e9
@@ -430,18 +453,14 @@ def run_ours(args, world, rank, local):
         "per_T_us": {str(T): round(statistics.median(v) * 1e3, 2) for T, v in per_T_ms.items()},
         "touched_experts": {str(T): touched[T] for T in Ts},
         "stage_share": {n: round(v / sum(stage_ms.values()), 4) for n, v in stage_ms.items()},
-        "roofline": {"kernel": f"{dominant} (T={Tr} launches)", "bound": "hbm",
-                     "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(achieved / hbm_peak, 4),
-                     "algorithmic_bytes_per_launch": counters[Tr][dominant],
-                     "avg_launch_us": round(dom_launch_s * 1e6, 2),
-                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
-                     else "fallback", "traffic": traffic},
+        "fp4_peak_frac": round(eff_tflops / (bf16_peak * FP4_PER_BF16), 4),
+        "roofline": dict(kernel=f"{dominant} (T={Tr} launches)", **roof,
+                         avg_launch_us=round(dom_launch_s * 1e6, 2), traffic=traffic),
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d // max(len(e_ms), 1),
                 "d2h_bytes_per_step": d2h // max(len(e_ms), 1)},
-        "gpu_launches": KERNELS_PER_CALL * args.steps,
+        "gpu_launches": sum(launches[T] for T in Tseq),
         "clocks": clocks,
         "wall_s_timed_region": round(w1 - w0, 4),
     }
@@ -454,7 +473,7 @@ def run_reference(args, world, rank, local):
         return
     import numpy as np
     import synth
-    cs, Ts = workload(args.workload)
+    cs, Ts = workload(args.workload, args.tokens)
     dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
     wg, wu, wd = synth.gen_all_experts(cs, device=dev)
     sh = synth.gen_shared(cs, device=dev) if cs.has_shared else None

@@ -172,6 +172,14 @@ int moe_plan_static(const float* logits, int32_t T, int32_t E, int32_t k, int32_
  * struct of device buffers that receive the intermediates.
  * ------------------------------------------------------------------------------------------- */
 size_t moe_workspace_size(const moe_config* cfg, int32_t T);
+
+/* Number of kernels one moe_run(cfg, ..., T, ...) launches (memset nodes not counted), or a
+ * negative moe_status for an invalid cfg / T.  Host-only arithmetic: no CUDA call, no device.
+ * It mirrors moe_run's choice of path: 4 for decode-sized batches (cluster prologue, GEMM1,
+ * GEMM2, row sum), 5 for other small batches, 7 or 9 for large ones (the router and plan take one
+ * kernel up to 2048 routed rows, three above).  A utility for launch accounting; the pages have
+ * no counterpart. */
+int moe_run_kernel_count(const moe_config* cfg, int32_t T);
 int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float* logits, int32_t T,
             int32_t k, void* y, void* workspace, size_t ws_bytes, moe_stream_t stream,
             const moe_debug* debug);

@@ -23,7 +23,7 @@ STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED_SHAPE
 EXPORTED = ["moe_status_string", "moe_config_check", "moe_weights_size", "moe_quantize_weights",
             "moe_weights_export", "moe_act_workspace_size", "moe_quantize_act",
             "moe_plan_workspace_size", "moe_plan", "moe_workspace_size", "moe_run",
-            "moe_last_device_status", "moe_plan_static"]
+            "moe_last_device_status", "moe_plan_static", "moe_run_kernel_count"]
 
 
 class MoeConfig(C.Structure):
@@ -73,6 +73,7 @@ def lib():
             "moe_run": (C.c_int, [cfgp, vp, vp, vp, i32, i32, vp, vp, sz, vp, C.POINTER(MoeDebug)]),
             "moe_last_device_status": (C.c_int, [vp, C.POINTER(C.c_int32)]),
             "moe_plan_static": (C.c_int, [vp, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]),
+            "moe_run_kernel_count": (C.c_int, [cfgp, i32]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -196,6 +197,14 @@ def plan_static(logits, k: int, out=None, stream=None):
 
 def workspace_size(cfg: MoeConfig, T: int) -> int:
     return int(lib().moe_workspace_size(C.byref(cfg), T))
+
+
+def run_kernel_count(cfg: MoeConfig, T: int) -> int:
+    """Kernels one run() at T tokens launches (host arithmetic, no device needed)."""
+    n = int(lib().moe_run_kernel_count(C.byref(cfg), T))
+    if n < 0:
+        raise RuntimeError(f"moe_run_kernel_count: {status_string(n)}")
+    return n
 
 
 class StageTimer:

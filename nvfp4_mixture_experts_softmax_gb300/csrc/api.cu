@@ -167,6 +167,18 @@ size_t moe_workspace_size(const moe_config* cfg, int32_t T) {
   return RunLayout(*cfg, T).total;
 }
 
+int moe_run_kernel_count(const moe_config* cfg, int32_t T) {
+  const int st = check_cfg(cfg);
+  if (st != MOE_OK) return st;
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return 0;
+  const RunLayout L(*cfg, T);
+  if (L.decode) return 4;     // cluster prologue, GEMM1, GEMM2, row sum
+  if (L.small) return 5;      // one-block prologue, permute, GEMM1, GEMM2, row sum
+  // amax + encode, router/plan (1 or 3), permute, GEMM1, GEMM2, BF16 conversion
+  return 2 + ((int64_t)T * cfg->top_k <= kSmallPlanRows ? 1 : 3) + 4;
+}
+
 int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float* logits, int32_t T,
             int32_t k, void* y, void* workspace, size_t ws_bytes, moe_stream_t stream,
             const moe_debug* debug) {

@@ -18,8 +18,9 @@
 // here the schedule is a static round robin over the device-built tile list):
 //   warps 0-3  epilogue: tensor memory -> registers -> global, one accumulator row per thread;
 //   warp  4    copy issue; warp 5 tensor-memory allocation and the single MMA-issuing thread.
-// A 6-stage shared-memory ring (mbarrier full/empty pairs) feeds the MMA; two 128-column FP32
-// accumulators let the epilogue of one tile overlap the main loop of the next.  Every wait is
+// A 6-stage shared-memory ring (5 stages for the reducing epilogue, whose transpose buffers take
+// the rest) of mbarrier full/empty pairs feeds the MMA; two 128-column FP32 accumulators let the
+// epilogue of one tile overlap the main loop of the next.  Every wait is
 // bounded in time and reports MOE_ERR_DEVICE_TIMEOUT instead of hanging.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -31,7 +32,6 @@ namespace nvfp4moe {
 
 namespace {
 
-constexpr int kStages = 6;
 constexpr int kEpiWarps = 4;
 constexpr int kTmaWarp = 4;
 constexpr int kMmaWarp = 5;
@@ -49,9 +49,26 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 static_assert(kBN == 128 && kTileBlockBytes == kBN * 128 + kSfBytes, "packed block = B stage");
 static_assert(kBOff % 1024 == 0, "B tile stays 1024-byte aligned for the 128B swizzle");
-static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "tensor memory budget");
 static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
-static_assert(kStages * kStageBytes + 1024 + 256 + 8 * 1027 <= 232448, "shared memory");
+
+// The reducing epilogue (mode 1) transposes each warp's 32 x 32 FP32 chunk through shared memory
+// so that one vector reduction instruction covers four rows x 128 contiguous bytes (eight lanes per
+// row) instead of 32 scattered 16-byte pieces: a quarter of the L2 requests, full sectors each.
+// 16-byte unit q of row r sits at r * 128 + ((q ^ (r & 7)) * 16), which keeps both the row-wise
+// stores and the column-wise loads free of bank conflicts.
+constexpr int kStgBufBytes = 32 * 128;
+constexpr int kStgBytes = kEpiWarps * kStgBufBytes;
+
+// Ring depth: 6 stages for the SwiGLU / row-store epilogues, 5 when the reduction staging takes
+// its share of shared memory.
+template <bool kRedStage>
+struct GemmShape {
+  static constexpr int kStages = kRedStage ? 5 : 6;
+  static constexpr int kStgOff = kStages * kStageBytes;
+  static constexpr int kBarOff = kStgOff + (kRedStage ? kStgBytes : 0);
+  static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "tensor memory budget");
+  static_assert(kBarOff + 1024 + 256 + 8 * 1027 <= 232448, "shared memory");
+};
 
 // Instruction descriptor of tcgen05.mma kind::mxf4nvf4: A and B E2M1 (format 1) at bits 7-9 and
 // 10-12, both K-major, N >> 3 at bits 17-22, UE4M3 scale type (bit 23 = 0), M >> 4 at bits 24-28,
@@ -87,19 +104,21 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
   return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
+template <bool kRedStage>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmArgs p) {
+  constexpr int kStages = GemmShape<kRedStage>::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + GemmShape<kRedStage>::kBarOff);
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* acc_full = bars + 2 * kStages;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  int32_t* s_tile = reinterpret_cast<int32_t*>(smem + kStages * kStageBytes + 256);
+  int32_t* s_tile = reinterpret_cast<int32_t*>(smem + GemmShape<kRedStage>::kBarOff + 256);
   int32_t* s_seg = s_tile + (p.nseg + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -288,7 +307,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t v[32];
           tmem_ld_32x32b_x32(tbase + c * 32, v);
           tmem_ld_wait();
-          if (ok_row) {
+          if constexpr (kRedStage) {
+            const uint32_t stg = smem0 + GemmShape<kRedStage>::kStgOff + (uint32_t)warp * kStgBufBytes;
+            const uint32_t wrow = stg + (uint32_t)lane * 128;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 d = make_float4((__uint_as_float(v[4 * i]) * alpha) * wr,
+                                           (__uint_as_float(v[4 * i + 1]) * alpha) * wr,
+                                           (__uint_as_float(v[4 * i + 2]) * alpha) * wr,
+                                           (__uint_as_float(v[4 * i + 3]) * alpha) * wr);
+              asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(
+                               wrow + (uint32_t)((i ^ (lane & 7)) * 16)),
+                           "f"(d.x), "f"(d.y), "f"(d.z), "f"(d.w)
+                           : "memory");
+            }
+            __syncwarp();
+            // lane l adds 16 bytes (unit l % 8) of row 4 * j + l / 8
+            const int q = lane & 7;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int rj = 4 * j + (lane >> 3);
+              const int ok_j = __shfl_sync(0xffffffffu, (int)ok_row, rj);
+              const int tok_j = __shfl_sync(0xffffffffu, tok, rj);
+              float4 d;
+              asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                           : "=f"(d.x), "=f"(d.y), "=f"(d.z), "=f"(d.w)
+                           : "r"(stg + (uint32_t)rj * 128 + (uint32_t)((q ^ (rj & 7)) * 16)));
+              if (ok_j)
+                red_add_v4(p.yacc + (size_t)tok_j * p.N + t.nt * kBN + c * 32 + 4 * q, d.x, d.y,
+                           d.z, d.w);
+            }
+            __syncwarp();
+          } else if (ok_row) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const float4 d = make_float4((__uint_as_float(v[4 * i]) * alpha) * wr,
@@ -315,8 +365,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+template <bool kRedStage>
 size_t gemm_smem_bytes(int nseg) {
-  return 1024 + (size_t)kStages * kStageBytes + 256 + sizeof(int32_t) * 2 * (nseg + 2);
+  return 1024 + (size_t)GemmShape<kRedStage>::kBarOff + 256 + sizeof(int32_t) * 2 * (nseg + 2);
+}
+
+template <bool kRedStage>
+cudaError_t launch_kernel(const CUtensorMap& tmap, const GemmArgs& a, cudaStream_t s) {
+  const size_t smem = gemm_smem_bytes<kRedStage>(a.nseg);
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<kRedStage>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int grid = a.max_ctas;
+  if (grid > num_sms()) grid = num_sms();
+  if (grid < 1) grid = 1;
+  return launch_pdl(grouped_gemm_kernel<kRedStage>, dim3(grid), dim3(kThreads), smem, s, tmap, a);
 }
 
 }  // namespace
@@ -347,14 +410,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s) {
              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  const size_t smem = gemm_smem_bytes(a.nseg);
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  int grid = a.max_ctas;
-  if (grid > num_sms()) grid = num_sms();
-  if (grid < 1) grid = 1;
-  return launch_pdl(grouped_gemm_kernel, dim3(grid), dim3(kThreads), smem, s, tmap, a);
+  return a.mode == 1 ? launch_kernel<true>(tmap, a, s) : launch_kernel<false>(tmap, a, s);
 }
 
 }  // namespace nvfp4moe

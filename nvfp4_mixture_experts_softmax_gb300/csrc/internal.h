@@ -19,6 +19,7 @@ constexpr int kBN = 128;       // output columns per tile (MMA N)
 constexpr int kBK = 256;       // FP4 elements of K per pipeline stage (128 bytes per row)
 constexpr int kMmaK = 64;      // K of one block-scaled FP4 MMA
 constexpr int kDecodeMaxRows = 64;   // batches up to this many tokens take the decode path
+constexpr int kSmallPlanRows = 2048; // T*k routed by the one-block plan
 
 // Router chunking: tokens per chunk (one router block and one scatter block each).
 inline int plan_tokens_per_chunk(int k) { return k <= 16 ? 64 : 32; }

@@ -8,7 +8,6 @@
 namespace nvfp4moe {
 
 constexpr int kMaxVpl = 32;             // experts per lane: E <= 1024
-constexpr int kSmallPlanRows = 2048;    // T*k handled by the one-block plan
 constexpr int kSmallPlanThreads = 1024;
 
 // Exclusive scan of one value per thread over the block (blockDim.x <= 1024).

@@ -87,3 +87,20 @@ def test_host_side_rejections(moe):
     assert L.moe_last_device_status(None, C.byref(st)) == -1
     assert L.moe_plan_static(None, 4, 8, 9, None, None, None, None, None, None, None) == -1
     assert L.moe_plan_static(None, 1 << 24, 1024, 8, None, None, None, None, None, None, None) == -3
+
+
+def test_run_kernel_count(moe):
+    """The launch count follows moe_run's path choice: decode-sized batches take four kernels,
+    other small batches five, large ones seven (one-kernel plan) or nine (three-kernel plan)."""
+    dec = moe.make_config(128, 2048, 768, 8, max_tokens=8192)
+    assert [moe.run_kernel_count(dec, T) for T in (1, 8, 32, 64)] == [4, 4, 4, 4]
+    assert moe.run_kernel_count(dec, 0) == 0
+    assert moe.run_kernel_count(dec, 8192) == 9
+    mid = moe.make_config(16, 2048, 256, 4, max_tokens=1024)
+    assert moe.run_kernel_count(mid, 100) == 5     # fits the one-block prologue
+    assert moe.run_kernel_count(mid, 500) == 7     # 2000 routed rows: one-kernel plan
+    assert moe.run_kernel_count(mid, 600) == 9     # 2400 routed rows: three-kernel plan
+    with pytest.raises(RuntimeError):
+        moe.run_kernel_count(dec, -1)
+    with pytest.raises(RuntimeError):
+        moe.run_kernel_count(moe.make_config(8, 200, 512, 2), 4)
