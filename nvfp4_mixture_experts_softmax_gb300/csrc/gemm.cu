@@ -17,7 +17,10 @@
 // SM, warp-specialised (the pages' design uses TMA / MMA / epilogue warps and a scheduler warp;
 // here the schedule is a static round robin over the device-built tile list):
 //   warps 0-3  epilogue: tensor memory -> registers -> global, one accumulator row per thread;
-//   warp  4    copy issue; warp 5 tensor-memory allocation and the single MMA-issuing thread.
+//   warp  4    copy issue; warp 5 tensor-memory allocation and the single MMA-issuing thread;
+//   warp  6    the eight shared -> tensor memory scale-factor copies of each stage, one stage
+//              ahead of the MMA thread (issued from the MMA thread they stall it for long
+//              enough to starve the tensor core).
 // A 6-stage shared-memory ring (5 stages for the reducing epilogue, whose transpose buffers take
 // the rest) of mbarrier full/empty pairs feeds the MMA; two 128-column FP32 accumulators let the
 // epilogue of one tile overlap the main loop of the next.  Every wait is
@@ -35,7 +38,8 @@ namespace {
 constexpr int kEpiWarps = 4;
 constexpr int kTmaWarp = 4;
 constexpr int kMmaWarp = 5;
-constexpr int kThreads = (kMmaWarp + 1) * 32;
+constexpr int kSfWarp = 6;
+constexpr int kThreads = (kSfWarp + 1) * 32;
 // Stage layout: A codes | A scales | B block (codes + scales, one packed weight block).
 constexpr int kABytes = kBM * 128;
 constexpr int kSfBytes = 4 * 512;  // four 512-byte scale groups (one per 64-wide MMA K step)
@@ -117,7 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_full = bars + 2 * kStages;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* sf_done = drain + 1;   // a stage's scale factors are in tensor memory
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_done + kStages);
   int32_t* s_tile = reinterpret_cast<int32_t*>(smem + GemmShape<kRedStage>::kBarOff + 256);
   int32_t* s_seg = s_tile + (p.nseg + 1);
 
@@ -136,6 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(acc_empty + b), kEpiWarps);
     }
     mbar_init(smem_u32(drain), 1);
+    for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(sf_done + s), 1);
     fence_barrier_init();
   }
   if (warp == kTmaWarp && lane == 0)
@@ -200,6 +206,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t acc_phase[2] = {0u, 0u};
+      // stage 0's operand descriptors; a stage (or a K step) further is an addition to the
+      // 14-bit address field, which never carries (shared addresses stay below 256 KB)
+      const uint64_t dA0 = smem_desc(smem0, 16, 1024, kLayoutSwizzle128B);
+      const uint64_t dB0 = smem_desc(smem0 + kBOff, 16, 1024, kLayoutSwizzle128B);
       bool ok = true;
       int it = 0;
       for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++it) {
@@ -213,28 +223,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + abuf * kAccCols;
         for (int ks = 0; ks < kst; ++ks) {
-          if (!mbar_wait_bounded(smem_u32(full + stage), phase, kWaitLimitNs, p.status)) {
+          if (!mbar_wait_bounded(smem_u32(sf_done + stage), phase, kWaitLimitNs, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sb = smem0 + stage * kStageBytes;
-          const uint32_t sfa_s = sb + kABytes;
-          const uint32_t sfb_s = sb + kBOff + kTileBytes;
+          const uint64_t so = (uint64_t)((uint32_t)(stage * kStageBytes) >> 4);
           const uint32_t sf_t = tmem_base + kSfCol0 + stage * kSfColsPerStage;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            tc_cp_32x128b_warpx4(sf_t + kk * 4, smem_desc(sfa_s + kk * 512, 0, 128, kLayoutSwizzleNone));
-            tc_cp_32x128b_warpx4(sf_t + 16 + kk * 4,
-                                 smem_desc(sfb_s + kk * 512, 0, 128, kLayoutSwizzleNone));
-          }
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = smem_desc(sb + kk * 32, 16, 1024, kLayoutSwizzle128B);
-            const uint64_t bd = smem_desc(sb + kBOff + kk * 32, 16, 1024, kLayoutSwizzle128B);
-            tc_mma_mxf4nvf4(d_tmem, ad, bd, idesc, sf_t + kk * 4, sf_t + 16 + kk * 4,
-                            (ks | kk) != 0 ? 1u : 0u);
-          }
+          for (int kk = 0; kk < 4; ++kk)   // K = 64 per MMA: 32 bytes -> 2 descriptor units
+            tc_mma_mxf4nvf4(d_tmem, dA0 + so + kk * 2, dB0 + so + kk * 2, idesc, sf_t + kk * 4,
+                            sf_t + 16 + kk * 4, (ks | kk) != 0 ? 1u : 0u);
           tc_commit(smem_u32(empty + stage));
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
@@ -243,6 +242,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       // make sure no tensor-core operation is still running before tensor memory is released
       tc_commit(smem_u32(drain));
       mbar_wait_bounded(smem_u32(drain), 0u, kWaitLimitNs, p.status);
+    }
+  } else if (warp == kSfWarp) {
+    // ---------------- scale factors: shared -> tensor memory, ahead of the MMA thread ---------
+    // A stage's scale columns are rewritten only after the copy engine refilled the stage, which
+    // waited for the MMAs of its previous use to complete.
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      const uint64_t dSa0 = smem_desc(smem0 + kABytes, 0, 128, kLayoutSwizzleNone);
+      const uint64_t dSb0 = smem_desc(smem0 + kBOff + kTileBytes, 0, 128, kLayoutSwizzleNone);
+      bool ok = true;
+      for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+        for (int ks = 0; ks < kst; ++ks) {
+          if (!mbar_wait_bounded(smem_u32(full + stage), phase, kWaitLimitNs, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t so = (uint64_t)((uint32_t)(stage * kStageBytes) >> 4);
+          const uint32_t sf_t = tmem_base + kSfCol0 + stage * kSfColsPerStage;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {   // one 512-byte scale group per K = 64
+            tc_cp_32x128b_warpx4(sf_t + kk * 4, dSa0 + so + kk * 32);
+            tc_cp_32x128b_warpx4(sf_t + 16 + kk * 4, dSb0 + so + kk * 32);
+          }
+          tc_commit(smem_u32(sf_done + stage));
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
     }
   } else {
     // ---------------- epilogue (warps 0-3) ----------------

@@ -13,9 +13,13 @@
 // 2-D TMA tile (128-byte swizzle) of the expert's token rows - the activations (GEMM1) or h
 // (GEMM2) are stored in expert order, so an expert's rows are contiguous - and one bulk copy of
 // the tokens' scales, which the producer kernels write pre-arranged per expert tile.  Warps:
-// 0-3 epilogue, 4 copy issue, 5 MMA ("nvfp4-megamoe-kernel compare pre-b1...master", section
-// "MoE kernel": TMA, MMA and epilogue warps; the pages keep decode on 1-CTA tiles).  Four TMEM
-// accumulators let the epilogue trail the main loop by up to three tiles.
+// 0-3 epilogue, 4 copy issue, 5 MMA, 6 scale factors ("nvfp4-megamoe-kernel compare
+// pre-b1...master", section "MoE kernel": TMA, MMA and epilogue warps; the pages keep decode on
+// 1-CTA tiles).  The eight shared -> tensor memory scale copies of a stage hold up the thread that
+// issues them for a long time, so a warp of their own issues them one stage ahead of the MMA
+// thread and signals it through an mbarrier; the MMA thread then issues only the four MMAs of a
+// stage, with descriptors advanced by additions.  Three TMEM accumulators let the epilogue trail
+// the main loop by up to two tiles.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -32,7 +36,8 @@ constexpr int kXBoxRows = 16;                          // token rows per TMA box
 constexpr int kEpiWarps = 4;
 constexpr int kTmaWarp = 4;
 constexpr int kMmaWarp = 5;
-constexpr int kThreads = (kMmaWarp + 1) * 32;
+constexpr int kSfWarp = 6;
+constexpr int kThreads = (kSfWarp + 1) * 32;
 constexpr int kNmax = kDecodeMaxRows;                 // token rows per expert tile
 constexpr int kXOff = kTileBlockBytes;                 // token codes after the weight block
 constexpr int kXBytes = kNmax * 128;
@@ -95,7 +100,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_full = bars + 2 * kStages;
   uint64_t* acc_empty = acc_full + kAccBufs;
   uint64_t* drain = acc_empty + kAccBufs;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* sf_done = drain + 1;   // a stage's scale factors are in tensor memory
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_done + kStages);
   int32_t* s_tile = reinterpret_cast<int32_t*>(smem + kStages * kStageBytes + 256);
   int32_t* s_seg = s_tile + (p.nseg + 1);
 
@@ -114,6 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(acc_empty + b), kEpiWarps);
     }
     mbar_init(smem_u32(drain), 1);
+    for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(sf_done + s), 1);
     fence_barrier_init();
   }
   if (warp == kTmaWarp && lane == 0)
@@ -179,6 +186,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t acc_phase[kAccBufs] = {};
+      // stage 0's operand descriptors; a stage (or a K step) further is an addition to the
+      // 14-bit address field, which never carries (shared addresses stay below 256 KB)
+      const uint64_t dA0 = smem_desc(smem0, 16, 1024, kLayoutSwizzle128B);
+      const uint64_t dB0 = smem_desc(smem0 + kXOff, 16, 1024, kLayoutSwizzle128B);
       bool ok = true;
       int it = 0;
       for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++it) {
@@ -195,28 +206,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + abuf * kAccCols;
         for (int ks = 0; ks < kst; ++ks) {
-          if (!mbar_wait_bounded(smem_u32(full + stage), phase, kWaitLimitNs, p.status)) {
+          if (!mbar_wait_bounded(smem_u32(sf_done + stage), phase, kWaitLimitNs, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sb = smem0 + stage * kStageBytes;
-          const uint32_t sfw_s = sb + kTileBytes;
-          const uint32_t sfx_s = sb + kXSfOff;
+          const uint64_t so = (uint64_t)((uint32_t)(stage * kStageBytes) >> 4);
           const uint32_t sf_t = tmem_base + kSfCol0 + stage * kSfColsPerStage;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            tc_cp_32x128b_warpx4(sf_t + kk * 4, smem_desc(sfw_s + kk * 512, 0, 128, kLayoutSwizzleNone));
-            tc_cp_32x128b_warpx4(sf_t + 16 + kk * 4,
-                                 smem_desc(sfx_s + kk * 512, 0, 128, kLayoutSwizzleNone));
-          }
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = smem_desc(sb + kk * 32, 16, 1024, kLayoutSwizzle128B);
-            const uint64_t bd = smem_desc(sb + kXOff + kk * 32, 16, 1024, kLayoutSwizzle128B);
-            tc_mma_mxf4nvf4(d_tmem, ad, bd, idesc, sf_t + kk * 4, sf_t + 16 + kk * 4,
-                            (ks | kk) != 0 ? 1u : 0u);
-          }
+          for (int kk = 0; kk < 4; ++kk)   // K = 64 per MMA: 32 bytes -> 2 descriptor units
+            tc_mma_mxf4nvf4(d_tmem, dA0 + so + kk * 2, dB0 + so + kk * 2, idesc, sf_t + kk * 4,
+                            sf_t + 16 + kk * 4, (ks | kk) != 0 ? 1u : 0u);
           tc_commit(smem_u32(empty + stage));
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
@@ -224,6 +224,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_commit(smem_u32(drain));
       mbar_wait_bounded(smem_u32(drain), 0u, kWaitLimitNs, p.status);
+    }
+  } else if (warp == kSfWarp) {
+    // ---------------- scale factors: shared -> tensor memory, ahead of the MMA thread ---------
+    // A stage's scale columns are rewritten only after the copy engine refilled the stage, which
+    // waited for the MMAs of its previous use to complete.
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      const uint64_t dSw0 = smem_desc(smem0 + kTileBytes, 0, 128, kLayoutSwizzleNone);
+      const uint64_t dSx0 = smem_desc(smem0 + kXSfOff, 0, 128, kLayoutSwizzleNone);
+      bool ok = true;
+      for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+        for (int ks = 0; ks < kst; ++ks) {
+          if (!mbar_wait_bounded(smem_u32(full + stage), phase, kWaitLimitNs, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t so = (uint64_t)((uint32_t)(stage * kStageBytes) >> 4);
+          const uint32_t sf_t = tmem_base + kSfCol0 + stage * kSfColsPerStage;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {   // one 512-byte scale group per K = 64
+            tc_cp_32x128b_warpx4(sf_t + kk * 4, dSw0 + so + kk * 32);
+            tc_cp_32x128b_warpx4(sf_t + 16 + kk * 4, dSx0 + so + kk * 32);
+          }
+          tc_commit(smem_u32(sf_done + stage));
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
     }
   } else {
     // ---------------- epilogue (warps 0-3): lane = weight row, column = token ----------------
