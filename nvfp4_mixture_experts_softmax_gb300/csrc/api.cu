@@ -367,6 +367,7 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
   g2.N = H;
   g2.K = I;
   g2.mode = L.small ? 2 : 1;
+  g2.plan_early = decode ? 1 : 0;   // GEMM1 waited for the decode prologue before releasing GEMM2
   g2.perm_src = i32(L.perm_src);
   g2.perm_w = f32(L.perm_w);
   g2.yacc = f32(L.yacc);

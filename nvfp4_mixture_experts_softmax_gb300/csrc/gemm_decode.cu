@@ -53,6 +53,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "tensor memory budget");
 static_assert(kStageBytes % 1024 == 0 && kXOff % 1024 == 0, "1024-byte aligned swizzled tiles");
 static_assert(kStages * kStageBytes + 1024 + 256 + 8 * 1027 <= 232448, "shared memory");
+static_assert((3 * kStages + 2 * kAccBufs + 1) * 8 + 4 <= 256, "mbarriers + TMEM slot fit 256 B");
 static_assert(kNmax % kXBoxRows == 0 && kNmax <= 64, "token tile");
 
 constexpr uint32_t make_idesc(int M, int N) {
@@ -125,11 +126,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == kTmaWarp && lane == 0)
     asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_x) : "memory");
-  griddep_wait();
+  // plan_early: the plan was written two kernels back and is complete (the kernel in between
+  // waited for it before it let this one start), so only the copy issuer waits, and only before
+  // its first load of the previous kernel's output; the weights of the first stages are in
+  // flight by then
+  if (!p.plan_early) griddep_wait();
   griddep_launch();
   for (int i = threadIdx.x; i <= p.nseg; i += blockDim.x) {
-    s_tile[i] = p.tile_start[i];
-    s_seg[i] = p.seg_off[i];
+    s_tile[i] = __ldcg(p.tile_start + i);
+    s_seg[i] = __ldcg(p.seg_off + i);
   }
   tc_fence_before();
   __syncthreads();
@@ -151,23 +156,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
+      // only the boxes that hold the expert's rows (16 rows each); the rest of the token tile
+      // stays stale and only feeds accumulator columns that are never stored
+      auto stage_bytes = [&](const TileInfo& t) {
+        return (uint32_t)(kTileBlockBytes + ((max(t.rows, 1) + kXBoxRows - 1) / kXBoxRows) *
+                                                kXBoxRows * 128 + kXSfBytes);
+      };
+      // weight blocks of the first stages (the ring is empty: no wait), before the wait for
+      // the previous kernel's output
+      int pre = 0;
+      if (p.plan_early) {
+        for (int item = blockIdx.x; item < total && pre < kStages; item += gridDim.x) {
+          const TileInfo t = decode_item(item, n_tiles, s_tile, s_seg, p.nseg);
+          const uint8_t* src = p.b_tiles + (size_t)t.seg * p.b_per_seg +
+                               (size_t)t.nt * kst * kTileBlockBytes;
+          for (int ks = 0; ks < kst && pre < kStages; ++ks, ++pre) {
+            const uint32_t fb = smem_u32(full + pre);
+            mbar_arrive_expect_tx(fb, stage_bytes(t));
+            bulk_load(smem0 + pre * kStageBytes, src + (size_t)ks * kTileBlockBytes,
+                      kTileBlockBytes, fb);
+          }
+        }
+        griddep_wait();
+      }
+      int g = 0;   // stages issued so far
       for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
         const TileInfo t = decode_item(item, n_tiles, s_tile, s_seg, p.nseg);
         const uint8_t* src = p.b_tiles + (size_t)t.seg * p.b_per_seg +
                              (size_t)t.nt * kst * kTileBlockBytes;
         const uint8_t* xsf = p.a_sf_tiles + (size_t)s_tile[t.seg] * (p.K / 64) * 512;
-        for (int ks = 0; ks < kst; ++ks) {
-          if (!mbar_wait_bounded(smem_u32(empty + stage), phase ^ 1u, kWaitLimitNs, p.status)) {
-            ok = false;
-            break;
-          }
+        const int nbox = (max(t.rows, 1) + kXBoxRows - 1) / kXBoxRows;
+        for (int ks = 0; ks < kst; ++ks, ++g) {
           const uint32_t sb = smem0 + stage * kStageBytes;
           const uint32_t fb = smem_u32(full + stage);
-          // only the boxes that hold the expert's rows (16 rows each); the rest of the token
-          // tile stays stale and only feeds accumulator columns that are never stored
-          const int nbox = (max(t.rows, 1) + kXBoxRows - 1) / kXBoxRows;
-          mbar_arrive_expect_tx(fb, kTileBlockBytes + nbox * kXBoxRows * 128 + kXSfBytes);
-          bulk_load(sb, src + (size_t)ks * kTileBlockBytes, kTileBlockBytes, fb);
+          if (g >= pre) {
+            if (!mbar_wait_bounded(smem_u32(empty + stage), phase ^ 1u, kWaitLimitNs, p.status)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(fb, stage_bytes(t));
+            bulk_load(sb, src + (size_t)ks * kTileBlockBytes, kTileBlockBytes, fb);
+          }
           for (int bx = 0; bx < nbox; ++bx)
             tma_load_2d(sb + kXOff + bx * kXBoxRows * 128, &tmap_x, ks * 128,
                         t.m0 + bx * kXBoxRows, fb);

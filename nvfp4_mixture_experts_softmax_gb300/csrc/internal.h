@@ -195,6 +195,8 @@ struct GemmArgs {
   const float* perm_w;      // mode 1
   float* yacc;              // mode 1 out [T, N]
   float* obuf;              // mode 2 out [rows, N]
+  int plan_early;           // decode kernel: the plan is complete at launch (written two kernels
+                            // back), only the previous kernel's output needs the wait
   int32_t* status;
   int max_ctas;
   // bounds used to reject malformed plan data instead of touching memory outside the buffers

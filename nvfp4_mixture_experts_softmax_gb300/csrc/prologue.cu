@@ -39,21 +39,25 @@ __global__ void __launch_bounds__(kSmallPlanThreads) prologue_small_kernel(const
                        a.tile_start, a.perm_src, a.perm_w, a.inv, s_dyn, a.perm_seg);
 }
 
-// Decode batches (T <= kDecodeMaxRows): a cluster of kDecodeProCtas CTAs in three phases
-// separated by cluster barriers.
-//   A: one warp per token routes (top-k + weights, written to global memory) while every CTA
-//      reduces max |x| over its slice of x into its shared memory;
+// Decode batches (T <= kDecodeMaxRows): a cluster of kDecodeProCtas CTAs in two phases around
+// one cluster barrier.
+//   A: one warp per token routes (top-k + weights, written to global memory and to the routing
+//      CTA's shared memory) while every CTA reduces max |x| over its slice of x;
 //   B: every CTA combines the partial maxima through distributed shared memory into the tensor
-//      scale; CTA 0 counts, scans and places the assignments (the plan); the other CTAs encode
-//      x in token order, one thread per 16-element block;
-//   C: all CTAs copy each permuted row p from token perm_src[p] into xq_perm (16-byte vectors)
-//      and its scale words into the 32x4x4 arrangement of the decode GEMM's token operand
-//      (tile = the expert's tile index, row = p - offsets[expert]).
+//      scale, gathers the other CTAs' routing results the same way and places all assignments
+//      itself (the same stable plan in every CTA; CTA 0 alone writes it to global memory).  Then
+//      one thread per (token, 16-element block) encodes the block once and writes it in token
+//      order and into each of the token's expert-ordered rows: the codes into xq_perm, the
+//      scale byte into the 32x4x4 arrangement of the decode GEMM's token operand (tile = the
+//      expert's tile index, row = expert-ordered row - the expert's offset).
+// A CTA keeps its shared memory until the cluster's other CTAs have finished reading it (split
+// cluster barrier: arrive after the last remote read, wait before exit).
 template <int VPL>
 __global__ void __launch_bounds__(kSmallPlanThreads) decode_prologue_kernel(const DecodePrologueArgs a) {
   extern __shared__ __align__(16) uint8_t s_dyn[];
   __shared__ uint32_t red[32];
   __shared__ uint32_t s_part;
+  __shared__ float s_ts;
   griddep_wait();
   griddep_launch();
   const uint32_t rank = cluster_ctarank();
@@ -63,6 +67,13 @@ __global__ void __launch_bounds__(kSmallPlanThreads) decode_prologue_kernel(cons
   const int R = a.T * a.k;
   const int Rt = R + a.shared_rows;
   const int nkb = a.H / 16;
+  // small_place's scratch, then the per-assignment expert-ordered row and the per-expert tile
+  int32_t* s_ids = reinterpret_cast<int32_t*>(s_dyn) + 3 * a.E;
+  float* s_w = reinterpret_cast<float*>(s_ids + kSmallPlanRows);
+  int32_t* s_off = reinterpret_cast<int32_t*>(s_dyn) + a.E;
+  int32_t* s_inv = reinterpret_cast<int32_t*>(s_dyn + small_plan_smem_bytes(a.E));
+  int32_t* s_toff = s_inv + kSmallPlanRows;
+  if (rank == 0 && threadIdx.x == 0) *a.status = 0;
 
   // ---- A: routing (warp per token) and partial max |x| ----
   for (int t = (int)rank * nw + warp; t < a.T; t += kDecodeProCtas * nw) {
@@ -73,6 +84,8 @@ __global__ void __launch_bounds__(kSmallPlanThreads) decode_prologue_kernel(cons
     if (lane < a.k) {
       a.ids[(int64_t)t * a.k + lane] = my_id;
       a.w[(int64_t)t * a.k + lane] = w;
+      s_ids[t * a.k + lane] = my_id;
+      s_w[t * a.k + lane] = w;
     }
   }
   {
@@ -86,8 +99,7 @@ __global__ void __launch_bounds__(kSmallPlanThreads) decode_prologue_kernel(cons
   }
   cluster_sync();
 
-  // ---- B: tensor scale; plan (CTA 0) | token-order encode (CTAs 1..) ----
-  __shared__ float s_ts;
+  // ---- B: tensor scale and routing results from every CTA, then the plan in every CTA ----
   if (threadIdx.x < 32) {
     uint32_t m = threadIdx.x < kDecodeProCtas ? ld_dsmem_u32(&s_part, threadIdx.x) : 0u;
 #pragma unroll
@@ -96,77 +108,79 @@ __global__ void __launch_bounds__(kSmallPlanThreads) decode_prologue_kernel(cons
       const float ts = __fdiv_rn(bf16_bits_to_f32(m), 2688.0f);
       s_ts = ts;
       if (rank == 0) {
-        *a.status = 0;
         if (m >= 0x7F80u) set_status(a.status, MOE_ERR_NONFINITE);
         *a.ts = ts;
       }
     }
   }
+  for (int i = threadIdx.x; i < R; i += blockDim.x) {
+    const uint32_t owner = (uint32_t)((i / a.k) / nw) % kDecodeProCtas;   // CTA that routed token
+    if (owner != rank) {
+      s_ids[i] = (int32_t)ld_dsmem_u32(&s_ids[i], owner);
+      s_w[i] = __uint_as_float(ld_dsmem_u32(&s_w[i], owner));
+    }
+  }
+  cluster_arrive();   // no remote reads of this cluster after this point
+  int32_t* s_cnt = reinterpret_cast<int32_t*>(s_dyn);
+  for (int e = threadIdx.x; e < a.E; e += blockDim.x) s_cnt[e] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < R; i += blockDim.x) {
+    const int e = s_ids[i];
+    if (e >= 0 && e < a.E) atomicAdd(&s_cnt[e], 1);
+  }
+  __syncthreads();
+  const bool out = rank == 0;
+  small_place(a.T, a.E, a.k, a.shared_rows, out ? a.counts : nullptr, out ? a.offsets : nullptr,
+              out ? a.tile_start : nullptr, out ? a.perm_src : nullptr, out ? a.perm_w : nullptr,
+              out ? a.inv : nullptr, s_dyn, out ? a.perm_seg : nullptr, s_inv, s_toff);
   __syncthreads();
   const float ts = s_ts;
-  if (rank == 0) {
-    int32_t* s_cnt = reinterpret_cast<int32_t*>(s_dyn);
-    int32_t* s_ids = s_cnt + 3 * a.E;
-    float* s_w = reinterpret_cast<float*>(s_ids + kSmallPlanRows);
-    for (int e = threadIdx.x; e < a.E; e += blockDim.x) s_cnt[e] = 0;
-    __syncthreads();
-    for (int i = threadIdx.x; i < R; i += blockDim.x) {
-      const int e = __ldcg(a.ids + i);   // written in phase A by other CTAs
-      s_ids[i] = e;
-      s_w[i] = __ldcg(a.w + i);
-      if (e >= 0 && e < a.E) atomicAdd(&s_cnt[e], 1);
-    }
-    __syncthreads();
-    small_place(a.T, a.E, a.k, a.shared_rows, a.counts, a.offsets, a.tile_start, a.perm_src,
-                a.perm_w, a.inv, s_dyn, a.perm_seg);
-  } else {
-    const int64_t nblk = (int64_t)a.T * nkb;
-    for (int64_t b = (int64_t)(rank - 1) * blockDim.x + threadIdx.x; b < nblk;
-         b += (int64_t)(kDecodeProCtas - 1) * blockDim.x)
-      encode_bf16_block16(x, b, ts, reinterpret_cast<uint2*>(a.xq), a.xsf);
-  }
-  cluster_sync();
 
-  // ---- C: expert-ordered copy of the codes and the arranged scale words ----
-  const int vec_per_row = a.H / 32;     // 16-byte vectors of codes per row
-  const int64_t nvec_c = (int64_t)Rt * vec_per_row;
-  const int64_t stride = (int64_t)kDecodeProCtas * blockDim.x;
-  for (int64_t i = (int64_t)rank * blockDim.x + threadIdx.x; i < nvec_c; i += stride) {
-    const int p = (int)(i / vec_per_row), v = (int)(i - (int64_t)p * vec_per_row);
-    const int t = __ldcg(a.perm_src + p);
-    if (t < 0 || t >= a.T) {
-      set_status(a.status, MOE_ERR_INVALID_ARG);
-      continue;
+  // ---- encode each (token, block) once into token order and into the token's expert rows ----
+  const int wpr = a.H / 64;   // 4-scale words per row
+  const int64_t nblk = (int64_t)a.T * nkb;
+  for (int64_t u = (int64_t)rank * blockDim.x + threadIdx.x; u < nblk;
+       u += (int64_t)kDecodeProCtas * blockDim.x) {
+    const int t = (int)(u / nkb), b = (int)(u - (int64_t)t * nkb);
+    uint32_t lo, hi, sf;
+    quant_bf16_block16(x, u, ts, lo, hi, sf);
+    reinterpret_cast<uint2*>(a.xq)[u] = make_uint2(lo, hi);
+    a.xsf[u] = (uint8_t)sf;
+    for (int j = 0; j <= a.k; ++j) {
+      int p, r, tile;
+      if (j < a.k) {
+        const int e = s_ids[t * a.k + j];
+        if (e < 0 || e >= a.E) {
+          set_status(a.status, MOE_ERR_INVALID_ARG);
+          continue;
+        }
+        p = s_inv[t * a.k + j];
+        r = p - s_off[e];
+        tile = s_toff[e];
+      } else {
+        if (a.shared_rows == 0) break;
+        p = R + t;        // the shared expert's rows follow the routed ones, in token order
+        r = t;
+        tile = s_toff[a.E];
+      }
+      if (p < 0 || p >= Rt || r < 0 || r >= kDecodeMaxRows || tile < 0 || tile > Rt) {
+        set_status(a.status, MOE_ERR_INVALID_ARG);
+        continue;
+      }
+      *reinterpret_cast<uint2*>(a.xq_perm + (size_t)p * (a.H / 2) + (size_t)b * 8) =
+          make_uint2(lo, hi);
+      a.xsf_tiles[((size_t)tile * wpr + b / 4) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (b & 3)] =
+          (uint8_t)sf;
     }
-    const uint4 c = __ldcg(reinterpret_cast<const uint4*>(a.xq + (size_t)t * (a.H / 2)) + v);
-    reinterpret_cast<uint4*>(a.xq_perm + (size_t)p * (a.H / 2))[v] = c;
   }
-  const int wpr = a.H / 64;             // 4-scale words per row
-  const int64_t nw_c = (int64_t)Rt * wpr;
-  for (int64_t i = (int64_t)rank * blockDim.x + threadIdx.x; i < nw_c; i += stride) {
-    const int p = (int)(i / wpr), wd = (int)(i - (int64_t)p * wpr);
-    const int t = __ldcg(a.perm_src + p);
-    const int e = __ldcg(a.perm_seg + p);
-    if (t < 0 || t >= a.T || e < 0 || e > a.E) {
-      set_status(a.status, MOE_ERR_INVALID_ARG);
-      continue;
-    }
-    const int r = p - __ldcg(a.offsets + e);
-    const int tile = __ldcg(a.tile_start + e);
-    if (r < 0 || r >= kDecodeMaxRows) {
-      set_status(a.status, MOE_ERR_INVALID_ARG);
-      continue;
-    }
-    const uint32_t word = __ldcg(reinterpret_cast<const uint32_t*>(a.xsf + (size_t)t * nkb) + wd);
-    *reinterpret_cast<uint32_t*>(a.xsf_tiles + ((size_t)tile * wpr + wd) * 512 + (r & 31) * 16 +
-                                 (r >> 5) * 4) = word;
-  }
+  cluster_wait();
 }
 
 }  // namespace
 
 cudaError_t launch_decode_prologue(const DecodePrologueArgs& a, cudaStream_t s) {
-  const size_t smem = small_plan_smem_bytes(a.E);
+  // small_place's scratch + expert-ordered row per assignment + first tile per segment
+  const size_t smem = small_plan_smem_bytes(a.E) + sizeof(int32_t) * (kSmallPlanRows + a.E + 1);
   const int vpl = (a.E + 31) / 32;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(kDecodeProCtas);

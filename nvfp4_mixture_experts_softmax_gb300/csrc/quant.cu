@@ -198,12 +198,25 @@ __global__ void __launch_bounds__(kThreads) finalize_gather_kernel(const float4*
        i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t t = i / H4, m = i - t * H4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < k; ++j) {
-      const float4 v = __ldcg(o + (int64_t)__ldg(inv + t * k + j) * H4 + m);
-      acc.x = __fadd_rn(acc.x, v.x);
-      acc.y = __fadd_rn(acc.y, v.y);
-      acc.z = __fadd_rn(acc.z, v.z);
-      acc.w = __fadd_rn(acc.w, v.w);
+    // eight slots at a time: their row indices, then their rows, then the in-order additions
+    // (two dependent memory round trips per group instead of two per slot)
+    for (int j0 = 0; j0 < k; j0 += 8) {
+      int row[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) row[u] = j0 + u < k ? __ldg(inv + t * k + j0 + u) : 0;
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        v[u] = j0 + u < k ? __ldcg(o + (int64_t)row[u] * H4 + m) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (j0 + u < k) {
+          acc.x = __fadd_rn(acc.x, v[u].x);
+          acc.y = __fadd_rn(acc.y, v[u].y);
+          acc.z = __fadd_rn(acc.z, v[u].z);
+          acc.w = __fadd_rn(acc.w, v[u].w);
+        }
+      }
     }
     if (shared) {
       const float4 v = __ldcg(o + (R + t) * H4 + m);

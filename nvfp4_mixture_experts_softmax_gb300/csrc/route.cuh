@@ -95,7 +95,7 @@ __device__ __forceinline__ float topk_weight(float my_l, int k, int lane) {
 }
 
 // Dynamic shared memory of small_plan_body for E experts.
-inline size_t small_plan_smem_bytes(int E) {
+__host__ __device__ inline size_t small_plan_smem_bytes(int E) {
   return (size_t)3 * E * sizeof(int32_t) + (size_t)kSmallPlanRows * (sizeof(int32_t) + sizeof(float)) +
          (size_t)(kSmallPlanThreads / 32) * E * sizeof(uint16_t);
 }
@@ -106,14 +106,18 @@ inline size_t small_plan_smem_bytes(int E) {
 // to e).  Assignments are taken 1024 at a time; inside a group a warp ranks equal experts with
 // match_any and each warp adds the counts of the warps before it; a per-expert cursor carries
 // the counts of earlier groups.  Must be called by all kSmallPlanThreads threads of the block;
-// `dyn` is the dynamic shared memory laid out as in small_plan_body.
+// `dyn` is the dynamic shared memory laid out as in small_plan_body.  Every global output may be
+// null (nothing written); s_inv (kSmallPlanRows entries) and s_toff (E + 1 entries), when given,
+// receive the expert-ordered row of each assignment and each expert's first tile in shared memory.
 __device__ __forceinline__ void small_place(int T, int E, int k, int shared_rows,
                                             int32_t* __restrict__ counts,
                                             int32_t* __restrict__ offsets,
                                             int32_t* __restrict__ tile_start,
                                             int32_t* __restrict__ perm_src,
                                             float* __restrict__ perm_w, int32_t* __restrict__ inv,
-                                            uint8_t* dyn, int32_t* __restrict__ perm_seg) {
+                                            uint8_t* dyn, int32_t* __restrict__ perm_seg,
+                                            int32_t* __restrict__ s_inv = nullptr,
+                                            int32_t* __restrict__ s_toff = nullptr) {
   int32_t* s_cnt = reinterpret_cast<int32_t*>(dyn);
   int32_t* s_off = s_cnt + E;
   int32_t* s_cur = s_off + E;
@@ -132,12 +136,14 @@ __device__ __forceinline__ void small_place(int T, int E, int k, int shared_rows
   if (e < E) {
     s_off[e] = off;
     if (counts) counts[e] = cnt;
-    offsets[e] = off;
+    if (offsets) offsets[e] = off;
     if (tile_start) tile_start[e] = toff;
+    if (s_toff) s_toff[e] = toff;
   }
   if (threadIdx.x == 0) {
-    offsets[E] = total;
-    if (shared_rows > 0) offsets[E + 1] = total + shared_rows;
+    if (s_toff) s_toff[E] = ttotal;
+    if (offsets) offsets[E] = total;
+    if (offsets && shared_rows > 0) offsets[E + 1] = total + shared_rows;
     if (tile_start) {
       tile_start[E] = ttotal;
       if (shared_rows > 0) tile_start[E + 1] = ttotal + (shared_rows + kBM - 1) / kBM;
@@ -158,10 +164,11 @@ __device__ __forceinline__ void small_place(int T, int E, int k, int shared_rows
       int rank = __popc(peers & lt) + s_cur[ea];
       for (int v = 0; v < warp; ++v) rank += s_wcnt[v * E + ea];
       const int p = s_off[ea] + rank;
-      perm_src[p] = a / k;
+      if (perm_src) perm_src[p] = a / k;
       if (perm_w) perm_w[p] = s_w[a];
       if (perm_seg) perm_seg[p] = ea;
-      inv[a] = p;
+      if (inv) inv[a] = p;
+      if (s_inv) s_inv[a] = p;
     }
     __syncthreads();
     for (int x = threadIdx.x; x < E; x += blockDim.x) {
@@ -171,7 +178,7 @@ __device__ __forceinline__ void small_place(int T, int E, int k, int shared_rows
     }
     __syncthreads();
   }
-  for (int t = threadIdx.x; t < shared_rows; t += blockDim.x) {
+  for (int t = threadIdx.x; t < shared_rows && perm_src; t += blockDim.x) {
     perm_src[R + t] = t;
     if (perm_w) perm_w[R + t] = 1.0f;
     if (perm_seg) perm_seg[R + t] = E;
