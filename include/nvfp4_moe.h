@@ -152,8 +152,9 @@ int moe_plan(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* topk
  * the process exits.  It calls no cudaMalloc, cudaFree or other allocating routine.
  *   - Arguments and outputs are those of moe_plan; the caller still owns every output buffer.
  *   - A problem whose moe_plan_workspace_size(T, E, k) exceeds MOE_PLAN_STATIC_SCRATCH_BYTES is
- *     rejected with MOE_ERR_WORKSPACE_TOO_SMALL: ceil(T/64)*E must stay within 131,040 for
- *     k <= 16 (ceil(T/32)*E for larger k), e.g. T = 8,192 tokens at E = 1,024 experts.
+ *     rejected with MOE_ERR_WORKSPACE_TOO_SMALL: ceil(T/64)*E (ceil(T/32)*E for k > 16) must
+ *     stay within about 130,000, e.g. up to T = 8,128 tokens at E = 1,024 experts, 32,704 at
+ *     E = 256, 65,472 at E = 128.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
  *     that device current; make that first call before any stream capture.
  *   - All calls share the one array per device, and it keeps the last call's contents: calls
@@ -176,7 +177,7 @@ size_t moe_workspace_size(const moe_config* cfg, int32_t T);
 /* Number of kernels one moe_run(cfg, ..., T, ...) launches (memset nodes not counted), or a
  * negative moe_status for an invalid cfg / T.  Host-only arithmetic: no CUDA call, no device.
  * It mirrors moe_run's choice of path: 4 for decode-sized batches (cluster prologue, GEMM1,
- * GEMM2, row sum), 5 for other small batches, 7 or 9 for large ones (the router and plan take one
+ * GEMM2, row sum), 5 for other small batches, 6 or 8 for large ones (the router and plan take one
  * kernel up to 2048 routed rows, three above).  A utility for launch accounting; the pages have
  * no counterpart. */
 int moe_run_kernel_count(const moe_config* cfg, int32_t T);

@@ -120,7 +120,7 @@ size_t moe_plan_workspace_size(int32_t T, int32_t E, int32_t k) {
   if (T < 0 || E < 1 || k < 1) return 0;
   const int tpc = plan_tokens_per_chunk(k);
   const size_t nchunks = ((size_t)T + tpc - 1) / tpc;
-  return 256 + align_up(4 * nchunks * E) * 2;
+  return 256 + align_up(4 * (nchunks * E + 1 + E)) + align_up(4 * nchunks * E);
 }
 
 int moe_plan(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* topk_ids,
@@ -157,7 +157,7 @@ int moe_plan(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* topk
   a.perm_w = nullptr;
   a.inv = inv;
   a.hist = reinterpret_cast<int32_t*>(w8 + 256);
-  a.base = reinterpret_cast<int32_t*>(w8 + 256 + align_up(4 * nchunks * E));
+  a.base = reinterpret_cast<int32_t*>(w8 + 256 + align_up(4 * (nchunks * E + 1 + E)));
   a.status = reinterpret_cast<int32_t*>(w8);
   return cuda_status(launch_plan(a, s));
 }
@@ -175,8 +175,8 @@ int moe_run_kernel_count(const moe_config* cfg, int32_t T) {
   const RunLayout L(*cfg, T);
   if (L.decode) return 4;     // cluster prologue, GEMM1, GEMM2, row sum
   if (L.small) return 5;      // one-block prologue, permute, GEMM1, GEMM2, row sum
-  // amax + encode, router/plan (1 or 3), permute, GEMM1, GEMM2, BF16 conversion
-  return 2 + ((int64_t)T * cfg->top_k <= kSmallPlanRows ? 1 : 3) + 4;
+  // amax, router/plan (1 or 3), encode into expert order, GEMM1, GEMM2, BF16 conversion
+  return 1 + ((int64_t)T * cfg->top_k <= kSmallPlanRows ? 1 : 3) + 4;
 }
 
 int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float* logits, int32_t T,
@@ -281,9 +281,10 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
   e = cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
-  // 1. activation quantiser (and zero the FP32 output accumulator on the way)
-  e = launch_act_quant(x, T, H, ws + L.xq, ws + L.xsf, nullptr, hdr,
-                       reinterpret_cast<uint32_t*>(ws + L.amax_part), f32(L.yacc), (int64_t)T * H, s);
+  // 1. activation tensor scale (and zero the FP32 output accumulator on the way); the encode
+  //    follows the plan so that it can write every expert row directly
+  e = launch_act_amax(x, T, H, nullptr, hdr, reinterpret_cast<uint32_t*>(ws + L.amax_part),
+                      f32(L.yacc), (int64_t)T * H, s);
   if (e == cudaSuccess) e = mark(1);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
@@ -313,11 +314,17 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
 
   const int nseg = E + shared;
   const int64_t max_mtiles = ((int64_t)L.Rt + (int64_t)nseg * (kBM - 1)) / kBM;
-  if (!L.decode) {
-    // activations into expert order (the decode prologue writes them there itself)
+  if (L.small && !L.decode) {
+    // activations (encoded in token order by the one-block prologue) into expert order
     e = launch_permute_rows(ws + L.xq, ws + L.xsf, T, H, L.Rt, E, i32(L.perm_src),
                             i32(L.perm_seg), i32(L.seg_off), i32(L.tile_start), ws + L.xq_perm,
                             ws + L.xsf_tiles, &hdr->status, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  } else if (!L.small) {
+    // encode each block once into token order and into every expert row of its token
+    e = launch_act_encode_perm(x, T, H, k, E, shared, L.Rt, &hdr->ts, i32(L.ids), i32(L.inv),
+                               i32(L.seg_off), i32(L.tile_start), ws + L.xq, ws + L.xsf,
+                               ws + L.xq_perm, ws + L.xsf_tiles, &hdr->status, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   const float* w_ts = reinterpret_cast<const float*>(wb + W.ts);

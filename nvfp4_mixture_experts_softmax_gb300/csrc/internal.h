@@ -102,7 +102,7 @@ struct RunLayout {
     amax_part = o;  o = align_up(o + 4 * 1024);
     ids = o;        o = align_up(o + 4 * (size_t)R);
     w = o;          o = align_up(o + 4 * (size_t)R);
-    hist = o;       o = align_up(o + 4 * (size_t)nchunks * E);
+    hist = o;       o = align_up(o + 4 * ((size_t)nchunks * E + 1 + E));
     base = o;       o = align_up(o + 4 * (size_t)nchunks * E);
     seg_off = o;    o = align_up(o + 4 * (size_t)(nseg + 2));
     tile_start = o; o = align_up(o + 4 * (size_t)(nseg + 2));
@@ -141,6 +141,18 @@ cudaError_t launch_act_quant(const void* x, int64_t rows, int64_t cols, uint8_t*
                              float* ts, WsHeader* hdr, uint32_t* partials, float* zero_buf,
                              int64_t zero_floats, cudaStream_t s);
 
+// The two halves of launch_act_quant for batches that are planned before they are encoded:
+// max |x| -> tensor scale (and the accumulator zeroing), then the encode into token order and
+// into every expert row of each token (xq_perm, xsf_tiles).
+cudaError_t launch_act_amax(const void* x, int64_t rows, int64_t cols, float* ts, WsHeader* hdr,
+                            uint32_t* partials, float* zero_buf, int64_t zero_floats,
+                            cudaStream_t s);
+cudaError_t launch_act_encode_perm(const void* x, int T, int H, int k, int E, int shared, int Rt,
+                                   const float* ts, const int32_t* ids, const int32_t* inv,
+                                   const int32_t* offsets, const int32_t* tile_start,
+                                   uint8_t* codes, uint8_t* sf, uint8_t* xq_perm,
+                                   uint8_t* xsf_tiles, int32_t* status, cudaStream_t s);
+
 cudaError_t launch_weight_quant(const moe_config& c, const WeightLayout& L, const void* wg,
                                 const void* wu, const void* wd, const void* sg, const void* su,
                                 const void* sd, uint8_t* wbuf, cudaStream_t s);
@@ -162,7 +174,7 @@ struct PlanArgs {
   float* perm_w;          // [R + shared_rows] (may be null)
   int32_t* inv;           // [T*k]
   int32_t* perm_seg;      // [R + shared_rows] expert (segment) of each permuted row (may be null)
-  int32_t* hist;          // [nchunks*E] scratch
+  int32_t* hist;          // [nchunks*E + 1 + E] scratch: histograms, scan block count, totals
   int32_t* base;          // [nchunks*E] scratch
   int32_t* status;
 };

@@ -233,6 +233,55 @@ __global__ void __launch_bounds__(kThreads) finalize_gather_kernel(const float4*
 
 // Expert-ordered copy of the quantised activations: 16-byte code vectors, then 4-scale words into
 // the 32x4x4 arrangement of the GEMM tiles (see launch_permute_rows).
+// Activation encode straight into expert order (batches planned before they are encoded): one
+// thread per 16-element block of x quantises it once and writes it in token order and into each
+// of the token's expert-ordered rows - its codes into xq_perm, its scale byte into the
+// 32x4x4 arrangement of the GEMM's A-operand scales (tile = the segment's first tile + row/128).
+__global__ void __launch_bounds__(kThreads) act_encode_perm_kernel(
+    const uint4* __restrict__ x, int T, int H, int k, int E, int shared, int Rt,
+    const float* __restrict__ ts_ptr, const int32_t* __restrict__ ids,
+    const int32_t* __restrict__ inv, const int32_t* __restrict__ offsets,
+    const int32_t* __restrict__ tile_start, uint2* __restrict__ codes, uint8_t* __restrict__ sf,
+    uint8_t* __restrict__ xq_perm, uint8_t* __restrict__ xsf_tiles, int32_t* status) {
+  griddep_wait();
+  griddep_launch();
+  const float ts = *ts_ptr;
+  const int nkb = H / 16, wpr = H / 64;
+  const int64_t nblk = (int64_t)T * nkb;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < nblk; u += stride) {
+    const int t = (int)(u / nkb), b = (int)(u - (int64_t)t * nkb);
+    uint32_t lo, hi, s8;
+    quant_bf16_block16(x, u, ts, lo, hi, s8);
+    codes[u] = make_uint2(lo, hi);
+    sf[u] = (uint8_t)s8;
+    for (int j = 0; j <= k; ++j) {
+      int p, seg;
+      if (j < k) {
+        seg = __ldg(ids + (int64_t)t * k + j);
+        p = __ldg(inv + (int64_t)t * k + j);
+      } else {
+        if (!shared) break;
+        seg = E;
+        p = T * k + t;   // the shared expert's rows follow the routed ones, in token order
+      }
+      if (seg < 0 || seg > E || p < 0 || p >= Rt) {
+        set_status(status, MOE_ERR_INVALID_ARG);
+        continue;
+      }
+      const int r = p - __ldg(offsets + seg);
+      if (r < 0) {
+        set_status(status, MOE_ERR_INVALID_ARG);
+        continue;
+      }
+      const int64_t tile = __ldg(tile_start + seg) + (r >> 7);
+      const int rr = r & 127;
+      *reinterpret_cast<uint2*>(xq_perm + (size_t)p * (H / 2) + (size_t)b * 8) = make_uint2(lo, hi);
+      xsf_tiles[(tile * wpr + b / 4) * 512 + (rr & 31) * 16 + (rr >> 5) * 4 + (b & 3)] = (uint8_t)s8;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kThreads) permute_rows_kernel(
     const uint4* __restrict__ xq, const uint32_t* __restrict__ xsf, int T, int H, int Rt, int E,
     const int32_t* __restrict__ perm_src, const int32_t* __restrict__ perm_seg,
@@ -305,15 +354,34 @@ int num_sms() {
   return n;
 }
 
+cudaError_t launch_act_amax(const void* x, int64_t rows, int64_t cols, float* ts, WsHeader* hdr,
+                            uint32_t* partials, float* zero_buf, int64_t zero_floats,
+                            cudaStream_t s) {
+  const int64_t nvec = rows * cols / 8;
+  const int g1 = grid_for(nvec, kThreads * 8, kMaxAmaxBlocks);
+  return launch_pdl(act_amax_kernel, dim3(g1), dim3(kThreads), 0, s,
+                    reinterpret_cast<const uint4*>(x), nvec, hdr, partials, ts,
+                    reinterpret_cast<float4*>(zero_buf), zero_floats / 4);
+}
+
+cudaError_t launch_act_encode_perm(const void* x, int T, int H, int k, int E, int shared, int Rt,
+                                   const float* ts, const int32_t* ids, const int32_t* inv,
+                                   const int32_t* offsets, const int32_t* tile_start,
+                                   uint8_t* codes, uint8_t* sf, uint8_t* xq_perm,
+                                   uint8_t* xsf_tiles, int32_t* status, cudaStream_t s) {
+  const int64_t nblk = (int64_t)T * H / 16;
+  const int g = grid_for(nblk, kThreads, num_sms() * 16);
+  return launch_pdl(act_encode_perm_kernel, dim3(g), dim3(kThreads), 0, s,
+                    reinterpret_cast<const uint4*>(x), T, H, k, E, shared, Rt, ts, ids, inv,
+                    offsets, tile_start, reinterpret_cast<uint2*>(codes), sf, xq_perm, xsf_tiles,
+                    status);
+}
+
 cudaError_t launch_act_quant(const void* x, int64_t rows, int64_t cols, uint8_t* codes, uint8_t* sf,
                              float* ts, WsHeader* hdr, uint32_t* partials, float* zero_buf,
                              int64_t zero_floats, cudaStream_t s) {
   const int64_t n = rows * cols;
-  const int64_t nvec = n / 8;
-  const int g1 = grid_for(nvec, kThreads * 8, kMaxAmaxBlocks);
-  cudaError_t e = launch_pdl(act_amax_kernel, dim3(g1), dim3(kThreads), 0, s,
-                             reinterpret_cast<const uint4*>(x), nvec, hdr, partials, ts,
-                             reinterpret_cast<float4*>(zero_buf), zero_floats / 4);
+  cudaError_t e = launch_act_amax(x, rows, cols, ts, hdr, partials, zero_buf, zero_floats, s);
   if (e != cudaSuccess) return e;
   const int64_t nblk = n / 16;
   const int g2 = grid_for(nblk, kThreads, num_sms() * 16);

@@ -63,49 +63,62 @@ __global__ void __launch_bounds__(kSmallPlanThreads) plan_small_kernel(
                        perm_src, perm_w, inv, s_dyn, perm_seg);
 }
 
-// One block of 1024 threads: per-expert exclusive scan over chunks (base), counts, segment
-// offsets and the prefix of 128-row tiles per segment.  Segment E (when shared_rows > 0) is the
-// shared expert: shared_rows rows starting at T*k.
-constexpr int kScanRows = 16;
-
+// Per-chunk bases and per-expert offsets from the chunk histograms, spread over blocks of 32
+// experts: lane l of every warp owns expert 32*block + l (so each chunk row is read coalesced),
+// warp w sums a contiguous range of chunks, a scan over the 32 warp sums gives each range its
+// start, and the range is written out as running sums.  The block that finishes last (atomic
+// count, reset to 0 for the next call) scans the per-expert totals into offsets and 128-row tile
+// starts.  scratch[0] is that count, scratch[1..E] the totals.
 __global__ void __launch_bounds__(1024) plan_scan_kernel(const int32_t* __restrict__ hist,
                                                         int nchunks, int E, int shared_rows,
                                                         int32_t* __restrict__ base,
                                                         int32_t* __restrict__ counts,
                                                         int32_t* __restrict__ offsets,
-                                                        int32_t* __restrict__ tile_start) {
-  extern __shared__ int32_t s_tile[];  // [kScanRows][E]
+                                                        int32_t* __restrict__ tile_start,
+                                                        int32_t* __restrict__ scratch) {
+  __shared__ int32_t s_part[32][33];
   __shared__ int32_t sw[32];
+  __shared__ int s_last;
   griddep_wait();
   griddep_launch();
-  const int e = threadIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 32 + lane;
+  const int cpw = (nchunks + 31) / 32;
+  const int c0 = min(nchunks, warp * cpw), c1 = min(nchunks, c0 + cpw);
+  int32_t sum = 0;
+  if (e < E)
+    for (int c = c0; c < c1; ++c) sum += __ldcg(hist + (int64_t)c * E + e);
+  s_part[warp][lane] = sum;
+  __syncthreads();
   int32_t run = 0;
-  for (int c0 = 0; c0 < nchunks; c0 += kScanRows) {
-    const int rows = min(kScanRows, nchunks - c0);
-    for (int i = threadIdx.x; i < rows * E; i += blockDim.x) s_tile[i] = hist[(int64_t)c0 * E + i];
-    __syncthreads();
-    if (e < E)
-      for (int r = 0; r < rows; ++r) {
-        const int32_t v = s_tile[r * E + e];
-        s_tile[r * E + e] = run;
-        run += v;
-      }
-    __syncthreads();
-    for (int i = threadIdx.x; i < rows * E; i += blockDim.x) base[(int64_t)c0 * E + i] = s_tile[i];
-    __syncthreads();
+  for (int v = 0; v < warp; ++v) run += s_part[v][lane];
+  if (e < E) {
+    if (warp == 31) scratch[1 + e] = run + sum;   // the expert's total
+    for (int c = c0; c < c1; ++c) {
+      const int32_t h = __ldcg(hist + (int64_t)c * E + e);
+      base[(int64_t)c * E + e] = run;
+      run += h;
+    }
   }
-  const int32_t cnt = e < E ? run : 0;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(scratch, 1) == (int)gridDim.x - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int t = threadIdx.x;
+  const int32_t cnt = t < E ? __ldcg(scratch + 1 + t) : 0;
   int32_t total;
   const int32_t off = block_exclusive_scan(cnt, sw, total);
   const int32_t ntile = (cnt + kBM - 1) / kBM;
   int32_t ttotal;
   const int32_t toff = block_exclusive_scan(ntile, sw, ttotal);
-  if (e < E) {
-    if (counts) counts[e] = cnt;
-    offsets[e] = off;
-    if (tile_start) tile_start[e] = toff;
+  if (t < E) {
+    if (counts) counts[t] = cnt;
+    offsets[t] = off;
+    if (tile_start) tile_start[t] = toff;
   }
-  if (threadIdx.x == 0) {
+  if (t == 0) {
     offsets[E] = total;
     const int32_t shared_tiles = (shared_rows + kBM - 1) / kBM;
     if (shared_rows > 0) offsets[E + 1] = total + shared_rows;
@@ -113,6 +126,7 @@ __global__ void __launch_bounds__(1024) plan_scan_kernel(const int32_t* __restri
       tile_start[E] = ttotal;
       if (shared_rows > 0) tile_start[E + 1] = ttotal + shared_tiles;
     }
+    scratch[0] = 0;
   }
 }
 
@@ -185,7 +199,8 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s) {
 #undef NVFP4MOE_SMALL
     return cudaGetLastError();
   }
-  cudaError_t err = cudaMemsetAsync(a.hist, 0, sizeof(int32_t) * (size_t)nchunks * a.E, s);
+  // the histograms and the scan's block count (scratch after them) start at zero
+  cudaError_t err = cudaMemsetAsync(a.hist, 0, sizeof(int32_t) * ((size_t)nchunks * a.E + 1), s);
   if (err != cudaSuccess) return err;
   const int rblocks = (a.T + kRouterWarps - 1) / kRouterWarps;
 #define NVFP4MOE_ROUTER(V)                                                                 \
@@ -200,14 +215,9 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s) {
 #undef NVFP4MOE_ROUTER
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  const size_t scan_smem = sizeof(int32_t) * kScanRows * a.E;
-  if (scan_smem > 48 * 1024) {
-    err = cudaFuncSetAttribute(plan_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)scan_smem);
-    if (err != cudaSuccess) return err;
-  }
-  err = launch_pdl(plan_scan_kernel, dim3(1), dim3(1024), scan_smem, s, (const int32_t*)a.hist,
-                   nchunks, a.E, a.shared_rows, a.base, a.counts, a.offsets, a.tile_start);
+  err = launch_pdl(plan_scan_kernel, dim3((a.E + 31) / 32), dim3(1024), 0, s,
+                   (const int32_t*)a.hist, nchunks, a.E, a.shared_rows, a.base, a.counts,
+                   a.offsets, a.tile_start, a.hist + (size_t)nchunks * a.E);
   if (err != cudaSuccess) return err;
   const int threads = ((tpc * a.k + 31) / 32) * 32;
   const size_t sc_smem = sizeof(int32_t) * (threads / 32) * a.E;

@@ -91,15 +91,15 @@ def test_host_side_rejections(moe):
 
 def test_run_kernel_count(moe):
     """The launch count follows moe_run's path choice: decode-sized batches take four kernels,
-    other small batches five, large ones seven (one-kernel plan) or nine (three-kernel plan)."""
+    other small batches five, large ones six (one-kernel plan) or eight (three-kernel plan)."""
     dec = moe.make_config(128, 2048, 768, 8, max_tokens=8192)
     assert [moe.run_kernel_count(dec, T) for T in (1, 8, 32, 64)] == [4, 4, 4, 4]
     assert moe.run_kernel_count(dec, 0) == 0
-    assert moe.run_kernel_count(dec, 8192) == 9
+    assert moe.run_kernel_count(dec, 8192) == 8
     mid = moe.make_config(16, 2048, 256, 4, max_tokens=1024)
     assert moe.run_kernel_count(mid, 100) == 5     # fits the one-block prologue
-    assert moe.run_kernel_count(mid, 500) == 7     # 2000 routed rows: one-kernel plan
-    assert moe.run_kernel_count(mid, 600) == 9     # 2400 routed rows: three-kernel plan
+    assert moe.run_kernel_count(mid, 500) == 6     # 2000 routed rows: one-kernel plan
+    assert moe.run_kernel_count(mid, 600) == 8     # 2400 routed rows: three-kernel plan
     with pytest.raises(RuntimeError):
         moe.run_kernel_count(dec, -1)
     with pytest.raises(RuntimeError):
