@@ -67,6 +67,18 @@ __device__ __forceinline__ uint32_t e2m1x8(float v0, float v1, float v2, float v
 //   sf = E4M3((max|x| / 6) / ts); S = decode(sf) * ts; code_i = E2M1(x_i / S)
 // with IEEE FP32 division and multiplication in that order; a zero block or a zero S gives scale
 // byte 0 and all-zero codes.
+// x / S rounded to nearest even, from r = RN(1/S): q0 = RN(x*r) is within one ulp of x/S, so the
+// residual x - q0*S is exact (one fma) and RN(q0 + residual*r) is the correctly rounded quotient
+// (Markstein's theorem for a correctly rounded reciprocal), provided nothing underflows or
+// overflows.  The caller takes this path only for S in [2^-90, 2^90] with |x| <= 8*S: then the
+// reciprocal, the quotient and the residual of any quotient >= 2^-3 stay normal, and a smaller
+// quotient (far below the first E2M1 rounding boundary, 0.25) only has to keep the sign of x.
+__device__ __forceinline__ float div_rn_by_recip(float x, float S, float r) {
+  const float q0 = __fmul_rn(x, r);
+  const float res = __fmaf_rn(-q0, S, x);
+  return copysignf(__fmaf_rn(res, r, q0), x);
+}
+
 __device__ __forceinline__ void quant_block16(const float* x, float ts, uint32_t& lo, uint32_t& hi,
                                               uint32_t& sf) {
   float bamax = 0.0f;
@@ -80,8 +92,14 @@ __device__ __forceinline__ void quant_block16(const float* x, float ts, uint32_t
   const float S = __fmul_rn(e4m3_to_f32(sf), ts);
   if (S == 0.0f) return;
   float q[16];
+  if (S >= 0x1p-90f && S <= 0x1p90f && bamax <= 8.0f * S) {
+    const float r = __frcp_rn(S);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) q[i] = __fdiv_rn(x[i], S);
+    for (int i = 0; i < 16; ++i) q[i] = div_rn_by_recip(x[i], S, r);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) q[i] = __fdiv_rn(x[i], S);
+  }
   lo = e2m1x8(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]);
   hi = e2m1x8(q[8], q[9], q[10], q[11], q[12], q[13], q[14], q[15]);
 }

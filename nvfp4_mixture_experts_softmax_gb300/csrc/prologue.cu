@@ -76,6 +76,14 @@ __global__ void __launch_bounds__(kSmallPlanThreads) decode_prologue_kernel(cons
   if (rank == 0 && threadIdx.x == 0) *a.status = 0;
 
   // ---- A: routing (warp per token) and partial max |x| ----
+  // the first two activation vectors of each thread are loaded before the routing so that their
+  // memory latency overlaps the logits'
+  const int64_t nvec = (int64_t)a.T * a.H / 8;
+  const int64_t vstride = (int64_t)kDecodeProCtas * blockDim.x;
+  const int64_t v0 = (int64_t)rank * blockDim.x + threadIdx.x;
+  uint4 xv0 = make_uint4(0u, 0u, 0u, 0u), xv1 = make_uint4(0u, 0u, 0u, 0u);
+  if (v0 < nvec) xv0 = __ldg(x + v0);
+  if (v0 + vstride < nvec) xv1 = __ldg(x + v0 + vstride);
   for (int t = (int)rank * nw + warp; t < a.T; t += kDecodeProCtas * nw) {
     int my_id;
     float my_l;
@@ -89,11 +97,8 @@ __global__ void __launch_bounds__(kSmallPlanThreads) decode_prologue_kernel(cons
     }
   }
   {
-    const int64_t nvec = (int64_t)a.T * a.H / 8;
-    uint32_t m = 0;
-    for (int64_t i = (int64_t)rank * blockDim.x + threadIdx.x; i < nvec;
-         i += (int64_t)kDecodeProCtas * blockDim.x)
-      m = max(m, abs_bf16_max8(__ldg(x + i)));
+    uint32_t m = max(abs_bf16_max8(xv0), abs_bf16_max8(xv1));
+    for (int64_t i = v0 + 2 * vstride; i < nvec; i += vstride) m = max(m, abs_bf16_max8(__ldg(x + i)));
     m = block_max_u32(m, red);
     if (threadIdx.x == 0) s_part = m;
   }

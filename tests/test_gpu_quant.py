@@ -110,3 +110,36 @@ def test_weight_quant_decode_sampled(moe):
             rc, rs, rts, _ = oracle.quantize_bf16(W.cpu())
             assert ts.item() == rts
             assert np.array_equal(sf.cpu().numpy(), rs) and np.array_equal(codes.cpu().numpy(), rc)
+
+
+def test_act_quant_every_bf16_every_scale(moe):
+    """Every finite BF16 value against every E4M3 block scale, bit-exact against the oracle.
+
+    The tensor's max is 2688, so the tensor scale is exactly 1 and a block whose max is
+    6*decode(sf) gets scale sf exactly (both divisions exact); the block's other 15 elements run
+    over every BF16 value v with |v| <= 6*decode(sf).  This covers every quotient the encoder can
+    meet at each scale, including those within an ulp of an E2M1 rounding boundary, so any
+    difference between the GPU's quotient and the IEEE division shows up as a code mismatch."""
+    bits = np.arange(1 << 16, dtype=np.uint32)
+    allv = (bits << 16).view(np.float32)
+    allv = allv[np.isfinite(allv)]
+    dec = torch.arange(1, 127, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    blocks = [np.array([2688.0] + [0.0] * 15, dtype=np.float32)]   # fixes the tensor scale at 1
+    for d in dec:
+        bamax = np.float32(6.0) * np.float32(d)
+        vals = allv[np.abs(allv) <= bamax]
+        pad = (-len(vals)) % 15
+        vals = np.concatenate([vals, np.zeros(pad, dtype=np.float32)]).reshape(-1, 15)
+        blk = np.concatenate([np.full((len(vals), 1), bamax, dtype=np.float32), vals], axis=1)
+        blocks.append(blk.reshape(-1))
+    flat = np.concatenate(blocks)
+    cols = 4096
+    flat = np.concatenate([flat, np.zeros((-len(flat)) % cols, dtype=np.float32)])
+    x = torch.from_numpy(flat.reshape(-1, cols)).to(torch.bfloat16)
+    assert torch.equal(x.float(), torch.from_numpy(flat.reshape(-1, cols)))   # all exact in BF16
+    codes, sf, ts = moe.quantize_act(x.cuda())
+    torch.cuda.synchronize()
+    rc, rs, rts, st = oracle.quantize_bf16(x)
+    assert st == 0 and rts == 1.0 and ts.item() == 1.0
+    assert np.array_equal(sf.cpu().numpy(), rs)
+    assert np.array_equal(codes.cpu().numpy(), rc)
