@@ -40,7 +40,11 @@ class MoeArgs(C.Structure):
                 ("logits", C.c_void_p), ("experts", C.c_void_p), ("y", C.c_void_p),
                 ("ids", C.c_void_p), ("w", C.c_void_p), ("counts", C.c_void_p),
                 ("offsets", C.c_void_p), ("perm_src", C.c_void_p), ("inv", C.c_void_p),
-                ("hq", C.c_void_p), ("hsf", C.c_void_p), ("shq", C.c_void_p), ("shsf", C.c_void_p)]
+                ("hq", C.c_void_p), ("hsf", C.c_void_p), ("shq", C.c_void_p), ("shsf", C.c_void_p),
+                ("router_mode", C.c_int32), ("router_bias", C.c_void_p),
+                ("swiglu_clamp", C.c_int32), ("swiglu_limit", C.c_float)]
+
+ROUTER_MODES = {"softmax": 0, "sqrtsoftplus": 1}
 
 
 def lib():
@@ -70,6 +74,13 @@ def lib():
         L.orc_dequantize.argtypes = [C.c_void_p, C.c_void_p, C.c_float, C.c_int64, C.c_int64, C.c_void_p]
         L.orc_router.restype = None
         L.orc_router.argtypes = [C.c_void_p, C.c_int64, C.c_int, C.c_int, C.c_void_p, C.c_void_p]
+        L.orc_router_ex.restype = None
+        L.orc_router_ex.argtypes = [C.c_void_p, C.c_int64, C.c_int, C.c_int, C.c_int, C.c_void_p,
+                                    C.c_void_p, C.c_void_p]
+        L.orc_sqrt_softplus.restype = C.c_float
+        L.orc_sqrt_softplus.argtypes = [C.c_float]
+        L.orc_swiglu.restype = C.c_float
+        L.orc_swiglu.argtypes = [C.c_float, C.c_float, C.c_int, C.c_float]
         L.orc_plan.restype = None
         L.orc_plan.argtypes = [C.c_void_p, C.c_int64, C.c_int, C.c_int] + [C.c_void_p] * 4
         L.orc_moe_forward.restype = C.c_int
@@ -150,13 +161,28 @@ def dequantize(codes: np.ndarray, sf: np.ndarray, ts: float) -> np.ndarray:
 
 
 # ----------------------------------------------------------------------------- routing
-def router(logits: np.ndarray, k: int):
+def router(logits: np.ndarray, k: int, mode: str = "softmax", bias=None):
+    """Top-k routing.  mode "softmax": selection on the logits, softmax weights renormalised over
+    the k; "sqrtsoftplus": scores sqrt(softplus(logit)), selection on score + bias (bias [E] or
+    None), weights = chosen unbiased scores / their sum."""
     logits = np.ascontiguousarray(logits, np.float32)
     T, E = logits.shape
     ids = np.zeros((T, k), np.int32)
     w = np.zeros((T, k), np.float32)
-    lib().orc_router(_p(logits), T, E, k, _p(ids), _p(w))
+    b = None if bias is None else np.ascontiguousarray(bias, np.float32)
+    lib().orc_router_ex(_p(logits), T, E, k, ROUTER_MODES[mode], _p(b) if b is not None else None,
+                        _p(ids), _p(w))
     return ids, w
+
+
+def sqrt_softplus(x: float) -> float:
+    return float(lib().orc_sqrt_softplus(float(x)))
+
+
+def swiglu(g: float, u: float, limit=None) -> float:
+    """silu(g) * u, or silu(min(g, L)) * clamp(u, -L, L) with limit L."""
+    return float(lib().orc_swiglu(float(g), float(u), 0 if limit is None else 1,
+                                  0.0 if limit is None else float(limit)))
 
 
 def plan(ids: np.ndarray, E: int):
@@ -191,9 +217,11 @@ class QuantExpert:
 
 
 def moe_forward(xq, xsf, ts_a, logits, experts, k, ts_h=1.0, shared=None, bruteforce=False,
-                want_debug=False):
+                want_debug=False, router_mode="softmax", router_bias=None, swiglu_limit=None):
     """The layer on quantised activations.  ``experts`` is a list of length E whose entries are
-    QuantExpert or None (None only for experts no token routes to); ``shared`` a QuantExpert."""
+    QuantExpert or None (None only for experts no token routes to); ``shared`` a QuantExpert.
+    ``router_mode``/``router_bias``: see router(); ``swiglu_limit``: None for plain SwiGLU, else
+    the clamp limit L of silu(min(g, L)) * clamp(u, -L, L)."""
     xq = np.ascontiguousarray(xq, np.uint8)
     xsf = np.ascontiguousarray(xsf, np.uint8)
     logits = np.ascontiguousarray(logits, np.float32)
@@ -227,6 +255,11 @@ def moe_forward(xq, xsf, ts_a, logits, experts, k, ts_h=1.0, shared=None, brutef
     a.logits = _p(logits)
     a.experts = C.cast(table, C.c_void_p)
     a.y = _p(y)
+    a.router_mode = ROUTER_MODES[router_mode]
+    rb = None if router_bias is None else np.ascontiguousarray(router_bias, np.float32)
+    a.router_bias = _p(rb) if rb is not None else None
+    a.swiglu_clamp = 0 if swiglu_limit is None else 1
+    a.swiglu_limit = 0.0 if swiglu_limit is None else float(swiglu_limit)
     dbg = {}
     if want_debug and not bruteforce:
         dbg = dict(ids=np.zeros((T, k), np.int32), w=np.zeros((T, k), np.float32),

@@ -17,6 +17,13 @@
 //  * Router: softmax, top-k under the strict order (value, lower index on ties), weights
 //    renormalised over the k chosen in slot order: "vllm.cpp docs/STATUS.md", row "DeepSeek-V4-
 //    Flash decode ds4-gap - Lever 3 (route -> warp-topk)".
+//  * Router variant: score sqrt(softplus(logit)), a per-expert correction bias added for the
+//    selection only, the weights gathered from the unbiased scores: "vllm.cpp docs/STATUS.md",
+//    paragraph "W6 sqrtsoftplus + hash-routed MoE"; "nvfp4-megamoe-kernel ...", section "Dense
+//    Router (L3+)" (sqrt(softplus(X @ W_gate)) + e_bias, top-k selection).
+//  * Clamped SwiGLU silu(min(g, L)) * clamp(u, -L, L): "vllm.cpp docs/STATUS.md" (gate clamped
+//    max-only, up clamped both-sided; a limit of 0 zeroes the expert); L = 10 in "nvfp4-megamoe-
+//    kernel ...", section "Nvfp4MoE (Routed Experts)" (swiglu_limit=10.0).
 //  * SwiGLU silu(g)*u on FP32 accumulators in the GEMM1 epilogue: "nvfp4-megamoe-kernel ...",
 //    section "MoE kernel (FusedSwiGLUScaledGroupedGemmKernel)"; shared expert with weight 1:
 //    section "6. MoE (Mixture of Experts) / Nvfp4SharedExpert".
@@ -32,7 +39,10 @@
 //  * the intermediate h is requantised with a fixed tensor scale (default 1.0);
 //  * rows of one expert are ordered by ascending flat assignment index t*k + j (stable);
 //  * no rounding between stages: g, u, h, the down projection and the combine stay FP32 and the
-//    output is rounded once to BF16 (nearest even).
+//    output is rounded once to BF16 (nearest even);
+//  * softplus(x) = x for x > 20, log1p(exp(x)) otherwise (FP32); the variant router's weights are
+//    the chosen unbiased scores divided by their sum (summed in slot order), as the base router
+//    renormalises over the k chosen.
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
@@ -206,6 +216,46 @@ void orc_dequantize(const uint8_t* codes, const uint8_t* sf, float ts, int64_t r
 // Per token: k repeated arg-maxes of the raw logits under (value descending, index ascending);
 // w_j = exp(l_j - l_0) / sum_{i<k} exp(l_i - l_0), summed in slot order (softmax then renormalise
 // over the chosen k; softmax is monotone, so selecting on logits selects the same experts).
+void orc_router(const float* logits, int64_t T, int E, int k, int32_t* ids, float* w);
+
+float orc_sqrt_softplus(float x) {
+  const float sp = x > 20.0f ? x : std::log1p(std::exp(x));
+  return std::sqrt(sp);
+}
+
+// mode 0: orc_router.  mode 1: per token, s_e = sqrt(softplus(l_e)); k repeated arg-maxes of
+// s_e + bias_e (bias may be null: 0) under (value descending, index ascending); w_j = s_(e_j) /
+// sum_{i<k} s_(e_i), the sum in slot order.
+void orc_router_ex(const float* logits, int64_t T, int E, int k, int mode, const float* bias,
+                   int32_t* ids, float* w) {
+  if (mode == 0) {
+    orc_router(logits, T, E, k, ids, w);
+    return;
+  }
+  std::vector<char> taken(E);
+  std::vector<float> sc(E), sel(E);
+  for (int64_t t = 0; t < T; ++t) {
+    const float* l = logits + t * E;
+    for (int e = 0; e < E; ++e) {
+      sc[e] = orc_sqrt_softplus(l[e]);
+      sel[e] = sc[e] + (bias ? bias[e] : 0.0f);
+    }
+    std::fill(taken.begin(), taken.end(), 0);
+    float sum = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      int best = -1;
+      for (int e = 0; e < E; ++e) {
+        if (taken[e]) continue;
+        if (best < 0 || sel[e] > sel[best]) best = e;
+      }
+      taken[best] = 1;
+      ids[t * k + j] = best;
+      sum = sum + sc[best];
+    }
+    for (int j = 0; j < k; ++j) w[t * k + j] = sc[ids[t * k + j]] / sum;
+  }
+}
+
 void orc_router(const float* logits, int64_t T, int E, int k, int32_t* ids, float* w) {
   std::vector<char> taken(E);
   std::vector<float> ex(k);
@@ -282,19 +332,35 @@ typedef struct {
   uint8_t* hsf;       // [T*k, I/16]
   uint8_t* shq;       // [T, I_shared/2]  shared-expert rows
   uint8_t* shsf;      // [T, I_shared/16]
+  // variants (zero: the base layer)
+  int32_t router_mode;       // 0 softmax over logits, 1 sqrt(softplus) scores + selection bias
+  const float* router_bias;  // [E] or null (mode 1 only)
+  int32_t swiglu_clamp;      // 1: silu(min(g, L)) * clamp(u, -L, L)
+  float swiglu_limit;        // L
 } orc_moe_args;
+
+// h = silu(g) * u, with the optional clamp of gate (from above) and up (both sides) first.
+static inline float swiglu(float g, float u, int clamp, float L) {
+  if (clamp) {
+    g = std::min(g, L);
+    u = std::min(std::max(u, -L), L);
+  }
+  return (g / (1.0f + std::exp(-g))) * u;
+}
+
+float orc_swiglu(float g, float u, int clamp, float L) { return swiglu(g, u, clamp, L); }
 
 // GEMM1 + SwiGLU + requant + GEMM2 for one row: x_hat [H] -> d [H], writing h codes and scales.
 static void expert_row(const float* xr, const float* Wg, const float* Wu, const float* Wd, int H,
-                       int I, float ts_h, float* h, float* hhat, uint8_t* hq_row,
-                       uint8_t* hsf_row, float* d) {
+                       int I, float ts_h, int clamp, float L, float* h, float* hhat,
+                       uint8_t* hq_row, uint8_t* hsf_row, float* d) {
   for (int n = 0; n < I; ++n) {
     const float* wg = Wg + (int64_t)n * H;
     const float* wu = Wu + (int64_t)n * H;
     float g = 0.0f, u = 0.0f;
     for (int c = 0; c < H; ++c) g = g + xr[c] * wg[c];
     for (int c = 0; c < H; ++c) u = u + xr[c] * wu[c];
-    h[n] = (g / (1.0f + std::exp(-g))) * u;
+    h[n] = swiglu(g, u, clamp, L);
   }
   orc_quantize_f32(h, 1, I, ts_h, hq_row, hsf_row);
   orc_dequantize(hq_row, hsf_row, ts_h, 1, I, hhat);
@@ -324,7 +390,7 @@ int orc_moe_forward(const orc_moe_args* a) {
   if (T == 0) return 0;
   std::vector<int32_t> ids(R), counts(E), offsets(E + 1), perm_src(R), inv(R);
   std::vector<float> w(R);
-  orc_router(a->logits, T, E, k, ids.data(), w.data());
+  orc_router_ex(a->logits, T, E, k, a->router_mode, a->router_bias, ids.data(), w.data());
   orc_plan(ids.data(), T, E, k, counts.data(), offsets.data(), perm_src.data(), inv.data());
 
   std::vector<float> xhat((size_t)T * H);
@@ -338,8 +404,9 @@ int orc_moe_forward(const orc_moe_args* a) {
     dequant_expert(a->experts[e], H, I, Wg, Wu, Wd);
     for (int32_t p = offsets[e]; p < offsets[e + 1]; ++p) {
       const float* xr = xhat.data() + (int64_t)perm_src[p] * H;
-      expert_row(xr, Wg.data(), Wu.data(), Wd.data(), H, I, a->ts_h, h.data(), hhat.data(),
-                 hq_row.data(), hsf_row.data(), D.data() + (int64_t)p * H);
+      expert_row(xr, Wg.data(), Wu.data(), Wd.data(), H, I, a->ts_h, a->swiglu_clamp,
+                 a->swiglu_limit, h.data(), hhat.data(), hq_row.data(), hsf_row.data(),
+                 D.data() + (int64_t)p * H);
       if (a->hq) std::memcpy(a->hq + (int64_t)p * (I / 2), hq_row.data(), I / 2);
       if (a->hsf) std::memcpy(a->hsf + (int64_t)p * (I / 16), hsf_row.data(), I / 16);
     }
@@ -350,8 +417,9 @@ int orc_moe_forward(const orc_moe_args* a) {
     S.resize((size_t)T * H);
     dequant_expert(a->experts[E], H, Is, Wg, Wu, Wd);
     for (int64_t t = 0; t < T; ++t) {
-      expert_row(xhat.data() + t * H, Wg.data(), Wu.data(), Wd.data(), H, Is, a->ts_h, h.data(),
-                 hhat.data(), hq_row.data(), hsf_row.data(), S.data() + t * H);
+      expert_row(xhat.data() + t * H, Wg.data(), Wu.data(), Wd.data(), H, Is, a->ts_h,
+                 a->swiglu_clamp, a->swiglu_limit, h.data(), hhat.data(), hq_row.data(),
+                 hsf_row.data(), S.data() + t * H);
       if (a->shq) std::memcpy(a->shq + t * (Is / 2), hq_row.data(), Is / 2);
       if (a->shsf) std::memcpy(a->shsf + t * (Is / 16), hsf_row.data(), Is / 16);
     }
@@ -380,7 +448,7 @@ int orc_moe_forward_bruteforce(const orc_moe_args* a) {
   if (T == 0) return 0;
   std::vector<int32_t> ids(T * k);
   std::vector<float> w(T * k);
-  orc_router(a->logits, T, E, k, ids.data(), w.data());
+  orc_router_ex(a->logits, T, E, k, a->router_mode, a->router_bias, ids.data(), w.data());
   const int Imax = std::max(I, a->I_shared);
   std::vector<float> xr(H), h(Imax), hhat(Imax), d(H), acc(H);
   std::vector<uint8_t> hq_row(Imax / 2), hsf_row(Imax / 16);
@@ -395,7 +463,7 @@ int orc_moe_forward_bruteforce(const orc_moe_args* a) {
       float g = 0.0f, u = 0.0f;
       for (int c = 0; c < H; ++c) g = g + xr[c] * wval(ex, 0, n, c, H);
       for (int c = 0; c < H; ++c) u = u + xr[c] * wval(ex, 1, n, c, H);
-      h[n] = (g / (1.0f + std::exp(-g))) * u;
+      h[n] = swiglu(g, u, a->swiglu_clamp, a->swiglu_limit);
     }
     for (int b = 0; b < Ie / 16; ++b) {  // requantise block by block, then decode
       quant_block16(h.data() + b * 16, a->ts_h, hq_row.data() + b * 8, hsf_row.data() + b);
