@@ -33,6 +33,18 @@ import torch  # noqa: E402
 METRIC = "NVFP4 MoE tokens/s & eff. TFLOPS; % of HBM BW (decode) / FP4 peak (prefill)"
 UNIT = "tokens/s"
 FP4_PER_BF16 = 6.0     # nominal dense FP4 / BF16 tensor rate of the part (13.5 / 2.25 PFLOP/s)
+# Layer variants: "base" = softmax router + SwiGLU; "sqrtsoftplus_clamp" = sqrt(softplus) router
+# with a seeded per-expert selection bias (N(0, 0.3)) + SwiGLU clamped at L = 10.
+VARIANTS = {"base": dict(router="softmax", swiglu_limit=None),
+            "sqrtsoftplus_clamp": dict(router="sqrtsoftplus", swiglu_limit=10.0)}
+
+
+def variant_bias(cs, variant):
+    import numpy as np
+    if VARIANTS[variant]["router"] != "sqrtsoftplus":
+        return None
+    return (np.random.default_rng(1000 + cs.config_id).standard_normal(cs.experts) * 0.3
+            ).astype(np.float32)
 
 
 def parse():
@@ -46,6 +58,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", default=None,
                     help="comma-separated batch sizes replacing the workload's own list")
+    ap.add_argument("--variant", default="base", choices=list(VARIANTS),
+                    help="router / activation variant of the layer")
     ap.add_argument("--ref-budget-s", type=float, default=150.0,
                     help="wall-time budget of the reference arm's timed + warm-up steps")
     return ap.parse_args()
@@ -222,10 +236,13 @@ def oracle_inputs(cs, wg, wu, wd, sh, need):
     return experts, sho
 
 
-def oracle_call(cs, x_cpu, lg_np, experts, sho):
+def oracle_call(cs, x_cpu, lg_np, experts, sho, variant="base"):
     import oracle
     xq, xsf, ts, st = oracle.quantize_bf16(x_cpu)
-    return oracle.moe_forward(xq, xsf, ts, lg_np, experts, cs.top_k, shared=sho)
+    v = VARIANTS[variant]
+    return oracle.moe_forward(xq, xsf, ts, lg_np, experts, cs.top_k, shared=sho,
+                              router_mode=v["router"], router_bias=variant_bias(cs, variant),
+                              swiglu_limit=v["swiglu_limit"])
 
 
 # ----------------------------------------------------------------------------------------- ours
@@ -241,20 +258,28 @@ def run_ours(args, world, rank, local):
     has_shared = cs.has_shared
     Tmax = max(Ts)
     cfg = moe.make_config(cs.experts, cs.hidden, cs.inter, cs.top_k, shared_inter=cs.shared_inter,
-                          max_tokens=Tmax)
+                          max_tokens=Tmax, **VARIANTS[args.variant])
     wg, wu, wd = synth.gen_all_experts(cs, device=dev)
     sh = synth.gen_shared(cs, device=dev) if has_shared else None
     wbuf = moe.quantize_weights(cfg, wg, wu, wd, shared=sh)
+    if variant_bias(cs, args.variant) is not None:
+        moe.set_router_bias(cfg, wbuf, torch.from_numpy(variant_bias(cs, args.variant)))
     xs = {T: synth.gen_x(cs, T, device=dev, row0=1000 * i) for i, T in enumerate(Ts)}
     lgs = {T: synth.gen_logits(cs, T, device=dev, row0=1000 * i) for i, T in enumerate(Ts)}
     ws = torch.empty(moe.workspace_size(cfg, Tmax), dtype=torch.uint8, device=dev)
     ys = {T: torch.empty(T, cs.hidden, dtype=torch.bfloat16, device=dev) for T in Ts}
 
-    # touched experts per call (from the device plan, read once before timing)
-    touched = {}
-    for T in Ts:
-        out = moe.plan(lgs[T], cs.top_k)
-        touched[T] = int((out["counts"] > 0).sum().item())
+    # touched experts per call (read once before timing: the device plan for the base router, the
+    # oracle's router for the variant, whose selection moe_plan does not implement)
+    def route_ids(T):
+        if VARIANTS[args.variant]["router"] == "softmax":
+            return moe.plan(lgs[T], cs.top_k)["topk_ids"].cpu().numpy()
+        import oracle
+        ids, _ = oracle.router(lgs[T].cpu().numpy(), cs.top_k, VARIANTS[args.variant]["router"],
+                               variant_bias(cs, args.variant))
+        return ids
+
+    touched = {T: len(np.unique(route_ids(T))) for T in Ts}
     counters = {T: layer_counters(cs, T, touched[T], has_shared) for T in Ts}
     launches = {T: moe.run_kernel_count(cfg, T) for T in Ts}
 
@@ -417,14 +442,13 @@ def run_ours(args, world, rank, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         need = set()
         for T in Ts:
-            out = moe.plan(lgs[T], cs.top_k)
-            need.update(out["topk_ids"].cpu().numpy().reshape(-1).tolist())
+            need.update(route_ids(T).reshape(-1).tolist())
         experts, sho = oracle_inputs(cs, wg, wu, wd, sh, need)
         c_tok, c_s = 0, 0.0
         for T in Ts:
             xc, lc = xs[T].cpu(), lgs[T].cpu().numpy()
             t0 = time.perf_counter()
-            oracle_call(cs, xc, lc, experts, sho)
+            oracle_call(cs, xc, lc, experts, sho, args.variant)
             c_s += time.perf_counter() - t0
             c_tok += T
         cpu = {"value": c_tok / c_s, "unit": UNIT, "cores": 1, "kind": "oracle",
@@ -440,6 +464,7 @@ def run_ours(args, world, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4(e2m1+e4m3) mma, f32 acc",
         "data": "synthetic (seeded SplitMix64/Box-Muller), random-init weights",
         "config": {"workload": f"{args.workload}: {cs.description}", "tokens_per_step": Ts,
+                   "variant": {"name": args.variant, **VARIANTS[args.variant]},
                    "step": f"one moe_run call at T = tokens_per_step[step mod {len(Ts)}]",
                    "l2": "flushed (2x L2 write) before every call, outside the timed events",
                    "launch": ("CUDA graph replay of one moe_run per T (programmatic dependent "
@@ -482,14 +507,15 @@ def run_reference(args, world, rank, local):
     import oracle
     need = set()
     for T in Ts:
-        ids, _ = oracle.router(lgs[T], cs.top_k)
+        ids, _ = oracle.router(lgs[T], cs.top_k, VARIANTS[args.variant]["router"],
+                               variant_bias(cs, args.variant))
         need.update(ids.reshape(-1).tolist())
     experts, sho = oracle_inputs(cs, wg, wu, wd, sh, need)
     del wg, wu, wd
     # per-step token sample: one token per call costs about one expert-set decode; size the
     # sample so that warm-up + timed steps fit the budget
     t0 = time.perf_counter()
-    oracle_call(cs, xs[Ts[0]][:1], lgs[Ts[0]][:1], experts, sho)
+    oracle_call(cs, xs[Ts[0]][:1], lgs[Ts[0]][:1], experts, sho, args.variant)
     one = max(time.perf_counter() - t0, 1e-3)
     nsteps = args.warmup + args.steps
     per_step = args.ref_budget_s / max(nsteps, 1)
@@ -499,7 +525,7 @@ def run_reference(args, world, rank, local):
         T = Ts[i % len(Ts)]
         n = min(T, cap)
         t0 = time.perf_counter()
-        oracle_call(cs, xs[T][:n], lgs[T][:n], experts, sho)
+        oracle_call(cs, xs[T][:n], lgs[T][:n], experts, sho, args.variant)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             tok += n
@@ -511,6 +537,7 @@ def run_reference(args, world, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32 (host oracle)",
         "data": "synthetic (seeded SplitMix64/Box-Muller), random-init weights",
         "config": {"workload": f"{args.workload}: {cs.description}", "tokens_per_step": Ts,
+                   "variant": {"name": args.variant, **VARIANTS[args.variant]},
                    "token_sample_cap": cap},
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"per step the first min(T, {cap}) tokens of that step's call"},

@@ -69,8 +69,21 @@ typedef struct {
   int32_t shared_inter;  /* 0: no shared expert; otherwise its intermediate size (must equal I) */
   float h_tensor_scale;  /* fixed FP32 tensor scale used to requantise h (1.0 by default) */
   int32_t max_tokens;    /* largest T a workspace sized with moe_workspace_size must serve */
-  uint32_t flags;        /* reserved, must be 0 */
+  uint32_t flags;        /* MOE_FLAG_* variant bits below; 0 = the base layer */
+  float swiglu_limit;    /* L of MOE_FLAG_SWIGLU_CLAMP: finite, >= 0 */
 } moe_config;
+
+/* Router variant ("vllm.cpp docs/STATUS.md", paragraph "W6 sqrtsoftplus + hash-routed MoE";
+ * "nvfp4-megamoe-kernel compare pre-b1...master", section "Dense Router (L3+)"): expert scores
+ * s_e = sqrt(softplus(logit_e)) (softplus(x) = x above 20), top-k selection on s_e + bias_e (the
+ * per-expert correction bias set with moe_set_router_bias; zero by default), weights
+ * w_j = s_(e_j) / sum of the k chosen s (in slot order).  Without the flag: top-k of the logits,
+ * softmax renormalised over the k. */
+#define MOE_FLAG_ROUTER_SQRTSOFTPLUS 1u
+/* Activation variant (same paragraph; "nvfp4-megamoe-kernel ...", section "Nvfp4MoE (Routed
+ * Experts)", swiglu_limit = 10): h = silu(min(g, L)) * clamp(u, -L, L); L = 0 zeroes every
+ * expert.  Without the flag: h = silu(g) * u. */
+#define MOE_FLAG_SWIGLU_CLAMP 2u
 
 /* Optional device buffers that receive the layer's intermediates (any field may be NULL). */
 typedef struct {
@@ -117,6 +130,12 @@ size_t moe_weights_size(const moe_config* cfg);
 int moe_quantize_weights(const moe_config* cfg, const void* w_gate, const void* w_up,
                          const void* w_down, const void* s_gate, const void* s_up,
                          const void* s_down, void* wbuf, size_t wbuf_bytes, moe_stream_t stream);
+
+/* Stores the router's per-expert selection bias (bias: device FP32 [E], copied) into wbuf, where
+ * MOE_FLAG_ROUTER_SQRTSOFTPLUS layers read it; moe_quantize_weights leaves it zero.  The bias
+ * only changes which experts are chosen, never their weights.  MOE_ERR_INVALID_ARG on null
+ * pointers. */
+int moe_set_router_bias(const moe_config* cfg, void* wbuf, const float* bias, moe_stream_t stream);
 
 /* Copies one expert matrix back out of wbuf in canonical layout.  expert: 0..E-1, or -1 for the
  * shared expert; matrix: 0 gate [I,H], 1 up [I,H], 2 down [H,I].  codes [N, K/2], sf [N, K/16]

@@ -23,13 +23,14 @@ STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED_SHAPE
 EXPORTED = ["moe_status_string", "moe_config_check", "moe_weights_size", "moe_quantize_weights",
             "moe_weights_export", "moe_act_workspace_size", "moe_quantize_act",
             "moe_plan_workspace_size", "moe_plan", "moe_workspace_size", "moe_run",
-            "moe_last_device_status", "moe_plan_static", "moe_run_kernel_count"]
+            "moe_last_device_status", "moe_plan_static", "moe_run_kernel_count",
+            "moe_set_router_bias"]
 
 
 class MoeConfig(C.Structure):
     _fields_ = [("num_experts", C.c_int32), ("hidden", C.c_int32), ("inter", C.c_int32),
                 ("top_k", C.c_int32), ("shared_inter", C.c_int32), ("h_tensor_scale", C.c_float),
-                ("max_tokens", C.c_int32), ("flags", C.c_uint32)]
+                ("max_tokens", C.c_int32), ("flags", C.c_uint32), ("swiglu_limit", C.c_float)]
 
     def __repr__(self):
         return (f"MoeConfig(E={self.num_experts}, H={self.hidden}, I={self.inter}, k={self.top_k}, "
@@ -74,6 +75,7 @@ def lib():
             "moe_last_device_status": (C.c_int, [vp, C.POINTER(C.c_int32)]),
             "moe_plan_static": (C.c_int, [vp, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]),
             "moe_run_kernel_count": (C.c_int, [cfgp, i32]),
+            "moe_set_router_bias": (C.c_int, [cfgp, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -101,9 +103,22 @@ def _stream(stream=None):
     return C.c_void_p(s.cuda_stream)
 
 
+FLAG_ROUTER_SQRTSOFTPLUS = 1
+FLAG_SWIGLU_CLAMP = 2
+
+
 def make_config(num_experts, hidden, inter, top_k, shared_inter=0, h_tensor_scale=1.0,
-                max_tokens=0) -> MoeConfig:
-    return MoeConfig(num_experts, hidden, inter, top_k, shared_inter, h_tensor_scale, max_tokens, 0)
+                max_tokens=0, router="softmax", swiglu_limit=None) -> MoeConfig:
+    """router: "softmax" (top-k of the logits, softmax over the k) or "sqrtsoftplus" (scores
+    sqrt(softplus(logit)), selection on score + the bias set by set_router_bias, weights the
+    normalised unbiased scores); swiglu_limit: None for silu(g)*u, else L of
+    silu(min(g, L)) * clamp(u, -L, L)."""
+    if router not in ("softmax", "sqrtsoftplus"):
+        raise ValueError(f"unknown router {router!r}")
+    flags = (FLAG_ROUTER_SQRTSOFTPLUS if router == "sqrtsoftplus" else 0) | \
+        (FLAG_SWIGLU_CLAMP if swiglu_limit is not None else 0)
+    return MoeConfig(num_experts, hidden, inter, top_k, shared_inter, h_tensor_scale, max_tokens,
+                     flags, 0.0 if swiglu_limit is None else float(swiglu_limit))
 
 
 def config_check(cfg: MoeConfig) -> int:
@@ -126,6 +141,16 @@ def quantize_weights(cfg: MoeConfig, w_gate, w_up, w_down, shared=None, wbuf=Non
                                       _ptr(sg), _ptr(su), _ptr(sd), _ptr(wbuf), wbuf.numel(),
                                       _stream(stream)), "moe_quantize_weights")
     return wbuf
+
+
+def set_router_bias(cfg: MoeConfig, wbuf: torch.Tensor, bias: torch.Tensor) -> None:
+    """Stores the sqrt-softplus router's per-expert selection bias (FP32 [E]) in wbuf."""
+    bias = bias.to(device=wbuf.device, dtype=torch.float32).contiguous()
+    if bias.numel() != cfg.num_experts:
+        raise ValueError("bias must have num_experts entries")
+    _check(lib().moe_set_router_bias(C.byref(cfg), _ptr(wbuf), _ptr(bias), _stream()),
+           "moe_set_router_bias")
+    torch.cuda.current_stream().synchronize()
 
 
 def weights_export(cfg: MoeConfig, wbuf, expert: int, matrix: int, stream=None):

@@ -15,7 +15,10 @@ inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 
 int check_cfg(const moe_config* c) {
   if (!c) return MOE_ERR_INVALID_ARG;
-  if (c->flags != 0u) return MOE_ERR_INVALID_ARG;
+  if ((c->flags & ~(MOE_FLAG_ROUTER_SQRTSOFTPLUS | MOE_FLAG_SWIGLU_CLAMP)) != 0u)
+    return MOE_ERR_INVALID_ARG;
+  if ((c->flags & MOE_FLAG_SWIGLU_CLAMP) && !(std::isfinite(c->swiglu_limit) && c->swiglu_limit >= 0.0f))
+    return MOE_ERR_INVALID_ARG;
   if (c->num_experts < 1 || c->top_k < 1 || c->hidden <= 0 || c->inter <= 0 || c->max_tokens < 0)
     return MOE_ERR_INVALID_ARG;
   if (c->top_k > c->num_experts) return MOE_ERR_INVALID_ARG;
@@ -69,8 +72,20 @@ int moe_quantize_weights(const moe_config* cfg, const void* w_gate, const void* 
   if (!aligned(wbuf, kAlign)) return MOE_ERR_INVALID_ARG;
   const WeightLayout L(*cfg);
   if (wbuf_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  return cuda_status(launch_weight_quant(*cfg, L, w_gate, w_up, w_down, s_gate, s_up, s_down,
-                                         static_cast<uint8_t*>(wbuf), to_cuda(stream)));
+  cudaStream_t s = to_cuda(stream);
+  uint8_t* wb = static_cast<uint8_t*>(wbuf);
+  if (cudaMemsetAsync(wb + L.bias, 0, sizeof(float) * L.E, s) != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_status(launch_weight_quant(*cfg, L, w_gate, w_up, w_down, s_gate, s_up, s_down, wb, s));
+}
+
+int moe_set_router_bias(const moe_config* cfg, void* wbuf, const float* bias, moe_stream_t stream) {
+  int st = check_cfg(cfg);
+  if (st != MOE_OK) return st;
+  if (!wbuf || !bias || !aligned(wbuf, kAlign)) return MOE_ERR_INVALID_ARG;
+  const WeightLayout L(*cfg);
+  return cuda_status(cudaMemcpyAsync(static_cast<uint8_t*>(wbuf) + L.bias, bias,
+                                     sizeof(float) * L.E, cudaMemcpyDeviceToDevice,
+                                     to_cuda(stream)));
 }
 
 int moe_weights_export(const moe_config* cfg, const void* wbuf, int32_t expert, int32_t matrix,
@@ -202,6 +217,8 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws + L.hdr);
   const int E = cfg->num_experts, H = cfg->hidden, I = cfg->inter;
   const int shared = cfg->shared_inter > 0 ? 1 : 0;
+  const int sqrtsp = (cfg->flags & MOE_FLAG_ROUTER_SQRTSOFTPLUS) ? 1 : 0;
+  const float* rbias = reinterpret_cast<const float*>(wb + W.bias);
 
   auto i32 = [&](size_t off) { return reinterpret_cast<int32_t*>(ws + off); };
   auto f32 = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
@@ -246,6 +263,8 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
     pr.perm_w = f32(L.perm_w);
     pr.inv = i32(L.inv);
     pr.perm_seg = i32(L.perm_seg);
+    pr.sqrtsp = sqrtsp;
+    pr.bias = rbias;
     e = launch_decode_prologue(pr, s);
     if (e == cudaSuccess) e = mark(1);
     if (e == cudaSuccess) e = mark(2);
@@ -273,6 +292,8 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
     pr.perm_w = f32(L.perm_w);
     pr.inv = i32(L.inv);
     pr.perm_seg = i32(L.perm_seg);
+    pr.sqrtsp = sqrtsp;
+    pr.bias = rbias;
     e = launch_prologue_small(pr, s);
     if (e == cudaSuccess) e = mark(1);
     if (e == cudaSuccess) e = mark(2);
@@ -307,6 +328,8 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
   pa.hist = i32(L.hist);
   pa.base = i32(L.base);
   pa.status = &hdr->status;
+  pa.sqrtsp = sqrtsp;
+  pa.bias = rbias;
   e = launch_plan(pa, s);
   if (e == cudaSuccess) e = mark(2);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
@@ -348,6 +371,8 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
   g.hq = ws + L.hq;
   g.hsf = ws + L.hsf;
   g.status = &hdr->status;
+  g.swiglu_clamp = (cfg->flags & MOE_FLAG_SWIGLU_CLAMP) ? 1 : 0;
+  g.swiglu_limit = cfg->swiglu_limit;
   // decode-sized batches: every expert has at most T <= kDecodeMaxRows rows, one tile each
   const bool decode = L.decode;
   g.a_codes = ws + L.xq_perm;            // expert-ordered activations, read by TMA boxes

@@ -304,8 +304,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (valid) {
             float h[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              h[i] = silu_mul(__uint_as_float(v[i]) * ag, __uint_as_float(v[16 + i]) * au);
+            for (int i = 0; i < 16; ++i) {
+              float g = __uint_as_float(v[i]) * ag, u = __uint_as_float(v[16 + i]) * au;
+              if (p.swiglu_clamp) {   // gate clamped from above, up on both sides
+                g = fminf(g, p.swiglu_limit);
+                u = fminf(fmaxf(u, -p.swiglu_limit), p.swiglu_limit);
+              }
+              h[i] = silu_mul(g, u);
+            }
             uint32_t lo, hi, s;
             quant_block16_fast(h, p.ts_h, inv_ts_h, lo, hi, s);
             const int f0 = t.nt * (kBN / 2) + c * 16;

@@ -319,10 +319,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float x0 = __shfl_xor_sync(0xffffffffu, a0, 16);
             const float x1 = __shfl_xor_sync(0xffffffffu, a1, 16);
             // the lower half-warp takes token cb+n, the upper half token cb+n+1
-            const float g = lo_half ? a0 : x1;
-            const float u = lo_half ? x0 : a1;
+            float g = (lo_half ? a0 : x1) * ag;
+            float u = (lo_half ? x0 : a1) * au;
             const int col = cb + n + (lo_half ? 0 : 1);
-            const float h = silu_mul(g * ag, u * au);
+            if (p.swiglu_clamp) {   // gate clamped from above, up on both sides
+              g = fminf(g, p.swiglu_limit);
+              u = fminf(fmaxf(u, -p.swiglu_limit), p.swiglu_limit);
+            }
+            const float h = silu_mul(g, u);
             float bamax = fabsf(h);
 #pragma unroll
             for (int o = 8; o > 0; o >>= 1) bamax = fmaxf(bamax, __shfl_xor_sync(0xffffffffu, bamax, o));

@@ -35,7 +35,8 @@ inline int plan_tokens_per_chunk(int k) { return k <= 16 ? 64 : 32; }
 //   w13 [Et][2I/128][H/256][18432]: GEMM1 rows interleaved by 16 (rows 32b+i are gate rows
 //       16b+i for i < 16, up rows 16b+i-16 otherwise);
 //   w2  [Et][H/128][I/256][18432]: GEMM2 (down) rows;
-//   ts  [Et][4] FP32: gate, up, down tensor scales (the 4th is padding).
+//   ts  [Et][4] FP32: gate, up, down tensor scales (the 4th is padding);
+//   bias [E] FP32: the variant router's per-expert selection bias (zero unless set).
 // Et = E + 1 with a shared expert, which is stored last.
 constexpr int kTileBytes = 128 * 128;             // codes of one (N tile, K stage) block
 constexpr int kTileSfBytes = 4 * 512;             // its scales
@@ -43,7 +44,7 @@ constexpr int kTileBlockBytes = kTileBytes + kTileSfBytes;
 
 struct WeightLayout {
   int E, Et, H, I;
-  size_t w13, w2, ts, total;
+  size_t w13, w2, ts, bias, total;
   size_t w13_per_e, w2_per_e;
   explicit WeightLayout(const moe_config& c) {
     E = c.num_experts;
@@ -56,6 +57,7 @@ struct WeightLayout {
     w13 = o; o = align_up(o + w13_per_e * Et);
     w2 = o;  o = align_up(o + w2_per_e * Et);
     ts = o;  o = align_up(o + sizeof(float) * 4 * Et);
+    bias = o; o = align_up(o + sizeof(float) * E);   // router selection bias (variant router)
     total = o;
   }
 };
@@ -177,6 +179,8 @@ struct PlanArgs {
   int32_t* hist;          // [nchunks*E + 1 + E] scratch: histograms, scan block count, totals
   int32_t* base;          // [nchunks*E] scratch
   int32_t* status;
+  int sqrtsp;             // 1: the variant router (sqrt-softplus scores + selection bias)
+  const float* bias;      // [E] selection bias of the variant router (may be null)
 };
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s);
 
@@ -207,6 +211,8 @@ struct GemmArgs {
   const float* perm_w;      // mode 1
   float* yacc;              // mode 1 out [T, N]
   float* obuf;              // mode 2 out [rows, N]
+  int swiglu_clamp;         // mode 0: h = silu(min(g, L)) * clamp(u, -L, L) with L = swiglu_limit
+  float swiglu_limit;
   int plan_early;           // decode kernel: the plan is complete at launch (written two kernels
                             // back), only the previous kernel's output needs the wait
   int32_t* status;
@@ -254,6 +260,8 @@ struct PrologueArgs {
   int E, k, shared_rows;
   int32_t *ids, *counts, *offsets, *tile_start, *perm_src, *inv, *perm_seg;
   float *w, *perm_w;
+  int sqrtsp;              // the variant router (see PlanArgs)
+  const float* bias;
 };
 cudaError_t launch_prologue_small(const PrologueArgs& a, cudaStream_t s);
 
@@ -272,6 +280,8 @@ struct DecodePrologueArgs {
   int E, k, shared_rows;
   int32_t *ids, *counts, *offsets, *tile_start, *perm_src, *inv, *perm_seg;
   float *w, *perm_w;
+  int sqrtsp;              // the variant router (see PlanArgs)
+  const float* bias;
 };
 cudaError_t launch_decode_prologue(const DecodePrologueArgs& a, cudaStream_t s);
 

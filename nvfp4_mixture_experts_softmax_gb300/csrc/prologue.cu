@@ -36,7 +36,8 @@ __global__ void __launch_bounds__(kSmallPlanThreads) prologue_small_kernel(const
   for (int64_t b = threadIdx.x; b < nblk; b += blockDim.x)
     encode_bf16_block16(x, b, ts, reinterpret_cast<uint2*>(a.xq), a.xsf);
   small_plan_body<VPL>(a.logits, a.T, a.E, a.k, a.shared_rows, a.ids, a.w, a.counts, a.offsets,
-                       a.tile_start, a.perm_src, a.perm_w, a.inv, s_dyn, a.perm_seg);
+                       a.tile_start, a.perm_src, a.perm_w, a.inv, s_dyn, a.perm_seg, a.sqrtsp,
+                       a.bias);
 }
 
 // Decode batches (T <= kDecodeMaxRows): a cluster of kDecodeProCtas CTAs in two phases around
@@ -87,8 +88,8 @@ __global__ void __launch_bounds__(kSmallPlanThreads) decode_prologue_kernel(cons
   for (int t = (int)rank * nw + warp; t < a.T; t += kDecodeProCtas * nw) {
     int my_id;
     float my_l;
-    warp_topk<VPL>(a.logits + (int64_t)t * a.E, a.E, a.k, lane, my_id, my_l);
-    const float w = topk_weight(my_l, a.k, lane);
+    warp_topk<VPL>(a.logits + (int64_t)t * a.E, a.E, a.k, lane, my_id, my_l, a.sqrtsp, a.bias);
+    const float w = topk_weight(my_l, a.k, lane, a.sqrtsp);
     if (lane < a.k) {
       a.ids[(int64_t)t * a.k + lane] = my_id;
       a.w[(int64_t)t * a.k + lane] = w;

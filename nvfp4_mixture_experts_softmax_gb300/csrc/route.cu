@@ -32,7 +32,8 @@ constexpr int kRouterWarps = 8;
 template <int VPL>
 __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(
     const float* __restrict__ logits, int T, int E, int k, int tpc, int32_t* __restrict__ ids,
-    float* __restrict__ wout, int32_t* __restrict__ hist) {
+    float* __restrict__ wout, int32_t* __restrict__ hist, int sqrtsp,
+    const float* __restrict__ bias) {
   griddep_wait();
   griddep_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -40,8 +41,8 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(
   if (t >= T) return;
   int my_id;
   float my_l;
-  warp_topk<VPL>(logits + (int64_t)t * E, E, k, lane, my_id, my_l);
-  const float w = topk_weight(my_l, k, lane);
+  warp_topk<VPL>(logits + (int64_t)t * E, E, k, lane, my_id, my_l, sqrtsp, bias);
+  const float w = topk_weight(my_l, k, lane, sqrtsp);
   if (lane < k) {
     ids[(int64_t)t * k + lane] = my_id;
     wout[(int64_t)t * k + lane] = w;
@@ -55,12 +56,12 @@ __global__ void __launch_bounds__(kSmallPlanThreads) plan_small_kernel(
     int32_t* __restrict__ ids, float* __restrict__ wout, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ tile_start,
     int32_t* __restrict__ perm_src, float* __restrict__ perm_w, int32_t* __restrict__ inv,
-    int32_t* __restrict__ perm_seg) {
+    int32_t* __restrict__ perm_seg, int sqrtsp, const float* __restrict__ bias) {
   extern __shared__ __align__(16) uint8_t s_dyn[];
   griddep_wait();
   griddep_launch();
   small_plan_body<VPL>(logits, T, E, k, shared_rows, ids, wout, counts, offsets, tile_start,
-                       perm_src, perm_w, inv, s_dyn, perm_seg);
+                       perm_src, perm_w, inv, s_dyn, perm_seg, sqrtsp, bias);
 }
 
 // Per-chunk bases and per-expert offsets from the chunk histograms, spread over blocks of 32
@@ -187,7 +188,7 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s) {
                            (int)smem);                                                          \
     cudaError_t le = launch_pdl(plan_small_kernel<V>, dim3(1), dim3(kSmallPlanThreads), smem, s,  \
         a.logits, a.T, a.E, a.k, a.shared_rows, a.ids, a.w, a.counts, a.offsets, a.tile_start, \
-        a.perm_src, a.perm_w, a.inv, a.perm_seg);                                               \
+        a.perm_src, a.perm_w, a.inv, a.perm_seg, a.sqrtsp, a.bias);                             \
     if (le != cudaSuccess) return le;                                                           \
   } while (0)
     if (vpl <= 1) NVFP4MOE_SMALL(1);
@@ -205,7 +206,7 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s) {
   const int rblocks = (a.T + kRouterWarps - 1) / kRouterWarps;
 #define NVFP4MOE_ROUTER(V)                                                                 \
   err = launch_pdl(router_kernel<V>, dim3(rblocks), dim3(kRouterWarps * 32), 0, s, a.logits, a.T, \
-                   a.E, a.k, tpc, a.ids, a.w, a.hist)
+                   a.E, a.k, tpc, a.ids, a.w, a.hist, a.sqrtsp, a.bias)
   if (vpl <= 1) NVFP4MOE_ROUTER(1);
   else if (vpl <= 2) NVFP4MOE_ROUTER(2);
   else if (vpl <= 4) NVFP4MOE_ROUTER(4);

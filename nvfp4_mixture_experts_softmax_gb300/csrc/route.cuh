@@ -44,13 +44,21 @@ __device__ __forceinline__ uint32_t order_key(float v) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// The variant router's expert score sqrt(softplus(x)), softplus(x) = x above 20.
+__device__ __forceinline__ float sqrt_softplus(float x) {
+  return sqrtf(x > 20.0f ? x : log1pf(expf(x)));
+}
+
 // Top-k of one token's logits by one warp: lane l holds experts l, l+32, ...  Each of the k
 // rounds takes the warp maximum of the lanes' best keys, then the lowest expert index among the
 // lanes holding it (hardware redux.sync), so ties go to the lower index.  Lane j < k ends with
-// the j-th choice (my_id, my_l).
+// the j-th choice (my_id, my_l).  sqrtsp: the keys are sqrt(softplus(logit)) + bias[e] (bias may
+// be null) and my_l is the unbiased score sqrt(softplus(logit)); otherwise keys and my_l are the
+// logits.
 template <int VPL>
 __device__ __forceinline__ void warp_topk(const float* __restrict__ row, int E, int k, int lane,
-                                          int& my_id, float& my_l) {
+                                          int& my_id, float& my_l, int sqrtsp = 0,
+                                          const float* __restrict__ bias = nullptr) {
   float v[VPL];
   uint32_t key[VPL];
   uint32_t taken = 0;
@@ -58,8 +66,14 @@ __device__ __forceinline__ void warp_topk(const float* __restrict__ row, int E, 
   for (int i = 0; i < VPL; ++i) {
     const int e = lane + 32 * i;
     if (e < E) {
-      v[i] = __ldg(row + e);
-      key[i] = order_key(v[i]);
+      const float l = __ldg(row + e);
+      if (sqrtsp) {
+        v[i] = sqrt_softplus(l);
+        key[i] = order_key(v[i] + (bias ? __ldg(bias + e) : 0.0f));
+      } else {
+        v[i] = l;
+        key[i] = order_key(l);
+      }
     } else {
       v[i] = 0.0f;
       key[i] = 0u;
@@ -86,7 +100,13 @@ __device__ __forceinline__ void warp_topk(const float* __restrict__ row, int E, 
 }
 
 // Renormalised softmax weights of the k chosen logits, summed in slot order; lanes < k write.
-__device__ __forceinline__ float topk_weight(float my_l, int k, int lane) {
+// sqrtsp: the chosen (unbiased) scores divided by their sum, summed in slot order.
+__device__ __forceinline__ float topk_weight(float my_l, int k, int lane, int sqrtsp = 0) {
+  if (sqrtsp) {
+    float sum = 0.0f;
+    for (int j = 0; j < k; ++j) sum = sum + __shfl_sync(0xffffffffu, my_l, j);
+    return __fdiv_rn(my_l, sum);
+  }
   const float l0 = __shfl_sync(0xffffffffu, my_l, 0);
   const float ex = lane < k ? expf(my_l - l0) : 0.0f;
   float sum = 0.0f;
@@ -192,7 +212,8 @@ __device__ __forceinline__ void small_plan_body(
     int32_t* __restrict__ ids, float* __restrict__ wout, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ tile_start,
     int32_t* __restrict__ perm_src, float* __restrict__ perm_w, int32_t* __restrict__ inv,
-    uint8_t* dyn, int32_t* __restrict__ perm_seg = nullptr) {
+    uint8_t* dyn, int32_t* __restrict__ perm_seg = nullptr, int sqrtsp = 0,
+    const float* __restrict__ bias = nullptr) {
   int32_t* s_cnt = reinterpret_cast<int32_t*>(dyn);
   int32_t* s_ids = s_cnt + 3 * E;
   float* s_w = reinterpret_cast<float*>(s_ids + kSmallPlanRows);
@@ -203,8 +224,8 @@ __device__ __forceinline__ void small_plan_body(
   for (int t = warp; t < T; t += nw) {
     int my_id;
     float my_l;
-    warp_topk<VPL>(logits + (int64_t)t * E, E, k, lane, my_id, my_l);
-    const float w = topk_weight(my_l, k, lane);
+    warp_topk<VPL>(logits + (int64_t)t * E, E, k, lane, my_id, my_l, sqrtsp, bias);
+    const float w = topk_weight(my_l, k, lane, sqrtsp);
     if (lane < k) {
       ids[(int64_t)t * k + lane] = my_id;
       wout[(int64_t)t * k + lane] = w;

@@ -55,6 +55,11 @@ def test_status_strings(moe):
     (dict(num_experts=8, hidden=256, inter=512, top_k=2, shared_inter=256), -2),
     (dict(num_experts=8, hidden=256, inter=512, top_k=2, h_tensor_scale=0.0), -1),
     (dict(num_experts=8, hidden=256, inter=512, top_k=2, h_tensor_scale=float("nan")), -1),
+    (dict(num_experts=8, hidden=256, inter=512, top_k=2, router="sqrtsoftplus"), 0),
+    (dict(num_experts=8, hidden=256, inter=512, top_k=2, swiglu_limit=10.0), 0),
+    (dict(num_experts=8, hidden=256, inter=512, top_k=2, swiglu_limit=0.0), 0),
+    (dict(num_experts=8, hidden=256, inter=512, top_k=2, swiglu_limit=-1.0), -1),
+    (dict(num_experts=8, hidden=256, inter=512, top_k=2, swiglu_limit=float("inf")), -1),
 ])
 def test_config_check(moe, kw, want):
     assert moe.config_check(moe.make_config(**kw)) == want
@@ -104,3 +109,14 @@ def test_run_kernel_count(moe):
         moe.run_kernel_count(dec, -1)
     with pytest.raises(RuntimeError):
         moe.run_kernel_count(moe.make_config(8, 200, 512, 2), 4)
+
+
+def test_variant_flags_and_bias_rejections(moe):
+    cfg = moe.make_config(8, 256, 512, 2)
+    cfg.flags = 4                                  # not a defined variant bit
+    assert moe.config_check(cfg) == -1
+    L = moe.lib()
+    ok = moe.make_config(8, 256, 512, 2, router="sqrtsoftplus")
+    assert L.moe_set_router_bias(C.byref(ok), None, None, None) == -1
+    with pytest.raises(ValueError):
+        moe.make_config(8, 256, 512, 2, router="sigmoid")
