@@ -39,6 +39,22 @@ VARIANTS = {"base": dict(router="softmax", swiglu_limit=None),
             "sqrtsoftplus_clamp": dict(router="sqrtsoftplus", swiglu_limit=10.0)}
 
 
+def sharing_level(args):
+    if not args.routing:
+        return None
+    if not args.routing.startswith("shared_") or not args.routing[7:].isdigit():
+        raise SystemExit(f"--routing wants shared_<percent>, got {args.routing!r}")
+    return int(args.routing[7:])
+
+
+def gen_router_logits(args, cs, T, i, dev):
+    import synth
+    share = sharing_level(args)
+    if share is None:
+        return synth.gen_logits(cs, T, device=dev, row0=1000 * i)
+    return synth.gen_sharing_logits(cs, T, share, device=dev)
+
+
 def variant_bias(cs, variant):
     import numpy as np
     if VARIANTS[variant]["router"] != "sqrtsoftplus":
@@ -60,6 +76,9 @@ def parse():
                     help="comma-separated batch sizes replacing the workload's own list")
     ap.add_argument("--variant", default="base", choices=list(VARIANTS),
                     help="router / activation variant of the layer")
+    ap.add_argument("--routing", default=None,
+                    help="shared_<p> (p in 0..100): the expert-sharing decode workload, whose "
+                         "batches reuse p%% of their token/expert assignments")
     ap.add_argument("--ref-budget-s", type=float, default=150.0,
                     help="wall-time budget of the reference arm's timed + warm-up steps")
     return ap.parse_args()
@@ -265,7 +284,7 @@ def run_ours(args, world, rank, local):
     if variant_bias(cs, args.variant) is not None:
         moe.set_router_bias(cfg, wbuf, torch.from_numpy(variant_bias(cs, args.variant)))
     xs = {T: synth.gen_x(cs, T, device=dev, row0=1000 * i) for i, T in enumerate(Ts)}
-    lgs = {T: synth.gen_logits(cs, T, device=dev, row0=1000 * i) for i, T in enumerate(Ts)}
+    lgs = {T: gen_router_logits(args, cs, T, i, dev) for i, T in enumerate(Ts)}
     ws = torch.empty(moe.workspace_size(cfg, Tmax), dtype=torch.uint8, device=dev)
     ys = {T: torch.empty(T, cs.hidden, dtype=torch.bfloat16, device=dev) for T in Ts}
 
@@ -280,6 +299,8 @@ def run_ours(args, world, rank, local):
         return ids
 
     touched = {T: len(np.unique(route_ids(T))) for T in Ts}
+    rows_per_expert = {T: sorted(np.unique(route_ids(T), return_counts=True)[1].tolist(),
+                                 reverse=True) for T in Ts}
     counters = {T: layer_counters(cs, T, touched[T], has_shared) for T in Ts}
     launches = {T: moe.run_kernel_count(cfg, T) for T in Ts}
 
@@ -465,6 +486,7 @@ def run_ours(args, world, rank, local):
         "data": "synthetic (seeded SplitMix64/Box-Muller), random-init weights",
         "config": {"workload": f"{args.workload}: {cs.description}", "tokens_per_step": Ts,
                    "variant": {"name": args.variant, **VARIANTS[args.variant]},
+                   "routing": args.routing or "iid",
                    "step": f"one moe_run call at T = tokens_per_step[step mod {len(Ts)}]",
                    "l2": "flushed (2x L2 write) before every call, outside the timed events",
                    "launch": ("CUDA graph replay of one moe_run per T (programmatic dependent "
@@ -477,6 +499,9 @@ def run_ours(args, world, rank, local):
         "layer_hbm_frac": round(layer_gbs / hbm_peak, 4),
         "per_T_us": {str(T): round(statistics.median(v) * 1e3, 2) for T, v in per_T_ms.items()},
         "touched_experts": {str(T): touched[T] for T in Ts},
+        "routing": {"workload": args.routing or "iid N(0,1) logits",
+                    "rows_per_expert": {str(T): rows_per_expert[T] for T in Ts},
+                    "useful_weight_bytes": {str(T): touched[T] * expert_bytes(cs) for T in Ts}},
         "stage_share": {n: round(v / sum(stage_ms.values()), 4) for n, v in stage_ms.items()},
         "fp4_peak_frac": round(eff_tflops / (bf16_peak * FP4_PER_BF16), 4),
         "roofline": dict(kernel=f"{dominant} (T={Tr} launches)", **roof,
@@ -503,7 +528,7 @@ def run_reference(args, world, rank, local):
     wg, wu, wd = synth.gen_all_experts(cs, device=dev)
     sh = synth.gen_shared(cs, device=dev) if cs.has_shared else None
     xs = {T: synth.gen_x(cs, T, device=dev, row0=1000 * i).cpu() for i, T in enumerate(Ts)}
-    lgs = {T: synth.gen_logits(cs, T, device=dev, row0=1000 * i).cpu().numpy() for i, T in enumerate(Ts)}
+    lgs = {T: gen_router_logits(args, cs, T, i, dev).cpu().numpy() for i, T in enumerate(Ts)}
     import oracle
     need = set()
     for T in Ts:

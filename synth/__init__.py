@@ -85,7 +85,7 @@ def normal(key: int, start: int, count: int, device="cpu") -> torch.Tensor:
 
 
 # tensor ids inside one configuration's stream family
-T_X, T_LOGITS, T_GATE, T_UP, T_DOWN, T_SGATE, T_SUP, T_SDOWN, T_ZIPF_RANK = range(9)
+T_X, T_LOGITS, T_GATE, T_UP, T_DOWN, T_SGATE, T_SUP, T_SDOWN, T_ZIPF_RANK, T_SHARE_POOL = range(10)
 
 
 @dataclass(frozen=True)
@@ -161,6 +161,35 @@ def gen_logits(cfg: MoeConfig, T: int, device="cpu", row0: int = 0, beta=None) -
             zipf_bias(MoeConfig(**{**cfg.__dict__, "zipf_beta": beta}), device))
         n = n + b[None, :]
     return n.to(torch.float32)
+
+
+def sharing_unique_experts(T: int, k: int, share: int, E: int) -> int:
+    """Distinct experts of a T-token batch at `share` percent expert sharing: the T*k
+    assignments reuse share% of them across the batch, never below the k experts of one token
+    (share 100 is that floor)."""
+    return min(E, max(k, round(T * k * (100 - share) / 100)))
+
+
+def sharing_routing(cfg: MoeConfig, T: int, share: int) -> torch.Tensor:
+    """Expert ids [T, k] of the expert-sharing decode workload shared_<share>: a pool of
+    U = sharing_unique_experts(...) experts drawn by a seeded permutation, token t's slot j taking
+    pool[(t*k + j) mod U] - every pool expert used, no expert twice within one token."""
+    k, E = cfg.top_k, cfg.experts
+    U = sharing_unique_experts(T, k, share, E)
+    u = uniform(_key(cfg, T_SHARE_POOL), share * E, E, "cpu")
+    pool = torch.argsort(u)[:U]
+    idx = (torch.arange(T)[:, None] * k + torch.arange(k)[None, :]) % U
+    return pool[idx]
+
+
+def gen_sharing_logits(cfg: MoeConfig, T: int, share: int, device="cpu") -> torch.Tensor:
+    """Router logits [T, E] that route the batch as sharing_routing(cfg, T, share): the N(0,1)
+    logits with each token's planted experts raised to 8 - j/4 (slot j), far above the rest."""
+    lg = gen_logits(cfg, T, "cpu")
+    ids = sharing_routing(cfg, T, share)
+    planted = 8.0 - 0.25 * torch.arange(cfg.top_k, dtype=torch.float32)
+    lg.scatter_(1, ids, planted.expand(T, -1).contiguous())
+    return lg.to(device)
 
 
 def gen_expert(cfg: MoeConfig, e: int, device="cpu"):
