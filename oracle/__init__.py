@@ -79,6 +79,9 @@ def lib():
                                     C.c_void_p, C.c_void_p]
         L.orc_sqrt_softplus.restype = C.c_float
         L.orc_sqrt_softplus.argtypes = [C.c_float]
+        L.orc_rmsnorm_quantize.restype = C.c_int
+        L.orc_rmsnorm_quantize.argtypes = [C.c_void_p, C.c_void_p, C.c_float, C.c_int64, C.c_int64,
+                                           C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]
         L.orc_swiglu.restype = C.c_float
         L.orc_swiglu.argtypes = [C.c_float, C.c_float, C.c_int, C.c_float]
         L.orc_plan.restype = None
@@ -149,6 +152,22 @@ def quantize_f32(x: np.ndarray, ts: float):
 def tensor_scale_bf16(x) -> float:
     xb = as_bf16_bits(x)
     return float(np.float32(lib().orc_tensor_scale_bf16(_p(xb), xb.size)))
+
+
+def rmsnorm_quantize(x, gamma, eps: float):
+    """RMSNorm of BF16 x [rows, cols] with BF16 gamma [cols] (sum of squares in float64, the rest
+    FP32), then NVFP4 with the tensor scale of the normalised values.  Returns (codes, sf, ts,
+    status, y) with y the FP32 normalised values."""
+    xb = as_bf16_bits(x)
+    gb = np.ascontiguousarray(as_bf16_bits(gamma).reshape(-1))
+    rows, cols = xb.shape
+    codes = np.zeros((rows, cols // 2), np.uint8)
+    sf = np.zeros((rows, cols // 16), np.uint8)
+    ts = np.zeros(1, np.float32)
+    y = np.zeros((rows, cols), np.float32)
+    st = lib().orc_rmsnorm_quantize(_p(xb), _p(gb), float(eps), rows, cols, _p(codes), _p(sf),
+                                    _p(ts), _p(y))
+    return codes, sf, float(ts[0]), int(st), y
 
 
 def dequantize(codes: np.ndarray, sf: np.ndarray, ts: float) -> np.ndarray:

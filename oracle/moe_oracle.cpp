@@ -198,6 +198,42 @@ int orc_quantize_bf16(const uint16_t* x, int64_t rows, int64_t cols, uint8_t* co
 }
 
 // v = (e2m1(code) * e4m3(sf)) * ts, rows [rows, cols].
+// RMSNorm then NVFP4 quantisation of x [rows, cols] BF16 with gamma [cols] BF16 (the producer
+// feeding the layer's activation quantiser: "nvfp4-megamoe-kernel compare pre-b1...master",
+// sections "P4 - Fused RMSNorm + NVFP4 quantize" and "P5"; two passes, the tensor scale taken
+// from the normalised values).  Per row: ms = (float)(sum_c x_c^2 in float64 / cols),
+// r = 1 / sqrt(ms + eps) (FP32), y_c = (x_c * r) * gamma_c (FP32, in that order); then
+// ts = max|y| / 2688 over the whole tensor and the block encode of y (as orc_quantize_f32).
+// Writes y [rows, cols] if y_out is not null.  Returns -6 when max|y| is not finite.
+int orc_rmsnorm_quantize(const uint16_t* x, const uint16_t* gamma, float eps, int64_t rows,
+                         int64_t cols, uint8_t* codes, uint8_t* sf, float* ts_out, float* y_out) {
+  std::vector<float> y((size_t)rows * cols);
+  float amax = 0.0f;
+  bool nan = false;
+  for (int64_t r = 0; r < rows; ++r) {
+    double ss = 0.0;
+    for (int64_t c = 0; c < cols; ++c) {
+      const double v = orc_bf16_to_f32(x[r * cols + c]);
+      ss = ss + v * v;
+    }
+    const float ms = (float)(ss / (double)cols);
+    const float rinv = 1.0f / std::sqrt(ms + eps);
+    for (int64_t c = 0; c < cols; ++c) {
+      const float v = (orc_bf16_to_f32(x[r * cols + c]) * rinv) * orc_bf16_to_f32(gamma[c]);
+      y[r * cols + c] = v;
+      const float a = std::fabs(v);
+      if (std::isnan(a)) nan = true;
+      else if (a > amax) amax = a;
+    }
+  }
+  const float ts = nan ? NAN : amax / 2688.0f;
+  *ts_out = ts;
+  if (y_out) std::copy(y.begin(), y.end(), y_out);
+  if (!std::isfinite(ts)) return -6;
+  orc_quantize_f32(y.data(), rows, cols, ts, codes, sf);
+  return 0;
+}
+
 void orc_dequantize(const uint8_t* codes, const uint8_t* sf, float ts, int64_t rows, int64_t cols,
                     float* out) {
   for (int64_t r = 0; r < rows; ++r)
