@@ -24,7 +24,7 @@ EXPORTED = ["moe_status_string", "moe_config_check", "moe_weights_size", "moe_qu
             "moe_weights_export", "moe_act_workspace_size", "moe_quantize_act",
             "moe_plan_workspace_size", "moe_plan", "moe_workspace_size", "moe_run",
             "moe_last_device_status", "moe_plan_static", "moe_run_kernel_count",
-            "moe_set_router_bias"]
+            "moe_set_router_bias", "moe_rmsnorm_workspace_size", "moe_rmsnorm_quantize_act"]
 
 
 class MoeConfig(C.Structure):
@@ -76,6 +76,9 @@ def lib():
             "moe_plan_static": (C.c_int, [vp, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]),
             "moe_run_kernel_count": (C.c_int, [cfgp, i32]),
             "moe_set_router_bias": (C.c_int, [cfgp, vp, vp, vp]),
+            "moe_rmsnorm_workspace_size": (sz, [i64]),
+            "moe_rmsnorm_quantize_act": (C.c_int, [vp, vp, C.c_float, i64, i64, vp, vp, vp, vp, sz,
+                                                   vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -178,6 +181,25 @@ def quantize_act(x, workspace=None, stream=None):
     _check(lib().moe_quantize_act(_ptr(x), rows, cols, _ptr(codes), _ptr(sf), _ptr(ts),
                                   _ptr(workspace), workspace.numel(), _stream(stream)),
            "moe_quantize_act")
+    return codes, sf, ts
+
+
+def rmsnorm_quantize_act(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6,
+                         workspace=None, stream=None):
+    """RMSNorm of BF16 x [rows, cols] by BF16 gamma [cols], then NVFP4 (codes, sf, ts) on the
+    device; raises on a non-finite result (device status) only via last_device_status."""
+    rows, cols = x.shape
+    dev = x.device
+    codes = torch.empty(rows, cols // 2, dtype=torch.uint8, device=dev)
+    sf = torch.empty(rows, cols // 16, dtype=torch.uint8, device=dev)
+    ts = torch.empty(1, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(lib().moe_rmsnorm_workspace_size(rows), dtype=torch.uint8,
+                                device=dev)
+    _check(lib().moe_rmsnorm_quantize_act(_ptr(x), _ptr(gamma), float(eps), rows, cols,
+                                          _ptr(codes), _ptr(sf), _ptr(ts), _ptr(workspace),
+                                          workspace.numel(), _stream(stream)),
+           "moe_rmsnorm_quantize_act")
     return codes, sf, ts
 
 

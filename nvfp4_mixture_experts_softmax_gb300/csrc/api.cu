@@ -131,6 +131,31 @@ int moe_quantize_act(const void* x, int64_t rows, int64_t cols, uint8_t* codes, 
   return cuda_status(launch_act_quant(x, rows, cols, codes, sf, ts, hdr, partials, nullptr, 0, s));
 }
 
+size_t moe_rmsnorm_workspace_size(int64_t rows) {
+  if (rows < 0) return 0;
+  return 256 + align_up(4 * (4 + (size_t)rows));
+}
+
+int moe_rmsnorm_quantize_act(const void* x, const void* gamma, float eps, int64_t rows,
+                             int64_t cols, uint8_t* codes, uint8_t* sf, float* ts,
+                             void* workspace, size_t ws_bytes, moe_stream_t stream) {
+  if (rows < 0 || cols <= 0 || cols % 16 != 0 || !(std::isfinite(eps) && eps >= 0.0f))
+    return MOE_ERR_INVALID_ARG;
+  if (rows > INT32_MAX) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!workspace || ws_bytes < moe_rmsnorm_workspace_size(rows)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned(workspace, 16)) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!x || !gamma || !codes || !sf || !ts) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(gamma, 16) || !aligned(codes, 8) || !aligned(ts, 4))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = to_cuda(stream);
+  WsHeader* hdr = static_cast<WsHeader*>(workspace);
+  if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return MOE_ERR_CUDA;
+  uint32_t* scratch = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + 256);
+  return cuda_status(launch_rmsnorm_quant(x, gamma, eps, rows, cols, codes, sf, ts, scratch,
+                                          &hdr->status, s));
+}
+
 size_t moe_plan_workspace_size(int32_t T, int32_t E, int32_t k) {
   if (T < 0 || E < 1 || k < 1) return 0;
   const int tpc = plan_tokens_per_chunk(k);

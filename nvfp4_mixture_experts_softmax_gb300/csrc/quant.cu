@@ -282,6 +282,109 @@ __global__ void __launch_bounds__(kThreads) act_encode_perm_kernel(
   }
 }
 
+// ---- RMSNorm + NVFP4 quantisation (the producer feeding the activation quantiser) ----
+// Scratch: [0] the tensor's max |y| as float bits, [1] the finished-block count, [2] the tensor
+// scale, [4 .. 4+rows) each row's 1/rms.
+
+// Pass 1, one block per row: the sum of squares in float64 (so the mean does not depend on the
+// reduction order), 1/rms = 1/sqrt(mean + eps) in FP32, y = (x * r) * gamma and the row's max |y|;
+// the last block to finish turns the tensor max into the tensor scale.
+__global__ void __launch_bounds__(kThreads) rmsnorm_amax_kernel(
+    const uint4* __restrict__ x, const uint4* __restrict__ gamma, float eps, int64_t rows,
+    int cols, uint32_t* __restrict__ scratch, int32_t* status) {
+  __shared__ double dred[kThreads / 32];
+  __shared__ uint32_t red[32];
+  __shared__ bool is_last;
+  griddep_wait();
+  griddep_launch();
+  const int64_t row = blockIdx.x;
+  const int vpr = cols / 8;
+  const uint4* xr = x + row * vpr;
+  double ss = 0.0;
+  for (int v = threadIdx.x; v < vpr; v += blockDim.x) {
+    const uint4 q = __ldg(xr + v);
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const double a = bf16_bits_to_f32(w[j] & 0xFFFFu), b = bf16_bits_to_f32(w[j] >> 16);
+      ss += a * a;
+      ss += b * b;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) dred[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  double tot = 0.0;
+  for (int wi = 0; wi < (int)(blockDim.x >> 5); ++wi) tot += dred[wi];
+  const float ms = (float)(tot / (double)cols);
+  const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+  uint32_t m = 0u;
+  for (int v = threadIdx.x; v < vpr; v += blockDim.x) {
+    const uint4 q = __ldg(xr + v), g = __ldg(gamma + v);
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w}, gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float y0 = __fmul_rn(__fmul_rn(bf16_bits_to_f32(w[j] & 0xFFFFu), r),
+                                 bf16_bits_to_f32(gw[j] & 0xFFFFu));
+      const float y1 = __fmul_rn(__fmul_rn(bf16_bits_to_f32(w[j] >> 16), r),
+                                 bf16_bits_to_f32(gw[j] >> 16));
+      m = max(m, max(__float_as_uint(fabsf(y0)), __float_as_uint(fabsf(y1))));
+    }
+  }
+  m = block_max_u32(m, red);
+  if (threadIdx.x == 0) {
+    reinterpret_cast<float*>(scratch)[4 + row] = r;
+    atomicMax(scratch, m);   // non-negative floats order like their bit patterns (NaN above inf)
+    __threadfence();
+    is_last = atomicAdd(scratch + 1, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!is_last || threadIdx.x != 0) return;
+  __threadfence();
+  const uint32_t amax = atomicAdd(scratch, 0u);
+  if (amax >= 0x7F800000u) set_status(status, MOE_ERR_NONFINITE);
+  reinterpret_cast<float*>(scratch)[2] = __fdiv_rn(__uint_as_float(amax), 2688.0f);
+  scratch[0] = 0u;
+  scratch[1] = 0u;
+}
+
+// Pass 2, one thread per 16-element block: y recomputed exactly as in pass 1, then encoded.
+__global__ void __launch_bounds__(kThreads) rmsnorm_encode_kernel(
+    const uint4* __restrict__ x, const uint4* __restrict__ gamma, int64_t rows, int cols,
+    const uint32_t* __restrict__ scratch, uint2* __restrict__ codes, uint8_t* __restrict__ sf,
+    float* ts_out) {
+  griddep_wait();
+  griddep_launch();
+  const float ts = __ldcg(reinterpret_cast<const float*>(scratch) + 2);
+  const float* rr = reinterpret_cast<const float*>(scratch) + 4;
+  const int bpr = cols / 16;
+  const int64_t nblk = rows * bpr;
+  if (blockIdx.x == 0 && threadIdx.x == 0 && ts_out) *ts_out = ts;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblk; b += stride) {
+    const int64_t row = b / bpr;
+    const int cb = (int)(b - row * bpr);
+    const float r = __ldcg(rr + row);
+    const uint4 q0 = __ldg(x + 2 * b), q1 = __ldg(x + 2 * b + 1);
+    const uint4 g0 = __ldg(gamma + 2 * cb), g1 = __ldg(gamma + 2 * cb + 1);
+    const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+    const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+    float y[16];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      y[2 * j] = __fmul_rn(__fmul_rn(bf16_bits_to_f32(w[j] & 0xFFFFu), r),
+                           bf16_bits_to_f32(gw[j] & 0xFFFFu));
+      y[2 * j + 1] = __fmul_rn(__fmul_rn(bf16_bits_to_f32(w[j] >> 16), r),
+                               bf16_bits_to_f32(gw[j] >> 16));
+    }
+    uint32_t lo, hi, s8;
+    quant_block16(y, ts, lo, hi, s8);
+    codes[b] = make_uint2(lo, hi);
+    sf[b] = (uint8_t)s8;
+  }
+}
+
 __global__ void __launch_bounds__(kThreads) permute_rows_kernel(
     const uint4* __restrict__ xq, const uint32_t* __restrict__ xsf, int T, int H, int Rt, int E,
     const int32_t* __restrict__ perm_src, const int32_t* __restrict__ perm_seg,
@@ -375,6 +478,22 @@ cudaError_t launch_act_encode_perm(const void* x, int T, int H, int k, int E, in
                     reinterpret_cast<const uint4*>(x), T, H, k, E, shared, Rt, ts, ids, inv,
                     offsets, tile_start, reinterpret_cast<uint2*>(codes), sf, xq_perm, xsf_tiles,
                     status);
+}
+
+cudaError_t launch_rmsnorm_quant(const void* x, const void* gamma, float eps, int64_t rows,
+                                 int64_t cols, uint8_t* codes, uint8_t* sf, float* ts,
+                                 uint32_t* scratch, int32_t* status, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(scratch, 0, 4 * sizeof(uint32_t), s);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(rmsnorm_amax_kernel, dim3((unsigned)rows), dim3(kThreads), 0, s,
+                 reinterpret_cast<const uint4*>(x), reinterpret_cast<const uint4*>(gamma), eps,
+                 rows, (int)cols, scratch, status);
+  if (e != cudaSuccess) return e;
+  const int64_t nblk = rows * cols / 16;
+  return launch_pdl(rmsnorm_encode_kernel, dim3(grid_for(nblk, kThreads, num_sms() * 16)),
+                    dim3(kThreads), 0, s, reinterpret_cast<const uint4*>(x),
+                    reinterpret_cast<const uint4*>(gamma), rows, (int)cols,
+                    (const uint32_t*)scratch, reinterpret_cast<uint2*>(codes), sf, ts);
 }
 
 cudaError_t launch_act_quant(const void* x, int64_t rows, int64_t cols, uint8_t* codes, uint8_t* sf,
