@@ -79,6 +79,8 @@ def lib():
                                     C.c_void_p, C.c_void_p]
         L.orc_sqrt_softplus.restype = C.c_float
         L.orc_sqrt_softplus.argtypes = [C.c_float]
+        L.orc_sum_squares_tree.restype = C.c_float
+        L.orc_sum_squares_tree.argtypes = [C.c_void_p, C.c_int64]
         L.orc_rmsnorm_quantize.restype = C.c_int
         L.orc_rmsnorm_quantize.argtypes = [C.c_void_p, C.c_void_p, C.c_float, C.c_int64, C.c_int64,
                                            C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]
@@ -155,8 +157,9 @@ def tensor_scale_bf16(x) -> float:
 
 
 def rmsnorm_quantize(x, gamma, eps: float):
-    """RMSNorm of BF16 x [rows, cols] with BF16 gamma [cols] (sum of squares in float64, the rest
-    FP32), then NVFP4 with the tensor scale of the normalised values.  Returns (codes, sf, ts,
+    """RMSNorm of BF16 x [rows, cols] with BF16 gamma [cols] (FP32; the mean square summed in
+    8-element chunks combined by a balanced pairwise tree), then NVFP4 with the tensor scale of
+    the normalised values.  Returns (codes, sf, ts,
     status, y) with y the FP32 normalised values."""
     xb = as_bf16_bits(x)
     gb = np.ascontiguousarray(as_bf16_bits(gamma).reshape(-1))
@@ -168,6 +171,13 @@ def rmsnorm_quantize(x, gamma, eps: float):
     st = lib().orc_rmsnorm_quantize(_p(xb), _p(gb), float(eps), rows, cols, _p(codes), _p(sf),
                                     _p(ts), _p(y))
     return codes, sf, float(ts[0]), int(st), y
+
+
+def sum_squares_tree(v) -> float:
+    """The mean-square numerator of rmsnorm_quantize: 8-element chunks summed left to right,
+    chunk sums combined by a balanced pairwise tree (FP32)."""
+    v = np.ascontiguousarray(v, np.float32)
+    return float(lib().orc_sum_squares_tree(_p(v), v.size))
 
 
 def dequantize(codes: np.ndarray, sf: np.ndarray, ts: float) -> np.ndarray:

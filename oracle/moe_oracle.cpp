@@ -201,25 +201,40 @@ int orc_quantize_bf16(const uint16_t* x, int64_t rows, int64_t cols, uint8_t* co
 // RMSNorm then NVFP4 quantisation of x [rows, cols] BF16 with gamma [cols] BF16 (the producer
 // feeding the layer's activation quantiser: "nvfp4-megamoe-kernel compare pre-b1...master",
 // sections "P4 - Fused RMSNorm + NVFP4 quantize" and "P5"; two passes, the tensor scale taken
-// from the normalised values).  Per row: ms = (float)(sum_c x_c^2 in float64 / cols),
-// r = 1 / sqrt(ms + eps) (FP32), y_c = (x_c * r) * gamma_c (FP32, in that order); then
-// ts = max|y| / 2688 over the whole tensor and the block encode of y (as orc_quantize_f32).
-// Writes y [rows, cols] if y_out is not null.  Returns -6 when max|y| is not finite.
+// from the normalised values).  The pages leave the summation order of the mean square open; the
+// reading taken fixes it so that the result is one exact FP32 value: the row is cut into chunks
+// of 8 consecutive elements, each chunk's squares are summed left to right, and the chunk sums
+// are combined by a balanced pairwise tree over the chunk index (padded with zeros to a power of
+// two).  Then ms = sum / cols, r = 1 / sqrt(ms + eps), y_c = (x_c * r) * gamma_c (FP32, in that
+// order); ts = max|y| / 2688 over the whole tensor and the block encode of y (as
+// orc_quantize_f32).  Writes y [rows, cols] if y_out is not null.  Returns -6 when max|y| is
+// not finite.  cols must be a multiple of 8.
+float orc_sum_squares_tree(const float* v, int64_t n) {
+  const int64_t nchunk = n / 8;
+  int64_t P = 1;
+  while (P < nchunk) P *= 2;
+  std::vector<float> part(P, 0.0f);
+  for (int64_t c = 0; c < nchunk; ++c) {
+    float s = v[c * 8] * v[c * 8];
+    for (int i = 1; i < 8; ++i) s = s + v[c * 8 + i] * v[c * 8 + i];
+    part[c] = s;
+  }
+  for (int64_t width = 1; width < P; width *= 2)
+    for (int64_t i = 0; i < P; i += 2 * width) part[i] = part[i] + part[i + width];
+  return part[0];
+}
+
 int orc_rmsnorm_quantize(const uint16_t* x, const uint16_t* gamma, float eps, int64_t rows,
                          int64_t cols, uint8_t* codes, uint8_t* sf, float* ts_out, float* y_out) {
-  std::vector<float> y((size_t)rows * cols);
+  std::vector<float> y((size_t)rows * cols), row(cols);
   float amax = 0.0f;
   bool nan = false;
   for (int64_t r = 0; r < rows; ++r) {
-    double ss = 0.0;
-    for (int64_t c = 0; c < cols; ++c) {
-      const double v = orc_bf16_to_f32(x[r * cols + c]);
-      ss = ss + v * v;
-    }
-    const float ms = (float)(ss / (double)cols);
+    for (int64_t c = 0; c < cols; ++c) row[c] = orc_bf16_to_f32(x[r * cols + c]);
+    const float ms = orc_sum_squares_tree(row.data(), cols) / (float)cols;
     const float rinv = 1.0f / std::sqrt(ms + eps);
     for (int64_t c = 0; c < cols; ++c) {
-      const float v = (orc_bf16_to_f32(x[r * cols + c]) * rinv) * orc_bf16_to_f32(gamma[c]);
+      const float v = (row[c] * rinv) * orc_bf16_to_f32(gamma[c]);
       y[r * cols + c] = v;
       const float a = std::fabs(v);
       if (std::isnan(a)) nan = true;

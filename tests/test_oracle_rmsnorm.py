@@ -57,3 +57,19 @@ def test_zero_gamma_gives_zero():
     x = torch.randn(4, 256).to(torch.bfloat16)
     codes, sf, ts, st, y = oracle.rmsnorm_quantize(x, torch.zeros(256).to(torch.bfloat16), 1e-6)
     assert st == 0 and ts == 0.0 and not y.any() and not codes.any() and not sf.any()
+
+
+def test_sum_squares_tree_exact_cases():
+    # a power-of-two count of equal squares sums exactly; sixteen chunks of ones = 128
+    assert oracle.sum_squares_tree(np.ones(128, np.float32)) == 128.0
+    # the pairwise order is observable: chunk sums 2^24, 1, 1, 1 give (2^24 + 1) + (1 + 1)
+    # = 2^24 + 2 (the first pair rounds to 2^24, the second is exact), where a left-to-right sum
+    # would stay at 2^24
+    v = np.zeros(32, np.float32)
+    v[0] = 4096.0
+    v[8] = v[16] = v[24] = 1.0
+    assert oracle.sum_squares_tree(v) == np.float32(2.0**24 + 2)
+    # agreement with float64 within the FP32 tree's error bound
+    r = np.random.default_rng(8).standard_normal(7168).astype(np.float32)
+    exact = float((r.astype(np.float64) ** 2).sum())
+    assert abs(oracle.sum_squares_tree(r) - exact) <= 7168 * 2 ** -24 * exact
