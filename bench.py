@@ -76,6 +76,8 @@ def parse():
                     help="comma-separated batch sizes replacing the workload's own list")
     ap.add_argument("--variant", default="base", choices=list(VARIANTS),
                     help="router / activation variant of the layer")
+    ap.add_argument("--producer", action="store_true",
+                    help="time the RMSNorm + NVFP4 producer of the layer's input instead of the layer")
     ap.add_argument("--routing", default=None,
                     help="shared_<p> (p in 0..100): the expert-sharing decode workload, whose "
                          "batches reuse p%% of their token/expert assignments")
@@ -517,6 +519,111 @@ def run_ours(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------------------- producer
+def run_producer(args, world, rank, local):
+    """RMSNorm + NVFP4 quantisation of the workload's activations [T, H] (two kernels per step)."""
+    import numpy as np
+    import synth
+    import oracle
+    import nvfp4_mixture_experts_softmax_gb300 as moe
+    from nvfp4_mixture_experts_softmax_gb300 import _build
+
+    _build.build()
+    dev = torch.device("cuda", local)
+    cs, Ts = workload(args.workload, args.tokens)
+    T, H = max(Ts), cs.hidden
+    x = synth.gen_x(cs, T, device=dev)
+    gamma = torch.from_numpy(np.random.default_rng(7).normal(1.0, 0.1, H).astype(np.float32))
+    gamma = gamma.to(torch.bfloat16).to(dev)
+    ws = torch.empty(moe.lib().moe_rmsnorm_workspace_size(T), dtype=torch.uint8, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        moe.rmsnorm_quantize_act(x, gamma, 1e-6, workspace=ws)
+    torch.cuda.synchronize()
+    assert moe.last_device_status(ws) == 0
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_settle = time.time()
+    while time.time() - t_settle < 0.4:
+        flush.zero_()
+        torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    w0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        moe.rmsnorm_quantize_act(x, gamma, 1e-6, workspace=ws)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    w1 = time.time()
+    time.sleep(0.1)
+    sampler.stop()
+    ms = [a.elapsed_time(b) for a, b in ev]
+    value, tmax = aggregate(T * args.steps, sum(ms) / 1e3, world)
+    hbm_peak, _, peak_src = measured_peaks()
+    nbytes = 2 * T * H * 2 + H * 2 + T * H * 9 // 16 + T * 4     # x twice, gamma, codes + scales
+    per = statistics.mean(ms) / 1e3
+    achieved = nbytes / per / 1e9
+    # end to end: host x in, host codes/scales out, copies inside the timed region
+    hx = x.cpu().pin_memory()
+    dx = torch.empty_like(x)
+    hc = torch.empty(T, H // 2, dtype=torch.uint8).pin_memory()
+    hs = torch.empty(T, H // 16, dtype=torch.uint8).pin_memory()
+    e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        dx.copy_(hx, non_blocking=True)
+        codes, sf, _ = moe.rmsnorm_quantize_act(dx, gamma, 1e-6, workspace=ws)
+        hc.copy_(codes, non_blocking=True)
+        hs.copy_(sf, non_blocking=True)
+        e1.record(stream)
+        if i >= args.warmup:
+            e_ms.append((e0, e1))
+    torch.cuda.synchronize()
+    e2e_value, _ = aggregate(T * len(e_ms), sum(a.elapsed_time(b) for a, b in e_ms) / 1e3, world)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n = min(T, 1024)
+        xc, gc = x[:n].cpu(), gamma.cpu()
+        t0 = time.perf_counter()
+        oracle.rmsnorm_quantize(xc, gc, 1e-6)
+        dt = time.perf_counter() - t0
+        cpu = {"value": n / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"the first {n} rows, single-threaded C++ oracle"}
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tmax * 1e3 / args.steps, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 in, f32 norm (f64 sum of squares), nvfp4 out",
+        "data": "synthetic (seeded SplitMix64/Box-Muller)",
+        "config": {"workload": f"RMSNorm + NVFP4 producer of the {args.workload} input: T={T}, H={H}",
+                   "l2": "flushed (2x L2 write) before every call, outside the timed events",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"kernel": "rmsnorm_amax_kernel + rmsnorm_encode_kernel", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "algorithmic_bytes_per_launch": nbytes,
+                     "avg_launch_us": round(per * 1e6, 2),
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)", "traffic": None},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": T * H * 2,
+                "d2h_bytes_per_step": T * H * 9 // 16},
+        "gpu_launches": 2 * args.steps,
+        "clocks": sampler.summary(t_settle, w1 + 0.05),
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------------------------------------- reference
 def run_reference(args, world, rank, local):
     if rank != 0:
@@ -577,6 +684,8 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, world, rank, local)
+        elif args.producer:
+            run_producer(args, world, rank, local)
         else:
             run_ours(args, world, rank, local)
     finally:

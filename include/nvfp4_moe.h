@@ -155,10 +155,12 @@ int moe_quantize_act(const void* x, int64_t rows, int64_t cols, uint8_t* codes, 
 /* RMSNorm followed by the activation quantiser: the producer that feeds the layer's quantised
  * input ("nvfp4-megamoe-kernel compare pre-b1...master", sections "P4 - Fused RMSNorm + NVFP4
  * quantize" and "P5": two kernels, no BF16 round trip between the norm and the quantiser).  Per
- * row: ms = (float)(sum of x^2 accumulated in float64 / cols), r = 1 / sqrt(ms + eps) (FP32),
- * y = (x * r) * gamma (FP32); then one tensor scale max|y| / 2688 for the whole tensor and the
- * per-16 encode of y, as moe_quantize_act does for x.  x: [rows, cols] BF16, gamma: [cols] BF16,
- * both 16-byte aligned, cols a multiple of 16; codes [rows, cols/2], sf [rows, cols/16], ts: device
+ * row: ms = (sum of x^2) / cols, r = 1 / sqrt(ms + eps), y = (x * r) * gamma, all FP32;
+ * then one tensor scale max|y| / 2688 for the whole tensor and the
+ * per-16 encode of y, as moe_quantize_act does for x.  The sum of squares is one exact FP32
+ * value: 8-element chunks summed left to right, the chunk sums combined by a balanced pairwise tree
+ * over the chunk index.  x: [rows, cols] BF16, gamma: [cols] BF16, both 16-byte aligned, cols a
+ * multiple of 16 and at most 16384; codes [rows, cols/2], sf [rows, cols/16], ts: device
  * FP32 scalar.  workspace: >= moe_rmsnorm_workspace_size(rows) bytes (its first word is the device
  * status: MOE_ERR_NONFINITE when max|y| is not finite).  rows == 0 is MOE_OK. */
 size_t moe_rmsnorm_workspace_size(int64_t rows);

@@ -141,6 +141,7 @@ int moe_rmsnorm_quantize_act(const void* x, const void* gamma, float eps, int64_
                              void* workspace, size_t ws_bytes, moe_stream_t stream) {
   if (rows < 0 || cols <= 0 || cols % 16 != 0 || !(std::isfinite(eps) && eps >= 0.0f))
     return MOE_ERR_INVALID_ARG;
+  if (cols > 16384) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (rows > INT32_MAX) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!workspace || ws_bytes < moe_rmsnorm_workspace_size(rows)) return MOE_ERR_WORKSPACE_TOO_SMALL;
   if (!aligned(workspace, 16)) return MOE_ERR_INVALID_ARG;

@@ -284,57 +284,93 @@ __global__ void __launch_bounds__(kThreads) act_encode_perm_kernel(
 
 // ---- RMSNorm + NVFP4 quantisation (the producer feeding the activation quantiser) ----
 // Scratch: [0] the tensor's max |y| as float bits, [1] the finished-block count, [2] the tensor
-// scale, [4 .. 4+rows) each row's 1/rms.
+// scale, [4 .. 4+rows) each row's 1/rms.  Every FP32 operation is an explicit round-to-nearest
+// intrinsic, so nothing is contracted into a fused multiply-add.
 
-// Pass 1, one block per row: the sum of squares in float64 (so the mean does not depend on the
-// reduction order), 1/rms = 1/sqrt(mean + eps) in FP32, y = (x * r) * gamma and the row's max |y|;
-// the last block to finish turns the tensor max into the tensor scale.
+// Pass 1: one warp per row (rows taken in turn).  A row's mean square is one exact FP32 value:
+// chunks of 8 elements summed left to right, chunk sums combined by a balanced pairwise tree over
+// the chunk index (zero-padded to a power of two).  In step j the warp loads chunks 32j .. 32j+31
+// (lane l: chunk 32j + l, one coalesced 512-byte run) and its xor butterfly forms the tree's
+// first five levels over them; the J step sums then form the remaining levels, in registers.
+// 1/rms = 1/sqrt(mean + eps), y = (x * r) * gamma;
+// each block keeps its max |y|, and the block that finishes last turns the tensor max into the
+// tensor scale.
+template <int J>
 __global__ void __launch_bounds__(kThreads) rmsnorm_amax_kernel(
     const uint4* __restrict__ x, const uint4* __restrict__ gamma, float eps, int64_t rows,
     int cols, uint32_t* __restrict__ scratch, int32_t* status) {
-  __shared__ double dred[kThreads / 32];
   __shared__ uint32_t red[32];
   __shared__ bool is_last;
   griddep_wait();
   griddep_launch();
-  const int64_t row = blockIdx.x;
-  const int vpr = cols / 8;
-  const uint4* xr = x + row * vpr;
-  double ss = 0.0;
-  for (int v = threadIdx.x; v < vpr; v += blockDim.x) {
-    const uint4 q = __ldg(xr + v);
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const double a = bf16_bits_to_f32(w[j] & 0xFFFFu), b = bf16_bits_to_f32(w[j] >> 16);
-      ss += a * a;
-      ss += b * b;
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  if ((threadIdx.x & 31) == 0) dred[threadIdx.x >> 5] = ss;
-  __syncthreads();
-  double tot = 0.0;
-  for (int wi = 0; wi < (int)(blockDim.x >> 5); ++wi) tot += dred[wi];
-  const float ms = (float)(tot / (double)cols);
-  const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+  const int lane = threadIdx.x & 31;
+  const int nchunk = cols / 8;
+  const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   uint32_t m = 0u;
-  for (int v = threadIdx.x; v < vpr; v += blockDim.x) {
-    const uint4 q = __ldg(xr + v), g = __ldg(gamma + v);
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w}, gw[4] = {g.x, g.y, g.z, g.w};
+  for (int64_t row = wid; row < rows; row += nwarps) {
+    const uint4* xr = x + row * nchunk;
+    float part[J];
+    // eight steps' loads in flight at a time, then their chunk sums and butterflies
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float y0 = __fmul_rn(__fmul_rn(bf16_bits_to_f32(w[j] & 0xFFFFu), r),
-                                 bf16_bits_to_f32(gw[j] & 0xFFFFu));
-      const float y1 = __fmul_rn(__fmul_rn(bf16_bits_to_f32(w[j] >> 16), r),
-                                 bf16_bits_to_f32(gw[j] >> 16));
-      m = max(m, max(__float_as_uint(fabsf(y0)), __float_as_uint(fabsf(y1))));
+    for (int j0 = 0; j0 < J; j0 += 8) {
+      uint4 q[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int c = (j0 + u) * 32 + lane;
+        q[u] = (j0 + u < J && c < nchunk) ? __ldg(xr + c) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (j0 + u >= J) break;
+        const uint32_t w[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+        float v = bf16_bits_to_f32(w[0] & 0xFFFFu);
+        float sq = __fmul_rn(v, v);
+#pragma unroll
+        for (int i = 1; i < 8; ++i) {
+          v = bf16_bits_to_f32((i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu));
+          sq = __fadd_rn(sq, __fmul_rn(v, v));
+        }
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) sq = __fadd_rn(sq, __shfl_xor_sync(0xffffffffu, sq, o));
+        part[j0 + u] = sq;
+      }
+    }
+#pragma unroll
+    for (int width = 1; width < J; width *= 2)
+#pragma unroll
+      for (int i = 0; i < J; i += 2 * width) part[i] = __fadd_rn(part[i], part[i + width]);
+    const float sum = part[0];
+    const float ms = __fdiv_rn(sum, (float)cols);
+    const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+    if (lane == 0) reinterpret_cast<float*>(scratch)[4 + row] = r;
+#pragma unroll
+    for (int j0 = 0; j0 < J; j0 += 8) {
+      uint4 q[8], gm[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int c = (j0 + u) * 32 + lane;
+        const bool in = j0 + u < J && c < nchunk;
+        q[u] = in ? __ldg(xr + c) : make_uint4(0u, 0u, 0u, 0u);
+        gm[u] = in ? __ldg(gamma + c) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t w[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+        const uint32_t gw[4] = {gm[u].x, gm[u].y, gm[u].z, gm[u].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {   // padding chunks are zero and leave the max unchanged
+          const float y0 = __fmul_rn(__fmul_rn(bf16_bits_to_f32(w[i] & 0xFFFFu), r),
+                                     bf16_bits_to_f32(gw[i] & 0xFFFFu));
+          const float y1 = __fmul_rn(__fmul_rn(bf16_bits_to_f32(w[i] >> 16), r),
+                                     bf16_bits_to_f32(gw[i] >> 16));
+          m = max(m, max(__float_as_uint(fabsf(y0)), __float_as_uint(fabsf(y1))));
+        }
+      }
     }
   }
   m = block_max_u32(m, red);
   if (threadIdx.x == 0) {
-    reinterpret_cast<float*>(scratch)[4 + row] = r;
     atomicMax(scratch, m);   // non-negative floats order like their bit patterns (NaN above inf)
     __threadfence();
     is_last = atomicAdd(scratch + 1, 1u) == gridDim.x - 1;
@@ -485,9 +521,26 @@ cudaError_t launch_rmsnorm_quant(const void* x, const void* gamma, float eps, in
                                  uint32_t* scratch, int32_t* status, cudaStream_t s) {
   cudaError_t e = cudaMemsetAsync(scratch, 0, 4 * sizeof(uint32_t), s);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(rmsnorm_amax_kernel, dim3((unsigned)rows), dim3(kThreads), 0, s,
-                 reinterpret_cast<const uint4*>(x), reinterpret_cast<const uint4*>(gamma), eps,
-                 rows, (int)cols, scratch, status);
+  // lanes own J chunks each: the padded chunk count (a power of two >= 32) over 32 lanes
+  const int nchunk = (int)(cols / 8);
+  int J = 1;
+  while (J * 32 < nchunk) J *= 2;
+  const int g1 = (int)std::min<int64_t>((rows + 7) / 8, (int64_t)num_sms() * 8);
+#define NVFP4MOE_RMS(JJ)                                                                      \
+  e = launch_pdl(rmsnorm_amax_kernel<JJ>, dim3(g1), dim3(kThreads), 0, s,                      \
+                 reinterpret_cast<const uint4*>(x), reinterpret_cast<const uint4*>(gamma), eps, \
+                 rows, (int)cols, scratch, status)
+  switch (J) {
+    case 1: NVFP4MOE_RMS(1); break;
+    case 2: NVFP4MOE_RMS(2); break;
+    case 4: NVFP4MOE_RMS(4); break;
+    case 8: NVFP4MOE_RMS(8); break;
+    case 16: NVFP4MOE_RMS(16); break;
+    case 32: NVFP4MOE_RMS(32); break;
+    case 64: NVFP4MOE_RMS(64); break;
+    default: return cudaErrorInvalidValue;
+  }
+#undef NVFP4MOE_RMS
   if (e != cudaSuccess) return e;
   const int64_t nblk = rows * cols / 16;
   return launch_pdl(rmsnorm_encode_kernel, dim3(grid_for(nblk, kThreads, num_sms() * 16)),
