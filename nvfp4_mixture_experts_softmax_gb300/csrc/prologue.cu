@@ -11,7 +11,7 @@ namespace nvfp4moe {
 
 namespace {
 
-template <int VPL>
+template <int VPL, bool SQRTSP>
 __global__ void __launch_bounds__(kSmallPlanThreads) prologue_small_kernel(const PrologueArgs a) {
   extern __shared__ __align__(16) uint8_t s_dyn[];
   __shared__ uint32_t red[32];
@@ -35,9 +35,9 @@ __global__ void __launch_bounds__(kSmallPlanThreads) prologue_small_kernel(const
   const int64_t nblk = (int64_t)a.T * a.H / 16;
   for (int64_t b = threadIdx.x; b < nblk; b += blockDim.x)
     encode_bf16_block16(x, b, ts, reinterpret_cast<uint2*>(a.xq), a.xsf);
-  small_plan_body<VPL>(a.logits, a.T, a.E, a.k, a.shared_rows, a.ids, a.w, a.counts, a.offsets,
-                       a.tile_start, a.perm_src, a.perm_w, a.inv, s_dyn, a.perm_seg, a.sqrtsp,
-                       a.bias);
+  small_plan_body<VPL, SQRTSP>(a.logits, a.T, a.E, a.k, a.shared_rows, a.ids, a.w, a.counts,
+                               a.offsets, a.tile_start, a.perm_src, a.perm_w, a.inv, s_dyn,
+                               a.perm_seg, a.bias);
 }
 
 // Decode batches (T <= kDecodeMaxRows): a cluster of kDecodeProCtas CTAs in two phases around
@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(kSmallPlanThreads) prologue_small_kernel(const
 //      expert's tile index, row = expert-ordered row - the expert's offset).
 // A CTA keeps its shared memory until the cluster's other CTAs have finished reading it (split
 // cluster barrier: arrive after the last remote read, wait before exit).
-template <int VPL>
+template <int VPL, bool SQRTSP>
 __global__ void __launch_bounds__(kSmallPlanThreads) decode_prologue_kernel(const DecodePrologueArgs a) {
   extern __shared__ __align__(16) uint8_t s_dyn[];
   __shared__ uint32_t red[32];
@@ -88,8 +88,8 @@ __global__ void __launch_bounds__(kSmallPlanThreads) decode_prologue_kernel(cons
   for (int t = (int)rank * nw + warp; t < a.T; t += kDecodeProCtas * nw) {
     int my_id;
     float my_l;
-    warp_topk<VPL>(a.logits + (int64_t)t * a.E, a.E, a.k, lane, my_id, my_l, a.sqrtsp, a.bias);
-    const float w = topk_weight(my_l, a.k, lane, a.sqrtsp);
+    warp_topk<VPL, SQRTSP>(a.logits + (int64_t)t * a.E, a.E, a.k, lane, my_id, my_l, a.bias);
+    const float w = topk_weight<SQRTSP>(my_l, a.k, lane);
     if (lane < a.k) {
       a.ids[(int64_t)t * a.k + lane] = my_id;
       a.w[(int64_t)t * a.k + lane] = w;
@@ -202,15 +202,20 @@ cudaError_t launch_decode_prologue(const DecodePrologueArgs& a, cudaStream_t s) 
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-#define NVFP4MOE_DPRO(V)                                                                       \
+#define NVFP4MOE_DPRO2(V, SP)                                                                  \
   do {                                                                                         \
     if (smem > 48 * 1024) {                                                                    \
-      cudaError_t e = cudaFuncSetAttribute(decode_prologue_kernel<V>,                          \
+      cudaError_t e = cudaFuncSetAttribute(decode_prologue_kernel<V, SP>,                      \
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,        \
                                            (int)smem);                                         \
       if (e != cudaSuccess) return e;                                                          \
     }                                                                                          \
-    return cudaLaunchKernelEx(&cfg, decode_prologue_kernel<V>, a);                             \
+    return cudaLaunchKernelEx(&cfg, decode_prologue_kernel<V, SP>, a);                         \
+  } while (0)
+#define NVFP4MOE_DPRO(V)                                                                       \
+  do {                                                                                         \
+    if (a.sqrtsp) NVFP4MOE_DPRO2(V, true);                                                     \
+    else NVFP4MOE_DPRO2(V, false);                                                             \
   } while (0)
   if (vpl <= 1) NVFP4MOE_DPRO(1);
   else if (vpl <= 2) NVFP4MOE_DPRO(2);
@@ -219,6 +224,7 @@ cudaError_t launch_decode_prologue(const DecodePrologueArgs& a, cudaStream_t s) 
   else if (vpl <= 16) NVFP4MOE_DPRO(16);
   else NVFP4MOE_DPRO(kMaxVpl);
 #undef NVFP4MOE_DPRO
+#undef NVFP4MOE_DPRO2
 }
 
 bool prologue_small_fits(int T, int H, int k) {
@@ -228,17 +234,22 @@ bool prologue_small_fits(int T, int H, int k) {
 cudaError_t launch_prologue_small(const PrologueArgs& a, cudaStream_t s) {
   const size_t smem = small_plan_smem_bytes(a.E);
   const int vpl = (a.E + 31) / 32;
-#define NVFP4MOE_PRO(V)                                                                        \
+#define NVFP4MOE_PRO2(V, SP)                                                                   \
   do {                                                                                         \
     if (smem > 48 * 1024) {                                                                    \
-      cudaError_t e = cudaFuncSetAttribute(prologue_small_kernel<V>,                           \
+      cudaError_t e = cudaFuncSetAttribute(prologue_small_kernel<V, SP>,                       \
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,        \
                                            (int)smem);                                         \
       if (e != cudaSuccess) return e;                                                          \
     }                                                                                          \
-    cudaError_t le = launch_pdl(prologue_small_kernel<V>, dim3(1), dim3(kSmallPlanThreads),    \
+    cudaError_t le = launch_pdl(prologue_small_kernel<V, SP>, dim3(1), dim3(kSmallPlanThreads), \
                                 smem, s, a);                                                   \
     if (le != cudaSuccess) return le;                                                          \
+  } while (0)
+#define NVFP4MOE_PRO(V)                                                                        \
+  do {                                                                                         \
+    if (a.sqrtsp) NVFP4MOE_PRO2(V, true);                                                      \
+    else NVFP4MOE_PRO2(V, false);                                                              \
   } while (0)
   if (vpl <= 1) NVFP4MOE_PRO(1);
   else if (vpl <= 2) NVFP4MOE_PRO(2);
@@ -247,6 +258,7 @@ cudaError_t launch_prologue_small(const PrologueArgs& a, cudaStream_t s) {
   else if (vpl <= 16) NVFP4MOE_PRO(16);
   else NVFP4MOE_PRO(kMaxVpl);
 #undef NVFP4MOE_PRO
+#undef NVFP4MOE_PRO2
   return cudaGetLastError();
 }
 

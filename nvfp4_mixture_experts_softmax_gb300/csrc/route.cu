@@ -29,11 +29,10 @@ constexpr int kRouterWarps = 8;
 
 // One warp per token; the per-chunk expert histogram (chunk = tpc tokens) is accumulated with
 // global atomics into `hist`, which the caller zeroes first.
-template <int VPL>
+template <int VPL, bool SQRTSP>
 __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(
     const float* __restrict__ logits, int T, int E, int k, int tpc, int32_t* __restrict__ ids,
-    float* __restrict__ wout, int32_t* __restrict__ hist, int sqrtsp,
-    const float* __restrict__ bias) {
+    float* __restrict__ wout, int32_t* __restrict__ hist, const float* __restrict__ bias) {
   griddep_wait();
   griddep_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -41,8 +40,8 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(
   if (t >= T) return;
   int my_id;
   float my_l;
-  warp_topk<VPL>(logits + (int64_t)t * E, E, k, lane, my_id, my_l, sqrtsp, bias);
-  const float w = topk_weight(my_l, k, lane, sqrtsp);
+  warp_topk<VPL, SQRTSP>(logits + (int64_t)t * E, E, k, lane, my_id, my_l, bias);
+  const float w = topk_weight<SQRTSP>(my_l, k, lane);
   if (lane < k) {
     ids[(int64_t)t * k + lane] = my_id;
     wout[(int64_t)t * k + lane] = w;
@@ -50,18 +49,18 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(
   }
 }
 
-template <int VPL>
+template <int VPL, bool SQRTSP>
 __global__ void __launch_bounds__(kSmallPlanThreads) plan_small_kernel(
     const float* __restrict__ logits, int T, int E, int k, int shared_rows,
     int32_t* __restrict__ ids, float* __restrict__ wout, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ tile_start,
     int32_t* __restrict__ perm_src, float* __restrict__ perm_w, int32_t* __restrict__ inv,
-    int32_t* __restrict__ perm_seg, int sqrtsp, const float* __restrict__ bias) {
+    int32_t* __restrict__ perm_seg, const float* __restrict__ bias) {
   extern __shared__ __align__(16) uint8_t s_dyn[];
   griddep_wait();
   griddep_launch();
-  small_plan_body<VPL>(logits, T, E, k, shared_rows, ids, wout, counts, offsets, tile_start,
-                       perm_src, perm_w, inv, s_dyn, perm_seg, sqrtsp, bias);
+  small_plan_body<VPL, SQRTSP>(logits, T, E, k, shared_rows, ids, wout, counts, offsets,
+                               tile_start, perm_src, perm_w, inv, s_dyn, perm_seg, bias);
 }
 
 // Per-chunk bases and per-expert offsets from the chunk histograms, spread over blocks of 32
@@ -181,15 +180,20 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s) {
   const int vpl = (a.E + 31) / 32;
   if ((int64_t)a.T * a.k <= kSmallPlanRows) {
     const size_t smem = small_plan_smem_bytes(a.E);
-#define NVFP4MOE_SMALL(V)                                                                       \
+#define NVFP4MOE_SMALL2(V, SP)                                                                  \
   do {                                                                                          \
     if (smem > 48 * 1024)                                                                       \
-      cudaFuncSetAttribute(plan_small_kernel<V>, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
-                           (int)smem);                                                          \
-    cudaError_t le = launch_pdl(plan_small_kernel<V>, dim3(1), dim3(kSmallPlanThreads), smem, s,  \
-        a.logits, a.T, a.E, a.k, a.shared_rows, a.ids, a.w, a.counts, a.offsets, a.tile_start, \
-        a.perm_src, a.perm_w, a.inv, a.perm_seg, a.sqrtsp, a.bias);                             \
+      cudaFuncSetAttribute(plan_small_kernel<V, SP>,                                            \
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);             \
+    cudaError_t le = launch_pdl(plan_small_kernel<V, SP>, dim3(1), dim3(kSmallPlanThreads), smem, \
+        s, a.logits, a.T, a.E, a.k, a.shared_rows, a.ids, a.w, a.counts, a.offsets,             \
+        a.tile_start, a.perm_src, a.perm_w, a.inv, a.perm_seg, a.bias);                         \
     if (le != cudaSuccess) return le;                                                           \
+  } while (0)
+#define NVFP4MOE_SMALL(V)                                                                       \
+  do {                                                                                          \
+    if (a.sqrtsp) NVFP4MOE_SMALL2(V, true);                                                     \
+    else NVFP4MOE_SMALL2(V, false);                                                             \
   } while (0)
     if (vpl <= 1) NVFP4MOE_SMALL(1);
     else if (vpl <= 2) NVFP4MOE_SMALL(2);
@@ -198,6 +202,7 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s) {
     else if (vpl <= 16) NVFP4MOE_SMALL(16);
     else NVFP4MOE_SMALL(kMaxVpl);
 #undef NVFP4MOE_SMALL
+#undef NVFP4MOE_SMALL2
     return cudaGetLastError();
   }
   // the histograms and the scan's block count (scratch after them) start at zero
@@ -205,8 +210,11 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s) {
   if (err != cudaSuccess) return err;
   const int rblocks = (a.T + kRouterWarps - 1) / kRouterWarps;
 #define NVFP4MOE_ROUTER(V)                                                                 \
-  err = launch_pdl(router_kernel<V>, dim3(rblocks), dim3(kRouterWarps * 32), 0, s, a.logits, a.T, \
-                   a.E, a.k, tpc, a.ids, a.w, a.hist, a.sqrtsp, a.bias)
+  err = a.sqrtsp                                                                            \
+            ? launch_pdl(router_kernel<V, true>, dim3(rblocks), dim3(kRouterWarps * 32), 0, s, \
+                         a.logits, a.T, a.E, a.k, tpc, a.ids, a.w, a.hist, a.bias)          \
+            : launch_pdl(router_kernel<V, false>, dim3(rblocks), dim3(kRouterWarps * 32), 0, s, \
+                         a.logits, a.T, a.E, a.k, tpc, a.ids, a.w, a.hist, a.bias)
   if (vpl <= 1) NVFP4MOE_ROUTER(1);
   else if (vpl <= 2) NVFP4MOE_ROUTER(2);
   else if (vpl <= 4) NVFP4MOE_ROUTER(4);

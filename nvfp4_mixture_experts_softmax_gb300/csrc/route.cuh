@@ -52,12 +52,12 @@ __device__ __forceinline__ float sqrt_softplus(float x) {
 // Top-k of one token's logits by one warp: lane l holds experts l, l+32, ...  Each of the k
 // rounds takes the warp maximum of the lanes' best keys, then the lowest expert index among the
 // lanes holding it (hardware redux.sync), so ties go to the lower index.  Lane j < k ends with
-// the j-th choice (my_id, my_l).  sqrtsp: the keys are sqrt(softplus(logit)) + bias[e] (bias may
+// the j-th choice (my_id, my_l).  SQRTSP: the keys are sqrt(softplus(logit)) + bias[e] (bias may
 // be null) and my_l is the unbiased score sqrt(softplus(logit)); otherwise keys and my_l are the
 // logits.
-template <int VPL>
+template <int VPL, bool SQRTSP = false>
 __device__ __forceinline__ void warp_topk(const float* __restrict__ row, int E, int k, int lane,
-                                          int& my_id, float& my_l, int sqrtsp = 0,
+                                          int& my_id, float& my_l,
                                           const float* __restrict__ bias = nullptr) {
   float v[VPL];
   uint32_t key[VPL];
@@ -67,7 +67,7 @@ __device__ __forceinline__ void warp_topk(const float* __restrict__ row, int E, 
     const int e = lane + 32 * i;
     if (e < E) {
       const float l = __ldg(row + e);
-      if (sqrtsp) {
+      if constexpr (SQRTSP) {
         v[i] = sqrt_softplus(l);
         key[i] = order_key(v[i] + (bias ? __ldg(bias + e) : 0.0f));
       } else {
@@ -100,9 +100,10 @@ __device__ __forceinline__ void warp_topk(const float* __restrict__ row, int E, 
 }
 
 // Renormalised softmax weights of the k chosen logits, summed in slot order; lanes < k write.
-// sqrtsp: the chosen (unbiased) scores divided by their sum, summed in slot order.
-__device__ __forceinline__ float topk_weight(float my_l, int k, int lane, int sqrtsp = 0) {
-  if (sqrtsp) {
+// SQRTSP: the chosen (unbiased) scores divided by their sum, summed in slot order.
+template <bool SQRTSP = false>
+__device__ __forceinline__ float topk_weight(float my_l, int k, int lane) {
+  if constexpr (SQRTSP) {
     float sum = 0.0f;
     for (int j = 0; j < k; ++j) sum = sum + __shfl_sync(0xffffffffu, my_l, j);
     return __fdiv_rn(my_l, sum);
@@ -206,13 +207,13 @@ __device__ __forceinline__ void small_place(int T, int E, int k, int shared_rows
 }
 
 // Route T tokens (T*k <= kSmallPlanRows) inside one block, count per expert, then place (above).
-template <int VPL>
+template <int VPL, bool SQRTSP>
 __device__ __forceinline__ void small_plan_body(
     const float* __restrict__ logits, int T, int E, int k, int shared_rows,
     int32_t* __restrict__ ids, float* __restrict__ wout, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ tile_start,
     int32_t* __restrict__ perm_src, float* __restrict__ perm_w, int32_t* __restrict__ inv,
-    uint8_t* dyn, int32_t* __restrict__ perm_seg = nullptr, int sqrtsp = 0,
+    uint8_t* dyn, int32_t* __restrict__ perm_seg = nullptr,
     const float* __restrict__ bias = nullptr) {
   int32_t* s_cnt = reinterpret_cast<int32_t*>(dyn);
   int32_t* s_ids = s_cnt + 3 * E;
@@ -224,8 +225,8 @@ __device__ __forceinline__ void small_plan_body(
   for (int t = warp; t < T; t += nw) {
     int my_id;
     float my_l;
-    warp_topk<VPL>(logits + (int64_t)t * E, E, k, lane, my_id, my_l, sqrtsp, bias);
-    const float w = topk_weight(my_l, k, lane, sqrtsp);
+    warp_topk<VPL, SQRTSP>(logits + (int64_t)t * E, E, k, lane, my_id, my_l, bias);
+    const float w = topk_weight<SQRTSP>(my_l, k, lane);
     if (lane < k) {
       ids[(int64_t)t * k + lane] = my_id;
       wout[(int64_t)t * k + lane] = w;
