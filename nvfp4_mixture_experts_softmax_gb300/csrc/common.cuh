@@ -127,10 +127,9 @@ __device__ __forceinline__ void quant_block16_fast(const float* x, float ts, flo
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
 
-// NVFP4 quantisation of BF16 block b (elements 16b .. 16b+15 of x) with tensor scale ts.
-__device__ __forceinline__ void quant_bf16_block16(const uint4* __restrict__ x, int64_t b, float ts,
-                                                   uint32_t& lo, uint32_t& hi, uint32_t& sf) {
-  const uint4 v0 = __ldg(x + 2 * b), v1 = __ldg(x + 2 * b + 1);
+// NVFP4 quantisation of one BF16 block held in registers (v0: elements 0-7, v1: elements 8-15).
+__device__ __forceinline__ void quant_bf16_regs16(uint4 v0, uint4 v1, float ts, uint32_t& lo,
+                                                  uint32_t& hi, uint32_t& sf) {
   const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
   float f[16];
 #pragma unroll
@@ -139,6 +138,12 @@ __device__ __forceinline__ void quant_bf16_block16(const uint4* __restrict__ x, 
     f[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
   }
   quant_block16(f, ts, lo, hi, sf);
+}
+
+// NVFP4 quantisation of BF16 block b (elements 16b .. 16b+15 of x) with tensor scale ts.
+__device__ __forceinline__ void quant_bf16_block16(const uint4* __restrict__ x, int64_t b, float ts,
+                                                   uint32_t& lo, uint32_t& hi, uint32_t& sf) {
+  quant_bf16_regs16(__ldg(x + 2 * b), __ldg(x + 2 * b + 1), ts, lo, hi, sf);
 }
 
 // NVFP4 encode of BF16 block b (elements 16b .. 16b+15 of x): 8 code bytes and 1 scale byte.

@@ -40,19 +40,39 @@ __global__ void __launch_bounds__(kSmallPlanThreads) prologue_small_kernel(const
                                a.perm_seg, a.bias);
 }
 
-// Decode batches (T <= kDecodeMaxRows): a cluster of kDecodeProCtas CTAs in two phases around
-// one cluster barrier.
-//   A: one warp per token routes (top-k + weights, written to global memory and to the routing
-//      CTA's shared memory) while every CTA reduces max |x| over its slice of x;
+// Decode batches (T <= kDecodeMaxRows = 64): a cluster of kDecodeProCtas CTAs around one cluster
+// barrier.
+//   A: every thread loads one 16-element block of x, which it keeps in registers for the encode,
+//      and takes its max |x|; token t is routed by warp t / C of CTA t % C (C = kDecodeProCtas), the
+//      results going to global memory and to the routing CTA's shared memory.
 //   B: every CTA combines the partial maxima through distributed shared memory into the tensor
-//      scale, gathers the other CTAs' routing results the same way and places all assignments
-//      itself (the same stable plan in every CTA; CTA 0 alone writes it to global memory).  Then
-//      one thread per (token, 16-element block) encodes the block once and writes it in token
-//      order and into each of the token's expert-ordered rows: the codes into xq_perm, the
-//      scale byte into the 32x4x4 arrangement of the decode GEMM's token operand (tile = the
-//      expert's tile index, row = expert-ordered row - the expert's offset).
+//      scale and gathers the other CTAs' routing results.  Each expert gets the mask of the tokens
+//      that chose it (one bit per token: T <= 64), so its count is popcount(mask) and the stable
+//      position of token t's assignment to it is offset + popcount(mask & (2^t - 1)): the order of
+//      the general plan (expert-major, then assignment order), because a token picks an expert at
+//      most once.  Every CTA computes the same plan; CTA 0 alone writes it to global memory.  A table
+//      gives each (token, slot) its expert-ordered row and the offset of its scale bytes in the
+//      32x4x4 arrangement of the decode GEMM's token operand (tile = the expert's tile index,
+//      row = rank within the expert); then every thread encodes its block once and writes it in
+//      token order and to each of the token's expert rows.
 // A CTA keeps its shared memory until the cluster's other CTAs have finished reading it (split
 // cluster barrier: arrive after the last remote read, wait before exit).
+struct DecodeSmem {
+  // byte offsets into the dynamic shared memory
+  size_t mask, sfo, ids, w, off, toff, dst, total;
+  __host__ __device__ DecodeSmem(int E, int k) {
+    const size_t kd = (size_t)k + 1;
+    mask = 0;                                                      // u64 [E]
+    sfo = mask + 8 * (size_t)E;                                    // i64 [64 * kd]
+    ids = sfo + 8 * kDecodeMaxRows * kd;                           // i32 [64 * k]
+    w = ids + 4 * (size_t)kDecodeMaxRows * k;                      // f32 [64 * k]
+    off = w + 4 * (size_t)kDecodeMaxRows * k;                      // i32 [E + 1]
+    toff = off + 4 * ((size_t)E + 1);                              // i32 [E + 1]
+    dst = toff + 4 * ((size_t)E + 1);                              // i32 [64 * kd]
+    total = dst + 4 * kDecodeMaxRows * kd;
+  }
+};
+
 template <int VPL, bool SQRTSP>
 __global__ void __launch_bounds__(kSmallPlanThreads) decode_prologue_kernel(const DecodePrologueArgs a) {
   extern __shared__ __align__(16) uint8_t s_dyn[];
@@ -61,53 +81,60 @@ __global__ void __launch_bounds__(kSmallPlanThreads) decode_prologue_kernel(cons
   __shared__ float s_ts;
   griddep_wait();
   griddep_launch();
+  constexpr int C = kDecodeProCtas;
+  constexpr int nw = kSmallPlanThreads / 32;
   const uint32_t rank = cluster_ctarank();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int nw = kSmallPlanThreads / 32;
   const uint4* x = reinterpret_cast<const uint4*>(a.x);
-  const int R = a.T * a.k;
+  const int T = a.T, E = a.E, k = a.k;
+  const int kd = k + 1;   // destinations of a token: its k expert rows, then the shared expert's
+  const int R = T * k;
   const int Rt = R + a.shared_rows;
   const int nkb = a.H / 16;
-  // small_place's scratch, then the per-assignment expert-ordered row and the per-expert tile
-  int32_t* s_ids = reinterpret_cast<int32_t*>(s_dyn) + 3 * a.E;
-  float* s_w = reinterpret_cast<float*>(s_ids + kSmallPlanRows);
-  int32_t* s_off = reinterpret_cast<int32_t*>(s_dyn) + a.E;
-  int32_t* s_inv = reinterpret_cast<int32_t*>(s_dyn + small_plan_smem_bytes(a.E));
-  int32_t* s_toff = s_inv + kSmallPlanRows;
+  const DecodeSmem L(E, k);
+  unsigned long long* s_mask = reinterpret_cast<unsigned long long*>(s_dyn + L.mask);
+  long long* s_sfo = reinterpret_cast<long long*>(s_dyn + L.sfo);
+  int32_t* s_ids = reinterpret_cast<int32_t*>(s_dyn + L.ids);
+  float* s_w = reinterpret_cast<float*>(s_dyn + L.w);
+  int32_t* s_off = reinterpret_cast<int32_t*>(s_dyn + L.off);
+  int32_t* s_toff = reinterpret_cast<int32_t*>(s_dyn + L.toff);
+  int32_t* s_dst = reinterpret_cast<int32_t*>(s_dyn + L.dst);
   if (rank == 0 && threadIdx.x == 0) *a.status = 0;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_mask[e] = 0ull;
 
-  // ---- A: routing (warp per token) and partial max |x| ----
-  // the first two activation vectors of each thread are loaded before the routing so that their
-  // memory latency overlaps the logits'
-  const int64_t nvec = (int64_t)a.T * a.H / 8;
-  const int64_t vstride = (int64_t)kDecodeProCtas * blockDim.x;
-  const int64_t v0 = (int64_t)rank * blockDim.x + threadIdx.x;
-  uint4 xv0 = make_uint4(0u, 0u, 0u, 0u), xv1 = make_uint4(0u, 0u, 0u, 0u);
-  if (v0 < nvec) xv0 = __ldg(x + v0);
-  if (v0 + vstride < nvec) xv1 = __ldg(x + v0 + vstride);
-  for (int t = (int)rank * nw + warp; t < a.T; t += kDecodeProCtas * nw) {
+  // ---- A: this thread's first block of x (its load overlaps the routing), routing, max |x| ----
+  const int64_t nblk = (int64_t)T * nkb;
+  const int64_t bstride = (int64_t)C * blockDim.x;
+  const int64_t u0 = (int64_t)rank * blockDim.x + threadIdx.x;
+  uint4 xa = make_uint4(0u, 0u, 0u, 0u), xb = xa;
+  if (u0 < nblk) {
+    xa = __ldg(x + 2 * u0);
+    xb = __ldg(x + 2 * u0 + 1);
+  }
+  for (int t = warp * C + (int)rank; t < T; t += nw * C) {
     int my_id;
     float my_l;
-    warp_topk<VPL, SQRTSP>(a.logits + (int64_t)t * a.E, a.E, a.k, lane, my_id, my_l, a.bias);
-    const float w = topk_weight<SQRTSP>(my_l, a.k, lane);
-    if (lane < a.k) {
-      a.ids[(int64_t)t * a.k + lane] = my_id;
-      a.w[(int64_t)t * a.k + lane] = w;
-      s_ids[t * a.k + lane] = my_id;
-      s_w[t * a.k + lane] = w;
+    warp_topk<VPL, SQRTSP>(a.logits + (int64_t)t * E, E, k, lane, my_id, my_l, a.bias);
+    const float w = topk_weight<SQRTSP>(my_l, k, lane);
+    if (lane < k) {
+      a.ids[(int64_t)t * k + lane] = my_id;
+      a.w[(int64_t)t * k + lane] = w;
+      s_ids[t * k + lane] = my_id;
+      s_w[t * k + lane] = w;
     }
   }
   {
-    uint32_t m = max(abs_bf16_max8(xv0), abs_bf16_max8(xv1));
-    for (int64_t i = v0 + 2 * vstride; i < nvec; i += vstride) m = max(m, abs_bf16_max8(__ldg(x + i)));
+    uint32_t m = max(abs_bf16_max8(xa), abs_bf16_max8(xb));
+    for (int64_t u = u0 + bstride; u < nblk; u += bstride)
+      m = max(m, max(abs_bf16_max8(__ldg(x + 2 * u)), abs_bf16_max8(__ldg(x + 2 * u + 1))));
     m = block_max_u32(m, red);
     if (threadIdx.x == 0) s_part = m;
   }
   cluster_sync();
 
-  // ---- B: tensor scale and routing results from every CTA, then the plan in every CTA ----
+  // ---- B: tensor scale, every CTA's routing results, token masks per expert ----
   if (threadIdx.x < 32) {
-    uint32_t m = threadIdx.x < kDecodeProCtas ? ld_dsmem_u32(&s_part, threadIdx.x) : 0u;
+    uint32_t m = threadIdx.x < C ? ld_dsmem_u32(&s_part, threadIdx.x) : 0u;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
     if (threadIdx.x == 0) {
@@ -120,63 +147,124 @@ __global__ void __launch_bounds__(kSmallPlanThreads) decode_prologue_kernel(cons
     }
   }
   for (int i = threadIdx.x; i < R; i += blockDim.x) {
-    const uint32_t owner = (uint32_t)((i / a.k) / nw) % kDecodeProCtas;   // CTA that routed token
+    const int t = i / k;
+    const uint32_t owner = (uint32_t)(t % C);
+    int32_t e = s_ids[i];
     if (owner != rank) {
-      s_ids[i] = (int32_t)ld_dsmem_u32(&s_ids[i], owner);
+      e = (int32_t)ld_dsmem_u32(&s_ids[i], owner);
+      s_ids[i] = e;
       s_w[i] = __uint_as_float(ld_dsmem_u32(&s_w[i], owner));
     }
+    if (e >= 0 && e < E) atomicOr(&s_mask[e], 1ull << t);
   }
   cluster_arrive();   // no remote reads of this cluster after this point
-  int32_t* s_cnt = reinterpret_cast<int32_t*>(s_dyn);
-  for (int e = threadIdx.x; e < a.E; e += blockDim.x) s_cnt[e] = 0;
   __syncthreads();
-  for (int i = threadIdx.x; i < R; i += blockDim.x) {
-    const int e = s_ids[i];
-    if (e >= 0 && e < a.E) atomicAdd(&s_cnt[e], 1);
+
+  // counts, offsets and tile starts: one warp, E / 32 consecutive experts per lane
+  const bool out = rank == 0;
+  if (warp == 0) {
+    const int per = (E + 31) / 32;
+    const int e0 = min(lane * per, E), e1 = min(e0 + per, E);
+    int c = 0, tc = 0;
+    for (int e = e0; e < e1; ++e) {
+      const int n = __popcll(s_mask[e]);
+      c += n;
+      tc += (n + kBM - 1) / kBM;
+    }
+    int ci = c, ti = tc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, ci, o);
+      const int z = __shfl_up_sync(0xffffffffu, ti, o);
+      if (lane >= o) {
+        ci += y;
+        ti += z;
+      }
+    }
+    int off = ci - c, toff = ti - tc;
+    for (int e = e0; e < e1; ++e) {
+      const int n = __popcll(s_mask[e]);
+      s_off[e] = off;
+      s_toff[e] = toff;
+      if (out) {
+        if (a.counts) a.counts[e] = n;
+        a.offsets[e] = off;
+        a.tile_start[e] = toff;
+      }
+      off += n;
+      toff += (n + kBM - 1) / kBM;
+    }
+    if (lane == 31) {
+      s_off[E] = ci;
+      s_toff[E] = ti;
+      if (out) {
+        a.offsets[E] = ci;
+        a.tile_start[E] = ti;
+        if (a.shared_rows > 0) {
+          a.offsets[E + 1] = ci + a.shared_rows;
+          a.tile_start[E + 1] = ti + (a.shared_rows + kBM - 1) / kBM;
+        }
+      }
+    }
   }
   __syncthreads();
-  const bool out = rank == 0;
-  small_place(a.T, a.E, a.k, a.shared_rows, out ? a.counts : nullptr, out ? a.offsets : nullptr,
-              out ? a.tile_start : nullptr, out ? a.perm_src : nullptr, out ? a.perm_w : nullptr,
-              out ? a.inv : nullptr, s_dyn, out ? a.perm_seg : nullptr, s_inv, s_toff);
-  __syncthreads();
-  const float ts = s_ts;
 
-  // ---- encode each (token, block) once into token order and into the token's expert rows ----
+  // destination table: expert-ordered row and scale-byte offset of each (token, slot)
   const int wpr = a.H / 64;   // 4-scale words per row
-  const int64_t nblk = (int64_t)a.T * nkb;
-  for (int64_t u = (int64_t)rank * blockDim.x + threadIdx.x; u < nblk;
-       u += (int64_t)kDecodeProCtas * blockDim.x) {
-    const int t = (int)(u / nkb), b = (int)(u - (int64_t)t * nkb);
-    uint32_t lo, hi, sf;
-    quant_bf16_block16(x, u, ts, lo, hi, sf);
-    reinterpret_cast<uint2*>(a.xq)[u] = make_uint2(lo, hi);
-    a.xsf[u] = (uint8_t)sf;
-    for (int j = 0; j <= a.k; ++j) {
-      int p, r, tile;
-      if (j < a.k) {
-        const int e = s_ids[t * a.k + j];
-        if (e < 0 || e >= a.E) {
-          set_status(a.status, MOE_ERR_INVALID_ARG);
-          continue;
-        }
-        p = s_inv[t * a.k + j];
-        r = p - s_off[e];
+  // tiles of the token-operand scale arrangement: one per active expert (and the shared one)
+  const int ntiles = min(E + (a.shared_rows > 0 ? 1 : 0), Rt);
+  for (int i = threadIdx.x; i < T * kd; i += blockDim.x) {
+    const int t = i / kd, j = i - t * kd;
+    int p = -1, r = 0, tile = 0, e = E;
+    if (j < k) {
+      e = s_ids[t * k + j];
+      if (e >= 0 && e < E) {
+        r = __popcll(s_mask[e] & ((1ull << t) - 1ull));
+        p = s_off[e] + r;
         tile = s_toff[e];
       } else {
-        if (a.shared_rows == 0) break;
-        p = R + t;        // the shared expert's rows follow the routed ones, in token order
-        r = t;
-        tile = s_toff[a.E];
-      }
-      if (p < 0 || p >= Rt || r < 0 || r >= kDecodeMaxRows || tile < 0 || tile > Rt) {
         set_status(a.status, MOE_ERR_INVALID_ARG);
-        continue;
       }
+    } else if (a.shared_rows > 0) {   // the shared expert's rows follow the routed ones
+      p = R + t;
+      r = t;
+      tile = s_toff[E];
+    }
+    if (p >= 0 && (p >= Rt || r >= kDecodeMaxRows || tile < 0 || tile >= ntiles)) {
+      set_status(a.status, MOE_ERR_INVALID_ARG);
+      p = -1;
+    }
+    if (out && p >= 0) {
+      a.perm_src[p] = t;
+      a.perm_w[p] = j < k ? s_w[t * k + j] : 1.0f;
+      a.perm_seg[p] = e;
+      if (j < k) a.inv[t * k + j] = p;
+    }
+    s_dst[i] = p;
+    s_sfo[i] = ((long long)tile * wpr) * 512 + (r & 31) * 16 + (r >> 5) * 4;
+  }
+  __syncthreads();
+
+  // ---- encode each (token, block) once into token order and into the token's expert rows ----
+  const float ts = s_ts;
+  for (int64_t u = u0; u < nblk; u += bstride) {
+    uint4 v0 = xa, v1 = xb;
+    if (u != u0) {
+      v0 = __ldg(x + 2 * u);
+      v1 = __ldg(x + 2 * u + 1);
+    }
+    const int t = (int)(u / nkb), b = (int)(u - (int64_t)t * nkb);
+    uint32_t lo, hi, sf;
+    quant_bf16_regs16(v0, v1, ts, lo, hi, sf);
+    reinterpret_cast<uint2*>(a.xq)[u] = make_uint2(lo, hi);
+    a.xsf[u] = (uint8_t)sf;
+    const long long boff = (long long)(b >> 2) * 512 + (b & 3);
+    for (int j = 0; j < kd; ++j) {
+      const int p = s_dst[t * kd + j];
+      if (p < 0) continue;
       *reinterpret_cast<uint2*>(a.xq_perm + (size_t)p * (a.H / 2) + (size_t)b * 8) =
           make_uint2(lo, hi);
-      a.xsf_tiles[((size_t)tile * wpr + b / 4) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (b & 3)] =
-          (uint8_t)sf;
+      a.xsf_tiles[s_sfo[t * kd + j] + boff] = (uint8_t)sf;
     }
   }
   cluster_wait();
@@ -185,8 +273,8 @@ __global__ void __launch_bounds__(kSmallPlanThreads) decode_prologue_kernel(cons
 }  // namespace
 
 cudaError_t launch_decode_prologue(const DecodePrologueArgs& a, cudaStream_t s) {
-  // small_place's scratch + expert-ordered row per assignment + first tile per segment
-  const size_t smem = small_plan_smem_bytes(a.E) + sizeof(int32_t) * (kSmallPlanRows + a.E + 1);
+  if (a.T > kDecodeMaxRows || a.k > 32) return cudaErrorInvalidValue;
+  const size_t smem = DecodeSmem(a.E, a.k).total;
   const int vpl = (a.E + 31) / 32;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(kDecodeProCtas);

@@ -128,17 +128,14 @@ __host__ __device__ inline size_t small_plan_smem_bytes(int E) {
 // match_any and each warp adds the counts of the warps before it; a per-expert cursor carries
 // the counts of earlier groups.  Must be called by all kSmallPlanThreads threads of the block;
 // `dyn` is the dynamic shared memory laid out as in small_plan_body.  Every global output may be
-// null (nothing written); s_inv (kSmallPlanRows entries) and s_toff (E + 1 entries), when given,
-// receive the expert-ordered row of each assignment and each expert's first tile in shared memory.
+// null (nothing written).
 __device__ __forceinline__ void small_place(int T, int E, int k, int shared_rows,
                                             int32_t* __restrict__ counts,
                                             int32_t* __restrict__ offsets,
                                             int32_t* __restrict__ tile_start,
                                             int32_t* __restrict__ perm_src,
                                             float* __restrict__ perm_w, int32_t* __restrict__ inv,
-                                            uint8_t* dyn, int32_t* __restrict__ perm_seg,
-                                            int32_t* __restrict__ s_inv = nullptr,
-                                            int32_t* __restrict__ s_toff = nullptr) {
+                                            uint8_t* dyn, int32_t* __restrict__ perm_seg) {
   int32_t* s_cnt = reinterpret_cast<int32_t*>(dyn);
   int32_t* s_off = s_cnt + E;
   int32_t* s_cur = s_off + E;
@@ -159,10 +156,8 @@ __device__ __forceinline__ void small_place(int T, int E, int k, int shared_rows
     if (counts) counts[e] = cnt;
     if (offsets) offsets[e] = off;
     if (tile_start) tile_start[e] = toff;
-    if (s_toff) s_toff[e] = toff;
   }
   if (threadIdx.x == 0) {
-    if (s_toff) s_toff[E] = ttotal;
     if (offsets) offsets[E] = total;
     if (offsets && shared_rows > 0) offsets[E + 1] = total + shared_rows;
     if (tile_start) {
@@ -189,7 +184,6 @@ __device__ __forceinline__ void small_place(int T, int E, int k, int shared_rows
       if (perm_w) perm_w[p] = s_w[a];
       if (perm_seg) perm_seg[p] = ea;
       if (inv) inv[a] = p;
-      if (s_inv) s_inv[a] = p;
     }
     __syncthreads();
     for (int x = threadIdx.x; x < E; x += blockDim.x) {
