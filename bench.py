@@ -505,6 +505,8 @@ def run_ours(args, world, rank, local):
                     "rows_per_expert": {str(T): rows_per_expert[T] for T in Ts},
                     "useful_weight_bytes": {str(T): touched[T] * expert_bytes(cs) for T in Ts}},
         "stage_share": {n: round(v / sum(stage_ms.values()), 4) for n, v in stage_ms.items()},
+        "stage_us_per_T": {str(T): {n: round(statistics.median(v) * 1e3, 2) for n, v in d.items() if v}
+                           for T, d in stage_ms_T.items()},
         "fp4_peak_frac": round(eff_tflops / (bf16_peak * FP4_PER_BF16), 4),
         "roofline": dict(kernel=f"{dominant} (T={Tr} launches)", **roof,
                          avg_launch_us=round(dom_launch_s * 1e6, 2), traffic=traffic),
