@@ -184,8 +184,10 @@ def expert_bytes(cs):
     return 3 * per_matrix * 9 // 16
 
 
-def layer_counters(cs, T, touched, has_shared):
-    """Algorithmic bytes / FLOPs of one call (touched experts' weights counted once)."""
+def layer_counters(cs, T, touched, has_shared, decode=False):
+    """Algorithmic bytes / FLOPs of one call (touched experts' weights counted once).  Decode-sized
+    batches run both grouped GEMMs as one launch ("grouped_gemms") whose down projection stores
+    one FP32 row per assignment instead of reducing into the token rows."""
     H, I, k = cs.hidden, cs.inter, cs.top_k
     R = T * k
     rows = R + (T if has_shared else 0)
@@ -194,15 +196,20 @@ def layer_counters(cs, T, touched, has_shared):
     w2 = n_exp * H * I * 9 // 16
     act_in = T * H * 2 + T * cs.experts * 4
     out = T * H * 2
+    g1 = w13 + rows * H * 9 // 16 + rows * I * 9 // 16
+    g2 = w2 + rows * I * 9 // 16 + (rows * H * 4 if decode else T * H * 4)
     return dict(
         flops=rows * 6 * H * I,
+        grouped_gemms_flops=rows * 6 * H * I,
+        grouped_gemms=g1 + g2,
         gemm1_swiglu_flops=rows * 4 * H * I,
         gemm2_combine_flops=rows * 2 * H * I,
         layer_bytes=w13 + w2 + act_in + out,
         # GEMM1: gate/up weights + gathered activation codes/scales + requantised h out
-        gemm1_swiglu=w13 + rows * H * 9 // 16 + rows * I * 9 // 16,
-        # GEMM2: down weights + h codes/scales in + the FP32 token accumulator written
-        gemm2_combine=w2 + rows * I * 9 // 16 + T * H * 4,
+        gemm1_swiglu=g1,
+        # GEMM2: down weights + h codes/scales in + the FP32 token accumulator (or, decode, the
+        # stored FP32 rows) written
+        gemm2_combine=g2,
         act_quant=2 * T * H * 2 + T * H * 9 // 16 + T * H * 4,
         router_plan=T * cs.experts * 4 + R * 16,
         bf16_out=T * H * 4 + T * H * 2,
@@ -303,8 +310,9 @@ def run_ours(args, world, rank, local):
     touched = {T: len(np.unique(route_ids(T))) for T in Ts}
     rows_per_expert = {T: sorted(np.unique(route_ids(T), return_counts=True)[1].tolist(),
                                  reverse=True) for T in Ts}
-    counters = {T: layer_counters(cs, T, touched[T], has_shared) for T in Ts}
     launches = {T: moe.run_kernel_count(cfg, T) for T in Ts}
+    fused = {T: launches[T] == 3 for T in Ts}   # decode path: both GEMMs in one launch
+    counters = {T: layer_counters(cs, T, touched[T], has_shared, fused[T]) for T in Ts}
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
@@ -393,11 +401,23 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize()
         stage_records.append(timer.stage_ms())
 
-    stage_ms = {n: 0.0 for n in moe.STAGES}
-    stage_ms_T = {T: {n: [] for n in moe.STAGES} for T in Ts}
+    # the decode path's one GEMM launch is recorded under GEMM1's stage and leaves GEMM2's empty
+    stage_names = list(moe.STAGES)
+    if all(fused.values()):
+        stage_names = [n for n in stage_names if n != "gemm2_combine"]
+        stage_names[stage_names.index("gemm1_swiglu")] = "grouped_gemms"
+
+    def stage_name(n):
+        return "grouped_gemms" if n == "gemm1_swiglu" and all(fused.values()) else n
+
+    stage_ms = {n: 0.0 for n in stage_names}
+    stage_ms_T = {T: {n: [] for n in stage_names} for T in Ts}
     per_T_ms = {T: [] for T in Ts}
     for T, s_, c in zip(Tseq, stage_records, call_ms):
-        for n, v in s_.items():
+        for n0, v in s_.items():
+            n = stage_name(n0)
+            if n not in stage_ms:
+                continue
             stage_ms[n] += v
             stage_ms_T[T][n].append(v)
         per_T_ms[T].append(c)
@@ -412,7 +432,7 @@ def run_ours(args, world, rank, local):
     # dense FP4 tensor peak (measured BF16 peak x the nominal FP4/BF16 ratio)
     Tr = max(Ts)
     dom_launch_s = statistics.mean(stage_ms_T[Tr][dominant]) / 1e3
-    tensor_bound = Tr > 64 and dominant in ("gemm1_swiglu", "gemm2_combine")
+    tensor_bound = Tr > 64 and dominant in ("gemm1_swiglu", "gemm2_combine", "grouped_gemms")
     if tensor_bound:
         fp4_peak = bf16_peak * FP4_PER_BF16
         achieved = counters[Tr][dominant + "_flops"] / dom_launch_s / 1e12

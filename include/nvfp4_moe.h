@@ -211,8 +211,8 @@ size_t moe_workspace_size(const moe_config* cfg, int32_t T);
 
 /* Number of kernels one moe_run(cfg, ..., T, ...) launches (memset nodes not counted), or a
  * negative moe_status for an invalid cfg / T.  Host-only arithmetic: no CUDA call, no device.
- * It mirrors moe_run's choice of path: 4 for decode-sized batches (cluster prologue, GEMM1,
- * GEMM2, row sum), 5 for other small batches, 6 or 8 for large ones (the router and plan take one
+ * It mirrors moe_run's choice of path: 3 for decode-sized batches (cluster prologue, both grouped
+ * GEMMs in one persistent launch, row sum), 5 for other small batches, 6 or 8 for large ones (the router and plan take one
  * kernel up to 2048 routed rows, three above).  A utility for launch accounting; the pages have
  * no counterpart. */
 int moe_run_kernel_count(const moe_config* cfg, int32_t T);

@@ -214,7 +214,7 @@ int moe_run_kernel_count(const moe_config* cfg, int32_t T) {
   if (T < 0) return MOE_ERR_INVALID_ARG;
   if (T == 0) return 0;
   const RunLayout L(*cfg, T);
-  if (L.decode) return 4;     // cluster prologue, GEMM1, GEMM2, row sum
+  if (L.decode) return 3;     // cluster prologue, both grouped GEMMs, row sum
   if (L.small) return 5;      // one-block prologue, permute, GEMM1, GEMM2, row sum
   // amax, router/plan (1 or 3), encode into expert order, GEMM1, GEMM2, BF16 conversion
   return 1 + ((int64_t)T * cfg->top_k <= kSmallPlanRows ? 1 : 3) + 4;
@@ -291,6 +291,9 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
     pr.perm_seg = i32(L.perm_seg);
     pr.sqrtsp = sqrtsp;
     pr.bias = rbias;
+    pr.ready = i32(L.ready);
+    pr.nready = L.dtiles;
+    pr.plan_flag = i32(L.ready) + L.dtiles;
     e = launch_decode_prologue(pr, s);
     if (e == cudaSuccess) e = mark(1);
     if (e == cudaSuccess) e = mark(2);
@@ -399,20 +402,22 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
   g.status = &hdr->status;
   g.swiglu_clamp = (cfg->flags & MOE_FLAG_SWIGLU_CLAMP) ? 1 : 0;
   g.swiglu_limit = cfg->swiglu_limit;
-  // decode-sized batches: every expert has at most T <= kDecodeMaxRows rows, one tile each
+  // decode-sized batches: tiles of kDecodeTileRows rows of one expert each
   const bool decode = L.decode;
   g.a_codes = ws + L.xq_perm;            // expert-ordered activations, read by TMA boxes
   g.a_sf_tiles = ws + L.xsf_tiles;
   g.hsf_tiles = ws + L.hsf_tiles;
-  const int64_t item_rows = decode ? std::min<int64_t>(nseg, L.Rt) : max_mtiles;
+  const int64_t item_rows = decode ? (int64_t)L.dtiles : max_mtiles;
   g.max_items = (int)std::min<int64_t>(item_rows * (g.N / kBN), INT32_MAX);
   g.max_ctas = g.max_items;
   g.a_rows = T;
   g.out_rows = L.Rt;
   g.y_rows = T;
-  e = decode ? launch_grouped_gemm_decode(g, s) : launch_grouped_gemm(g, s);
-  if (e == cudaSuccess) e = mark(3);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (!decode) {
+    e = launch_grouped_gemm(g, s);
+    if (e == cudaSuccess) e = mark(3);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
 
   // 4. GEMM2 (down projection) with the router-weighted accumulation into the token rows
   GemmArgs g2 = g;
@@ -425,7 +430,6 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
   g2.N = H;
   g2.K = I;
   g2.mode = L.small ? 2 : 1;
-  g2.plan_early = decode ? 1 : 0;   // GEMM1 waited for the decode prologue before releasing GEMM2
   g2.perm_src = i32(L.perm_src);
   g2.perm_w = f32(L.perm_w);
   g2.yacc = f32(L.yacc);
@@ -433,7 +437,18 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
   g2.max_items = (int)std::min<int64_t>(item_rows * (g2.N / kBN), INT32_MAX);
   g2.max_ctas = g2.max_items;
   g2.a_rows = L.Rt;
-  e = decode ? launch_grouped_gemm_decode(g2, s) : launch_grouped_gemm(g2, s);
+  if (decode) {
+    // both GEMMs in one persistent launch; its time is reported as GEMM1's stage
+    DecodeGemmArgs dg{};
+    dg.g1 = g;
+    dg.g2 = g2;
+    dg.ready = i32(L.ready);
+    dg.plan_flag = i32(L.ready) + L.dtiles;
+    e = launch_grouped_gemm_decode(dg, s);
+    if (e == cudaSuccess) e = mark(3);
+  } else {
+    e = launch_grouped_gemm(g2, s);
+  }
   if (e == cudaSuccess) e = mark(4);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 

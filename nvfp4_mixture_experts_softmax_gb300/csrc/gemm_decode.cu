@@ -1,25 +1,35 @@
-// Grouped block-scaled FP4 GEMM for decode-sized batches (every expert receives at most 64 rows),
-// with the operands swapped: the expert's weights are the MMA's A operand (M = 128 weight rows of
-// one packed block per K stage, loaded by one bulk copy) and the expert's token rows are the
-// B operand (N = the rows rounded up to 16).  The tensor core then works on the real tokens
-// only, a pipeline stage is 28 KB instead of 36 KB (7 stages in flight), and the accumulator
-// holds one weight row per TMEM lane and one token per column:
-//   GEMM1 (mode 0): warp w of the epilogue holds the 16 gate rows and the 16 up rows of one
-//          16-feature NVFP4 block, so each half-warp computes silu(g)*u of one token and
-//          requantises the block with half-warp reductions;
-//   GEMM2 (mode 1 / 2): lanes hold consecutive output features, so a token's row is written (or
-//          reduced) 128 contiguous bytes per warp.
-// Every operand arrives by the copy engine: per stage one bulk copy of the weight block, one
-// 2-D TMA tile (128-byte swizzle) of the expert's token rows - the activations (GEMM1) or h
-// (GEMM2) are stored in expert order, so an expert's rows are contiguous - and one bulk copy of
-// the tokens' scales, which the producer kernels write pre-arranged per expert tile.  Warps:
-// 0-3 epilogue, 4 copy issue, 5 MMA, 6 scale factors ("nvfp4-megamoe-kernel compare
-// pre-b1...master", section "MoE kernel": TMA, MMA and epilogue warps; the pages keep decode on
-// 1-CTA tiles).  The eight shared -> tensor memory scale copies of a stage hold up the thread that
-// issues them for a long time, so a warp of their own issues them one stage ahead of the MMA
-// thread and signals it through an mbarrier; the MMA thread then issues only the four MMAs of a
-// stage, with descriptors advanced by additions.  Three TMEM accumulators let the epilogue trail
-// the main loop by up to two tiles.
+// Both grouped block-scaled FP4 GEMMs of a decode-sized batch (every expert receives at most 64
+// rows) in one persistent launch, with the operands swapped: the expert's weights are the MMA's
+// A operand (M = 128 weight rows of one packed block per K stage, loaded by one bulk copy) and
+// the expert's token rows are the B operand (N = the rows rounded up to 16).  The tensor core
+// then works on the real tokens only, a pipeline stage is 28 KB (7 stages in flight), and the
+// accumulator holds one weight row per TMEM lane and one token per column.
+//   GEMM1 items (phase 0): warp w of the epilogue holds the 16 gate rows and the 16 up rows of
+//          one 16-feature NVFP4 block, so each half-warp computes silu(g)*u of one token and
+//          requantises the block with half-warp reductions; each warp then publishes its share
+//          of the expert's h rows (release add on the expert's readiness count);
+//   GEMM2 items (phase 1): lanes hold consecutive output features, so a token's router-weighted
+//          row is stored 128 contiguous bytes per warp.
+// Every CTA takes its GEMM1 items first, then its GEMM2 items, all through one ring of stages:
+// the down-projection weights stream in as soon as ring slots free up (they depend on nothing),
+// and only the h rows of a GEMM2 item wait until all GEMM1 tiles of that expert are published.
+// This removes the second launch's ramp and the full drain between the two GEMMs, which at
+// decode sizes cost more than the weight stream itself.  CTAs wait on each other only through
+// the readiness counts, and only after finishing every GEMM1 item of their own, so with one CTA
+// per SM and a grid no larger than the SM count they cannot deadlock; every wait is bounded.
+// Every operand arrives by the copy engine: per stage one bulk copy of the weight block, 2-D TMA
+// tiles (128-byte swizzle) of the expert's token rows - the activations (GEMM1) or h (GEMM2) are
+// stored in expert order, so an expert's rows are contiguous - and one bulk copy of the tokens'
+// scales, which the producers write pre-arranged per expert tile.  Warps: 0-3 epilogue, 4 copy
+// issue, 5 MMA, 6 scale factors ("nvfp4-megamoe-kernel compare pre-b1...master", section "MoE
+// kernel": TMA, MMA and epilogue warps; the pages keep decode on 1-CTA tiles).  The eight
+// shared -> tensor memory scale copies of a stage hold up the thread that issues them for a long
+// time, so a warp of their own issues them one stage ahead of the MMA thread and signals it
+// through an mbarrier; the MMA thread then issues only the four MMAs of a stage, with
+// descriptors advanced by additions.  Three TMEM accumulators let the epilogue trail the main
+// loop by up to two tiles.
+#include <algorithm>
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -30,7 +40,7 @@ namespace nvfp4moe {
 
 namespace {
 
-constexpr int kStages = 7;
+constexpr int kStages = 9;
 constexpr int kAccBufs = 3;
 constexpr int kXBoxRows = 16;                          // token rows per TMA box
 constexpr int kEpiWarps = 4;
@@ -38,47 +48,49 @@ constexpr int kTmaWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kSfWarp = 6;
 constexpr int kThreads = (kSfWarp + 1) * 32;
-constexpr int kNmax = kDecodeMaxRows;                 // token rows per expert tile
+constexpr int kNmax = kDecodeTileRows;                // token rows per tile (the MMA N)
 constexpr int kXOff = kTileBlockBytes;                 // token codes after the weight block
 constexpr int kXBytes = kNmax * 128;
 constexpr int kXSfOff = kXOff + kXBytes;               // token scales
 constexpr int kXSfBytes = 4 * 512;
 constexpr int kStageBytes = kXSfOff + kXSfBytes;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCols = kNmax;
+constexpr uint32_t kAccCols = 32;                      // accumulator spacing (>= kNmax)
 constexpr uint32_t kSfCol0 = kAccBufs * kAccCols;
 constexpr uint32_t kSfColsPerStage = 32;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr int kBarBytes = 512;                          // mbarriers + TMEM slot
 
 static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "tensor memory budget");
 static_assert(kStageBytes % 1024 == 0 && kXOff % 1024 == 0, "1024-byte aligned swizzled tiles");
-static_assert(kStages * kStageBytes + 1024 + 256 + 8 * 1027 <= 232448, "shared memory");
-static_assert((3 * kStages + 2 * kAccBufs + 1) * 8 + 4 <= 256, "mbarriers + TMEM slot fit 256 B");
-static_assert(kNmax % kXBoxRows == 0 && kNmax <= 64, "token tile");
+static_assert(kStages * kStageBytes + 1024 + kBarBytes + 12 * 1028 <= 232448, "shared memory");
+static_assert((3 * kStages + 2 * kAccBufs + 3) * 8 + 4 <= kBarBytes, "mbarriers + TMEM slot");
+static_assert(kNmax == kXBoxRows && kNmax <= (int)kAccCols, "one TMA box of token rows per stage");
 
 constexpr uint32_t make_idesc(int M, int N) {
   return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-struct TileInfo {
-  int seg, m0, rows, nt;
+// One work item: (m-tile, 128-row weight tile) of GEMM1 (phase 0, items [0, total1)) or of GEMM2
+// (phase 1, items [total1, total1 + total2)).  An m-tile is kNmax consecutive rows of one expert
+// (s_tseg gives its segment); an expert with more rows than that owns several.
+struct Item {
+  int ph, seg, mt, m0, rows, nt, kst;
 };
 
-// Items are (active expert, 128-row weight tile); an active expert owns exactly one m-tile here.
-__device__ __forceinline__ TileInfo decode_item(int item, int n_tiles, const int32_t* s_tile,
-                                                const int32_t* s_seg, int nseg) {
-  TileInfo t;
-  const int mt = item / n_tiles;
-  t.nt = item - mt * n_tiles;
-  int lo = 0, hi = nseg - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (s_tile[mid] <= mt) lo = mid;
-    else hi = mid - 1;
-  }
-  t.seg = lo;
-  t.m0 = s_seg[lo];
-  t.rows = min(kNmax, s_seg[lo + 1] - t.m0);
+__device__ __forceinline__ Item decode_item(int item, int total1, int nt1, int nt2, int kst1,
+                                            int kst2, const int32_t* s_tseg, const int32_t* s_seg,
+                                            const int32_t* s_tile) {
+  Item t;
+  t.ph = item >= total1 ? 1 : 0;
+  const int local = t.ph ? item - total1 : item;
+  const int ntl = t.ph ? nt2 : nt1;
+  t.mt = local / ntl;
+  t.nt = local - t.mt * ntl;
+  t.kst = t.ph ? kst2 : kst1;
+  t.seg = s_tseg[t.mt];
+  t.m0 = s_seg[t.seg] + (t.mt - s_tile[t.seg]) * kNmax;
+  t.rows = min(kNmax, s_seg[t.seg + 1] - t.m0);
   return t;
 }
 
@@ -86,12 +98,10 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
   return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
-__device__ __forceinline__ void red_add_f32(float* addr, float v) {
-  asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
-    grouped_gemm_decode_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmArgs p) {
+    grouped_gemm_decode_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                               const __grid_constant__ CUtensorMap tmap_h,
+                               const DecodeGemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -102,11 +112,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_empty = acc_full + kAccBufs;
   uint64_t* drain = acc_empty + kAccBufs;
   uint64_t* sf_done = drain + 1;   // a stage's scale factors are in tensor memory
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_done + kStages);
-  int32_t* s_tile = reinterpret_cast<int32_t*>(smem + kStages * kStageBytes + 256);
-  int32_t* s_seg = s_tile + (p.nseg + 1);
+  uint64_t* plan_bar = sf_done + kStages;   // [0] the plan is in shared memory, [1] its copy
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(plan_bar + 2);
+  const int nseg = p.g1.nseg;
+  const int plan_ints = (nseg + 1 + 3) & ~3;    // 16-byte multiples for the bulk copies
+  int32_t* s_tile = reinterpret_cast<int32_t*>(smem + kStages * kStageBytes + kBarBytes);
+  int32_t* s_seg = s_tile + plan_ints;
+  int32_t* s_tseg = s_seg + plan_ints;     // m-tile -> segment
+  int32_t* status = p.g1.status;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  griddep_launch();   // the row sum may be scheduled; it waits for this grid to complete
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
@@ -122,92 +138,183 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(smem_u32(drain), 1);
     for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(sf_done + s), 1);
+    mbar_init(smem_u32(plan_bar), 1);
+    mbar_init(smem_u32(plan_bar + 1), 1);
     fence_barrier_init();
-  }
-  if (warp == kTmaWarp && lane == 0)
-    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_x) : "memory");
-  // plan_early: the plan was written two kernels back and is complete (the kernel in between
-  // waited for it before it let this one start), so only the copy issuer waits, and only before
-  // its first load of the previous kernel's output; the weights of the first stages are in
-  // flight by then
-  if (!p.plan_early) griddep_wait();
-  griddep_launch();
-  for (int i = threadIdx.x; i <= p.nseg; i += blockDim.x) {
-    s_tile[i] = __ldcg(p.tile_start + i);
-    s_seg[i] = __ldcg(p.seg_off + i);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int n_tiles = p.N / 128;
-  int total = s_tile[p.nseg] * n_tiles;
-  if (total < 0 || total > p.max_items) {
-    if (threadIdx.x == 0) set_status(p.status, MOE_ERR_INVALID_ARG);
-    total = 0;
+  if (warp == kTmaWarp) {
+    // The plan (segment offsets and tile starts) is published by the decode prologue before it
+    // encodes the activations: waiting for that flag instead of the prologue's completion lets
+    // the weight stream start while the prologue still runs.  A wait that times out leaves an
+    // empty plan (no items) and the status word set.
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_x) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_h) : "memory");
+    }
+    int ok = 1;
+    if (lane == 0) {
+      uint64_t t0 = 0;
+      for (uint32_t i = 0; ld_acquire_s32(p.plan_flag) == 0; ++i) {
+        if ((i & 63u) == 63u) {
+          const uint64_t now = global_timer_ns();
+          if (t0 == 0) {
+            t0 = now;
+          } else if (now - t0 > kWaitLimitNs) {
+            set_status(status, MOE_ERR_DEVICE_TIMEOUT);
+            ok = 0;
+            break;
+          }
+        }
+      }
+      if (ok) {
+        // both arrays in one round trip: two bulk copies (16-byte multiples; the arrays are
+        // allocated in 256-byte units, so the rounded-up tail stays inside them)
+        fence_proxy_async_global();
+        const uint32_t bytes = (uint32_t)((4 * (nseg + 1) + 15) & ~15);
+        const uint32_t pb = smem_u32(plan_bar + 1);
+        mbar_arrive_expect_tx(pb, 2 * bytes);
+        bulk_load(smem_u32(s_tile), p.g1.tile_start, bytes, pb);
+        bulk_load(smem_u32(s_seg), p.g1.seg_off, bytes, pb);
+        if (!mbar_wait_bounded(pb, 0u, kWaitLimitNs, status)) ok = 0;
+      }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    for (int i = lane; i <= nseg; i += 32) {
+      if (!ok) s_tile[i] = 0;
+      s_tseg[i] = 0;
+    }
+    __syncwarp();
+    for (int sg = lane; sg < nseg; sg += 32)
+      for (int mt = max(s_tile[sg], 0); mt < s_tile[sg + 1] && mt <= nseg; ++mt) s_tseg[mt] = sg;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(plan_bar));
+  } else {
+    mbar_wait_bounded(smem_u32(plan_bar), 0u, kWaitLimitNs, status);
   }
-  const int kst = p.K / kBK;
+
+  const int nt1 = p.g1.N / 128, nt2 = p.g2.N / 128;
+  const int kst1 = p.g1.K / kBK, kst2 = p.g2.K / kBK;
+  const int mtiles = s_tile[nseg];
+  int total1 = mtiles * nt1, total2 = mtiles * nt2;
+  if (mtiles < 0 || total1 > p.g1.max_items || total2 > p.g2.max_items) {
+    if (threadIdx.x == 0) set_status(status, MOE_ERR_INVALID_ARG);
+    total1 = total2 = 0;
+  }
+  const int total = total1 + total2;
+  // an expert's h rows are complete once every epilogue warp of its GEMM1 tiles has published
+  const int ready_target = nt1 * kEpiWarps;
   const uint32_t smem0 = smem_u32(smem);
+#define NVFP4MOE_ITEM(i) decode_item((i), total1, nt1, nt2, kst1, kst2, s_tseg, s_seg, s_tile)
 
   if (warp == kTmaWarp) {
-    // ---------------- all operands: bulk copies + one 2-D TMA tile per stage ----------------
+    // ---------------- all operands: bulk copies + 2-D TMA tiles ----------------
+    // Two cursors over this CTA's stages: the weight cursor issues a stage's weight block as
+    // soon as its ring slot is free (weights depend on nothing but the plan), the token cursor
+    // follows with the stage's token rows and their scales once they exist - after the
+    // prologue's completion for GEMM1, after the expert's h rows are published for GEMM2.  The
+    // full barrier of a stage expects both parts from the weight issue on.
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
       // only the boxes that hold the expert's rows (16 rows each); the rest of the token tile
       // stays stale and only feeds accumulator columns that are never stored
-      auto stage_bytes = [&](const TileInfo& t) {
+      auto stage_bytes = [&](const Item& t) {
         return (uint32_t)(kTileBlockBytes + ((max(t.rows, 1) + kXBoxRows - 1) / kXBoxRows) *
                                                 kXBoxRows * 128 + kXSfBytes);
       };
-      // weight blocks of the first stages (the ring is empty: no wait), before the wait for
-      // the previous kernel's output
-      int pre = 0;
-      if (p.plan_early) {
-        for (int item = blockIdx.x; item < total && pre < kStages; item += gridDim.x) {
-          const TileInfo t = decode_item(item, n_tiles, s_tile, s_seg, p.nseg);
-          const uint8_t* src = p.b_tiles + (size_t)t.seg * p.b_per_seg +
-                               (size_t)t.nt * kst * kTileBlockBytes;
-          for (int ks = 0; ks < kst && pre < kStages; ++ks, ++pre) {
-            const uint32_t fb = smem_u32(full + pre);
-            mbar_arrive_expect_tx(fb, stage_bytes(t));
-            bulk_load(smem0 + pre * kStageBytes, src + (size_t)ks * kTileBlockBytes,
-                      kTileBlockBytes, fb);
+      int wi = blockIdx.x, wks = 0, wstage = 0;
+      uint32_t wphase = 0;
+      int xi = blockIdx.x, xks = 0, xstage = 0;
+      Item wt{}, xt{};
+      if (wi < total) wt = xt = NVFP4MOE_ITEM(wi);
+      int nw = 0, nx = 0;           // stages whose weight / token parts are issued
+      bool x_ok = false, dep = false, ok = true;
+      uint64_t t0 = 0;
+      uint32_t idle = 0;
+      while (xi < total && ok) {
+        bool progress = false;
+        // 1. a free slot takes the next weight block at once
+        if (wi < total && mbar_test_wait(smem_u32(empty + wstage), wphase ^ 1u)) {
+          const uint32_t fb = smem_u32(full + wstage);
+          const GemmArgs& q = wt.ph ? p.g2 : p.g1;
+          const uint8_t* src = q.b_tiles + (size_t)wt.seg * q.b_per_seg +
+                               ((size_t)wt.nt * wt.kst + wks) * kTileBlockBytes;
+          mbar_arrive_expect_tx(fb, stage_bytes(wt));
+          bulk_load(smem0 + wstage * kStageBytes, src, kTileBlockBytes, fb);
+          ++nw;
+          if (++wstage == kStages) { wstage = 0; wphase ^= 1u; }
+          if (++wks == wt.kst) {
+            wks = 0;
+            wi += gridDim.x;
+            if (wi < total) wt = NVFP4MOE_ITEM(wi);
           }
+          progress = true;
         }
-        griddep_wait();
-      }
-      int g = 0;   // stages issued so far
-      for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
-        const TileInfo t = decode_item(item, n_tiles, s_tile, s_seg, p.nseg);
-        const uint8_t* src = p.b_tiles + (size_t)t.seg * p.b_per_seg +
-                             (size_t)t.nt * kst * kTileBlockBytes;
-        const uint8_t* xsf = p.a_sf_tiles + (size_t)s_tile[t.seg] * (p.K / 64) * 512;
-        const int nbox = (max(t.rows, 1) + kXBoxRows - 1) / kXBoxRows;
-        for (int ks = 0; ks < kst; ++ks, ++g) {
-          const uint32_t sb = smem0 + stage * kStageBytes;
-          const uint32_t fb = smem_u32(full + stage);
-          if (g >= pre) {
-            if (!mbar_wait_bounded(smem_u32(empty + stage), phase ^ 1u, kWaitLimitNs, p.status)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(fb, stage_bytes(t));
-            bulk_load(sb, src + (size_t)ks * kTileBlockBytes, kTileBlockBytes, fb);
-          }
+        // 2. token rows of every stage that has its weights and whose rows exist
+        while (nx < nw && dep && (xt.ph == 0 || x_ok)) {
+          const uint32_t sb = smem0 + xstage * kStageBytes;
+          const uint32_t fb = smem_u32(full + xstage);
+          const GemmArgs& q = xt.ph ? p.g2 : p.g1;
+          const uint8_t* sft = q.a_sf_tiles + ((size_t)xt.mt * (q.K / 64) + xks * 4) * 512;
+          const void* tm = xt.ph ? (const void*)&tmap_h : (const void*)&tmap_x;
+          const int nbox = (max(xt.rows, 1) + kXBoxRows - 1) / kXBoxRows;
           for (int bx = 0; bx < nbox; ++bx)
-            tma_load_2d(sb + kXOff + bx * kXBoxRows * 128, &tmap_x, ks * 128,
-                        t.m0 + bx * kXBoxRows, fb);
-          bulk_load(sb + kXSfOff, xsf + (size_t)ks * kXSfBytes, kXSfBytes, fb);
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+            tma_load_2d(sb + kXOff + bx * kXBoxRows * 128, tm, xks * 128,
+                        xt.m0 + bx * kXBoxRows, fb);
+          bulk_load(sb + kXSfOff, sft, kXSfBytes, fb);
+          ++nx;
+          if (++xstage == kStages) xstage = 0;
+          if (++xks == xt.kst) {
+            xks = 0;
+            xi += gridDim.x;
+            x_ok = false;
+            if (xi < total) {
+              xt = NVFP4MOE_ITEM(xi);
+              if (xt.ph == 1) {   // usually published long ago: look once right away
+                x_ok = ld_acquire_s32(p.ready + xt.mt) >= ready_target;
+                if (x_ok) fence_proxy_async_global();
+              }
+            }
+          }
+          progress = true;
+        }
+        if (progress) {
+          t0 = 0;
+          continue;
+        }
+        // 3. nothing to issue: wait for what the oldest stage's token rows need
+        if (nx < nw && !dep) {   // the activations, encoded by the prologue
+          griddep_wait();
+          dep = true;
+          continue;
+        }
+        if (nx < nw && xt.ph == 1 && !x_ok) {   // the expert's h rows, published by GEMM1
+          x_ok = ld_acquire_s32(p.ready + xt.mt) >= ready_target;
+          if (x_ok) {
+            fence_proxy_async_global();
+            continue;
+          }
+        }
+        if ((++idle & 255u) == 0u) {
+          const uint64_t now = global_timer_ns();
+          if (t0 == 0) {
+            t0 = now;
+          } else if (now - t0 > kWaitLimitNs) {
+            set_status(status, MOE_ERR_DEVICE_TIMEOUT);
+            ok = false;
+          }
         }
       }
+      // the MMAs of the last stages must finish before the CTA may exit
       for (int i = 0; i < kStages && ok; ++i) {
-        if (!mbar_wait_bounded(smem_u32(empty + stage), phase ^ 1u, kWaitLimitNs, p.status)) break;
-        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        if (!mbar_wait_bounded(smem_u32(empty + wstage), wphase ^ 1u, kWaitLimitNs, status)) break;
+        if (++wstage == kStages) { wstage = 0; wphase ^= 1u; }
       }
+      if (!dep) griddep_wait();
     }
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issue: D[weight row][token] ----------------
@@ -222,20 +329,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int it = 0;
       for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++it) {
-        const TileInfo t = decode_item(item, n_tiles, s_tile, s_seg, p.nseg);
+        const Item t = NVFP4MOE_ITEM(item);
         const int nmma = max(16, (t.rows + 15) & ~15);
         const uint32_t idesc = make_idesc(128, nmma);
         const int abuf = it % kAccBufs;
         if (!mbar_wait_bounded(smem_u32(acc_empty + abuf), acc_phase[abuf] ^ 1u, kWaitLimitNs,
-                               p.status)) {
+                               status)) {
           ok = false;
           break;
         }
         acc_phase[abuf] ^= 1u;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + abuf * kAccCols;
-        for (int ks = 0; ks < kst; ++ks) {
-          if (!mbar_wait_bounded(smem_u32(sf_done + stage), phase, kWaitLimitNs, p.status)) {
+        for (int ks = 0; ks < t.kst; ++ks) {
+          if (!mbar_wait_bounded(smem_u32(sf_done + stage), phase, kWaitLimitNs, status)) {
             ok = false;
             break;
           }
@@ -252,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) tc_commit(smem_u32(acc_full + abuf));
       }
       tc_commit(smem_u32(drain));
-      mbar_wait_bounded(smem_u32(drain), 0u, kWaitLimitNs, p.status);
+      mbar_wait_bounded(smem_u32(drain), 0u, kWaitLimitNs, status);
     }
   } else if (warp == kSfWarp) {
     // ---------------- scale factors: shared -> tensor memory, ahead of the MMA thread ---------
@@ -265,8 +372,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dSx0 = smem_desc(smem0 + kXSfOff, 0, 128, kLayoutSwizzleNone);
       bool ok = true;
       for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+        const int kst = item < total1 ? kst1 : kst2;
         for (int ks = 0; ks < kst; ++ks) {
-          if (!mbar_wait_bounded(smem_u32(full + stage), phase, kWaitLimitNs, p.status)) {
+          if (!mbar_wait_bounded(smem_u32(full + stage), phase, kWaitLimitNs, status)) {
             ok = false;
             break;
           }
@@ -285,117 +393,106 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------- epilogue (warps 0-3): lane = weight row, column = token ----------------
+    griddep_wait();     // the activation tensor scale and the router weights
     uint32_t acc_phase[kAccBufs] = {};
     int it = 0;
-    const float ts_a = p.mode == 0 ? *p.ts_a : 0.0f;
-    const float inv_ts_h = 1.0f / p.ts_h;
+    const float ts_a = *p.g1.ts_a;
+    const float ts_h = p.g1.ts_h;
+    const float inv_ts_h = 1.0f / ts_h;
     const bool lo_half = lane < 16;
     for (int item = blockIdx.x; item < total; item += gridDim.x, ++it) {
-      const TileInfo t = decode_item(item, n_tiles, s_tile, s_seg, p.nseg);
+      const Item t = NVFP4MOE_ITEM(item);
+      const GemmArgs& q = t.ph ? p.g2 : p.g1;
       const int abuf = it % kAccBufs;
-      if (!mbar_wait_bounded(smem_u32(acc_full + abuf), acc_phase[abuf], kWaitLimitNs, p.status))
+      if (!mbar_wait_bounded(smem_u32(acc_full + abuf), acc_phase[abuf], kWaitLimitNs, status))
         break;
       acc_phase[abuf] ^= 1u;
       tc_fence_after();
-      const int rows = (t.m0 >= 0 && t.m0 + t.rows <= p.out_rows) ? t.rows : 0;
+      const int rows = (t.m0 >= 0 && t.m0 + t.rows <= q.out_rows) ? t.rows : 0;
       const uint32_t tbase = tmem_base + abuf * kAccCols + ((uint32_t)(warp * 32) << 16);
-      if (p.mode == 0) {
+      if (t.ph == 0) {
         // block b of h: 16 features; lanes < 16 hold gate rows, lanes >= 16 the up rows
-        const int I = p.N / 2;
+        const int I = q.N / 2;
         const int b = t.nt * 4 + warp;
-        uint8_t* hsf_tile = p.hsf_tiles + ((size_t)s_tile[t.seg] * (I / 64) + b / 4) * 512 + (b & 3);
-        const float ag = ts_a * p.w_ts[t.seg * 4 + 0];
-        const float au = ts_a * p.w_ts[t.seg * 4 + 1];
-#pragma unroll 1
-        for (int cb = 0; cb < kNmax; cb += 32) {
-          if (cb >= rows) break;
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tbase + cb, v);
+        uint8_t* hsf_tile = q.hsf_tiles + ((size_t)t.mt * (I / 64) + b / 4) * 512 + (b & 3);
+        const float ag = ts_a * q.w_ts[t.seg * 4 + 0];
+        const float au = ts_a * q.w_ts[t.seg * 4 + 1];
+        if (rows > 0) {
+          uint32_t v[kNmax];
+          tmem_ld_32x32b_x16(tbase, v);
           tmem_ld_wait();
 #pragma unroll
-          for (int n = 0; n < 32; n += 2) {
-            if (cb + n >= rows) break;
+          for (int n = 0; n < kNmax; n += 2) {
+            if (n >= rows) break;
             const float a0 = __uint_as_float(v[n]), a1 = __uint_as_float(v[n + 1]);
             const float x0 = __shfl_xor_sync(0xffffffffu, a0, 16);
             const float x1 = __shfl_xor_sync(0xffffffffu, a1, 16);
-            // the lower half-warp takes token cb+n, the upper half token cb+n+1
+            // the lower half-warp takes token n, the upper half token n+1
             float g = (lo_half ? a0 : x1) * ag;
             float u = (lo_half ? x0 : a1) * au;
-            const int col = cb + n + (lo_half ? 0 : 1);
-            if (p.swiglu_clamp) {   // gate clamped from above, up on both sides
-              g = fminf(g, p.swiglu_limit);
-              u = fminf(fmaxf(u, -p.swiglu_limit), p.swiglu_limit);
+            const int col = n + (lo_half ? 0 : 1);
+            if (q.swiglu_clamp) {   // gate clamped from above, up on both sides
+              g = fminf(g, q.swiglu_limit);
+              u = fminf(fmaxf(u, -q.swiglu_limit), q.swiglu_limit);
             }
             const float h = silu_mul(g, u);
             float bamax = fabsf(h);
 #pragma unroll
             for (int o = 8; o > 0; o >>= 1) bamax = fmaxf(bamax, __shfl_xor_sync(0xffffffffu, bamax, o));
             uint32_t sf = 0u;
-            float q = 0.0f;
+            float qv = 0.0f;
             if (bamax != 0.0f) {
               sf = f32_to_e4m3(bamax * (1.0f / 6.0f) * inv_ts_h);
-              const float S = e4m3_to_f32(sf) * p.ts_h;
-              if (S != 0.0f) q = h * __frcp_rn(S);
+              const float S = e4m3_to_f32(sf) * ts_h;
+              if (S != 0.0f) qv = h * __frcp_rn(S);
             }
             // gather the eight quotients of each quarter-warp into its first lane
             const int g0 = lane & ~7;
             float qq[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) qq[e] = __shfl_sync(0xffffffffu, q, g0 + e);
+            for (int e = 0; e < 8; ++e) qq[e] = __shfl_sync(0xffffffffu, qv, g0 + e);
             const uint32_t word = e2m1x8(qq[0], qq[1], qq[2], qq[3], qq[4], qq[5], qq[6], qq[7]);
             const uint32_t word_hi = __shfl_down_sync(0xffffffffu, word, 8);
             if ((lane & 15) == 0 && col < rows) {
               const size_t prow = (size_t)(t.m0 + col);
-              *reinterpret_cast<uint2*>(p.hq + prow * (I / 2) + b * 8) = make_uint2(word, word_hi);
-              p.hsf[prow * (I / 16) + b] = (uint8_t)sf;
-              hsf_tile[(col & 31) * 16 + (col >> 5) * 4] = (uint8_t)sf;
+              *reinterpret_cast<uint2*>(q.hq + prow * (I / 2) + b * 8) = make_uint2(word, word_hi);
+              q.hsf[prow * (I / 16) + b] = (uint8_t)sf;
+              hsf_tile[col * 16] = (uint8_t)sf;
             }
           }
         }
       } else {
         // output features m = nt*128 + warp*32 + lane; token column n -> permuted row m0 + n
-        const float alpha = p.ts_h * p.w_ts[t.seg * 4 + 2];
+        const float alpha = ts_h * q.w_ts[t.seg * 4 + 2];
         const int m = t.nt * 128 + warp * 32 + lane;
-        float wr[2] = {0.0f, 0.0f};
-        int tok[2] = {0, 0};
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int r = lane + 32 * i;
-          if (r < rows) {
-            wr[i] = __ldg(p.perm_w + t.m0 + r);
-            int tk = __ldg(p.perm_src + t.m0 + r);
-            if (tk < 0 || tk >= p.y_rows) {
-              set_status(p.status, MOE_ERR_INVALID_ARG);
-              tk = -1;
-            }
-            tok[i] = tk;
-          }
-        }
-#pragma unroll 1
-        for (int cb = 0; cb < kNmax; cb += 32) {
-          if (cb >= rows) break;
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tbase + cb, v);
+        const float wr = lane < rows ? __ldg(q.perm_w + t.m0 + lane) : 0.0f;
+        if (rows > 0) {
+          uint32_t v[kNmax];
+          tmem_ld_32x32b_x16(tbase, v);
           tmem_ld_wait();
 #pragma unroll
-          for (int n = 0; n < 32; ++n) {
-            if (cb + n >= rows) break;
-            const float w = __shfl_sync(0xffffffffu, wr[cb >> 5], n);
-            const float d = (__uint_as_float(v[n]) * alpha) * w;
-            if (p.mode == 2) {
-              p.obuf[(size_t)(t.m0 + cb + n) * p.N + m] = d;
-            } else {
-              const int tk = __shfl_sync(0xffffffffu, tok[cb >> 5], n);
-              if (tk >= 0) red_add_f32(p.yacc + (size_t)tk * p.N + m, d);
-            }
+          for (int n = 0; n < kNmax; ++n) {
+            if (n >= rows) break;
+            const float w = __shfl_sync(0xffffffffu, wr, n);
+            q.obuf[(size_t)(t.m0 + n) * q.N + m] = (__uint_as_float(v[n]) * alpha) * w;
           }
         }
       }
+      // the accumulator is free once its values are in registers; the publication of h below
+      // waits for this warp's stores and stays off the MMA thread's path
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(acc_empty + abuf));
+      if (t.ph == 0) {
+        // publish this warp's share of the expert's h rows to the copy engines of every CTA
+        fence_proxy_async_global();
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) red_release_add_s32(p.ready + t.mt, 1);
+      }
     }
   }
+#undef NVFP4MOE_ITEM
 
   tc_fence_before();
   __syncthreads();
@@ -406,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 size_t smem_bytes(int nseg) {
-  return 1024 + (size_t)kStages * kStageBytes + 256 + sizeof(int32_t) * 2 * (nseg + 2);
+  return 1024 + (size_t)kStages * kStageBytes + kBarBytes + sizeof(int32_t) * 3 * (((nseg + 1 + 3) & ~3));
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -426,27 +523,44 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 bool tensor_map_available() { return encode_fn() != nullptr; }
 
-cudaError_t launch_grouped_gemm_decode(const GemmArgs& a, cudaStream_t s) {
+namespace {
+
+// Token rows [rows, K/2] bytes in expert order; box = 128 bytes x 16 rows, 128-byte swizzle.
+bool encode_token_map(CUtensorMap* tmap, const uint8_t* codes, int K, int rows) {
   auto encode = encode_fn();
-  if (!encode) return cudaErrorNotSupported;
-  // token rows [out_rows, K/2] bytes in expert order; box = 128 bytes x 16 rows, 128B swizzle
-  CUtensorMap tmap;
-  const cuuint64_t dims[2] = {(cuuint64_t)(a.K / 2), (cuuint64_t)a.out_rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)(a.K / 2)};
+  if (!encode) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
   const cuuint32_t box[2] = {128, (cuuint32_t)kXBoxRows};
   const cuuint32_t estr[2] = {1, 1};
-  if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.a_codes), dims,
-             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+  return encode(tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(codes), dims, strides,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm_decode(const DecodeGemmArgs& a, cudaStream_t s) {
+  if (!encode_fn()) return cudaErrorNotSupported;
+  if (a.g1.nseg != a.g2.nseg || a.g1.tile_start != a.g2.tile_start || a.g1.seg_off != a.g2.seg_off ||
+      a.g1.mode != 0 || a.g2.mode != 2 || !a.ready || !a.plan_flag)
     return cudaErrorInvalidValue;
-  const size_t smem = smem_bytes(a.nseg);
+  CUtensorMap tmap_x, tmap_h;
+  if (!encode_token_map(&tmap_x, a.g1.a_codes, a.g1.K, a.g1.out_rows) ||
+      !encode_token_map(&tmap_h, a.g2.a_codes, a.g2.K, a.g2.out_rows))
+    return cudaErrorInvalidValue;
+  const size_t smem = smem_bytes(a.g1.nseg);
   cudaError_t e = cudaFuncSetAttribute(grouped_gemm_decode_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  int grid = a.max_ctas;
-  if (grid > num_sms()) grid = num_sms();
+  // one CTA per SM at most: CTAs wait on each other's GEMM1 tiles, so all of them must be
+  // resident together (one 200 KB CTA fits an SM; the grid never exceeds the SM count)
+  const int64_t items = (int64_t)a.g1.max_items + a.g2.max_items;
+  int grid = (int)std::min<int64_t>(items, num_sms());
   if (grid < 1) grid = 1;
-  return launch_pdl(grouped_gemm_decode_kernel, dim3(grid), dim3(kThreads), smem, s, tmap, a);
+  return launch_pdl(grouped_gemm_decode_kernel, dim3(grid), dim3(kThreads), smem, s, tmap_x,
+                    tmap_h, a);
 }
 
 }  // namespace nvfp4moe

@@ -19,6 +19,7 @@ constexpr int kBN = 128;       // output columns per tile (MMA N)
 constexpr int kBK = 256;       // FP4 elements of K per pipeline stage (128 bytes per row)
 constexpr int kMmaK = 64;      // K of one block-scaled FP4 MMA
 constexpr int kDecodeMaxRows = 64;   // batches up to this many tokens take the decode path
+constexpr int kDecodeTileRows = 16;  // rows of an expert per decode GEMM tile (its MMA N)
 constexpr int kSmallPlanRows = 2048; // T*k routed by the one-block plan
 
 // Router chunking: tokens per chunk (one router block and one scatter block each).
@@ -86,7 +87,7 @@ bool prologue_small_fits(int T, int H, int k);
 // Workspace of moe_run for T tokens.  Offset 0 holds the device status word.
 struct RunLayout {
   size_t hdr, amax_part, ids, w, hist, base, seg_off, tile_start, perm_src, perm_w, inv, xq, xsf,
-      hq, hsf, yacc, obuf, perm_seg, xq_perm, xsf_tiles, hsf_tiles, total;
+      hq, hsf, yacc, obuf, perm_seg, xq_perm, xsf_tiles, hsf_tiles, ready, total;
   int T, R, Rt, nseg, nchunks, tpc, dtiles;
   bool small;   // fused prologue + stored-row combine
   bool decode;  // T <= kDecodeMaxRows: cluster prologue and the swapped-operand decode GEMM
@@ -120,12 +121,19 @@ struct RunLayout {
     yacc = o;       o = align_up(o + (small ? 0 : 4 * (size_t)T * H));
     obuf = o;       o = align_up(o + (small ? 4 * (size_t)Rt * H : 0));
     decode = small && T <= kDecodeMaxRows;
-    // m-tiles of 128 expert-ordered rows (decode: one per active expert)
-    dtiles = decode ? (nseg < Rt ? nseg : Rt) : (int)(((int64_t)Rt + (int64_t)nseg * 127) / 128);
+    // m-tiles of expert-ordered rows: 128 rows (general), kDecodeTileRows rows (decode, where an
+    // active expert owns ceil(rows / kDecodeTileRows) of them)
+    if (decode) {
+      const int64_t bound = (int64_t)nseg + (Rt + kDecodeTileRows - 1) / kDecodeTileRows;
+      dtiles = (int)(bound < Rt ? bound : Rt);
+    } else {
+      dtiles = (int)(((int64_t)Rt + (int64_t)nseg * 127) / 128);
+    }
     perm_seg = o;   o = align_up(o + 4 * (size_t)Rt);
     xq_perm = o;    o = align_up(o + (size_t)Rt * H / 2);
     xsf_tiles = o;  o = align_up(o + (size_t)dtiles * (H / 64) * 512);
     hsf_tiles = o;  o = align_up(o + (size_t)dtiles * (I / 64) * 512);
+    ready = o;      o = align_up(o + (decode ? 4 * ((size_t)dtiles + 1) : 0));   // + plan flag
     total = o;
   }
 };
@@ -219,8 +227,6 @@ struct GemmArgs {
   float* obuf;              // mode 2 out [rows, N]
   int swiglu_clamp;         // mode 0: h = silu(min(g, L)) * clamp(u, -L, L) with L = swiglu_limit
   float swiglu_limit;
-  int plan_early;           // decode kernel: the plan is complete at launch (written two kernels
-                            // back), only the previous kernel's output needs the wait
   int32_t* status;
   int max_ctas;
   // bounds used to reject malformed plan data instead of touching memory outside the buffers
@@ -238,7 +244,18 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s);
 
 // Decode-sized batches (T <= kDecodeMaxRows, so no expert receives more rows): weights as the
 // MMA's M operand, tokens as N (gemm_decode.cu).  Same arguments as launch_grouped_gemm.
-cudaError_t launch_grouped_gemm_decode(const GemmArgs& a, cudaStream_t s);
+// Decode batches: both grouped GEMMs in one persistent launch.  Every CTA first takes its GEMM1
+// items (expert, 128-row tile of the interleaved gate/up weights), then its GEMM2 items (expert,
+// 128-row tile of the down weights); a GEMM2 item reads the expert's h rows only once all GEMM1
+// epilogue warps of that expert have published them in `ready`.
+struct DecodeGemmArgs {
+  GemmArgs g1;          // gate/up projection, SwiGLU + requantisation (mode 0)
+  GemmArgs g2;          // down projection, router-weighted rows stored to obuf (mode 2)
+  int32_t* ready;       // [m-tiles] finished GEMM1 epilogue warps per expert tile; zeroed by the
+                        // decode prologue of the same call
+  const int32_t* plan_flag;   // set by the decode prologue once the plan is in global memory
+};
+cudaError_t launch_grouped_gemm_decode(const DecodeGemmArgs& a, cudaStream_t s);
 // 2-D tensor map encoder of the driver, fetched through the runtime (no libcuda link).
 bool tensor_map_available();
 
@@ -288,6 +305,9 @@ struct DecodePrologueArgs {
   float *w, *perm_w;
   int sqrtsp;              // the variant router (see PlanArgs)
   const float* bias;
+  int32_t* ready;          // [nready] readiness counts of the decode GEMM, zeroed here
+  int nready;
+  int32_t* plan_flag;      // 0 before this kernel lets the GEMM launch, 1 once the plan is written
 };
 cudaError_t launch_decode_prologue(const DecodePrologueArgs& a, cudaStream_t s);
 

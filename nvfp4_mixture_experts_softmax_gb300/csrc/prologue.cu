@@ -52,9 +52,14 @@ __global__ void __launch_bounds__(kSmallPlanThreads) prologue_small_kernel(const
 //      the general plan (expert-major, then assignment order), because a token picks an expert at
 //      most once.  Every CTA computes the same plan; CTA 0 alone writes it to global memory.  A table
 //      gives each (token, slot) its expert-ordered row and the offset of its scale bytes in the
-//      32x4x4 arrangement of the decode GEMM's token operand (tile = the expert's tile index,
-//      row = rank within the expert); then every thread encodes its block once and writes it in
+//      arrangement of the decode GEMM's token operand (tiles of kDecodeTileRows rows: tile = the
+//      expert's first tile + rank / kDecodeTileRows, row = rank mod kDecodeTileRows, rank = the
+//      row's rank within the expert); then every thread encodes its block once and writes it in
 //      token order and to each of the token's expert rows.
+// As soon as the segment offsets and tile starts are in global memory, CTA 0 sets a flag that the
+// decode GEMM (launched early through programmatic dependent launch) polls before it reads its
+// plan, so the weight stream starts while this kernel still encodes; the flag is cleared before
+// this grid lets the GEMM launch.
 // A CTA keeps its shared memory until the cluster's other CTAs have finished reading it (split
 // cluster barrier: arrive after the last remote read, wait before exit).
 struct DecodeSmem {
@@ -80,6 +85,16 @@ __global__ void __launch_bounds__(kSmallPlanThreads) decode_prologue_kernel(cons
   __shared__ uint32_t s_part;
   __shared__ float s_ts;
   griddep_wait();
+  // the decode GEMM may start once every CTA of this grid has passed griddep_launch; it reads the
+  // plan after polling the flag, which must therefore read 0 until this call's plan is written
+  // (the CTA that routes the fewest tokens clears it, off the plan's path)
+  if (cluster_ctarank() == kDecodeProCtas - 1) {
+    if (threadIdx.x == 0) {
+      *a.plan_flag = 0;
+      __threadfence();
+    }
+    __syncthreads();
+  }
   griddep_launch();
   constexpr int C = kDecodeProCtas;
   constexpr int nw = kSmallPlanThreads / 32;
@@ -100,6 +115,8 @@ __global__ void __launch_bounds__(kSmallPlanThreads) decode_prologue_kernel(cons
   int32_t* s_toff = reinterpret_cast<int32_t*>(s_dyn + L.toff);
   int32_t* s_dst = reinterpret_cast<int32_t*>(s_dyn + L.dst);
   if (rank == 0 && threadIdx.x == 0) *a.status = 0;
+  if (rank == 1 % C)
+    for (int i = threadIdx.x; i < a.nready; i += blockDim.x) a.ready[i] = 0;
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_mask[e] = 0ull;
 
   // ---- A: this thread's first block of x (its load overlaps the routing), routing, max |x| ----
@@ -169,7 +186,7 @@ __global__ void __launch_bounds__(kSmallPlanThreads) decode_prologue_kernel(cons
     for (int e = e0; e < e1; ++e) {
       const int n = __popcll(s_mask[e]);
       c += n;
-      tc += (n + kBM - 1) / kBM;
+      tc += (n + kDecodeTileRows - 1) / kDecodeTileRows;
     }
     int ci = c, ti = tc;
 #pragma unroll
@@ -192,7 +209,7 @@ __global__ void __launch_bounds__(kSmallPlanThreads) decode_prologue_kernel(cons
         a.tile_start[e] = toff;
       }
       off += n;
-      toff += (n + kBM - 1) / kBM;
+      toff += (n + kDecodeTileRows - 1) / kDecodeTileRows;
     }
     if (lane == 31) {
       s_off[E] = ci;
@@ -202,17 +219,22 @@ __global__ void __launch_bounds__(kSmallPlanThreads) decode_prologue_kernel(cons
         a.tile_start[E] = ti;
         if (a.shared_rows > 0) {
           a.offsets[E + 1] = ci + a.shared_rows;
-          a.tile_start[E + 1] = ti + (a.shared_rows + kBM - 1) / kBM;
+          a.tile_start[E + 1] = ti + (a.shared_rows + kDecodeTileRows - 1) / kDecodeTileRows;
         }
       }
     }
   }
   __syncthreads();
+  // segment offsets and tile starts are in global memory: the decode GEMM may read its plan
+  if (out && threadIdx.x == 0) {
+    __threadfence();
+    st_release_s32(a.plan_flag, 1);
+  }
 
   // destination table: expert-ordered row and scale-byte offset of each (token, slot)
   const int wpr = a.H / 64;   // 4-scale words per row
-  // tiles of the token-operand scale arrangement: one per active expert (and the shared one)
-  const int ntiles = min(E + (a.shared_rows > 0 ? 1 : 0), Rt);
+  // tiles of the token-operand scale arrangement: kDecodeTileRows rows of one expert each
+  const int ntiles = a.nready;
   for (int i = threadIdx.x; i < T * kd; i += blockDim.x) {
     const int t = i / kd, j = i - t * kd;
     int p = -1, r = 0, tile = 0, e = E;
@@ -221,14 +243,14 @@ __global__ void __launch_bounds__(kSmallPlanThreads) decode_prologue_kernel(cons
       if (e >= 0 && e < E) {
         r = __popcll(s_mask[e] & ((1ull << t) - 1ull));
         p = s_off[e] + r;
-        tile = s_toff[e];
+        tile = s_toff[e] + r / kDecodeTileRows;
       } else {
         set_status(a.status, MOE_ERR_INVALID_ARG);
       }
     } else if (a.shared_rows > 0) {   // the shared expert's rows follow the routed ones
       p = R + t;
       r = t;
-      tile = s_toff[E];
+      tile = s_toff[E] + r / kDecodeTileRows;
     }
     if (p >= 0 && (p >= Rt || r >= kDecodeMaxRows || tile < 0 || tile >= ntiles)) {
       set_status(a.status, MOE_ERR_INVALID_ARG);
@@ -241,7 +263,7 @@ __global__ void __launch_bounds__(kSmallPlanThreads) decode_prologue_kernel(cons
       if (j < k) a.inv[t * k + j] = p;
     }
     s_dst[i] = p;
-    s_sfo[i] = ((long long)tile * wpr) * 512 + (r & 31) * 16 + (r >> 5) * 4;
+    s_sfo[i] = ((long long)tile * wpr) * 512 + (r % kDecodeTileRows) * 16;
   }
   __syncthreads();
 

@@ -95,10 +95,10 @@ def test_host_side_rejections(moe):
 
 
 def test_run_kernel_count(moe):
-    """The launch count follows moe_run's path choice: decode-sized batches take four kernels,
+    """The launch count follows moe_run's path choice: decode-sized batches take three kernels,
     other small batches five, large ones six (one-kernel plan) or eight (three-kernel plan)."""
     dec = moe.make_config(128, 2048, 768, 8, max_tokens=8192)
-    assert [moe.run_kernel_count(dec, T) for T in (1, 8, 32, 64)] == [4, 4, 4, 4]
+    assert [moe.run_kernel_count(dec, T) for T in (1, 8, 32, 64)] == [3, 3, 3, 3]
     assert moe.run_kernel_count(dec, 0) == 0
     assert moe.run_kernel_count(dec, 8192) == 8
     mid = moe.make_config(16, 2048, 256, 4, max_tokens=1024)
