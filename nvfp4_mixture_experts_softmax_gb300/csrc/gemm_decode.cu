@@ -1,9 +1,10 @@
-// Both grouped block-scaled FP4 GEMMs of a decode-sized batch (every expert receives at most 64
-// rows) in one persistent launch, with the operands swapped: the expert's weights are the MMA's
-// A operand (M = 128 weight rows of one packed block per K stage, loaded by one bulk copy) and
-// the expert's token rows are the B operand (N = the rows rounded up to 16).  The tensor core
-// then works on the real tokens only, a pipeline stage is 28 KB (7 stages in flight), and the
-// accumulator holds one weight row per TMEM lane and one token per column.
+// Both grouped block-scaled FP4 GEMMs of a decode-sized batch (at most 64 tokens) in one
+// persistent launch, with the operands swapped: the expert's weights are the MMA's A operand
+// (M = 128 weight rows of one packed block per K stage, loaded by one bulk copy) and a tile of at
+// most 16 of the expert's token rows is the B operand (N = 16; an expert with more rows owns
+// several tiles).  The tensor core then works on the real tokens only, a pipeline stage is
+// 22.5 KB (nine stages in flight), and the accumulator holds one weight row per TMEM lane and one
+// token per column.
 //   GEMM1 items (phase 0): warp w of the epilogue holds the 16 gate rows and the 16 up rows of
 //          one 16-feature NVFP4 block, so each half-warp computes silu(g)*u of one token and
 //          requantises the block with half-warp reductions; each warp then publishes its share
@@ -11,8 +12,10 @@
 //   GEMM2 items (phase 1): lanes hold consecutive output features, so a token's router-weighted
 //          row is stored 128 contiguous bytes per warp.
 // Every CTA takes its GEMM1 items first, then its GEMM2 items, all through one ring of stages:
-// the down-projection weights stream in as soon as ring slots free up (they depend on nothing),
-// and only the h rows of a GEMM2 item wait until all GEMM1 tiles of that expert are published.
+// one thread streams the weight blocks into every slot as soon as it is free (weights depend on
+// nothing but the plan), another adds each stage's token rows once they exist - the activations
+// after the prologue, the h rows of a GEMM2 item after all GEMM1 tiles of its expert are
+// published - and a stage is full when both parts have landed.
 // This removes the second launch's ramp and the full drain between the two GEMMs, which at
 // decode sizes cost more than the weight stream itself.  CTAs wait on each other only through
 // the readiness counts, and only after finishing every GEMM1 item of their own, so with one CTA
@@ -20,10 +23,10 @@
 // Every operand arrives by the copy engine: per stage one bulk copy of the weight block, 2-D TMA
 // tiles (128-byte swizzle) of the expert's token rows - the activations (GEMM1) or h (GEMM2) are
 // stored in expert order, so an expert's rows are contiguous - and one bulk copy of the tokens'
-// scales, which the producers write pre-arranged per expert tile.  Warps: 0-3 epilogue, 4 copy
-// issue, 5 MMA, 6 scale factors ("nvfp4-megamoe-kernel compare pre-b1...master", section "MoE
-// kernel": TMA, MMA and epilogue warps; the pages keep decode on 1-CTA tiles).  The eight
-// shared -> tensor memory scale copies of a stage hold up the thread that issues them for a long
+// scales, which the producers write pre-arranged per expert tile.  Warps: 0-3 epilogue, 4 weight
+// copies, 5 MMA, 6 scale factors, 7 token copies ("nvfp4-megamoe-kernel compare pre-b1...master",
+// section "MoE kernel": TMA, MMA and epilogue warps; the pages keep decode on 1-CTA tiles).  The
+// eight shared -> tensor memory scale copies of a stage hold up the thread that issues them for a long
 // time, so a warp of their own issues them one stage ahead of the MMA thread and signals it
 // through an mbarrier; the MMA thread then issues only the four MMAs of a stage, with
 // descriptors advanced by additions.  Three TMEM accumulators let the epilogue trail the main
@@ -47,7 +50,8 @@ constexpr int kEpiWarps = 4;
 constexpr int kTmaWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kSfWarp = 6;
-constexpr int kThreads = (kSfWarp + 1) * 32;
+constexpr int kXWarp = 7;                              // token rows (and what they wait for)
+constexpr int kThreads = (kXWarp + 1) * 32;
 constexpr int kNmax = kDecodeTileRows;                // token rows per tile (the MMA N)
 constexpr int kXOff = kTileBlockBytes;                 // token codes after the weight block
 constexpr int kXBytes = kNmax * 128;
@@ -129,7 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(full + s), 1);  // the copy-issuing thread (expect_tx)
+      mbar_init(smem_u32(full + s), 2);  // the weight and the token issuers (expect_tx each)
       mbar_init(smem_u32(empty + s), 1);
     }
     for (int b = 0; b < kAccBufs; ++b) {
@@ -213,108 +217,82 @@ __global__ void __launch_bounds__(kThreads, 1)
 #define NVFP4MOE_ITEM(i) decode_item((i), total1, nt1, nt2, kst1, kst2, s_tseg, s_seg, s_tile)
 
   if (warp == kTmaWarp) {
-    // ---------------- all operands: bulk copies + 2-D TMA tiles ----------------
-    // Two cursors over this CTA's stages: the weight cursor issues a stage's weight block as
-    // soon as its ring slot is free (weights depend on nothing but the plan), the token cursor
-    // follows with the stage's token rows and their scales once they exist - after the
-    // prologue's completion for GEMM1, after the expert's h rows are published for GEMM2.  The
-    // full barrier of a stage expects both parts from the weight issue on.
+    // ---------------- weight blocks: one bulk copy per stage ----------------
+    // Weights depend on nothing but the plan, so this thread only waits for free ring slots;
+    // the stage's token rows come from the token issuer (warp kXWarp), and the stage's full
+    // barrier completes once both parts have landed.
     if (lane == 0) {
-      // only the boxes that hold the expert's rows (16 rows each); the rest of the token tile
-      // stays stale and only feeds accumulator columns that are never stored
-      auto stage_bytes = [&](const Item& t) {
-        return (uint32_t)(kTileBlockBytes + ((max(t.rows, 1) + kXBoxRows - 1) / kXBoxRows) *
-                                                kXBoxRows * 128 + kXSfBytes);
-      };
-      int wi = blockIdx.x, wks = 0, wstage = 0;
-      uint32_t wphase = 0;
-      int xi = blockIdx.x, xks = 0, xstage = 0;
-      Item wt{}, xt{};
-      if (wi < total) wt = xt = NVFP4MOE_ITEM(wi);
-      int nw = 0, nx = 0;           // stages whose weight / token parts are issued
-      bool x_ok = false, dep = false, ok = true;
-      uint64_t t0 = 0;
-      uint32_t idle = 0;
-      while (xi < total && ok) {
-        bool progress = false;
-        // 1. a free slot takes the next weight block at once
-        if (wi < total && mbar_test_wait(smem_u32(empty + wstage), wphase ^ 1u)) {
-          const uint32_t fb = smem_u32(full + wstage);
-          const GemmArgs& q = wt.ph ? p.g2 : p.g1;
-          const uint8_t* src = q.b_tiles + (size_t)wt.seg * q.b_per_seg +
-                               ((size_t)wt.nt * wt.kst + wks) * kTileBlockBytes;
-          mbar_arrive_expect_tx(fb, stage_bytes(wt));
-          bulk_load(smem0 + wstage * kStageBytes, src, kTileBlockBytes, fb);
-          ++nw;
-          if (++wstage == kStages) { wstage = 0; wphase ^= 1u; }
-          if (++wks == wt.kst) {
-            wks = 0;
-            wi += gridDim.x;
-            if (wi < total) wt = NVFP4MOE_ITEM(wi);
-          }
-          progress = true;
-        }
-        // 2. token rows of every stage that has its weights and whose rows exist
-        while (nx < nw && dep && (xt.ph == 0 || x_ok)) {
-          const uint32_t sb = smem0 + xstage * kStageBytes;
-          const uint32_t fb = smem_u32(full + xstage);
-          const GemmArgs& q = xt.ph ? p.g2 : p.g1;
-          const uint8_t* sft = q.a_sf_tiles + ((size_t)xt.mt * (q.K / 64) + xks * 4) * 512;
-          const void* tm = xt.ph ? (const void*)&tmap_h : (const void*)&tmap_x;
-          const int nbox = (max(xt.rows, 1) + kXBoxRows - 1) / kXBoxRows;
-          for (int bx = 0; bx < nbox; ++bx)
-            tma_load_2d(sb + kXOff + bx * kXBoxRows * 128, tm, xks * 128,
-                        xt.m0 + bx * kXBoxRows, fb);
-          bulk_load(sb + kXSfOff, sft, kXSfBytes, fb);
-          ++nx;
-          if (++xstage == kStages) xstage = 0;
-          if (++xks == xt.kst) {
-            xks = 0;
-            xi += gridDim.x;
-            x_ok = false;
-            if (xi < total) {
-              xt = NVFP4MOE_ITEM(xi);
-              if (xt.ph == 1) {   // usually published long ago: look once right away
-                x_ok = ld_acquire_s32(p.ready + xt.mt) >= ready_target;
-                if (x_ok) fence_proxy_async_global();
-              }
-            }
-          }
-          progress = true;
-        }
-        if (progress) {
-          t0 = 0;
-          continue;
-        }
-        // 3. nothing to issue: wait for what the oldest stage's token rows need
-        if (nx < nw && !dep) {   // the activations, encoded by the prologue
-          griddep_wait();
-          dep = true;
-          continue;
-        }
-        if (nx < nw && xt.ph == 1 && !x_ok) {   // the expert's h rows, published by GEMM1
-          x_ok = ld_acquire_s32(p.ready + xt.mt) >= ready_target;
-          if (x_ok) {
-            fence_proxy_async_global();
-            continue;
-          }
-        }
-        if ((++idle & 255u) == 0u) {
-          const uint64_t now = global_timer_ns();
-          if (t0 == 0) {
-            t0 = now;
-          } else if (now - t0 > kWaitLimitNs) {
-            set_status(status, MOE_ERR_DEVICE_TIMEOUT);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+        const Item t = NVFP4MOE_ITEM(item);
+        const GemmArgs& q = t.ph ? p.g2 : p.g1;
+        const uint8_t* src = q.b_tiles + (size_t)t.seg * q.b_per_seg +
+                             (size_t)t.nt * t.kst * kTileBlockBytes;
+        for (int ks = 0; ks < t.kst; ++ks) {
+          if (!mbar_wait_bounded(smem_u32(empty + stage), phase ^ 1u, kWaitLimitNs, status)) {
             ok = false;
+            break;
           }
+          const uint32_t fb = smem_u32(full + stage);
+          mbar_arrive_expect_tx(fb, kTileBlockBytes);
+          bulk_load(smem0 + stage * kStageBytes, src + (size_t)ks * kTileBlockBytes,
+                    kTileBlockBytes, fb);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
       // the MMAs of the last stages must finish before the CTA may exit
       for (int i = 0; i < kStages && ok; ++i) {
-        if (!mbar_wait_bounded(smem_u32(empty + wstage), wphase ^ 1u, kWaitLimitNs, status)) break;
-        if (++wstage == kStages) { wstage = 0; wphase ^= 1u; }
+        if (!mbar_wait_bounded(smem_u32(empty + stage), phase ^ 1u, kWaitLimitNs, status)) break;
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
-      if (!dep) griddep_wait();
+    }
+  } else if (warp == kXWarp) {
+    // ---------------- token rows: one 2-D TMA box + their scales per stage ----------------
+    // GEMM1 reads the activations the prologue encoded (the dependency wait), GEMM2 the h rows
+    // of the item's expert once every GEMM1 epilogue warp of it has published them.
+    if (lane == 0) {
+      griddep_wait();
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+        const Item t = NVFP4MOE_ITEM(item);
+        const GemmArgs& q = t.ph ? p.g2 : p.g1;
+        if (t.ph == 1) {
+          uint64_t t0 = 0;
+          for (uint32_t i = 0; ld_acquire_s32(p.ready + t.mt) < ready_target; ++i) {
+            if ((i & 63u) == 63u) {
+              const uint64_t now = global_timer_ns();
+              if (t0 == 0) {
+                t0 = now;
+              } else if (now - t0 > kWaitLimitNs) {
+                set_status(status, MOE_ERR_DEVICE_TIMEOUT);
+                ok = false;
+                break;
+              }
+            }
+          }
+          if (!ok) break;
+          fence_proxy_async_global();
+        }
+        const void* tm = t.ph ? (const void*)&tmap_h : (const void*)&tmap_x;
+        const uint8_t* sft = q.a_sf_tiles + (size_t)t.mt * (q.K / 64) * 512;
+        const uint32_t xbytes = (uint32_t)(kXBoxRows * 128 + kXSfBytes);
+        for (int ks = 0; ks < t.kst; ++ks) {
+          if (!mbar_wait_bounded(smem_u32(empty + stage), phase ^ 1u, kWaitLimitNs, status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sb = smem0 + stage * kStageBytes;
+          const uint32_t fb = smem_u32(full + stage);
+          mbar_arrive_expect_tx(fb, xbytes);
+          tma_load_2d(sb + kXOff, tm, ks * 128, t.m0, fb);
+          bulk_load(sb + kXSfOff, sft + (size_t)ks * kXSfBytes, kXSfBytes, fb);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
     }
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issue: D[weight row][token] ----------------
