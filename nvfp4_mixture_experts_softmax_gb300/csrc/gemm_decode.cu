@@ -67,7 +67,11 @@ constexpr int kBarBytes = 512;                          // mbarriers + TMEM slot
 
 static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "tensor memory budget");
 static_assert(kStageBytes % 1024 == 0 && kXOff % 1024 == 0, "1024-byte aligned swizzled tiles");
-static_assert(kStages * kStageBytes + 1024 + kBarBytes + 12 * 1028 <= 232448, "shared memory");
+constexpr size_t kMaxDynSmem = 232448;                   // 227 KB per CTA
+// plan arrays of up to 1025 segments and a tile table of up to 2112 tiles (64 tokens, k <= 32,
+// plus the shared expert's rows)
+static_assert(kStages * kStageBytes + 1024 + kBarBytes + 4 * (2 * 1028 + 2112) <= kMaxDynSmem,
+              "shared memory");
 static_assert((3 * kStages + 2 * kAccBufs + 3) * 8 + 4 <= kBarBytes, "mbarriers + TMEM slot");
 static_assert(kNmax == kXBoxRows && kNmax <= (int)kAccCols, "one TMA box of token rows per stage");
 
@@ -92,7 +96,7 @@ __device__ __forceinline__ Item decode_item(int item, int total1, int nt1, int n
   t.mt = local / ntl;
   t.nt = local - t.mt * ntl;
   t.kst = t.ph ? kst2 : kst1;
-  t.seg = s_tseg[t.mt];
+  t.seg = s_tseg[t.mt];    // always in [0, nseg): every entry is initialised
   t.m0 = s_seg[t.seg] + (t.mt - s_tile[t.seg]) * kNmax;
   t.rows = min(kNmax, s_seg[t.seg + 1] - t.m0);
   return t;
@@ -120,9 +124,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(plan_bar + 2);
   const int nseg = p.g1.nseg;
   const int plan_ints = (nseg + 1 + 3) & ~3;    // 16-byte multiples for the bulk copies
+  // m-tiles can outnumber segments (an expert with more than kNmax rows owns several): the
+  // m-tile -> segment table has an entry for every tile the launch can hold
+  const int max_tiles = p.g1.max_items / (p.g1.N / 128);
   int32_t* s_tile = reinterpret_cast<int32_t*>(smem + kStages * kStageBytes + kBarBytes);
   int32_t* s_seg = s_tile + plan_ints;
-  int32_t* s_tseg = s_seg + plan_ints;     // m-tile -> segment
+  int32_t* s_tseg = s_seg + plan_ints;     // m-tile -> segment, max_tiles entries
   int32_t* status = p.g1.status;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -189,13 +196,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ok = __shfl_sync(0xffffffffu, ok, 0);
     __syncwarp();
-    for (int i = lane; i <= nseg; i += 32) {
-      if (!ok) s_tile[i] = 0;
-      s_tseg[i] = 0;
-    }
+    if (!ok)
+      for (int i = lane; i <= nseg; i += 32) s_tile[i] = 0;
+    for (int i = lane; i < max_tiles; i += 32) s_tseg[i] = 0;
     __syncwarp();
     for (int sg = lane; sg < nseg; sg += 32)
-      for (int mt = max(s_tile[sg], 0); mt < s_tile[sg + 1] && mt <= nseg; ++mt) s_tseg[mt] = sg;
+      for (int mt = max(s_tile[sg], 0); mt < s_tile[sg + 1] && mt < max_tiles; ++mt) s_tseg[mt] = sg;
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(plan_bar));
   } else {
@@ -206,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kst1 = p.g1.K / kBK, kst2 = p.g2.K / kBK;
   const int mtiles = s_tile[nseg];
   int total1 = mtiles * nt1, total2 = mtiles * nt2;
-  if (mtiles < 0 || total1 > p.g1.max_items || total2 > p.g2.max_items) {
+  if (mtiles < 0 || mtiles > max_tiles || total1 > p.g1.max_items || total2 > p.g2.max_items) {
     if (threadIdx.x == 0) set_status(status, MOE_ERR_INVALID_ARG);
     total1 = total2 = 0;
   }
@@ -480,8 +486,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-size_t smem_bytes(int nseg) {
-  return 1024 + (size_t)kStages * kStageBytes + kBarBytes + sizeof(int32_t) * 3 * (((nseg + 1 + 3) & ~3));
+size_t smem_bytes(int nseg, int max_tiles) {
+  return 1024 + (size_t)kStages * kStageBytes + kBarBytes +
+         sizeof(int32_t) * (2 * ((nseg + 1 + 3) & ~3) + (size_t)max_tiles);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -528,7 +535,10 @@ cudaError_t launch_grouped_gemm_decode(const DecodeGemmArgs& a, cudaStream_t s) 
   if (!encode_token_map(&tmap_x, a.g1.a_codes, a.g1.K, a.g1.out_rows) ||
       !encode_token_map(&tmap_h, a.g2.a_codes, a.g2.K, a.g2.out_rows))
     return cudaErrorInvalidValue;
-  const size_t smem = smem_bytes(a.g1.nseg);
+  const int nt1 = a.g1.N / 128;
+  if (nt1 < 1 || a.g1.max_items % nt1 != 0) return cudaErrorInvalidValue;
+  const size_t smem = smem_bytes(a.g1.nseg, a.g1.max_items / nt1);
+  if (smem > kMaxDynSmem) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(grouped_gemm_decode_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

@@ -104,6 +104,22 @@ def test_popular_expert_many_tiles(moe):
     run_and_check(moe, cs, 700, logits=lg.cuda())
 
 
+def test_decode_popular_expert_multi_tile(moe):
+    """Decode path with one expert taking all 64 tokens: four 16-row tiles of that expert."""
+    cs = synth.custom_config("decode_popular", 64, 512, 8, 2, 256, config_id=128)
+    lg = synth.gen_logits(cs, 64)
+    lg[:, 5] += 50.0
+    run_and_check(moe, cs, 64, logits=lg.cuda())
+
+
+def test_decode_every_expert_multi_tile_with_shared(moe):
+    """Decode path with k = E (every expert gets all 48 tokens: three tiles each) and a shared
+    expert (three more tiles)."""
+    cs = synth.custom_config("decode_k_eq_e_shared", 48, 512, 4, 4, 256, shared_inter=256,
+                             config_id=129)
+    run_and_check(moe, cs, 48)
+
+
 def test_repeat_calls_consistent(moe):
     cs = synth.CONFIGS["tiny"]
     y1, _, _ = run_and_check(moe, cs, 16)
