@@ -42,9 +42,14 @@ class MoeArgs(C.Structure):
                 ("offsets", C.c_void_p), ("perm_src", C.c_void_p), ("inv", C.c_void_p),
                 ("hq", C.c_void_p), ("hsf", C.c_void_p), ("shq", C.c_void_p), ("shsf", C.c_void_p),
                 ("router_mode", C.c_int32), ("router_bias", C.c_void_p),
-                ("swiglu_clamp", C.c_int32), ("swiglu_limit", C.c_float)]
+                ("swiglu_clamp", C.c_int32), ("swiglu_limit", C.c_float),
+                ("act_mode", C.c_int32), ("x_bf16", C.c_void_p), ("hb", C.c_void_p),
+                ("shb", C.c_void_p), ("hf", C.c_void_p)]
 
 ROUTER_MODES = {"softmax": 0, "sqrtsoftplus": 1}
+# activation precision of the layer: NVFP4 activations with h requantised to NVFP4, or W4A16
+# (BF16 activations as they are, h rounded to BF16)
+ACT_MODES = {"nvfp4": 0, "bf16": 1}
 
 
 def lib():
@@ -246,16 +251,29 @@ class QuantExpert:
 
 
 def moe_forward(xq, xsf, ts_a, logits, experts, k, ts_h=1.0, shared=None, bruteforce=False,
-                want_debug=False, router_mode="softmax", router_bias=None, swiglu_limit=None):
+                want_debug=False, router_mode="softmax", router_bias=None, swiglu_limit=None,
+                act="nvfp4", x_bf16=None):
     """The layer on quantised activations.  ``experts`` is a list of length E whose entries are
     QuantExpert or None (None only for experts no token routes to); ``shared`` a QuantExpert.
     ``router_mode``/``router_bias``: see router(); ``swiglu_limit``: None for plain SwiGLU, else
-    the clamp limit L of silu(min(g, L)) * clamp(u, -L, L)."""
-    xq = np.ascontiguousarray(xq, np.uint8)
-    xsf = np.ascontiguousarray(xsf, np.uint8)
+    the clamp limit L of silu(min(g, L)) * clamp(u, -L, L).  ``act="bf16"`` is the W4A16 layer:
+    ``x_bf16`` (BF16 bits or a bfloat16 tensor [T, H]) enters GEMM1 as it is (xq, xsf and ts_a
+    are then unused and may be None) and h is rounded to BF16; its debug output holds ``hb`` (and
+    ``shb``) instead of the NVFP4 codes.  Debug output ``hf``: h in FP32 before its rounding or
+    requantisation (routed rows, permuted order)."""
     logits = np.ascontiguousarray(logits, np.float32)
     T, E = logits.shape
-    H = xq.shape[1] * 2
+    if act == "bf16":
+        xb = np.ascontiguousarray(as_bf16_bits(x_bf16), np.uint16)
+        H = xb.shape[1]
+        xq = np.zeros((T, H // 2), np.uint8)
+        xsf = np.zeros((T, H // 16), np.uint8)
+        ts_a = 0.0
+    else:
+        xb = None
+        xq = np.ascontiguousarray(xq, np.uint8)
+        xsf = np.ascontiguousarray(xsf, np.uint8)
+        H = xq.shape[1] * 2
     I = None
     for ex in experts:
         if ex is not None:
@@ -289,15 +307,24 @@ def moe_forward(xq, xsf, ts_a, logits, experts, k, ts_h=1.0, shared=None, brutef
     a.router_bias = _p(rb) if rb is not None else None
     a.swiglu_clamp = 0 if swiglu_limit is None else 1
     a.swiglu_limit = 0.0 if swiglu_limit is None else float(swiglu_limit)
+    a.act_mode = ACT_MODES[act]
+    a.x_bf16 = _p(xb) if xb is not None else None
     dbg = {}
     if want_debug and not bruteforce:
         dbg = dict(ids=np.zeros((T, k), np.int32), w=np.zeros((T, k), np.float32),
                    counts=np.zeros(E, np.int32), offsets=np.zeros(E + 1, np.int32),
                    perm_src=np.zeros(T * k, np.int32), inv=np.zeros(T * k, np.int32),
-                   hq=np.zeros((T * k, I // 2), np.uint8), hsf=np.zeros((T * k, I // 16), np.uint8))
-        if shared is not None:
-            dbg["shq"] = np.zeros((T, Is // 2), np.uint8)
-            dbg["shsf"] = np.zeros((T, Is // 16), np.uint8)
+                   hf=np.zeros((T * k, I), np.float32))
+        if act == "bf16":
+            dbg["hb"] = np.zeros((T * k, I), np.uint16)
+            if shared is not None:
+                dbg["shb"] = np.zeros((T, Is), np.uint16)
+        else:
+            dbg["hq"] = np.zeros((T * k, I // 2), np.uint8)
+            dbg["hsf"] = np.zeros((T * k, I // 16), np.uint8)
+            if shared is not None:
+                dbg["shq"] = np.zeros((T, Is // 2), np.uint8)
+                dbg["shsf"] = np.zeros((T, Is // 16), np.uint8)
         for name, arr in dbg.items():
             setattr(a, name, _p(arr))
     fn = lib().orc_moe_forward_bruteforce if bruteforce else lib().orc_moe_forward

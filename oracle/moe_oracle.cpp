@@ -29,6 +29,10 @@
 //    section "6. MoE (Mixture of Experts) / Nvfp4SharedExpert".
 //  * Weighted combine y = sum_j w_j * expert_out_j: "vllm.cpp docs/STATUS.md", row "Brick C part 1"
 //    (MoeCombineKernel).
+//  * W4A16 activation precision: BF16 activations enter the expert GEMMs as they are (no
+//    activation scale), the NVFP4 weights are decoded at the point of use: "b12x" README,
+//    section "What's in here" (moe: "W4A16 (BF16 activations, inline FP4 weight dequant - no
+//    activation-scale math)").
 //
 // Readings where the pages are silent (each also listed in the design notes):
 //  * two E2M1 codes per byte, element 2i in the low nibble;
@@ -42,7 +46,9 @@
 //    output is rounded once to BF16 (nearest even);
 //  * softplus(x) = x for x > 20, log1p(exp(x)) otherwise (FP32); the variant router's weights are
 //    the chosen unbiased scores divided by their sum (summed in slot order), as the base router
-//    renormalises over the k chosen.
+//    renormalises over the k chosen;
+//  * W4A16: the intermediate h is rounded to BF16 (nearest even) before the down projection, the
+//    16-bit activation format of that path; everything else is the base layer.
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
@@ -388,6 +394,12 @@ typedef struct {
   const float* router_bias;  // [E] or null (mode 1 only)
   int32_t swiglu_clamp;      // 1: silu(min(g, L)) * clamp(u, -L, L)
   float swiglu_limit;        // L
+  // activation precision (zero: NVFP4 activations, h requantised to NVFP4)
+  int32_t act_mode;          // 1: W4A16 - x_bf16 enters GEMM1 as is, h is rounded to BF16
+  const uint16_t* x_bf16;    // [T, H] (act_mode 1; xq / xsf / ts_a unused)
+  uint16_t* hb;              // [T*k, I] BF16 h of the routed rows, permuted order (act_mode 1)
+  uint16_t* shb;             // [T, I_shared] BF16 h of the shared expert (act_mode 1)
+  float* hf;                 // [T*k, I] FP32 h before its rounding or requantisation (any mode)
 } orc_moe_args;
 
 // h = silu(g) * u, with the optional clamp of gate (from above) and up (both sides) first.
@@ -401,10 +413,11 @@ static inline float swiglu(float g, float u, int clamp, float L) {
 
 float orc_swiglu(float g, float u, int clamp, float L) { return swiglu(g, u, clamp, L); }
 
-// GEMM1 + SwiGLU + requant + GEMM2 for one row: x_hat [H] -> d [H], writing h codes and scales.
+// GEMM1 + SwiGLU, then h requantised to NVFP4 (act_mode 0: codes and scales to hq_row /
+// hsf_row) or rounded to BF16 (act_mode 1: bits to hb_row), + GEMM2 for one row: x [H] -> d [H].
 static void expert_row(const float* xr, const float* Wg, const float* Wu, const float* Wd, int H,
-                       int I, float ts_h, int clamp, float L, float* h, float* hhat,
-                       uint8_t* hq_row, uint8_t* hsf_row, float* d) {
+                       int I, float ts_h, int clamp, float L, int act_mode, float* h, float* hhat,
+                       uint8_t* hq_row, uint8_t* hsf_row, uint16_t* hb_row, float* d) {
   for (int n = 0; n < I; ++n) {
     const float* wg = Wg + (int64_t)n * H;
     const float* wu = Wu + (int64_t)n * H;
@@ -413,8 +426,15 @@ static void expert_row(const float* xr, const float* Wg, const float* Wu, const 
     for (int c = 0; c < H; ++c) u = u + xr[c] * wu[c];
     h[n] = swiglu(g, u, clamp, L);
   }
-  orc_quantize_f32(h, 1, I, ts_h, hq_row, hsf_row);
-  orc_dequantize(hq_row, hsf_row, ts_h, 1, I, hhat);
+  if (act_mode == 1) {
+    for (int n = 0; n < I; ++n) {
+      hb_row[n] = orc_f32_to_bf16(h[n]);
+      hhat[n] = orc_bf16_to_f32(hb_row[n]);
+    }
+  } else {
+    orc_quantize_f32(h, 1, I, ts_h, hq_row, hsf_row);
+    orc_dequantize(hq_row, hsf_row, ts_h, 1, I, hhat);
+  }
   for (int m = 0; m < H; ++m) {
     const float* wd = Wd + (int64_t)m * I;
     float acc = 0.0f;
@@ -444,22 +464,31 @@ int orc_moe_forward(const orc_moe_args* a) {
   orc_router_ex(a->logits, T, E, k, a->router_mode, a->router_bias, ids.data(), w.data());
   orc_plan(ids.data(), T, E, k, counts.data(), offsets.data(), perm_src.data(), inv.data());
 
+  // the activations entering GEMM1: decoded NVFP4 (act_mode 0) or the BF16 values (act_mode 1)
   std::vector<float> xhat((size_t)T * H);
-  orc_dequantize(a->xq, a->xsf, a->ts_a, T, H, xhat.data());
+  if (a->act_mode == 1) {
+    for (int64_t i = 0; i < T * H; ++i) xhat[i] = orc_bf16_to_f32(a->x_bf16[i]);
+  } else {
+    orc_dequantize(a->xq, a->xsf, a->ts_a, T, H, xhat.data());
+  }
 
   std::vector<float> D((size_t)R * H);
-  std::vector<float> Wg, Wu, Wd, h(std::max(I, a->I_shared)), hhat(std::max(I, a->I_shared));
-  std::vector<uint8_t> hq_row(std::max(I, a->I_shared) / 2), hsf_row(std::max(I, a->I_shared) / 16);
+  const int Imax = std::max(I, a->I_shared);
+  std::vector<float> Wg, Wu, Wd, h(Imax), hhat(Imax);
+  std::vector<uint8_t> hq_row(Imax / 2), hsf_row(Imax / 16);
+  std::vector<uint16_t> hb_row(Imax);
   for (int e = 0; e < E; ++e) {
     if (counts[e] == 0) continue;
     dequant_expert(a->experts[e], H, I, Wg, Wu, Wd);
     for (int32_t p = offsets[e]; p < offsets[e + 1]; ++p) {
       const float* xr = xhat.data() + (int64_t)perm_src[p] * H;
       expert_row(xr, Wg.data(), Wu.data(), Wd.data(), H, I, a->ts_h, a->swiglu_clamp,
-                 a->swiglu_limit, h.data(), hhat.data(), hq_row.data(), hsf_row.data(),
-                 D.data() + (int64_t)p * H);
-      if (a->hq) std::memcpy(a->hq + (int64_t)p * (I / 2), hq_row.data(), I / 2);
-      if (a->hsf) std::memcpy(a->hsf + (int64_t)p * (I / 16), hsf_row.data(), I / 16);
+                 a->swiglu_limit, a->act_mode, h.data(), hhat.data(), hq_row.data(),
+                 hsf_row.data(), hb_row.data(), D.data() + (int64_t)p * H);
+      if (a->act_mode != 1 && a->hq) std::memcpy(a->hq + (int64_t)p * (I / 2), hq_row.data(), I / 2);
+      if (a->act_mode != 1 && a->hsf) std::memcpy(a->hsf + (int64_t)p * (I / 16), hsf_row.data(), I / 16);
+      if (a->act_mode == 1 && a->hb) std::copy(hb_row.begin(), hb_row.begin() + I, a->hb + (int64_t)p * I);
+      if (a->hf) std::copy(h.begin(), h.begin() + I, a->hf + (int64_t)p * I);
     }
   }
   std::vector<float> S;
@@ -469,10 +498,11 @@ int orc_moe_forward(const orc_moe_args* a) {
     dequant_expert(a->experts[E], H, Is, Wg, Wu, Wd);
     for (int64_t t = 0; t < T; ++t) {
       expert_row(xhat.data() + t * H, Wg.data(), Wu.data(), Wd.data(), H, Is, a->ts_h,
-                 a->swiglu_clamp, a->swiglu_limit, h.data(), hhat.data(), hq_row.data(),
-                 hsf_row.data(), S.data() + t * H);
-      if (a->shq) std::memcpy(a->shq + t * (Is / 2), hq_row.data(), Is / 2);
-      if (a->shsf) std::memcpy(a->shsf + t * (Is / 16), hsf_row.data(), Is / 16);
+                 a->swiglu_clamp, a->swiglu_limit, a->act_mode, h.data(), hhat.data(),
+                 hq_row.data(), hsf_row.data(), hb_row.data(), S.data() + t * H);
+      if (a->act_mode != 1 && a->shq) std::memcpy(a->shq + t * (Is / 2), hq_row.data(), Is / 2);
+      if (a->act_mode != 1 && a->shsf) std::memcpy(a->shsf + t * (Is / 16), hsf_row.data(), Is / 16);
+      if (a->act_mode == 1 && a->shb) std::copy(hb_row.begin(), hb_row.begin() + Is, a->shb + t * Is);
     }
   }
   for (int64_t t = 0; t < T; ++t)
@@ -516,13 +546,17 @@ int orc_moe_forward_bruteforce(const orc_moe_args* a) {
       for (int c = 0; c < H; ++c) u = u + xr[c] * wval(ex, 1, n, c, H);
       h[n] = swiglu(g, u, a->swiglu_clamp, a->swiglu_limit);
     }
-    for (int b = 0; b < Ie / 16; ++b) {  // requantise block by block, then decode
-      quant_block16(h.data() + b * 16, a->ts_h, hq_row.data() + b * 8, hsf_row.data() + b);
-      float s = orc_e4m3_decode(hsf_row[b]);
-      for (int i = 0; i < 16; ++i) {
-        uint8_t byte = hq_row[b * 8 + i / 2];
-        uint8_t code = (i & 1) ? (byte >> 4) : (byte & 15);
-        hhat[b * 16 + i] = (orc_e2m1_decode(code) * s) * a->ts_h;
+    if (a->act_mode == 1) {              // W4A16: h in BF16
+      for (int n = 0; n < Ie; ++n) hhat[n] = orc_bf16_to_f32(orc_f32_to_bf16(h[n]));
+    } else {
+      for (int b = 0; b < Ie / 16; ++b) {  // requantise block by block, then decode
+        quant_block16(h.data() + b * 16, a->ts_h, hq_row.data() + b * 8, hsf_row.data() + b);
+        float s = orc_e4m3_decode(hsf_row[b]);
+        for (int i = 0; i < 16; ++i) {
+          uint8_t byte = hq_row[b * 8 + i / 2];
+          uint8_t code = (i & 1) ? (byte >> 4) : (byte & 15);
+          hhat[b * 16 + i] = (orc_e2m1_decode(code) * s) * a->ts_h;
+        }
       }
     }
     for (int m = 0; m < H; ++m) {
@@ -533,6 +567,10 @@ int orc_moe_forward_bruteforce(const orc_moe_args* a) {
   };
   for (int64_t t = 0; t < T; ++t) {
     for (int c = 0; c < H; ++c) {
+      if (a->act_mode == 1) {
+        xr[c] = orc_bf16_to_f32(a->x_bf16[t * H + c]);
+        continue;
+      }
       uint8_t byte = a->xq[t * (H / 2) + c / 2];
       uint8_t code = (c & 1) ? (byte >> 4) : (byte & 15);
       xr[c] = (orc_e2m1_decode(code) * orc_e4m3_decode(a->xsf[t * (H / 16) + c / 16])) * a->ts_a;
