@@ -47,7 +47,7 @@ constexpr int kStages = 9;
 constexpr int kAccBufs = 3;
 constexpr int kXBoxRows = 16;                          // token rows per TMA box
 constexpr int kEpiWarps = 4;
-constexpr int kTmaWarp = 4;
+constexpr int kWeightWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kSfWarp = 6;
 constexpr int kXWarp = 7;                              // token rows (and what they wait for)
@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == kTmaWarp) {
+  if (warp == kWeightWarp) {
     // The plan (segment offsets and tile starts) is published by the decode prologue before it
     // encodes the activations: waiting for that flag instead of the prologue's completion lets
     // the weight stream start while the prologue still runs.  A wait that times out leaves an
@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t smem0 = smem_u32(smem);
 #define NVFP4MOE_ITEM(i) decode_item((i), total1, nt1, nt2, kst1, kst2, s_tseg, s_seg, s_tile)
 
-  if (warp == kTmaWarp) {
+  if (warp == kWeightWarp) {
     // ---------------- weight blocks: one bulk copy per stage ----------------
     // Weights depend on nothing but the plan, so this thread only waits for free ring slots;
     // the stage's token rows come from the token issuer (warp kXWarp), and the stage's full

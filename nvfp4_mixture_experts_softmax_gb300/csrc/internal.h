@@ -221,8 +221,8 @@ struct GemmArgs {
   float ts_h;
   uint8_t* hq;            // mode 0 out [rows, N/4]   (h has N/2 features)
   uint8_t* hsf;           // mode 0 out [rows, N/32]
-  const int32_t* perm_src;  // mode 1
-  const float* perm_w;      // mode 1
+  const int32_t* perm_src;  // mode 1: token of each permuted row
+  const float* perm_w;      // modes 1 and 2: router weight of each permuted row
   float* yacc;              // mode 1 out [T, N]
   float* obuf;              // mode 2 out [rows, N]
   int swiglu_clamp;         // mode 0: h = silu(min(g, L)) * clamp(u, -L, L) with L = swiglu_limit
@@ -242,17 +242,17 @@ struct GemmArgs {
 };
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s);
 
-// Decode-sized batches (T <= kDecodeMaxRows, so no expert receives more rows): weights as the
-// MMA's M operand, tokens as N (gemm_decode.cu).  Same arguments as launch_grouped_gemm.
-// Decode batches: both grouped GEMMs in one persistent launch.  Every CTA first takes its GEMM1
-// items (expert, 128-row tile of the interleaved gate/up weights), then its GEMM2 items (expert,
-// 128-row tile of the down weights); a GEMM2 item reads the expert's h rows only once all GEMM1
-// epilogue warps of that expert have published them in `ready`.
+// Decode-sized batches (T <= kDecodeMaxRows): both grouped GEMMs in one persistent launch
+// (gemm_decode.cu), weights as the MMA's M operand and tiles of kDecodeTileRows token rows of one
+// expert as N.  Every CTA first takes its GEMM1 items (tile, 128-row tile of the interleaved
+// gate/up weights), then its GEMM2 items (tile, 128-row tile of the down weights); a GEMM2 item
+// reads the tile's h rows only once all GEMM1 epilogue warps of that tile have published them in
+// `ready`.
 struct DecodeGemmArgs {
   GemmArgs g1;          // gate/up projection, SwiGLU + requantisation (mode 0)
   GemmArgs g2;          // down projection, router-weighted rows stored to obuf (mode 2)
-  int32_t* ready;       // [m-tiles] finished GEMM1 epilogue warps per expert tile; zeroed by the
-                        // decode prologue of the same call
+  int32_t* ready;       // [tiles] finished GEMM1 epilogue warps per tile; zeroed by the decode
+                        // prologue of the same call
   const int32_t* plan_flag;   // set by the decode prologue once the plan is in global memory
 };
 cudaError_t launch_grouped_gemm_decode(const DecodeGemmArgs& a, cudaStream_t s);
