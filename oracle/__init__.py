@@ -47,9 +47,9 @@ class MoeArgs(C.Structure):
                 ("shb", C.c_void_p), ("hf", C.c_void_p)]
 
 ROUTER_MODES = {"softmax": 0, "sqrtsoftplus": 1}
-# activation precision of the layer: NVFP4 activations with h requantised to NVFP4, or W4A16
-# (BF16 activations as they are, h rounded to BF16)
-ACT_MODES = {"nvfp4": 0, "bf16": 1}
+# activation precision of the layer: NVFP4 activations with h requantised to NVFP4, W4A16 (BF16
+# activations as they are, h rounded to BF16) or W4A8 (MXFP8 activations and h, MXFP4 weights)
+ACT_MODES = {"nvfp4": 0, "bf16": 1, "mxfp8": 2}
 
 
 def lib():
@@ -77,6 +77,16 @@ def lib():
         L.orc_quantize_bf16.argtypes = [C.c_void_p, C.c_int64, C.c_int64, C.c_void_p, C.c_void_p, C.c_void_p]
         L.orc_dequantize.restype = None
         L.orc_dequantize.argtypes = [C.c_void_p, C.c_void_p, C.c_float, C.c_int64, C.c_int64, C.c_void_p]
+        L.orc_e8m0_decode.restype = C.c_float
+        L.orc_e8m0_decode.argtypes = [C.c_uint8]
+        L.orc_mx_scale.restype = C.c_uint8
+        L.orc_mx_scale.argtypes = [C.c_float, C.c_int]
+        L.orc_mx_quantize_f32.restype = None
+        L.orc_mx_quantize_f32.argtypes = [C.c_void_p, C.c_int64, C.c_int64, C.c_int, C.c_void_p,
+                                          C.c_void_p]
+        L.orc_mx_dequantize.restype = None
+        L.orc_mx_dequantize.argtypes = [C.c_void_p, C.c_void_p, C.c_int64, C.c_int64, C.c_int,
+                                        C.c_void_p]
         L.orc_router.restype = None
         L.orc_router.argtypes = [C.c_void_p, C.c_int64, C.c_int, C.c_int, C.c_void_p, C.c_void_p]
         L.orc_router_ex.restype = None
@@ -194,6 +204,39 @@ def dequantize(codes: np.ndarray, sf: np.ndarray, ts: float) -> np.ndarray:
     return out
 
 
+# ----------------------------------------------------------------------------- MX formats
+MX_KINDS = {"e4m3": 0, "e2m1": 1}   # MXFP8 / MXFP4 elements
+
+
+def e8m0_decode(b: int) -> float:
+    return float(lib().orc_e8m0_decode(b))
+
+
+def mx_scale(amax: float, emax: int) -> int:
+    return int(lib().orc_mx_scale(amax, emax))
+
+
+def mx_quantize(x: np.ndarray, kind: str):
+    """MX quantisation of FP32 rows [rows, cols] (cols % 32 == 0): element codes (E4M3: one byte
+    each, [rows, cols]; E2M1: two per byte, [rows, cols/2]) and E8M0 scales [rows, cols/32]."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    rows, cols = x.shape
+    codes = np.zeros((rows, cols if kind == "e4m3" else cols // 2), np.uint8)
+    sc = np.zeros((rows, cols // 32), np.uint8)
+    lib().orc_mx_quantize_f32(_p(x), rows, cols, MX_KINDS[kind], _p(codes), _p(sc))
+    return codes, sc
+
+
+def mx_dequantize(codes: np.ndarray, scales: np.ndarray, kind: str) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, np.uint8)
+    scales = np.ascontiguousarray(scales, np.uint8)
+    rows = codes.shape[0]
+    cols = codes.shape[1] if kind == "e4m3" else codes.shape[1] * 2
+    out = np.zeros((rows, cols), np.float32)
+    lib().orc_mx_dequantize(_p(codes), _p(scales), rows, cols, MX_KINDS[kind], _p(out))
+    return out
+
+
 # ----------------------------------------------------------------------------- routing
 def router(logits: np.ndarray, k: int, mode: str = "softmax", bias=None):
     """Top-k routing.  mode "softmax": selection on the logits, softmax weights renormalised over
@@ -250,6 +293,20 @@ class QuantExpert:
         return cls(cs, ss, ts)
 
 
+class QuantExpertMX(QuantExpert):
+    """MXFP4 weights of one expert (the W4A8 layer): gate/up [I,H], down [H,I] E2M1 codes [N, K/2]
+    + E8M0 scales [N, K/32]; no tensor scale (ts = 1)."""
+
+    @classmethod
+    def from_bf16(cls, gate, up, down):
+        cs, ss = [], []
+        for w in (gate, up, down):
+            wf = (np.asarray(as_bf16_bits(w), np.uint32) << 16).view(np.float32)
+            c, s = mx_quantize(wf, "e2m1")
+            cs.append(c), ss.append(s)
+        return cls(cs, ss, [1.0, 1.0, 1.0])
+
+
 def moe_forward(xq, xsf, ts_a, logits, experts, k, ts_h=1.0, shared=None, bruteforce=False,
                 want_debug=False, router_mode="softmax", router_bias=None, swiglu_limit=None,
                 act="nvfp4", x_bf16=None):
@@ -260,10 +317,12 @@ def moe_forward(xq, xsf, ts_a, logits, experts, k, ts_h=1.0, shared=None, brutef
     ``x_bf16`` (BF16 bits or a bfloat16 tensor [T, H]) enters GEMM1 as it is (xq, xsf and ts_a
     are then unused and may be None) and h is rounded to BF16; its debug output holds ``hb`` (and
     ``shb``) instead of the NVFP4 codes.  Debug output ``hf``: h in FP32 before its rounding or
-    requantisation (routed rows, permuted order)."""
+    requantisation (routed rows, permuted order).  ``act="mxfp8"`` is the W4A8 layer: x_bf16 is
+    quantised to MXFP8, ``experts`` / ``shared`` are QuantExpertMX (MXFP4), h is requantised to
+    MXFP8 (debug ``hq`` [rows, I] E4M3 codes, ``hsf`` [rows, I/32] E8M0 scales)."""
     logits = np.ascontiguousarray(logits, np.float32)
     T, E = logits.shape
-    if act == "bf16":
+    if act in ("bf16", "mxfp8"):
         xb = np.ascontiguousarray(as_bf16_bits(x_bf16), np.uint16)
         H = xb.shape[1]
         xq = np.zeros((T, H // 2), np.uint8)
@@ -319,6 +378,12 @@ def moe_forward(xq, xsf, ts_a, logits, experts, k, ts_h=1.0, shared=None, brutef
             dbg["hb"] = np.zeros((T * k, I), np.uint16)
             if shared is not None:
                 dbg["shb"] = np.zeros((T, Is), np.uint16)
+        elif act == "mxfp8":
+            dbg["hq"] = np.zeros((T * k, I), np.uint8)
+            dbg["hsf"] = np.zeros((T * k, I // 32), np.uint8)
+            if shared is not None:
+                dbg["shq"] = np.zeros((T, Is), np.uint8)
+                dbg["shsf"] = np.zeros((T, Is // 32), np.uint8)
         else:
             dbg["hq"] = np.zeros((T * k, I // 2), np.uint8)
             dbg["hsf"] = np.zeros((T * k, I // 16), np.uint8)

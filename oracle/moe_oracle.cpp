@@ -33,6 +33,12 @@
 //    activation scale), the NVFP4 weights are decoded at the point of use: "b12x" README,
 //    section "What's in here" (moe: "W4A16 (BF16 activations, inline FP4 weight dequant - no
 //    activation-scale math)").
+//  * W4A8 activation precision: MXFP4 weights (E2M1 values, one E8M0 scale per 32 elements along
+//    K) and MXFP8 activations (E4M3 values, one E8M0 scale per 32), no tensor scale: "b12x"
+//    README, section "DeepSeek V4 Flash 0731 MoE reproduction" ("MXFP4 E8M0/K32 weights, MXFP8
+//    activations"); E8M0 = 2^(byte - 127), group 32, no global scale: "vllm.cpp docs/STATUS.md",
+//    the MXFP4 weight-dequant row; "four E8M0 scales, one per 32 values": "b12x" README (the
+//    compressed all-reduce modes).
 //
 // Readings where the pages are silent (each also listed in the design notes):
 //  * two E2M1 codes per byte, element 2i in the low nibble;
@@ -48,7 +54,11 @@
 //    the chosen unbiased scores divided by their sum (summed in slot order), as the base router
 //    renormalises over the k chosen;
 //  * W4A16: the intermediate h is rounded to BF16 (nearest even) before the down projection, the
-//    16-bit activation format of that path; everything else is the base layer.
+//    16-bit activation format of that path; everything else is the base layer;
+//  * MX block scale (the pages give only the decode rule): 2^(floor(log2 max|x|) - emax) with emax
+//    the exponent of the element format's largest power of two (E4M3: 8, E2M1: 2), the byte
+//    clamped to [0, 254], byte 0 for an all-zero block; elements x / scale rounded to nearest even
+//    and saturated (to 448 or 6); W4A8 requantises h to MXFP8 the same way.
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
@@ -201,6 +211,72 @@ int orc_quantize_bf16(const uint16_t* x, int64_t rows, int64_t cols, uint8_t* co
     orc_quantize_f32(row.data(), 1, cols, ts, codes + r * (cols / 2), sf + r * (cols / 16));
   }
   return 0;
+}
+
+// ---------------------------------------------------------------------------------------------
+// MX formats (W4A8): one E8M0 scale per 32 elements, no tensor scale
+// ---------------------------------------------------------------------------------------------
+
+// E8M0: the byte is a biased exponent, value 2^(b - 127); 0xFF is NaN.
+float orc_e8m0_decode(uint8_t b) {
+  if (b == 0xFF) return NAN;
+  return std::ldexp(1.0f, (int)b - 127);
+}
+
+// Scale byte of a block with max |x| = amax for elements whose largest power of two is 2^emax:
+// 2^(floor(log2 amax) - emax), the byte clamped to [0, 254]; amax = 0 gives byte 0.
+uint8_t orc_mx_scale(float amax, int emax) {
+  if (!(amax > 0.0f)) return 0;
+  int e = 0;
+  std::frexp(amax, &e);  // amax = m * 2^e, m in [0.5, 1): floor(log2 amax) = e - 1
+  int b = (e - 1) - emax + 127;
+  if (b < 0) b = 0;
+  if (b > 254) b = 254;
+  return (uint8_t)b;
+}
+
+// kind 0: MXFP8 (E4M3 elements, one byte each); kind 1: MXFP4 (E2M1, two per byte, element 2i in
+// the low nibble).  Rows [rows, cols], cols % 32 == 0; scales [rows, cols / 32].
+void orc_mx_quantize_f32(const float* x, int64_t rows, int64_t cols, int kind, uint8_t* codes,
+                         uint8_t* scales) {
+  const int emax = kind == 0 ? 8 : 2;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t b = 0; b < cols / 32; ++b) {
+      const float* xb = x + r * cols + b * 32;
+      float amax = 0.0f;
+      for (int i = 0; i < 32; ++i) amax = std::max(amax, std::fabs(xb[i]));
+      const uint8_t sb = orc_mx_scale(amax, emax);
+      scales[r * (cols / 32) + b] = sb;
+      const float X = orc_e8m0_decode(sb);
+      for (int i = 0; i < 32; ++i) {
+        const float q = xb[i] / X;
+        const int64_t c = r * cols + b * 32 + i;
+        if (kind == 0) {
+          codes[c] = orc_e4m3_encode(q);
+        } else {
+          const uint8_t nib = orc_e2m1_encode(q);
+          uint8_t& byte = codes[c / 2];
+          byte = (c & 1) ? (uint8_t)((byte & 0x0F) | (nib << 4)) : (uint8_t)((byte & 0xF0) | nib);
+        }
+      }
+    }
+}
+
+// v = element * 2^(scale byte - 127).
+void orc_mx_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t rows, int64_t cols,
+                       int kind, float* out) {
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t c = 0; c < cols; ++c) {
+      const int64_t i = r * cols + c;
+      float v;
+      if (kind == 0) {
+        v = orc_e4m3_decode(codes[i]);
+      } else {
+        const uint8_t byte = codes[i / 2];
+        v = orc_e2m1_decode((i & 1) ? (byte >> 4) : (byte & 15));
+      }
+      out[i] = v * orc_e8m0_decode(scales[r * (cols / 32) + c / 32]);
+    }
 }
 
 // v = (e2m1(code) * e4m3(sf)) * ts, rows [rows, cols].
@@ -395,8 +471,11 @@ typedef struct {
   int32_t swiglu_clamp;      // 1: silu(min(g, L)) * clamp(u, -L, L)
   float swiglu_limit;        // L
   // activation precision (zero: NVFP4 activations, h requantised to NVFP4)
-  int32_t act_mode;          // 1: W4A16 - x_bf16 enters GEMM1 as is, h is rounded to BF16
-  const uint16_t* x_bf16;    // [T, H] (act_mode 1; xq / xsf / ts_a unused)
+  int32_t act_mode;          // 1: W4A16 - x_bf16 enters GEMM1 as is, h is rounded to BF16;
+                             // 2: W4A8 - x_bf16 quantised to MXFP8, experts in MXFP4 (codes
+                             //    [N, K/2], sf = E8M0 [N, K/32], ts unused), h requantised to
+                             //    MXFP8 (hq / shq [rows, I] E4M3, hsf / shsf [rows, I/32] E8M0)
+  const uint16_t* x_bf16;    // [T, H] (act_mode 1 and 2; xq / xsf / ts_a unused)
   uint16_t* hb;              // [T*k, I] BF16 h of the routed rows, permuted order (act_mode 1)
   uint16_t* shb;             // [T, I_shared] BF16 h of the shared expert (act_mode 1)
   float* hf;                 // [T*k, I] FP32 h before its rounding or requantisation (any mode)
@@ -431,6 +510,9 @@ static void expert_row(const float* xr, const float* Wg, const float* Wu, const 
       hb_row[n] = orc_f32_to_bf16(h[n]);
       hhat[n] = orc_bf16_to_f32(hb_row[n]);
     }
+  } else if (act_mode == 2) {
+    orc_mx_quantize_f32(h, 1, I, 0, hq_row, hsf_row);
+    orc_mx_dequantize(hq_row, hsf_row, 1, I, 0, hhat);
   } else {
     orc_quantize_f32(h, 1, I, ts_h, hq_row, hsf_row);
     orc_dequantize(hq_row, hsf_row, ts_h, 1, I, hhat);
@@ -443,11 +525,17 @@ static void expert_row(const float* xr, const float* Wg, const float* Wu, const 
   }
 }
 
-static void dequant_expert(const orc_expert& ex, int H, int I, std::vector<float>& Wg,
-                           std::vector<float>& Wu, std::vector<float>& Wd) {
+static void dequant_expert(const orc_expert& ex, int H, int I, int act_mode,
+                           std::vector<float>& Wg, std::vector<float>& Wu, std::vector<float>& Wd) {
   Wg.resize((size_t)I * H);
   Wu.resize((size_t)I * H);
   Wd.resize((size_t)H * I);
+  if (act_mode == 2) {  // MXFP4 weights
+    orc_mx_dequantize(ex.codes[0], ex.sf[0], I, H, 1, Wg.data());
+    orc_mx_dequantize(ex.codes[1], ex.sf[1], I, H, 1, Wu.data());
+    orc_mx_dequantize(ex.codes[2], ex.sf[2], H, I, 1, Wd.data());
+    return;
+  }
   orc_dequantize(ex.codes[0], ex.sf[0], ex.ts[0], I, H, Wg.data());
   orc_dequantize(ex.codes[1], ex.sf[1], ex.ts[1], I, H, Wu.data());
   orc_dequantize(ex.codes[2], ex.sf[2], ex.ts[2], H, I, Wd.data());
@@ -464,10 +552,16 @@ int orc_moe_forward(const orc_moe_args* a) {
   orc_router_ex(a->logits, T, E, k, a->router_mode, a->router_bias, ids.data(), w.data());
   orc_plan(ids.data(), T, E, k, counts.data(), offsets.data(), perm_src.data(), inv.data());
 
-  // the activations entering GEMM1: decoded NVFP4 (act_mode 0) or the BF16 values (act_mode 1)
+  // the activations entering GEMM1: decoded NVFP4 (act_mode 0), the BF16 values (act_mode 1)
+  // or the BF16 values quantised to MXFP8 and decoded (act_mode 2)
   std::vector<float> xhat((size_t)T * H);
-  if (a->act_mode == 1) {
+  if (a->act_mode == 1 || a->act_mode == 2) {
     for (int64_t i = 0; i < T * H; ++i) xhat[i] = orc_bf16_to_f32(a->x_bf16[i]);
+    if (a->act_mode == 2) {
+      std::vector<uint8_t> c8((size_t)T * H), s8((size_t)T * H / 32);
+      orc_mx_quantize_f32(xhat.data(), T, H, 0, c8.data(), s8.data());
+      orc_mx_dequantize(c8.data(), s8.data(), T, H, 0, xhat.data());
+    }
   } else {
     orc_dequantize(a->xq, a->xsf, a->ts_a, T, H, xhat.data());
   }
@@ -475,18 +569,20 @@ int orc_moe_forward(const orc_moe_args* a) {
   std::vector<float> D((size_t)R * H);
   const int Imax = std::max(I, a->I_shared);
   std::vector<float> Wg, Wu, Wd, h(Imax), hhat(Imax);
-  std::vector<uint8_t> hq_row(Imax / 2), hsf_row(Imax / 16);
+  std::vector<uint8_t> hq_row(Imax), hsf_row(Imax / 16);   // room for every mode's codes
   std::vector<uint16_t> hb_row(Imax);
+  const int mx = a->act_mode == 2;
+  const int64_t hq_w = mx ? I : I / 2, hs_w = mx ? I / 32 : I / 16;   // bytes per routed h row
   for (int e = 0; e < E; ++e) {
     if (counts[e] == 0) continue;
-    dequant_expert(a->experts[e], H, I, Wg, Wu, Wd);
+    dequant_expert(a->experts[e], H, I, a->act_mode, Wg, Wu, Wd);
     for (int32_t p = offsets[e]; p < offsets[e + 1]; ++p) {
       const float* xr = xhat.data() + (int64_t)perm_src[p] * H;
       expert_row(xr, Wg.data(), Wu.data(), Wd.data(), H, I, a->ts_h, a->swiglu_clamp,
                  a->swiglu_limit, a->act_mode, h.data(), hhat.data(), hq_row.data(),
                  hsf_row.data(), hb_row.data(), D.data() + (int64_t)p * H);
-      if (a->act_mode != 1 && a->hq) std::memcpy(a->hq + (int64_t)p * (I / 2), hq_row.data(), I / 2);
-      if (a->act_mode != 1 && a->hsf) std::memcpy(a->hsf + (int64_t)p * (I / 16), hsf_row.data(), I / 16);
+      if (a->act_mode != 1 && a->hq) std::memcpy(a->hq + (int64_t)p * hq_w, hq_row.data(), hq_w);
+      if (a->act_mode != 1 && a->hsf) std::memcpy(a->hsf + (int64_t)p * hs_w, hsf_row.data(), hs_w);
       if (a->act_mode == 1 && a->hb) std::copy(hb_row.begin(), hb_row.begin() + I, a->hb + (int64_t)p * I);
       if (a->hf) std::copy(h.begin(), h.begin() + I, a->hf + (int64_t)p * I);
     }
@@ -495,13 +591,14 @@ int orc_moe_forward(const orc_moe_args* a) {
   if (a->has_shared) {
     const int Is = a->I_shared;
     S.resize((size_t)T * H);
-    dequant_expert(a->experts[E], H, Is, Wg, Wu, Wd);
+    dequant_expert(a->experts[E], H, Is, a->act_mode, Wg, Wu, Wd);
+    const int64_t shq_w = mx ? Is : Is / 2, shs_w = mx ? Is / 32 : Is / 16;
     for (int64_t t = 0; t < T; ++t) {
       expert_row(xhat.data() + t * H, Wg.data(), Wu.data(), Wd.data(), H, Is, a->ts_h,
                  a->swiglu_clamp, a->swiglu_limit, a->act_mode, h.data(), hhat.data(),
                  hq_row.data(), hsf_row.data(), hb_row.data(), S.data() + t * H);
-      if (a->act_mode != 1 && a->shq) std::memcpy(a->shq + t * (Is / 2), hq_row.data(), Is / 2);
-      if (a->act_mode != 1 && a->shsf) std::memcpy(a->shsf + t * (Is / 16), hsf_row.data(), Is / 16);
+      if (a->act_mode != 1 && a->shq) std::memcpy(a->shq + t * shq_w, hq_row.data(), shq_w);
+      if (a->act_mode != 1 && a->shsf) std::memcpy(a->shsf + t * shs_w, hsf_row.data(), shs_w);
       if (a->act_mode == 1 && a->shb) std::copy(hb_row.begin(), hb_row.begin() + Is, a->shb + t * Is);
     }
   }
@@ -533,9 +630,12 @@ int orc_moe_forward_bruteforce(const orc_moe_args* a) {
   const int Imax = std::max(I, a->I_shared);
   std::vector<float> xr(H), h(Imax), hhat(Imax), d(H), acc(H);
   std::vector<uint8_t> hq_row(Imax / 2), hsf_row(Imax / 16);
-  auto wval = [](const orc_expert& ex, int mat, int64_t row, int64_t col, int64_t K) {
+  const int mode = a->act_mode;
+  auto wval = [mode](const orc_expert& ex, int mat, int64_t row, int64_t col, int64_t K) {
     uint8_t byte = ex.codes[mat][row * (K / 2) + col / 2];
     uint8_t code = (col & 1) ? (byte >> 4) : (byte & 15);
+    if (mode == 2)  // MXFP4: E8M0 per 32, no tensor scale
+      return orc_e2m1_decode(code) * orc_e8m0_decode(ex.sf[mat][row * (K / 32) + col / 32]);
     return (orc_e2m1_decode(code) * orc_e4m3_decode(ex.sf[mat][row * (K / 16) + col / 16])) *
            ex.ts[mat];
   };
@@ -548,6 +648,14 @@ int orc_moe_forward_bruteforce(const orc_moe_args* a) {
     }
     if (a->act_mode == 1) {              // W4A16: h in BF16
       for (int n = 0; n < Ie; ++n) hhat[n] = orc_bf16_to_f32(orc_f32_to_bf16(h[n]));
+    } else if (a->act_mode == 2) {       // W4A8: h in MXFP8, block by block
+      for (int b = 0; b < Ie / 32; ++b) {
+        float amax = 0.0f;
+        for (int i = 0; i < 32; ++i) amax = std::max(amax, std::fabs(h[b * 32 + i]));
+        const float X = orc_e8m0_decode(orc_mx_scale(amax, 8));
+        for (int i = 0; i < 32; ++i)
+          hhat[b * 32 + i] = orc_e4m3_decode(orc_e4m3_encode(h[b * 32 + i] / X)) * X;
+      }
     } else {
       for (int b = 0; b < Ie / 16; ++b) {  // requantise block by block, then decode
         quant_block16(h.data() + b * 16, a->ts_h, hq_row.data() + b * 8, hsf_row.data() + b);
@@ -569,6 +677,17 @@ int orc_moe_forward_bruteforce(const orc_moe_args* a) {
     for (int c = 0; c < H; ++c) {
       if (a->act_mode == 1) {
         xr[c] = orc_bf16_to_f32(a->x_bf16[t * H + c]);
+        continue;
+      }
+      if (a->act_mode == 2) {  // MXFP8 of the token's row, block by block
+        if (c % 32 == 0) {
+          float amax = 0.0f;
+          for (int i = 0; i < 32; ++i)
+            amax = std::max(amax, std::fabs(orc_bf16_to_f32(a->x_bf16[t * H + c + i])));
+          const float X = orc_e8m0_decode(orc_mx_scale(amax, 8));
+          for (int i = 0; i < 32; ++i)
+            xr[c + i] = orc_e4m3_decode(orc_e4m3_encode(orc_bf16_to_f32(a->x_bf16[t * H + c + i]) / X)) * X;
+        }
         continue;
       }
       uint8_t byte = a->xq[t * (H / 2) + c / 2];
