@@ -154,18 +154,21 @@ int moe_quantize_act(const void* x, int64_t rows, int64_t cols, uint8_t* codes, 
 
 /* RMSNorm followed by the activation quantiser: the producer that feeds the layer's quantised
  * input ("nvfp4-megamoe-kernel compare pre-b1...master", sections "P4 - Fused RMSNorm + NVFP4
- * quantize" and "P5": two kernels, no BF16 round trip between the norm and the quantiser).  Per
- * row: ms = (sum of x^2) / cols, r = 1 / sqrt(ms + eps), y = (x * r) * gamma, all FP32;
- * then one tensor scale max|y| / 2688 for the whole tensor and the
- * per-16 encode of y, as moe_quantize_act does for x.  The sum of squares is one exact FP32
- * value: 8-element chunks summed left to right, the chunk sums combined by a balanced pairwise tree
- * over the chunk index.  x: [rows, cols] BF16, gamma: [cols] BF16, both 16-byte aligned, cols a
- * multiple of 16 and at most 16384; codes [rows, cols/2], sf [rows, cols/16], ts: device
- * FP32 scalar.  workspace: >= moe_rmsnorm_workspace_size(rows) bytes (its first word is the device
- * status: MOE_ERR_NONFINITE when max|y| is not finite).  rows == 0 is MOE_OK. */
+ * quantize" and "P5": two kernels, no BF16 round trip between the norm and the quantiser; its
+ * output goes straight into moe_run_quantized).  Per row: ms = (sum of x^2) / cols,
+ * r = 1 / sqrt(ms + eps), y = (x * r) * gamma, all FP32; then one tensor scale max|y| / 2688 for
+ * the whole tensor and the per-16 encode of y, as moe_quantize_act does for x.  The sum of
+ * squares is defined as the exact sum rounded once to FP32; the kernel forms it in FP32 in its
+ * own (coalesced) order, within (7 + 5 + log2(ceil(cols / 256))) * 2^-24 of the exact sum
+ * relative, so r, ts and the few codes whose quotients lie that close to a rounding boundary may
+ * differ from the exact definition by one step.  x: [rows, cols] BF16, gamma: [cols] BF16, both
+ * 16-byte aligned, cols a multiple of 16 and at most 16384; codes [rows, cols/2],
+ * sf [rows, cols/16], ts: device FP32 scalar; rrms: NULL or device FP32 [rows] that receives
+ * each row's r.  workspace: >= moe_rmsnorm_workspace_size(rows) bytes (its first word is the
+ * device status: MOE_ERR_NONFINITE when max|y| is not finite).  rows == 0 is MOE_OK. */
 size_t moe_rmsnorm_workspace_size(int64_t rows);
 int moe_rmsnorm_quantize_act(const void* x, const void* gamma, float eps, int64_t rows,
-                             int64_t cols, uint8_t* codes, uint8_t* sf, float* ts,
+                             int64_t cols, uint8_t* codes, uint8_t* sf, float* ts, float* rrms,
                              void* workspace, size_t ws_bytes, moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------------
@@ -190,8 +193,12 @@ int moe_plan(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* topk
  *     rejected with MOE_ERR_WORKSPACE_TOO_SMALL: ceil(T/64)*E (ceil(T/32)*E for k > 16) must
  *     stay within about 130,000, e.g. up to T = 8,128 tokens at E = 1,024 experts, 32,704 at
  *     E = 256, 65,472 at E = 128.
- *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
- *     that device current; make that first call before any stream capture.
+ *   - Every call that is not being recorded into a CUDA graph looks up the array's device
+ *     address (cudaGetSymbolAddress) on the current device, so a device reset, which may move
+ *     the array, is picked up by the next call.  A call made during stream capture reuses the
+ *     address found by the last uncaptured call on that device: make the first call on a device,
+ *     and the first call after a reset, outside any capture (a captured call with no earlier
+ *     lookup returns MOE_ERR_CUDA).
  *   - All calls share the one array per device, and it keeps the last call's contents: calls
  *     that may overlap on the GPU (two streams, two threads) race and must be serialised by the
  *     caller.  The device status word in the array is cleared at the start of every call.

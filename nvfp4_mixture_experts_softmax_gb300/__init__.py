@@ -77,7 +77,7 @@ def lib():
             "moe_run_kernel_count": (C.c_int, [cfgp, i32]),
             "moe_set_router_bias": (C.c_int, [cfgp, vp, vp, vp]),
             "moe_rmsnorm_workspace_size": (sz, [i64]),
-            "moe_rmsnorm_quantize_act": (C.c_int, [vp, vp, C.c_float, i64, i64, vp, vp, vp, vp, sz,
+            "moe_rmsnorm_quantize_act": (C.c_int, [vp, vp, C.c_float, i64, i64, vp, vp, vp, vp, vp, sz,
                                                    vp]),
         }
         for name, (res, args) in sig.items():
@@ -185,22 +185,25 @@ def quantize_act(x, workspace=None, stream=None):
 
 
 def rmsnorm_quantize_act(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6,
-                         workspace=None, stream=None):
+                         workspace=None, stream=None, want_rrms: bool = False):
     """RMSNorm of BF16 x [rows, cols] by BF16 gamma [cols], then NVFP4 (codes, sf, ts) on the
-    device; raises on a non-finite result (device status) only via last_device_status."""
+    device (+ each row's 1/rms when want_rrms); a non-finite result is reported through the
+    device status (last_device_status), not raised here."""
     rows, cols = x.shape
     dev = x.device
     codes = torch.empty(rows, cols // 2, dtype=torch.uint8, device=dev)
     sf = torch.empty(rows, cols // 16, dtype=torch.uint8, device=dev)
     ts = torch.empty(1, dtype=torch.float32, device=dev)
+    rr = torch.empty(rows, dtype=torch.float32, device=dev) if want_rrms else None
     if workspace is None:
         workspace = torch.empty(lib().moe_rmsnorm_workspace_size(rows), dtype=torch.uint8,
                                 device=dev)
     _check(lib().moe_rmsnorm_quantize_act(_ptr(x), _ptr(gamma), float(eps), rows, cols,
-                                          _ptr(codes), _ptr(sf), _ptr(ts), _ptr(workspace),
+                                          _ptr(codes), _ptr(sf), _ptr(ts),
+                                          _ptr(rr) if rr is not None else None, _ptr(workspace),
                                           workspace.numel(), _stream(stream)),
            "moe_rmsnorm_quantize_act")
-    return codes, sf, ts
+    return (codes, sf, ts, rr) if want_rrms else (codes, sf, ts)
 
 
 def plan(logits, k: int, workspace=None, stream=None):

@@ -137,7 +137,7 @@ size_t moe_rmsnorm_workspace_size(int64_t rows) {
 }
 
 int moe_rmsnorm_quantize_act(const void* x, const void* gamma, float eps, int64_t rows,
-                             int64_t cols, uint8_t* codes, uint8_t* sf, float* ts,
+                             int64_t cols, uint8_t* codes, uint8_t* sf, float* ts, float* rrms,
                              void* workspace, size_t ws_bytes, moe_stream_t stream) {
   if (rows < 0 || cols <= 0 || cols % 16 != 0 || !(std::isfinite(eps) && eps >= 0.0f))
     return MOE_ERR_INVALID_ARG;
@@ -153,7 +153,8 @@ int moe_rmsnorm_quantize_act(const void* x, const void* gamma, float eps, int64_
   WsHeader* hdr = static_cast<WsHeader*>(workspace);
   if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return MOE_ERR_CUDA;
   uint32_t* scratch = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + 256);
-  return cuda_status(launch_rmsnorm_quant(x, gamma, eps, rows, cols, codes, sf, ts, scratch,
+  if (rrms && !aligned(rrms, 4)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_rmsnorm_quant(x, gamma, eps, rows, cols, codes, sf, ts, rrms, scratch,
                                           &hdr->status, s));
 }
 

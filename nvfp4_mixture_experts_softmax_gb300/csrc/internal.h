@@ -163,11 +163,11 @@ cudaError_t launch_act_encode_perm(const void* x, int T, int H, int k, int E, in
                                    uint8_t* codes, uint8_t* sf, uint8_t* xq_perm,
                                    uint8_t* xsf_tiles, int32_t* status, cudaStream_t s);
 
-// RMSNorm (sum of squares in float64, then FP32) of x [rows, cols] BF16 with gamma [cols] BF16,
-// then NVFP4 with the tensor scale of the normalised values; scratch: 4 + rows words.
+// RMSNorm (FP32) of x [rows, cols] BF16 with gamma [cols] BF16, then NVFP4 with the tensor scale
+// of the normalised values; each row's 1/rms also to rrms (may be null); scratch: 4 + rows words.
 cudaError_t launch_rmsnorm_quant(const void* x, const void* gamma, float eps, int64_t rows,
                                  int64_t cols, uint8_t* codes, uint8_t* sf, float* ts,
-                                 uint32_t* scratch, int32_t* status, cudaStream_t s);
+                                 float* rrms, uint32_t* scratch, int32_t* status, cudaStream_t s);
 
 cudaError_t launch_weight_quant(const moe_config& c, const WeightLayout& L, const void* wg,
                                 const void* wu, const void* wd, const void* sg, const void* su,

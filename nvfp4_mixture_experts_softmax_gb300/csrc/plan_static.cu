@@ -4,9 +4,17 @@
 // framework that owns every device allocation, code that runs while a memory pool is frozen or
 // capped, or a thin C caller with no allocator of its own.  This entry point therefore keeps its
 // scratch in a file-scope static device array of a fixed size.  Every GPU that loads the library
-// reserves that array until the process exits.  The array's address is looked up with
-// cudaGetSymbolAddress once per device (on that device's first call), because in host code the
-// array's name is only a host-side stand-in, not a device address.
+// reserves that array until the process exits.  In host code the array's name is only a
+// host-side stand-in, not a device address, so the address is looked up with
+// cudaGetSymbolAddress, with the target device current.
+//
+// The lookup is repeated on every call that is not being recorded into a CUDA graph: a device
+// reset (cudaDeviceReset, or a reset of the primary context by another runtime in the process)
+// reloads the module and may move the array, and a cached address would then point at freed
+// memory.  A call made during stream capture cannot take that lookup safely (it may load the
+// module, which capture forbids), so it uses the address found by the last uncaptured call on
+// the same device: the first call on a device, and the first call after a reset, must come before
+// any capture.
 #include <mutex>
 
 #include "internal.h"
@@ -19,18 +27,22 @@ static __device__ __align__(256) uint8_t g_plan_scratch[kStaticPlanScratchBytes]
 
 constexpr int kMaxDevices = 128;
 std::mutex g_setup_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
+void* g_scratch_ptr[kMaxDevices] = {};   // address found by the last uncaptured call per device
 
-// Device address of g_plan_scratch on the current device (looked up once per device).
-int scratch_on_current_device(uint8_t** out) {
+// Device address of g_plan_scratch on the current device.
+int scratch_on_current_device(cudaStream_t s, uint8_t** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return MOE_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
+  if (cap == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_plan_scratch) != cudaSuccess || p == nullptr)
       return MOE_ERR_CUDA;
     g_scratch_ptr[dev] = p;
+  } else if (g_scratch_ptr[dev] == nullptr) {
+    return MOE_ERR_CUDA;   // never looked up outside a capture on this device
   }
   *out = static_cast<uint8_t*>(g_scratch_ptr[dev]);
   return MOE_OK;
@@ -47,7 +59,7 @@ extern "C" int moe_plan_static(const float* logits, int32_t T, int32_t E, int32_
   const size_t need = moe_plan_workspace_size(T, E, k);
   if (need == 0 || need > kStaticPlanScratchBytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* scratch = nullptr;
-  const int st = scratch_on_current_device(&scratch);
+  const int st = scratch_on_current_device(reinterpret_cast<cudaStream_t>(stream), &scratch);
   if (st != MOE_OK) return st;
   // The plan clears the status word at the start of every call and overwrites every histogram
   // and base entry it later reads, so nothing left over from the previous call is used.

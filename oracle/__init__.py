@@ -1,8 +1,12 @@
-"""ctypes wrapper around the single-threaded C++ oracle of the NVFP4 MoE layer.
+"""ctypes wrapper around the C++ oracle of the NVFP4 MoE layer.
 
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this module; the product library never does, and the two share no code.
 Every function here only marshals numpy arrays into the C routines of ``moe_oracle.cpp``.
+
+The source builds twice: ``liboracle_moe.so`` (single-threaded, the oracle proper) and, where the
+compiler has OpenMP, ``liboracle_moe_omp.so`` (the same loops spread over independent experts,
+rows and tokens; identical bits).  ``use_threads(n)`` routes later calls to the second build.
 """
 from __future__ import annotations
 
@@ -15,18 +19,50 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "moe_oracle.cpp")
 _LIB_PATH = os.path.join(_HERE, "liboracle_moe.so")
-_lib = None
+_OMP_PATH = os.path.join(_HERE, "liboracle_moe_omp.so")
+_libs = {}          # path -> loaded library
+_active = _LIB_PATH
+
+
+def _compile(path: str, extra) -> bool:
+    if os.path.exists(path) and os.path.getmtime(path) >= os.path.getmtime(_SRC):
+        return True
+    tmp = path + f".tmp{os.getpid()}"
+    cmd = ["g++", "-O2", "-std=c++17", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+           *extra, "-o", tmp, _SRC]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        if not extra:
+            raise RuntimeError(f"oracle build failed:\n{r.stderr}")
+        return False
+    os.replace(tmp, path)
+    return True
 
 
 def build(force: bool = False) -> str:
-    """Compile the oracle with g++ (-ffp-contract=off: no fused multiply-add anywhere)."""
-    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
-        tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        cmd = ["g++", "-O2", "-std=c++17", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
-               "-o", tmp, _SRC]
-        subprocess.run(cmd, check=True)
-        os.replace(tmp, _LIB_PATH)
+    """Compile the oracle with g++ (-ffp-contract=off: no fused multiply-add anywhere), once
+    single-threaded and once with OpenMP (skipped where the compiler has none)."""
+    if force:
+        for p in (_LIB_PATH, _OMP_PATH):
+            if os.path.exists(p):
+                os.remove(p)
+    _compile(_LIB_PATH, [])
+    _compile(_OMP_PATH, ["-fopenmp"])
     return _LIB_PATH
+
+
+def use_threads(n) -> int:
+    """Route later oracle calls to the OpenMP build with n threads (n = None or 0: all host cores;
+    n = 1: the single-threaded build).  Returns the thread count in use."""
+    global _active
+    build()
+    if n == 1 or not os.path.exists(_OMP_PATH):
+        _active = _LIB_PATH
+        return 1
+    _active = _OMP_PATH
+    L = lib()
+    L.orc_set_threads(int(n or 0))
+    return int(L.orc_threads())
 
 
 class Expert(C.Structure):
@@ -46,6 +82,7 @@ class MoeArgs(C.Structure):
                 ("act_mode", C.c_int32), ("x_bf16", C.c_void_p), ("hb", C.c_void_p),
                 ("shb", C.c_void_p), ("hf", C.c_void_p)]
 
+
 ROUTER_MODES = {"softmax": 0, "sqrtsoftplus": 1}
 # activation precision of the layer: NVFP4 activations with h requantised to NVFP4, W4A16 (BF16
 # activations as they are, h rounded to BF16) or W4A8 (MXFP8 activations and h, MXFP4 weights)
@@ -53,10 +90,13 @@ ACT_MODES = {"nvfp4": 0, "bf16": 1, "mxfp8": 2}
 
 
 def lib():
-    global _lib
-    if _lib is None:
+    if _active not in _libs:
         build()
-        L = C.CDLL(_LIB_PATH)
+        L = C.CDLL(_active)
+        L.orc_set_threads.restype = None
+        L.orc_set_threads.argtypes = [C.c_int]
+        L.orc_threads.restype = C.c_int
+        L.orc_threads.argtypes = []
         L.orc_bf16_to_f32.restype = C.c_float
         L.orc_bf16_to_f32.argtypes = [C.c_uint16]
         L.orc_f32_to_bf16.restype = C.c_uint16
@@ -94,11 +134,12 @@ def lib():
                                     C.c_void_p, C.c_void_p]
         L.orc_sqrt_softplus.restype = C.c_float
         L.orc_sqrt_softplus.argtypes = [C.c_float]
-        L.orc_sum_squares_tree.restype = C.c_float
-        L.orc_sum_squares_tree.argtypes = [C.c_void_p, C.c_int64]
+        L.orc_sum_squares.restype = C.c_float
+        L.orc_sum_squares.argtypes = [C.c_void_p, C.c_int64]
         L.orc_rmsnorm_quantize.restype = C.c_int
         L.orc_rmsnorm_quantize.argtypes = [C.c_void_p, C.c_void_p, C.c_float, C.c_int64, C.c_int64,
-                                           C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]
+                                           C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                           C.c_void_p]
         L.orc_swiglu.restype = C.c_float
         L.orc_swiglu.argtypes = [C.c_float, C.c_float, C.c_int, C.c_float]
         L.orc_plan.restype = None
@@ -107,8 +148,8 @@ def lib():
         L.orc_moe_forward.argtypes = [C.POINTER(MoeArgs)]
         L.orc_moe_forward_bruteforce.restype = C.c_int
         L.orc_moe_forward_bruteforce.argtypes = [C.POINTER(MoeArgs)]
-        _lib = L
-    return _lib
+        _libs[_active] = L
+    return _libs[_active]
 
 
 def _p(a: np.ndarray):
@@ -171,11 +212,11 @@ def tensor_scale_bf16(x) -> float:
     return float(np.float32(lib().orc_tensor_scale_bf16(_p(xb), xb.size)))
 
 
-def rmsnorm_quantize(x, gamma, eps: float):
-    """RMSNorm of BF16 x [rows, cols] with BF16 gamma [cols] (FP32; the mean square summed in
-    8-element chunks combined by a balanced pairwise tree), then NVFP4 with the tensor scale of
-    the normalised values.  Returns (codes, sf, ts,
-    status, y) with y the FP32 normalised values."""
+def rmsnorm_quantize(x, gamma, eps: float, want_r: bool = False):
+    """RMSNorm of BF16 x [rows, cols] with BF16 gamma [cols] (FP32 arithmetic; the sum of squares
+    accumulated in float64 and rounded once to FP32), then NVFP4 with the tensor scale of the
+    normalised values.  Returns (codes, sf, ts, status, y) with y the FP32 normalised values, and
+    each row's 1/rms as a sixth item when want_r is set."""
     xb = as_bf16_bits(x)
     gb = np.ascontiguousarray(as_bf16_bits(gamma).reshape(-1))
     rows, cols = xb.shape
@@ -183,16 +224,18 @@ def rmsnorm_quantize(x, gamma, eps: float):
     sf = np.zeros((rows, cols // 16), np.uint8)
     ts = np.zeros(1, np.float32)
     y = np.zeros((rows, cols), np.float32)
+    r = np.zeros(rows, np.float32)
     st = lib().orc_rmsnorm_quantize(_p(xb), _p(gb), float(eps), rows, cols, _p(codes), _p(sf),
-                                    _p(ts), _p(y))
-    return codes, sf, float(ts[0]), int(st), y
+                                    _p(ts), _p(y), _p(r))
+    out = (codes, sf, float(ts[0]), int(st), y)
+    return out + (r,) if want_r else out
 
 
-def sum_squares_tree(v) -> float:
-    """The mean-square numerator of rmsnorm_quantize: 8-element chunks summed left to right,
-    chunk sums combined by a balanced pairwise tree (FP32)."""
+def sum_squares(v) -> float:
+    """The mean-square numerator of rmsnorm_quantize: the squares summed in float64, rounded once
+    to FP32."""
     v = np.ascontiguousarray(v, np.float32)
-    return float(lib().orc_sum_squares_tree(_p(v), v.size))
+    return float(lib().orc_sum_squares(_p(v), v.size))
 
 
 def dequantize(codes: np.ndarray, sf: np.ndarray, ts: float) -> np.ndarray:

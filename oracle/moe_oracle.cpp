@@ -5,6 +5,10 @@
 // table or header with the CUDA library; it is written from the format and layer definitions.
 // Build with -ffp-contract=off so that every FP32 product and sum is rounded on its own (the
 // sequential-FP32 arithmetic below is the definition, on x86-64 and on AArch64 alike).
+// The same source builds a second time with -fopenmp for the all-core CPU baseline: the only
+// parallel loops run over independent experts, rows or tokens (each writes its own outputs with
+// its own scratch), and every sum inside a row keeps its sequential order, so both builds give
+// identical bits.  The maxima use max, which is exact in any order.
 //
 // Definitions followed (page title, section):
 //  * NVFP4 = E2M1 values, FP8 E4M3 block scales over 16-element microblocks, FP32 tensor scale:
@@ -64,8 +68,28 @@
 #include <cstdint>
 #include <cstring>
 #include <vector>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 extern "C" {
+
+// Thread count of the OpenMP build (n <= 0: all host cores); the single-threaded build ignores it.
+void orc_set_threads(int n) {
+#ifdef _OPENMP
+  omp_set_num_threads(n > 0 ? n : omp_get_num_procs());
+#else
+  (void)n;
+#endif
+}
+
+int orc_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
 
 // ---------------------------------------------------------------------------------------------
 // Scalar formats
@@ -188,10 +212,11 @@ void orc_quantize_f32(const float* x, int64_t rows, int64_t cols, float ts, uint
 // Tensor scale of a BF16 tensor: max|x| / 2688 (2688 = 6 * 448, exact in FP32).
 float orc_tensor_scale_bf16(const uint16_t* x, int64_t n) {
   float amax = 0.0f;
-  bool nan = false;
+  int nan = 0;
+#pragma omp parallel for reduction(max : amax) reduction(| : nan)
   for (int64_t i = 0; i < n; ++i) {
     float a = std::fabs(orc_bf16_to_f32(x[i]));
-    if (std::isnan(a)) nan = true;
+    if (std::isnan(a)) nan = 1;
     else if (a > amax) amax = a;
   }
   if (nan) return NAN;
@@ -205,10 +230,14 @@ int orc_quantize_bf16(const uint16_t* x, int64_t rows, int64_t cols, uint8_t* co
   float ts = orc_tensor_scale_bf16(x, rows * cols);
   *ts_out = ts;
   if (!std::isfinite(ts)) return -6;
-  std::vector<float> row(cols);
-  for (int64_t r = 0; r < rows; ++r) {
-    for (int64_t c = 0; c < cols; ++c) row[c] = orc_bf16_to_f32(x[r * cols + c]);
-    orc_quantize_f32(row.data(), 1, cols, ts, codes + r * (cols / 2), sf + r * (cols / 16));
+#pragma omp parallel
+  {
+    std::vector<float> row(cols);
+#pragma omp for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+      for (int64_t c = 0; c < cols; ++c) row[c] = orc_bf16_to_f32(x[r * cols + c]);
+      orc_quantize_f32(row.data(), 1, cols, ts, codes + r * (cols / 2), sf + r * (cols / 16));
+    }
   }
   return 0;
 }
@@ -284,37 +313,30 @@ void orc_mx_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t rows
 // feeding the layer's activation quantiser: "nvfp4-megamoe-kernel compare pre-b1...master",
 // sections "P4 - Fused RMSNorm + NVFP4 quantize" and "P5"; two passes, the tensor scale taken
 // from the normalised values).  The pages leave the summation order of the mean square open; the
-// reading taken fixes it so that the result is one exact FP32 value: the row is cut into chunks
-// of 8 consecutive elements, each chunk's squares are summed left to right, and the chunk sums
-// are combined by a balanced pairwise tree over the chunk index (padded with zeros to a power of
-// two).  Then ms = sum / cols, r = 1 / sqrt(ms + eps), y_c = (x_c * r) * gamma_c (FP32, in that
-// order); ts = max|y| / 2688 over the whole tensor and the block encode of y (as
-// orc_quantize_f32).  Writes y [rows, cols] if y_out is not null.  Returns -6 when max|y| is
-// not finite.  cols must be a multiple of 8.
-float orc_sum_squares_tree(const float* v, int64_t n) {
-  const int64_t nchunk = n / 8;
-  int64_t P = 1;
-  while (P < nchunk) P *= 2;
-  std::vector<float> part(P, 0.0f);
-  for (int64_t c = 0; c < nchunk; ++c) {
-    float s = v[c * 8] * v[c * 8];
-    for (int i = 1; i < 8; ++i) s = s + v[c * 8 + i] * v[c * 8 + i];
-    part[c] = s;
-  }
-  for (int64_t width = 1; width < P; width *= 2)
-    for (int64_t i = 0; i < P; i += 2 * width) part[i] = part[i] + part[i + width];
-  return part[0];
+// reading taken is the plain one: the sum of the squares, accumulated in float64 (each square of
+// a BF16 value is exact in float64, and the float64 sum of up to 2^14 of them is within
+// n * 2^-53 of the exact sum, far below the FP32 rounding that follows) and rounded once to FP32.
+// Then ms = sum / cols, r = 1 / sqrt(ms + eps), y_c = (x_c * r) * gamma_c (FP32, in that order);
+// ts = max|y| / 2688 over the whole tensor and the block encode of y (as orc_quantize_f32).
+// Writes y [rows, cols] if y_out is not null and each row's r into r_out if it is not null.
+// Returns -6 when max|y| is not finite.
+float orc_sum_squares(const float* v, int64_t n) {
+  double s = 0.0;
+  for (int64_t i = 0; i < n; ++i) s += (double)v[i] * (double)v[i];
+  return (float)s;
 }
 
 int orc_rmsnorm_quantize(const uint16_t* x, const uint16_t* gamma, float eps, int64_t rows,
-                         int64_t cols, uint8_t* codes, uint8_t* sf, float* ts_out, float* y_out) {
+                         int64_t cols, uint8_t* codes, uint8_t* sf, float* ts_out, float* y_out,
+                         float* r_out) {
   std::vector<float> y((size_t)rows * cols), row(cols);
   float amax = 0.0f;
   bool nan = false;
   for (int64_t r = 0; r < rows; ++r) {
     for (int64_t c = 0; c < cols; ++c) row[c] = orc_bf16_to_f32(x[r * cols + c]);
-    const float ms = orc_sum_squares_tree(row.data(), cols) / (float)cols;
+    const float ms = orc_sum_squares(row.data(), cols) / (float)cols;
     const float rinv = 1.0f / std::sqrt(ms + eps);
+    if (r_out) r_out[r] = rinv;
     for (int64_t c = 0; c < cols; ++c) {
       const float v = (row[c] * rinv) * orc_bf16_to_f32(gamma[c]);
       y[r * cols + c] = v;
@@ -568,40 +590,54 @@ int orc_moe_forward(const orc_moe_args* a) {
 
   std::vector<float> D((size_t)R * H);
   const int Imax = std::max(I, a->I_shared);
-  std::vector<float> Wg, Wu, Wd, h(Imax), hhat(Imax);
-  std::vector<uint8_t> hq_row(Imax), hsf_row(Imax / 16);   // room for every mode's codes
-  std::vector<uint16_t> hb_row(Imax);
   const int mx = a->act_mode == 2;
   const int64_t hq_w = mx ? I : I / 2, hs_w = mx ? I / 32 : I / 16;   // bytes per routed h row
-  for (int e = 0; e < E; ++e) {
-    if (counts[e] == 0) continue;
-    dequant_expert(a->experts[e], H, I, a->act_mode, Wg, Wu, Wd);
-    for (int32_t p = offsets[e]; p < offsets[e + 1]; ++p) {
-      const float* xr = xhat.data() + (int64_t)perm_src[p] * H;
-      expert_row(xr, Wg.data(), Wu.data(), Wd.data(), H, I, a->ts_h, a->swiglu_clamp,
-                 a->swiglu_limit, a->act_mode, h.data(), hhat.data(), hq_row.data(),
-                 hsf_row.data(), hb_row.data(), D.data() + (int64_t)p * H);
-      if (a->act_mode != 1 && a->hq) std::memcpy(a->hq + (int64_t)p * hq_w, hq_row.data(), hq_w);
-      if (a->act_mode != 1 && a->hsf) std::memcpy(a->hsf + (int64_t)p * hs_w, hsf_row.data(), hs_w);
-      if (a->act_mode == 1 && a->hb) std::copy(hb_row.begin(), hb_row.begin() + I, a->hb + (int64_t)p * I);
-      if (a->hf) std::copy(h.begin(), h.begin() + I, a->hf + (int64_t)p * I);
+  // experts are independent: each writes only its own permuted rows of D, hq, hsf, hb, hf
+#pragma omp parallel
+  {
+    std::vector<float> Wg, Wu, Wd, h(Imax), hhat(Imax);
+    std::vector<uint8_t> hq_row(Imax), hsf_row(Imax / 16);   // room for every mode's codes
+    std::vector<uint16_t> hb_row(Imax);
+#pragma omp for schedule(dynamic, 1)
+    for (int e = 0; e < E; ++e) {
+      if (counts[e] == 0) continue;
+      dequant_expert(a->experts[e], H, I, a->act_mode, Wg, Wu, Wd);
+      for (int32_t p = offsets[e]; p < offsets[e + 1]; ++p) {
+        const float* xr = xhat.data() + (int64_t)perm_src[p] * H;
+        expert_row(xr, Wg.data(), Wu.data(), Wd.data(), H, I, a->ts_h, a->swiglu_clamp,
+                   a->swiglu_limit, a->act_mode, h.data(), hhat.data(), hq_row.data(),
+                   hsf_row.data(), hb_row.data(), D.data() + (int64_t)p * H);
+        if (a->act_mode != 1 && a->hq) std::memcpy(a->hq + (int64_t)p * hq_w, hq_row.data(), hq_w);
+        if (a->act_mode != 1 && a->hsf) std::memcpy(a->hsf + (int64_t)p * hs_w, hsf_row.data(), hs_w);
+        if (a->act_mode == 1 && a->hb) std::copy(hb_row.begin(), hb_row.begin() + I, a->hb + (int64_t)p * I);
+        if (a->hf) std::copy(h.begin(), h.begin() + I, a->hf + (int64_t)p * I);
+      }
     }
   }
   std::vector<float> S;
   if (a->has_shared) {
     const int Is = a->I_shared;
     S.resize((size_t)T * H);
+    std::vector<float> Wg, Wu, Wd;
     dequant_expert(a->experts[E], H, Is, a->act_mode, Wg, Wu, Wd);
     const int64_t shq_w = mx ? Is : Is / 2, shs_w = mx ? Is / 32 : Is / 16;
-    for (int64_t t = 0; t < T; ++t) {
-      expert_row(xhat.data() + t * H, Wg.data(), Wu.data(), Wd.data(), H, Is, a->ts_h,
-                 a->swiglu_clamp, a->swiglu_limit, a->act_mode, h.data(), hhat.data(),
-                 hq_row.data(), hsf_row.data(), hb_row.data(), S.data() + t * H);
-      if (a->act_mode != 1 && a->shq) std::memcpy(a->shq + t * shq_w, hq_row.data(), shq_w);
-      if (a->act_mode != 1 && a->shsf) std::memcpy(a->shsf + t * shs_w, hsf_row.data(), shs_w);
-      if (a->act_mode == 1 && a->shb) std::copy(hb_row.begin(), hb_row.begin() + Is, a->shb + t * Is);
+#pragma omp parallel
+    {
+      std::vector<float> h(Imax), hhat(Imax);
+      std::vector<uint8_t> hq_row(Imax), hsf_row(Imax / 16);
+      std::vector<uint16_t> hb_row(Imax);
+#pragma omp for schedule(dynamic, 4)
+      for (int64_t t = 0; t < T; ++t) {
+        expert_row(xhat.data() + t * H, Wg.data(), Wu.data(), Wd.data(), H, Is, a->ts_h,
+                   a->swiglu_clamp, a->swiglu_limit, a->act_mode, h.data(), hhat.data(),
+                   hq_row.data(), hsf_row.data(), hb_row.data(), S.data() + t * H);
+        if (a->act_mode != 1 && a->shq) std::memcpy(a->shq + t * shq_w, hq_row.data(), shq_w);
+        if (a->act_mode != 1 && a->shsf) std::memcpy(a->shsf + t * shs_w, hsf_row.data(), shs_w);
+        if (a->act_mode == 1 && a->shb) std::copy(hb_row.begin(), hb_row.begin() + Is, a->shb + t * Is);
+      }
     }
   }
+#pragma omp parallel for schedule(static)
   for (int64_t t = 0; t < T; ++t)
     for (int m = 0; m < H; ++m) {
       float acc = 0.0f;

@@ -120,12 +120,36 @@ def test_decode_every_expert_multi_tile_with_shared(moe):
     run_and_check(moe, cs, 48)
 
 
-def test_repeat_calls_consistent(moe):
-    cs = synth.CONFIGS["tiny"]
-    y1, _, _ = run_and_check(moe, cs, 16)
-    y2, _, _ = run_and_check(moe, cs, 16)
-    d = (y1.float() - y2.float()).abs().max().item()
-    assert d <= 1e-2 * y1.float().abs().max().item()
+def test_repeat_calls_bit_identical_on_decode_path(moe):
+    """Decode-sized batches combine each token's stored rows in slot order: two calls give the
+    same bits (a stale plan or a race between the GEMMs would show here)."""
+    for name, T in (("tiny", 16), ("decode", 64), ("decode", 1)):
+        cs = synth.CONFIGS[name]
+        y1, _, _ = run_and_check(moe, cs, T)
+        y2, _, _ = run_and_check(moe, cs, T)
+        assert torch.equal(y1, y2), (name, T)
+
+
+def test_repeat_calls_general_path_within_rounding(moe):
+    """Large batches add the k routed contributions (and the shared one) into the token row with
+    FP32 reductions in arbitrary order, so two calls may differ by FP32 rounding, which the final
+    BF16 rounding turns into at most one BF16 step, and only for rare values."""
+    cs = synth.custom_config("general_repeat", 3000, 512, 16, 4, 256, shared_inter=256,
+                             config_id=171)
+    cfg = moe.make_config(cs.experts, cs.hidden, cs.inter, cs.top_k, shared_inter=256,
+                          max_tokens=3000)
+    assert moe.run_kernel_count(cfg, 3000) >= 6          # the general path
+    wg, wu, wd = synth.gen_all_experts(cs, device="cuda")
+    wbuf = moe.quantize_weights(cfg, wg, wu, wd, shared=synth.gen_shared(cs, device="cuda"))
+    x = synth.gen_x(cs, 3000, device="cuda")
+    lg = synth.gen_logits(cs, 3000, device="cuda")
+    ys = [moe.run(cfg, wbuf, x, lg).float() for _ in range(3)]
+    for y in ys[1:]:
+        d = (y - ys[0]).abs()
+        mag = torch.maximum(y.abs(), ys[0].abs())
+        ulp = torch.pow(2.0, torch.floor(torch.log2(torch.clamp(mag, min=1e-30))) - 7)
+        assert bool((d <= ulp).all()), float((d / ulp).max())
+        assert float((d > 0).float().mean()) <= 1e-2
 
 
 def test_zero_tokens_and_errors(moe):
@@ -172,7 +196,6 @@ def test_cuda_graph_replay_matches_eager(moe):
         g.replay()
         torch.cuda.synchronize()
         assert moe.last_device_status(ws) == 0
-        d = (y.float() - y_eager.float()).abs().max().item()
-        assert d <= 1e-2 * y_eager.float().abs().max().item()
+        assert torch.equal(y, y_eager)      # the decode path is deterministic
         ms = timer.stage_ms()
         assert all(v >= 0 for v in ms.values()) and sum(ms.values()) > 0

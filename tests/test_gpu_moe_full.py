@@ -1,7 +1,15 @@
 """GPU parity at the full sizes of the prefill, large (+ shared expert) and Zipf-skewed
-workloads, in the launch configuration the benchmark times.  Whole-tensor bit-exact checks where
-the oracle is cheap (activation quantiser, router, permutation, sampled experts' weights) and
-per-token checks of the layer output and the requantised intermediate on sampled tokens."""
+workloads, in the launch configuration the benchmark times.
+
+Whole-tensor bit-exact checks where the oracle is cheap (activation quantiser, router,
+permutation) and per-token checks of the layer output and the requantised intermediate on tokens
+chosen from the plan: at least one compared token in every 128-row tile of expert-ordered rows
+(the GEMMs' M tiles, the shared expert's included), plus the token of the last row of the last,
+ragged tile of each of the five busiest experts.  Every expert that any compared token uses is
+quantised by the oracle and its packed weights are compared bit for bit.  The oracle runs on
+all host cores (its OpenMP build, whose bits equal the single-threaded build's)."""
+import concurrent.futures as cf
+
 import numpy as np
 import pytest
 import torch
@@ -12,6 +20,8 @@ from parity import assert_h_close, assert_y_close
 
 pytestmark = pytest.mark.gpu
 
+TILE = 128
+
 
 @pytest.fixture(scope="module")
 def moe():
@@ -19,11 +29,42 @@ def moe():
         pytest.skip("no CUDA device")
     import nvfp4_mixture_experts_softmax_gb300 as m
     m.lib()
-    return m
+    oracle.use_threads(None)
+    yield m
+    oracle.use_threads(1)
 
 
-@pytest.mark.parametrize("name,nsample", [("prefill", 12), ("skewed", 8), ("large", 3)])
-def test_full_size_sampled(moe, name, nsample):
+def covering_tokens(counts, offsets, perm_src, inv, T, k, shared):
+    """Tokens such that every TILE-row tile of every segment (expert, then the shared expert's T
+    rows) holds a row of one of them, plus the last row of the five busiest experts."""
+    E = len(counts)
+    tiles = []                       # (first row, end row) in the permuted row space
+    for e in range(E):
+        for r0 in range(int(offsets[e]), int(offsets[e + 1]), TILE):
+            tiles.append((r0, min(r0 + TILE, int(offsets[e + 1]))))
+    R = T * k
+    tile_of = np.empty(R, np.int64)
+    for i, (a, b) in enumerate(tiles):
+        tile_of[a:b] = i
+    covered = np.zeros(len(tiles), bool)
+    chosen = []
+    for i, (a, b) in enumerate(tiles):
+        if covered[i]:
+            continue
+        t = int(perm_src[b - 1])      # the tile's last row (the ragged end for a last tile)
+        chosen.append(t)
+        covered[tile_of[inv[t * k:(t + 1) * k]]] = True
+    for e in np.argsort(-counts, kind="stable")[:5]:
+        chosen.append(int(perm_src[offsets[e + 1] - 1]))
+    toks = set(chosen)
+    if shared:                       # the shared expert's rows are the tokens in order
+        toks.update(range(0, T, TILE))
+        toks.add(T - 1)
+    return np.array(sorted(toks)), len(tiles) + (-(-T // TILE) if shared else 0)
+
+
+@pytest.mark.parametrize("name", ["prefill", "skewed", "large"])
+def test_full_size_every_tile(moe, name):
     cs = synth.CONFIGS[name]
     T, k, E = cs.tokens[0], cs.top_k, cs.experts
     dev = "cuda"
@@ -50,31 +91,32 @@ def test_full_size_sampled(moe, name, nsample):
     assert np.array_equal(g["counts"], counts) and np.array_equal(g["offsets"], offsets)
     assert np.array_equal(g["perm_src"], perm_src) and np.array_equal(g["inv"], inv)
 
-    # sampled tokens: first, last, the busiest expert's first token, and seeded random ones
-    rng = np.random.default_rng(cs.config_id)
-    busiest = int(np.argmax(counts))
-    first_busy = int(perm_src[offsets[busiest]])
-    toks = sorted(set([0, T - 1, first_busy] + rng.choice(T, nsample, replace=False).tolist()))
-    toks = np.array(toks[:nsample + 3])
+    toks, ntiles = covering_tokens(counts, offsets, perm_src, inv, T, k, sh is not None)
     used = np.unique(ids[toks])
-    experts = [None] * E
+    # oracle quantisation of every expert the compared tokens use (threads: the C calls release
+    # the interpreter lock), and the packed weights of each of them bit for bit
+    def quant(e):
+        return oracle.QuantExpert.from_bf16(wg[e].cpu(), wu[e].cpu(), wd[e].cpu())
+
+    with cf.ThreadPoolExecutor(4) as ex:
+        qs = dict(zip(used.tolist(), ex.map(quant, used.tolist())))
+    experts = [qs.get(e) for e in range(E)]
     for e in used:
-        experts[e] = oracle.QuantExpert.from_bf16(wg[e].cpu(), wu[e].cpu(), wd[e].cpu())
-        if e in (used[0], used[-1]):   # the packed weights of a few experts, bit-exact
-            for m, W in enumerate((wg[e], wu[e], wd[e])):
-                c, s, t = moe.weights_export(cfg, wbuf, int(e), m)
-                assert t.item() == experts[e].ts[m]
-                assert np.array_equal(c.cpu().numpy(), experts[e].codes[m])
-                assert np.array_equal(s.cpu().numpy(), experts[e].sf[m])
+        for m in range(3):
+            c, s, t = moe.weights_export(cfg, wbuf, int(e), m)
+            assert t.item() == experts[e].ts[m]
+            assert np.array_equal(c.cpu().numpy(), experts[e].codes[m])
+            assert np.array_equal(s.cpu().numpy(), experts[e].sf[m])
     sho = oracle.QuantExpert.from_bf16(*[s.cpu() for s in sh]) if sh is not None else None
     y_ref, od = oracle.moe_forward(xq[toks], xsf[toks], ts_a, lg[toks], experts, k, shared=sho,
                                    want_debug=True)
     yg = y.float().cpu().numpy()[toks]
     assert_y_close(yg, oracle.bf16_bits_to_f32(y_ref))
-    # intermediate rows of the sampled assignments
+    # intermediate rows of the compared tokens' assignments (and shared-expert rows)
     rows_gpu = np.array([inv[t * k + j] for t in toks for j in range(k)])
     rows_ref = np.array([od["inv"][i * k + j] for i in range(len(toks)) for j in range(k)])
     assert_h_close(g["hq"][rows_gpu], g["hsf"][rows_gpu], od["hq"][rows_ref], od["hsf"][rows_ref])
     if sh is not None:
         R = T * k
         assert_h_close(g["hq"][R + toks], g["hsf"][R + toks], od["shq"], od["shsf"])
+    print(f"{name}: {len(toks)} tokens cover {ntiles} tiles, {len(used)} experts")

@@ -143,3 +143,50 @@ def test_act_quant_every_bf16_every_scale(moe):
     assert st == 0 and rts == 1.0 and ts.item() == 1.0
     assert np.array_equal(sf.cpu().numpy(), rs)
     assert np.array_equal(codes.cpu().numpy(), rc)
+
+
+def boundary_blocks(A: float, nblk: int, seed: int):
+    """BF16 rows [nblk, 16] whose tensor maximum is A (a non-power-of-two value) and whose
+    elements sit on and around b * S for every E2M1 rounding boundary b, S being the block's
+    decoded scale times the tensor scale: the quotients x / S that the encoder divides fall on,
+    just below and just above the boundaries (at BF16 resolution), a small share of them within
+    one FP32 step of a boundary.  Also returns the host-side quotients, for counting those."""
+    rng = np.random.default_rng(seed)
+    bounds = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+    ts = np.float32(A) / np.float32(2688.0)
+    # block maxima M in (A/64, A]: BF16 values with random significands
+    M = torch.from_numpy((A * np.exp2(-rng.uniform(0, 6, nblk))).astype(np.float32))
+    M = M.to(torch.bfloat16).float().numpy()
+    M[0] = A
+    t = (M / np.float32(6.0)).astype(np.float32) / ts
+    sf = torch.from_numpy(t.astype(np.float32)).to(torch.float8_e4m3fn).float().numpy()
+    S = (sf * ts).astype(np.float32)
+    x = np.zeros((nblk, 16), np.float32)
+    x[:, 0] = M
+    b = bounds[rng.integers(0, 7, (nblk, 15))]
+    c = torch.from_numpy((b * S[:, None]).astype(np.float32)).to(torch.bfloat16)
+    step = torch.from_numpy(rng.integers(-1, 2, (nblk, 15)).astype(np.int16))
+    bits = c.view(torch.int16) + step                 # BF16 neighbours (all values positive)
+    v = bits.view(torch.bfloat16).float().numpy()
+    sign = np.where(rng.random((nblk, 15)) < 0.5, -1.0, 1.0).astype(np.float32)
+    x[:, 1:] = v * sign
+    q = np.abs(x[:, 1:].astype(np.float64)) / S[:, None].astype(np.float64)
+    return torch.from_numpy(x).to(torch.bfloat16), q, b
+
+
+def test_act_quant_quotients_at_e2m1_boundaries_non_power_of_two_scale(moe):
+    """The encoder's quotient x / S comes from a reciprocal, a product and one correction step;
+    on inputs built so that x / S falls on and next to every E2M1 rounding boundary, with tensor
+    scales whose significands are not powers of two (so S has a full 24-bit significand), the
+    codes must equal the oracle's IEEE-division codes bit for bit."""
+    near = 0
+    ties = 0
+    for i, A in enumerate((3.140625, 0.0107421875, 77.5, 1234.0, 5.96875e-3, 0.83984375)):
+        A = float(torch.tensor(A).to(torch.bfloat16).float())
+        x, q, b = boundary_blocks(A, 1 << 16, seed=40 + i)
+        _check_act(moe, x)
+        d = np.abs(q - b)
+        ties += int((d == 0).sum())
+        near += int(((d > 0) & (d <= np.spacing(b.astype(np.float32)).astype(np.float64))).sum())
+    # the inputs reach the cases the correction step exists for
+    assert ties > 0 and near > 0, (ties, near)

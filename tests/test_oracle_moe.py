@@ -139,3 +139,26 @@ def test_exact_products_against_float64(orc):
         yt = Wd @ hhat
         want = torch.from_numpy(yt.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy()
         assert np.array_equal(y[t].view(np.int16), want)
+
+
+def test_openmp_build_gives_identical_bits(orc):
+    """The all-core build of the oracle (OpenMP over independent experts, rows and tokens) gives
+    the single-threaded oracle's bits: outputs, routing, plan and requantised intermediates."""
+    cs = synth.custom_config("omp", 24, 256, 6, 3, 256, shared_inter=256, config_id=170)
+    x = synth.gen_x(cs, 24)
+    lg = synth.gen_logits(cs, 24).numpy()
+    ex = [orc.QuantExpert.from_bf16(*synth.gen_expert(cs, e)) for e in range(cs.experts)]
+    sh = orc.QuantExpert.from_bf16(*synth.gen_shared(cs))
+    outs = []
+    for n in (1, 4):
+        if orc.use_threads(n) != n and n != 1:
+            pytest.skip("no OpenMP build of the oracle on this host")
+        xq, xsf, ts, _ = orc.quantize_bf16(x)
+        y, d = orc.moe_forward(xq, xsf, ts, lg, ex, cs.top_k, shared=sh, want_debug=True)
+        outs.append((xq, xsf, ts, y, d))
+    orc.use_threads(1)
+    a, b = outs
+    assert a[2] == b[2] and np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    assert np.array_equal(a[3], b[3])
+    for key in a[4]:
+        assert np.array_equal(a[4][key], b[4][key]), key

@@ -1,7 +1,7 @@
 """Oracle pins for RMSNorm + NVFP4 quantisation (the producer feeding the activation quantiser;
 "nvfp4-megamoe-kernel compare pre-b1...master", sections "P4 - Fused RMSNorm + NVFP4 quantize"
-and "P5"): exact special cases, scale invariance, float64 agreement and the reduction to the
-plain quantiser of the normalised values."""
+and "P5"): exact special cases, scale invariance, float64 agreement, the sum of squares against
+exact rational arithmetic, and the reduction to the plain quantiser of the normalised values."""
 import numpy as np
 import torch
 
@@ -59,17 +59,50 @@ def test_zero_gamma_gives_zero():
     assert st == 0 and ts == 0.0 and not y.any() and not codes.any() and not sf.any()
 
 
-def test_sum_squares_tree_exact_cases():
-    # a power-of-two count of equal squares sums exactly; sixteen chunks of ones = 128
-    assert oracle.sum_squares_tree(np.ones(128, np.float32)) == 128.0
-    # the pairwise order is observable: chunk sums 2^24, 1, 1, 1 give (2^24 + 1) + (1 + 1)
-    # = 2^24 + 2 (the first pair rounds to 2^24, the second is exact), where a left-to-right sum
-    # would stay at 2^24
+def _round_f32(q):
+    """The FP32 value nearest to the exact rational q >= 0 (ties to even), in exact arithmetic."""
+    from fractions import Fraction
+    if q == 0:
+        return 0.0
+    e = q.numerator.bit_length() - q.denominator.bit_length()
+    if Fraction(2) ** e > q:
+        e -= 1
+    quantum = Fraction(2) ** (e - 23)          # 24 significant bits (normal range)
+    n, rem = divmod(q, quantum)
+    if rem * 2 > quantum or (rem * 2 == quantum and n % 2 == 1):
+        n += 1
+    return float(n * quantum)
+
+
+def test_sum_squares_is_the_exact_sum_rounded_once():
+    from fractions import Fraction
+    # a power-of-two count of equal squares sums exactly
+    assert oracle.sum_squares(np.ones(128, np.float32)) == 128.0
+    # squares 2^24, 1, 1, 1: the exact sum 2^24 + 3 lies halfway between two FP32 values and
+    # rounds to the even one, 2^24 + 4.  A left-to-right FP32 sum stays at 2^24 and a pairwise
+    # tree over chunks of 8 gives 2^24 + 2: both fail here.
     v = np.zeros(32, np.float32)
     v[0] = 4096.0
     v[8] = v[16] = v[24] = 1.0
-    assert oracle.sum_squares_tree(v) == np.float32(2.0**24 + 2)
-    # agreement with float64 within the FP32 tree's error bound
-    r = np.random.default_rng(8).standard_normal(7168).astype(np.float32)
-    exact = float((r.astype(np.float64) ** 2).sum())
-    assert abs(oracle.sum_squares_tree(r) - exact) <= 7168 * 2 ** -24 * exact
+    assert oracle.sum_squares(v) == 2.0**24 + 4
+    # BF16-valued rows with a wide spread of magnitudes (tiny values included): the correctly
+    # rounded FP32 of the exact rational sum, whatever the order of the elements
+    rng = np.random.default_rng(8)
+    for n in (7, 2048, 7168):
+        r = (rng.standard_normal(n) * np.exp2(rng.integers(-20, 8, n))).astype(np.float32)
+        r = torch.from_numpy(r).to(torch.bfloat16).float().numpy()
+        exact = sum(Fraction(float(a)) ** 2 for a in r)
+        assert oracle.sum_squares(r) == _round_f32(exact)
+        assert oracle.sum_squares(rng.permutation(r)) == oracle.sum_squares(r)
+
+
+def test_rms_of_each_row():
+    """Each row's 1/rms follows from the rounded sum: r = 1 / sqrt(sum / cols + eps) in FP32."""
+    rng = np.random.default_rng(9)
+    x = torch.from_numpy(rng.standard_normal((6, 512)).astype(np.float32)).to(torch.bfloat16)
+    g = _gamma(512, 10)
+    *_, r = oracle.rmsnorm_quantize(x, g, 1e-5, want_r=True)
+    for i in range(6):
+        s = np.float32(oracle.sum_squares(x[i].float().numpy()))
+        want = np.float32(1.0) / np.sqrt(s / np.float32(512) + np.float32(1e-5))
+        assert r[i] == want
