@@ -83,6 +83,9 @@ def parse():
                          "batches reuse p%% of their token/expert assignments")
     ap.add_argument("--ref-budget-s", type=float, default=150.0,
                     help="wall-time budget of the reference arm's timed + warm-up steps")
+    ap.add_argument("--workloads", default="tiny,prefill,large,skewed",
+                    help="comma-separated configurations measured after the headline workload "
+                         "(each one its own sub-record); 'none' skips them")
     return ap.parse_args()
 
 
@@ -168,6 +171,26 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_activity(index: int):
+    """Utilisation, memory in use and compute processes of the GPU (nvidia-smi), to show that
+    nothing else ran on it around the measurement."""
+    out = {}
+    try:
+        q = subprocess.run(["nvidia-smi", f"--id={index}",
+                            "--query-gpu=utilization.gpu,memory.used,clocks.sm",
+                            "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                           timeout=20)
+        u, m, c = [v.strip() for v in q.stdout.strip().split(",")[:3]]
+        out = {"util_pct": float(u), "mem_used_mib": float(m), "sm_mhz": float(c)}
+        q = subprocess.run(["nvidia-smi", f"--id={index}", "--query-compute-apps=pid",
+                            "--format=csv,noheader"], capture_output=True, text=True, timeout=20)
+        pids = [int(v) for v in q.stdout.split() if v.strip().isdigit()]
+        out["other_processes"] = len([p for p in pids if p != os.getpid()])
+    except (OSError, ValueError, subprocess.TimeoutExpired):
+        pass
+    return out
 
 
 # ----------------------------------------------------------------------------------------- helpers
@@ -273,6 +296,199 @@ def oracle_call(cs, x_cpu, lg_np, experts, sho, variant="base"):
                               swiglu_limit=v["swiglu_limit"])
 
 
+# ----------------------------------------------------------------------------------------- configs
+def time_graph(graph, flush, stream, reps):
+    """Device time of each replay of a captured layer call (L2 flushed before each, outside the
+    events), in ms."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    for a, b in ev:
+        flush.zero_()
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def roofline_of(counters, stage_ms, key, hbm_peak, fp4_peak, peak_src):
+    """Roofline entry of one kernel: its algorithmic bytes and FLOPs per launch over its measured
+    duration, against whichever of the two roofs bounds it (the larger time at 100%%)."""
+    sec = stage_ms / 1e3
+    nbytes = counters.get(key, 0)
+    flops = counters.get(key + "_flops", 0)
+    t_hbm = nbytes / (hbm_peak * 1e9)
+    t_fp4 = flops / (fp4_peak * 1e12)
+    r = {"kernel": key, "avg_launch_us": round(sec * 1e6, 2),
+         "algorithmic_bytes_per_launch": nbytes, "algorithmic_flops_per_launch": flops,
+         "hbm_frac": round(nbytes / sec / 1e9 / hbm_peak, 4),
+         "fp4_frac": round(flops / sec / 1e12 / fp4_peak, 4)}
+    if t_fp4 > t_hbm:
+        r.update(bound="tensor", achieved=round(flops / sec / 1e12, 1), peak=round(fp4_peak, 1),
+                 unit="TFLOP/s", frac=r["fp4_frac"],
+                 peak_source=f"{peak_src} bf16 x {FP4_PER_BF16} nominal FP4/BF16 ratio")
+    else:
+        r.update(bound="hbm", achieved=round(nbytes / sec / 1e9, 1), peak=hbm_peak, unit="GB/s",
+                 frac=r["hbm_frac"], peak_source=f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)")
+    return r
+
+
+def oracle_baselines(cs, x_cpu, lg_np, experts, sho, ntok, variant="base"):
+    """The oracle on the first ntok tokens of a call: single-threaded, then on every host core
+    (its OpenMP build).  Returns the two cpu_baseline records."""
+    import oracle
+    out = []
+    for threads in (1, None):
+        used = oracle.use_threads(threads)
+        t0 = time.perf_counter()
+        oracle_call(cs, x_cpu[:ntok], lg_np[:ntok], experts, sho, variant)
+        dt = time.perf_counter() - t0
+        out.append({"value": round(ntok / dt, 4), "unit": UNIT, "cores": used, "kind": "oracle",
+                    "sample": f"the first {ntok} token(s) of the call (router, plan, both GEMMs, "
+                              f"combine; activation quantisation included, weight quantisation "
+                              f"untimed)"})
+    oracle.use_threads(1)
+    return out
+
+
+def measure_config(args, name, dev, hbm_peak, fp4_peak, peak_src, beta=None, cpu_tokens=0):
+    """One layer configuration at its own token count: CUDA-graph replays (L2 flushed before
+    each), per-stage times from a replay that records the stage events, the dominant kernel's
+    roofline and the oracle on a token sample.  beta replaces the Zipf strength of the routing."""
+    import numpy as np
+    import oracle
+    import synth
+    import nvfp4_mixture_experts_softmax_gb300 as moe
+    cs = synth.CONFIGS[name]
+    T = cs.tokens[0]
+    cfg = moe.make_config(cs.experts, cs.hidden, cs.inter, cs.top_k,
+                          shared_inter=cs.shared_inter, max_tokens=T)
+    wg, wu, wd = synth.gen_all_experts(cs, device=dev)
+    sh = synth.gen_shared(cs, device=dev) if cs.has_shared else None
+    wbuf = moe.quantize_weights(cfg, wg, wu, wd, shared=sh)
+    x = synth.gen_x(cs, T, device=dev)
+    lg = synth.gen_logits(cs, T, device=dev, beta=beta)
+    ids = moe.plan(lg, cs.top_k)["topk_ids"].cpu().numpy()
+    loads = np.bincount(ids.reshape(-1), minlength=cs.experts)
+    # the oracle's inputs for the CPU sample: only the experts its tokens use, before the BF16
+    # weights are released
+    cpu = []
+    if cpu_tokens:
+        need = set(ids[:cpu_tokens].reshape(-1).tolist())
+        oracle.use_threads(None)
+        experts, sho = oracle_inputs(cs, wg, wu, wd, sh, need)
+        oracle.use_threads(1)
+        x_cpu, lg_np = x[:cpu_tokens].cpu(), lg[:cpu_tokens].cpu().numpy()
+    del wg, wu, wd, sh
+    torch.cuda.empty_cache()
+    ws = torch.empty(moe.workspace_size(cfg, T), dtype=torch.uint8, device=dev)
+    y = torch.empty(T, cs.hidden, dtype=torch.bfloat16, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(args.warmup, 3)):
+        moe.run(cfg, wbuf, x, lg, y=y, workspace=ws)
+    torch.cuda.synchronize()
+    assert moe.last_device_status(ws) == 0
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        moe.run(cfg, wbuf, x, lg, y=y, workspace=ws)
+    timer = moe.StageTimer()
+    gs = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gs):
+        moe.run(cfg, wbuf, x, lg, y=y, workspace=ws, timer=timer)
+    reps = max(5, min(args.steps, 20))
+    time_graph(g, flush, stream, 3)
+    ms = time_graph(g, flush, stream, reps)
+    stages = []
+    for _ in range(reps):
+        flush.zero_()
+        gs.replay()
+        torch.cuda.synchronize()
+        stages.append(timer.stage_ms())
+    assert moe.last_device_status(ws) == 0
+    stage_ms = {n: statistics.median(s_[n] for s_ in stages) for n in stages[0]}
+    touched = int((loads > 0).sum())
+    fused = moe.run_kernel_count(cfg, T) == 3     # decode path: both GEMMs in one launch
+    counters = layer_counters(cs, T, touched, cs.has_shared, fused)
+    per = statistics.median(ms) / 1e3
+    if fused:
+        stage_ms["grouped_gemms"] = stage_ms.pop("gemm1_swiglu") + stage_ms.pop("gemm2_combine")
+        dom = "grouped_gemms"
+    else:
+        dom = max(("gemm1_swiglu", "gemm2_combine"), key=lambda n: stage_ms[n])
+    rec = {
+        "workload": f"{name}: {cs.description}" + (f" (Zipf beta {beta})" if beta else ""),
+        "tokens": T, "per_call_us": round(per * 1e6, 2),
+        "samples_us": [round(v * 1e3, 2) for v in ms],
+        "tokens_per_s": round(T / per, 1),
+        "eff_tflops": round(counters["flops"] / per / 1e12, 2),
+        "layer_hbm_frac": round(counters["layer_bytes"] / per / 1e9 / hbm_peak, 4),
+        "fp4_peak_frac": round(counters["flops"] / per / 1e12 / fp4_peak, 4),
+        "stage_us": {n: round(v * 1e3, 2) for n, v in stage_ms.items()},
+        "roofline": roofline_of(counters, stage_ms[dom], dom, hbm_peak, fp4_peak, peak_src),
+        "gpu_launches_per_call": moe.run_kernel_count(cfg, T),
+        "touched_experts": touched,
+        "expert_loads": {"min": int(loads.min()), "max": int(loads.max()),
+                         "empty": int((loads == 0).sum())},
+    }
+    rec["roofline"]["traffic"] = measured_traffic(f"{dom}@{name}_T{T}")
+    if cpu_tokens:
+        cpu = oracle_baselines(cs, x_cpu, lg_np, experts, sho, cpu_tokens)
+        rec["cpu_baseline"] = cpu[1]
+        rec["cpu_baseline_1core"] = cpu[0]
+    del wbuf, ws, flush, g, gs
+    torch.cuda.empty_cache()
+    return rec
+
+
+def steady_state_decode(args, dev, hbm_peak):
+    """Decode without an L2 flush, as consecutive layers of a model run: the call cycles through
+    enough distinct weight sets (each its own buffer) that their total is at least 4x the L2, so
+    no call finds its weights cached by the previous one."""
+    import synth
+    import nvfp4_mixture_experts_softmax_gb300 as moe
+    cs = synth.CONFIGS["decode"]
+    Ts = list(cs.tokens)
+    cfg = moe.make_config(cs.experts, cs.hidden, cs.inter, cs.top_k, max_tokens=max(Ts))
+    wg, wu, wd = synth.gen_all_experts(cs, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    w0 = moe.quantize_weights(cfg, wg, wu, wd)
+    del wg, wu, wd
+    nsets = max(2, -(-4 * l2 // w0.numel()))
+    sets = [w0] + [w0.clone() for _ in range(nsets - 1)]
+    ws = torch.empty(moe.workspace_size(cfg, max(Ts)), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    out = {}
+    for i, T in enumerate(Ts):
+        x = synth.gen_x(cs, T, device=dev, row0=1000 * i)
+        lg = synth.gen_logits(cs, T, device=dev, row0=1000 * i)
+        y = torch.empty(T, cs.hidden, dtype=torch.bfloat16, device=dev)
+        graphs = []
+        for w in sets:
+            g = torch.cuda.CUDAGraph()
+            moe.run(cfg, w, x, lg, y=y, workspace=ws)
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g):
+                moe.run(cfg, w, x, lg, y=y, workspace=ws)
+            graphs.append(g)
+        reps = 8 * nsets
+        for j in range(2 * nsets):
+            graphs[j % nsets].replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for j in range(reps):
+            graphs[j % nsets].replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out[str(T)] = round(e0.elapsed_time(e1) * 1e3 / reps, 2)
+        del graphs
+    assert moe.last_device_status(ws) == 0
+    return {"per_T_us": out, "weight_sets": nsets,
+            "weight_set_bytes": int(w0.numel()),
+            "note": "back-to-back calls, no flush; each call reads a different weight set"}
+
+
 # ----------------------------------------------------------------------------------------- ours
 def run_ours(args, world, rank, local):
     import numpy as np
@@ -354,6 +570,7 @@ def run_ours(args, world, rank, local):
     except RuntimeError:
         graphs, staged = {}, {}
 
+    idle_before = gpu_activity(local)
     sampler = ClockSampler(local)
     sampler.start()
     t_settle = time.time()
@@ -480,23 +697,52 @@ def run_ours(args, world, rank, local):
         d2h += T * cs.hidden * 2
     e2e_value, _ = aggregate(e2e_tokens, e2e_s, world)
 
-    # ---- CPU baseline: the oracle, single thread, one pass over the workload's token counts
-    cpu = None
+    idle_after = gpu_activity(local)
+
+    # ---- CPU baseline: the oracle, one pass over the workload's token counts, on one core and
+    # on every host core (its OpenMP build)
+    cpu = cpu1 = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
         need = set()
         for T in Ts:
             need.update(route_ids(T).reshape(-1).tolist())
         experts, sho = oracle_inputs(cs, wg, wu, wd, sh, need)
-        c_tok, c_s = 0, 0.0
-        for T in Ts:
-            xc, lc = xs[T].cpu(), lgs[T].cpu().numpy()
-            t0 = time.perf_counter()
-            oracle_call(cs, xc, lc, experts, sho, args.variant)
-            c_s += time.perf_counter() - t0
-            c_tok += T
-        cpu = {"value": c_tok / c_s, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"one layer call at each T in {Ts} ({c_tok} tokens), single-threaded C++ "
-                         f"oracle incl. activation quantisation; weight quantisation untimed"}
+        recs = []
+        for threads in (1, None):
+            used = oracle.use_threads(threads)
+            c_tok, c_s = 0, 0.0
+            for T in Ts:
+                xc, lc = xs[T].cpu(), lgs[T].cpu().numpy()
+                t0 = time.perf_counter()
+                oracle_call(cs, xc, lc, experts, sho, args.variant)
+                c_s += time.perf_counter() - t0
+                c_tok += T
+            recs.append({"value": c_tok / c_s, "unit": UNIT, "cores": used, "kind": "oracle",
+                         "sample": f"one layer call at each T in {Ts} ({c_tok} tokens), C++ oracle "
+                                   f"on {used} thread(s) incl. activation quantisation; weight "
+                                   f"quantisation untimed"})
+        oracle.use_threads(1)
+        cpu1, cpu = recs
+
+    # ---- every other configuration, each at its own token count (one sub-record each)
+    workloads = {}
+    if world == 1 and args.workloads != "none" and not args.tokens and args.variant == "base" \
+            and not args.routing and args.workload == "decode":
+        del wg, wu, wd
+        torch.cuda.empty_cache()
+        fp4_peak = bf16_peak * FP4_PER_BF16
+        cpu_tok = {"tiny": 16, "prefill": 4, "large": 1, "skewed": 2}
+        for name in [w for w in args.workloads.split(",") if w]:
+            workloads[name] = measure_config(
+                args, name, dev, hbm_peak, fp4_peak, peak_src,
+                cpu_tokens=0 if args.no_cpu_baseline else cpu_tok.get(name, 1))
+            if name == "skewed":
+                # the same layer with a much stronger Zipf bias: a few experts take nearly all
+                # tokens and most get a handful or none
+                workloads["skewed_beta1"] = measure_config(args, name, dev, hbm_peak, fp4_peak,
+                                                           peak_src, beta=1.0)
+        workloads["decode_steady_state"] = steady_state_decode(args, dev, hbm_peak)
 
     clocks = sampler.summary(t_settle, w1 + 0.05)
     if rank != 0:
@@ -531,12 +777,16 @@ def run_ours(args, world, rank, local):
         "roofline": dict(kernel=f"{dominant} (T={Tr} launches)", **roof,
                          avg_launch_us=round(dom_launch_s * 1e6, 2), traffic=traffic),
         "cpu_baseline": cpu,
+        "cpu_baseline_1core": cpu1,
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d // max(len(e_ms), 1),
                 "d2h_bytes_per_step": d2h // max(len(e_ms), 1)},
         "gpu_launches": sum(launches[T] for T in Tseq),
         "clocks": clocks,
+        "gpu_idle": {"before": idle_before, "after": idle_after},
+        "samples_us": [round(v * 1e3, 2) for v in call_ms],
         "wall_s_timed_region": round(w1 - w0, 4),
+        "workloads": workloads,
     }
     print(json.dumps(line), flush=True)
 

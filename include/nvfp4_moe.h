@@ -70,7 +70,8 @@ typedef struct {
   float h_tensor_scale;  /* fixed FP32 tensor scale used to requantise h (1.0 by default) */
   int32_t max_tokens;    /* largest T a workspace sized with moe_workspace_size must serve */
   uint32_t flags;        /* MOE_FLAG_* variant bits below; 0 = the base layer */
-  float swiglu_limit;    /* L of MOE_FLAG_SWIGLU_CLAMP: finite, >= 0 */
+  float swiglu_limit;    /* L of MOE_FLAG_SWIGLU_CLAMP and MOE_FLAG_ACT_SWIGLU_OAI: finite, >= 0 */
+  float swiglu_alpha;    /* slope of MOE_FLAG_ACT_SWIGLU_OAI (1.702 in gpt-oss): finite */
 } moe_config;
 
 /* Router variant ("vllm.cpp docs/STATUS.md", paragraph "W6 sqrtsoftplus + hash-routed MoE";
@@ -84,6 +85,24 @@ typedef struct {
  * Experts)", swiglu_limit = 10): h = silu(min(g, L)) * clamp(u, -L, L); L = 0 zeroes every
  * expert.  Without the flag: h = silu(g) * u. */
 #define MOE_FLAG_SWIGLU_CLAMP 2u
+/* The other two activations of the pages' MoE ("b12x" README, section "What's in here", moe:
+ * "with SiLU/ReLU2/SwiGLU-OAI activations"; SiLU is the base SwiGLU).  The pages give only their
+ * names; the formulas are the published definitions.  At most one activation flag is set.
+ *   MOE_FLAG_ACT_RELU2: non-gated experts, h = max(u, 0)^2 with u the up projection alone.  The
+ *     experts have no gate matrix: moe_quantize_weights ignores w_gate / s_gate (pass NULL), GEMM1
+ *     has I output rows per expert instead of 2I, and moe_weights_export of matrix 0 is an error.
+ *   MOE_FLAG_ACT_SWIGLU_OAI: the gpt-oss SwiGLU, g' = min(g, L), u' = clamp(u, -L, L),
+ *     h = (u' + 1) * g' * sigmoid(alpha * g') with L = swiglu_limit, alpha = swiglu_alpha. */
+#define MOE_FLAG_ACT_RELU2 4u
+#define MOE_FLAG_ACT_SWIGLU_OAI 8u
+/* W4A16 activation precision ("b12x" README, section "What's in here", moe: "W4A16 (BF16
+ * activations, inline FP4 weight dequant - no activation-scale math)"): the BF16 x enters the
+ * gate/up GEMM as it is (no activation quantiser, no tensor scale), the NVFP4 weights are
+ * decoded to BF16 inside the GEMMs (BF16 tensor-core MMAs), and h is rounded to BF16 (nearest
+ * even) before the down projection; routing, plan and combine are those of the base layer.  Any
+ * activation flag may be combined with it.  The weights are the same NVFP4 buffer.  In the
+ * debug struct, hq / hsf are not written and hb receives h. */
+#define MOE_FLAG_ACT_BF16 16u
 
 /* Optional device buffers that receive the layer's intermediates (any field may be NULL). */
 typedef struct {
@@ -102,9 +121,18 @@ typedef struct {
   void** stage_events; /* NULL, or an array of MOE_STAGE_EVENTS cudaEvent_t handles recorded on
                           `stream`: [0] before the layer, then after the activation quantiser,
                           the router + plan, GEMM1, GEMM2 and the BF16 output respectively */
+  uint32_t inject;     /* test hooks for the failure path, MOE_INJECT_* bits; 0 in normal use */
+  void* hb;            /* [T*k + T*shared, I] BF16 h of a MOE_FLAG_ACT_BF16 layer, same row order as
+                          hq */
 } moe_debug;
 
 #define MOE_STAGE_EVENTS 6
+/* Decode-sized batches: the prologue never raises the flag that tells the grouped-GEMM launch
+ * its plan is ready, so that launch's bounded wait (about 2 s) runs out before it issues any
+ * copy; the call then leaves MOE_ERR_DEVICE_TIMEOUT in the device status and unspecified
+ * output, and the next call without the hook runs normally.  It tests the timeout path without
+ * faulting or hanging the GPU; the pages have no counterpart. */
+#define MOE_INJECT_NO_PLAN_FLAG 1u
 
 /* Text for a status code (static storage). */
 const char* moe_status_string(int status);
@@ -124,7 +152,8 @@ int moe_config_check(const moe_config* cfg);
 size_t moe_weights_size(const moe_config* cfg);
 
 /* w_gate, w_up: [E, I, H] BF16; w_down: [E, H, I] BF16; s_gate, s_up: [I, H], s_down: [H, I]
- * (NULL unless cfg->shared_inter > 0).  wbuf: 256-byte aligned device buffer of wbuf_bytes.
+ * (NULL unless cfg->shared_inter > 0; w_gate and s_gate are not read, and may be NULL, with
+ * MOE_FLAG_ACT_RELU2).  wbuf: 256-byte aligned device buffer of wbuf_bytes.
  * Returns MOE_ERR_INVALID_ARG on null pointers, MOE_ERR_WORKSPACE_TOO_SMALL if wbuf_bytes is too
  * small.  Non-finite weights give unspecified codes. */
 int moe_quantize_weights(const moe_config* cfg, const void* w_gate, const void* w_up,
@@ -226,6 +255,20 @@ int moe_run_kernel_count(const moe_config* cfg, int32_t T);
 int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float* logits, int32_t T,
             int32_t k, void* y, void* workspace, size_t ws_bytes, moe_stream_t stream,
             const moe_debug* debug);
+
+/* The layer on activations that are already NVFP4 (the output of moe_quantize_act or of the
+ * fused RMSNorm producer moe_rmsnorm_quantize_act): the router, plan, both grouped GEMMs and the
+ * combine of moe_run, without the BF16 read and the activation quantiser, so the normalised
+ * activations never make a BF16 round trip ("nvfp4-megamoe-kernel compare pre-b1...master",
+ * sections "P4 - Fused RMSNorm + NVFP4 quantize" and "P5": the norm's quantised output feeds the
+ * MoE directly).  xq [T, H/2] E2M1 codes (16-byte aligned), xsf [T, H/16] E4M3 scales (4-byte
+ * aligned) and ts_a (device FP32 scalar, the tensor scale the codes were made with) are read
+ * as they are; everything else as for moe_run, with the same workspace size, launch count and
+ * output.  A negative, NaN or infinite *ts_a sets MOE_ERR_NONFINITE in the device status. */
+int moe_run_quantized(const moe_config* cfg, const void* wbuf, const uint8_t* xq,
+                      const uint8_t* xsf, const float* ts_a, const float* logits, int32_t T,
+                      int32_t k, void* y, void* workspace, size_t ws_bytes, moe_stream_t stream,
+                      const moe_debug* debug);
 
 /* Synchronises `stream`'s device and copies the device status word at the start of a workspace
  * used by moe_quantize_act, moe_plan or moe_run into *host_status (MOE_OK or a device error). */

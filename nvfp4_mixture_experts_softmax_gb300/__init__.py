@@ -24,13 +24,15 @@ EXPORTED = ["moe_status_string", "moe_config_check", "moe_weights_size", "moe_qu
             "moe_weights_export", "moe_act_workspace_size", "moe_quantize_act",
             "moe_plan_workspace_size", "moe_plan", "moe_workspace_size", "moe_run",
             "moe_last_device_status", "moe_plan_static", "moe_run_kernel_count",
-            "moe_set_router_bias", "moe_rmsnorm_workspace_size", "moe_rmsnorm_quantize_act"]
+            "moe_set_router_bias", "moe_rmsnorm_workspace_size", "moe_rmsnorm_quantize_act",
+            "moe_run_quantized"]
 
 
 class MoeConfig(C.Structure):
     _fields_ = [("num_experts", C.c_int32), ("hidden", C.c_int32), ("inter", C.c_int32),
                 ("top_k", C.c_int32), ("shared_inter", C.c_int32), ("h_tensor_scale", C.c_float),
-                ("max_tokens", C.c_int32), ("flags", C.c_uint32), ("swiglu_limit", C.c_float)]
+                ("max_tokens", C.c_int32), ("flags", C.c_uint32), ("swiglu_limit", C.c_float),
+                ("swiglu_alpha", C.c_float)]
 
     def __repr__(self):
         return (f"MoeConfig(E={self.num_experts}, H={self.hidden}, I={self.inter}, k={self.top_k}, "
@@ -47,7 +49,11 @@ N_STAGE_EVENTS = len(STAGES) + 1
 class MoeDebug(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in ("topk_ids", "topk_w", "counts", "offsets", "perm_src",
                                           "inv", "xq", "xsf", "ts_a", "hq", "hsf",
-                                          "stage_events")]
+                                          "stage_events")] + [("inject", C.c_uint32),
+                                                              ("hb", C.c_void_p)]
+
+
+MOE_INJECT_NO_PLAN_FLAG = 1
 
 
 def lib():
@@ -72,6 +78,8 @@ def lib():
             "moe_plan": (C.c_int, [vp, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
             "moe_workspace_size": (sz, [cfgp, i32]),
             "moe_run": (C.c_int, [cfgp, vp, vp, vp, i32, i32, vp, vp, sz, vp, C.POINTER(MoeDebug)]),
+            "moe_run_quantized": (C.c_int, [cfgp, vp, vp, vp, vp, vp, i32, i32, vp, vp, sz, vp,
+                                            C.POINTER(MoeDebug)]),
             "moe_last_device_status": (C.c_int, [vp, C.POINTER(C.c_int32)]),
             "moe_plan_static": (C.c_int, [vp, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]),
             "moe_run_kernel_count": (C.c_int, [cfgp, i32]),
@@ -108,20 +116,42 @@ def _stream(stream=None):
 
 FLAG_ROUTER_SQRTSOFTPLUS = 1
 FLAG_SWIGLU_CLAMP = 2
+FLAG_ACT_RELU2 = 4
+FLAG_ACT_SWIGLU_OAI = 8
+FLAG_ACT_BF16 = 16
+ACTIVATIONS = ("swiglu", "relu2", "swiglu_oai")
 
 
 def make_config(num_experts, hidden, inter, top_k, shared_inter=0, h_tensor_scale=1.0,
-                max_tokens=0, router="softmax", swiglu_limit=None) -> MoeConfig:
+                max_tokens=0, router="softmax", swiglu_limit=None, activation="swiglu",
+                swiglu_alpha=1.702, precision="nvfp4") -> MoeConfig:
     """router: "softmax" (top-k of the logits, softmax over the k) or "sqrtsoftplus" (scores
     sqrt(softplus(logit)), selection on score + the bias set by set_router_bias, weights the
-    normalised unbiased scores); swiglu_limit: None for silu(g)*u, else L of
-    silu(min(g, L)) * clamp(u, -L, L)."""
+    normalised unbiased scores).  activation: "swiglu" (silu(g)*u, or with swiglu_limit L
+    silu(min(g, L)) * clamp(u, -L, L)), "relu2" (non-gated experts, max(u, 0)^2) or "swiglu_oai"
+    ((clamp(u, -L, L) + 1) * g' * sigmoid(alpha * g'), g' = min(g, L); needs swiglu_limit).
+    precision: "nvfp4" (activations and h quantised to NVFP4) or "w4a16" (BF16 activations as
+    they are, weights decoded to BF16 in the GEMMs, h rounded to BF16)."""
     if router not in ("softmax", "sqrtsoftplus"):
         raise ValueError(f"unknown router {router!r}")
-    flags = (FLAG_ROUTER_SQRTSOFTPLUS if router == "sqrtsoftplus" else 0) | \
-        (FLAG_SWIGLU_CLAMP if swiglu_limit is not None else 0)
+    if activation not in ACTIVATIONS:
+        raise ValueError(f"unknown activation {activation!r}")
+    if activation == "swiglu_oai" and swiglu_limit is None:
+        raise ValueError("swiglu_oai needs swiglu_limit")
+    flags = FLAG_ROUTER_SQRTSOFTPLUS if router == "sqrtsoftplus" else 0
+    if activation == "relu2":
+        flags |= FLAG_ACT_RELU2
+    elif activation == "swiglu_oai":
+        flags |= FLAG_ACT_SWIGLU_OAI
+    elif swiglu_limit is not None:
+        flags |= FLAG_SWIGLU_CLAMP
+    if precision == "w4a16":
+        flags |= FLAG_ACT_BF16
+    elif precision != "nvfp4":
+        raise ValueError(f"unknown precision {precision!r}")
     return MoeConfig(num_experts, hidden, inter, top_k, shared_inter, h_tensor_scale, max_tokens,
-                     flags, 0.0 if swiglu_limit is None else float(swiglu_limit))
+                     flags, 0.0 if swiglu_limit is None else float(swiglu_limit),
+                     float(swiglu_alpha))
 
 
 def config_check(cfg: MoeConfig) -> int:
@@ -133,12 +163,13 @@ def weights_size(cfg: MoeConfig) -> int:
 
 
 def quantize_weights(cfg: MoeConfig, w_gate, w_up, w_down, shared=None, wbuf=None, stream=None):
-    """BF16 expert weights -> packed NVFP4 weight buffer (a uint8 CUDA tensor)."""
+    """BF16 expert weights -> packed NVFP4 weight buffer (a uint8 CUDA tensor).  w_gate (and the
+    shared expert's gate) may be None for non-gated (relu2) layers; they are not read there."""
     n = weights_size(cfg)
     if n == 0:
         _check(config_check(cfg), "moe_weights_size")
     if wbuf is None:
-        wbuf = torch.empty(n, dtype=torch.uint8, device=w_gate.device)
+        wbuf = torch.empty(n, dtype=torch.uint8, device=w_up.device)
     sg, su, sd = shared if shared is not None else (None, None, None)
     _check(lib().moe_quantize_weights(C.byref(cfg), _ptr(w_gate), _ptr(w_up), _ptr(w_down),
                                       _ptr(sg), _ptr(su), _ptr(sd), _ptr(wbuf), wbuf.numel(),
@@ -273,11 +304,18 @@ class StageTimer:
 
 
 def run(cfg: MoeConfig, wbuf, x, logits, k=None, y=None, workspace=None, debug=False, stream=None,
-        timer: StageTimer = None):
-    """The layer: y [T, H] BF16 (and, with debug=True, a dict of its intermediates)."""
-    T, H = x.shape
+        timer: StageTimer = None, quantized=None, inject: int = 0):
+    """The layer: y [T, H] BF16 (and, with debug=True, a dict of its intermediates).  x is the BF16
+    input [T, H]; or pass x=None and quantized=(xq [T, H/2] u8, xsf [T, H/16] u8, ts_a [1] f32),
+    already-NVFP4 activations (moe_run_quantized)."""
+    if quantized is not None:
+        xq, xsf, ts_a = quantized
+        T, H = xq.shape[0], xq.shape[1] * 2
+        dev = xq.device
+    else:
+        T, H = x.shape
+        dev = x.device
     k = cfg.top_k if k is None else k
-    dev = x.device
     if y is None:
         y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
     if workspace is None:
@@ -298,13 +336,29 @@ def run(cfg: MoeConfig, wbuf, x, logits, k=None, y=None, workspace=None, debug=F
                    ts_a=torch.empty(1, dtype=torch.float32, device=dev),
                    hq=torch.empty(Rt, I // 2, dtype=torch.uint8, device=dev),
                    hsf=torch.empty(Rt, I // 16, dtype=torch.uint8, device=dev))
-        dbg_c = MoeDebug(*[dbg[n].data_ptr() for n, _ in MoeDebug._fields_[:11]],
+        if cfg.flags & FLAG_ACT_BF16:        # nothing is quantised; h stays BF16 (hb)
+            for n in ("hq", "hsf", "xq", "xsf", "ts_a"):
+                del dbg[n]
+            dbg["hb"] = torch.empty(Rt, I, dtype=torch.bfloat16, device=dev)
+        dbg_c = MoeDebug(*[dbg[n].data_ptr() if n in dbg else None
+                           for n, _ in MoeDebug._fields_[:11]],
                          C.cast(timer._handles, C.c_void_p) if timer is not None else None)
+        if "hb" in dbg:
+            dbg_c.hb = dbg["hb"].data_ptr()
     elif timer is not None:
         dbg_c = timer.c_debug
-    _check(lib().moe_run(C.byref(cfg), _ptr(wbuf), _ptr(x), _ptr(logits), T, k, _ptr(y),
-                         _ptr(workspace), workspace.numel(), _stream(stream),
-                         C.byref(dbg_c) if dbg_c is not None else None), "moe_run")
+    if inject:
+        dbg_c = MoeDebug.from_buffer_copy(dbg_c) if dbg_c is not None else MoeDebug()
+        dbg_c.inject = inject
+    dptr = C.byref(dbg_c) if dbg_c is not None else None
+    if quantized is not None:
+        _check(lib().moe_run_quantized(C.byref(cfg), _ptr(wbuf), _ptr(xq), _ptr(xsf), _ptr(ts_a),
+                                       _ptr(logits), T, k, _ptr(y), _ptr(workspace),
+                                       workspace.numel(), _stream(stream), dptr),
+               "moe_run_quantized")
+    else:
+        _check(lib().moe_run(C.byref(cfg), _ptr(wbuf), _ptr(x), _ptr(logits), T, k, _ptr(y),
+                             _ptr(workspace), workspace.numel(), _stream(stream), dptr), "moe_run")
     return (y, dbg) if debug else y
 
 

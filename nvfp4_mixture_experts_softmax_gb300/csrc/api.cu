@@ -1,7 +1,9 @@
 // C ABI of the NVFP4 MoE library: argument checks, workspace carving and the launch sequence.
 // Nothing here allocates device memory or reads device values back to the host (the single
 // exception is moe_last_device_status, which exists to do exactly that).
+#include <algorithm>
 #include <cmath>
+#include <tuple>
 
 #include "internal.h"
 
@@ -15,10 +17,15 @@ inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 
 int check_cfg(const moe_config* c) {
   if (!c) return MOE_ERR_INVALID_ARG;
-  if ((c->flags & ~(MOE_FLAG_ROUTER_SQRTSOFTPLUS | MOE_FLAG_SWIGLU_CLAMP)) != 0u)
+  const uint32_t acts = MOE_FLAG_SWIGLU_CLAMP | MOE_FLAG_ACT_RELU2 | MOE_FLAG_ACT_SWIGLU_OAI;
+  if ((c->flags & ~(MOE_FLAG_ROUTER_SQRTSOFTPLUS | acts | MOE_FLAG_ACT_BF16)) != 0u)
     return MOE_ERR_INVALID_ARG;
-  if ((c->flags & MOE_FLAG_SWIGLU_CLAMP) && !(std::isfinite(c->swiglu_limit) && c->swiglu_limit >= 0.0f))
+  const uint32_t act = c->flags & acts;
+  if (act & (act - 1u)) return MOE_ERR_INVALID_ARG;   // at most one activation
+  if ((act & (MOE_FLAG_SWIGLU_CLAMP | MOE_FLAG_ACT_SWIGLU_OAI)) &&
+      !(std::isfinite(c->swiglu_limit) && c->swiglu_limit >= 0.0f))
     return MOE_ERR_INVALID_ARG;
+  if ((act & MOE_FLAG_ACT_SWIGLU_OAI) && !std::isfinite(c->swiglu_alpha)) return MOE_ERR_INVALID_ARG;
   if (c->num_experts < 1 || c->top_k < 1 || c->hidden <= 0 || c->inter <= 0 || c->max_tokens < 0)
     return MOE_ERR_INVALID_ARG;
   if (c->top_k > c->num_experts) return MOE_ERR_INVALID_ARG;
@@ -62,13 +69,18 @@ int moe_quantize_weights(const moe_config* cfg, const void* w_gate, const void* 
                          const void* s_down, void* wbuf, size_t wbuf_bytes, moe_stream_t stream) {
   int st = check_cfg(cfg);
   if (st != MOE_OK) return st;
-  if (!w_gate || !w_up || !w_down || !wbuf) return MOE_ERR_INVALID_ARG;
-  if (cfg->shared_inter > 0 && (!s_gate || !s_up || !s_down)) return MOE_ERR_INVALID_ARG;
+  const bool gated = gated_experts(*cfg);
+  if (!gated) {   // non-gated experts: the gate matrices are not read
+    w_gate = nullptr;
+    s_gate = nullptr;
+  }
+  if ((gated && !w_gate) || !w_up || !w_down || !wbuf) return MOE_ERR_INVALID_ARG;
+  if (cfg->shared_inter > 0 && ((gated && !s_gate) || !s_up || !s_down)) return MOE_ERR_INVALID_ARG;
   for (const void* p : {w_gate, w_up, w_down})
-    if (!aligned(p, 16)) return MOE_ERR_INVALID_ARG;
+    if (p && !aligned(p, 16)) return MOE_ERR_INVALID_ARG;
   if (cfg->shared_inter > 0)
     for (const void* p : {s_gate, s_up, s_down})
-      if (!aligned(p, 16)) return MOE_ERR_INVALID_ARG;
+      if (p && !aligned(p, 16)) return MOE_ERR_INVALID_ARG;
   if (!aligned(wbuf, kAlign)) return MOE_ERR_INVALID_ARG;
   const WeightLayout L(*cfg);
   if (wbuf_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
@@ -94,6 +106,7 @@ int moe_weights_export(const moe_config* cfg, const void* wbuf, int32_t expert, 
   if (st != MOE_OK) return st;
   if (!wbuf || !codes || !sf || !ts) return MOE_ERR_INVALID_ARG;
   if (matrix < 0 || matrix > 2) return MOE_ERR_INVALID_ARG;
+  if (matrix == 0 && !gated_experts(*cfg)) return MOE_ERR_INVALID_ARG;   // no gate matrix
   int slot;
   if (expert == -1) {
     if (cfg->shared_inter <= 0) return MOE_ERR_INVALID_ARG;
@@ -217,13 +230,21 @@ int moe_run_kernel_count(const moe_config* cfg, int32_t T) {
   const RunLayout L(*cfg, T);
   if (L.decode) return 3;     // cluster prologue, both grouped GEMMs, row sum
   if (L.small) return 5;      // one-block prologue, permute, GEMM1, GEMM2, row sum
-  // amax, router/plan (1 or 3), encode into expert order, GEMM1, GEMM2, BF16 conversion
+  // accumulator zeroing (+ amax), router/plan (1 or 3), encode (or, W4A16, the BF16 rows) into
+  // expert order, GEMM1, GEMM2, BF16 conversion
   return 1 + ((int64_t)T * cfg->top_k <= kSmallPlanRows ? 1 : 3) + 4;
 }
 
-int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float* logits, int32_t T,
-            int32_t k, void* y, void* workspace, size_t ws_bytes, moe_stream_t stream,
-            const moe_debug* debug) {
+}  // extern "C"
+
+namespace {
+
+// The layer for BF16 input x (qx == nullptr) or for already quantised input (qx: codes
+// [T, H/2], qsf: scales [T, H/16], qts: device tensor scale; x unused).
+int run_layer(const moe_config* cfg, const void* wbuf, const void* x, const uint8_t* qx,
+              const uint8_t* qsf, const float* qts, const float* logits, int32_t T, int32_t k,
+              void* y, void* workspace, size_t ws_bytes, moe_stream_t stream,
+              const moe_debug* debug) {
   int st = check_cfg(cfg);
   if (st != MOE_OK) return st;
   if (T < 0 || k != cfg->top_k) return MOE_ERR_INVALID_ARG;
@@ -234,8 +255,16 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   if (!aligned(workspace, kAlign)) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
-  if (!wbuf || !x || !logits || !y) return MOE_ERR_INVALID_ARG;
-  if (!aligned(wbuf, kAlign) || !aligned(x, 16) || !aligned(y, 8)) return MOE_ERR_INVALID_ARG;
+  const bool quantised = qx != nullptr || qsf != nullptr || qts != nullptr;
+  if (quantised && L.w16) return MOE_ERR_INVALID_ARG;   // a W4A16 layer takes BF16 input
+  if (!wbuf || !logits || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned(wbuf, kAlign) || !aligned(y, 8)) return MOE_ERR_INVALID_ARG;
+  if (quantised) {
+    if (!qx || !qsf || !qts) return MOE_ERR_INVALID_ARG;
+    if (!aligned(qx, 16) || !aligned(qsf, 4) || !aligned(qts, 4)) return MOE_ERR_INVALID_ARG;
+  } else if (!x || !aligned(x, 16)) {
+    return MOE_ERR_INVALID_ARG;
+  }
 
   cudaStream_t s = to_cuda(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -264,6 +293,97 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
 
   cudaError_t e = mark(0);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  if (L.w16) {
+    // W4A16: accumulator zeroing, router + plan, BF16 rows into expert order, both GEMMs on the
+    // BF16 tensor cores (weights decoded in shared memory), BF16 output
+    if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s) != cudaSuccess) return MOE_ERR_CUDA;
+    e = launch_act_amax(x, 0, H, nullptr, hdr, reinterpret_cast<uint32_t*>(ws + L.amax_part),
+                        f32(L.yacc), (int64_t)T * H, s, nullptr);
+    if (e == cudaSuccess) e = mark(1);
+    PlanArgs pa{};
+    pa.logits = logits;
+    pa.T = T;
+    pa.E = E;
+    pa.k = k;
+    pa.shared_rows = shared ? T : 0;
+    pa.ids = i32(L.ids);
+    pa.w = f32(L.w);
+    pa.counts = debug ? debug->counts : nullptr;
+    pa.offsets = i32(L.seg_off);
+    pa.tile_start = i32(L.tile_start);
+    pa.perm_src = i32(L.perm_src);
+    pa.perm_w = f32(L.perm_w);
+    pa.inv = i32(L.inv);
+    pa.perm_seg = i32(L.perm_seg);
+    pa.hist = i32(L.hist);
+    pa.base = i32(L.base);
+    pa.status = &hdr->status;
+    pa.sqrtsp = sqrtsp;
+    pa.bias = rbias;
+    if (e == cudaSuccess) e = launch_plan(pa, s);
+    if (e == cudaSuccess) e = mark(2);
+    if (e == cudaSuccess)
+      e = launch_permute_rows_bf16(x, T, H, L.Rt, i32(L.perm_src), ws + L.xb_perm, &hdr->status, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    const int nseg = E + shared;
+    const int64_t mtiles = ((int64_t)L.Rt + (int64_t)nseg * (kBM - 1)) / kBM;
+    GemmW16Args g{};
+    g.a_rows = ws + L.xb_perm;
+    g.b_tiles = wb + W.w13;
+    g.b_per_seg = W.w13_per_e;
+    g.w_ts = reinterpret_cast<const float*>(wb + W.ts);
+    g.seg_off = i32(L.seg_off);
+    g.tile_start = i32(L.tile_start);
+    g.nseg = nseg;
+    g.N = gemm1_rows(*cfg);
+    g.K = H;
+    g.mode = 0;
+    g.act = (cfg->flags & MOE_FLAG_SWIGLU_CLAMP) ? kActSwigluClamp
+            : (cfg->flags & MOE_FLAG_ACT_RELU2)   ? kActRelu2
+            : (cfg->flags & MOE_FLAG_ACT_SWIGLU_OAI) ? kActSwigluOai
+                                                    : kActSwiglu;
+    g.swiglu_limit = cfg->swiglu_limit;
+    g.swiglu_alpha = cfg->swiglu_alpha;
+    g.hb = ws + L.hb;
+    g.out_rows = L.Rt;
+    g.y_rows = T;
+    g.max_items = (int)std::min<int64_t>(mtiles * (g.N / kBN), INT32_MAX);
+    g.status = &hdr->status;
+    e = launch_grouped_gemm_w16(g, s);
+    if (e == cudaSuccess) e = mark(3);
+    GemmW16Args g2 = g;
+    g2.a_rows = ws + L.hb;
+    g2.b_tiles = wb + W.w2;
+    g2.b_per_seg = W.w2_per_e;
+    g2.N = H;
+    g2.K = I;
+    g2.mode = 1;
+    g2.perm_src = i32(L.perm_src);
+    g2.perm_w = f32(L.perm_w);
+    g2.yacc = f32(L.yacc);
+    g2.max_items = (int)std::min<int64_t>(mtiles * (g2.N / kBN), INT32_MAX);
+    if (e == cudaSuccess) e = launch_grouped_gemm_w16(g2, s);
+    if (e == cudaSuccess) e = mark(4);
+    if (e == cudaSuccess) e = launch_finalize(f32(L.yacc), y, (int64_t)T * H, s);
+    if (e == cudaSuccess) e = mark(5);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (debug) {
+      auto cp = [&](void* dst, size_t off, size_t bytes) {
+        if (dst && e == cudaSuccess)
+          e = cudaMemcpyAsync(dst, ws + off, bytes, cudaMemcpyDeviceToDevice, s);
+      };
+      const size_t R = (size_t)L.R, Rt = (size_t)L.Rt;
+      cp(debug->topk_ids, L.ids, 4 * R);
+      cp(debug->topk_w, L.w, 4 * R);
+      cp(debug->offsets, L.seg_off, 4 * (size_t)(E + 1));
+      cp(debug->perm_src, L.perm_src, 4 * R);
+      cp(debug->inv, L.inv, 4 * R);
+      cp(debug->hb, L.hb, Rt * I * 2);
+      if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+  }
 
   if (L.decode) {
     // 1+2. a cluster: status reset, router and plan, activation quantiser in expert order
@@ -295,6 +415,10 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
     pr.ready = i32(L.ready);
     pr.nready = L.dtiles;
     pr.plan_flag = i32(L.ready) + L.dtiles;
+    pr.in_xq = qx;
+    pr.in_xsf = qsf;
+    pr.in_ts = qts;
+    pr.no_plan_flag = (debug && (debug->inject & MOE_INJECT_NO_PLAN_FLAG)) ? 1 : 0;
     e = launch_decode_prologue(pr, s);
     if (e == cudaSuccess) e = mark(1);
     if (e == cudaSuccess) e = mark(2);
@@ -324,6 +448,7 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
     pr.perm_seg = i32(L.perm_seg);
     pr.sqrtsp = sqrtsp;
     pr.bias = rbias;
+    pr.in_ts = qts;
     e = launch_prologue_small(pr, s);
     if (e == cudaSuccess) e = mark(1);
     if (e == cudaSuccess) e = mark(2);
@@ -335,7 +460,7 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
   // 1. activation tensor scale (and zero the FP32 output accumulator on the way); the encode
   //    follows the plan so that it can write every expert row directly
   e = launch_act_amax(x, T, H, nullptr, hdr, reinterpret_cast<uint32_t*>(ws + L.amax_part),
-                      f32(L.yacc), (int64_t)T * H, s);
+                      f32(L.yacc), (int64_t)T * H, s, qts);
   if (e == cudaSuccess) e = mark(1);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
@@ -367,9 +492,13 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
 
   const int nseg = E + shared;
   const int64_t max_mtiles = ((int64_t)L.Rt + (int64_t)nseg * (kBM - 1)) / kBM;
-  if (L.small && !L.decode) {
-    // activations (encoded in token order by the one-block prologue) into expert order
-    e = launch_permute_rows(ws + L.xq, ws + L.xsf, T, H, L.Rt, E, i32(L.perm_src),
+  // token-order codes and scales of the activations: the caller's (quantised input) or the
+  // workspace copy the quantiser wrote
+  const uint8_t* xq_tok = quantised ? qx : ws + L.xq;
+  const uint8_t* xsf_tok = quantised ? qsf : ws + L.xsf;
+  if ((L.small && !L.decode) || (quantised && !L.small)) {
+    // activations (token order) into expert order
+    e = launch_permute_rows(xq_tok, xsf_tok, T, H, L.Rt, E, i32(L.perm_src),
                             i32(L.perm_seg), i32(L.seg_off), i32(L.tile_start), ws + L.xq_perm,
                             ws + L.xsf_tiles, &hdr->status, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
@@ -393,7 +522,7 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
   g.seg_off = i32(L.seg_off);
   g.tile_start = i32(L.tile_start);
   g.nseg = nseg;
-  g.N = 2 * I;
+  g.N = gemm1_rows(*cfg);
   g.K = H;
   g.mode = 0;
   g.ts_a = &hdr->ts;
@@ -401,8 +530,12 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
   g.hq = ws + L.hq;
   g.hsf = ws + L.hsf;
   g.status = &hdr->status;
-  g.swiglu_clamp = (cfg->flags & MOE_FLAG_SWIGLU_CLAMP) ? 1 : 0;
+  g.act = (cfg->flags & MOE_FLAG_SWIGLU_CLAMP) ? kActSwigluClamp
+          : (cfg->flags & MOE_FLAG_ACT_RELU2)   ? kActRelu2
+          : (cfg->flags & MOE_FLAG_ACT_SWIGLU_OAI) ? kActSwigluOai
+                                                  : kActSwiglu;
   g.swiglu_limit = cfg->swiglu_limit;
+  g.swiglu_alpha = cfg->swiglu_alpha;
   // decode-sized batches: tiles of kDecodeTileRows rows of one expert each
   const bool decode = L.decode;
   g.a_codes = ws + L.xq_perm;            // expert-ordered activations, read by TMA boxes
@@ -469,14 +602,41 @@ int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float*
     cp(debug->offsets, L.seg_off, 4 * (size_t)(E + 1));
     cp(debug->perm_src, L.perm_src, 4 * R);
     cp(debug->inv, L.inv, 4 * R);
-    cp(debug->xq, L.xq, (size_t)T * H / 2);
-    cp(debug->xsf, L.xsf, (size_t)T * H / 16);
+    if (quantised) {
+      for (auto [dst, src, bytes] : {std::tuple<void*, const void*, size_t>{debug->xq, qx, (size_t)T * H / 2},
+                                     {debug->xsf, qsf, (size_t)T * H / 16}})
+        if (dst && e == cudaSuccess)
+          e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s);
+    } else {
+      cp(debug->xq, L.xq, (size_t)T * H / 2);
+      cp(debug->xsf, L.xsf, (size_t)T * H / 16);
+    }
     cp(debug->ts_a, L.hdr + offsetof(WsHeader, ts), 4);
     cp(debug->hq, L.hq, Rt * I / 2);
     cp(debug->hsf, L.hsf, Rt * I / 16);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_run(const moe_config* cfg, const void* wbuf, const void* x, const float* logits, int32_t T,
+            int32_t k, void* y, void* workspace, size_t ws_bytes, moe_stream_t stream,
+            const moe_debug* debug) {
+  return run_layer(cfg, wbuf, x, nullptr, nullptr, nullptr, logits, T, k, y, workspace, ws_bytes,
+                   stream, debug);
+}
+
+int moe_run_quantized(const moe_config* cfg, const void* wbuf, const uint8_t* xq,
+                      const uint8_t* xsf, const float* ts_a, const float* logits, int32_t T,
+                      int32_t k, void* y, void* workspace, size_t ws_bytes, moe_stream_t stream,
+                      const moe_debug* debug) {
+  if (T > 0 && (!xq || !xsf || !ts_a)) return MOE_ERR_INVALID_ARG;
+  return run_layer(cfg, wbuf, nullptr, xq, xsf, ts_a, logits, T, k, y, workspace, ws_bytes,
+                   stream, debug);
 }
 
 int moe_last_device_status(const void* workspace, int32_t* host_status) {

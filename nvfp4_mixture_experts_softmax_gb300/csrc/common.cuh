@@ -136,6 +136,21 @@ __device__ __forceinline__ void quant_block16_fast(const float* x, float ts, flo
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
 
+// GEMM1's activation of one feature from its FP32 gate and up values (kAct* of internal.h; g is
+// unused by the non-gated ReLU2).  Fast exponential and division: h is requantised right after
+// and compared within one code step.  For a very negative argument the denominator overflows to
+// infinity and the sigmoid term is a signed zero.
+__device__ __forceinline__ float glu_activation(float g, float u, int act, float L, float alpha) {
+  if (act == 2) return u > 0.0f ? u * u : 0.0f;   // kActRelu2
+  if (act == 1 || act == 3) {                     // clamped: gate from above, up on both sides
+    g = fminf(g, L);
+    u = fminf(fmaxf(u, -L), L);
+  }
+  if (act == 3)                                   // kActSwigluOai
+    return (u + 1.0f) * __fdividef(g, 1.0f + __expf(-(alpha * g)));
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
+
 // NVFP4 quantisation of one BF16 block held in registers (v0: elements 0-7, v1: elements 8-15).
 __device__ __forceinline__ void quant_bf16_regs16(uint4 v0, uint4 v1, float ts, uint32_t& lo,
                                                   uint32_t& hi, uint32_t& sf) {

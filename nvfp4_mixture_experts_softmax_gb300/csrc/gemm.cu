@@ -1,8 +1,9 @@
 // Persistent grouped GEMM on the 5th-generation tensor cores with block-scaled FP4 operands
 // (tcgen05.mma kind::mxf4nvf4, E2M1 values, one E4M3 scale per 16 elements), used twice per layer
 // for batches larger than the decode path's:
-//   GEMM1: the expert-ordered quantised activations x the expert's interleaved gate/up weights;
-//          the epilogue applies the tensor scales, SwiGLU silu(g)*u, and requantises h to NVFP4
+//   GEMM1: the expert-ordered quantised activations x the expert's interleaved gate/up weights
+//          (or up weights alone for non-gated experts); the epilogue applies the tensor scales,
+//          the activation (SwiGLU silu(g)*u, clamped, gpt-oss, or ReLU2), and requantises h to NVFP4
 //          ("nvfp4-megamoe-kernel compare pre-b1...master", section "MoE kernel
 //          (FusedSwiGLUScaledGroupedGemmKernel)": epilogue with global scale + SwiGLU in
 //          registers between the tensor-memory load and the store);
@@ -72,6 +73,9 @@ struct GemmShape {
   static constexpr int kBarOff = kStgOff + (kRedStage ? kStgBytes : 0);
   static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "tensor memory budget");
   static_assert(kBarOff + 1024 + 256 + 8 * 1027 <= 232448, "shared memory");
+  // full, empty, sf_done per stage; two acc_full, two acc_empty, drain, sf_drain; TMEM slot and
+  // the issue count, all before the plan arrays at kBarOff + 256
+  static_assert((3 * kStages + 6) * 8 + 2 * 4 <= 256, "mbarriers + TMEM slot + issue count");
 };
 
 // Instruction descriptor of tcgen05.mma kind::mxf4nvf4: A and B E2M1 (format 1) at bits 7-9 and
@@ -102,12 +106,6 @@ __device__ __forceinline__ TileInfo decode_tile(int item, int n_tiles, const int
   return t;
 }
 
-// silu(g) * u with the fast exponential and division (h is requantised to NVFP4 right after;
-// for g < -88 the denominator overflows to inf and the quotient is a signed zero).
-__device__ __forceinline__ float silu_mul(float g, float u) {
-  return __fdividef(g, 1.0f + __expf(-g)) * u;
-}
-
 template <bool kRedStage>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmArgs p) {
@@ -122,7 +120,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
   uint64_t* sf_done = drain + 1;   // a stage's scale factors are in tensor memory
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_done + kStages);
+  uint64_t* sf_drain = sf_done + kStages;   // the scale-factor warp's last tensor-memory copies
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_drain + 1);
+  uint32_t* s_issued = tmem_slot + 1;       // stage fills the copy thread issued
   int32_t* s_tile = reinterpret_cast<int32_t*>(smem + GemmShape<kRedStage>::kBarOff + 256);
   int32_t* s_seg = s_tile + (p.nseg + 1);
 
@@ -142,6 +142,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(smem_u32(drain), 1);
     for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(sf_done + s), 1);
+    mbar_init(smem_u32(sf_drain), 1);
+    *s_issued = 0u;
     fence_barrier_init();
   }
   if (warp == kTmaWarp && lane == 0)
@@ -171,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- all operands: TMA box of A rows + bulk copies ----------------
     if (lane == 0) {
       int stage = 0;
-      uint32_t phase = 0;
+      uint32_t phase = 0, n_issued = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
         const TileInfo t = decode_tile(item, n_tiles, s_tile, s_seg, p.nseg);
@@ -190,6 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(sb, &tmap_a, ks * 128, t.m0, fb);
           bulk_load(sb + kABytes, asf + (size_t)ks * kSfBytes, kSfBytes, fb);
           bulk_load(sb + kBOff, bsrc + (size_t)ks * kTileBlockBytes, kTileBlockBytes, fb);
+          ++n_issued;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
@@ -198,6 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait_bounded(smem_u32(empty + stage), phase ^ 1u, kWaitLimitNs, p.status)) break;
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
+      *s_issued = n_issued;
     }
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issue (one thread) ----------------
@@ -271,6 +275,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
+      // tensor memory is released only once this thread's last scale copies have completed
+      tc_commit(smem_u32(sf_drain));
+      mbar_wait_bounded(smem_u32(sf_drain), 0u, kWaitLimitNs, p.status);
     }
   } else {
     // ---------------- epilogue (warps 0-3) ----------------
@@ -282,7 +289,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int item = blockIdx.x; item < total; item += gridDim.x, ++it) {
       const TileInfo t = decode_tile(item, n_tiles, s_tile, s_seg, p.nseg);
       const int abuf = it & 1;
-      if (!mbar_wait_bounded(smem_u32(acc_full + abuf), acc_phase[abuf], kWaitLimitNs, p.status))
+      // every lane waits; the decision is taken together so that the warp never diverges
+      // before the warp-wide tensor-memory loads
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(acc_full + abuf), acc_phase[abuf],
+                                                     kWaitLimitNs, p.status)))
         break;
       acc_phase[abuf] ^= 1u;
       tc_fence_after();
@@ -292,7 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p.mode == 0) {
         const float ag = ts_a * p.w_ts[t.seg * 4 + 0];
         const float au = ts_a * p.w_ts[t.seg * 4 + 1];
-        const int I = p.N / 2;
+        const bool gated = p.act != kActRelu2;
+        const int I = gated ? p.N / 2 : p.N;
         const size_t mt = (size_t)(item / n_tiles);
         const int rr = r & 127;
         uint8_t* hsf_tile = p.hsf_tiles + mt * (I / 64) * 512 + (rr & 31) * 16 + (rr >> 5) * 4;
@@ -301,20 +312,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t v[32];
           tmem_ld_32x32b_x32(tbase + c * 32, v);
           tmem_ld_wait();
-          if (valid) {
+          if (!valid) continue;
+          // a 32-column chunk is one 16-feature block of h from (16 gate | 16 up) columns, or,
+          // without a gate, two blocks from 32 up columns (indices stay compile-time constants so
+          // that v stays in registers)
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            if (gated && half == 1) break;
             float h[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              float g = __uint_as_float(v[i]) * ag, u = __uint_as_float(v[16 + i]) * au;
-              if (p.swiglu_clamp) {   // gate clamped from above, up on both sides
-                g = fminf(g, p.swiglu_limit);
-                u = fminf(fmaxf(u, -p.swiglu_limit), p.swiglu_limit);
-              }
-              h[i] = silu_mul(g, u);
+              const float g = gated ? __uint_as_float(v[i]) * ag : 0.0f;
+              const float u = __uint_as_float(gated ? v[16 + i] : v[16 * half + i]) * au;
+              h[i] = glu_activation(g, u, p.act, p.swiglu_limit, p.swiglu_alpha);
             }
             uint32_t lo, hi, s;
             quant_block16_fast(h, p.ts_h, inv_ts_h, lo, hi, s);
-            const int f0 = t.nt * (kBN / 2) + c * 16;
+            const int f0 = gated ? t.nt * (kBN / 2) + c * 16 : t.nt * kBN + c * 32 + half * 16;
             *reinterpret_cast<uint2*>(p.hq + (size_t)prow * (I / 2) + f0 / 2) = make_uint2(lo, hi);
             p.hsf[(size_t)prow * (I / 16) + f0 / 16] = (uint8_t)s;
             hsf_tile[(size_t)(f0 / 64) * 512 + ((f0 / 16) & 3)] = (uint8_t)s;
@@ -391,6 +405,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  // Teardown.  After a wait ran out, stage fills may still be in flight: the copy thread's last
+  // kStages fills are waited for (bounded) before the CTA exits.  Without a timeout every fill
+  // was consumed and these waits return at once.
+  __syncthreads();
+  if (warp == kTmaWarp && lane == 0) {
+    const uint32_t n = *s_issued;
+    for (uint32_t i = n > (uint32_t)kStages ? n - kStages : 0u; i < n; ++i)
+      if (!mbar_wait_bounded(smem_u32(full + i % kStages), (i / kStages) & 1u, kWaitLimitNs,
+                             p.status))
+        break;
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {

@@ -72,7 +72,8 @@ constexpr size_t kMaxDynSmem = 232448;                   // 227 KB per CTA
 // plus the shared expert's rows)
 static_assert(kStages * kStageBytes + 1024 + kBarBytes + 4 * (2 * 1028 + 2112) <= kMaxDynSmem,
               "shared memory");
-static_assert((3 * kStages + 2 * kAccBufs + 3) * 8 + 4 <= kBarBytes, "mbarriers + TMEM slot");
+static_assert((3 * kStages + 2 * kAccBufs + 3) * 8 + 5 * 4 <= kBarBytes,
+              "mbarriers, TMEM slot, issue counts and plan flags");
 static_assert(kNmax == kXBoxRows && kNmax <= (int)kAccCols, "one TMA box of token rows per stage");
 
 constexpr uint32_t make_idesc(int M, int N) {
@@ -102,10 +103,6 @@ __device__ __forceinline__ Item decode_item(int item, int total1, int nt1, int n
   return t;
 }
 
-__device__ __forceinline__ float silu_mul(float g, float u) {
-  return __fdividef(g, 1.0f + __expf(-g)) * u;
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_decode_kernel(const __grid_constant__ CUtensorMap tmap_x,
                                const __grid_constant__ CUtensorMap tmap_h,
@@ -120,8 +117,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_empty = acc_full + kAccBufs;
   uint64_t* drain = acc_empty + kAccBufs;
   uint64_t* sf_done = drain + 1;   // a stage's scale factors are in tensor memory
-  uint64_t* plan_bar = sf_done + kStages;   // [0] the plan is in shared memory, [1] its copy
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(plan_bar + 2);
+  uint64_t* plan_bar = sf_done + kStages;   // the bulk copy of the plan
+  uint64_t* sf_drain = plan_bar + 1;         // the scale-factor warp's last tensor-memory copies
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_drain + 1);
+  // stage fills issued by the weight and the token issuers, whether the plan copy may still be
+  // in flight, and whether the plan is usable (read by every role after the plan barrier)
+  uint32_t* s_issued = tmem_slot + 1;
+  uint32_t* s_plan_pending = s_issued + 2;
+  uint32_t* s_plan_ok = s_plan_pending + 1;
   const int nseg = p.g1.nseg;
   const int plan_ints = (nseg + 1 + 3) & ~3;    // 16-byte multiples for the bulk copies
   // m-tiles can outnumber segments (an expert with more than kNmax rows owns several): the
@@ -150,7 +153,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(drain), 1);
     for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(sf_done + s), 1);
     mbar_init(smem_u32(plan_bar), 1);
-    mbar_init(smem_u32(plan_bar + 1), 1);
+    mbar_init(smem_u32(sf_drain), 1);
+    s_issued[0] = s_issued[1] = 0u;
+    *s_plan_pending = 0u;
+    *s_plan_ok = 0u;
     fence_barrier_init();
   }
   tc_fence_before();
@@ -187,30 +193,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         // allocated in 256-byte units, so the rounded-up tail stays inside them)
         fence_proxy_async_global();
         const uint32_t bytes = (uint32_t)((4 * (nseg + 1) + 15) & ~15);
-        const uint32_t pb = smem_u32(plan_bar + 1);
+        const uint32_t pb = smem_u32(plan_bar);
         mbar_arrive_expect_tx(pb, 2 * bytes);
         bulk_load(smem_u32(s_tile), p.g1.tile_start, bytes, pb);
         bulk_load(smem_u32(s_seg), p.g1.seg_off, bytes, pb);
-        if (!mbar_wait_bounded(pb, 0u, kWaitLimitNs, status)) ok = 0;
+        if (!mbar_wait_bounded(pb, 0u, kWaitLimitNs, status)) {
+          ok = 0;
+          *s_plan_pending = 1u;   // the copy may still land: drained before the CTA exits
+        }
       }
+      *s_plan_ok = (uint32_t)ok;
     }
     ok = __shfl_sync(0xffffffffu, ok, 0);
     __syncwarp();
-    if (!ok)
-      for (int i = lane; i <= nseg; i += 32) s_tile[i] = 0;
-    for (int i = lane; i < max_tiles; i += 32) s_tseg[i] = 0;
-    __syncwarp();
-    for (int sg = lane; sg < nseg; sg += 32)
-      for (int mt = max(s_tile[sg], 0); mt < s_tile[sg + 1] && mt < max_tiles; ++mt) s_tseg[mt] = sg;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(plan_bar));
-  } else {
-    mbar_wait_bounded(smem_u32(plan_bar), 0u, kWaitLimitNs, status);
+    if (ok) {
+      for (int i = lane; i < max_tiles; i += 32) s_tseg[i] = 0;
+      __syncwarp();
+      for (int sg = lane; sg < nseg; sg += 32)
+        for (int mt = max(s_tile[sg], 0); mt < s_tile[sg + 1] && mt < max_tiles; ++mt)
+          s_tseg[mt] = sg;
+    }
   }
+  // every role reads the plan (or, after a timeout, runs no item) only after this barrier; the
+  // weight warp's waits above are bounded, so the barrier is reached
+  __syncthreads();
 
   const int nt1 = p.g1.N / 128, nt2 = p.g2.N / 128;
   const int kst1 = p.g1.K / kBK, kst2 = p.g2.K / kBK;
-  const int mtiles = s_tile[nseg];
+  const int mtiles = *s_plan_ok ? s_tile[nseg] : 0;
   int total1 = mtiles * nt1, total2 = mtiles * nt2;
   if (mtiles < 0 || mtiles > max_tiles || total1 > p.g1.max_items || total2 > p.g2.max_items) {
     if (threadIdx.x == 0) set_status(status, MOE_ERR_INVALID_ARG);
@@ -229,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // barrier completes once both parts have landed.
     if (lane == 0) {
       int stage = 0;
-      uint32_t phase = 0;
+      uint32_t phase = 0, n_issued = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
         const Item t = NVFP4MOE_ITEM(item);
@@ -245,6 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(fb, kTileBlockBytes);
           bulk_load(smem0 + stage * kStageBytes, src + (size_t)ks * kTileBlockBytes,
                     kTileBlockBytes, fb);
+          ++n_issued;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
@@ -253,6 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait_bounded(smem_u32(empty + stage), phase ^ 1u, kWaitLimitNs, status)) break;
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
+      s_issued[0] = n_issued;
     }
   } else if (warp == kXWarp) {
     // ---------------- token rows: one 2-D TMA box + their scales per stage ----------------
@@ -261,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       griddep_wait();
       int stage = 0;
-      uint32_t phase = 0;
+      uint32_t phase = 0, n_issued = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
         const Item t = NVFP4MOE_ITEM(item);
@@ -296,9 +308,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(fb, xbytes);
           tma_load_2d(sb + kXOff, tm, ks * 128, t.m0, fb);
           bulk_load(sb + kXSfOff, sft + (size_t)ks * kXSfBytes, kXSfBytes, fb);
+          ++n_issued;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
+      s_issued[1] = n_issued;
     }
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issue: D[weight row][token] ----------------
@@ -374,6 +388,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
+      // tensor memory is released only once this thread's last scale copies have completed
+      tc_commit(smem_u32(sf_drain));
+      mbar_wait_bounded(smem_u32(sf_drain), 0u, kWaitLimitNs, status);
     }
   } else {
     // ---------------- epilogue (warps 0-3): lane = weight row, column = token ----------------
@@ -388,16 +405,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Item t = NVFP4MOE_ITEM(item);
       const GemmArgs& q = t.ph ? p.g2 : p.g1;
       const int abuf = it % kAccBufs;
-      if (!mbar_wait_bounded(smem_u32(acc_full + abuf), acc_phase[abuf], kWaitLimitNs, status))
+      // every lane waits; the decision is taken together so that the warp never diverges
+      // before the warp-wide tensor-memory loads
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(acc_full + abuf), acc_phase[abuf],
+                                                     kWaitLimitNs, status)))
         break;
       acc_phase[abuf] ^= 1u;
       tc_fence_after();
       const int rows = (t.m0 >= 0 && t.m0 + t.rows <= q.out_rows) ? t.rows : 0;
       const uint32_t tbase = tmem_base + abuf * kAccCols + ((uint32_t)(warp * 32) << 16);
       if (t.ph == 0) {
-        // block b of h: 16 features; lanes < 16 hold gate rows, lanes >= 16 the up rows
-        const int I = q.N / 2;
-        const int b = t.nt * 4 + warp;
+        // Gated experts: block b of h (16 features); lanes < 16 hold its gate rows, lanes >= 16
+        // its up rows, and each half-warp takes one token of a pair.  Non-gated experts (ReLU2):
+        // lanes < 16 hold the up rows of block 2w, lanes >= 16 those of block 2w + 1 (w = the
+        // warp's 32-row slice of the tile), and both halves take the same token.
+        const bool gated = q.act != kActRelu2;
+        const int I = gated ? q.N / 2 : q.N;
+        const int b = gated ? t.nt * 4 + warp : t.nt * 8 + warp * 2 + (lo_half ? 0 : 1);
         uint8_t* hsf_tile = q.hsf_tiles + ((size_t)t.mt * (I / 64) + b / 4) * 512 + (b & 3);
         const float ag = ts_a * q.w_ts[t.seg * 4 + 0];
         const float au = ts_a * q.w_ts[t.seg * 4 + 1];
@@ -406,20 +430,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_32x32b_x16(tbase, v);
           tmem_ld_wait();
 #pragma unroll
-          for (int n = 0; n < kNmax; n += 2) {
+          for (int n = 0; n < kNmax; ++n) {
             if (n >= rows) break;
-            const float a0 = __uint_as_float(v[n]), a1 = __uint_as_float(v[n + 1]);
-            const float x0 = __shfl_xor_sync(0xffffffffu, a0, 16);
-            const float x1 = __shfl_xor_sync(0xffffffffu, a1, 16);
-            // the lower half-warp takes token n, the upper half token n+1
-            float g = (lo_half ? a0 : x1) * ag;
-            float u = (lo_half ? x0 : a1) * au;
-            const int col = n + (lo_half ? 0 : 1);
-            if (q.swiglu_clamp) {   // gate clamped from above, up on both sides
-              g = fminf(g, q.swiglu_limit);
-              u = fminf(fmaxf(u, -q.swiglu_limit), q.swiglu_limit);
+            if (gated && (n & 1)) continue;
+            float h;
+            int col;
+            if (gated) {
+              const float a0 = __uint_as_float(v[n]), a1 = __uint_as_float(v[(n + 1) & (kNmax - 1)]);
+              const float x0 = __shfl_xor_sync(0xffffffffu, a0, 16);
+              const float x1 = __shfl_xor_sync(0xffffffffu, a1, 16);
+              // the lower half-warp takes token n, the upper half token n+1
+              const float g = (lo_half ? a0 : x1) * ag;
+              const float u = (lo_half ? x0 : a1) * au;
+              col = n + (lo_half ? 0 : 1);
+              h = glu_activation(g, u, q.act, q.swiglu_limit, q.swiglu_alpha);
+            } else {
+              col = n;
+              h = glu_activation(0.0f, __uint_as_float(v[n]) * au, q.act, q.swiglu_limit,
+                                 q.swiglu_alpha);
             }
-            const float h = silu_mul(g, u);
             float bamax = fabsf(h);
 #pragma unroll
             for (int o = 8; o > 0; o >>= 1) bamax = fmaxf(bamax, __shfl_xor_sync(0xffffffffu, bamax, o));
@@ -478,6 +507,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 #undef NVFP4MOE_ITEM
 
+  // Teardown.  After a wait ran out, copies into shared memory may still be in flight: a stage
+  // whose fill one issuer made and the other did not gets the missing arrival here (the leading
+  // issuer is at most kStages fills ahead, since every fill waits for the slot's release, which
+  // needs the previous phase complete), so every issued phase completes once its bytes land;
+  // then the last kStages fills and the plan copy are waited for (bounded) before the CTA exits.
+  // Without a timeout every fill was consumed and these waits return at once.
+  __syncthreads();
+  if (warp == kWeightWarp && lane == 0) {
+    const uint32_t wi = s_issued[0], xi = s_issued[1];
+    const uint32_t lo = min(wi, xi), hi = max(wi, xi);
+    for (uint32_t i = lo; i < hi; ++i) mbar_arrive(smem_u32(full + i % kStages));
+    for (uint32_t i = hi > (uint32_t)kStages ? hi - kStages : 0u; i < hi; ++i)
+      if (!mbar_wait_bounded(smem_u32(full + i % kStages), (i / kStages) & 1u, kWaitLimitNs,
+                             status))
+        break;
+    if (*s_plan_pending) mbar_wait_bounded(smem_u32(plan_bar), 0u, kWaitLimitNs, status);
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {

@@ -1,0 +1,477 @@
+// Grouped GEMMs of the W4A16 layer: BF16 activations as they are, NVFP4 expert weights decoded
+// to BF16 inside the kernel ("b12x" README, section "What's in here", moe: "W4A16 (BF16
+// activations, inline FP4 weight dequant - no activation-scale math)").
+//
+// Tiles are 128 expert-ordered rows (MMA M) x 128 weight rows (MMA N) on the 5th-generation
+// tensor cores (tcgen05.mma kind::f16, BF16 x BF16 -> FP32 in tensor memory), K in sub-stages of
+// 64.  Per K block of 256 the copy warp fetches the expert's packed NVFP4 weight block (18 KB,
+// the layout the FP4 GEMMs read) with one bulk copy into a raw ring, and per sub-stage one 2-D
+// TMA box (64 BF16 x 128 rows, 128-byte swizzle) of the expert-ordered activation rows.  Four
+// converter warps, one thread per weight row, decode the sub-stage's 64 E2M1 codes of their row
+// with its four E4M3 block scales into BF16 (e2m1 * scale has at most 6 significant bits and lies
+// in [2^-10, 2688], so it is exact in BF16) and store the row into the sub-stage's B tile in the
+// same 128-byte-swizzled K-major layout; the per-matrix FP32 tensor scale is applied in the
+// epilogue.  Warps: 0-3 epilogue, 4 copies, 5 tensor-memory allocation + the MMA thread, 6-9
+// converters.  Two 128-column FP32 accumulators let the epilogue overlap the next tile.
+//   GEMM1 epilogue: g, u (times their tensor scales) -> the activation -> h rounded to BF16
+//                   (row-major [rows, I], expert order: the next GEMM's A operand);
+//   GEMM2 epilogue: (acc * ts_down) * router weight, reduced into the token's FP32 output row.
+// Every wait is bounded and reports MOE_ERR_DEVICE_TIMEOUT; after a timeout the copies already
+// issued are waited for before the CTA exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace nvfp4moe {
+
+namespace {
+
+constexpr int kEpiWarps = 4;
+constexpr int kCopyWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kConvWarp0 = 6;
+constexpr int kConvWarps = 4;
+constexpr int kThreads = (kConvWarp0 + kConvWarps) * 32;
+constexpr int kRawStages = 2;                 // raw NVFP4 weight blocks (K = 256 each)
+constexpr int kSubStages = 4;                 // converted sub-stages (K = 64 each)
+constexpr int kSubK = 64;
+constexpr int kTileBytes16 = 128 * 128;       // 128 rows x 64 BF16
+constexpr int kSubBytes = 2 * kTileBytes16;   // A tile | B tile
+constexpr int kRawOff = kSubStages * kSubBytes;
+constexpr int kBarOff = kRawOff + kRawStages * kTileBlockBytes;
+constexpr uint32_t kTmemCols = 256;           // two 128-column accumulators
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr size_t kSmemBytes = 1024 + kBarOff + 256 + 8 * 1027;
+
+static_assert(kRawOff % 1024 == 0 && kTileBlockBytes % 1024 == 0, "1024-byte aligned tiles");
+static_assert(kSmemBytes <= 232448, "shared memory");
+// raw full/empty, sub full/empty, acc full/empty x2, drain; TMEM slot, issue and arrival counts
+static_assert((2 * kRawStages + 2 * kSubStages + 4 + 1) * 8 + (3 + kConvWarps) * 4 <= 256,
+              "barrier area");
+
+// Instruction descriptor of tcgen05.mma kind::f16: FP32 accumulator (bits 4-5 = 1), A and B BF16
+// (bits 7-9 and 10-12 = 1), both K-major, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t make_idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "setp.ne.u32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+      "}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Two E2M1 codes (low nibble = first element) times an E4M3 scale as BF16x2 (exact).
+__device__ __forceinline__ uint32_t e2m1x2_scaled_bf16x2(uint32_t byte, __half2 scale2) {
+  uint32_t h2;
+  const uint16_t in = (uint16_t)(byte & 0xFFu);
+  asm("{\n"
+      ".reg .b8 b;\n"
+      "cvt.u8.u16 b, %1;\n"
+      "cvt.rn.f16x2.e2m1x2 %0, b;\n"
+      "}"
+      : "=r"(h2)
+      : "h"(in));
+  const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&h2), scale2);
+  const float2 f = __half22float2(v);
+  const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+struct TileW16 {
+  int seg, m0, rows, nt;
+};
+
+__device__ __forceinline__ TileW16 decode_tile_w16(int item, int n_tiles, const int32_t* s_tile,
+                                                   const int32_t* s_seg, int nseg) {
+  TileW16 t;
+  const int mt = item / n_tiles;
+  t.nt = item - mt * n_tiles;
+  int lo = 0, hi = nseg - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_tile[mid] <= mt) lo = mid;
+    else hi = mid - 1;
+  }
+  t.seg = lo;
+  t.m0 = s_seg[lo] + (mt - s_tile[lo]) * kBM;
+  t.rows = min(kBM, s_seg[lo + 1] - t.m0);
+  return t;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_w16_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmW16Args p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
+  uint64_t* raw_full = bars;
+  uint64_t* raw_empty = raw_full + kRawStages;
+  uint64_t* sub_full = raw_empty + kRawStages;
+  uint64_t* sub_empty = sub_full + kSubStages;
+  uint64_t* acc_full = sub_empty + kSubStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint32_t* s_issued = tmem_slot + 1;   // [0] raw blocks, [1] A boxes issued by the copy thread
+  uint32_t* s_conv = s_issued + 2;      // sub-stage arrivals of each converter warp
+  int32_t* s_tile = reinterpret_cast<int32_t*>(smem + kBarOff + 256);
+  int32_t* s_seg = s_tile + (p.nseg + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kRawStages; ++s) {
+      mbar_init(smem_u32(raw_full + s), 1);            // the bulk copy (expect_tx)
+      mbar_init(smem_u32(raw_empty + s), kConvWarps);  // every converter warp is done with it
+    }
+    for (int s = 0; s < kSubStages; ++s) {
+      mbar_init(smem_u32(sub_full + s), 1 + kConvWarps);   // the A box (expect_tx) + converters
+      mbar_init(smem_u32(sub_empty + s), 1);               // the MMA commit
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(acc_full + b), 1);
+      mbar_init(smem_u32(acc_empty + b), kEpiWarps);
+    }
+    mbar_init(smem_u32(drain), 1);
+    s_issued[0] = s_issued[1] = 0u;
+    for (int w = 0; w < kConvWarps; ++w) s_conv[w] = 0u;
+    fence_barrier_init();
+  }
+  if (warp == kCopyWarp && lane == 0)
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_a) : "memory");
+  griddep_wait();
+  griddep_launch();
+  for (int i = threadIdx.x; i <= p.nseg; i += blockDim.x) {
+    s_tile[i] = p.tile_start[i];
+    s_seg[i] = p.seg_off[i];
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int n_tiles = p.N / kBN;
+  int total = s_tile[p.nseg] * n_tiles;
+  if (total < 0 || total > p.max_items) {
+    if (threadIdx.x == 0) set_status(p.status, MOE_ERR_INVALID_ARG);
+    total = 0;
+  }
+  const int kblk = p.K / kBK;        // raw weight blocks per tile
+  const uint32_t smem0 = smem_u32(smem);
+
+  if (warp == kCopyWarp) {
+    // ---------------- raw weight blocks (bulk) and activation boxes (TMA) ----------------
+    if (lane == 0) {
+      int rs = 0, ss = 0;
+      uint32_t rph = 0, sph = 0, n_raw = 0, n_sub = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+        const TileW16 t = decode_tile_w16(item, n_tiles, s_tile, s_seg, p.nseg);
+        const uint8_t* bsrc = p.b_tiles + (size_t)t.seg * p.b_per_seg +
+                              (size_t)t.nt * kblk * kTileBlockBytes;
+        for (int kb = 0; kb < kblk && ok; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(raw_empty + rs), rph ^ 1u, kWaitLimitNs, p.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t rb = smem_u32(raw_full + rs);
+          mbar_arrive_expect_tx(rb, kTileBlockBytes);
+          bulk_load(smem0 + kRawOff + rs * kTileBlockBytes, bsrc + (size_t)kb * kTileBlockBytes,
+                    kTileBlockBytes, rb);
+          ++n_raw;
+          if (++rs == kRawStages) { rs = 0; rph ^= 1u; }
+          for (int q = 0; q < kBK / kSubK; ++q) {
+            if (!mbar_wait_bounded(smem_u32(sub_empty + ss), sph ^ 1u, kWaitLimitNs, p.status)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = smem_u32(sub_full + ss);
+            mbar_arrive_expect_tx(fb, kTileBytes16);
+            tma_load_2d(smem0 + ss * kSubBytes, &tmap_a, kb * kBK + q * kSubK, t.m0, fb);
+            ++n_sub;
+            if (++ss == kSubStages) { ss = 0; sph ^= 1u; }
+          }
+        }
+      }
+      s_issued[0] = n_raw;
+      s_issued[1] = n_sub;
+    }
+  } else if (warp >= kConvWarp0) {
+    // ---------------- NVFP4 weight row -> BF16 row of the B tile ----------------
+    const int r = (warp - kConvWarp0) * 32 + lane;      // weight row of the tile
+    int rs = 0, ss = 0;
+    uint32_t rph = 0, sph = 0, n_arr = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+      for (int kb = 0; kb < kblk && ok; ++kb) {
+        // every lane waits; the decision is made together, so the warp never diverges
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(raw_full + rs), rph,
+                                                       kWaitLimitNs, p.status))) {
+          ok = false;
+          break;
+        }
+        const uint8_t* raw = smem + kRawOff + rs * kTileBlockBytes;
+        for (int q = 0; q < kBK / kSubK; ++q) {
+          if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(sub_empty + ss), sph ^ 1u,
+                                                         kWaitLimitNs, p.status))) {
+            ok = false;
+            break;
+          }
+          // the 64 codes of sub-stage q are 16-byte chunks 2q and 2q+1 of the row (stored at
+          // chunk ^ (row % 8)); its four scales are one word of scale group q
+          const uint4 c0 = *reinterpret_cast<const uint4*>(raw + r * 128 + (((2 * q) ^ (r & 7)) << 4));
+          const uint4 c1 = *reinterpret_cast<const uint4*>(raw + r * 128 + (((2 * q + 1) ^ (r & 7)) << 4));
+          const uint32_t sw = *reinterpret_cast<const uint32_t*>(
+              raw + kTileBytes + q * 512 + (r & 31) * 16 + (r >> 5) * 4);
+          const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          uint8_t* brow = smem + ss * kSubBytes + kTileBytes16 + r * 128;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {         // 16-byte chunk j of the BF16 row: 8 values
+            // elements 8j .. 8j+7 use block scale (8j) / 16 = j / 2
+            const uint32_t sb = (sw >> (8 * (j >> 1))) & 0xFFu;
+            const __half hs = __float2half_rn(e4m3_to_f32(sb));
+            const __half2 s2 = __halves2half2(hs, hs);
+            const uint32_t w = cw[j];
+            uint4 o;
+            o.x = e2m1x2_scaled_bf16x2(w & 0xFFu, s2);
+            o.y = e2m1x2_scaled_bf16x2((w >> 8) & 0xFFu, s2);
+            o.z = e2m1x2_scaled_bf16x2((w >> 16) & 0xFFu, s2);
+            o.w = e2m1x2_scaled_bf16x2(w >> 24, s2);
+            *reinterpret_cast<uint4*>(brow + ((j ^ (r & 7)) << 4)) = o;
+          }
+          fence_proxy_async_smem();     // the tensor core reads what these stores wrote
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(sub_full + ss));
+          ++n_arr;
+          if (++ss == kSubStages) { ss = 0; sph ^= 1u; }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(raw_empty + rs));
+        if (++rs == kRawStages) { rs = 0; rph ^= 1u; }
+      }
+    }
+    if (lane == 0) s_conv[warp - kConvWarp0] = n_arr;
+  } else if (warp == kMmaWarp) {
+    // ---------------- MMA issue (one thread) ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc_bf16(kBM, kBN);
+      int ss = 0;
+      uint32_t sph = 0;
+      uint32_t acc_phase[2] = {0u, 0u};
+      const uint64_t dA0 = smem_desc(smem0, 16, 1024, kLayoutSwizzle128B);
+      const uint64_t dB0 = smem_desc(smem0 + kTileBytes16, 16, 1024, kLayoutSwizzle128B);
+      bool ok = true;
+      int it = 0;
+      const int nsub = kblk * (kBK / kSubK);
+      for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++it) {
+        const int abuf = it & 1;
+        if (!mbar_wait_bounded(smem_u32(acc_empty + abuf), acc_phase[abuf] ^ 1u, kWaitLimitNs,
+                               p.status)) {
+          ok = false;
+          break;
+        }
+        acc_phase[abuf] ^= 1u;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + abuf * kBN;
+        for (int k = 0; k < nsub; ++k) {
+          if (!mbar_wait_bounded(smem_u32(sub_full + ss), sph, kWaitLimitNs, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t so = (uint64_t)((uint32_t)(ss * kSubBytes) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < kSubK / 16; ++kk)   // K = 16 per MMA: 32 bytes -> 2 units
+            tc_mma_bf16(d_tmem, dA0 + so + kk * 2, dB0 + so + kk * 2, idesc,
+                        (k | kk) != 0 ? 1u : 0u);
+          tc_commit(smem_u32(sub_empty + ss));
+          if (++ss == kSubStages) { ss = 0; sph ^= 1u; }
+        }
+        if (ok) tc_commit(smem_u32(acc_full + abuf));
+      }
+      tc_commit(smem_u32(drain));
+      mbar_wait_bounded(smem_u32(drain), 0u, kWaitLimitNs, p.status);
+    }
+  } else {
+    // ---------------- epilogue (warps 0-3): one accumulator row per thread ----------------
+    uint32_t acc_phase[2] = {0u, 0u};
+    int it = 0;
+    const int r = warp * 32 + lane;
+    for (int item = blockIdx.x; item < total; item += gridDim.x, ++it) {
+      const TileW16 t = decode_tile_w16(item, n_tiles, s_tile, s_seg, p.nseg);
+      const int abuf = it & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(acc_full + abuf), acc_phase[abuf],
+                                                     kWaitLimitNs, p.status)))
+        break;
+      acc_phase[abuf] ^= 1u;
+      tc_fence_after();
+      const int prow = t.m0 + r;
+      const bool valid = r < t.rows && prow >= 0 && prow < p.out_rows;
+      const uint32_t tbase = tmem_base + abuf * kBN + ((uint32_t)(warp * 32) << 16);
+      if (p.mode == 0) {
+        const bool gated = p.act != kActRelu2;
+        const int I = gated ? p.N / 2 : p.N;
+        const float ag = p.w_ts[t.seg * 4 + 0];
+        const float au = p.w_ts[t.seg * 4 + 1];
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tbase + c * 32, v);
+          tmem_ld_wait();
+          if (!valid) continue;
+          // gated: (16 gate | 16 up) columns -> 16 features; non-gated: 32 up columns -> 32
+          uint32_t packed[16];
+          if (gated) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float h0 = glu_activation(__uint_as_float(v[2 * i]) * ag,
+                                              __uint_as_float(v[16 + 2 * i]) * au, p.act,
+                                              p.swiglu_limit, p.swiglu_alpha);
+              const float h1 = glu_activation(__uint_as_float(v[2 * i + 1]) * ag,
+                                              __uint_as_float(v[17 + 2 * i]) * au, p.act,
+                                              p.swiglu_limit, p.swiglu_alpha);
+              const __nv_bfloat162 b = __floats2bfloat162_rn(h0, h1);
+              packed[i] = *reinterpret_cast<const uint32_t*>(&b);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float h0 = glu_activation(0.0f, __uint_as_float(v[2 * i]) * au, p.act,
+                                              p.swiglu_limit, p.swiglu_alpha);
+              const float h1 = glu_activation(0.0f, __uint_as_float(v[2 * i + 1]) * au, p.act,
+                                              p.swiglu_limit, p.swiglu_alpha);
+              const __nv_bfloat162 b = __floats2bfloat162_rn(h0, h1);
+              packed[i] = *reinterpret_cast<const uint32_t*>(&b);
+            }
+          }
+          const int f0 = gated ? t.nt * (kBN / 2) + c * 16 : t.nt * kBN + c * 32;
+          uint4* dst = reinterpret_cast<uint4*>(p.hb + ((size_t)prow * I + f0) * 2);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (i < (gated ? 2 : 4))
+              dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                  packed[4 * i + 3]);
+        }
+      } else {
+        const float alpha = p.w_ts[t.seg * 4 + 2];
+        int tok = 0;
+        float wr = 0.0f;
+        bool ok_row = valid;
+        if (valid) {
+          tok = __ldg(p.perm_src + prow);
+          wr = __ldg(p.perm_w + prow);
+          if (tok < 0 || tok >= p.y_rows) {
+            set_status(p.status, MOE_ERR_INVALID_ARG);
+            ok_row = false;
+          }
+        }
+        float* yrow = p.yacc + (size_t)(ok_row ? tok : 0) * p.N + t.nt * kBN;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tbase + c * 32, v);
+          tmem_ld_wait();
+          if (!ok_row) continue;
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            red_add_v4(yrow + c * 32 + 4 * i, (__uint_as_float(v[4 * i]) * alpha) * wr,
+                       (__uint_as_float(v[4 * i + 1]) * alpha) * wr,
+                       (__uint_as_float(v[4 * i + 2]) * alpha) * wr,
+                       (__uint_as_float(v[4 * i + 3]) * alpha) * wr);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(acc_empty + abuf));
+    }
+  }
+
+  // Teardown.  After a timeout, copies into shared memory may still be in flight.  A sub-stage
+  // completes on the A box (copy thread, with its bytes) and one arrival per converter warp;
+  // every participant waits for the slot's release before it arrives, so only the last
+  // kSubStages indices can be open, and the arrivals missing there are made here on behalf of
+  // whoever stopped, after which every issued phase completes once its bytes land.  Then the
+  // last phases of both rings are waited for (bounded).  Without a timeout every phase was
+  // consumed and these waits return at once.
+  __syncthreads();
+  if (warp == kCopyWarp && lane == 0) {
+    const uint32_t nr = s_issued[0], na = s_issued[1];
+    uint32_t hi = na;
+    for (int w = 0; w < kConvWarps; ++w) hi = max(hi, s_conv[w]);
+    const uint32_t lo = hi > (uint32_t)kSubStages ? hi - kSubStages : 0u;
+    for (uint32_t i = lo; i < hi; ++i) {
+      const uint32_t bar = smem_u32(sub_full + i % kSubStages);
+      if (i >= na) mbar_arrive(bar);
+      for (int w = 0; w < kConvWarps; ++w)
+        if (i >= s_conv[w]) mbar_arrive(bar);
+    }
+    for (uint32_t i = lo; i < hi; ++i)
+      if (!mbar_wait_bounded(smem_u32(sub_full + i % kSubStages), (i / kSubStages) & 1u,
+                             kWaitLimitNs, p.status))
+        break;
+    for (uint32_t i = nr > (uint32_t)kRawStages ? nr - kRawStages : 0u; i < nr; ++i)
+      if (!mbar_wait_bounded(smem_u32(raw_full + i % kRawStages), (i / kRawStages) & 1u,
+                             kWaitLimitNs, p.status))
+        break;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn_w16() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm_w16(const GemmW16Args& a, cudaStream_t s) {
+  auto encode = encode_fn_w16();
+  if (!encode) return cudaErrorNotSupported;
+  if (a.N % kBN != 0 || a.K % kBK != 0 || a.nseg < 1) return cudaErrorInvalidValue;
+  // expert-ordered BF16 rows [out_rows, K]; box = 64 elements (128 bytes) x 128 rows
+  CUtensorMap tmap;
+  const cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.out_rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kSubK, (cuuint32_t)kBM};
+  const cuuint32_t estr[2] = {1, 1};
+  if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.a_rows), dims,
+             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  const size_t smem = kSmemBytes - 8 * 1027 + sizeof(int32_t) * 2 * ((size_t)a.nseg + 2);
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_w16_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int grid = a.max_items;
+  if (grid > num_sms()) grid = num_sms();
+  if (grid < 1) grid = 1;
+  return launch_pdl(grouped_gemm_w16_kernel, dim3(grid), dim3(kThreads), smem, s, tmap, a);
+}
+
+}  // namespace nvfp4moe

@@ -22,6 +22,12 @@ constexpr int kDecodeMaxRows = 64;   // batches up to this many tokens take the 
 constexpr int kDecodeTileRows = 16;  // rows of an expert per decode GEMM tile (its MMA N)
 constexpr int kSmallPlanRows = 2048; // T*k routed by the one-block plan
 
+// Activation of GEMM1's epilogue (GemmArgs::act).
+constexpr int kActSwiglu = 0;        // silu(g) * u
+constexpr int kActSwigluClamp = 1;   // silu(min(g, L)) * clamp(u, -L, L)
+constexpr int kActRelu2 = 2;         // max(u, 0)^2, non-gated experts
+constexpr int kActSwigluOai = 3;     // (clamp(u, -L, L) + 1) * g' * sigmoid(alpha * g'), g' = min(g, L)
+
 // Router chunking: tokens per chunk (one router block and one scatter block each).
 inline int plan_tokens_per_chunk(int k) { return k <= 16 ? 64 : 32; }
 
@@ -34,7 +40,8 @@ inline int plan_tokens_per_chunk(int k) { return k <= 16 ? 64 : 32; }
 //                   tensor-memory scale copy expects).
 // A tile of the MMA's B operand for one pipeline stage is therefore one contiguous bulk copy.
 //   w13 [Et][2I/128][H/256][18432]: GEMM1 rows interleaved by 16 (rows 32b+i are gate rows
-//       16b+i for i < 16, up rows 16b+i-16 otherwise);
+//       16b+i for i < 16, up rows 16b+i-16 otherwise); for non-gated experts (ReLU2)
+//       [Et][I/128][H/256][18432], the up rows in order;
 //   w2  [Et][H/128][I/256][18432]: GEMM2 (down) rows;
 //   ts  [Et][4] FP32: gate, up, down tensor scales (the 4th is padding);
 //   bias [E] FP32: the variant router's per-expert selection bias (zero unless set).
@@ -43,8 +50,14 @@ constexpr int kTileBytes = 128 * 128;             // codes of one (N tile, K sta
 constexpr int kTileSfBytes = 4 * 512;             // its scales
 constexpr int kTileBlockBytes = kTileBytes + kTileSfBytes;
 
+// GEMM1 output rows per expert: gate and up rows (2I), or the up rows alone for non-gated
+// experts (I).
+inline bool gated_experts(const moe_config& c) { return (c.flags & MOE_FLAG_ACT_RELU2) == 0u; }
+inline int gemm1_rows(const moe_config& c) { return gated_experts(c) ? 2 * c.inter : c.inter; }
+
 struct WeightLayout {
   int E, Et, H, I;
+  bool gated;
   size_t w13, w2, ts, bias, total;
   size_t w13_per_e, w2_per_e;
   explicit WeightLayout(const moe_config& c) {
@@ -52,7 +65,8 @@ struct WeightLayout {
     Et = E + (c.shared_inter > 0 ? 1 : 0);
     H = c.hidden;
     I = c.inter;
-    w13_per_e = (size_t)(2 * I / 128) * (H / 256) * kTileBlockBytes;
+    gated = gated_experts(c);
+    w13_per_e = (size_t)(gemm1_rows(c) / 128) * (H / 256) * kTileBlockBytes;
     w2_per_e = (size_t)(H / 128) * (I / 256) * kTileBlockBytes;
     size_t o = 0;
     w13 = o; o = align_up(o + w13_per_e * Et);
@@ -87,10 +101,11 @@ bool prologue_small_fits(int T, int H, int k);
 // Workspace of moe_run for T tokens.  Offset 0 holds the device status word.
 struct RunLayout {
   size_t hdr, amax_part, ids, w, hist, base, seg_off, tile_start, perm_src, perm_w, inv, xq, xsf,
-      hq, hsf, yacc, obuf, perm_seg, xq_perm, xsf_tiles, hsf_tiles, ready, total;
+      hq, hsf, yacc, obuf, perm_seg, xq_perm, xsf_tiles, hsf_tiles, ready, xb_perm, hb, total;
   int T, R, Rt, nseg, nchunks, tpc, dtiles;
   bool small;   // fused prologue + stored-row combine
   bool decode;  // T <= kDecodeMaxRows: cluster prologue and the swapped-operand decode GEMM
+  bool w16;     // W4A16 layer: BF16 activation and h rows, one path for every batch size
   RunLayout(const moe_config& c, int T_) {
     T = T_;
     const int k = c.top_k, E = c.num_experts, H = c.hidden, I = c.inter;
@@ -116,7 +131,8 @@ struct RunLayout {
     xsf = o;        o = align_up(o + (size_t)T * H / 16);
     hq = o;         o = align_up(o + (size_t)Rt * I / 2);
     hsf = o;        o = align_up(o + (size_t)Rt * I / 16);
-    small = (int64_t)R <= 2048 && (int64_t)T * H <= kSmallPrologueElems &&
+    w16 = (c.flags & MOE_FLAG_ACT_BF16) != 0u;
+    small = !w16 && (int64_t)R <= 2048 && (int64_t)T * H <= kSmallPrologueElems &&
             (int64_t)Rt * H <= kStoreCombineElems;
     yacc = o;       o = align_up(o + (small ? 0 : 4 * (size_t)T * H));
     obuf = o;       o = align_up(o + (small ? 4 * (size_t)Rt * H : 0));
@@ -134,6 +150,8 @@ struct RunLayout {
     xsf_tiles = o;  o = align_up(o + (size_t)dtiles * (H / 64) * 512);
     hsf_tiles = o;  o = align_up(o + (size_t)dtiles * (I / 64) * 512);
     ready = o;      o = align_up(o + (decode ? 4 * ((size_t)dtiles + 1) : 0));   // + plan flag
+    xb_perm = o;    o = align_up(o + (w16 ? 2 * (size_t)Rt * H : 0));
+    hb = o;         o = align_up(o + (w16 ? 2 * (size_t)Rt * I : 0));
     total = o;
   }
 };
@@ -153,10 +171,11 @@ cudaError_t launch_act_quant(const void* x, int64_t rows, int64_t cols, uint8_t*
 
 // The two halves of launch_act_quant for batches that are planned before they are encoded:
 // max |x| -> tensor scale (and the accumulator zeroing), then the encode into token order and
-// into every expert row of each token (xq_perm, xsf_tiles).
+// into every expert row of each token (xq_perm, xsf_tiles).  With ts_in (already quantised
+// input) the first half only zeroes the accumulator and copies *ts_in into the header.
 cudaError_t launch_act_amax(const void* x, int64_t rows, int64_t cols, float* ts, WsHeader* hdr,
                             uint32_t* partials, float* zero_buf, int64_t zero_floats,
-                            cudaStream_t s);
+                            cudaStream_t s, const float* ts_in);
 cudaError_t launch_act_encode_perm(const void* x, int T, int H, int k, int E, int shared, int Rt,
                                    const float* ts, const int32_t* ids, const int32_t* inv,
                                    const int32_t* offsets, const int32_t* tile_start,
@@ -225,8 +244,10 @@ struct GemmArgs {
   const float* perm_w;      // modes 1 and 2: router weight of each permuted row
   float* yacc;              // mode 1 out [T, N]
   float* obuf;              // mode 2 out [rows, N]
-  int swiglu_clamp;         // mode 0: h = silu(min(g, L)) * clamp(u, -L, L) with L = swiglu_limit
+  int act;                  // mode 0, the activation (kAct* in common.cuh): SwiGLU, clamped
+                            // SwiGLU, ReLU2 (non-gated: N = I columns, no gate), SwiGLU-OAI
   float swiglu_limit;
+  float swiglu_alpha;
   int32_t* status;
   int max_ctas;
   // bounds used to reject malformed plan data instead of touching memory outside the buffers
@@ -241,6 +262,34 @@ struct GemmArgs {
   uint8_t* hsf_tiles;         // mode 0 out [tiles][(N/2)/64][512]
 };
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s);
+
+// The W4A16 layer (BF16 activations, NVFP4 weights decoded to BF16 in shared memory): one
+// grouped GEMM on kind::f16 tensor cores (gemm_w16.cu), 128 expert-ordered rows x 128 weight rows.
+struct GemmW16Args {
+  const void* a_rows;         // A operand: BF16 rows [out_rows, K] in expert order
+  const uint8_t* b_tiles;     // packed NVFP4 weight blocks (WeightLayout), expert s at s*b_per_seg
+  size_t b_per_seg;
+  const float* w_ts;          // [nseg][4] tensor scales
+  const int32_t* seg_off;     // [nseg+1]
+  const int32_t* tile_start;  // [nseg+1] 128-row tiles
+  int nseg;
+  int N, K;
+  int mode;                   // 0: activation, h to BF16 rows (hb [out_rows, I]); 1: router-
+                              // weighted FP32 reduction into yacc [y_rows, N]
+  int act;                    // kAct* (mode 0)
+  float swiglu_limit, swiglu_alpha;
+  uint8_t* hb;                // mode 0 out, BF16 [out_rows, I]
+  const int32_t* perm_src;    // mode 1: token of each permuted row
+  const float* perm_w;        // mode 1: router weight of each permuted row
+  float* yacc;                // mode 1 out [y_rows, N]
+  int out_rows, y_rows, max_items;
+  int32_t* status;
+};
+cudaError_t launch_grouped_gemm_w16(const GemmW16Args& a, cudaStream_t s);
+
+// Copies BF16 token rows into expert order: row p of xb_perm is row perm_src[p] of x [T, H].
+cudaError_t launch_permute_rows_bf16(const void* x, int T, int H, int Rt, const int32_t* perm_src,
+                                     void* xb_perm, int32_t* status, cudaStream_t s);
 
 // Decode-sized batches (T <= kDecodeMaxRows): both grouped GEMMs in one persistent launch
 // (gemm_decode.cu), weights as the MMA's M operand and tiles of kDecodeTileRows token rows of one
@@ -285,6 +334,8 @@ struct PrologueArgs {
   float *w, *perm_w;
   int sqrtsp;              // the variant router (see PlanArgs)
   const float* bias;
+  const float* in_ts;      // non-null: x is already quantised (its codes are permuted later);
+                           // only this tensor scale is copied to ts, nothing is encoded
 };
 cudaError_t launch_prologue_small(const PrologueArgs& a, cudaStream_t s);
 
@@ -308,6 +359,12 @@ struct DecodePrologueArgs {
   int32_t* ready;          // [nready] readiness counts of the decode GEMM, zeroed here
   int nready;
   int32_t* plan_flag;      // 0 before this kernel lets the GEMM launch, 1 once the plan is written
+  // already quantised input (all null for BF16 x): codes [T, H/2], scales [T, H/16] and the
+  // tensor scale, copied into expert order as they are (xq / xsf are then not written)
+  const uint8_t* in_xq;
+  const uint8_t* in_xsf;
+  const float* in_ts;
+  int no_plan_flag;        // test hook (MOE_INJECT_NO_PLAN_FLAG): never raise plan_flag
 };
 cudaError_t launch_decode_prologue(const DecodePrologueArgs& a, cudaStream_t s);
 

@@ -18,11 +18,13 @@ constexpr int kMaxAmaxBlocks = 1024;
 
 // Pass 1: max |x| over the whole tensor (BF16 magnitudes compare as their bit patterns), with a
 // last-block reduction that writes ts = amax / 2688 and re-arms the block counter.  Optionally
-// zero-fills `zero` (the FP32 output accumulator of the layer) on the way.
+// zero-fills `zero` (the FP32 output accumulator of the layer) on the way.  With ts_in (input
+// already quantised, nvec = 0) the last block takes that tensor scale over instead.
 __global__ void __launch_bounds__(kThreads) act_amax_kernel(const uint4* __restrict__ x,
                                                            int64_t nvec, WsHeader* hdr,
                                                            uint32_t* partials, float* ts_out,
-                                                           float4* zero, int64_t nzero4) {
+                                                           float4* zero, int64_t nzero4,
+                                                           const float* ts_in) {
   __shared__ uint32_t red[32];
   __shared__ bool is_last;
   griddep_wait();
@@ -50,9 +52,14 @@ __global__ void __launch_bounds__(kThreads) act_amax_kernel(const uint4* __restr
   __syncthreads();
   v = block_max_u32(v, red);
   if (threadIdx.x == 0) {
-    if (v >= 0x7F80u) set_status(&hdr->status, MOE_ERR_NONFINITE);
-    const float amax = bf16_bits_to_f32(v);
-    const float ts = __fdiv_rn(amax, 2688.0f);
+    float ts;
+    if (ts_in) {
+      ts = *ts_in;
+      if (!(ts >= 0.0f && ts <= 3.402823466e38f)) set_status(&hdr->status, MOE_ERR_NONFINITE);
+    } else {
+      if (v >= 0x7F80u) set_status(&hdr->status, MOE_ERR_NONFINITE);
+      ts = __fdiv_rn(bf16_bits_to_f32(v), 2688.0f);
+    }
     hdr->ts = ts;
     if (ts_out) *ts_out = ts;
     hdr->counter = 0u;
@@ -80,6 +87,7 @@ struct WeightSrc {
   const uint16_t* routed[3];  // gate [E,I,H], up [E,I,H], down [E,H,I]
   const uint16_t* shared[3];  // [I,H], [I,H], [H,I] or null
   int E, H, I;
+  int gated;                  // 0: non-gated experts (ReLU2), no gate matrix to read or pack
 };
 
 __device__ __forceinline__ const uint16_t* matrix_ptr(const WeightSrc& w, int slot, int m,
@@ -87,9 +95,10 @@ __device__ __forceinline__ const uint16_t* matrix_ptr(const WeightSrc& w, int sl
   return slot < w.E ? w.routed[m] + (int64_t)slot * per : w.shared[m];
 }
 
-// Row of the gate (m=0) or up (m=1) row n inside the 16-interleaved w13 layout.
-__host__ __device__ __forceinline__ int64_t w13_row(int64_t n, int m) {
-  return (n >> 4) * 32 + (m ? 16 : 0) + (n & 15);
+// Row of the gate (m=0) or up (m=1) row n inside the 16-interleaved w13 layout (gated experts),
+// or of up row n in the up-only w13 layout (non-gated experts).
+__host__ __device__ __forceinline__ int64_t w13_row(int64_t n, int m, int gated) {
+  return gated ? (n >> 4) * 32 + (m ? 16 : 0) + (n & 15) : n;
 }
 
 // max |W| per (slot, matrix) as BF16 magnitude bits, atomically max-ed into amax_bits[slot*4+m].
@@ -97,6 +106,7 @@ __global__ void __launch_bounds__(kThreads) weight_amax_kernel(WeightSrc w, uint
   __shared__ uint32_t red[32];
   const int mi = blockIdx.y;
   const int slot = mi / 3, m = mi % 3;
+  if (m == 0 && !w.gated) return;   // no gate matrix: its tensor scale stays 0
   const int64_t per = (int64_t)w.I * w.H;
   const uint4* src = reinterpret_cast<const uint4*>(matrix_ptr(w, slot, m, per));
   const int64_t nvec = per / 8;
@@ -117,16 +127,18 @@ __global__ void weight_ts_kernel(uint32_t* amax_bits_then_ts, int n) {
 }
 
 struct WeightDst {
-  uint8_t* w13;     // [Et][2I/128][H/256][block]
+  uint8_t* w13;     // [Et][2I/128][H/256][block] ([Et][I/128][H/256][block] when not gated)
   uint8_t* w2;      // [Et][H/128][I/256][block]
   const float* ts;  // [Et][4]
   int64_t w13_per_e, w2_per_e;
+  int gated;
 };
 
 // One thread per 16-element block of one matrix row: quantise and store into the packed layout.
 __global__ void __launch_bounds__(kThreads) weight_encode_kernel(WeightSrc w, WeightDst d) {
   const int mi = blockIdx.y;
   const int slot = mi / 3, m = mi % 3;
+  if (m == 0 && !w.gated) return;
   const int64_t per = (int64_t)w.I * w.H;
   const int64_t K = m < 2 ? w.H : w.I;
   const int64_t nblk = per / 16;
@@ -147,7 +159,7 @@ __global__ void __launch_bounds__(kThreads) weight_encode_kernel(WeightSrc w, We
     uint32_t lo, hi, s;
     quant_block16(f, ts, lo, hi, s);
     uint8_t* base = m < 2 ? d.w13 + slot * d.w13_per_e : d.w2 + slot * d.w2_per_e;
-    const int64_t r = m < 2 ? w13_row(n, m) : n;
+    const int64_t r = m < 2 ? w13_row(n, m, d.gated) : n;
     *reinterpret_cast<uint2*>(base + packed_code_offset(r, kb, K)) = make_uint2(lo, hi);
     base[packed_sf_offset(r, kb, K)] = (uint8_t)s;
   }
@@ -162,7 +174,7 @@ __global__ void __launch_bounds__(kThreads) weight_export_kernel(WeightDst d, in
        b += (int64_t)gridDim.x * blockDim.x) {
     const int64_t n = b / (K / 16), kb = b % (K / 16);
     const uint8_t* base = m < 2 ? d.w13 + slot * d.w13_per_e : d.w2 + slot * d.w2_per_e;
-    const int64_t r = m < 2 ? w13_row(n, m) : n;
+    const int64_t r = m < 2 ? w13_row(n, m, d.gated) : n;
     const uint2 c = *reinterpret_cast<const uint2*>(base + packed_code_offset(r, kb, K));
     const uint8_t s = base[packed_sf_offset(r, kb, K)];
     *reinterpret_cast<uint2*>(codes + n * (K / 2) + kb * 8) = c;
@@ -469,6 +481,26 @@ __global__ void __launch_bounds__(kThreads) permute_rows_kernel(
   }
 }
 
+// BF16 token rows into expert order (the W4A16 layer's A operand): 16-byte vectors.
+__global__ void __launch_bounds__(kThreads) permute_rows_bf16_kernel(
+    const uint4* __restrict__ x, int T, int vpr, int Rt, const int32_t* __restrict__ perm_src,
+    uint4* __restrict__ xb_perm, int32_t* status) {
+  griddep_wait();
+  griddep_launch();
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t nvec = (int64_t)Rt * vpr;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+    const int64_t p = i / vpr;
+    const int v = (int)(i - p * vpr);
+    const int t = __ldg(perm_src + p);
+    if (t < 0 || t >= T) {
+      set_status(status, MOE_ERR_INVALID_ARG);
+      continue;
+    }
+    xb_perm[p * vpr + v] = __ldg(x + (int64_t)t * vpr + v);
+  }
+}
+
 int grid_for(int64_t work, int per_block, int cap) {
   int64_t g = (work + per_block - 1) / per_block;
   if (g < 1) g = 1;
@@ -483,6 +515,7 @@ WeightDst make_dst(const WeightLayout& L, uint8_t* wbuf) {
   d.ts = reinterpret_cast<const float*>(wbuf + L.ts);
   d.w13_per_e = (int64_t)L.w13_per_e;
   d.w2_per_e = (int64_t)L.w2_per_e;
+  d.gated = L.gated ? 1 : 0;
   return d;
 }
 
@@ -501,12 +534,12 @@ int num_sms() {
 
 cudaError_t launch_act_amax(const void* x, int64_t rows, int64_t cols, float* ts, WsHeader* hdr,
                             uint32_t* partials, float* zero_buf, int64_t zero_floats,
-                            cudaStream_t s) {
-  const int64_t nvec = rows * cols / 8;
-  const int g1 = grid_for(nvec, kThreads * 8, kMaxAmaxBlocks);
+                            cudaStream_t s, const float* ts_in) {
+  const int64_t nvec = ts_in ? 0 : rows * cols / 8;
+  const int g1 = grid_for(ts_in ? zero_floats / 4 : nvec, kThreads * 8, kMaxAmaxBlocks);
   return launch_pdl(act_amax_kernel, dim3(g1), dim3(kThreads), 0, s,
                     reinterpret_cast<const uint4*>(x), nvec, hdr, partials, ts,
-                    reinterpret_cast<float4*>(zero_buf), zero_floats / 4);
+                    reinterpret_cast<float4*>(zero_buf), zero_floats / 4, ts_in);
 }
 
 cudaError_t launch_act_encode_perm(const void* x, int T, int H, int k, int E, int shared, int Rt,
@@ -559,7 +592,8 @@ cudaError_t launch_act_quant(const void* x, int64_t rows, int64_t cols, uint8_t*
                              float* ts, WsHeader* hdr, uint32_t* partials, float* zero_buf,
                              int64_t zero_floats, cudaStream_t s) {
   const int64_t n = rows * cols;
-  cudaError_t e = launch_act_amax(x, rows, cols, ts, hdr, partials, zero_buf, zero_floats, s);
+  cudaError_t e = launch_act_amax(x, rows, cols, ts, hdr, partials, zero_buf, zero_floats, s,
+                                  nullptr);
   if (e != cudaSuccess) return e;
   const int64_t nblk = n / 16;
   const int g2 = grid_for(nblk, kThreads, num_sms() * 16);
@@ -581,6 +615,7 @@ cudaError_t launch_weight_quant(const moe_config& c, const WeightLayout& L, cons
   w.E = c.num_experts;
   w.H = c.hidden;
   w.I = c.inter;
+  w.gated = L.gated ? 1 : 0;
   uint32_t* amax = reinterpret_cast<uint32_t*>(wbuf + L.ts);
   cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float) * 4 * L.Et, s);
   if (e != cudaSuccess) return e;
@@ -623,6 +658,15 @@ cudaError_t launch_permute_rows(const uint8_t* xq, const uint8_t* xsf, int T, in
                     dim3(kThreads), 0, s, reinterpret_cast<const uint4*>(xq),
                     reinterpret_cast<const uint32_t*>(xsf), T, H, Rt, E, perm_src, perm_seg,
                     offsets, tile_start, reinterpret_cast<uint4*>(xq_perm), xsf_tiles, status);
+}
+
+cudaError_t launch_permute_rows_bf16(const void* x, int T, int H, int Rt, const int32_t* perm_src,
+                                     void* xb_perm, int32_t* status, cudaStream_t s) {
+  const int vpr = H / 8;
+  const int64_t work = (int64_t)Rt * vpr;
+  return launch_pdl(permute_rows_bf16_kernel, dim3(grid_for(work, kThreads, num_sms() * 8)),
+                    dim3(kThreads), 0, s, reinterpret_cast<const uint4*>(x), T, vpr, Rt, perm_src,
+                    reinterpret_cast<uint4*>(xb_perm), status);
 }
 
 cudaError_t launch_finalize(const float* yacc, void* y, int64_t n, cudaStream_t s) {

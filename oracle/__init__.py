@@ -80,7 +80,12 @@ class MoeArgs(C.Structure):
                 ("router_mode", C.c_int32), ("router_bias", C.c_void_p),
                 ("swiglu_clamp", C.c_int32), ("swiglu_limit", C.c_float),
                 ("act_mode", C.c_int32), ("x_bf16", C.c_void_p), ("hb", C.c_void_p),
-                ("shb", C.c_void_p), ("hf", C.c_void_p)]
+                ("shb", C.c_void_p), ("hf", C.c_void_p), ("act_kind", C.c_int32),
+                ("swiglu_alpha", C.c_float)]
+
+
+# activation of the expert: SwiGLU (optionally clamped), non-gated squared ReLU, gpt-oss SwiGLU
+ACT_KINDS = {"swiglu": 0, "relu2": 1, "swiglu_oai": 2}
 
 
 ROUTER_MODES = {"softmax": 0, "sqrtsoftplus": 1}
@@ -142,6 +147,8 @@ def lib():
                                            C.c_void_p]
         L.orc_swiglu.restype = C.c_float
         L.orc_swiglu.argtypes = [C.c_float, C.c_float, C.c_int, C.c_float]
+        L.orc_activation.restype = C.c_float
+        L.orc_activation.argtypes = [C.c_float, C.c_float, C.c_int, C.c_int, C.c_float, C.c_float]
         L.orc_plan.restype = None
         L.orc_plan.argtypes = [C.c_void_p, C.c_int64, C.c_int, C.c_int] + [C.c_void_p] * 4
         L.orc_moe_forward.restype = C.c_int
@@ -152,7 +159,9 @@ def lib():
     return _libs[_active]
 
 
-def _p(a: np.ndarray):
+def _p(a):
+    if a is None:
+        return None
     assert a.flags["C_CONTIGUOUS"]
     return a.ctypes.data
 
@@ -305,6 +314,15 @@ def swiglu(g: float, u: float, limit=None) -> float:
                                   0.0 if limit is None else float(limit)))
 
 
+def activation(g: float, u: float, kind: str = "swiglu", limit=None, alpha: float = 1.702) -> float:
+    """One feature of h from its gate and up values: "swiglu" silu(g) * u (clamped with limit),
+    "relu2" max(u, 0)^2 (g unused), "swiglu_oai" (clamp(u, -L, L) + 1) * g' * sigmoid(alpha * g'),
+    g' = min(g, L)."""
+    return float(lib().orc_activation(float(g), float(u), ACT_KINDS[kind],
+                                      0 if limit is None else 1,
+                                      0.0 if limit is None else float(limit), float(alpha)))
+
+
 def plan(ids: np.ndarray, E: int):
     ids = np.ascontiguousarray(ids, np.int32)
     T, k = ids.shape
@@ -321,14 +339,18 @@ class QuantExpert:
     """Canonical NVFP4 weights of one expert: gate/up [I,H], down [H,I] codes + scales + ts."""
 
     def __init__(self, codes, sf, ts):
-        self.codes = [np.ascontiguousarray(c, np.uint8) for c in codes]
-        self.sf = [np.ascontiguousarray(s, np.uint8) for s in sf]
+        self.codes = [None if c is None else np.ascontiguousarray(c, np.uint8) for c in codes]
+        self.sf = [None if s is None else np.ascontiguousarray(s, np.uint8) for s in sf]
         self.ts = [float(t) for t in ts]
 
     @classmethod
     def from_bf16(cls, gate, up, down):
+        """gate may be None (a non-gated ReLU2 expert)."""
         cs, ss, ts = [], [], []
         for w in (gate, up, down):
+            if w is None:
+                cs.append(None), ss.append(None), ts.append(0.0)
+                continue
             c, s, t, st = quantize_bf16(w)
             if st != 0:
                 raise ValueError("non-finite weight")
@@ -352,7 +374,7 @@ class QuantExpertMX(QuantExpert):
 
 def moe_forward(xq, xsf, ts_a, logits, experts, k, ts_h=1.0, shared=None, bruteforce=False,
                 want_debug=False, router_mode="softmax", router_bias=None, swiglu_limit=None,
-                act="nvfp4", x_bf16=None):
+                act="nvfp4", x_bf16=None, activation="swiglu", swiglu_alpha=1.702):
     """The layer on quantised activations.  ``experts`` is a list of length E whose entries are
     QuantExpert or None (None only for experts no token routes to); ``shared`` a QuantExpert.
     ``router_mode``/``router_bias``: see router(); ``swiglu_limit``: None for plain SwiGLU, else
@@ -362,7 +384,9 @@ def moe_forward(xq, xsf, ts_a, logits, experts, k, ts_h=1.0, shared=None, brutef
     ``shb``) instead of the NVFP4 codes.  Debug output ``hf``: h in FP32 before its rounding or
     requantisation (routed rows, permuted order).  ``act="mxfp8"`` is the W4A8 layer: x_bf16 is
     quantised to MXFP8, ``experts`` / ``shared`` are QuantExpertMX (MXFP4), h is requantised to
-    MXFP8 (debug ``hq`` [rows, I] E4M3 codes, ``hsf`` [rows, I/32] E8M0 scales)."""
+    MXFP8 (debug ``hq`` [rows, I] E4M3 codes, ``hsf`` [rows, I/32] E8M0 scales).
+    ``activation``: "swiglu" (clamped by swiglu_limit when given), "relu2" (non-gated experts:
+    their gate entries are None) or "swiglu_oai" (limit swiglu_limit, slope swiglu_alpha)."""
     logits = np.ascontiguousarray(logits, np.float32)
     T, E = logits.shape
     if act in ("bf16", "mxfp8"):
@@ -379,11 +403,11 @@ def moe_forward(xq, xsf, ts_a, logits, experts, k, ts_h=1.0, shared=None, brutef
     I = None
     for ex in experts:
         if ex is not None:
-            I = ex.codes[0].shape[0]
+            I = ex.codes[1].shape[0]
             break
     if I is None:
         I = 16
-    Is = shared.codes[0].shape[0] if shared is not None else 0
+    Is = shared.codes[1].shape[0] if shared is not None else 0
     table = (Expert * (E + (1 if shared is not None else 0)))()
     keep = []
     for i, ex in enumerate(list(experts) + ([shared] if shared is not None else [])):
@@ -409,6 +433,10 @@ def moe_forward(xq, xsf, ts_a, logits, experts, k, ts_h=1.0, shared=None, brutef
     a.router_bias = _p(rb) if rb is not None else None
     a.swiglu_clamp = 0 if swiglu_limit is None else 1
     a.swiglu_limit = 0.0 if swiglu_limit is None else float(swiglu_limit)
+    a.act_kind = ACT_KINDS[activation]
+    a.swiglu_alpha = float(swiglu_alpha)
+    if activation == "swiglu_oai" and swiglu_limit is None:
+        raise ValueError("swiglu_oai needs swiglu_limit")
     a.act_mode = ACT_MODES[act]
     a.x_bf16 = _p(xb) if xb is not None else None
     dbg = {}

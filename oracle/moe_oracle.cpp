@@ -28,6 +28,12 @@
 //  * Clamped SwiGLU silu(min(g, L)) * clamp(u, -L, L): "vllm.cpp docs/STATUS.md" (gate clamped
 //    max-only, up clamped both-sided; a limit of 0 zeroes the expert); L = 10 in "nvfp4-megamoe-
 //    kernel ...", section "Nvfp4MoE (Routed Experts)" (swiglu_limit=10.0).
+//  * The other activations of the pages' MoE ("b12x" README, section "What's in here", moe:
+//    "with SiLU/ReLU2/SwiGLU-OAI activations"): ReLU2 is the squared ReLU of a non-gated expert,
+//    h = max(u, 0)^2 with u the up projection alone (no gate matrix); SwiGLU-OAI is the clamped
+//    variant h = (clamp(u, -L, L) + 1) * g' * sigmoid(alpha * g'), g' = min(g, L).  The pages give
+//    only the names; the formulas are the published definitions of these activations (squared
+//    ReLU; the gpt-oss SwiGLU with its alpha = 1.702 and limit 7 as the defaults of the tests).
 //  * SwiGLU silu(g)*u on FP32 accumulators in the GEMM1 epilogue: "nvfp4-megamoe-kernel ...",
 //    section "MoE kernel (FusedSwiGLUScaledGroupedGemmKernel)"; shared expert with weight 1:
 //    section "6. MoE (Mixture of Experts) / Nvfp4SharedExpert".
@@ -501,6 +507,11 @@ typedef struct {
   uint16_t* hb;              // [T*k, I] BF16 h of the routed rows, permuted order (act_mode 1)
   uint16_t* shb;             // [T, I_shared] BF16 h of the shared expert (act_mode 1)
   float* hf;                 // [T*k, I] FP32 h before its rounding or requantisation (any mode)
+  // activation function (zero: SwiGLU, clamped when swiglu_clamp is set)
+  int32_t act_kind;          // 1: ReLU2, non-gated: h = max(u, 0)^2 (the gate matrix is unused
+                             //    and may be null); 2: SwiGLU-OAI with limit swiglu_limit and
+                             //    slope swiglu_alpha
+  float swiglu_alpha;
 } orc_moe_args;
 
 // h = silu(g) * u, with the optional clamp of gate (from above) and up (both sides) first.
@@ -514,18 +525,49 @@ static inline float swiglu(float g, float u, int clamp, float L) {
 
 float orc_swiglu(float g, float u, int clamp, float L) { return swiglu(g, u, clamp, L); }
 
+// Squared ReLU of the up projection (non-gated expert).
+static inline float relu2(float u) { return u > 0.0f ? u * u : 0.0f; }
+
+// SwiGLU-OAI: g' = min(g, L), u' = clamp(u, -L, L), h = (u' + 1) * (g' * sigmoid(alpha * g')),
+// sigmoid(z) = 1 / (1 + exp(-z)), FP32 in that order.
+static inline float swiglu_oai(float g, float u, float L, float alpha) {
+  g = std::min(g, L);
+  u = std::min(std::max(u, -L), L);
+  const float sig = 1.0f / (1.0f + std::exp(-(alpha * g)));
+  return (u + 1.0f) * (g * sig);
+}
+
+// The activation of one feature from its gate and up values (g unused for ReLU2).
+static inline float activation(float g, float u, const orc_moe_args* a) {
+  if (a->act_kind == 1) return relu2(u);
+  if (a->act_kind == 2) return swiglu_oai(g, u, a->swiglu_limit, a->swiglu_alpha);
+  return swiglu(g, u, a->swiglu_clamp, a->swiglu_limit);
+}
+
+float orc_activation(float g, float u, int kind, int clamp, float L, float alpha) {
+  orc_moe_args a{};
+  a.act_kind = kind;
+  a.swiglu_clamp = clamp;
+  a.swiglu_limit = L;
+  a.swiglu_alpha = alpha;
+  return activation(g, u, &a);
+}
+
 // GEMM1 + SwiGLU, then h requantised to NVFP4 (act_mode 0: codes and scales to hq_row /
 // hsf_row) or rounded to BF16 (act_mode 1: bits to hb_row), + GEMM2 for one row: x [H] -> d [H].
 static void expert_row(const float* xr, const float* Wg, const float* Wu, const float* Wd, int H,
-                       int I, float ts_h, int clamp, float L, int act_mode, float* h, float* hhat,
-                       uint8_t* hq_row, uint8_t* hsf_row, uint16_t* hb_row, float* d) {
+                       int I, float ts_h, const orc_moe_args* act, int act_mode, float* h,
+                       float* hhat, uint8_t* hq_row, uint8_t* hsf_row, uint16_t* hb_row,
+                       float* d) {
   for (int n = 0; n < I; ++n) {
-    const float* wg = Wg + (int64_t)n * H;
     const float* wu = Wu + (int64_t)n * H;
     float g = 0.0f, u = 0.0f;
-    for (int c = 0; c < H; ++c) g = g + xr[c] * wg[c];
+    if (act->act_kind != 1) {   // ReLU2 experts have no gate
+      const float* wg = Wg + (int64_t)n * H;
+      for (int c = 0; c < H; ++c) g = g + xr[c] * wg[c];
+    }
     for (int c = 0; c < H; ++c) u = u + xr[c] * wu[c];
-    h[n] = swiglu(g, u, clamp, L);
+    h[n] = activation(g, u, act);
   }
   if (act_mode == 1) {
     for (int n = 0; n < I; ++n) {
@@ -549,16 +591,17 @@ static void expert_row(const float* xr, const float* Wg, const float* Wu, const 
 
 static void dequant_expert(const orc_expert& ex, int H, int I, int act_mode,
                            std::vector<float>& Wg, std::vector<float>& Wu, std::vector<float>& Wd) {
-  Wg.resize((size_t)I * H);
+  const bool gated = ex.codes[0] != nullptr;   // a ReLU2 expert has no gate matrix
+  Wg.resize(gated ? (size_t)I * H : 0);
   Wu.resize((size_t)I * H);
   Wd.resize((size_t)H * I);
   if (act_mode == 2) {  // MXFP4 weights
-    orc_mx_dequantize(ex.codes[0], ex.sf[0], I, H, 1, Wg.data());
+    if (gated) orc_mx_dequantize(ex.codes[0], ex.sf[0], I, H, 1, Wg.data());
     orc_mx_dequantize(ex.codes[1], ex.sf[1], I, H, 1, Wu.data());
     orc_mx_dequantize(ex.codes[2], ex.sf[2], H, I, 1, Wd.data());
     return;
   }
-  orc_dequantize(ex.codes[0], ex.sf[0], ex.ts[0], I, H, Wg.data());
+  if (gated) orc_dequantize(ex.codes[0], ex.sf[0], ex.ts[0], I, H, Wg.data());
   orc_dequantize(ex.codes[1], ex.sf[1], ex.ts[1], I, H, Wu.data());
   orc_dequantize(ex.codes[2], ex.sf[2], ex.ts[2], H, I, Wd.data());
 }
@@ -604,9 +647,9 @@ int orc_moe_forward(const orc_moe_args* a) {
       dequant_expert(a->experts[e], H, I, a->act_mode, Wg, Wu, Wd);
       for (int32_t p = offsets[e]; p < offsets[e + 1]; ++p) {
         const float* xr = xhat.data() + (int64_t)perm_src[p] * H;
-        expert_row(xr, Wg.data(), Wu.data(), Wd.data(), H, I, a->ts_h, a->swiglu_clamp,
-                   a->swiglu_limit, a->act_mode, h.data(), hhat.data(), hq_row.data(),
-                   hsf_row.data(), hb_row.data(), D.data() + (int64_t)p * H);
+        expert_row(xr, Wg.data(), Wu.data(), Wd.data(), H, I, a->ts_h, a, a->act_mode,
+                   h.data(), hhat.data(), hq_row.data(), hsf_row.data(), hb_row.data(),
+                   D.data() + (int64_t)p * H);
         if (a->act_mode != 1 && a->hq) std::memcpy(a->hq + (int64_t)p * hq_w, hq_row.data(), hq_w);
         if (a->act_mode != 1 && a->hsf) std::memcpy(a->hsf + (int64_t)p * hs_w, hsf_row.data(), hs_w);
         if (a->act_mode == 1 && a->hb) std::copy(hb_row.begin(), hb_row.begin() + I, a->hb + (int64_t)p * I);
@@ -628,9 +671,9 @@ int orc_moe_forward(const orc_moe_args* a) {
       std::vector<uint16_t> hb_row(Imax);
 #pragma omp for schedule(dynamic, 4)
       for (int64_t t = 0; t < T; ++t) {
-        expert_row(xhat.data() + t * H, Wg.data(), Wu.data(), Wd.data(), H, Is, a->ts_h,
-                   a->swiglu_clamp, a->swiglu_limit, a->act_mode, h.data(), hhat.data(),
-                   hq_row.data(), hsf_row.data(), hb_row.data(), S.data() + t * H);
+        expert_row(xhat.data() + t * H, Wg.data(), Wu.data(), Wd.data(), H, Is, a->ts_h, a,
+                   a->act_mode, h.data(), hhat.data(), hq_row.data(), hsf_row.data(),
+                   hb_row.data(), S.data() + t * H);
         if (a->act_mode != 1 && a->shq) std::memcpy(a->shq + t * shq_w, hq_row.data(), shq_w);
         if (a->act_mode != 1 && a->shsf) std::memcpy(a->shsf + t * shs_w, hsf_row.data(), shs_w);
         if (a->act_mode == 1 && a->shb) std::copy(hb_row.begin(), hb_row.begin() + Is, a->shb + t * Is);
@@ -678,9 +721,10 @@ int orc_moe_forward_bruteforce(const orc_moe_args* a) {
   auto run_expert = [&](const orc_expert& ex, int Ie) {
     for (int n = 0; n < Ie; ++n) {
       float g = 0.0f, u = 0.0f;
-      for (int c = 0; c < H; ++c) g = g + xr[c] * wval(ex, 0, n, c, H);
+      if (a->act_kind != 1)
+        for (int c = 0; c < H; ++c) g = g + xr[c] * wval(ex, 0, n, c, H);
       for (int c = 0; c < H; ++c) u = u + xr[c] * wval(ex, 1, n, c, H);
-      h[n] = swiglu(g, u, a->swiglu_clamp, a->swiglu_limit);
+      h[n] = activation(g, u, a);
     }
     if (a->act_mode == 1) {              // W4A16: h in BF16
       for (int n = 0; n < Ie; ++n) hhat[n] = orc_bf16_to_f32(orc_f32_to_bf16(h[n]));

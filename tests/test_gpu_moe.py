@@ -132,8 +132,9 @@ def test_repeat_calls_bit_identical_on_decode_path(moe):
 
 def test_repeat_calls_general_path_within_rounding(moe):
     """Large batches add the k routed contributions (and the shared one) into the token row with
-    FP32 reductions in arbitrary order, so two calls may differ by FP32 rounding, which the final
-    BF16 rounding turns into at most one BF16 step, and only for rare values."""
+    FP32 reductions in arbitrary order, so two calls may differ by the FP32 rounding of a sum of
+    k + 1 terms, at most (k + 1) * 2^-24 times the sum of their magnitudes (taken here as 4x the
+    output's maximum), plus one BF16 step of the result; and only for few values."""
     cs = synth.custom_config("general_repeat", 3000, 512, 16, 4, 256, shared_inter=256,
                              config_id=171)
     cfg = moe.make_config(cs.experts, cs.hidden, cs.inter, cs.top_k, shared_inter=256,
@@ -144,11 +145,13 @@ def test_repeat_calls_general_path_within_rounding(moe):
     x = synth.gen_x(cs, 3000, device="cuda")
     lg = synth.gen_logits(cs, 3000, device="cuda")
     ys = [moe.run(cfg, wbuf, x, lg).float() for _ in range(3)]
+    scale = float(ys[0].abs().max())
     for y in ys[1:]:
         d = (y - ys[0]).abs()
         mag = torch.maximum(y.abs(), ys[0].abs())
         ulp = torch.pow(2.0, torch.floor(torch.log2(torch.clamp(mag, min=1e-30))) - 7)
-        assert bool((d <= ulp).all()), float((d / ulp).max())
+        bound = ulp + (cs.top_k + 1) * 2.0 ** -24 * 4 * scale
+        assert bool((d <= bound).all()), float((d / bound).max())
         assert float((d > 0).float().mean()) <= 1e-2
 
 
@@ -199,3 +202,25 @@ def test_cuda_graph_replay_matches_eager(moe):
         assert torch.equal(y, y_eager)      # the decode path is deterministic
         ms = timer.stage_ms()
         assert all(v >= 0 for v in ms.values()) and sum(ms.values()) > 0
+
+
+def test_forced_timeout_is_reported_and_the_next_call_is_clean(moe):
+    """A wait that runs out ends the call with MOE_ERR_DEVICE_TIMEOUT in the device status and
+    leaves the context usable.  The hook keeps the decode prologue from raising its plan-ready
+    flag, so the grouped-GEMM launch's bounded wait for it (about 2 s) expires before any copy is
+    issued; the next call without the hook must be green and give the same bits as before."""
+    cs = synth.CONFIGS["decode"]
+    T = 8
+    cfg = moe.make_config(cs.experts, cs.hidden, cs.inter, cs.top_k, max_tokens=T)
+    wg, wu, wd = synth.gen_all_experts(cs, device="cuda")
+    wbuf = moe.quantize_weights(cfg, wg, wu, wd)
+    x = synth.gen_x(cs, T, device="cuda")
+    lg = synth.gen_logits(cs, T, device="cuda")
+    ws = torch.empty(moe.workspace_size(cfg, T), dtype=torch.uint8, device="cuda")
+    y0 = moe.run(cfg, wbuf, x, lg, workspace=ws).clone()
+    assert moe.last_device_status(ws) == 0
+    moe.run(cfg, wbuf, x, lg, workspace=ws, inject=moe.MOE_INJECT_NO_PLAN_FLAG)
+    assert moe.last_device_status(ws) == -5           # MOE_ERR_DEVICE_TIMEOUT
+    y1 = moe.run(cfg, wbuf, x, lg, workspace=ws)
+    assert moe.last_device_status(ws) == 0
+    assert torch.equal(y0, y1)

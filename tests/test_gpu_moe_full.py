@@ -16,7 +16,7 @@ import torch
 
 import oracle
 import synth
-from parity import assert_h_close, assert_y_close
+from parity import assert_h_close, assert_y_close_h_aware
 
 pytestmark = pytest.mark.gpu
 
@@ -110,13 +110,36 @@ def test_full_size_every_tile(moe, name):
     sho = oracle.QuantExpert.from_bf16(*[s.cpu() for s in sh]) if sh is not None else None
     y_ref, od = oracle.moe_forward(xq[toks], xsf[toks], ts_a, lg[toks], experts, k, shared=sho,
                                    want_debug=True)
-    yg = y.float().cpu().numpy()[toks]
-    assert_y_close(yg, oracle.bf16_bits_to_f32(y_ref))
     # intermediate rows of the compared tokens' assignments (and shared-expert rows)
     rows_gpu = np.array([inv[t * k + j] for t in toks for j in range(k)])
     rows_ref = np.array([od["inv"][i * k + j] for i in range(len(toks)) for j in range(k)])
     assert_h_close(g["hq"][rows_gpu], g["hsf"][rows_gpu], od["hq"][rows_ref], od["hsf"][rows_ref])
+    R = T * k
     if sh is not None:
-        R = T * k
         assert_h_close(g["hq"][R + toks], g["hsf"][R + toks], od["shq"], od["shsf"])
-    print(f"{name}: {len(toks)} tokens cover {ntiles} tiles, {len(used)} experts")
+    # the output, allowing for the h codes that differ by one step
+    wd_cache = {}
+
+    def down(e):
+        def get():
+            if e not in wd_cache:
+                ex = sho if e < 0 else experts[e]
+                wd_cache[e] = oracle.dequantize(ex.codes[2], ex.sf[2], ex.ts[2])
+            return wd_cache[e]
+        return get
+
+    rows = []
+    for i, t in enumerate(toks):
+        slots = []
+        for j in range(k):
+            pg, pr = inv[t * k + j], od["inv"][i * k + j]
+            slots.append((od["w"][i, j], g["hq"][pg], g["hsf"][pg], od["hq"][pr], od["hsf"][pr],
+                          down(int(ids[t, j]))))
+        if sh is not None:
+            slots.append((1.0, g["hq"][R + t], g["hsf"][R + t], od["shq"][i], od["shsf"][i],
+                          down(-1)))
+        rows.append(slots)
+    yg = y.float().cpu().numpy()[toks]
+    rel, mx, nflip = assert_y_close_h_aware(yg, oracle.bf16_bits_to_f32(y_ref), rows)
+    print(f"{name}: {len(toks)} tokens cover {ntiles} tiles, {len(used)} experts; "
+          f"rel_l2 {rel:.2e}, max/rms {mx:.2e}, {nflip} tokens with a differing h block")

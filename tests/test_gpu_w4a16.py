@@ -1,0 +1,127 @@
+"""GPU parity of the W4A16 layer (BF16 activations as they are, NVFP4 weights decoded to BF16 in
+the GEMMs, h rounded to BF16; "b12x" README, section "What's in here", moe: "W4A16 (BF16
+activations, inline FP4 weight dequant - no activation-scale math)") through the C ABI against
+the oracle's act_mode 1.
+
+Bit-exact: router ids, counts, offsets, permutation.  The BF16 h: at most 0.1% of its values
+differ from the oracle's, each by one BF16 step (the tensor core sums the products in its own
+order, so a value within rounding noise of a BF16 rounding boundary has two correct roundings).
+The output: relative L2 <= 5e-3 and max |err| <= 3e-2 * RMS."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from parity import H_CODE_FRAC, assert_y_close, bf16_to_np_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import nvfp4_mixture_experts_softmax_gb300 as m
+    m.lib()
+    return m
+
+
+def bf16_rank(bits):
+    """BF16 bit patterns -> integers in the order of the values (+0 and -0 both 0)."""
+    b = bits.astype(np.int32)
+    return np.where(b & 0x8000, -(b & 0x7FFF), b & 0x7FFF)
+
+
+def assert_hb_close(gpu_bits, ref_bits):
+    d = np.abs(bf16_rank(gpu_bits) - bf16_rank(ref_bits))
+    frac = float(np.mean(d > 0)) if d.size else 0.0
+    assert frac <= H_CODE_FRAC and (d.max() if d.size else 0) <= 1, \
+        f"h (BF16): {frac:.2e} differ, max step {d.max()}"
+    return frac
+
+
+def check_w4a16(moe, cs, T, activation="swiglu", limit=None, sample=None):
+    dev = "cuda"
+    k = cs.top_k
+    x = synth.gen_x(cs, T, device=dev)
+    logits = synth.gen_logits(cs, T, device=dev)
+    wg, wu, wd = synth.gen_all_experts(cs, device=dev)
+    sh = synth.gen_shared(cs, device=dev) if cs.shared_inter else None
+    gated = activation != "relu2"
+    cfg = moe.make_config(cs.experts, cs.hidden, cs.inter, k, shared_inter=cs.shared_inter,
+                          max_tokens=T, activation=activation, swiglu_limit=limit,
+                          precision="w4a16")
+    wbuf = moe.quantize_weights(cfg, wg if gated else None, wu, wd,
+                                shared=None if sh is None else (sh[0] if gated else None, sh[1], sh[2]))
+    ws = torch.empty(moe.workspace_size(cfg, T), dtype=torch.uint8, device=dev)
+    y, dbg = moe.run(cfg, wbuf, x, logits, workspace=ws, debug=True)
+    assert moe.last_device_status(ws) == 0
+    g = {n: t.cpu() for n, t in dbg.items()}
+    lg = logits.cpu().numpy()
+    ids, w = oracle.router(lg, k)
+    counts, offsets, perm_src, inv = oracle.plan(ids, cs.experts)
+    assert np.array_equal(g["topk_ids"].numpy(), ids)
+    assert np.array_equal(g["offsets"].numpy(), offsets)
+    assert np.array_equal(g["perm_src"].numpy(), perm_src) and np.array_equal(g["inv"].numpy(), inv)
+    toks = np.arange(T) if sample is None else sample
+    experts = [None] * cs.experts
+    for e in np.unique(ids[toks]):
+        experts[e] = oracle.QuantExpert.from_bf16(wg[e].cpu() if gated else None, wu[e].cpu(),
+                                                  wd[e].cpu())
+    sho = None
+    if sh is not None:
+        sho = oracle.QuantExpert.from_bf16(sh[0].cpu() if gated else None, sh[1].cpu(), sh[2].cpu())
+    xc = x.cpu()[toks]
+    y_ref, od = oracle.moe_forward(None, None, None, lg[toks], experts, k, shared=sho,
+                                   want_debug=True, act="bf16", x_bf16=xc, activation=activation,
+                                   swiglu_limit=limit)
+    hb = bf16_to_np_bits(g["hb"])
+    rows_gpu = np.array([inv[t * k + j] for t in toks for j in range(k)])
+    rows_ref = np.array([od["inv"][i * k + j] for i in range(len(toks)) for j in range(k)])
+    assert_hb_close(hb[rows_gpu], od["hb"][rows_ref])
+    if sh is not None:
+        assert_hb_close(hb[T * k + toks], od["shb"])
+    assert_y_close(y.float().cpu().numpy()[toks], oracle.bf16_bits_to_f32(y_ref))
+
+
+@pytest.mark.parametrize("T", [1, 8, 64])
+def test_w4a16_decode(moe, T):
+    check_w4a16(moe, synth.CONFIGS["decode"], T)
+
+
+def test_w4a16_tiny(moe):
+    check_w4a16(moe, synth.CONFIGS["tiny"], 16)
+
+
+@pytest.mark.parametrize("activation,limit", [("swiglu", None), ("relu2", None),
+                                              ("swiglu_oai", 7.0), ("swiglu", 0.5)])
+def test_w4a16_shared_expert_and_activations(moe, activation, limit):
+    cs = synth.custom_config("w4a16_sh", 300, 512, 16, 4, 256, shared_inter=256, config_id=160)
+    check_w4a16(moe, cs, 300, activation, limit)
+
+
+def test_w4a16_one_expert_many_tiles(moe):
+    """Every token on one expert (k = 1 of E = 2 with a planted logit): five 128-row tiles, the
+    last one ragged."""
+    cs = synth.custom_config("w4a16_pop", 600, 256, 2, 1, 256, config_id=161)
+    check_w4a16(moe, cs, 600)
+
+
+def test_w4a16_prefill_size_sampled(moe):
+    cs = synth.CONFIGS["prefill"]
+    T = cs.tokens[0]
+    rng = np.random.default_rng(5)
+    sample = np.sort(np.concatenate([[0, T - 1], rng.choice(np.arange(1, T - 1), 30, replace=False)]))
+    check_w4a16(moe, cs, T, sample=sample)
+
+
+def test_w4a16_refuses_quantised_input(moe):
+    cs = synth.CONFIGS["tiny"]
+    cfg = moe.make_config(cs.experts, cs.hidden, cs.inter, cs.top_k, precision="w4a16")
+    wg, wu, wd = synth.gen_all_experts(cs, device="cuda")
+    wbuf = moe.quantize_weights(cfg, wg, wu, wd)
+    x = synth.gen_x(cs, 16, device="cuda")
+    xq, xsf, ts = moe.quantize_act(x)
+    with pytest.raises(RuntimeError, match="INVALID_ARG"):
+        moe.run(cfg, wbuf, None, synth.gen_logits(cs, 16, device="cuda"), quantized=(xq, xsf, ts))

@@ -150,3 +150,109 @@ def test_swiglu_zero_limit_is_zero():
     for g in (-3.0, -0.1, 0.0, 0.1, 50.0):
         for u in (-2.0, 0.0, 9.0):
             assert oracle.swiglu(g, u, 0.0) == 0.0
+
+
+# ---- the other activations of the pages' MoE ("b12x" README, "What's in here", moe: "with
+# SiLU/ReLU2/SwiGLU-OAI activations"): squared ReLU of a non-gated expert, gpt-oss SwiGLU
+
+def test_relu2_closed_forms():
+    for u, want in ((3.0, 9.0), (0.5, 0.25), (-2.0, 0.0), (0.0, 0.0), (-0.0, 0.0), (1e-20, 0.0)):
+        for g in (-7.0, 0.0, 11.0):                              # the gate plays no part
+            assert oracle.activation(g, u, "relu2") == np.float32(np.float32(u) * np.float32(u)
+                                                                  if u > 0 else 0.0)
+            assert oracle.activation(g, u, "relu2") == want or u == 1e-20
+
+
+def _oai64(g, u, L, a):
+    g = min(g, L)
+    u = min(max(u, -L), L)
+    return (u + 1.0) * g / (1.0 + math.exp(-a * g))
+
+
+@pytest.mark.parametrize("g,u", [(0.3, 0.2), (-2.0, 1.5), (3.0, -0.5), (12.0, 3.0), (2.0, 9.0),
+                                 (2.0, -9.0), (-30.0, 2.0), (6.99, 6.99)])
+def test_swiglu_oai_closed_forms(g, u):
+    L, a = 7.0, 1.702
+    want = _oai64(g, u, L, a)
+    got = oracle.activation(g, u, "swiglu_oai", L, a)
+    # the rounding of alpha * g' moves exp(-alpha * g') by |alpha * g'| * 2^-24 relative
+    rel = (abs(a * min(g, L)) + 8) * 2.0 ** -24
+    assert abs(got - want) <= rel * max(abs(want), 1e-30) + 1e-30
+
+
+def test_swiglu_oai_special_values():
+    L, a = 7.0, 1.702
+    for g in (-3.0, 0.5, 40.0):
+        assert oracle.activation(g, -1.0, "swiglu_oai", L, a) == 0.0    # u + 1 = 0
+    for u in (-5.0, 0.0, 5.0):
+        assert oracle.activation(0.0, u, "swiglu_oai", L, a) == 0.0     # g = 0
+    # the gate is clamped from above only, the up value on both sides
+    assert oracle.activation(100.0, 2.0, "swiglu_oai", L, a) == \
+        oracle.activation(L, 2.0, "swiglu_oai", L, a)
+    assert oracle.activation(1.0, 100.0, "swiglu_oai", L, a) == \
+        oracle.activation(1.0, L, "swiglu_oai", L, a)
+    assert oracle.activation(1.0, -100.0, "swiglu_oai", L, a) == \
+        oracle.activation(1.0, -L, "swiglu_oai", L, a)
+    assert oracle.activation(-100.0, 2.0, "swiglu_oai", L, a) != \
+        oracle.activation(-L, 2.0, "swiglu_oai", L, a)
+
+
+@pytest.fixture(scope="module")
+def act_layer():
+    """A layer with a shared expert whose expert weights serve all three activations (the ReLU2
+    experts drop their gate matrix)."""
+    cs = synth.custom_config("act_variants", 12, 256, 6, 2, 256, shared_inter=256, config_id=172)
+    x = synth.gen_x(cs, 12)
+    lg = synth.gen_logits(cs, 12).numpy()
+    ws = [synth.gen_expert(cs, e) for e in range(cs.experts)]
+    sh = synth.gen_shared(cs)
+    xq, xsf, ts_a, st = oracle.quantize_bf16(x)
+    gated = [oracle.QuantExpert.from_bf16(*w) for w in ws]
+    plain = [oracle.QuantExpert.from_bf16(None, w[1], w[2]) for w in ws]
+    return dict(cs=cs, xq=xq, xsf=xsf, ts=ts_a, lg=lg, gated=gated, plain=plain,
+                sh_g=oracle.QuantExpert.from_bf16(*sh), sh_p=oracle.QuantExpert.from_bf16(None, *sh[1:]))
+
+
+def _act_run(L, kind, bruteforce=False, debug=False):
+    ex, sh = (L["plain"], L["sh_p"]) if kind == "relu2" else (L["gated"], L["sh_g"])
+    lim = 7.0 if kind == "swiglu_oai" else None
+    return oracle.moe_forward(L["xq"], L["xsf"], L["ts"], L["lg"], ex, L["cs"].top_k, shared=sh,
+                              activation=kind, swiglu_limit=lim, bruteforce=bruteforce,
+                              want_debug=debug)
+
+
+@pytest.mark.parametrize("kind", ["relu2", "swiglu_oai"])
+def test_activation_variants_permuted_equals_brute_force(act_layer, kind):
+    assert np.array_equal(_act_run(act_layer, kind), _act_run(act_layer, kind, bruteforce=True))
+
+
+@pytest.mark.parametrize("kind", ["relu2", "swiglu_oai"])
+def test_activation_variants_h_against_float64(act_layer, kind):
+    """The FP32 h of every routed row equals a float64 evaluation of the activation's formula on
+    the decoded operands within the FP32 summation bound of its dot products: a gated ReLU2, an
+    unsquared one, or swapped gate and up values of SwiGLU-OAI all fail here."""
+    L = act_layer
+    cs = L["cs"]
+    _, d = _act_run(L, kind, debug=True)
+    xh = oracle.dequantize(L["xq"], L["xsf"], L["ts"]).astype(np.float64)
+    ex = L["plain"] if kind == "relu2" else L["gated"]
+    H, k = cs.hidden, cs.top_k
+    for p in range(cs.tokens[0] * k):
+        t = d["perm_src"][p]
+        e = d["ids"].reshape(-1)[[i for i in range(len(d["inv"])) if d["inv"][i] == p][0]]
+        wu = oracle.dequantize(ex[e].codes[1], ex[e].sf[1], ex[e].ts[1]).astype(np.float64)
+        u = wu @ xh[t]
+        bu = H * 2.0 ** -24 * (np.abs(wu) @ np.abs(xh[t]))
+        if kind == "relu2":
+            want = np.maximum(u, 0) ** 2
+            bound = 2 * np.abs(u) * bu + bu ** 2 + 2 ** -23 * want
+        else:
+            wg = oracle.dequantize(ex[e].codes[0], ex[e].sf[0], ex[e].ts[0]).astype(np.float64)
+            g = wg @ xh[t]
+            bg = H * 2.0 ** -24 * (np.abs(wg) @ np.abs(xh[t]))
+            want = np.array([_oai64(a, b, 7.0, 1.702) for a, b in zip(g, u)])
+            # |d h / d g| <= (|u'| + 1) * 1.2 and |d h / d u| <= |g'| sigmoid: first-order bound
+            gc = np.minimum(g, 7.0)
+            uc = np.clip(u, -7.0, 7.0)
+            bound = (np.abs(uc) + 1) * 1.2 * bg + np.abs(gc) * bu + 2 ** -20 * np.abs(want)
+        assert np.all(np.abs(d["hf"][p] - want) <= bound + 1e-30), (kind, p)
