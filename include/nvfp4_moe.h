@@ -103,6 +103,17 @@ typedef struct {
  * activation flag may be combined with it.  The weights are the same NVFP4 buffer.  In the
  * debug struct, hq / hsf are not written and hb receives h. */
 #define MOE_FLAG_ACT_BF16 16u
+/* W4A8 activation precision ("b12x" README, section "DeepSeek V4 Flash 0731 MoE reproduction":
+ * "MXFP4 E8M0/K32 weights, MXFP8 activations"): the weights are MXFP4 (E2M1 codes, one E8M0
+ * scale 2^(byte - 127) per 32 along K, no tensor scale) instead of NVFP4; x is quantised to
+ * MXFP8 (E4M3 codes, one E8M0 scale per 32, no tensor scale) and h is requantised to MXFP8.  The
+ * scale byte of a block is 2^(floor(log2 max|v|) - emax), emax = 2 for E2M1 and 8 for E4M3,
+ * clamped to [0, 254] (0 for an all-zero block); elements are v / scale rounded to nearest even
+ * and saturated.  The GEMMs decode both operands exactly to BF16 and run on the BF16 tensor cores.
+ * moe_weights_export returns E8M0 scales [N, K/32] (and ts = 1); in the debug struct xq / xsf
+ * receive the MXFP8 codes [T, H] and scales [T, H/32] of x, hq / hsf those of h ([rows, I],
+ * [rows, I/32]) and hb its decoded BF16 values.  Not combinable with MOE_FLAG_ACT_BF16. */
+#define MOE_FLAG_ACT_MXFP8 32u
 
 /* Optional device buffers that receive the layer's intermediates (any field may be NULL). */
 typedef struct {

@@ -119,6 +119,7 @@ FLAG_SWIGLU_CLAMP = 2
 FLAG_ACT_RELU2 = 4
 FLAG_ACT_SWIGLU_OAI = 8
 FLAG_ACT_BF16 = 16
+FLAG_ACT_MXFP8 = 32
 ACTIVATIONS = ("swiglu", "relu2", "swiglu_oai")
 
 
@@ -130,8 +131,9 @@ def make_config(num_experts, hidden, inter, top_k, shared_inter=0, h_tensor_scal
     normalised unbiased scores).  activation: "swiglu" (silu(g)*u, or with swiglu_limit L
     silu(min(g, L)) * clamp(u, -L, L)), "relu2" (non-gated experts, max(u, 0)^2) or "swiglu_oai"
     ((clamp(u, -L, L) + 1) * g' * sigmoid(alpha * g'), g' = min(g, L); needs swiglu_limit).
-    precision: "nvfp4" (activations and h quantised to NVFP4) or "w4a16" (BF16 activations as
-    they are, weights decoded to BF16 in the GEMMs, h rounded to BF16)."""
+    precision: "nvfp4" (activations and h quantised to NVFP4), "w4a16" (BF16 activations as
+    they are, weights decoded to BF16 in the GEMMs, h rounded to BF16) or "w4a8" (MXFP4 weights,
+    MXFP8 activations and h)."""
     if router not in ("softmax", "sqrtsoftplus"):
         raise ValueError(f"unknown router {router!r}")
     if activation not in ACTIVATIONS:
@@ -147,6 +149,8 @@ def make_config(num_experts, hidden, inter, top_k, shared_inter=0, h_tensor_scal
         flags |= FLAG_SWIGLU_CLAMP
     if precision == "w4a16":
         flags |= FLAG_ACT_BF16
+    elif precision == "w4a8":
+        flags |= FLAG_ACT_MXFP8
     elif precision != "nvfp4":
         raise ValueError(f"unknown precision {precision!r}")
     return MoeConfig(num_experts, hidden, inter, top_k, shared_inter, h_tensor_scale, max_tokens,
@@ -188,11 +192,13 @@ def set_router_bias(cfg: MoeConfig, wbuf: torch.Tensor, bias: torch.Tensor) -> N
 
 
 def weights_export(cfg: MoeConfig, wbuf, expert: int, matrix: int, stream=None):
-    """Canonical (codes [N,K/2], sf [N,K/16], ts [1]) of one expert matrix (-1 = shared)."""
+    """Canonical (codes [N,K/2], sf [N,K/16] E4M3 - or [N,K/32] E8M0 for a W4A8 layer's MXFP4
+    weights - and ts [1]) of one expert matrix (-1 = shared)."""
     N, K = (cfg.inter, cfg.hidden) if matrix < 2 else (cfg.hidden, cfg.inter)
     dev = wbuf.device
     codes = torch.empty(N, K // 2, dtype=torch.uint8, device=dev)
-    sf = torch.empty(N, K // 16, dtype=torch.uint8, device=dev)
+    sf = torch.empty(N, K // (32 if cfg.flags & FLAG_ACT_MXFP8 else 16), dtype=torch.uint8,
+                     device=dev)
     ts = torch.empty(1, dtype=torch.float32, device=dev)
     _check(lib().moe_weights_export(C.byref(cfg), _ptr(wbuf), expert, matrix, _ptr(codes), _ptr(sf),
                                     _ptr(ts), _stream(stream)), "moe_weights_export")
@@ -339,6 +345,14 @@ def run(cfg: MoeConfig, wbuf, x, logits, k=None, y=None, workspace=None, debug=F
         if cfg.flags & FLAG_ACT_BF16:        # nothing is quantised; h stays BF16 (hb)
             for n in ("hq", "hsf", "xq", "xsf", "ts_a"):
                 del dbg[n]
+            dbg["hb"] = torch.empty(Rt, I, dtype=torch.bfloat16, device=dev)
+        if cfg.flags & FLAG_ACT_MXFP8:       # MXFP8 codes + E8M0 scales of x and h, decoded h
+            del dbg["ts_a"]
+            dbg["xq"] = torch.empty(T, H, dtype=torch.uint8, device=dev)
+            dbg["xsf"] = torch.empty(T, H // 32, dtype=torch.uint8, device=dev)
+            dbg["hq"] = torch.empty(Rt, I, dtype=torch.uint8, device=dev)
+            dbg["hsf"] = torch.empty(Rt, I // 32, dtype=torch.uint8, device=dev)
+            dbg["hb"] = torch.empty(Rt, I, dtype=torch.bfloat16, device=dev)
             dbg["hb"] = torch.empty(Rt, I, dtype=torch.bfloat16, device=dev)
         dbg_c = MoeDebug(*[dbg[n].data_ptr() if n in dbg else None
                            for n, _ in MoeDebug._fields_[:11]],

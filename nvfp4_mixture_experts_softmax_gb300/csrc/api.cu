@@ -18,8 +18,10 @@ inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 int check_cfg(const moe_config* c) {
   if (!c) return MOE_ERR_INVALID_ARG;
   const uint32_t acts = MOE_FLAG_SWIGLU_CLAMP | MOE_FLAG_ACT_RELU2 | MOE_FLAG_ACT_SWIGLU_OAI;
-  if ((c->flags & ~(MOE_FLAG_ROUTER_SQRTSOFTPLUS | acts | MOE_FLAG_ACT_BF16)) != 0u)
+  if ((c->flags & ~(MOE_FLAG_ROUTER_SQRTSOFTPLUS | acts | MOE_FLAG_ACT_BF16 |
+                    MOE_FLAG_ACT_MXFP8)) != 0u)
     return MOE_ERR_INVALID_ARG;
+  if ((c->flags & MOE_FLAG_ACT_BF16) && (c->flags & MOE_FLAG_ACT_MXFP8)) return MOE_ERR_INVALID_ARG;
   const uint32_t act = c->flags & acts;
   if (act & (act - 1u)) return MOE_ERR_INVALID_ARG;   // at most one activation
   if ((act & (MOE_FLAG_SWIGLU_CLAMP | MOE_FLAG_ACT_SWIGLU_OAI)) &&
@@ -107,6 +109,7 @@ int moe_weights_export(const moe_config* cfg, const void* wbuf, int32_t expert, 
   if (!wbuf || !codes || !sf || !ts) return MOE_ERR_INVALID_ARG;
   if (matrix < 0 || matrix > 2) return MOE_ERR_INVALID_ARG;
   if (matrix == 0 && !gated_experts(*cfg)) return MOE_ERR_INVALID_ARG;   // no gate matrix
+  // (sf receives [N, K/16] E4M3 scales, or [N, K/32] E8M0 scales for MXFP4 weights)
   int slot;
   if (expert == -1) {
     if (cfg->shared_inter <= 0) return MOE_ERR_INVALID_ARG;
@@ -324,7 +327,11 @@ int run_layer(const moe_config* cfg, const void* wbuf, const void* x, const uint
     if (e == cudaSuccess) e = launch_plan(pa, s);
     if (e == cudaSuccess) e = mark(2);
     if (e == cudaSuccess)
-      e = launch_permute_rows_bf16(x, T, H, L.Rt, i32(L.perm_src), ws + L.xb_perm, &hdr->status, s);
+      e = L.mx ? launch_act_mx_encode_perm(x, T, H, k, shared, L.Rt, i32(L.inv), ws + L.xq8,
+                                           ws + L.xq8 + (size_t)T * H, ws + L.xb_perm,
+                                           &hdr->status, s)
+               : launch_permute_rows_bf16(x, T, H, L.Rt, i32(L.perm_src), ws + L.xb_perm,
+                                          &hdr->status, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     const int nseg = E + shared;
     const int64_t mtiles = ((int64_t)L.Rt + (int64_t)nseg * (kBM - 1)) / kBM;
@@ -346,6 +353,9 @@ int run_layer(const moe_config* cfg, const void* wbuf, const void* x, const uint
     g.swiglu_limit = cfg->swiglu_limit;
     g.swiglu_alpha = cfg->swiglu_alpha;
     g.hb = ws + L.hb;
+    g.mx = L.mx ? 1 : 0;
+    g.hq8 = ws + L.hq8;
+    g.hsf8 = ws + L.hq8 + (size_t)L.Rt * I;
     g.out_rows = L.Rt;
     g.y_rows = T;
     g.max_items = (int)std::min<int64_t>(mtiles * (g.N / kBN), INT32_MAX);
@@ -380,6 +390,12 @@ int run_layer(const moe_config* cfg, const void* wbuf, const void* x, const uint
       cp(debug->perm_src, L.perm_src, 4 * R);
       cp(debug->inv, L.inv, 4 * R);
       cp(debug->hb, L.hb, Rt * I * 2);
+      if (L.mx) {   // MXFP8 codes and E8M0 scales of x and h
+        cp(debug->xq, L.xq8, (size_t)T * H);
+        cp(debug->xsf, L.xq8 + (size_t)T * H, (size_t)T * H / 32);
+        cp(debug->hq, L.hq8, Rt * I);
+        cp(debug->hsf, L.hq8 + Rt * I, Rt * I / 32);
+      }
       if (e != cudaSuccess) return MOE_ERR_CUDA;
     }
     return MOE_OK;
@@ -587,7 +603,8 @@ int run_layer(const moe_config* cfg, const void* wbuf, const void* x, const uint
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
   // 5. BF16 output (small batches: sum each token's stored rows in slot order)
-  e = L.small ? launch_finalize_gather(f32(L.obuf), i32(L.inv), T, k, H, shared, y, s)
+  e = L.small ? launch_finalize_gather(f32(L.obuf), i32(L.inv), T, k, H, shared, y, s,
+                                       L.decode ? i32(L.ready) + L.dtiles : nullptr)
               : launch_finalize(f32(L.yacc), y, (int64_t)T * H, s);
   if (e == cudaSuccess) e = mark(5);
   if (e != cudaSuccess) return MOE_ERR_CUDA;

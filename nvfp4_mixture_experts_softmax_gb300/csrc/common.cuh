@@ -39,6 +39,21 @@ __device__ __forceinline__ uint32_t f32_to_e4m3(float v) {
   return r & 0xFFu;
 }
 
+// Two FP32 values -> two E4M3 codes in the low 16 bits, the first value in the low byte.
+__device__ __forceinline__ uint32_t f32_to_e4m3x2(float v0, float v1) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(v1), "f"(v0));
+  return r;
+}
+
+// Two E4M3 codes (low byte first) -> two FP32 values (exact).
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t b2) {
+  uint32_t h2;
+  const uint16_t in = (uint16_t)(b2 & 0xFFFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+  return __half22float2(*reinterpret_cast<const __half2*>(&h2));
+}
+
 __device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
   uint32_t h2;
   uint16_t in = (uint16_t)(b & 0xFFu);
@@ -135,6 +150,30 @@ __device__ __forceinline__ void quant_block16_fast(const float* x, float ts, flo
 }
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
+
+// ---- MX formats (one E8M0 scale per 32 elements, value 2^(byte - 127)) ----
+// Scale byte of a block whose largest magnitude is amax, for elements whose largest power of two
+// is 2^emax (E2M1: 2, E4M3: 8): 2^(floor(log2 amax) - emax), the byte clamped to [0, 254]; 0 for
+// an all-zero block.  floor(log2) is read off the exponent field (normal) or the leading bit of
+// the fraction (subnormal), so it is exact.
+__device__ __forceinline__ uint32_t mx_scale_byte(float amax, int emax) {
+  if (!(amax > 0.0f)) return 0u;
+  const uint32_t u = __float_as_uint(amax);
+  const int ef = (int)((u >> 23) & 0xFFu);
+  const int fl = ef > 0 ? ef - 127 : (31 - __clz(u & 0x7FFFFFu)) - 149;
+  const int b = fl - emax + 127;
+  return (uint32_t)(b < 0 ? 0 : (b > 254 ? 254 : b));
+}
+
+// 2^(byte - 127) as an FP32 value (byte 0 is the subnormal 2^-127).
+__device__ __forceinline__ float e8m0_to_f32(uint32_t b) {
+  return b == 0u ? __uint_as_float(0x00400000u) : __uint_as_float(b << 23);
+}
+
+// x / 2^(byte - 127): a multiplication by a power of two, exact unless the product underflows.
+__device__ __forceinline__ float mx_unscale(float x, uint32_t b) {
+  return ldexpf(x, 127 - (int)b);
+}
 
 // GEMM1's activation of one feature from its FP32 gate and up values (kAct* of internal.h; g is
 // unused by the non-gated ReLU2).  Fast exponential and division: h is requantised right after
@@ -364,6 +403,12 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
           "r"(dst),
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
+}
+
+// Asks the L2 to fetch [src, src + bytes) from memory (16-byte aligned, a multiple of 16); no
+// completion to wait for.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // 16-byte cp.async with zero fill of the bytes beyond src_bytes (0 or 16).

@@ -75,7 +75,7 @@ struct GemmShape {
   static_assert(kBarOff + 1024 + 256 + 8 * 1027 <= 232448, "shared memory");
   // full, empty, sf_done per stage; two acc_full, two acc_empty, drain, sf_drain; TMEM slot and
   // the issue count, all before the plan arrays at kBarOff + 256
-  static_assert((3 * kStages + 6) * 8 + 2 * 4 <= 256, "mbarriers + TMEM slot + issue count");
+  static_assert((3 * kStages + 6) * 8 + 3 * 4 <= 256, "mbarriers + TMEM slot + counts");
 };
 
 // Instruction descriptor of tcgen05.mma kind::mxf4nvf4: A and B E2M1 (format 1) at bits 7-9 and
@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* sf_drain = sf_done + kStages;   // the scale-factor warp's last tensor-memory copies
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_drain + 1);
   uint32_t* s_issued = tmem_slot + 1;       // stage fills the copy thread issued
+  volatile uint32_t* s_abort = s_issued + 1;   // set by any role whose bounded wait ran out
   int32_t* s_tile = reinterpret_cast<int32_t*>(smem + GemmShape<kRedStage>::kBarOff + 256);
   int32_t* s_seg = s_tile + (p.nseg + 1);
 
@@ -144,6 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(sf_done + s), 1);
     mbar_init(smem_u32(sf_drain), 1);
     *s_issued = 0u;
+    *s_abort = 0u;
     fence_barrier_init();
   }
   if (warp == kTmaWarp && lane == 0)
@@ -198,10 +200,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // tail: wait until the MMA has released every stage, so no arrival is still in flight
       for (int i = 0; i < kStages && ok; ++i) {
-        if (!mbar_wait_bounded(smem_u32(empty + stage), phase ^ 1u, kWaitLimitNs, p.status)) break;
+        if (!mbar_wait_bounded(smem_u32(empty + stage), phase ^ 1u, kWaitLimitNs, p.status)) {
+          ok = false;
+          break;
+        }
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
       *s_issued = n_issued;
+      if (!ok) *s_abort = 1u;
     }
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issue (one thread) ----------------
@@ -245,7 +251,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // make sure no tensor-core operation is still running before tensor memory is released
       tc_commit(smem_u32(drain));
-      mbar_wait_bounded(smem_u32(drain), 0u, kWaitLimitNs, p.status);
+      if (!mbar_wait_bounded(smem_u32(drain), 0u, kWaitLimitNs, p.status)) ok = false;
+      if (!ok) *s_abort = 1u;
     }
   } else if (warp == kSfWarp) {
     // ---------------- scale factors: shared -> tensor memory, ahead of the MMA thread ---------
@@ -275,9 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
-      // tensor memory is released only once this thread's last scale copies have completed
-      tc_commit(smem_u32(sf_drain));
-      mbar_wait_bounded(smem_u32(sf_drain), 0u, kWaitLimitNs, p.status);
+      if (!ok) *s_abort = 1u;
     }
   } else {
     // ---------------- epilogue (warps 0-3) ----------------
@@ -292,8 +297,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every lane waits; the decision is taken together so that the warp never diverges
       // before the warp-wide tensor-memory loads
       if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(acc_full + abuf), acc_phase[abuf],
-                                                     kWaitLimitNs, p.status)))
+                                                     kWaitLimitNs, p.status))) {
+        if (lane == 0) *s_abort = 1u;
         break;
+      }
       acc_phase[abuf] ^= 1u;
       tc_fence_after();
       const int prow = t.m0 + r;
@@ -405,19 +412,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  // Teardown.  After a wait ran out, stage fills may still be in flight: the copy thread's last
-  // kStages fills are waited for (bounded) before the CTA exits.  Without a timeout every fill
-  // was consumed and these waits return at once.
-  __syncthreads();
-  if (warp == kTmaWarp && lane == 0) {
-    const uint32_t n = *s_issued;
-    for (uint32_t i = n > (uint32_t)kStages ? n - kStages : 0u; i < n; ++i)
-      if (!mbar_wait_bounded(smem_u32(full + i % kStages), (i / kStages) & 1u, kWaitLimitNs,
-                             p.status))
-        break;
-  }
+  // Teardown.  After a wait ran out, stage fills and scale copies may still be in flight: the
+  // copy thread's last kStages fills and the scale-factor thread's last tensor-memory copies are
+  // waited for (bounded) before tensor memory is released.  Without a timeout every fill and
+  // copy was consumed by a completed MMA, and none of this runs.
   tc_fence_before();
   __syncthreads();
+  if (*s_abort) {
+    if (warp == kTmaWarp && lane == 0) {
+      const uint32_t n = *s_issued;
+      for (uint32_t i = n > (uint32_t)kStages ? n - kStages : 0u; i < n; ++i)
+        if (!mbar_wait_bounded(smem_u32(full + i % kStages), (i / kStages) & 1u, kWaitLimitNs,
+                               p.status))
+          break;
+    } else if (warp == kSfWarp && lane == 0) {
+      tc_commit(smem_u32(sf_drain));
+      mbar_wait_bounded(smem_u32(sf_drain), 0u, kWaitLimitNs, p.status);
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);

@@ -64,6 +64,7 @@ constexpr uint32_t kSfCol0 = kAccBufs * kAccCols;
 constexpr uint32_t kSfColsPerStage = 32;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int kBarBytes = 512;                          // mbarriers + TMEM slot
+constexpr uint32_t kPrefetchAhead = 12;                 // L2 prefetch distance, in weight blocks
 
 static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "tensor memory budget");
 static_assert(kStageBytes % 1024 == 0 && kXOff % 1024 == 0, "1024-byte aligned swizzled tiles");
@@ -72,7 +73,7 @@ constexpr size_t kMaxDynSmem = 232448;                   // 227 KB per CTA
 // plus the shared expert's rows)
 static_assert(kStages * kStageBytes + 1024 + kBarBytes + 4 * (2 * 1028 + 2112) <= kMaxDynSmem,
               "shared memory");
-static_assert((3 * kStages + 2 * kAccBufs + 3) * 8 + 5 * 4 <= kBarBytes,
+static_assert((3 * kStages + 2 * kAccBufs + 3) * 8 + 6 * 4 <= kBarBytes,
               "mbarriers, TMEM slot, issue counts and plan flags");
 static_assert(kNmax == kXBoxRows && kNmax <= (int)kAccCols, "one TMA box of token rows per stage");
 
@@ -103,6 +104,7 @@ __device__ __forceinline__ Item decode_item(int item, int total1, int nt1, int n
   return t;
 }
 
+template <bool kGated>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_decode_kernel(const __grid_constant__ CUtensorMap tmap_x,
                                const __grid_constant__ CUtensorMap tmap_h,
@@ -125,6 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* s_issued = tmem_slot + 1;
   uint32_t* s_plan_pending = s_issued + 2;
   uint32_t* s_plan_ok = s_plan_pending + 1;
+  volatile uint32_t* s_abort = s_plan_ok + 1;   // set by any role whose bounded wait ran out
   const int nseg = p.g1.nseg;
   const int plan_ints = (nseg + 1 + 3) & ~3;    // 16-byte multiples for the bulk copies
   // m-tiles can outnumber segments (an expert with more than kNmax rows owns several): the
@@ -157,6 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_issued[0] = s_issued[1] = 0u;
     *s_plan_pending = 0u;
     *s_plan_ok = 0u;
+    *s_abort = 0u;
     fence_barrier_init();
   }
   tc_fence_before();
@@ -203,6 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       *s_plan_ok = (uint32_t)ok;
+      if (!ok) *s_abort = 1u;
     }
     ok = __shfl_sync(0xffffffffu, ok, 0);
     __syncwarp();
@@ -236,35 +241,79 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- weight blocks: one bulk copy per stage ----------------
     // Weights depend on nothing but the plan, so this thread only waits for free ring slots;
     // the stage's token rows come from the token issuer (warp kXWarp), and the stage's full
-    // barrier completes once both parts have landed.
+    // barrier completes once both parts have landed.  While the ring is full (the first stages
+    // wait for the prologue's token rows, later ones for the MMAs), the thread asks the L2 for
+    // the CTA's next weight blocks (bulk prefetch, up to kPrefetchAhead blocks past the ring), so
+    // the HBM stream keeps going and the copies that follow are served from the L2.
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0, n_issued = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+      // cursors over this CTA's weight blocks: the next to copy and the next to prefetch
+      int c_item = blockIdx.x, c_ks = 0, c_kst = 0;
+      int f_item = blockIdx.x, f_ks = 0, f_kst = 0;
+      uint32_t f_idx = 0;
+      const uint8_t* c_src = nullptr;
+      const uint8_t* f_src = nullptr;
+      auto block_base = [&](int item, int& kst) -> const uint8_t* {
         const Item t = NVFP4MOE_ITEM(item);
         const GemmArgs& q = t.ph ? p.g2 : p.g1;
-        const uint8_t* src = q.b_tiles + (size_t)t.seg * q.b_per_seg +
-                             (size_t)t.nt * t.kst * kTileBlockBytes;
-        for (int ks = 0; ks < t.kst; ++ks) {
-          if (!mbar_wait_bounded(smem_u32(empty + stage), phase ^ 1u, kWaitLimitNs, status)) {
+        kst = t.kst;
+        return q.b_tiles + (size_t)t.seg * q.b_per_seg + (size_t)t.nt * t.kst * kTileBlockBytes;
+      };
+      if (c_item < total) {
+        c_src = block_base(c_item, c_kst);
+        f_src = c_src;
+        f_kst = c_kst;
+      }
+      while (c_item < total && ok) {
+        const uint32_t eb = smem_u32(empty + stage);
+        if (!mbar_test_wait(eb, phase ^ 1u)) {
+          // the ring is full: prefetch a later block, or wait (bounded) once there is none
+          if (f_idx < n_issued) {   // catch up with the copies
+            f_item = c_item;
+            f_ks = c_ks;
+            f_kst = c_kst;
+            f_src = c_src;
+            f_idx = n_issued;
+          }
+          if (f_item < total && f_idx < n_issued + kPrefetchAhead) {
+            bulk_prefetch_l2(f_src + (size_t)f_ks * kTileBlockBytes, kTileBlockBytes);
+            ++f_idx;
+            if (++f_ks == f_kst) {
+              f_item += gridDim.x;
+              f_ks = 0;
+              if (f_item < total) f_src = block_base(f_item, f_kst);
+            }
+            continue;
+          }
+          if (!mbar_wait_bounded(eb, phase ^ 1u, kWaitLimitNs, status)) {
             ok = false;
             break;
           }
-          const uint32_t fb = smem_u32(full + stage);
-          mbar_arrive_expect_tx(fb, kTileBlockBytes);
-          bulk_load(smem0 + stage * kStageBytes, src + (size_t)ks * kTileBlockBytes,
-                    kTileBlockBytes, fb);
-          ++n_issued;
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        const uint32_t fb = smem_u32(full + stage);
+        mbar_arrive_expect_tx(fb, kTileBlockBytes);
+        bulk_load(smem0 + stage * kStageBytes, c_src + (size_t)c_ks * kTileBlockBytes,
+                  kTileBlockBytes, fb);
+        ++n_issued;
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        if (++c_ks == c_kst) {
+          c_item += gridDim.x;
+          c_ks = 0;
+          if (c_item < total) c_src = block_base(c_item, c_kst);
         }
       }
       // the MMAs of the last stages must finish before the CTA may exit
       for (int i = 0; i < kStages && ok; ++i) {
-        if (!mbar_wait_bounded(smem_u32(empty + stage), phase ^ 1u, kWaitLimitNs, status)) break;
+        if (!mbar_wait_bounded(smem_u32(empty + stage), phase ^ 1u, kWaitLimitNs, status)) {
+          ok = false;
+          break;
+        }
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
       s_issued[0] = n_issued;
+      if (!ok) *s_abort = 1u;
     }
   } else if (warp == kXWarp) {
     // ---------------- token rows: one 2-D TMA box + their scales per stage ----------------
@@ -313,6 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       s_issued[1] = n_issued;
+      if (!ok) *s_abort = 1u;
     }
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issue: D[weight row][token] ----------------
@@ -357,7 +407,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) tc_commit(smem_u32(acc_full + abuf));
       }
       tc_commit(smem_u32(drain));
-      mbar_wait_bounded(smem_u32(drain), 0u, kWaitLimitNs, status);
+      if (!mbar_wait_bounded(smem_u32(drain), 0u, kWaitLimitNs, status)) ok = false;
+      if (!ok) *s_abort = 1u;
     }
   } else if (warp == kSfWarp) {
     // ---------------- scale factors: shared -> tensor memory, ahead of the MMA thread ---------
@@ -388,9 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
-      // tensor memory is released only once this thread's last scale copies have completed
-      tc_commit(smem_u32(sf_drain));
-      mbar_wait_bounded(smem_u32(sf_drain), 0u, kWaitLimitNs, status);
+      if (!ok) *s_abort = 1u;
     }
   } else {
     // ---------------- epilogue (warps 0-3): lane = weight row, column = token ----------------
@@ -408,8 +457,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every lane waits; the decision is taken together so that the warp never diverges
       // before the warp-wide tensor-memory loads
       if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(acc_full + abuf), acc_phase[abuf],
-                                                     kWaitLimitNs, status)))
+                                                     kWaitLimitNs, status))) {
+        if (lane == 0) *s_abort = 1u;
         break;
+      }
       acc_phase[abuf] ^= 1u;
       tc_fence_after();
       const int rows = (t.m0 >= 0 && t.m0 + t.rows <= q.out_rows) ? t.rows : 0;
@@ -419,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // its up rows, and each half-warp takes one token of a pair.  Non-gated experts (ReLU2):
         // lanes < 16 hold the up rows of block 2w, lanes >= 16 those of block 2w + 1 (w = the
         // warp's 32-row slice of the tile), and both halves take the same token.
-        const bool gated = q.act != kActRelu2;
+        constexpr bool gated = kGated;
         const int I = gated ? q.N / 2 : q.N;
         const int b = gated ? t.nt * 4 + warp : t.nt * 8 + warp * 2 + (lo_half ? 0 : 1);
         uint8_t* hsf_tile = q.hsf_tiles + ((size_t)t.mt * (I / 64) + b / 4) * 512 + (b & 3);
@@ -429,26 +480,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t v[kNmax];
           tmem_ld_32x32b_x16(tbase, v);
           tmem_ld_wait();
-#pragma unroll
-          for (int n = 0; n < kNmax; ++n) {
-            if (n >= rows) break;
-            if (gated && (n & 1)) continue;
-            float h;
-            int col;
-            if (gated) {
-              const float a0 = __uint_as_float(v[n]), a1 = __uint_as_float(v[(n + 1) & (kNmax - 1)]);
-              const float x0 = __shfl_xor_sync(0xffffffffu, a0, 16);
-              const float x1 = __shfl_xor_sync(0xffffffffu, a1, 16);
-              // the lower half-warp takes token n, the upper half token n+1
-              const float g = (lo_half ? a0 : x1) * ag;
-              const float u = (lo_half ? x0 : a1) * au;
-              col = n + (lo_half ? 0 : 1);
-              h = glu_activation(g, u, q.act, q.swiglu_limit, q.swiglu_alpha);
-            } else {
-              col = n;
-              h = glu_activation(0.0f, __uint_as_float(v[n]) * au, q.act, q.swiglu_limit,
-                                 q.swiglu_alpha);
-            }
+          // h of one token column per half-warp -> its NVFP4 block (half-warp reductions), codes
+          // and scale stored by the half's first lane
+          auto requant_store = [&](float h, int col) {
             float bamax = fabsf(h);
 #pragma unroll
             for (int o = 8; o > 0; o >>= 1) bamax = fmaxf(bamax, __shfl_xor_sync(0xffffffffu, bamax, o));
@@ -471,6 +505,28 @@ __global__ void __launch_bounds__(kThreads, 1)
               *reinterpret_cast<uint2*>(q.hq + prow * (I / 2) + b * 8) = make_uint2(word, word_hi);
               q.hsf[prow * (I / 16) + b] = (uint8_t)sf;
               hsf_tile[col * 16] = (uint8_t)sf;
+            }
+          };
+          if constexpr (kGated) {
+#pragma unroll
+            for (int n = 0; n < kNmax; n += 2) {
+              if (n >= rows) break;
+              const float a0 = __uint_as_float(v[n]), a1 = __uint_as_float(v[n + 1]);
+              const float x0 = __shfl_xor_sync(0xffffffffu, a0, 16);
+              const float x1 = __shfl_xor_sync(0xffffffffu, a1, 16);
+              // the lower half-warp takes token n, the upper half token n+1
+              const float g = (lo_half ? a0 : x1) * ag;
+              const float u = (lo_half ? x0 : a1) * au;
+              requant_store(glu_activation(g, u, q.act, q.swiglu_limit, q.swiglu_alpha),
+                            n + (lo_half ? 0 : 1));
+            }
+          } else {
+#pragma unroll
+            for (int n = 0; n < kNmax; ++n) {
+              if (n >= rows) break;
+              requant_store(glu_activation(0.0f, __uint_as_float(v[n]) * au, q.act,
+                                           q.swiglu_limit, q.swiglu_alpha),
+                            n);
             }
           }
         }
@@ -511,21 +567,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   // whose fill one issuer made and the other did not gets the missing arrival here (the leading
   // issuer is at most kStages fills ahead, since every fill waits for the slot's release, which
   // needs the previous phase complete), so every issued phase completes once its bytes land;
-  // then the last kStages fills and the plan copy are waited for (bounded) before the CTA exits.
-  // Without a timeout every fill was consumed and these waits return at once.
-  __syncthreads();
-  if (warp == kWeightWarp && lane == 0) {
-    const uint32_t wi = s_issued[0], xi = s_issued[1];
-    const uint32_t lo = min(wi, xi), hi = max(wi, xi);
-    for (uint32_t i = lo; i < hi; ++i) mbar_arrive(smem_u32(full + i % kStages));
-    for (uint32_t i = hi > (uint32_t)kStages ? hi - kStages : 0u; i < hi; ++i)
-      if (!mbar_wait_bounded(smem_u32(full + i % kStages), (i / kStages) & 1u, kWaitLimitNs,
-                             status))
-        break;
-    if (*s_plan_pending) mbar_wait_bounded(smem_u32(plan_bar), 0u, kWaitLimitNs, status);
-  }
+  // then the last kStages fills, the plan copy and the scale-factor thread's last tensor-memory
+  // copies are waited for (bounded) before tensor memory is released.  Without a timeout every
+  // fill and copy was consumed by a completed MMA, and none of this runs.
   tc_fence_before();
   __syncthreads();
+  if (*s_abort) {
+    if (warp == kWeightWarp && lane == 0) {
+      const uint32_t wi = s_issued[0], xi = s_issued[1];
+      const uint32_t lo = min(wi, xi), hi = max(wi, xi);
+      for (uint32_t i = lo; i < hi; ++i) mbar_arrive(smem_u32(full + i % kStages));
+      for (uint32_t i = hi > (uint32_t)kStages ? hi - kStages : 0u; i < hi; ++i)
+        if (!mbar_wait_bounded(smem_u32(full + i % kStages), (i / kStages) & 1u, kWaitLimitNs,
+                               status))
+          break;
+      if (*s_plan_pending) mbar_wait_bounded(smem_u32(plan_bar), 0u, kWaitLimitNs, status);
+    } else if (warp == kSfWarp && lane == 0) {
+      tc_commit(smem_u32(sf_drain));
+      mbar_wait_bounded(smem_u32(sf_drain), 0u, kWaitLimitNs, status);
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
@@ -585,16 +648,19 @@ cudaError_t launch_grouped_gemm_decode(const DecodeGemmArgs& a, cudaStream_t s) 
   if (nt1 < 1 || a.g1.max_items % nt1 != 0) return cudaErrorInvalidValue;
   const size_t smem = smem_bytes(a.g1.nseg, a.g1.max_items / nt1);
   if (smem > kMaxDynSmem) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_decode_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  // one instantiation per GEMM1 layout (gate/up interleaved, or up rows alone), so that the
+  // epilogue of either carries no code for the other
+  auto kernel = a.g1.act == kActRelu2 ? grouped_gemm_decode_kernel<false>
+                                      : grouped_gemm_decode_kernel<true>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
   if (e != cudaSuccess) return e;
   // one CTA per SM at most: CTAs wait on each other's GEMM1 tiles, so all of them must be
   // resident together (one 200 KB CTA fits an SM; the grid never exceeds the SM count)
   const int64_t items = (int64_t)a.g1.max_items + a.g2.max_items;
   int grid = (int)std::min<int64_t>(items, num_sms());
   if (grid < 1) grid = 1;
-  return launch_pdl(grouped_gemm_decode_kernel, dim3(grid), dim3(kThreads), smem, s, tmap_x,
-                    tmap_h, a);
+  return launch_pdl(kernel, dim3(grid), dim3(kThreads), smem, s, tmap_x, tmap_h, a);
 }
 
 }  // namespace nvfp4moe

@@ -1,6 +1,12 @@
 // Grouped GEMMs of the W4A16 layer: BF16 activations as they are, NVFP4 expert weights decoded
 // to BF16 inside the kernel ("b12x" README, section "What's in here", moe: "W4A16 (BF16
-// activations, inline FP4 weight dequant - no activation-scale math)").
+// activations, inline FP4 weight dequant - no activation-scale math)"); and of the W4A8 layer
+// (same page, "DeepSeek V4 Flash 0731 MoE reproduction": MXFP4 weights with one E8M0 scale per 32,
+// MXFP8 activations), whose MXFP8 activations arrive already decoded to BF16 (exact), whose
+// MXFP4 weights are decoded the same way as the NVFP4 ones (e2m1 * 2^(scale - 127), exact in
+// BF16), and whose GEMM1 epilogue requantises h to MXFP8 (codes and scales are written out, the
+// decoded BF16 values feed the down projection).  Exact decoding keeps the layer's arithmetic
+// that of its definition: every product of two decoded operands is exact in FP32.
 //
 // Tiles are 128 expert-ordered rows (MMA M) x 128 weight rows (MMA N) on the 5th-generation
 // tensor cores (tcgen05.mma kind::f16, BF16 x BF16 -> FP32 in tensor memory), K in sub-stages of
@@ -48,7 +54,7 @@ constexpr size_t kSmemBytes = 1024 + kBarOff + 256 + 8 * 1027;
 static_assert(kRawOff % 1024 == 0 && kTileBlockBytes % 1024 == 0, "1024-byte aligned tiles");
 static_assert(kSmemBytes <= 232448, "shared memory");
 // raw full/empty, sub full/empty, acc full/empty x2, drain; TMEM slot, issue and arrival counts
-static_assert((2 * kRawStages + 2 * kSubStages + 4 + 1) * 8 + (3 + kConvWarps) * 4 <= 256,
+static_assert((2 * kRawStages + 2 * kSubStages + 4 + 1) * 8 + (4 + kConvWarps) * 4 <= 256,
               "barrier area");
 
 // Instruction descriptor of tcgen05.mma kind::f16: FP32 accumulator (bits 4-5 = 1), A and B BF16
@@ -108,6 +114,51 @@ __device__ __forceinline__ TileW16 decode_tile_w16(int item, int n_tiles, const 
   return t;
 }
 
+// Two E2M1 codes (low nibble first) times 2^(b - 127) as BF16x2 (exact).
+__device__ __forceinline__ uint32_t e2m1x2_mx_bf16x2(uint32_t byte, float scale) {
+  uint32_t h2;
+  const uint16_t in = (uint16_t)(byte & 0xFFu);
+  asm("{\n"
+      ".reg .b8 b;\n"
+      "cvt.u8.u16 b, %1;\n"
+      "cvt.rn.f16x2.e2m1x2 %0, b;\n"
+      "}"
+      : "=r"(h2)
+      : "h"(in));
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+  const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale, f.y * scale);
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+// MXFP8 requantisation of 32 consecutive h values: E8M0 scale, E4M3 codes (nearest even,
+// saturated), and the decoded values as BF16 (exact) for the next GEMM.
+__device__ __forceinline__ void mx8_requant_store(const float* h, uint8_t* codes, uint8_t* sf,
+                                                  uint8_t* hb) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(h[i]));
+  const uint32_t sb = mx_scale_byte(amax, 8);
+  const float X = e8m0_to_f32(sb);
+  uint32_t cw[8], bw[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t c2 = f32_to_e4m3x2(mx_unscale(h[2 * i], sb), mx_unscale(h[2 * i + 1], sb));
+    if (i & 1) cw[i >> 1] |= c2 << 16;
+    else cw[i >> 1] = c2;
+    const float2 v = e4m3x2_to_f32x2(c2);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(v.x * X, v.y * X);
+    bw[i] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+  uint4* cd = reinterpret_cast<uint4*>(codes);
+  cd[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+  cd[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+  *sf = (uint8_t)sb;
+  uint4* bd = reinterpret_cast<uint4*>(hb);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) bd[q] = make_uint4(bw[4 * q], bw[4 * q + 1], bw[4 * q + 2], bw[4 * q + 3]);
+}
+
+template <bool kMx>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_w16_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmW16Args p) {
   extern __shared__ uint8_t smem_raw[];
@@ -124,6 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   uint32_t* s_issued = tmem_slot + 1;   // [0] raw blocks, [1] A boxes issued by the copy thread
   uint32_t* s_conv = s_issued + 2;      // sub-stage arrivals of each converter warp
+  volatile uint32_t* s_abort = s_conv + kConvWarps;   // set by any role whose wait ran out
   int32_t* s_tile = reinterpret_cast<int32_t*>(smem + kBarOff + 256);
   int32_t* s_seg = s_tile + (p.nseg + 1);
 
@@ -148,6 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(drain), 1);
     s_issued[0] = s_issued[1] = 0u;
     for (int w = 0; w < kConvWarps; ++w) s_conv[w] = 0u;
+    *s_abort = 0u;
     fence_barrier_init();
   }
   if (warp == kCopyWarp && lane == 0)
@@ -208,6 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       s_issued[0] = n_raw;
       s_issued[1] = n_sub;
+      if (!ok) *s_abort = 1u;
     }
   } else if (warp >= kConvWarp0) {
     // ---------------- NVFP4 weight row -> BF16 row of the B tile ----------------
@@ -234,22 +288,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           // chunk ^ (row % 8)); its four scales are one word of scale group q
           const uint4 c0 = *reinterpret_cast<const uint4*>(raw + r * 128 + (((2 * q) ^ (r & 7)) << 4));
           const uint4 c1 = *reinterpret_cast<const uint4*>(raw + r * 128 + (((2 * q + 1) ^ (r & 7)) << 4));
-          const uint32_t sw = *reinterpret_cast<const uint32_t*>(
-              raw + kTileBytes + q * 512 + (r & 31) * 16 + (r >> 5) * 4);
+          // NVFP4: the four E4M3 scales of the sub-stage are one word of scale group q; MXFP4:
+          // its two E8M0 scales are bytes 2q, 2q+1 of the row's eight
+          const uint32_t sw = kMx ? (uint32_t)*reinterpret_cast<const uint16_t*>(
+                                        raw + kTileBytes + r * 8 + 2 * q)
+                                  : *reinterpret_cast<const uint32_t*>(
+                                        raw + kTileBytes + q * 512 + (r & 31) * 16 + (r >> 5) * 4);
           const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
           uint8_t* brow = smem + ss * kSubBytes + kTileBytes16 + r * 128;
 #pragma unroll
           for (int j = 0; j < 8; ++j) {         // 16-byte chunk j of the BF16 row: 8 values
-            // elements 8j .. 8j+7 use block scale (8j) / 16 = j / 2
-            const uint32_t sb = (sw >> (8 * (j >> 1))) & 0xFFu;
-            const __half hs = __float2half_rn(e4m3_to_f32(sb));
-            const __half2 s2 = __halves2half2(hs, hs);
             const uint32_t w = cw[j];
             uint4 o;
-            o.x = e2m1x2_scaled_bf16x2(w & 0xFFu, s2);
-            o.y = e2m1x2_scaled_bf16x2((w >> 8) & 0xFFu, s2);
-            o.z = e2m1x2_scaled_bf16x2((w >> 16) & 0xFFu, s2);
-            o.w = e2m1x2_scaled_bf16x2(w >> 24, s2);
+            if constexpr (kMx) {
+              // elements 8j .. 8j+7 use 32-block scale j / 4
+              const float sc = e8m0_to_f32((sw >> (8 * (j >> 2))) & 0xFFu);
+              o.x = e2m1x2_mx_bf16x2(w & 0xFFu, sc);
+              o.y = e2m1x2_mx_bf16x2((w >> 8) & 0xFFu, sc);
+              o.z = e2m1x2_mx_bf16x2((w >> 16) & 0xFFu, sc);
+              o.w = e2m1x2_mx_bf16x2(w >> 24, sc);
+            } else {
+              // elements 8j .. 8j+7 use block scale (8j) / 16 = j / 2
+              const uint32_t sb = (sw >> (8 * (j >> 1))) & 0xFFu;
+              const __half hs = __float2half_rn(e4m3_to_f32(sb));
+              const __half2 s2 = __halves2half2(hs, hs);
+              o.x = e2m1x2_scaled_bf16x2(w & 0xFFu, s2);
+              o.y = e2m1x2_scaled_bf16x2((w >> 8) & 0xFFu, s2);
+              o.z = e2m1x2_scaled_bf16x2((w >> 16) & 0xFFu, s2);
+              o.w = e2m1x2_scaled_bf16x2(w >> 24, s2);
+            }
             *reinterpret_cast<uint4*>(brow + ((j ^ (r & 7)) << 4)) = o;
           }
           fence_proxy_async_smem();     // the tensor core reads what these stores wrote
@@ -263,7 +330,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++rs == kRawStages) { rs = 0; rph ^= 1u; }
       }
     }
-    if (lane == 0) s_conv[warp - kConvWarp0] = n_arr;
+    if (lane == 0) {
+      s_conv[warp - kConvWarp0] = n_arr;
+      if (!ok) *s_abort = 1u;
+    }
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issue (one thread) ----------------
     if (lane == 0) {
@@ -303,7 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) tc_commit(smem_u32(acc_full + abuf));
       }
       tc_commit(smem_u32(drain));
-      mbar_wait_bounded(smem_u32(drain), 0u, kWaitLimitNs, p.status);
+      if (!mbar_wait_bounded(smem_u32(drain), 0u, kWaitLimitNs, p.status)) ok = false;
+      if (!ok) *s_abort = 1u;
     }
   } else {
     // ---------------- epilogue (warps 0-3): one accumulator row per thread ----------------
@@ -314,8 +385,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const TileW16 t = decode_tile_w16(item, n_tiles, s_tile, s_seg, p.nseg);
       const int abuf = it & 1;
       if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(acc_full + abuf), acc_phase[abuf],
-                                                     kWaitLimitNs, p.status)))
+                                                     kWaitLimitNs, p.status))) {
+        if (lane == 0) *s_abort = 1u;
         break;
+      }
       acc_phase[abuf] ^= 1u;
       tc_fence_after();
       const int prow = t.m0 + r;
@@ -326,12 +399,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int I = gated ? p.N / 2 : p.N;
         const float ag = p.w_ts[t.seg * 4 + 0];
         const float au = p.w_ts[t.seg * 4 + 1];
+        float hk[16];   // W4A8, gated: the first 16 features of a 32-feature MXFP8 block
 #pragma unroll 1
         for (int c = 0; c < kBN / 32; ++c) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(tbase + c * 32, v);
           tmem_ld_wait();
           if (!valid) continue;
+          if constexpr (kMx) {
+            float h32[32];
+            if (gated) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float hv = glu_activation(__uint_as_float(v[i]) * ag,
+                                                __uint_as_float(v[16 + i]) * au, p.act,
+                                                p.swiglu_limit, p.swiglu_alpha);
+                if (c & 1) h32[16 + i] = hv;
+                else hk[i] = hv;
+              }
+              if ((c & 1) == 0) continue;
+#pragma unroll
+              for (int i = 0; i < 16; ++i) h32[i] = hk[i];
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                h32[i] = glu_activation(0.0f, __uint_as_float(v[i]) * au, p.act, p.swiglu_limit,
+                                        p.swiglu_alpha);
+            }
+            const int f0 = gated ? t.nt * (kBN / 2) + (c - 1) * 16 : t.nt * kBN + c * 32;
+            mx8_requant_store(h32, p.hq8 + (size_t)prow * I + f0,
+                              p.hsf8 + (size_t)prow * (I / 32) + f0 / 32,
+                              p.hb + ((size_t)prow * I + f0) * 2);
+            continue;
+          }
           // gated: (16 gate | 16 up) columns -> 16 features; non-gated: 32 up columns -> 32
           uint32_t packed[16];
           if (gated) {
@@ -405,9 +505,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // kSubStages indices can be open, and the arrivals missing there are made here on behalf of
   // whoever stopped, after which every issued phase completes once its bytes land.  Then the
   // last phases of both rings are waited for (bounded).  Without a timeout every phase was
-  // consumed and these waits return at once.
+  // consumed, and none of this runs.
+  tc_fence_before();
   __syncthreads();
-  if (warp == kCopyWarp && lane == 0) {
+  if (*s_abort && warp == kCopyWarp && lane == 0) {
     const uint32_t nr = s_issued[0], na = s_issued[1];
     uint32_t hi = na;
     for (int w = 0; w < kConvWarps; ++w) hi = max(hi, s_conv[w]);
@@ -427,8 +528,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                              kWaitLimitNs, p.status))
         break;
   }
-  tc_fence_before();
-  __syncthreads();
+  if (*s_abort) {
+    tc_fence_before();
+    __syncthreads();
+  }
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
@@ -465,13 +568,14 @@ cudaError_t launch_grouped_gemm_w16(const GemmW16Args& a, cudaStream_t s) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   const size_t smem = kSmemBytes - 8 * 1027 + sizeof(int32_t) * 2 * ((size_t)a.nseg + 2);
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_w16_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto kernel = a.mx ? grouped_gemm_w16_kernel<true> : grouped_gemm_w16_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
   if (e != cudaSuccess) return e;
   int grid = a.max_items;
   if (grid > num_sms()) grid = num_sms();
   if (grid < 1) grid = 1;
-  return launch_pdl(grouped_gemm_w16_kernel, dim3(grid), dim3(kThreads), smem, s, tmap, a);
+  return launch_pdl(kernel, dim3(grid), dim3(kThreads), smem, s, tmap, a);
 }
 
 }  // namespace nvfp4moe

@@ -101,11 +101,13 @@ bool prologue_small_fits(int T, int H, int k);
 // Workspace of moe_run for T tokens.  Offset 0 holds the device status word.
 struct RunLayout {
   size_t hdr, amax_part, ids, w, hist, base, seg_off, tile_start, perm_src, perm_w, inv, xq, xsf,
-      hq, hsf, yacc, obuf, perm_seg, xq_perm, xsf_tiles, hsf_tiles, ready, xb_perm, hb, total;
+      hq, hsf, yacc, obuf, perm_seg, xq_perm, xsf_tiles, hsf_tiles, ready, xb_perm, hb, xq8,
+      hq8, total;
   int T, R, Rt, nseg, nchunks, tpc, dtiles;
   bool small;   // fused prologue + stored-row combine
   bool decode;  // T <= kDecodeMaxRows: cluster prologue and the swapped-operand decode GEMM
-  bool w16;     // W4A16 layer: BF16 activation and h rows, one path for every batch size
+  bool w16;     // W4A16 or W4A8 layer: BF16 activation and h rows (decoded), one path
+  bool mx;      // W4A8 layer: MXFP8 codes and scales of x and h as well
   RunLayout(const moe_config& c, int T_) {
     T = T_;
     const int k = c.top_k, E = c.num_experts, H = c.hidden, I = c.inter;
@@ -131,7 +133,8 @@ struct RunLayout {
     xsf = o;        o = align_up(o + (size_t)T * H / 16);
     hq = o;         o = align_up(o + (size_t)Rt * I / 2);
     hsf = o;        o = align_up(o + (size_t)Rt * I / 16);
-    w16 = (c.flags & MOE_FLAG_ACT_BF16) != 0u;
+    mx = (c.flags & MOE_FLAG_ACT_MXFP8) != 0u;
+    w16 = mx || (c.flags & MOE_FLAG_ACT_BF16) != 0u;
     small = !w16 && (int64_t)R <= 2048 && (int64_t)T * H <= kSmallPrologueElems &&
             (int64_t)Rt * H <= kStoreCombineElems;
     yacc = o;       o = align_up(o + (small ? 0 : 4 * (size_t)T * H));
@@ -152,6 +155,8 @@ struct RunLayout {
     ready = o;      o = align_up(o + (decode ? 4 * ((size_t)dtiles + 1) : 0));   // + plan flag
     xb_perm = o;    o = align_up(o + (w16 ? 2 * (size_t)Rt * H : 0));
     hb = o;         o = align_up(o + (w16 ? 2 * (size_t)Rt * I : 0));
+    xq8 = o;        o = align_up(o + (mx ? (size_t)T * H + (size_t)T * H / 32 : 0));
+    hq8 = o;        o = align_up(o + (mx ? (size_t)Rt * I + (size_t)Rt * I / 32 : 0));
     total = o;
   }
 };
@@ -279,6 +284,10 @@ struct GemmW16Args {
   int act;                    // kAct* (mode 0)
   float swiglu_limit, swiglu_alpha;
   uint8_t* hb;                // mode 0 out, BF16 [out_rows, I]
+  int mx;                     // W4A8: MXFP4 weight blocks (E8M0 scales, no tensor scale) and h
+                              // requantised to MXFP8 (codes to hq8, scales to hsf8; hb decoded)
+  uint8_t* hq8;               // mode 0, mx: E4M3 codes [out_rows, I]
+  uint8_t* hsf8;              // mode 0, mx: E8M0 scales [out_rows, I/32]
   const int32_t* perm_src;    // mode 1: token of each permuted row
   const float* perm_w;        // mode 1: router weight of each permuted row
   float* yacc;                // mode 1 out [y_rows, N]
@@ -286,6 +295,12 @@ struct GemmW16Args {
   int32_t* status;
 };
 cudaError_t launch_grouped_gemm_w16(const GemmW16Args& a, cudaStream_t s);
+
+// The W4A8 layer's activation quantiser: MXFP8 codes [T, H] and E8M0 scales [T, H/32] in token
+// order, and the decoded BF16 values in every expert row of each token (xb_perm [Rt, H]).
+cudaError_t launch_act_mx_encode_perm(const void* x, int T, int H, int k, int shared, int Rt,
+                                      const int32_t* inv, uint8_t* codes, uint8_t* sf,
+                                      void* xb_perm, int32_t* status, cudaStream_t s);
 
 // Copies BF16 token rows into expert order: row p of xb_perm is row perm_src[p] of x [T, H].
 cudaError_t launch_permute_rows_bf16(const void* x, int T, int H, int Rt, const int32_t* perm_src,
@@ -319,7 +334,8 @@ cudaError_t launch_permute_rows(const uint8_t* xq, const uint8_t* xsf, int T, in
                                 uint8_t* xq_perm, uint8_t* xsf_tiles, int32_t* status,
                                 cudaStream_t s);
 cudaError_t launch_finalize_gather(const float* o, const int32_t* inv, int T, int k, int H,
-                                   int shared, void* y, cudaStream_t s);
+                                   int shared, void* y, cudaStream_t s,
+                                   int32_t* plan_flag = nullptr);
 
 struct PrologueArgs {
   const void* x;           // [T, H] BF16

@@ -165,6 +165,80 @@ __global__ void __launch_bounds__(kThreads) weight_encode_kernel(WeightSrc w, We
   }
 }
 
+// MXFP4 weights (the W4A8 layer): one thread per 32-element block of one matrix row.  Codes go to
+// the same packed positions as NVFP4 codes; the block's E8M0 scale byte to the block's scale
+// area at row * 8 + (32-block within the 256-wide K stage).
+__host__ __device__ __forceinline__ size_t packed_mx_sf_offset(int64_t n, int64_t kb32, int64_t K) {
+  const int64_t kst = K / 256, r = n & 127;
+  const int64_t blk = (n >> 7) * kst + kb32 / 8;
+  return (size_t)(blk * kTileBlockBytes + kTileBytes + r * 8 + (kb32 & 7));
+}
+
+__global__ void __launch_bounds__(kThreads) weight_encode_mx_kernel(WeightSrc w, WeightDst d) {
+  const int mi = blockIdx.y;
+  const int slot = mi / 3, m = mi % 3;
+  if (m == 0 && !w.gated) return;
+  const int64_t per = (int64_t)w.I * w.H;
+  const int64_t K = m < 2 ? w.H : w.I;
+  const int64_t nblk = per / 32;
+  const uint16_t* src = matrix_ptr(w, slot, m, per);
+  for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblk;
+       b += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t n = b / (K / 32), kb = b % (K / 32);
+    const uint4* p = reinterpret_cast<const uint4*>(src + n * K + kb * 32);
+    float f[32];
+    float amax = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 v = __ldg(p + q);
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        f[8 * q + 2 * i] = bf16_bits_to_f32(wv[i] & 0xFFFFu);
+        f[8 * q + 2 * i + 1] = bf16_bits_to_f32(wv[i] >> 16);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    const uint32_t sb = mx_scale_byte(amax, 2);
+    uint32_t words[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      words[q] = e2m1x8(mx_unscale(f[8 * q], sb), mx_unscale(f[8 * q + 1], sb),
+                        mx_unscale(f[8 * q + 2], sb), mx_unscale(f[8 * q + 3], sb),
+                        mx_unscale(f[8 * q + 4], sb), mx_unscale(f[8 * q + 5], sb),
+                        mx_unscale(f[8 * q + 6], sb), mx_unscale(f[8 * q + 7], sb));
+    uint8_t* base = m < 2 ? d.w13 + slot * d.w13_per_e : d.w2 + slot * d.w2_per_e;
+    const int64_t r = m < 2 ? w13_row(n, m, d.gated) : n;
+    *reinterpret_cast<uint2*>(base + packed_code_offset(r, 2 * kb, K)) = make_uint2(words[0], words[1]);
+    *reinterpret_cast<uint2*>(base + packed_code_offset(r, 2 * kb + 1, K)) = make_uint2(words[2], words[3]);
+    base[packed_mx_sf_offset(r, kb, K)] = (uint8_t)sb;
+  }
+}
+
+__global__ void weight_ts_one_kernel(float* ts, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) ts[i] = 1.0f;
+}
+
+// Canonical MXFP4 export: codes [N, K/2], E8M0 scales [N, K/32].
+__global__ void __launch_bounds__(kThreads) weight_export_mx_kernel(WeightDst d, int slot, int m,
+                                                                   int64_t N, int64_t K,
+                                                                   uint8_t* codes, uint8_t* sf,
+                                                                   float* ts) {
+  const int64_t nblk = N * K / 16;
+  for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblk;
+       b += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t n = b / (K / 16), kb = b % (K / 16);
+    const uint8_t* base = m < 2 ? d.w13 + slot * d.w13_per_e : d.w2 + slot * d.w2_per_e;
+    const int64_t r = m < 2 ? w13_row(n, m, d.gated) : n;
+    *reinterpret_cast<uint2*>(codes + n * (K / 2) + kb * 8) =
+        *reinterpret_cast<const uint2*>(base + packed_code_offset(r, kb, K));
+    if ((kb & 1) == 0) sf[n * (K / 32) + kb / 2] = base[packed_mx_sf_offset(r, kb / 2, K)];
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) *ts = d.ts[slot * 4 + m];
+}
+
 __global__ void __launch_bounds__(kThreads) weight_export_kernel(WeightDst d, int slot, int m,
                                                                 int64_t N, int64_t K,
                                                                 uint8_t* codes, uint8_t* sf,
@@ -201,9 +275,14 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const float4* __rest
 __global__ void __launch_bounds__(kThreads) finalize_gather_kernel(const float4* __restrict__ o,
                                                                   const int32_t* __restrict__ inv,
                                                                   int T, int k, int H4,
-                                                                  int shared, uint2* __restrict__ y) {
+                                                                  int shared, uint2* __restrict__ y,
+                                                                  int32_t* plan_flag) {
   griddep_wait();
   griddep_launch();
+  // the decode GEMM of this call has completed (the wait above), so nothing reads the plan-ready
+  // flag any more: lower it for the next call (its prologue lowers it again before the next GEMM
+  // may launch)
+  if (plan_flag && blockIdx.x == 0 && threadIdx.x == 0) *plan_flag = 0;
   const int64_t n = (int64_t)T * H4;
   const int64_t R = (int64_t)T * k;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
@@ -501,6 +580,83 @@ __global__ void __launch_bounds__(kThreads) permute_rows_bf16_kernel(
   }
 }
 
+// The W4A8 layer's activations: one thread per 32-element block of x: MXFP8 (E8M0 scale for E4M3
+// elements, codes rounded to nearest even and saturated), written in token order (codes [T, H],
+// scales [T, H/32]) and, decoded back to BF16 (exact: 4 significant bits times a power of two),
+// into each of the token's expert-ordered rows of xb_perm [Rt, H] (the GEMM's A operand).
+__global__ void __launch_bounds__(kThreads) act_mx_encode_perm_kernel(
+    const uint4* __restrict__ x, int T, int H, int k, int shared, int Rt,
+    const int32_t* __restrict__ inv, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+    uint4* __restrict__ xb_perm, int32_t* status) {
+  griddep_wait();
+  griddep_launch();
+  const int nkb = H / 32;
+  const int64_t nblk = (int64_t)T * nkb;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < nblk; u += stride) {
+    const int t = (int)(u / nkb), b = (int)(u - (int64_t)t * nkb);
+    float f[32];
+    float amax = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 v = __ldg(x + 4 * u + q);
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        f[8 * q + 2 * i] = bf16_bits_to_f32(wv[i] & 0xFFFFu);
+        f[8 * q + 2 * i + 1] = bf16_bits_to_f32(wv[i] >> 16);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    if (!(amax <= 3.402823466e38f)) set_status(status, MOE_ERR_NONFINITE);
+    const uint32_t sb = mx_scale_byte(amax, 8);
+    const float X = e8m0_to_f32(sb);
+    uint32_t cw[8];
+    uint4 out[4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      uint32_t c = 0u;
+#pragma unroll
+      for (int j = 0; j < 4; j += 2)
+        c |= f32_to_e4m3x2(mx_unscale(f[4 * i + j], sb), mx_unscale(f[4 * i + j + 1], sb)) << (8 * j);
+      cw[i] = c;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t ow[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t c2 = (cw[2 * q + i / 2] >> (16 * (i & 1))) & 0xFFFFu;
+        const float2 v = e4m3x2_to_f32x2(c2);
+        const __nv_bfloat162 bb = __floats2bfloat162_rn(v.x * X, v.y * X);
+        ow[i] = *reinterpret_cast<const uint32_t*>(&bb);
+      }
+      out[q] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+    }
+    uint4* cdst = reinterpret_cast<uint4*>(codes + u * 32);
+    cdst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+    cdst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+    sf[u] = (uint8_t)sb;
+    for (int j = 0; j <= k; ++j) {
+      int p;
+      if (j < k) {
+        p = __ldg(inv + (int64_t)t * k + j);
+      } else {
+        if (!shared) break;
+        p = T * k + t;
+      }
+      if (p < 0 || p >= Rt) {
+        set_status(status, MOE_ERR_INVALID_ARG);
+        continue;
+      }
+      uint4* dst = xb_perm + ((size_t)p * H + (size_t)b * 32) / 8;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) dst[q] = out[q];
+    }
+  }
+}
+
 int grid_for(int64_t work, int per_block, int cap) {
   int64_t g = (work + per_block - 1) / per_block;
   if (g < 1) g = 1;
@@ -624,6 +780,13 @@ cudaError_t launch_weight_quant(const moe_config& c, const WeightLayout& L, cons
   weight_amax_kernel<<<g1, kThreads, 0, s>>>(w, amax);
   weight_ts_kernel<<<(L.Et * 4 + 255) / 256, 256, 0, s>>>(amax, L.Et * 4);
   WeightDst d = make_dst(L, wbuf);
+  if (c.flags & MOE_FLAG_ACT_MXFP8) {   // MXFP4: E8M0 per 32, no tensor scale (kept at 1)
+    weight_ts_one_kernel<<<(L.Et * 4 + 255) / 256, 256, 0, s>>>(reinterpret_cast<float*>(amax),
+                                                                 L.Et * 4);
+    dim3 gm(grid_for(per / 32, kThreads, 4096), L.Et * 3);
+    weight_encode_mx_kernel<<<gm, kThreads, 0, s>>>(w, d);
+    return cudaGetLastError();
+  }
   dim3 g2(grid_for(per / 16, kThreads, 4096), L.Et * 3);
   weight_encode_kernel<<<g2, kThreads, 0, s>>>(w, d);
   return cudaGetLastError();
@@ -635,17 +798,21 @@ cudaError_t launch_weight_export(const moe_config& c, const WeightLayout& L, con
   WeightDst d = make_dst(L, const_cast<uint8_t*>(wbuf));
   const int64_t N = m < 2 ? c.inter : c.hidden;
   const int64_t K = m < 2 ? c.hidden : c.inter;
-  weight_export_kernel<<<grid_for(N * K / 16, kThreads, 4096), kThreads, 0, s>>>(d, slot, m, N, K,
-                                                                                codes, sf, ts);
+  if (c.flags & MOE_FLAG_ACT_MXFP8)
+    weight_export_mx_kernel<<<grid_for(N * K / 16, kThreads, 4096), kThreads, 0, s>>>(
+        d, slot, m, N, K, codes, sf, ts);
+  else
+    weight_export_kernel<<<grid_for(N * K / 16, kThreads, 4096), kThreads, 0, s>>>(
+        d, slot, m, N, K, codes, sf, ts);
   return cudaGetLastError();
 }
 
 cudaError_t launch_finalize_gather(const float* o, const int32_t* inv, int T, int k, int H,
-                                   int shared, void* y, cudaStream_t s) {
+                                   int shared, void* y, cudaStream_t s, int32_t* plan_flag) {
   const int64_t n4 = (int64_t)T * (H / 4);
   return launch_pdl(finalize_gather_kernel, dim3(grid_for(n4, kThreads, num_sms() * 8)),
                     dim3(kThreads), 0, s, reinterpret_cast<const float4*>(o), inv, T, k, H / 4,
-                    shared, reinterpret_cast<uint2*>(y));
+                    shared, reinterpret_cast<uint2*>(y), plan_flag);
 }
 
 cudaError_t launch_permute_rows(const uint8_t* xq, const uint8_t* xsf, int T, int H, int Rt,
@@ -667,6 +834,15 @@ cudaError_t launch_permute_rows_bf16(const void* x, int T, int H, int Rt, const 
   return launch_pdl(permute_rows_bf16_kernel, dim3(grid_for(work, kThreads, num_sms() * 8)),
                     dim3(kThreads), 0, s, reinterpret_cast<const uint4*>(x), T, vpr, Rt, perm_src,
                     reinterpret_cast<uint4*>(xb_perm), status);
+}
+
+cudaError_t launch_act_mx_encode_perm(const void* x, int T, int H, int k, int shared, int Rt,
+                                      const int32_t* inv, uint8_t* codes, uint8_t* sf,
+                                      void* xb_perm, int32_t* status, cudaStream_t s) {
+  const int64_t nblk = (int64_t)T * H / 32;
+  return launch_pdl(act_mx_encode_perm_kernel, dim3(grid_for(nblk, kThreads, num_sms() * 16)),
+                    dim3(kThreads), 0, s, reinterpret_cast<const uint4*>(x), T, H, k, shared, Rt,
+                    inv, codes, sf, reinterpret_cast<uint4*>(xb_perm), status);
 }
 
 cudaError_t launch_finalize(const float* yacc, void* y, int64_t n, cudaStream_t s) {

@@ -364,8 +364,12 @@ class QuantExpertMX(QuantExpert):
 
     @classmethod
     def from_bf16(cls, gate, up, down):
+        """gate may be None (a non-gated ReLU2 expert)."""
         cs, ss = [], []
         for w in (gate, up, down):
+            if w is None:
+                cs.append(None), ss.append(None)
+                continue
             wf = (np.asarray(as_bf16_bits(w), np.uint32) << 16).view(np.float32)
             c, s = mx_quantize(wf, "e2m1")
             cs.append(c), ss.append(s)

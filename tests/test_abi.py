@@ -113,7 +113,7 @@ def test_run_kernel_count(moe):
 
 def test_variant_flags_and_bias_rejections(moe):
     cfg = moe.make_config(8, 256, 512, 2)
-    cfg.flags = 32                                 # not a defined variant bit
+    cfg.flags = 64                                 # not a defined variant bit
     assert moe.config_check(cfg) == -1
     cfg.flags = 4 | 8                              # two activations at once
     assert moe.config_check(cfg) == -1

@@ -3,17 +3,20 @@ the GEMMs, h rounded to BF16; "b12x" README, section "What's in here", moe: "W4A
 activations, inline FP4 weight dequant - no activation-scale math)") through the C ABI against
 the oracle's act_mode 1.
 
-Bit-exact: router ids, counts, offsets, permutation.  The BF16 h: at most 0.1% of its values
-differ from the oracle's, each by one BF16 step (the tensor core sums the products in its own
-order, so a value within rounding noise of a BF16 rounding boundary has two correct roundings).
-The output: relative L2 <= 5e-3 and max |err| <= 3e-2 * RMS."""
+Bit-exact: router ids, counts, offsets, permutation.  The BF16 h: the tensor core sums the
+products in its own order, so the FP32 g and u differ from the oracle's sequential sums by
+rounding (relative ~sqrt(K) * 2^-24), and a value within that distance of a BF16 rounding
+boundary rounds the other way: about one value in 10^3.  Asserted: at most 1% of the values
+differ, each by at most one BF16 step of the oracle's value plus 2^-12 of the row's largest
+|h| (values near zero, where g * sigmoid(g) * u or u^2 cancel to far below the row's scale,
+move by more steps than one).  The output: relative L2 <= 5e-3 and max |err| <= 3e-2 * RMS."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 import synth
-from parity import H_CODE_FRAC, assert_y_close, bf16_to_np_bits
+from parity import assert_y_close, bf16_to_np_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -27,17 +30,17 @@ def moe():
     return m
 
 
-def bf16_rank(bits):
-    """BF16 bit patterns -> integers in the order of the values (+0 and -0 both 0)."""
-    b = bits.astype(np.int32)
-    return np.where(b & 0x8000, -(b & 0x7FFF), b & 0x7FFF)
-
-
 def assert_hb_close(gpu_bits, ref_bits):
-    d = np.abs(bf16_rank(gpu_bits) - bf16_rank(ref_bits))
+    g = (gpu_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    r = (ref_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    d = np.abs(g - r)
+    mag = np.abs(r)
+    ulp = np.exp2(np.floor(np.log2(np.maximum(mag, 1e-38))) - 7)
+    row_max = np.abs(r).max(axis=1, keepdims=True)
+    bound = ulp + 2.0 ** -12 * row_max
     frac = float(np.mean(d > 0)) if d.size else 0.0
-    assert frac <= H_CODE_FRAC and (d.max() if d.size else 0) <= 1, \
-        f"h (BF16): {frac:.2e} differ, max step {d.max()}"
+    assert frac <= 1e-2, f"h (BF16): {frac:.2e} of the values differ"
+    assert (d <= bound).all(), f"h (BF16): max |diff| / bound = {(d / bound).max():.2f}"
     return frac
 
 
