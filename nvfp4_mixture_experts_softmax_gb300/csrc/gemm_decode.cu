@@ -64,7 +64,6 @@ constexpr uint32_t kSfCol0 = kAccBufs * kAccCols;
 constexpr uint32_t kSfColsPerStage = 32;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int kBarBytes = 512;                          // mbarriers + TMEM slot
-constexpr uint32_t kPrefetchAhead = 12;                 // L2 prefetch distance, in weight blocks
 
 static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "tensor memory budget");
 static_assert(kStageBytes % 1024 == 0 && kXOff % 1024 == 0, "1024-byte aligned swizzled tiles");
@@ -241,67 +240,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- weight blocks: one bulk copy per stage ----------------
     // Weights depend on nothing but the plan, so this thread only waits for free ring slots;
     // the stage's token rows come from the token issuer (warp kXWarp), and the stage's full
-    // barrier completes once both parts have landed.  While the ring is full (the first stages
-    // wait for the prologue's token rows, later ones for the MMAs), the thread asks the L2 for
-    // the CTA's next weight blocks (bulk prefetch, up to kPrefetchAhead blocks past the ring), so
-    // the HBM stream keeps going and the copies that follow are served from the L2.
+    // barrier completes once both parts have landed.
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0, n_issued = 0;
       bool ok = true;
-      // cursors over this CTA's weight blocks: the next to copy and the next to prefetch
-      int c_item = blockIdx.x, c_ks = 0, c_kst = 0;
-      int f_item = blockIdx.x, f_ks = 0, f_kst = 0;
-      uint32_t f_idx = 0;
-      const uint8_t* c_src = nullptr;
-      const uint8_t* f_src = nullptr;
-      auto block_base = [&](int item, int& kst) -> const uint8_t* {
+      for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
         const Item t = NVFP4MOE_ITEM(item);
         const GemmArgs& q = t.ph ? p.g2 : p.g1;
-        kst = t.kst;
-        return q.b_tiles + (size_t)t.seg * q.b_per_seg + (size_t)t.nt * t.kst * kTileBlockBytes;
-      };
-      if (c_item < total) {
-        c_src = block_base(c_item, c_kst);
-        f_src = c_src;
-        f_kst = c_kst;
-      }
-      while (c_item < total && ok) {
-        const uint32_t eb = smem_u32(empty + stage);
-        if (!mbar_test_wait(eb, phase ^ 1u)) {
-          // the ring is full: prefetch a later block, or wait (bounded) once there is none
-          if (f_idx < n_issued) {   // catch up with the copies
-            f_item = c_item;
-            f_ks = c_ks;
-            f_kst = c_kst;
-            f_src = c_src;
-            f_idx = n_issued;
-          }
-          if (f_item < total && f_idx < n_issued + kPrefetchAhead) {
-            bulk_prefetch_l2(f_src + (size_t)f_ks * kTileBlockBytes, kTileBlockBytes);
-            ++f_idx;
-            if (++f_ks == f_kst) {
-              f_item += gridDim.x;
-              f_ks = 0;
-              if (f_item < total) f_src = block_base(f_item, f_kst);
-            }
-            continue;
-          }
-          if (!mbar_wait_bounded(eb, phase ^ 1u, kWaitLimitNs, status)) {
+        const uint8_t* src = q.b_tiles + (size_t)t.seg * q.b_per_seg +
+                             (size_t)t.nt * t.kst * kTileBlockBytes;
+        for (int ks = 0; ks < t.kst; ++ks) {
+          if (!mbar_wait_bounded(smem_u32(empty + stage), phase ^ 1u, kWaitLimitNs, status)) {
             ok = false;
             break;
           }
-        }
-        const uint32_t fb = smem_u32(full + stage);
-        mbar_arrive_expect_tx(fb, kTileBlockBytes);
-        bulk_load(smem0 + stage * kStageBytes, c_src + (size_t)c_ks * kTileBlockBytes,
-                  kTileBlockBytes, fb);
-        ++n_issued;
-        if (++stage == kStages) { stage = 0; phase ^= 1u; }
-        if (++c_ks == c_kst) {
-          c_item += gridDim.x;
-          c_ks = 0;
-          if (c_item < total) c_src = block_base(c_item, c_kst);
+          const uint32_t fb = smem_u32(full + stage);
+          mbar_arrive_expect_tx(fb, kTileBlockBytes);
+          bulk_load(smem0 + stage * kStageBytes, src + (size_t)ks * kTileBlockBytes,
+                    kTileBlockBytes, fb);
+          ++n_issued;
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
       // the MMAs of the last stages must finish before the CTA may exit
