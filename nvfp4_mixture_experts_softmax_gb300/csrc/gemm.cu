@@ -56,21 +56,29 @@ static_assert(kBN == 128 && kTileBlockBytes == kBN * 128 + kSfBytes, "packed blo
 static_assert(kBOff % 1024 == 0, "B tile stays 1024-byte aligned for the 128B swizzle");
 static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
 
-// The reducing epilogue (mode 1) transposes each warp's 32 x 32 FP32 chunk through shared memory
-// so that one vector reduction instruction covers four rows x 128 contiguous bytes (eight lanes per
-// row) instead of 32 scattered 16-byte pieces: a quarter of the L2 requests, full sectors each.
-// 16-byte unit q of row r sits at r * 128 + ((q ^ (r & 7)) * 16), which keeps both the row-wise
-// stores and the column-wise loads free of bank conflicts.
-constexpr int kStgBufBytes = 32 * 128;
-constexpr int kStgBytes = kEpiWarps * kStgBufBytes;
+// The reducing epilogue (mode 1) adds router-weighted FP32 rows into the L2-resident token
+// accumulator in one of two ways:
+//  kRed == 1: each warp's 32 x 32 chunk is transposed through shared memory so that one vector
+//    reduction instruction covers four rows x 128 contiguous bytes (eight lanes per row).
+//    16-byte unit q of row r sits at r * 128 + ((q ^ (r & 7)) * 16): conflict free both ways.
+//    4 KB per warp.
+//  kRed == 2: each lane's whole 128-column row goes to shared memory and then to the bulk-copy
+//    engine as one 512-byte reduce-add, performed by the memory system; rows sit 528 bytes apart
+//    so the eight lanes of a 16-byte store phase cover all 32 banks.  16.5 KB per warp.
+// The second frees the epilogue warps sooner (one instruction per row instead of 32) but its
+// rows cost the ring a stage; it wins when an item has few K stages (the epilogue dominates).
+constexpr int kRedRowStride = kBN * 4 + 16;
+template <int kRed>
+constexpr int stg_buf_bytes() { return kRed == 2 ? 32 * kRedRowStride : kRed == 1 ? 32 * 128 : 0; }
 
-// Ring depth: 6 stages for the SwiGLU / row-store epilogues, 5 when the reduction staging takes
-// its share of shared memory.
-template <bool kRedStage>
+// Ring depth: 6 stages for the SwiGLU / row-store epilogues, 5 with the transpose buffers, 4 with
+// the bulk-reduction rows.
+template <int kRed>
 struct GemmShape {
-  static constexpr int kStages = kRedStage ? 5 : 6;
+  static constexpr int kStages = kRed == 2 ? 4 : kRed == 1 ? 5 : 6;
+  static constexpr int kStgBufBytes = stg_buf_bytes<kRed>();
   static constexpr int kStgOff = kStages * kStageBytes;
-  static constexpr int kBarOff = kStgOff + (kRedStage ? kStgBytes : 0);
+  static constexpr int kBarOff = kStgOff + kEpiWarps * kStgBufBytes;
   static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "tensor memory budget");
   static_assert(kBarOff + 1024 + 256 + 8 * 1027 <= 232448, "shared memory");
   // full, empty, sf_done per stage; two acc_full, two acc_empty, drain, sf_drain; TMEM slot and
@@ -106,14 +114,14 @@ __device__ __forceinline__ TileInfo decode_tile(int item, int n_tiles, const int
   return t;
 }
 
-template <bool kRedStage>
+template <int kRed>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmArgs p) {
-  constexpr int kStages = GemmShape<kRedStage>::kStages;
+  constexpr int kStages = GemmShape<kRed>::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + GemmShape<kRedStage>::kBarOff);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + GemmShape<kRed>::kBarOff);
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* acc_full = bars + 2 * kStages;
@@ -124,7 +132,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_drain + 1);
   uint32_t* s_issued = tmem_slot + 1;       // stage fills the copy thread issued
   volatile uint32_t* s_abort = s_issued + 1;   // set by any role whose bounded wait ran out
-  int32_t* s_tile = reinterpret_cast<int32_t*>(smem + GemmShape<kRedStage>::kBarOff + 256);
+  int32_t* s_tile = reinterpret_cast<int32_t*>(smem + GemmShape<kRed>::kBarOff + 256);
   int32_t* s_seg = s_tile + (p.nseg + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -215,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = make_idesc(kBM, kBN);
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t acc_phase[2] = {0u, 0u};
+      uint32_t acc_phase = 0u;   // bit b: the phase of accumulator buffer b
       // stage 0's operand descriptors; a stage (or a K step) further is an addition to the
       // 14-bit address field, which never carries (shared addresses stay below 256 KB)
       const uint64_t dA0 = smem_desc(smem0, 16, 1024, kLayoutSwizzle128B);
@@ -224,12 +232,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0;
       for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++it) {
         const int abuf = it & 1;
-        if (!mbar_wait_bounded(smem_u32(acc_empty + abuf), acc_phase[abuf] ^ 1u, kWaitLimitNs,
+        const uint32_t acc_par = (acc_phase >> abuf) & 1u;
+        if (!mbar_wait_bounded(smem_u32(acc_empty + abuf), acc_par ^ 1u, kWaitLimitNs,
                                p.status)) {
           ok = false;
           break;
         }
-        acc_phase[abuf] ^= 1u;
+        acc_phase ^= 1u << abuf;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + abuf * kAccCols;
         for (int ks = 0; ks < kst; ++ks) {
@@ -286,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------- epilogue (warps 0-3) ----------------
-    uint32_t acc_phase[2] = {0u, 0u};
+    uint32_t acc_phase = 0u;   // bit b: the phase of accumulator buffer b
     int it = 0;
     const int r = warp * 32 + lane;   // this thread's accumulator lane = tile row
     const float ts_a = p.mode == 0 ? *p.ts_a : 0.0f;
@@ -296,12 +305,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int abuf = it & 1;
       // every lane waits; the decision is taken together so that the warp never diverges
       // before the warp-wide tensor-memory loads
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(acc_full + abuf), acc_phase[abuf],
+      const uint32_t acc_par = (acc_phase >> abuf) & 1u;
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(acc_full + abuf), acc_par,
                                                      kWaitLimitNs, p.status))) {
         if (lane == 0) *s_abort = 1u;
         break;
       }
-      acc_phase[abuf] ^= 1u;
+      acc_phase ^= 1u << abuf;
       tc_fence_after();
       const int prow = t.m0 + r;
       const bool valid = r < t.rows && prow >= 0 && prow < p.out_rows;
@@ -355,27 +365,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             tok = 0;
           }
         }
-        float* yrow = p.mode == 1 ? p.yacc + (size_t)tok * p.N + t.nt * kBN
-                                  : p.obuf + (size_t)(ok_row ? prow : 0) * p.N + t.nt * kBN;
+        if constexpr (kRed == 2) {
+          const uint32_t srow = smem0 + GemmShape<kRed>::kStgOff +
+                                (uint32_t)warp * GemmShape<kRed>::kStgBufBytes +
+                                (uint32_t)lane * kRedRowStride;
+          bulk_wait_group_read<0>();   // this lane's previous reduction has read its row
 #pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tbase + c * 32, v);
-          tmem_ld_wait();
-          if constexpr (kRedStage) {
-            const uint32_t stg = smem0 + GemmShape<kRedStage>::kStgOff + (uint32_t)warp * kStgBufBytes;
-            const uint32_t wrow = stg + (uint32_t)lane * 128;
+          for (int c = 0; c < kBN / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tbase + c * 32, v);
+            tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float4 d = make_float4((__uint_as_float(v[4 * i]) * alpha) * wr,
-                                           (__uint_as_float(v[4 * i + 1]) * alpha) * wr,
-                                           (__uint_as_float(v[4 * i + 2]) * alpha) * wr,
-                                           (__uint_as_float(v[4 * i + 3]) * alpha) * wr);
+            for (int i = 0; i < 8; ++i)
+              asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(
+                               srow + (uint32_t)(c * 128 + i * 16)),
+                           "f"((__uint_as_float(v[4 * i]) * alpha) * wr),
+                           "f"((__uint_as_float(v[4 * i + 1]) * alpha) * wr),
+                           "f"((__uint_as_float(v[4 * i + 2]) * alpha) * wr),
+                           "f"((__uint_as_float(v[4 * i + 3]) * alpha) * wr)
+                           : "memory");
+          }
+          if (ok_row) {
+            fence_proxy_async_smem();   // the row's stores, before the bulk engine reads them
+            bulk_reduce_add_f32(p.yacc + (size_t)tok * p.N + t.nt * kBN, srow, kBN * 4);
+            bulk_commit_group();
+          }
+        } else if constexpr (kRed == 1) {
+          const uint32_t stg = smem0 + GemmShape<kRed>::kStgOff +
+                               (uint32_t)warp * GemmShape<kRed>::kStgBufBytes;
+          const uint32_t wrow = stg + (uint32_t)lane * 128;
+#pragma unroll 1
+          for (int c = 0; c < kBN / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tbase + c * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
               asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(
                                wrow + (uint32_t)((i ^ (lane & 7)) * 16)),
-                           "f"(d.x), "f"(d.y), "f"(d.z), "f"(d.w)
+                           "f"((__uint_as_float(v[4 * i]) * alpha) * wr),
+                           "f"((__uint_as_float(v[4 * i + 1]) * alpha) * wr),
+                           "f"((__uint_as_float(v[4 * i + 2]) * alpha) * wr),
+                           "f"((__uint_as_float(v[4 * i + 3]) * alpha) * wr)
                            : "memory");
-            }
             __syncwarp();
             // lane l adds 16 bytes (unit l % 8) of row 4 * j + l / 8
             const int q = lane & 7;
@@ -393,15 +425,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                            d.z, d.w);
             }
             __syncwarp();
-          } else if (ok_row) {
+          }
+        } else {
+          float* yrow = p.obuf + (size_t)(ok_row ? prow : 0) * p.N + t.nt * kBN;
+#pragma unroll 1
+          for (int c = 0; c < kBN / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tbase + c * 32, v);
+            tmem_ld_wait();
+            if (ok_row) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float4 d = make_float4((__uint_as_float(v[4 * i]) * alpha) * wr,
-                                           (__uint_as_float(v[4 * i + 1]) * alpha) * wr,
-                                           (__uint_as_float(v[4 * i + 2]) * alpha) * wr,
-                                           (__uint_as_float(v[4 * i + 3]) * alpha) * wr);
-              if (p.mode == 1) red_add_v4(yrow + c * 32 + 4 * i, d.x, d.y, d.z, d.w);
-              else *reinterpret_cast<float4*>(yrow + c * 32 + 4 * i) = d;
+              for (int i = 0; i < 8; ++i)
+                *reinterpret_cast<float4*>(yrow + c * 32 + 4 * i) =
+                    make_float4((__uint_as_float(v[4 * i]) * alpha) * wr,
+                                (__uint_as_float(v[4 * i + 1]) * alpha) * wr,
+                                (__uint_as_float(v[4 * i + 2]) * alpha) * wr,
+                                (__uint_as_float(v[4 * i + 3]) * alpha) * wr);
             }
           }
         }
@@ -415,7 +454,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Teardown.  After a wait ran out, stage fills and scale copies may still be in flight: the
   // copy thread's last kStages fills and the scale-factor thread's last tensor-memory copies are
   // waited for (bounded) before tensor memory is released.  Without a timeout every fill and
-  // copy was consumed by a completed MMA, and none of this runs.
+  // copy was consumed by a completed MMA, and none of this runs.  The reducing epilogue first
+  // waits for its row reductions, whose sources live in shared memory.
+  if constexpr (kRed == 2)
+    if (warp < kEpiWarps) bulk_wait_group<0>();
   tc_fence_before();
   __syncthreads();
   if (*s_abort) {
@@ -438,21 +480,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool kRedStage>
+template <int kRed>
 size_t gemm_smem_bytes(int nseg) {
-  return 1024 + (size_t)GemmShape<kRedStage>::kBarOff + 256 + sizeof(int32_t) * 2 * (nseg + 2);
+  return 1024 + (size_t)GemmShape<kRed>::kBarOff + 256 + sizeof(int32_t) * 2 * (nseg + 2);
 }
 
-template <bool kRedStage>
+template <int kRed>
 cudaError_t launch_kernel(const CUtensorMap& tmap, const GemmArgs& a, cudaStream_t s) {
-  const size_t smem = gemm_smem_bytes<kRedStage>(a.nseg);
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<kRedStage>,
+  const size_t smem = gemm_smem_bytes<kRed>(a.nseg);
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<kRed>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int grid = a.max_ctas;
   if (grid > num_sms()) grid = num_sms();
   if (grid < 1) grid = 1;
-  return launch_pdl(grouped_gemm_kernel<kRedStage>, dim3(grid), dim3(kThreads), smem, s, tmap, a);
+  return launch_pdl(grouped_gemm_kernel<kRed>, dim3(grid), dim3(kThreads), smem, s, tmap, a);
 }
 
 }  // namespace
@@ -483,7 +525,11 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s) {
              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  return a.mode == 1 ? launch_kernel<true>(tmap, a, s) : launch_kernel<false>(tmap, a, s);
+  // reductions: bulk rows when an item has at most four K stages (measured: prefill GEMM2, K=512,
+  // 217 -> 154 us), the transposed vector reductions and their deeper ring otherwise (K=1536 and
+  // 2048 were 2-6% slower with bulk rows)
+  if (a.mode != 1) return launch_kernel<0>(tmap, a, s);
+  return a.K <= 4 * kBK ? launch_kernel<2>(tmap, a, s) : launch_kernel<1>(tmap, a, s);
 }
 
 }  // namespace nvfp4moe

@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t acc_phase[kAccBufs] = {};
+      uint32_t acc_phase = 0u;   // bit b: the phase of accumulator buffer b
       // stage 0's operand descriptors; a stage (or a K step) further is an addition to the
       // 14-bit address field, which never carries (shared addresses stay below 256 KB)
       const uint64_t dA0 = smem_desc(smem0, 16, 1024, kLayoutSwizzle128B);
@@ -340,12 +340,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nmma = max(16, (t.rows + 15) & ~15);
         const uint32_t idesc = make_idesc(128, nmma);
         const int abuf = it % kAccBufs;
-        if (!mbar_wait_bounded(smem_u32(acc_empty + abuf), acc_phase[abuf] ^ 1u, kWaitLimitNs,
+        const uint32_t acc_par = (acc_phase >> abuf) & 1u;
+        if (!mbar_wait_bounded(smem_u32(acc_empty + abuf), acc_par ^ 1u, kWaitLimitNs,
                                status)) {
           ok = false;
           break;
         }
-        acc_phase[abuf] ^= 1u;
+        acc_phase ^= 1u << abuf;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + abuf * kAccCols;
         for (int ks = 0; ks < t.kst; ++ks) {
@@ -403,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------- epilogue (warps 0-3): lane = weight row, column = token ----------------
     griddep_wait();     // the activation tensor scale and the router weights
-    uint32_t acc_phase[kAccBufs] = {};
+    uint32_t acc_phase = 0u;   // bit b: the phase of accumulator buffer b
     int it = 0;
     const float ts_a = *p.g1.ts_a;
     const float ts_h = p.g1.ts_h;
@@ -415,12 +416,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int abuf = it % kAccBufs;
       // every lane waits; the decision is taken together so that the warp never diverges
       // before the warp-wide tensor-memory loads
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(acc_full + abuf), acc_phase[abuf],
+      const uint32_t acc_par = (acc_phase >> abuf) & 1u;
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(acc_full + abuf), acc_par,
                                                      kWaitLimitNs, status))) {
         if (lane == 0) *s_abort = 1u;
         break;
       }
-      acc_phase[abuf] ^= 1u;
+      acc_phase ^= 1u << abuf;
       tc_fence_after();
       const int rows = (t.m0 >= 0 && t.m0 + t.rows <= q.out_rows) ? t.rows : 0;
       const uint32_t tbase = tmem_base + abuf * kAccCols + ((uint32_t)(warp * 32) << 16);

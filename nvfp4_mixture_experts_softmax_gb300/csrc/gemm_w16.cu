@@ -340,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = make_idesc_bf16(kBM, kBN);
       int ss = 0;
       uint32_t sph = 0;
-      uint32_t acc_phase[2] = {0u, 0u};
+      uint32_t acc_phase = 0u;   // bit b: the phase of accumulator buffer b
       const uint64_t dA0 = smem_desc(smem0, 16, 1024, kLayoutSwizzle128B);
       const uint64_t dB0 = smem_desc(smem0 + kTileBytes16, 16, 1024, kLayoutSwizzle128B);
       bool ok = true;
@@ -348,12 +348,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nsub = kblk * (kBK / kSubK);
       for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++it) {
         const int abuf = it & 1;
-        if (!mbar_wait_bounded(smem_u32(acc_empty + abuf), acc_phase[abuf] ^ 1u, kWaitLimitNs,
+        const uint32_t acc_par = (acc_phase >> abuf) & 1u;
+        if (!mbar_wait_bounded(smem_u32(acc_empty + abuf), acc_par ^ 1u, kWaitLimitNs,
                                p.status)) {
           ok = false;
           break;
         }
-        acc_phase[abuf] ^= 1u;
+        acc_phase ^= 1u << abuf;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + abuf * kBN;
         for (int k = 0; k < nsub; ++k) {
@@ -378,18 +379,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------- epilogue (warps 0-3): one accumulator row per thread ----------------
-    uint32_t acc_phase[2] = {0u, 0u};
+    uint32_t acc_phase = 0u;   // bit b: the phase of accumulator buffer b
     int it = 0;
     const int r = warp * 32 + lane;
     for (int item = blockIdx.x; item < total; item += gridDim.x, ++it) {
       const TileW16 t = decode_tile_w16(item, n_tiles, s_tile, s_seg, p.nseg);
       const int abuf = it & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(acc_full + abuf), acc_phase[abuf],
+      const uint32_t acc_par = (acc_phase >> abuf) & 1u;
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(acc_full + abuf), acc_par,
                                                      kWaitLimitNs, p.status))) {
         if (lane == 0) *s_abort = 1u;
         break;
       }
-      acc_phase[abuf] ^= 1u;
+      acc_phase ^= 1u << abuf;
       tc_fence_after();
       const int prow = t.m0 + r;
       const bool valid = r < t.rows && prow >= 0 && prow < p.out_rows;
