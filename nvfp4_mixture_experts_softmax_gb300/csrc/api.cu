@@ -409,8 +409,9 @@ int run_layer(const moe_config* cfg, const void* wbuf, const void* x, const uint
     pr.H = H;
     pr.status = &hdr->status;
     pr.ts = &hdr->ts;
-    pr.xq = ws + L.xq;
-    pr.xsf = ws + L.xsf;
+    // token-order codes feed nothing on this path but the debug copies
+    pr.xq = debug ? ws + L.xq : nullptr;
+    pr.xsf = debug ? ws + L.xsf : nullptr;
     pr.xq_perm = ws + L.xq_perm;
     pr.xsf_tiles = ws + L.xsf_tiles;
     pr.logits = logits;

@@ -362,7 +362,7 @@ struct DecodePrologueArgs {
   int T, H;
   int32_t* status;
   float* ts;
-  uint8_t* xq;             // [T, H/2]  token order
+  uint8_t* xq;             // [T, H/2]  token order (null: not written)
   uint8_t* xsf;            // [T, H/16]
   uint8_t* xq_perm;        // [Rt, H/2] permuted (expert) order
   uint8_t* xsf_tiles;      // [tiles][H/64][512] token-operand scale arrangement

@@ -132,8 +132,11 @@ __global__ void __launch_bounds__(kSmallPlanThreads) decode_prologue_kernel(cons
   // (already quantised input: the block's 8 code bytes and its scale byte instead)
   const bool qin = a.in_xq != nullptr;
   const int64_t nblk = (int64_t)T * nkb;
+  // 32-block chunks (one per warp: coalesced stores) dealt round robin over the cluster's CTAs,
+  // so that a small batch spreads its encode stores over every CTA's memory pipeline instead of
+  // loading the first CTA with all of them (T=8: one SM's 20k scattered stores took ~4 us)
   const int64_t bstride = (int64_t)C * blockDim.x;
-  const int64_t u0 = (int64_t)rank * blockDim.x + threadIdx.x;
+  const int64_t u0 = ((int64_t)warp * C + rank) * 32 + lane;
   uint4 xa = make_uint4(0u, 0u, 0u, 0u), xb = xa;
   if (u0 < nblk) {
     if (qin) {
@@ -315,8 +318,10 @@ __global__ void __launch_bounds__(kSmallPlanThreads) decode_prologue_kernel(cons
       sf = v0.z;
     } else {
       quant_bf16_regs16(v0, v1, ts, lo, hi, sf);
-      reinterpret_cast<uint2*>(a.xq)[u] = make_uint2(lo, hi);
-      a.xsf[u] = (uint8_t)sf;
+      if (a.xq) {
+        reinterpret_cast<uint2*>(a.xq)[u] = make_uint2(lo, hi);
+        a.xsf[u] = (uint8_t)sf;
+      }
     }
     const long long boff = (long long)(b >> 2) * 512 + (b & 3);
     for (int j = 0; j < kd; ++j) {
