@@ -52,7 +52,7 @@ typedef struct CUstream_st* moe_stream_t; /* the same type as cudaStream_t */
 typedef enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = -1,       /* null pointer, k < 1 or k > E, negative size ... */
-  MOE_ERR_UNSUPPORTED_SHAPE = -2, /* H or I not a multiple of 256, T > max_tokens, E > 1024 ... */
+  MOE_ERR_UNSUPPORTED_SHAPE = -2, /* H or I not a multiple of 32, T > max_tokens, E > 1024 ... */
   MOE_ERR_WORKSPACE_TOO_SMALL = -3,
   MOE_ERR_CUDA = -4,              /* a CUDA runtime call failed (launch error ...) */
   MOE_ERR_DEVICE_TIMEOUT = -5,    /* device status: a bounded pipeline wait ran out */
@@ -63,8 +63,8 @@ typedef enum {
 /* Shape of one MoE layer. */
 typedef struct {
   int32_t num_experts;   /* E, routed experts, 1..1024 */
-  int32_t hidden;        /* H, multiple of 256 */
-  int32_t inter;         /* I, routed-expert intermediate size, multiple of 256 */
+  int32_t hidden;        /* H, multiple of 32 (16-byte code rows); see the note below */
+  int32_t inter;         /* I, routed-expert intermediate size, multiple of 32 */
   int32_t top_k;         /* k, 1..min(E, 32) */
   int32_t shared_inter;  /* 0: no shared expert; otherwise its intermediate size (must equal I) */
   float h_tensor_scale;  /* fixed FP32 tensor scale used to requantise h (1.0 by default) */
@@ -73,6 +73,14 @@ typedef struct {
   float swiglu_limit;    /* L of MOE_FLAG_SWIGLU_CLAMP and MOE_FLAG_ACT_SWIGLU_OAI: finite, >= 0 */
   float swiglu_alpha;    /* slope of MOE_FLAG_ACT_SWIGLU_OAI (1.702 in gpt-oss): finite */
 } moe_config;
+
+/* Widths.  H and I need only be multiples of 32.  A width that is not a multiple of 256 (the K
+ * stage of the packed weight blocks) is padded inside the library: the weight buffer holds zero
+ * rows and columns up to the next multiple of 256 (moe_weights_size counts them), and moe_run /
+ * moe_run_quantized copy x (or its codes and scales) into zero-padded rows of the workspace and
+ * the output rows back into y (moe_workspace_size counts both buffers).  The results are those
+ * of the unpadded layer: a padded column of x meets only zero weights, and a padded feature of
+ * h is activation(0, 0) = 0 for every activation flag, quantised to a zero block. */
 
 /* Router variant ("vllm.cpp docs/STATUS.md", paragraph "W6 sqrtsoftplus + hash-routed MoE";
  * "nvfp4-megamoe-kernel compare pre-b1...master", section "Dense Router (L3+)"): expert scores

@@ -15,6 +15,14 @@ inline cudaStream_t to_cuda(moe_stream_t s) { return reinterpret_cast<cudaStream
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Workspace behind the layer's own when a width is padded (pc = padded_config(c)): x, or its
+// codes and scales, in rows of the padded width; then the BF16 output rows before their copy
+// into y.
+size_t pad_bytes(const moe_config& c, const moe_config& pc, int32_t T) {
+  if (!needs_padding(c)) return 0;
+  return 2 * align_up((size_t)T * pc.hidden * 2);
+}
+
 int check_cfg(const moe_config* c) {
   if (!c) return MOE_ERR_INVALID_ARG;
   const uint32_t acts = MOE_FLAG_SWIGLU_CLAMP | MOE_FLAG_ACT_RELU2 | MOE_FLAG_ACT_SWIGLU_OAI;
@@ -33,7 +41,8 @@ int check_cfg(const moe_config* c) {
   if (c->top_k > c->num_experts) return MOE_ERR_INVALID_ARG;
   if (!(std::isfinite(c->h_tensor_scale) && c->h_tensor_scale > 0.0f)) return MOE_ERR_INVALID_ARG;
   if (c->num_experts > 1024 || c->top_k > 32) return MOE_ERR_UNSUPPORTED_SHAPE;
-  if (c->hidden % kBK != 0 || c->inter % kBK != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (c->hidden % 32 != 0 || c->inter % 32 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (c->hidden > (1 << 20) || c->inter > (1 << 20)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (c->shared_inter != 0 && c->shared_inter != c->inter) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (c->shared_inter < 0) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
@@ -63,7 +72,7 @@ int moe_config_check(const moe_config* cfg) { return check_cfg(cfg); }
 
 size_t moe_weights_size(const moe_config* cfg) {
   if (check_cfg(cfg) != MOE_OK) return 0;
-  return WeightLayout(*cfg).total;
+  return WeightLayout(padded_config(*cfg)).total;
 }
 
 int moe_quantize_weights(const moe_config* cfg, const void* w_gate, const void* w_up,
@@ -84,11 +93,14 @@ int moe_quantize_weights(const moe_config* cfg, const void* w_gate, const void* 
     for (const void* p : {s_gate, s_up, s_down})
       if (p && !aligned(p, 16)) return MOE_ERR_INVALID_ARG;
   if (!aligned(wbuf, kAlign)) return MOE_ERR_INVALID_ARG;
-  const WeightLayout L(*cfg);
+  const WeightLayout L(padded_config(*cfg));
   if (wbuf_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t s = to_cuda(stream);
   uint8_t* wb = static_cast<uint8_t*>(wbuf);
   if (cudaMemsetAsync(wb + L.bias, 0, sizeof(float) * L.E, s) != cudaSuccess) return MOE_ERR_CUDA;
+  // padded widths: the packed blocks' padding rows and columns are zero codes and zero scales
+  if (needs_padding(*cfg) && cudaMemsetAsync(wb + L.w13, 0, L.ts - L.w13, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
   return cuda_status(launch_weight_quant(*cfg, L, w_gate, w_up, w_down, s_gate, s_up, s_down, wb, s));
 }
 
@@ -96,7 +108,7 @@ int moe_set_router_bias(const moe_config* cfg, void* wbuf, const float* bias, mo
   int st = check_cfg(cfg);
   if (st != MOE_OK) return st;
   if (!wbuf || !bias || !aligned(wbuf, kAlign)) return MOE_ERR_INVALID_ARG;
-  const WeightLayout L(*cfg);
+  const WeightLayout L(padded_config(*cfg));
   return cuda_status(cudaMemcpyAsync(static_cast<uint8_t*>(wbuf) + L.bias, bias,
                                      sizeof(float) * L.E, cudaMemcpyDeviceToDevice,
                                      to_cuda(stream)));
@@ -120,7 +132,7 @@ int moe_weights_export(const moe_config* cfg, const void* wbuf, int32_t expert, 
     return MOE_ERR_INVALID_ARG;
   }
   if (!aligned(codes, 8)) return MOE_ERR_INVALID_ARG;
-  const WeightLayout L(*cfg);
+  const WeightLayout L(padded_config(*cfg));
   return cuda_status(launch_weight_export(*cfg, L, static_cast<const uint8_t*>(wbuf), slot, matrix,
                                           codes, sf, ts, to_cuda(stream)));
 }
@@ -222,7 +234,8 @@ int moe_plan(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* topk
 
 size_t moe_workspace_size(const moe_config* cfg, int32_t T) {
   if (check_cfg(cfg) != MOE_OK || T < 0) return 0;
-  return RunLayout(*cfg, T).total;
+  const moe_config pc = padded_config(*cfg);
+  return RunLayout(pc, T).total + pad_bytes(*cfg, pc, T);
 }
 
 int moe_run_kernel_count(const moe_config* cfg, int32_t T) {
@@ -230,7 +243,7 @@ int moe_run_kernel_count(const moe_config* cfg, int32_t T) {
   if (st != MOE_OK) return st;
   if (T < 0) return MOE_ERR_INVALID_ARG;
   if (T == 0) return 0;
-  const RunLayout L(*cfg, T);
+  const RunLayout L(padded_config(*cfg), T);
   if (L.decode) return 3;     // cluster prologue, both grouped GEMMs, row sum
   if (L.small) return 5;      // one-block prologue, permute, GEMM1, GEMM2, row sum
   // accumulator zeroing (+ amax), router/plan (1 or 3), encode (or, W4A16, the BF16 rows) into
@@ -243,11 +256,13 @@ int moe_run_kernel_count(const moe_config* cfg, int32_t T) {
 namespace {
 
 // The layer for BF16 input x (qx == nullptr) or for already quantised input (qx: codes
-// [T, H/2], qsf: scales [T, H/16], qts: device tensor scale; x unused).
-int run_layer(const moe_config* cfg, const void* wbuf, const void* x, const uint8_t* qx,
-              const uint8_t* qsf, const float* qts, const float* logits, int32_t T, int32_t k,
-              void* y, void* workspace, size_t ws_bytes, moe_stream_t stream,
-              const moe_debug* debug) {
+// [T, H/2], qsf: scales [T, H/16], qts: device tensor scale; x unused), at widths that are
+// multiples of 256.  Hl, Il: the caller's widths (equal to cfg's unless run_layer padded them),
+// used for the debug copies.
+int run_core(const moe_config* cfg, int Hl, int Il, const void* wbuf, const void* x,
+             const uint8_t* qx, const uint8_t* qsf, const float* qts, const float* logits,
+             int32_t T, int32_t k, void* y, void* workspace, size_t ws_bytes,
+             moe_stream_t stream, const moe_debug* debug) {
   int st = check_cfg(cfg);
   if (st != MOE_OK) return st;
   if (T < 0 || k != cfg->top_k) return MOE_ERR_INVALID_ARG;
@@ -383,18 +398,24 @@ int run_layer(const moe_config* cfg, const void* wbuf, const void* x, const uint
         if (dst && e == cudaSuccess)
           e = cudaMemcpyAsync(dst, ws + off, bytes, cudaMemcpyDeviceToDevice, s);
       };
+      // rows of the caller's width out of rows of the layer's width
+      auto cp2 = [&](void* dst, size_t off, size_t rows, size_t width, size_t pitch) {
+        if (dst && e == cudaSuccess && rows > 0)
+          e = cudaMemcpy2DAsync(dst, width, ws + off, pitch, width, rows,
+                                cudaMemcpyDeviceToDevice, s);
+      };
       const size_t R = (size_t)L.R, Rt = (size_t)L.Rt;
       cp(debug->topk_ids, L.ids, 4 * R);
       cp(debug->topk_w, L.w, 4 * R);
       cp(debug->offsets, L.seg_off, 4 * (size_t)(E + 1));
       cp(debug->perm_src, L.perm_src, 4 * R);
       cp(debug->inv, L.inv, 4 * R);
-      cp(debug->hb, L.hb, Rt * I * 2);
+      cp2(debug->hb, L.hb, Rt, (size_t)Il * 2, (size_t)I * 2);
       if (L.mx) {   // MXFP8 codes and E8M0 scales of x and h
-        cp(debug->xq, L.xq8, (size_t)T * H);
-        cp(debug->xsf, L.xq8 + (size_t)T * H, (size_t)T * H / 32);
-        cp(debug->hq, L.hq8, Rt * I);
-        cp(debug->hsf, L.hq8 + Rt * I, Rt * I / 32);
+        cp2(debug->xq, L.xq8, T, Hl, H);
+        cp2(debug->xsf, L.xq8 + (size_t)T * H, T, Hl / 32, H / 32);
+        cp2(debug->hq, L.hq8, Rt, Il, I);
+        cp2(debug->hsf, L.hq8 + Rt * I, Rt, Il / 32, I / 32);
       }
       if (e != cudaSuccess) return MOE_ERR_CUDA;
     }
@@ -614,6 +635,14 @@ int run_layer(const moe_config* cfg, const void* wbuf, const void* x, const uint
     auto cp = [&](void* dst, size_t off, size_t bytes) {
       if (dst && e == cudaSuccess) e = cudaMemcpyAsync(dst, ws + off, bytes, cudaMemcpyDeviceToDevice, s);
     };
+    // rows of the caller's width out of rows of the layer's width
+    auto cp2p = [&](void* dst, const void* src, size_t rows, size_t width, size_t pitch) {
+      if (dst && e == cudaSuccess && rows > 0)
+        e = cudaMemcpy2DAsync(dst, width, src, pitch, width, rows, cudaMemcpyDeviceToDevice, s);
+    };
+    auto cp2 = [&](void* dst, size_t off, size_t rows, size_t width, size_t pitch) {
+      cp2p(dst, ws + off, rows, width, pitch);
+    };
     const size_t R = (size_t)L.R, Rt = (size_t)L.Rt;
     cp(debug->topk_ids, L.ids, 4 * R);
     cp(debug->topk_w, L.w, 4 * R);
@@ -621,20 +650,74 @@ int run_layer(const moe_config* cfg, const void* wbuf, const void* x, const uint
     cp(debug->perm_src, L.perm_src, 4 * R);
     cp(debug->inv, L.inv, 4 * R);
     if (quantised) {
-      for (auto [dst, src, bytes] : {std::tuple<void*, const void*, size_t>{debug->xq, qx, (size_t)T * H / 2},
-                                     {debug->xsf, qsf, (size_t)T * H / 16}})
-        if (dst && e == cudaSuccess)
-          e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s);
+      cp2p(debug->xq, qx, T, Hl / 2, H / 2);
+      cp2p(debug->xsf, qsf, T, Hl / 16, H / 16);
     } else {
-      cp(debug->xq, L.xq, (size_t)T * H / 2);
-      cp(debug->xsf, L.xsf, (size_t)T * H / 16);
+      cp2(debug->xq, L.xq, T, Hl / 2, H / 2);
+      cp2(debug->xsf, L.xsf, T, Hl / 16, H / 16);
     }
     cp(debug->ts_a, L.hdr + offsetof(WsHeader, ts), 4);
-    cp(debug->hq, L.hq, Rt * I / 2);
-    cp(debug->hsf, L.hsf, Rt * I / 16);
+    cp2(debug->hq, L.hq, Rt, Il / 2, I / 2);
+    cp2(debug->hsf, L.hsf, Rt, Il / 16, I / 16);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   return MOE_OK;
+}
+
+// The layer at the caller's widths: directly when they are multiples of 256, otherwise through
+// zero-padded copies of x (or of its codes and scales) and of the output rows in the workspace
+// behind the layer's own (see padded_config).
+int run_layer(const moe_config* cfg, const void* wbuf, const void* x, const uint8_t* qx,
+              const uint8_t* qsf, const float* qts, const float* logits, int32_t T, int32_t k,
+              void* y, void* workspace, size_t ws_bytes, moe_stream_t stream,
+              const moe_debug* debug) {
+  int st = check_cfg(cfg);
+  if (st != MOE_OK) return st;
+  if (!needs_padding(*cfg))
+    return run_core(cfg, cfg->hidden, cfg->inter, wbuf, x, qx, qsf, qts, logits, T, k, y,
+                    workspace, ws_bytes, stream, debug);
+  if (T < 0 || k != cfg->top_k) return MOE_ERR_INVALID_ARG;
+  if (cfg->max_tokens > 0 && T > cfg->max_tokens) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if ((int64_t)T * (cfg->top_k + 1) > (int64_t)INT32_MAX / 2) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!workspace) return MOE_ERR_INVALID_ARG;
+  const moe_config pc = padded_config(*cfg);
+  const size_t core = RunLayout(pc, T).total;
+  if (ws_bytes < core + pad_bytes(*cfg, pc, T)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned(workspace, kAlign)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  const bool quantised = qx != nullptr || qsf != nullptr || qts != nullptr;
+  if (!y || !aligned(y, 8)) return MOE_ERR_INVALID_ARG;
+  if (quantised) {
+    if (!qx || !qsf || !qts) return MOE_ERR_INVALID_ARG;
+    if (!aligned(qx, 16) || !aligned(qsf, 4) || !aligned(qts, 4)) return MOE_ERR_INVALID_ARG;
+  } else if (!x || !aligned(x, 16)) {
+    return MOE_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = to_cuda(stream);
+  const size_t H = (size_t)cfg->hidden, Hp = (size_t)pc.hidden, rows = (size_t)T;
+  uint8_t* xp = static_cast<uint8_t*>(workspace) + core;
+  uint8_t* yp = xp + align_up(rows * Hp * 2);
+  uint8_t* sfp = xp + align_up(rows * Hp / 2);   // quantised input: the scales after the codes
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  if (quantised) {
+    if (!ok(cudaMemsetAsync(xp, 0, align_up(rows * Hp / 2) + rows * Hp / 16, s)) ||
+        !ok(cudaMemcpy2DAsync(xp, Hp / 2, qx, H / 2, H / 2, rows, cudaMemcpyDeviceToDevice, s)) ||
+        !ok(cudaMemcpy2DAsync(sfp, Hp / 16, qsf, H / 16, H / 16, rows, cudaMemcpyDeviceToDevice,
+                              s)))
+      return MOE_ERR_CUDA;
+    st = run_core(&pc, cfg->hidden, cfg->inter, wbuf, nullptr, xp, sfp, qts, logits, T, k, yp,
+                  workspace, core, stream, debug);
+  } else {
+    if (!ok(cudaMemsetAsync(xp, 0, rows * Hp * 2, s)) ||
+        !ok(cudaMemcpy2DAsync(xp, Hp * 2, x, H * 2, H * 2, rows, cudaMemcpyDeviceToDevice, s)))
+      return MOE_ERR_CUDA;
+    st = run_core(&pc, cfg->hidden, cfg->inter, wbuf, xp, nullptr, nullptr, nullptr, logits, T,
+                  k, yp, workspace, core, stream, debug);
+  }
+  if (st != MOE_OK) return st;
+  return ok(cudaMemcpy2DAsync(y, H * 2, yp, Hp * 2, H * 2, rows, cudaMemcpyDeviceToDevice, s))
+             ? MOE_OK
+             : MOE_ERR_CUDA;
 }
 
 }  // namespace

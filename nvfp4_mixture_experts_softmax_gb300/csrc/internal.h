@@ -50,6 +50,24 @@ constexpr int kTileBytes = 128 * 128;             // codes of one (N tile, K sta
 constexpr int kTileSfBytes = 4 * 512;             // its scales
 constexpr int kTileBlockBytes = kTileBytes + kTileSfBytes;
 
+// Widths that are multiples of 32 but not of the K stage (256) run at the next multiple of 256:
+// weights are packed with zero rows and columns up to it, and x (or its codes) is copied into a
+// zero-padded row of the workspace.  A padded column of x meets only zero weights, a padded
+// weight row yields h = activation(0, 0) = 0 for every activation of the layer (quantised to a
+// zero block), and a padded output column is never copied out, so every sum of the layer takes
+// exactly the same nonzero terms as the unpadded definition.
+inline int pad_stage(int v) { return (v + 255) / 256 * 256; }
+inline bool needs_padding(const moe_config& c) {
+  return c.hidden % 256 != 0 || c.inter % 256 != 0;
+}
+inline moe_config padded_config(const moe_config& c) {
+  moe_config p = c;
+  p.hidden = pad_stage(c.hidden);
+  p.inter = pad_stage(c.inter);
+  if (c.shared_inter > 0) p.shared_inter = p.inter;
+  return p;
+}
+
 // GEMM1 output rows per expert: gate and up rows (2I), or the up rows alone for non-gated
 // experts (I).
 inline bool gated_experts(const moe_config& c) { return (c.flags & MOE_FLAG_ACT_RELU2) == 0u; }

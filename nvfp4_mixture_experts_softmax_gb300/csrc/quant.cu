@@ -132,6 +132,7 @@ struct WeightDst {
   const float* ts;  // [Et][4]
   int64_t w13_per_e, w2_per_e;
   int gated;
+  int H, I;         // the packed (256-multiple) widths: K of the packed blocks
 };
 
 // One thread per 16-element block of one matrix row: quantise and store into the packed layout.
@@ -144,6 +145,7 @@ __global__ void __launch_bounds__(kThreads) weight_encode_kernel(WeightSrc w, We
   const int64_t nblk = per / 16;
   const uint16_t* src = matrix_ptr(w, slot, m, per);
   const float ts = d.ts[slot * 4 + m];
+  const int64_t Kp = m < 2 ? d.H : d.I;
   for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblk;
        b += (int64_t)gridDim.x * blockDim.x) {
     const int64_t n = b / (K / 16), kb = b % (K / 16);
@@ -160,8 +162,8 @@ __global__ void __launch_bounds__(kThreads) weight_encode_kernel(WeightSrc w, We
     quant_block16(f, ts, lo, hi, s);
     uint8_t* base = m < 2 ? d.w13 + slot * d.w13_per_e : d.w2 + slot * d.w2_per_e;
     const int64_t r = m < 2 ? w13_row(n, m, d.gated) : n;
-    *reinterpret_cast<uint2*>(base + packed_code_offset(r, kb, K)) = make_uint2(lo, hi);
-    base[packed_sf_offset(r, kb, K)] = (uint8_t)s;
+    *reinterpret_cast<uint2*>(base + packed_code_offset(r, kb, Kp)) = make_uint2(lo, hi);
+    base[packed_sf_offset(r, kb, Kp)] = (uint8_t)s;
   }
 }
 
@@ -182,6 +184,7 @@ __global__ void __launch_bounds__(kThreads) weight_encode_mx_kernel(WeightSrc w,
   const int64_t K = m < 2 ? w.H : w.I;
   const int64_t nblk = per / 32;
   const uint16_t* src = matrix_ptr(w, slot, m, per);
+  const int64_t Kp = m < 2 ? d.H : d.I;
   for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblk;
        b += (int64_t)gridDim.x * blockDim.x) {
     const int64_t n = b / (K / 32), kb = b % (K / 32);
@@ -210,9 +213,11 @@ __global__ void __launch_bounds__(kThreads) weight_encode_mx_kernel(WeightSrc w,
                         mx_unscale(f[8 * q + 6], sb), mx_unscale(f[8 * q + 7], sb));
     uint8_t* base = m < 2 ? d.w13 + slot * d.w13_per_e : d.w2 + slot * d.w2_per_e;
     const int64_t r = m < 2 ? w13_row(n, m, d.gated) : n;
-    *reinterpret_cast<uint2*>(base + packed_code_offset(r, 2 * kb, K)) = make_uint2(words[0], words[1]);
-    *reinterpret_cast<uint2*>(base + packed_code_offset(r, 2 * kb + 1, K)) = make_uint2(words[2], words[3]);
-    base[packed_mx_sf_offset(r, kb, K)] = (uint8_t)sb;
+    *reinterpret_cast<uint2*>(base + packed_code_offset(r, 2 * kb, Kp)) =
+        make_uint2(words[0], words[1]);
+    *reinterpret_cast<uint2*>(base + packed_code_offset(r, 2 * kb + 1, Kp)) =
+        make_uint2(words[2], words[3]);
+    base[packed_mx_sf_offset(r, kb, Kp)] = (uint8_t)sb;
   }
 }
 
@@ -227,14 +232,15 @@ __global__ void __launch_bounds__(kThreads) weight_export_mx_kernel(WeightDst d,
                                                                    uint8_t* codes, uint8_t* sf,
                                                                    float* ts) {
   const int64_t nblk = N * K / 16;
+  const int64_t Kp = m < 2 ? d.H : d.I;
   for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblk;
        b += (int64_t)gridDim.x * blockDim.x) {
     const int64_t n = b / (K / 16), kb = b % (K / 16);
     const uint8_t* base = m < 2 ? d.w13 + slot * d.w13_per_e : d.w2 + slot * d.w2_per_e;
     const int64_t r = m < 2 ? w13_row(n, m, d.gated) : n;
     *reinterpret_cast<uint2*>(codes + n * (K / 2) + kb * 8) =
-        *reinterpret_cast<const uint2*>(base + packed_code_offset(r, kb, K));
-    if ((kb & 1) == 0) sf[n * (K / 32) + kb / 2] = base[packed_mx_sf_offset(r, kb / 2, K)];
+        *reinterpret_cast<const uint2*>(base + packed_code_offset(r, kb, Kp));
+    if ((kb & 1) == 0) sf[n * (K / 32) + kb / 2] = base[packed_mx_sf_offset(r, kb / 2, Kp)];
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) *ts = d.ts[slot * 4 + m];
 }
@@ -244,13 +250,14 @@ __global__ void __launch_bounds__(kThreads) weight_export_kernel(WeightDst d, in
                                                                 uint8_t* codes, uint8_t* sf,
                                                                 float* ts) {
   const int64_t nblk = N * K / 16;
+  const int64_t Kp = m < 2 ? d.H : d.I;
   for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblk;
        b += (int64_t)gridDim.x * blockDim.x) {
     const int64_t n = b / (K / 16), kb = b % (K / 16);
     const uint8_t* base = m < 2 ? d.w13 + slot * d.w13_per_e : d.w2 + slot * d.w2_per_e;
     const int64_t r = m < 2 ? w13_row(n, m, d.gated) : n;
-    const uint2 c = *reinterpret_cast<const uint2*>(base + packed_code_offset(r, kb, K));
-    const uint8_t s = base[packed_sf_offset(r, kb, K)];
+    const uint2 c = *reinterpret_cast<const uint2*>(base + packed_code_offset(r, kb, Kp));
+    const uint8_t s = base[packed_sf_offset(r, kb, Kp)];
     *reinterpret_cast<uint2*>(codes + n * (K / 2) + kb * 8) = c;
     sf[n * (K / 16) + kb] = s;
   }
@@ -672,6 +679,8 @@ WeightDst make_dst(const WeightLayout& L, uint8_t* wbuf) {
   d.w13_per_e = (int64_t)L.w13_per_e;
   d.w2_per_e = (int64_t)L.w2_per_e;
   d.gated = L.gated ? 1 : 0;
+  d.H = L.H;
+  d.I = L.I;
   return d;
 }
 

@@ -2,7 +2,11 @@
 
 Criteria (the layer's correctness contract):
   * router ids, permutation, offsets, quantised codes and block scales: bit-exact;
-  * final output: relative L2 error <= 5e-3 and max |error| <= 3e-2 * RMS(reference);
+  * final output: relative L2 error <= 5e-3 and, per element, |error| <= 3e-2 * RMS(reference)
+    plus one BF16 unit in the last place of the element: both sides round an FP32 sum to the
+    BF16 output, and sums that differ in their last FP32 bits (the tensor core's accumulation
+    order) can round one BF16 step apart, 2^-8 relative, which for an output of 4-8 RMS is
+    about 3e-2 * RMS by itself;
   * requantised intermediate codes: at most 0.1% differ, each by one step of the ordered E2M1
     value list (+-0 counted as one value); block scales likewise at most 0.1%, one E4M3 step.
 """
@@ -46,6 +50,19 @@ def assert_h_close(gpu_codes, gpu_sf, ref_codes, ref_sf):
     assert fs <= H_CODE_FRAC and ms <= 1, f"h scales: {fs:.2e} differ, max step {ms}"
 
 
+def bf16_ulp(a) -> np.ndarray:
+    """One BF16 unit in the last place at |a| (8 significant bits; the normal range's spacing
+    below 2^-126)."""
+    a = np.abs(np.asarray(a, np.float64))
+    return np.exp2(np.floor(np.log2(np.maximum(a, 2.0 ** -126))) - 7)
+
+
+def y_max_abs_bound(yg: np.ndarray, yr: np.ndarray, rms: float) -> np.ndarray:
+    """Per-element max |error| of the output: Y_MAX_ABS_RMS * RMS plus one BF16 step at the
+    larger of the two magnitudes."""
+    return Y_MAX_ABS_RMS * rms + bf16_ulp(np.maximum(np.abs(yg), np.abs(yr)))
+
+
 def y_errors(y_gpu_f32: np.ndarray, y_ref_f32: np.ndarray):
     yg = y_gpu_f32.astype(np.float64)
     yr = y_ref_f32.astype(np.float64)
@@ -56,7 +73,10 @@ def y_errors(y_gpu_f32: np.ndarray, y_ref_f32: np.ndarray):
 
 def assert_y_close(y_gpu_f32, y_ref_f32):
     rel, mx = y_errors(y_gpu_f32, y_ref_f32)
-    assert rel <= Y_REL_L2 and mx <= Y_MAX_ABS_RMS, f"y: rel_l2={rel:.3e} max/rms={mx:.3e}"
+    yg, yr = y_gpu_f32.astype(np.float64), y_ref_f32.astype(np.float64)
+    rms = np.sqrt(np.mean(yr ** 2))
+    ok = bool((np.abs(yg - yr) <= y_max_abs_bound(yg, yr, rms)).all())
+    assert rel <= Y_REL_L2 and ok, f"y: rel_l2={rel:.3e} max/rms={mx:.3e}"
     return rel, mx
 
 
@@ -93,7 +113,8 @@ def assert_y_close_h_aware(yg, yr, rows, ts_h=1.0):
     by that step times the down-projection column, which at the shared expert's weight of 1 can
     exceed the max-abs bound on its own.  So:
       * relative L2 over all compared outputs <= Y_REL_L2 (unchanged);
-      * per element |y_gpu - y_ref| <= Y_MAX_ABS_RMS * RMS + sum over the differing h blocks of
+      * per element |y_gpu - y_ref| <= Y_MAX_ABS_RMS * RMS + one BF16 step of the element (see
+        the module docstring) + sum over the differing h blocks of
         the token of w * 3 * S+ * |W_down[:, n]|, where S+ is the oracle block scale one E4M3
         step up and 3 * S+ bounds a one-step change of code and scale together (E2M1 steps are at
         most 2 units, an E4M3 step at most 1/8 relative of at most 6 units).
@@ -106,7 +127,7 @@ def assert_y_close_h_aware(yg, yr, rows, ts_h=1.0):
     rel = np.linalg.norm(yg - yr) / max(np.linalg.norm(yr), 1e-30)
     assert rel <= Y_REL_L2, f"y: rel_l2={rel:.3e}"
     rms = np.sqrt(np.mean(yr ** 2))
-    bound = np.full(yg.shape, Y_MAX_ABS_RMS * rms)
+    bound = y_max_abs_bound(yg, yr, rms)
     flipped_tokens = 0
     for i, slots in enumerate(rows):
         hit = False

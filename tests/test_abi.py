@@ -50,6 +50,10 @@ def test_status_strings(moe):
     (dict(num_experts=0, hidden=256, inter=512, top_k=1), -1),
     (dict(num_experts=8, hidden=200, inter=512, top_k=2), -2),
     (dict(num_experts=8, hidden=256, inter=100, top_k=2), -2),
+    (dict(num_experts=8, hidden=288, inter=160, top_k=2), 0),      # multiples of 32: padded
+    (dict(num_experts=8, hidden=32, inter=32, top_k=2), 0),
+    (dict(num_experts=8, hidden=2080, inter=1408, top_k=2, shared_inter=1408), 0),
+    (dict(num_experts=8, hidden=2 ** 21, inter=256, top_k=2), -2),
     (dict(num_experts=2048, hidden=256, inter=256, top_k=2), -2),
     (dict(num_experts=64, hidden=256, inter=256, top_k=33), -2),
     (dict(num_experts=8, hidden=256, inter=512, top_k=2, shared_inter=256), -2),
@@ -74,6 +78,11 @@ def test_sizes(moe):
     assert moe.workspace_size(moe.make_config(8, 200, 512, 2), 4) == 0
     shared = moe.make_config(256, 7168, 2048, 8, shared_inter=2048)
     assert moe.weights_size(shared) > moe.weights_size(moe.make_config(256, 7168, 2048, 8))
+    # widths that are multiples of 32 only run at the next multiples of 256: the packed weights
+    # are those of the padded layer, the workspace adds the padded rows of x and of the output
+    pad, full = moe.make_config(8, 288, 160, 2), moe.make_config(8, 512, 256, 2)
+    assert moe.weights_size(pad) == moe.weights_size(full)
+    assert moe.workspace_size(pad, 10) == moe.workspace_size(full, 10) + 2 * (10 * 512 * 2)
 
 
 def test_host_side_rejections(moe):

@@ -15,7 +15,7 @@ import torch
 
 import oracle
 import synth
-from parity import H_CODE_FRAC, Y_MAX_ABS_RMS, Y_REL_L2
+from parity import H_CODE_FRAC, Y_REL_L2, y_max_abs_bound
 
 pytestmark = pytest.mark.gpu
 
@@ -95,7 +95,7 @@ def check_w4a8(moe, cs, T, activation="swiglu", limit=None, sample=None):
     rel = np.linalg.norm(yg - yr) / np.linalg.norm(yr)
     assert rel <= Y_REL_L2, rel
     rms = np.sqrt(np.mean(yr ** 2))
-    bound = np.full(yg.shape, Y_MAX_ABS_RMS * rms)
+    bound = y_max_abs_bound(yg, yr, rms)
     wd_cache = {}
     for i, t in enumerate(toks):
         slots = [(od["w"][i, j], inv[t * k + j], od["inv"][i * k + j], od["hq"], od["hsf"],
