@@ -489,7 +489,6 @@ int run_core(const moe_config* cfg, int Hl, int Il, const void* wbuf, const void
     pr.in_ts = qts;
     e = launch_prologue_small(pr, s);
     if (e == cudaSuccess) e = mark(1);
-    if (e == cudaSuccess) e = mark(2);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   } else {
   e = cudaMemsetAsync(hdr, 0, sizeof(WsHeader), s);
@@ -524,7 +523,6 @@ int run_core(const moe_config* cfg, int Hl, int Il, const void* wbuf, const void
   pa.sqrtsp = sqrtsp;
   pa.bias = rbias;
   e = launch_plan(pa, s);
-  if (e == cudaSuccess) e = mark(2);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
 
@@ -547,6 +545,9 @@ int run_core(const moe_config* cfg, int Hl, int Il, const void* wbuf, const void
                                ws + L.xq_perm, ws + L.xsf_tiles, &hdr->status, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
+  // the router / plan stage ends once the activations are in expert order (the decode prologue
+  // marked it already), so that GEMM1's stage times the GEMM alone
+  if (!L.decode && mark(2) != cudaSuccess) return MOE_ERR_CUDA;
   const float* w_ts = reinterpret_cast<const float*>(wb + W.ts);
 
   // 3. GEMM1 + SwiGLU + requantisation
