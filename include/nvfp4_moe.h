@@ -66,7 +66,8 @@ typedef struct {
   int32_t hidden;        /* H, multiple of 32 (16-byte code rows); see the note below */
   int32_t inter;         /* I, routed-expert intermediate size, multiple of 32 */
   int32_t top_k;         /* k, 1..min(E, 32) */
-  int32_t shared_inter;  /* 0: no shared expert; otherwise its intermediate size (must equal I) */
+  int32_t shared_inter;  /* 0: no shared expert; otherwise its intermediate size, a multiple of 32
+                            (one other than I runs, like an unaligned width, padded: see below) */
   float h_tensor_scale;  /* fixed FP32 tensor scale used to requantise h (1.0 by default) */
   int32_t max_tokens;    /* largest T a workspace sized with moe_workspace_size must serve */
   uint32_t flags;        /* MOE_FLAG_* variant bits below; 0 = the base layer */
@@ -74,13 +75,17 @@ typedef struct {
   float swiglu_alpha;    /* slope of MOE_FLAG_ACT_SWIGLU_OAI (1.702 in gpt-oss): finite */
 } moe_config;
 
-/* Widths.  H and I need only be multiples of 32.  A width that is not a multiple of 256 (the K
- * stage of the packed weight blocks) is padded inside the library: the weight buffer holds zero
- * rows and columns up to the next multiple of 256 (moe_weights_size counts them), and moe_run /
- * moe_run_quantized copy x (or its codes and scales) into zero-padded rows of the workspace and
- * the output rows back into y (moe_workspace_size counts both buffers).  The results are those
- * of the unpadded layer: a padded column of x meets only zero weights, and a padded feature of
- * h is activation(0, 0) = 0 for every activation flag, quantised to a zero block. */
+/* Widths.  H, I and the shared expert's intermediate size need only be multiples of 32.  A width
+ * that is not a multiple of 256 (the K stage of the packed weight blocks), or a shared expert
+ * whose intermediate size differs from I, is padded inside the library: H runs rounded up to a
+ * multiple of 256, and both intermediate sizes run at the larger of the two rounded up to a
+ * multiple of 256.  The weight buffer holds zero rows and columns up to those widths
+ * (moe_weights_size counts them), and moe_run / moe_run_quantized copy x (or its codes and
+ * scales) into zero-padded rows of the workspace and the output rows back into y
+ * (moe_workspace_size counts both buffers).  Debug rows of h are as wide as the larger
+ * intermediate size (a narrower expert's rows end in zeros).  The results are those of the
+ * unpadded layer: a padded column of x meets only zero weights, and a padded feature of h is
+ * activation(0, 0) = 0 for every activation flag, quantised to a zero block. */
 
 /* Router variant ("vllm.cpp docs/STATUS.md", paragraph "W6 sqrtsoftplus + hash-routed MoE";
  * "nvfp4-megamoe-kernel compare pre-b1...master", section "Dense Router (L3+)"): expert scores

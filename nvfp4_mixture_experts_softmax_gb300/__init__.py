@@ -194,7 +194,8 @@ def set_router_bias(cfg: MoeConfig, wbuf: torch.Tensor, bias: torch.Tensor) -> N
 def weights_export(cfg: MoeConfig, wbuf, expert: int, matrix: int, stream=None):
     """Canonical (codes [N,K/2], sf [N,K/16] E4M3 - or [N,K/32] E8M0 for a W4A8 layer's MXFP4
     weights - and ts [1]) of one expert matrix (-1 = shared)."""
-    N, K = (cfg.inter, cfg.hidden) if matrix < 2 else (cfg.hidden, cfg.inter)
+    Iw = cfg.shared_inter if expert == -1 else cfg.inter   # this expert's intermediate size
+    N, K = (Iw, cfg.hidden) if matrix < 2 else (cfg.hidden, Iw)
     dev = wbuf.device
     codes = torch.empty(N, K // 2, dtype=torch.uint8, device=dev)
     sf = torch.empty(N, K // (32 if cfg.flags & FLAG_ACT_MXFP8 else 16), dtype=torch.uint8,
@@ -329,7 +330,9 @@ def run(cfg: MoeConfig, wbuf, x, logits, k=None, y=None, workspace=None, debug=F
     dbg = None
     dbg_c = None
     if debug:
-        E, I = cfg.num_experts, cfg.inter
+        # h rows are as wide as the layer's widest intermediate (a shared expert of another
+        # width than the routed ones: the narrower rows end in zeros)
+        E, I = cfg.num_experts, max(cfg.inter, cfg.shared_inter)
         Rt = T * k + (T if cfg.shared_inter else 0)
         dbg = dict(topk_ids=torch.empty(T, k, dtype=torch.int32, device=dev),
                    topk_w=torch.empty(T, k, dtype=torch.float32, device=dev),
@@ -352,7 +355,6 @@ def run(cfg: MoeConfig, wbuf, x, logits, k=None, y=None, workspace=None, debug=F
             dbg["xsf"] = torch.empty(T, H // 32, dtype=torch.uint8, device=dev)
             dbg["hq"] = torch.empty(Rt, I, dtype=torch.uint8, device=dev)
             dbg["hsf"] = torch.empty(Rt, I // 32, dtype=torch.uint8, device=dev)
-            dbg["hb"] = torch.empty(Rt, I, dtype=torch.bfloat16, device=dev)
             dbg["hb"] = torch.empty(Rt, I, dtype=torch.bfloat16, device=dev)
         dbg_c = MoeDebug(*[dbg[n].data_ptr() if n in dbg else None
                            for n, _ in MoeDebug._fields_[:11]],

@@ -43,8 +43,8 @@ int check_cfg(const moe_config* c) {
   if (c->num_experts > 1024 || c->top_k > 32) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (c->hidden % 32 != 0 || c->inter % 32 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (c->hidden > (1 << 20) || c->inter > (1 << 20)) return MOE_ERR_UNSUPPORTED_SHAPE;
-  if (c->shared_inter != 0 && c->shared_inter != c->inter) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (c->shared_inter < 0) return MOE_ERR_INVALID_ARG;
+  if (c->shared_inter % 32 != 0 || c->shared_inter > (1 << 20)) return MOE_ERR_UNSUPPORTED_SHAPE;
   return MOE_OK;
 }
 
@@ -540,9 +540,11 @@ int run_core(const moe_config* cfg, int Hl, int Il, const void* wbuf, const void
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   } else if (!L.small) {
     // encode each block once into token order and into every expert row of its token
+    // (the token-order codes feed nothing on this path but the debug copies)
     e = launch_act_encode_perm(x, T, H, k, E, shared, L.Rt, &hdr->ts, i32(L.ids), i32(L.inv),
-                               i32(L.seg_off), i32(L.tile_start), ws + L.xq, ws + L.xsf,
-                               ws + L.xq_perm, ws + L.xsf_tiles, &hdr->status, s);
+                               i32(L.seg_off), i32(L.tile_start), debug ? ws + L.xq : nullptr,
+                               debug ? ws + L.xsf : nullptr, ws + L.xq_perm, ws + L.xsf_tiles,
+                               &hdr->status, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   // the router / plan stage ends once the activations are in expert order (the decode prologue
@@ -677,6 +679,7 @@ int run_layer(const moe_config* cfg, const void* wbuf, const void* x, const uint
   if (!needs_padding(*cfg))
     return run_core(cfg, cfg->hidden, cfg->inter, wbuf, x, qx, qsf, qts, logits, T, k, y,
                     workspace, ws_bytes, stream, debug);
+  const int Il = h_width(*cfg);   // debug rows of h: the layer's widest intermediate
   if (T < 0 || k != cfg->top_k) return MOE_ERR_INVALID_ARG;
   if (cfg->max_tokens > 0 && T > cfg->max_tokens) return MOE_ERR_UNSUPPORTED_SHAPE;
   if ((int64_t)T * (cfg->top_k + 1) > (int64_t)INT32_MAX / 2) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -706,14 +709,14 @@ int run_layer(const moe_config* cfg, const void* wbuf, const void* x, const uint
         !ok(cudaMemcpy2DAsync(sfp, Hp / 16, qsf, H / 16, H / 16, rows, cudaMemcpyDeviceToDevice,
                               s)))
       return MOE_ERR_CUDA;
-    st = run_core(&pc, cfg->hidden, cfg->inter, wbuf, nullptr, xp, sfp, qts, logits, T, k, yp,
+    st = run_core(&pc, cfg->hidden, Il, wbuf, nullptr, xp, sfp, qts, logits, T, k, yp,
                   workspace, core, stream, debug);
   } else {
     if (!ok(cudaMemsetAsync(xp, 0, rows * Hp * 2, s)) ||
         !ok(cudaMemcpy2DAsync(xp, Hp * 2, x, H * 2, H * 2, rows, cudaMemcpyDeviceToDevice, s)))
       return MOE_ERR_CUDA;
-    st = run_core(&pc, cfg->hidden, cfg->inter, wbuf, xp, nullptr, nullptr, nullptr, logits, T,
-                  k, yp, workspace, core, stream, debug);
+    st = run_core(&pc, cfg->hidden, Il, wbuf, xp, nullptr, nullptr, nullptr, logits, T, k, yp,
+                  workspace, core, stream, debug);
   }
   if (st != MOE_OK) return st;
   return ok(cudaMemcpy2DAsync(y, H * 2, yp, Hp * 2, H * 2, rows, cudaMemcpyDeviceToDevice, s))

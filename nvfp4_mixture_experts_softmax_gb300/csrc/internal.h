@@ -56,14 +56,20 @@ constexpr int kTileBlockBytes = kTileBytes + kTileSfBytes;
 // weight row yields h = activation(0, 0) = 0 for every activation of the layer (quantised to a
 // zero block), and a padded output column is never copied out, so every sum of the layer takes
 // exactly the same nonzero terms as the unpadded definition.
+// A shared expert whose intermediate size differs from the routed experts' runs at the same
+// padded width: both are padded to the next multiple of 256 above the larger of the two.
 inline int pad_stage(int v) { return (v + 255) / 256 * 256; }
+inline int h_width(const moe_config& c) {   // the widest intermediate of the layer
+  return c.shared_inter > c.inter ? c.shared_inter : c.inter;
+}
 inline bool needs_padding(const moe_config& c) {
-  return c.hidden % 256 != 0 || c.inter % 256 != 0;
+  return c.hidden % 256 != 0 || c.inter % 256 != 0 ||
+         (c.shared_inter > 0 && c.shared_inter != c.inter);
 }
 inline moe_config padded_config(const moe_config& c) {
   moe_config p = c;
   p.hidden = pad_stage(c.hidden);
-  p.inter = pad_stage(c.inter);
+  p.inter = pad_stage(h_width(c));
   if (c.shared_inter > 0) p.shared_inter = p.inter;
   return p;
 }
@@ -193,9 +199,10 @@ cudaError_t launch_act_quant(const void* x, int64_t rows, int64_t cols, uint8_t*
                              int64_t zero_floats, cudaStream_t s);
 
 // The two halves of launch_act_quant for batches that are planned before they are encoded:
-// max |x| -> tensor scale (and the accumulator zeroing), then the encode into token order and
-// into every expert row of each token (xq_perm, xsf_tiles).  With ts_in (already quantised
-// input) the first half only zeroes the accumulator and copies *ts_in into the header.
+// max |x| -> tensor scale (and the accumulator zeroing), then the encode into token order
+// (codes / sf; null: skipped) and into every expert row of each token (xq_perm, xsf_tiles).
+// With ts_in (already quantised input) the first half only zeroes the accumulator and copies
+// *ts_in into the header.
 cudaError_t launch_act_amax(const void* x, int64_t rows, int64_t cols, float* ts, WsHeader* hdr,
                             uint32_t* partials, float* zero_buf, int64_t zero_floats,
                             cudaStream_t s, const float* ts_in);

@@ -85,8 +85,8 @@ __global__ void __launch_bounds__(kThreads) act_encode_kernel(const uint4* __res
 
 struct WeightSrc {
   const uint16_t* routed[3];  // gate [E,I,H], up [E,I,H], down [E,H,I]
-  const uint16_t* shared[3];  // [I,H], [I,H], [H,I] or null
-  int E, H, I;
+  const uint16_t* shared[3];  // [Is,H], [Is,H], [H,Is] or null
+  int E, H, I, Is;
   int gated;                  // 0: non-gated experts (ReLU2), no gate matrix to read or pack
 };
 
@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(kThreads) weight_amax_kernel(WeightSrc w, uint
   const int mi = blockIdx.y;
   const int slot = mi / 3, m = mi % 3;
   if (m == 0 && !w.gated) return;   // no gate matrix: its tensor scale stays 0
-  const int64_t per = (int64_t)w.I * w.H;
+  const int64_t per = (int64_t)(slot < w.E ? w.I : w.Is) * w.H;
   const uint4* src = reinterpret_cast<const uint4*>(matrix_ptr(w, slot, m, per));
   const int64_t nvec = per / 8;
   uint32_t v = 0;
@@ -140,8 +140,9 @@ __global__ void __launch_bounds__(kThreads) weight_encode_kernel(WeightSrc w, We
   const int mi = blockIdx.y;
   const int slot = mi / 3, m = mi % 3;
   if (m == 0 && !w.gated) return;
-  const int64_t per = (int64_t)w.I * w.H;
-  const int64_t K = m < 2 ? w.H : w.I;
+  const int Iw = slot < w.E ? w.I : w.Is;   // this expert's intermediate size
+  const int64_t per = (int64_t)Iw * w.H;
+  const int64_t K = m < 2 ? w.H : Iw;
   const int64_t nblk = per / 16;
   const uint16_t* src = matrix_ptr(w, slot, m, per);
   const float ts = d.ts[slot * 4 + m];
@@ -180,8 +181,9 @@ __global__ void __launch_bounds__(kThreads) weight_encode_mx_kernel(WeightSrc w,
   const int mi = blockIdx.y;
   const int slot = mi / 3, m = mi % 3;
   if (m == 0 && !w.gated) return;
-  const int64_t per = (int64_t)w.I * w.H;
-  const int64_t K = m < 2 ? w.H : w.I;
+  const int Iw = slot < w.E ? w.I : w.Is;   // this expert's intermediate size
+  const int64_t per = (int64_t)Iw * w.H;
+  const int64_t K = m < 2 ? w.H : Iw;
   const int64_t nblk = per / 32;
   const uint16_t* src = matrix_ptr(w, slot, m, per);
   const int64_t Kp = m < 2 ? d.H : d.I;
@@ -351,8 +353,10 @@ __global__ void __launch_bounds__(kThreads) act_encode_perm_kernel(
     const int t = (int)(u / nkb), b = (int)(u - (int64_t)t * nkb);
     uint32_t lo, hi, s8;
     quant_bf16_block16(x, u, ts, lo, hi, s8);
-    codes[u] = make_uint2(lo, hi);
-    sf[u] = (uint8_t)s8;
+    if (codes) {   // the token-order copy (read only by the debug copies)
+      codes[u] = make_uint2(lo, hi);
+      sf[u] = (uint8_t)s8;
+    }
     for (int j = 0; j <= k; ++j) {
       int p, seg;
       if (j < k) {
@@ -780,11 +784,12 @@ cudaError_t launch_weight_quant(const moe_config& c, const WeightLayout& L, cons
   w.E = c.num_experts;
   w.H = c.hidden;
   w.I = c.inter;
+  w.Is = c.shared_inter > 0 ? c.shared_inter : c.inter;
   w.gated = L.gated ? 1 : 0;
   uint32_t* amax = reinterpret_cast<uint32_t*>(wbuf + L.ts);
   cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float) * 4 * L.Et, s);
   if (e != cudaSuccess) return e;
-  const int64_t per = (int64_t)c.inter * c.hidden;
+  const int64_t per = (int64_t)h_width(c) * c.hidden;   // the largest matrix
   dim3 g1(grid_for(per / 8, kThreads * 8, 256), L.Et * 3);
   weight_amax_kernel<<<g1, kThreads, 0, s>>>(w, amax);
   weight_ts_kernel<<<(L.Et * 4 + 255) / 256, 256, 0, s>>>(amax, L.Et * 4);
@@ -805,8 +810,9 @@ cudaError_t launch_weight_export(const moe_config& c, const WeightLayout& L, con
                                  int slot, int m, uint8_t* codes, uint8_t* sf, float* ts,
                                  cudaStream_t s) {
   WeightDst d = make_dst(L, const_cast<uint8_t*>(wbuf));
-  const int64_t N = m < 2 ? c.inter : c.hidden;
-  const int64_t K = m < 2 ? c.hidden : c.inter;
+  const int64_t Iw = slot < c.num_experts ? c.inter : c.shared_inter;   // this expert's width
+  const int64_t N = m < 2 ? Iw : c.hidden;
+  const int64_t K = m < 2 ? c.hidden : Iw;
   if (c.flags & MOE_FLAG_ACT_MXFP8)
     weight_export_mx_kernel<<<grid_for(N * K / 16, kThreads, 4096), kThreads, 0, s>>>(
         d, slot, m, N, K, codes, sf, ts);

@@ -56,7 +56,9 @@ def test_status_strings(moe):
     (dict(num_experts=8, hidden=2 ** 21, inter=256, top_k=2), -2),
     (dict(num_experts=2048, hidden=256, inter=256, top_k=2), -2),
     (dict(num_experts=64, hidden=256, inter=256, top_k=33), -2),
-    (dict(num_experts=8, hidden=256, inter=512, top_k=2, shared_inter=256), -2),
+    (dict(num_experts=8, hidden=256, inter=512, top_k=2, shared_inter=256), 0),  # own width
+    (dict(num_experts=8, hidden=256, inter=512, top_k=2, shared_inter=96), 0),
+    (dict(num_experts=8, hidden=256, inter=512, top_k=2, shared_inter=100), -2),
     (dict(num_experts=8, hidden=256, inter=512, top_k=2, h_tensor_scale=0.0), -1),
     (dict(num_experts=8, hidden=256, inter=512, top_k=2, h_tensor_scale=float("nan")), -1),
     (dict(num_experts=8, hidden=256, inter=512, top_k=2, router="sqrtsoftplus"), 0),
@@ -83,6 +85,11 @@ def test_sizes(moe):
     pad, full = moe.make_config(8, 288, 160, 2), moe.make_config(8, 512, 256, 2)
     assert moe.weights_size(pad) == moe.weights_size(full)
     assert moe.workspace_size(pad, 10) == moe.workspace_size(full, 10) + 2 * (10 * 512 * 2)
+    # a shared expert of its own width: both intermediates at the larger one, rounded up
+    assert (moe.weights_size(moe.make_config(8, 512, 256, 2, shared_inter=160)) ==
+            moe.weights_size(moe.make_config(8, 512, 256, 2, shared_inter=256)))
+    assert (moe.weights_size(moe.make_config(8, 512, 256, 2, shared_inter=640)) ==
+            moe.weights_size(moe.make_config(8, 512, 768, 2, shared_inter=768)))
 
 
 def test_host_side_rejections(moe):

@@ -8,13 +8,15 @@ padded h feature is activation(0, 0) = 0, a zero block), so the bounds of the un
 apply unchanged: bit-exact router, permutation, activation codes and weight export; the layer's
 bounds for h and y.  Widths of the pages that need it: the intermediate width 576 of DeepSeek
 V4.1 and 1408 ("b12x" README, sections "DeepSeek V4.1 Flash MoE benchmark" and "What's in
-here")."""
+here").  A shared expert of its own intermediate size runs the same way, at the larger of the two
+widths."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 import synth
+from parity import assert_h_close, assert_y_close_layer
 from test_gpu_producer_layer import _layer
 from test_gpu_variants import check_activation, check_variant
 from test_gpu_w4a8 import check_w4a8
@@ -111,3 +113,64 @@ def test_padded_widths_weight_export_bit_exact(moe):
             assert np.array_equal(c.cpu().numpy(), ref.codes[m])
             assert np.array_equal(s.cpu().numpy(), ref.sf[m])
             assert t.item() == ref.ts[m]
+
+
+# ---- a shared expert of its own intermediate size (the routed and the shared intermediates both
+# run at the larger one rounded up to a multiple of 256; debug rows of h are that wide)
+
+def check_shared_width(moe, H, I, Is, T, cid, activation="swiglu"):
+    cs = synth.custom_config(f"shw_{H}_{I}_{Is}", T, H, 16, 4, I, shared_inter=Is,
+                             config_id=cid)
+    dev, k = "cuda", cs.top_k
+    gated = activation != "relu2"
+    x = synth.gen_x(cs, T, device=dev)
+    logits = synth.gen_logits(cs, T, device=dev)
+    wg, wu, wd = synth.gen_all_experts(cs, device=dev)
+    sh = synth.gen_shared(cs, device=dev)
+    cfg = moe.make_config(cs.experts, H, I, k, shared_inter=Is, max_tokens=T,
+                          activation=activation)
+    wbuf = moe.quantize_weights(cfg, wg if gated else None, wu, wd,
+                                shared=(sh[0] if gated else None, sh[1], sh[2]))
+    y, dbg = moe.run(cfg, wbuf, x, logits, debug=True)
+    torch.cuda.synchronize()
+    lg = logits.cpu().numpy()
+    xq, xsf, ts_a, _ = oracle.quantize_bf16(x.cpu())
+    ids_o, _ = oracle.router(lg, k)
+    experts = [None] * cs.experts
+    for e in np.unique(ids_o):
+        experts[e] = oracle.QuantExpert.from_bf16(wg[e].cpu() if gated else None, wu[e].cpu(),
+                                                  wd[e].cpu())
+    sho = oracle.QuantExpert.from_bf16(sh[0].cpu() if gated else None, sh[1].cpu(), sh[2].cpu())
+    y_ref, od = oracle.moe_forward(xq, xsf, ts_a, lg, experts, k, shared=sho, want_debug=True,
+                                   activation=activation)
+    g = {n: t.cpu().numpy() for n, t in dbg.items()}
+    R, Ih = T * k, max(I, Is)
+    assert g["hq"].shape[1] == Ih // 2
+    # each expert's rows at its own width, then zero codes and zero scales
+    assert not g["hq"][:R, I // 2:].any() and not g["hsf"][:R, I // 16:].any()
+    assert not g["hq"][R:, Is // 2:].any() and not g["hsf"][R:, Is // 16:].any()
+    assert np.array_equal(g["topk_ids"], od["ids"]) and np.array_equal(g["inv"], od["inv"])
+    assert_h_close(g["hq"][:R, :I // 2], g["hsf"][:R, :I // 16], od["hq"], od["hsf"])
+    assert_h_close(g["hq"][R:, :Is // 2], g["hsf"][R:, :Is // 16], od["shq"], od["shsf"])
+    gv = dict(g)
+    gv["hq"] = [g["hq"][r, :(I if r < R else Is) // 2] for r in range(g["hq"].shape[0])]
+    gv["hsf"] = [g["hsf"][r, :(I if r < R else Is) // 16] for r in range(g["hsf"].shape[0])]
+    assert_y_close_layer(y.float().cpu().numpy(), oracle.bf16_bits_to_f32(y_ref), gv, od,
+                         np.arange(T), T, k, experts, sho)
+    for m in range(3):             # the shared expert's matrices come back at its own width
+        if m == 0 and not gated:
+            continue
+        c, s, t = moe.weights_export(cfg, wbuf, -1, m)
+        assert np.array_equal(c.cpu().numpy(), sho.codes[m])
+        assert np.array_equal(s.cpu().numpy(), sho.sf[m]) and t.item() == sho.ts[m]
+
+
+@pytest.mark.parametrize("H,I,Is", [(2048, 512, 1024), (288, 160, 96), (512, 256, 640)])
+@pytest.mark.parametrize("T", [5, 300, 1500])
+def test_shared_expert_of_its_own_width(moe, H, I, Is, T):
+    check_shared_width(moe, H, I, Is, T, cid=198)
+
+
+@pytest.mark.parametrize("T", [5, 300])
+def test_shared_expert_of_its_own_width_non_gated(moe, T):
+    check_shared_width(moe, 544, 96, 224, T, cid=199, activation="relu2")
