@@ -489,6 +489,107 @@ def steady_state_decode(args, dev, hbm_peak):
             "note": "back-to-back calls, no flush; each call reads a different weight set"}
 
 
+# Layer variants and precisions measured beside the base layer (the further rows of the layer's
+# scope: activations, the variant router, expert sharing, the fused RMSNorm producer feeding the
+# quantised-input entry, W4A16 and W4A8): the decode batch sizes, the W4A16 / W4A8 layers also at
+# the prefill size; CUDA-graph replays with the L2 flushed before each, as for the headline.
+VARIANT_RECORDS = (
+    ("relu2", "decode", dict(activation="relu2"), None, False),
+    ("swiglu_oai", "decode", dict(activation="swiglu_oai", swiglu_limit=7.0), None, False),
+    ("sqrtsoftplus_clamp", "decode", dict(router="sqrtsoftplus", swiglu_limit=10.0), None, False),
+    ("sharing_80pct", "decode", {}, "shared_80", False),
+    ("rmsnorm_producer_into_layer", "decode", {}, None, True),
+    ("w4a16", "decode", dict(precision="w4a16"), None, False),
+    ("w4a8", "decode", dict(precision="w4a8"), None, False),
+    ("w4a16_prefill", "prefill", dict(precision="w4a16"), None, False),
+    ("w4a8_prefill", "prefill", dict(precision="w4a8"), None, False),
+)
+
+
+def measure_variants(args, dev, hbm_peak):
+    """One record per entry of VARIANT_RECORDS: per-call time at each batch size, tokens/s, the
+    touched experts and their weight bytes over the call time as a fraction of HBM bandwidth."""
+    import types
+    import numpy as np
+    import oracle
+    import synth
+    import nvfp4_mixture_experts_softmax_gb300 as moe
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    out = {}
+    for name, wl, kw, routing, producer in VARIANT_RECORDS:
+        cs, Ts = workload(wl)
+        if routing:            # the sharing workloads are defined for small batches
+            Ts = [8]
+        Tmax = max(Ts)
+        gated = kw.get("activation") != "relu2"
+        cfg = moe.make_config(cs.experts, cs.hidden, cs.inter, cs.top_k,
+                              shared_inter=cs.shared_inter, max_tokens=Tmax, **kw)
+        wg, wu, wd = synth.gen_all_experts(cs, device=dev)
+        sh = synth.gen_shared(cs, device=dev) if cs.has_shared else None
+        wbuf = moe.quantize_weights(
+            cfg, wg if gated else None, wu, wd,
+            shared=None if sh is None else (sh[0] if gated else None, sh[1], sh[2]))
+        del wg, wu, wd, sh
+        torch.cuda.empty_cache()
+        bias = None
+        if kw.get("router") == "sqrtsoftplus":
+            bias = variant_bias(cs, "sqrtsoftplus_clamp")
+            moe.set_router_bias(cfg, wbuf, torch.from_numpy(bias))
+        ws = torch.empty(moe.workspace_size(cfg, Tmax), dtype=torch.uint8, device=dev)
+        gamma = torch.from_numpy(np.random.default_rng(7).normal(1.0, 0.1, cs.hidden)
+                                 .astype(np.float32)).to(torch.bfloat16).to(dev)
+        pws = torch.empty(max(int(moe.lib().moe_rmsnorm_workspace_size(Tmax)), 256),
+                          dtype=torch.uint8, device=dev)
+        # weight bytes per element: NVFP4 (also the W4A16 layer's weights) 1/2 + 1/16, MXFP4 1/2 + 1/32
+        per_elem = (1 / 2 + 1 / 32) if kw.get("precision") == "w4a8" else (1 / 2 + 1 / 16)
+        exp_bytes = (3 if gated else 2) * cs.inter * cs.hidden * per_elem
+        rec = {"workload": f"{wl}: {cs.description}", "variant": {**kw, "routing": routing,
+               "producer": producer}, "per_T_us": {}, "touched_experts": {},
+               "weight_hbm_frac": {}, "gpu_launches_per_call": {}}
+        tot_tok, tot_s = 0, 0.0
+        for i, T in enumerate(Ts):
+            x = synth.gen_x(cs, T, device=dev, row0=1000 * i)
+            lg = gen_router_logits(types.SimpleNamespace(routing=routing), cs, T, i, dev)
+            y = torch.empty(T, cs.hidden, dtype=torch.bfloat16, device=dev)
+
+            def call():
+                if producer:
+                    q = moe.rmsnorm_quantize_act(x, gamma, 1e-6, workspace=pws)
+                    moe.run(cfg, wbuf, None, lg, y=y, workspace=ws, quantized=q)
+                else:
+                    moe.run(cfg, wbuf, x, lg, y=y, workspace=ws)
+            for _ in range(3):
+                flush.zero_()
+                call()
+            torch.cuda.synchronize()
+            assert moe.last_device_status(ws) == 0, name
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                call()
+            ms = statistics.median(time_graph(g, flush, stream, max(5, min(args.steps, 20))))
+            del g
+            if kw.get("router") == "sqrtsoftplus":
+                ids, _ = oracle.router(lg.cpu().numpy(), cs.top_k, "sqrtsoftplus", bias)
+            else:
+                ids = moe.plan(lg, cs.top_k)["topk_ids"].cpu().numpy()
+            touched = len(np.unique(ids)) + (1 if cs.has_shared else 0)
+            rec["per_T_us"][str(T)] = round(ms * 1e3, 2)
+            rec["touched_experts"][str(T)] = touched
+            rec["weight_hbm_frac"][str(T)] = round(touched * exp_bytes / (ms / 1e3) / 1e9 / hbm_peak,
+                                                   4)
+            rec["gpu_launches_per_call"][str(T)] = moe.run_kernel_count(cfg, T) + (2 if producer
+                                                                                 else 0)
+            tot_tok += T
+            tot_s += ms / 1e3
+        rec["tokens_per_s"] = round(tot_tok / tot_s, 1)
+        out[name] = rec
+        del wbuf, ws
+        torch.cuda.empty_cache()
+    return out
+
+
 # ----------------------------------------------------------------------------------------- ours
 def run_ours(args, world, rank, local):
     import numpy as np
@@ -743,6 +844,7 @@ def run_ours(args, world, rank, local):
                 workloads["skewed_beta1"] = measure_config(args, name, dev, hbm_peak, fp4_peak,
                                                            peak_src, beta=1.0)
         workloads["decode_steady_state"] = steady_state_decode(args, dev, hbm_peak)
+        workloads["variants"] = measure_variants(args, dev, hbm_peak)
 
     clocks = sampler.summary(t_settle, w1 + 0.05)
     if rank != 0:
