@@ -17,8 +17,11 @@
 // with its four E4M3 block scales into BF16 (e2m1 * scale has at most 6 significant bits and lies
 // in [2^-10, 2688], so it is exact in BF16) and store the row into the sub-stage's B tile in the
 // same 128-byte-swizzled K-major layout; the per-matrix FP32 tensor scale is applied in the
-// epilogue.  Warps: 0-3 epilogue, 4 copies, 5 tensor-memory allocation + the MMA thread, 6-9
-// converters.  Two 128-column FP32 accumulators let the epilogue overlap the next tile.
+// epilogue.  Warps: 0-3 epilogue, 4 copies, 5 tensor-memory allocation + the MMA thread, 6-13
+// converters (two per weight row, each decoding half of the sub-stage's 64 codes: two converter
+// warps per scheduler hide the decode's dependent instruction chains; with one warp per
+// scheduler decoding whole rows the conversion took ~4x the sub-stage's MMA time).  Two
+// 128-column FP32 accumulators let the epilogue overlap the next tile.
 //   GEMM1 epilogue: g, u (times their tensor scales) -> the activation -> h rounded to BF16
 //                   (row-major [rows, I], expert order: the next GEMM's A operand);
 //   GEMM2 epilogue: (acc * ts_down) * router weight, reduced into the token's FP32 output row.
@@ -38,7 +41,7 @@ constexpr int kEpiWarps = 4;
 constexpr int kCopyWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kConvWarp0 = 6;
-constexpr int kConvWarps = 4;
+constexpr int kConvWarps = 8;   // two per 32-row slice of the tile: half a row each
 constexpr int kThreads = (kConvWarp0 + kConvWarps) * 32;
 constexpr int kRawStages = 2;                 // raw NVFP4 weight blocks (K = 256 each)
 constexpr int kSubStages = 4;                 // converted sub-stages (K = 64 each)
@@ -265,7 +268,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kConvWarp0) {
     // ---------------- NVFP4 weight row -> BF16 row of the B tile ----------------
-    const int r = (warp - kConvWarp0) * 32 + lane;      // weight row of the tile
+    const int cwarp = warp - kConvWarp0;
+    const int r = (cwarp & 3) * 32 + lane;   // weight row of the tile
+    const int hf = cwarp >> 2;               // which half of the sub-stage's 64 codes
     int rs = 0, ss = 0;
     uint32_t rph = 0, sph = 0, n_arr = 0;
     bool ok = true;
@@ -285,20 +290,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           // the 64 codes of sub-stage q are 16-byte chunks 2q and 2q+1 of the row (stored at
-          // chunk ^ (row % 8)); its four scales are one word of scale group q
-          const uint4 c0 = *reinterpret_cast<const uint4*>(raw + r * 128 + (((2 * q) ^ (r & 7)) << 4));
-          const uint4 c1 = *reinterpret_cast<const uint4*>(raw + r * 128 + (((2 * q + 1) ^ (r & 7)) << 4));
+          // chunk ^ (row % 8)); this warp decodes chunk 2q + hf (32 codes: output chunks
+          // 4hf .. 4hf+3 of the BF16 row); its four scales are one word of scale group q
+          const uint4 c0 = *reinterpret_cast<const uint4*>(raw + r * 128 +
+                                                           (((2 * q + hf) ^ (r & 7)) << 4));
           // NVFP4: the four E4M3 scales of the sub-stage are one word of scale group q; MXFP4:
           // its two E8M0 scales are bytes 2q, 2q+1 of the row's eight
           const uint32_t sw = kMx ? (uint32_t)*reinterpret_cast<const uint16_t*>(
                                         raw + kTileBytes + r * 8 + 2 * q)
                                   : *reinterpret_cast<const uint32_t*>(
                                         raw + kTileBytes + q * 512 + (r & 31) * 16 + (r >> 5) * 4);
-          const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          const uint32_t cw[4] = {c0.x, c0.y, c0.z, c0.w};
           uint8_t* brow = smem + ss * kSubBytes + kTileBytes16 + r * 128;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {         // 16-byte chunk j of the BF16 row: 8 values
-            const uint32_t w = cw[j];
+          for (int jj = 0; jj < 4; ++jj) {      // 16-byte chunk j of the BF16 row: 8 values
+            const int j = 4 * hf + jj;
+            const uint32_t w = cw[jj];
             uint4 o;
             if constexpr (kMx) {
               // elements 8j .. 8j+7 use 32-block scale j / 4
