@@ -349,7 +349,10 @@ int run_core(const moe_config* cfg, int Hl, int Il, const void* wbuf, const void
                                           &hdr->status, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     const int nseg = E + shared;
-    const int64_t mtiles = ((int64_t)L.Rt + (int64_t)nseg * (kBM - 1)) / kBM;
+    // decode-sized batches: weights as the MMA's M operand, kDecodeTileRows token rows as its N
+    const bool swap = T <= kDecodeMaxRows;
+    const int tr = swap ? kDecodeTileRows : kBM;
+    const int64_t mtiles = ((int64_t)L.Rt + (int64_t)nseg * (tr - 1)) / tr;
     GemmW16Args g{};
     g.a_rows = ws + L.xb_perm;
     g.b_tiles = wb + W.w13;
@@ -375,6 +378,7 @@ int run_core(const moe_config* cfg, int Hl, int Il, const void* wbuf, const void
     g.y_rows = T;
     g.max_items = (int)std::min<int64_t>(mtiles * (g.N / kBN), INT32_MAX);
     g.status = &hdr->status;
+    g.swap = swap ? 1 : 0;
     e = launch_grouped_gemm_w16(g, s);
     if (e == cudaSuccess) e = mark(3);
     GemmW16Args g2 = g;

@@ -12,12 +12,17 @@
 // tensor cores (tcgen05.mma kind::f16, BF16 x BF16 -> FP32 in tensor memory), K in sub-stages of
 // 64.  Per K block of 256 the copy warp fetches the expert's packed NVFP4 weight block (18 KB,
 // the layout the FP4 GEMMs read) with one bulk copy into a raw ring, and per sub-stage one 2-D
-// TMA box (64 BF16 x 128 rows, 128-byte swizzle) of the expert-ordered activation rows.  Four
-// converter warps, one thread per weight row, decode the sub-stage's 64 E2M1 codes of their row
-// with its four E4M3 block scales into BF16 (e2m1 * scale has at most 6 significant bits and lies
-// in [2^-10, 2688], so it is exact in BF16) and store the row into the sub-stage's B tile in the
-// same 128-byte-swizzled K-major layout; the per-matrix FP32 tensor scale is applied in the
-// epilogue.  Warps: 0-3 epilogue, 4 copies, 5 tensor-memory allocation + the MMA thread, 6-13
+// TMA box (64 BF16 x 128 rows, 128-byte swizzle) of the expert-ordered activation rows.  The
+// converter warps decode the sub-stage's 64 E2M1 codes of each weight row with their block
+// scales into BF16 (e2m1 * scale has at most 6 significant bits and lies in [2^-10, 2688], so it
+// is exact in BF16) by placing the codes' bits into BF16 fields and two exact BF16
+// multiplications, with no per-element float conversion, and store the row into the sub-stage's
+// weight tile in the same 128-byte-swizzled K-major layout; the per-matrix FP32 tensor scale is
+// applied in the epilogue.  Batches of at most 64 tokens swap the operands: the decoded weight tile is the MMA's
+// M = 128 and tiles of 16 expert-ordered token rows its N, so neither the MMA nor the token copies
+// carry the padding of a 128-row token tile (an active expert averages a few rows there); the
+// epilogue then holds one weight row per thread and one token per accumulator column.
+// Warps: 0-3 epilogue, 4 copies, 5 tensor-memory allocation + the MMA thread, 6-13
 // converters (two per weight row, each decoding half of the sub-stage's 64 codes: two converter
 // warps per scheduler hide the decode's dependent instruction chains; with one warp per
 // scheduler decoding whole rows the conversion took ~4x the sub-stage's MMA time).  Two
@@ -43,26 +48,41 @@ constexpr int kMmaWarp = 5;
 constexpr int kConvWarp0 = 6;
 constexpr int kConvWarps = 8;   // two per 32-row slice of the tile: half a row each
 constexpr int kThreads = (kConvWarp0 + kConvWarps) * 32;
-constexpr int kRawStages = 2;                 // raw NVFP4 weight blocks (K = 256 each)
 constexpr int kSubStages = 4;                 // converted sub-stages (K = 64 each)
 constexpr int kSubK = 64;
 constexpr int kTileBytes16 = 128 * 128;       // 128 rows x 64 BF16
-constexpr int kSubBytes = 2 * kTileBytes16;   // A tile | B tile
-constexpr int kRawOff = kSubStages * kSubBytes;
-constexpr int kBarOff = kRawOff + kRawStages * kTileBlockBytes;
 constexpr uint32_t kTmemCols = 256;           // two 128-column accumulators
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-constexpr size_t kSmemBytes = 1024 + kBarOff + 256 + 8 * 1027;
+constexpr int kMaxSegTable = 1027;            // s_tile + s_seg entries the layout reserves
 
-static_assert(kRawOff % 1024 == 0 && kTileBlockBytes % 1024 == 0, "1024-byte aligned tiles");
-static_assert(kSmemBytes <= 232448, "shared memory");
-// raw full/empty, sub full/empty, acc full/empty x2, drain; TMEM slot, issue and arrival counts
-static_assert((2 * kRawStages + 2 * kSubStages + 4 + 1) * 8 + (4 + kConvWarps) * 4 <= 256,
-              "barrier area");
+// Shared memory: kSubStages converted sub-stages (the 128 x 64 BF16 tile of the token rows and
+// the decoded weight tile; swapped: the weight tile and a 16-row token tile), a ring of raw
+// NVFP4 weight blocks as deep as the rest leaves room for (the weight stream's bytes in flight),
+// barriers, the swapped W4A8 amax exchange and the tile tables.
+template <bool kSwap>
+struct W16Layout {
+  static constexpr int kTokBytes = kSwap ? kSubK * kDecodeTileRows * 2 : kTileBytes16;
+  static constexpr int kSubBytes = kTileBytes16 + kTokBytes;
+  static constexpr int kWgtOff = kSwap ? 0 : kTileBytes16;   // within a sub-stage
+  static constexpr int kTokOff = kSwap ? kTileBytes16 : 0;
+  static constexpr int kRawStages = kSwap ? 8 : 4;
+  static constexpr int kRawOff = kSubStages * kSubBytes;
+  static constexpr int kBarOff = kRawOff + kRawStages * kTileBlockBytes;
+  static constexpr int kAmaxOff = kBarOff + 512;   // swapped W4A8 GEMM1: [2][kEpiWarps][16] FP32
+  static constexpr int kTableOff = kAmaxOff + 2 * kEpiWarps * 16 * 4;
+  static constexpr size_t kSmemFixed = 1024 + kTableOff;
+  static_assert(kSubBytes % 1024 == 0 && kRawOff % 1024 == 0 && kTileBlockBytes % 1024 == 0,
+                "1024-byte aligned tiles");
+  static_assert(kSmemFixed + 8 * kMaxSegTable <= 232448, "shared memory");
+  // raw full/empty, sub full/empty, acc full/empty x2, drain, 2 epilogue pairs x 2; TMEM slot,
+  // issue and arrival counts
+  static_assert((2 * kRawStages + 2 * kSubStages + 4 + 1 + 4) * 8 + (4 + kConvWarps) * 4 <= 512,
+                "barrier area");
+};
 
 // Instruction descriptor of tcgen05.mma kind::f16: FP32 accumulator (bits 4-5 = 1), A and B BF16
 // (bits 7-9 and 10-12 = 1), both K-major, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
-constexpr uint32_t make_idesc_bf16(int M, int N) {
+__host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
          ((uint32_t)(M >> 4) << 24);
 }
@@ -79,21 +99,51 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uin
       : "memory");
 }
 
-// Two E2M1 codes (low nibble = first element) times an E4M3 scale as BF16x2 (exact).
-__device__ __forceinline__ uint32_t e2m1x2_scaled_bf16x2(uint32_t byte, __half2 scale2) {
-  uint32_t h2;
-  const uint16_t in = (uint16_t)(byte & 0xFFu);
-  asm("{\n"
-      ".reg .b8 b;\n"
-      "cvt.u8.u16 b, %1;\n"
-      "cvt.rn.f16x2.e2m1x2 %0, b;\n"
-      "}"
-      : "=r"(h2)
-      : "h"(in));
-  const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&h2), scale2);
-  const float2 f = __half22float2(v);
-  const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
-  return *reinterpret_cast<const uint32_t*>(&b);
+// Eight E2M1 codes (a 32-bit word, the first code in the low nibble) as four BF16x2 words of
+// their values times 2^-126, by placing bits: a code's three magnitude bits (e1 e0 m) become the
+// two lowest exponent bits and the top mantissa bit of a BF16, its sign bit the sign.  With
+// e1 e0 = 0 that is the subnormal m * 2^-127 = (m / 2) * 2^-126, otherwise
+// 2^(e - 127) * (1 + m / 2) = 2^(e - 1) * (1 + m / 2) * 2^-126: E2M1's own definition, scaled.
+// Word i holds codes 2i (low half) and 2i+1 (high half).
+__device__ __forceinline__ void e2m1x8_to_bf16x2_scaled_down(uint32_t w, uint32_t (&o)[4]) {
+  const uint32_t ev = w & 0x0F0F0F0Fu;          // codes 0, 2, 4, 6: the low nibble of each byte
+  const uint32_t od = (w >> 4) & 0x0F0F0F0Fu;   // codes 1, 3, 5, 7
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    // byte 0 <- byte i of ev, byte 2 <- byte i of od, bytes 1 and 3 <- the sign of ev's byte 0
+    // (selector 8), which is clear: code 2i in bits 0-3 and code 2i+1 in bits 16-19
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;"
+        : "=r"(r)
+        : "r"(ev), "r"(od), "r"(0x8080u | (uint32_t)i | ((uint32_t)(4 + i) << 8)));
+    // magnitude to bits 6-8 (x 2^6) and sign to bit 15 (x 2^12) of each half; the two shifted
+    // copies occupy disjoint bits, so the sum is their union
+    o[i] = (r * 4160u) & 0x81C081C0u;
+  }
+}
+
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+constexpr uint32_t kBf16x2Pow2_126 = 0x7E807E80u;   // 2^126 in both halves
+constexpr uint32_t kBf16x2Pow2_120 = 0x7B807B80u;   // 2^120 in both halves
+
+// An E4M3 block scale as BF16x2 (exact): its seven magnitude bits shifted to the top of a BF16's
+// exponent-and-mantissa field are the scale times 2^-120 (subnormal E4M3 to subnormal BF16
+// likewise), and one multiplication by 2^120 restores it.
+__device__ __forceinline__ uint32_t e4m3_scale_bf16x2(uint32_t b) {
+  const uint32_t h = ((b & 0x7Fu) << 4) | ((b & 0x80u) << 8);
+  return mul_bf16x2(h | (h << 16), kBf16x2Pow2_120);
+}
+
+// An E8M0 block scale 2^(b - 127) as BF16x2: the byte is the BF16 exponent field (b = 0: the
+// subnormal 2^-127).
+__device__ __forceinline__ uint32_t e8m0_scale_bf16x2(uint32_t b) {
+  const uint32_t h = b ? (b << 7) : 0x40u;
+  return h | (h << 16);
 }
 
 struct TileW16 {
@@ -101,7 +151,7 @@ struct TileW16 {
 };
 
 __device__ __forceinline__ TileW16 decode_tile_w16(int item, int n_tiles, const int32_t* s_tile,
-                                                   const int32_t* s_seg, int nseg) {
+                                                   const int32_t* s_seg, int nseg, int tr) {
   TileW16 t;
   const int mt = item / n_tiles;
   t.nt = item - mt * n_tiles;
@@ -112,25 +162,9 @@ __device__ __forceinline__ TileW16 decode_tile_w16(int item, int n_tiles, const 
     else hi = mid - 1;
   }
   t.seg = lo;
-  t.m0 = s_seg[lo] + (mt - s_tile[lo]) * kBM;
-  t.rows = min(kBM, s_seg[lo + 1] - t.m0);
+  t.m0 = s_seg[lo] + (mt - s_tile[lo]) * tr;
+  t.rows = min(tr, s_seg[lo + 1] - t.m0);
   return t;
-}
-
-// Two E2M1 codes (low nibble first) times 2^(b - 127) as BF16x2 (exact).
-__device__ __forceinline__ uint32_t e2m1x2_mx_bf16x2(uint32_t byte, float scale) {
-  uint32_t h2;
-  const uint16_t in = (uint16_t)(byte & 0xFFu);
-  asm("{\n"
-      ".reg .b8 b;\n"
-      "cvt.u8.u16 b, %1;\n"
-      "cvt.rn.f16x2.e2m1x2 %0, b;\n"
-      "}"
-      : "=r"(h2)
-      : "h"(in));
-  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-  const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale, f.y * scale);
-  return *reinterpret_cast<const uint32_t*>(&b);
 }
 
 // MXFP8 requantisation of 32 consecutive h values: E8M0 scale, E4M3 codes (nearest even,
@@ -161,13 +195,22 @@ __device__ __forceinline__ void mx8_requant_store(const float* h, uint8_t* codes
   for (int q = 0; q < 4; ++q) bd[q] = make_uint4(bw[4 * q], bw[4 * q + 1], bw[4 * q + 2], bw[4 * q + 3]);
 }
 
-template <bool kMx>
+// kSwap (decode-sized batches): the decoded weight tile is the MMA's A operand (M = 128) and a
+// tile of kDecodeTileRows expert-ordered token rows its B operand (N = 16), so neither the MMA
+// nor the token copies carry the padding of a 128-row token tile; the accumulator holds
+// D[weight row][token] and the epilogue works per token column.
+template <bool kMx, bool kSwap>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_w16_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmW16Args p) {
+  using L = W16Layout<kSwap>;
+  constexpr int kTR = kSwap ? kDecodeTileRows : kBM;            // token rows per tile
+  constexpr uint32_t kBoxBytes = (uint32_t)kSubK * kTR * 2;      // one sub-stage's token box
+  constexpr uint32_t kTokOff = L::kTokOff, kWgtOff = L::kWgtOff;
+  constexpr int kRawStages = L::kRawStages, kSubBytes = L::kSubBytes, kRawOff = L::kRawOff;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   uint64_t* raw_full = bars;
   uint64_t* raw_empty = raw_full + kRawStages;
   uint64_t* sub_full = raw_empty + kRawStages;
@@ -175,11 +218,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_full = sub_empty + kSubStages;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* pair_bar = drain + 1;   // [warp pair][tile parity]: swapped W4A8 amax exchange
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pair_bar + 4);
   uint32_t* s_issued = tmem_slot + 1;   // [0] raw blocks, [1] A boxes issued by the copy thread
   uint32_t* s_conv = s_issued + 2;      // sub-stage arrivals of each converter warp
   volatile uint32_t* s_abort = s_conv + kConvWarps;   // set by any role whose wait ran out
-  int32_t* s_tile = reinterpret_cast<int32_t*>(smem + kBarOff + 256);
+  float* s_amax = reinterpret_cast<float*>(smem + L::kAmaxOff);
+  int32_t* s_tile = reinterpret_cast<int32_t*>(smem + L::kTableOff);
   int32_t* s_seg = s_tile + (p.nseg + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -201,6 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(acc_empty + b), kEpiWarps);
     }
     mbar_init(smem_u32(drain), 1);
+    for (int i = 0; i < 4; ++i) mbar_init(smem_u32(pair_bar + i), 2);
     s_issued[0] = s_issued[1] = 0u;
     for (int w = 0; w < kConvWarps; ++w) s_conv[w] = 0u;
     *s_abort = 0u;
@@ -211,8 +257,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   griddep_wait();
   griddep_launch();
   for (int i = threadIdx.x; i <= p.nseg; i += blockDim.x) {
-    s_tile[i] = p.tile_start[i];
+    if constexpr (!kSwap) s_tile[i] = p.tile_start[i];
     s_seg[i] = p.seg_off[i];
+  }
+  if constexpr (kSwap) {
+    // tiles of kTR rows per segment: a prefix over ceil(rows / kTR), one warp (lane l takes a
+    // run of consecutive segments)
+    __syncthreads();
+    if (warp == 0) {
+      const int per = (p.nseg + 31) / 32;
+      const int s0 = min(lane * per, p.nseg), s1 = min(s0 + per, p.nseg);
+      int c = 0;
+      for (int i = s0; i < s1; ++i) c += (max(s_seg[i + 1] - s_seg[i], 0) + kTR - 1) / kTR;
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      int off = incl - c;
+      for (int i = s0; i < s1; ++i) {
+        s_tile[i] = off;
+        off += (max(s_seg[i + 1] - s_seg[i], 0) + kTR - 1) / kTR;
+      }
+      if (lane == 31) s_tile[p.nseg] = incl;
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -235,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t rph = 0, sph = 0, n_raw = 0, n_sub = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
-        const TileW16 t = decode_tile_w16(item, n_tiles, s_tile, s_seg, p.nseg);
+        const TileW16 t = decode_tile_w16(item, n_tiles, s_tile, s_seg, p.nseg, kTR);
         const uint8_t* bsrc = p.b_tiles + (size_t)t.seg * p.b_per_seg +
                               (size_t)t.nt * kblk * kTileBlockBytes;
         for (int kb = 0; kb < kblk && ok; ++kb) {
@@ -255,8 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             const uint32_t fb = smem_u32(sub_full + ss);
-            mbar_arrive_expect_tx(fb, kTileBytes16);
-            tma_load_2d(smem0 + ss * kSubBytes, &tmap_a, kb * kBK + q * kSubK, t.m0, fb);
+            mbar_arrive_expect_tx(fb, kBoxBytes);
+            tma_load_2d(smem0 + ss * kSubBytes + kTokOff, &tmap_a, kb * kBK + q * kSubK, t.m0, fb);
             ++n_sub;
             if (++ss == kSubStages) { ss = 0; sph ^= 1u; }
           }
@@ -301,29 +370,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   : *reinterpret_cast<const uint32_t*>(
                                         raw + kTileBytes + q * 512 + (r & 31) * 16 + (r >> 5) * 4);
           const uint32_t cw[4] = {c0.x, c0.y, c0.z, c0.w};
-          uint8_t* brow = smem + ss * kSubBytes + kTileBytes16 + r * 128;
+          uint8_t* brow = smem + ss * kSubBytes + kWgtOff + r * 128;
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {      // 16-byte chunk j of the BF16 row: 8 values
             const int j = 4 * hf + jj;
-            const uint32_t w = cw[jj];
+            // elements 8j .. 8j+7 use NVFP4 block scale (8j) / 16 = j / 2, MXFP4 block j / 4
+            const uint32_t s2 = kMx ? e8m0_scale_bf16x2((sw >> (8 * (j >> 2))) & 0xFFu)
+                                    : e4m3_scale_bf16x2((sw >> (8 * (j >> 1))) & 0xFFu);
+            uint32_t q[4];
+            e2m1x8_to_bf16x2_scaled_down(cw[jj], q);
+            // (value * 2^-126) * 2^126 is the E2M1 value; times the scale the product has at
+            // most 6 significant bits: each multiplication is exact unless it underflows, as the
+            // FP32 product rounded to BF16 would be
             uint4 o;
-            if constexpr (kMx) {
-              // elements 8j .. 8j+7 use 32-block scale j / 4
-              const float sc = e8m0_to_f32((sw >> (8 * (j >> 2))) & 0xFFu);
-              o.x = e2m1x2_mx_bf16x2(w & 0xFFu, sc);
-              o.y = e2m1x2_mx_bf16x2((w >> 8) & 0xFFu, sc);
-              o.z = e2m1x2_mx_bf16x2((w >> 16) & 0xFFu, sc);
-              o.w = e2m1x2_mx_bf16x2(w >> 24, sc);
-            } else {
-              // elements 8j .. 8j+7 use block scale (8j) / 16 = j / 2
-              const uint32_t sb = (sw >> (8 * (j >> 1))) & 0xFFu;
-              const __half hs = __float2half_rn(e4m3_to_f32(sb));
-              const __half2 s2 = __halves2half2(hs, hs);
-              o.x = e2m1x2_scaled_bf16x2(w & 0xFFu, s2);
-              o.y = e2m1x2_scaled_bf16x2((w >> 8) & 0xFFu, s2);
-              o.z = e2m1x2_scaled_bf16x2((w >> 16) & 0xFFu, s2);
-              o.w = e2m1x2_scaled_bf16x2(w >> 24, s2);
-            }
+            o.x = mul_bf16x2(mul_bf16x2(q[0], kBf16x2Pow2_126), s2);
+            o.y = mul_bf16x2(mul_bf16x2(q[1], kBf16x2Pow2_126), s2);
+            o.z = mul_bf16x2(mul_bf16x2(q[2], kBf16x2Pow2_126), s2);
+            o.w = mul_bf16x2(mul_bf16x2(q[3], kBf16x2Pow2_126), s2);
             *reinterpret_cast<uint4*>(brow + ((j ^ (r & 7)) << 4)) = o;
           }
           fence_proxy_async_smem();     // the tensor core reads what these stores wrote
@@ -344,12 +407,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issue (one thread) ----------------
     if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc_bf16(kBM, kBN);
+      constexpr uint32_t idesc = kSwap ? make_idesc_bf16(128, kTR) : make_idesc_bf16(kBM, kBN);
       int ss = 0;
       uint32_t sph = 0;
       uint32_t acc_phase = 0u;   // bit b: the phase of accumulator buffer b
-      const uint64_t dA0 = smem_desc(smem0, 16, 1024, kLayoutSwizzle128B);
-      const uint64_t dB0 = smem_desc(smem0 + kTileBytes16, 16, 1024, kLayoutSwizzle128B);
+      // A: the token rows (or, kSwap, the decoded weights); B: the other tile of the sub-stage
+      const uint64_t dA0 = smem_desc(smem0 + (kSwap ? kWgtOff : kTokOff), 16, 1024,
+                                     kLayoutSwizzle128B);
+      const uint64_t dB0 = smem_desc(smem0 + (kSwap ? kTokOff : kWgtOff), 16, 1024,
+                                     kLayoutSwizzle128B);
       bool ok = true;
       int it = 0;
       const int nsub = kblk * (kBK / kSubK);
@@ -384,13 +450,145 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait_bounded(smem_u32(drain), 0u, kWaitLimitNs, p.status)) ok = false;
       if (!ok) *s_abort = 1u;
     }
+  } else if constexpr (kSwap) {
+    // ---------------- epilogue (warps 0-3), swapped: lane = weight row, column = token ----------
+    uint32_t acc_phase = 0u;   // bit b: the phase of accumulator buffer b
+    int it = 0;
+    const int r = warp * 32 + lane;
+    const bool lo = lane < 16;
+    for (int item = blockIdx.x; item < total; item += gridDim.x, ++it) {
+      const TileW16 t = decode_tile_w16(item, n_tiles, s_tile, s_seg, p.nseg, kTR);
+      const int abuf = it & 1;
+      const uint32_t acc_par = (acc_phase >> abuf) & 1u;
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(acc_full + abuf), acc_par,
+                                                     kWaitLimitNs, p.status))) {
+        if (lane == 0) *s_abort = 1u;
+        break;
+      }
+      acc_phase ^= 1u << abuf;
+      tc_fence_after();
+      uint32_t v[16];
+      tmem_ld_32x32b_x16(tmem_base + abuf * kBN + ((uint32_t)(warp * 32) << 16), v);
+      tmem_ld_wait();
+      // the accumulator is in registers: the buffer goes back before the stores
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(acc_empty + abuf));
+      const int nrow = min(t.rows, p.out_rows - t.m0);   // valid token columns 0 .. nrow-1
+      if (p.mode == 0) {
+        const bool gated = p.act != kActRelu2;
+        const int I = gated ? p.N / 2 : p.N;
+        const float ag = p.w_ts[t.seg * 4 + 0];
+        const float au = p.w_ts[t.seg * 4 + 1];
+        __nv_bfloat16* hb = reinterpret_cast<__nv_bfloat16*>(p.hb);
+        if (gated) {
+          // rows 32w .. 32w+15 are the gates and 32w+16 .. 32w+31 the ups of features
+          // 16w .. 16w+15 of the tile's 64: lane l takes tokens 8 (l / 16) .. +7 of feature
+          // l % 16 with its partner lane's half of the pair
+          const int j0 = lo ? 0 : 8;
+          const int f = t.nt * (kBN / 2) + warp * 16 + (lane & 15);
+          float h[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t got = __shfl_xor_sync(0xffffffffu, lo ? v[8 + j] : v[j], 16);
+            const float g = __uint_as_float(lo ? v[j] : got);
+            const float u = __uint_as_float(lo ? got : v[8 + j]);
+            h[j] = glu_activation(g * ag, u * au, p.act, p.swiglu_limit, p.swiglu_alpha);
+          }
+          if constexpr (kMx) {
+            // a 32-feature MXFP8 block spans warps 2i and 2i+1: the amax of each token over
+            // the warp's 16 features, then over the pair through shared memory
+            float am[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              am[j] = fabsf(h[j]);
+#pragma unroll
+              for (int o = 1; o < 16; o <<= 1)
+                am[j] = fmaxf(am[j], __shfl_xor_sync(0xffffffffu, am[j], o));
+            }
+            float* mine = s_amax + (abuf * kEpiWarps + warp) * 16;
+            if ((lane & 15) == 0)
+#pragma unroll
+              for (int j = 0; j < 8; ++j) mine[j0 + j] = am[j];
+            __syncwarp();
+            const uint32_t pb = smem_u32(pair_bar + (warp >> 1) * 2 + abuf);
+            if (lane == 0) mbar_arrive(pb);
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(pb, (uint32_t)(it >> 1) & 1u,
+                                                           kWaitLimitNs, p.status))) {
+              if (lane == 0) *s_abort = 1u;
+              break;
+            }
+            const float* other = s_amax + (abuf * kEpiWarps + (warp ^ 1)) * 16;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              if (j0 + j >= nrow) continue;
+              const size_t prow = (size_t)(t.m0 + j0 + j);
+              const uint32_t sb = mx_scale_byte(fmaxf(am[j], other[j0 + j]), 8);
+              const uint32_t code = f32_to_e4m3x2(mx_unscale(h[j], sb), 0.0f) & 0xFFu;
+              p.hq8[prow * I + f] = (uint8_t)code;
+              hb[prow * I + f] = __float2bfloat16_rn(e4m3x2_to_f32x2(code).x * e8m0_to_f32(sb));
+              if ((lane & 15) == 0 && (warp & 1) == 0) p.hsf8[prow * (I / 32) + f / 32] = (uint8_t)sb;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              if (j0 + j < nrow)
+                hb[(size_t)(t.m0 + j0 + j) * I + f] = __float2bfloat16_rn(h[j]);
+          }
+        } else {
+          // non-gated: row r is feature r of the tile's 128, 16 tokens per lane; a warp's 32
+          // features are one MXFP8 block
+          const int f = t.nt * kBN + r;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float hv = glu_activation(0.0f, __uint_as_float(v[j]) * au, p.act,
+                                            p.swiglu_limit, p.swiglu_alpha);
+            const size_t prow = (size_t)(t.m0 + j);
+            if constexpr (kMx) {
+              float am = fabsf(hv);
+#pragma unroll
+              for (int o = 1; o < 32; o <<= 1)
+                am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+              if (j >= nrow) continue;
+              const uint32_t sb = mx_scale_byte(am, 8);
+              const uint32_t code = f32_to_e4m3x2(mx_unscale(hv, sb), 0.0f) & 0xFFu;
+              p.hq8[prow * I + f] = (uint8_t)code;
+              hb[prow * I + f] = __float2bfloat16_rn(e4m3x2_to_f32x2(code).x * e8m0_to_f32(sb));
+              if (lane == 0) p.hsf8[prow * (I / 32) + f / 32] = (uint8_t)sb;
+            } else {
+              if (j < nrow) hb[prow * I + f] = __float2bfloat16_rn(hv);
+            }
+          }
+        }
+      } else {
+        // lane j < 16 fetches the token and router weight of the tile's row j
+        const float alpha = p.w_ts[t.seg * 4 + 2];
+        int tok = -1;
+        float wr = 0.0f;
+        if (lane < nrow) {
+          tok = __ldg(p.perm_src + t.m0 + lane);
+          wr = __ldg(p.perm_w + t.m0 + lane);
+          if (tok < 0 || tok >= p.y_rows) {
+            set_status(p.status, MOE_ERR_INVALID_ARG);
+            tok = -1;
+          }
+        }
+        float* ycol = p.yacc + t.nt * kBN + r;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int tj = __shfl_sync(0xffffffffu, tok, j);
+          const float wj = __shfl_sync(0xffffffffu, wr, j);
+          if (tj >= 0) atomicAdd(ycol + (size_t)tj * p.N, (__uint_as_float(v[j]) * alpha) * wj);
+        }
+      }
+    }
   } else {
     // ---------------- epilogue (warps 0-3): one accumulator row per thread ----------------
     uint32_t acc_phase = 0u;   // bit b: the phase of accumulator buffer b
     int it = 0;
     const int r = warp * 32 + lane;
     for (int item = blockIdx.x; item < total; item += gridDim.x, ++it) {
-      const TileW16 t = decode_tile_w16(item, n_tiles, s_tile, s_seg, p.nseg);
+      const TileW16 t = decode_tile_w16(item, n_tiles, s_tile, s_seg, p.nseg, kTR);
       const int abuf = it & 1;
       const uint32_t acc_par = (acc_phase >> abuf) & 1u;
       if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(acc_full + abuf), acc_par,
@@ -566,18 +764,24 @@ cudaError_t launch_grouped_gemm_w16(const GemmW16Args& a, cudaStream_t s) {
   auto encode = encode_fn_w16();
   if (!encode) return cudaErrorNotSupported;
   if (a.N % kBN != 0 || a.K % kBK != 0 || a.nseg < 1) return cudaErrorInvalidValue;
-  // expert-ordered BF16 rows [out_rows, K]; box = 64 elements (128 bytes) x 128 rows
+  // expert-ordered BF16 rows [out_rows, K]; box = 64 elements (128 bytes) x 128 rows (swapped:
+  // kDecodeTileRows rows)
   CUtensorMap tmap;
   const cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.out_rows};
   const cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kSubK, (cuuint32_t)kBM};
+  const cuuint32_t box[2] = {(cuuint32_t)kSubK, (cuuint32_t)(a.swap ? kDecodeTileRows : kBM)};
   const cuuint32_t estr[2] = {1, 1};
   if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.a_rows), dims,
              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  const size_t smem = kSmemBytes - 8 * 1027 + sizeof(int32_t) * 2 * ((size_t)a.nseg + 2);
-  auto kernel = a.mx ? grouped_gemm_w16_kernel<true> : grouped_gemm_w16_kernel<false>;
+  if (a.nseg + 2 > kMaxSegTable) return cudaErrorInvalidValue;
+  const size_t smem = (a.swap ? W16Layout<true>::kSmemFixed : W16Layout<false>::kSmemFixed) +
+                      sizeof(int32_t) * 2 * ((size_t)a.nseg + 2);
+  auto kernel = a.mx ? (a.swap ? grouped_gemm_w16_kernel<true, true>
+                               : grouped_gemm_w16_kernel<true, false>)
+                     : (a.swap ? grouped_gemm_w16_kernel<false, true>
+                               : grouped_gemm_w16_kernel<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;

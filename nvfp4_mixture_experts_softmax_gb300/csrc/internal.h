@@ -318,6 +318,10 @@ struct GemmW16Args {
   float* yacc;                // mode 1 out [y_rows, N]
   int out_rows, y_rows, max_items;
   int32_t* status;
+  // decode-sized batches: the decoded weights are the MMA's 128-row A operand and tiles of
+  // kDecodeTileRows expert-ordered token rows its N (the tile table is built in the kernel from
+  // seg_off; tile_start is not read); max_items then counts those tiles x N/128
+  int swap;
 };
 cudaError_t launch_grouped_gemm_w16(const GemmW16Args& a, cudaStream_t s);
 

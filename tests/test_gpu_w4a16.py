@@ -44,11 +44,12 @@ def assert_hb_close(gpu_bits, ref_bits):
     return frac
 
 
-def check_w4a16(moe, cs, T, activation="swiglu", limit=None, sample=None):
+def check_w4a16(moe, cs, T, activation="swiglu", limit=None, sample=None, logits=None):
     dev = "cuda"
     k = cs.top_k
     x = synth.gen_x(cs, T, device=dev)
-    logits = synth.gen_logits(cs, T, device=dev)
+    if logits is None:
+        logits = synth.gen_logits(cs, T, device=dev)
     wg, wu, wd = synth.gen_all_experts(cs, device=dev)
     sh = synth.gen_shared(cs, device=dev) if cs.shared_inter else None
     gated = activation != "relu2"
@@ -110,6 +111,25 @@ def test_w4a16_one_expert_many_tiles(moe):
     cs = synth.custom_config("w4a16_pop", 600, 256, 2, 1, 256, config_id=161)
     check_w4a16(moe, cs, 600)
 
+
+
+def test_w4a16_swapped_popular_expert(moe):
+    """Batches of at most 64 tokens take the swapped-operand GEMMs (16-row token tiles): one
+    expert holds all 64 tokens (four full tiles), the others a few rows each."""
+    cs = synth.custom_config("w4a16_dpop", 64, 512, 8, 2, 256, config_id=170)
+    lg = synth.gen_logits(cs, 64)
+    lg[:, 5] += 50.0
+    check_w4a16(moe, cs, 64, logits=lg.cuda())
+
+
+@pytest.mark.parametrize("activation,limit", [("swiglu", None), ("relu2", None),
+                                              ("swiglu_oai", 7.0)])
+def test_w4a16_swapped_every_expert_ragged(moe, activation, limit):
+    """k = E with 50 tokens: every expert and the shared one own four 16-row tiles, the last
+    one of two rows."""
+    cs = synth.custom_config("w4a16_dkes", 50, 512, 4, 4, 256, shared_inter=256,
+                             config_id=171)
+    check_w4a16(moe, cs, 50, activation, limit)
 
 def test_w4a16_prefill_size_sampled(moe):
     cs = synth.CONFIGS["prefill"]

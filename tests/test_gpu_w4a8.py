@@ -42,11 +42,12 @@ def assert_mx8_close(gc, gs, rc, rs):
     assert fs <= H_CODE_FRAC and ds.max() <= 1, f"h scales: {fs:.2e} differ, max step {ds.max()}"
 
 
-def check_w4a8(moe, cs, T, activation="swiglu", limit=None, sample=None):
+def check_w4a8(moe, cs, T, activation="swiglu", limit=None, sample=None, logits=None):
     dev = "cuda"
     k, E = cs.top_k, cs.experts
     x = synth.gen_x(cs, T, device=dev)
-    logits = synth.gen_logits(cs, T, device=dev)
+    if logits is None:
+        logits = synth.gen_logits(cs, T, device=dev)
     wg, wu, wd = synth.gen_all_experts(cs, device=dev)
     sh = synth.gen_shared(cs, device=dev) if cs.shared_inter else None
     gated = activation != "relu2"
@@ -131,6 +132,25 @@ def test_w4a8_shared_expert_and_activations(moe, activation, limit):
     cs = synth.custom_config("w4a8_sh", 300, 512, 16, 4, 256, shared_inter=256, config_id=162)
     check_w4a8(moe, cs, 300, activation, limit)
 
+
+
+def test_w4a8_swapped_popular_expert(moe):
+    """Batches of at most 64 tokens take the swapped-operand GEMMs (16-row token tiles): one
+    expert holds all 64 tokens (four full tiles), the others a few rows each."""
+    cs = synth.custom_config("w4a8_dpop", 64, 512, 8, 2, 256, config_id=172)
+    lg = synth.gen_logits(cs, 64)
+    lg[:, 5] += 50.0
+    check_w4a8(moe, cs, 64, logits=lg.cuda())
+
+
+@pytest.mark.parametrize("activation,limit", [("swiglu", None), ("relu2", None),
+                                              ("swiglu_oai", 7.0)])
+def test_w4a8_swapped_every_expert_ragged(moe, activation, limit):
+    """k = E with 50 tokens: every expert and the shared one own four 16-row tiles, the last
+    one of two rows."""
+    cs = synth.custom_config("w4a8_dkes", 50, 512, 4, 4, 256, shared_inter=256,
+                             config_id=173)
+    check_w4a8(moe, cs, 50, activation, limit)
 
 def test_w4a8_prefill_size_sampled(moe):
     cs = synth.CONFIGS["prefill"]
