@@ -131,12 +131,24 @@ __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
 constexpr uint32_t kBf16x2Pow2_126 = 0x7E807E80u;   // 2^126 in both halves
 constexpr uint32_t kBf16x2Pow2_120 = 0x7B807B80u;   // 2^120 in both halves
 
-// An E4M3 block scale as BF16x2 (exact): its seven magnitude bits shifted to the top of a BF16's
-// exponent-and-mantissa field are the scale times 2^-120 (subnormal E4M3 to subnormal BF16
-// likewise), and one multiplication by 2^120 restores it.
-__device__ __forceinline__ uint32_t e4m3_scale_bf16x2(uint32_t b) {
+constexpr uint32_t kBf16x2Pow2_118 = 0x7A807A80u;   // 2^118 in both halves
+
+// An E4M3 block scale times 2^118 as BF16x2 (exact; at most 448 * 2^118 < 2^127): its seven
+// magnitude bits shifted to the top of a BF16's exponent-and-mantissa field are the scale times
+// 2^-120 (subnormal E4M3 to subnormal BF16 likewise), then two multiplications by powers of two.
+// Times an E2M1 value placed at 2^-126 this gives the product times 2^-8, at least 2^-19: a
+// normal BF16, exact, and only a power of two away from the decoded weight.
+__device__ __forceinline__ uint32_t e4m3_scale_x2118_bf16x2(uint32_t b) {
   const uint32_t h = ((b & 0x7Fu) << 4) | ((b & 0x80u) << 8);
-  return mul_bf16x2(h | (h << 16), kBf16x2Pow2_120);
+  return mul_bf16x2(mul_bf16x2(h | (h << 16), kBf16x2Pow2_120), kBf16x2Pow2_118);
+}
+
+// NVFP4 weights sit in the BF16 tile times 2^-8; the epilogue's tensor scales take the 2^8 back
+// (a power of two: the FP32 accumulator is the exact-weight accumulator times 2^-8, bit for bit,
+// unless a product falls below 2^-118 into FP32's subnormal range).
+template <bool kMx>
+__device__ __forceinline__ float weight_tile_comp() {
+  return kMx ? 1.0f : 256.0f;
 }
 
 // An E8M0 block scale 2^(b - 127) as BF16x2: the byte is the BF16 exponent field (b = 0: the
@@ -208,8 +220,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kTokOff = L::kTokOff, kWgtOff = L::kWgtOff;
   constexpr int kRawStages = L::kRawStages, kSubBytes = L::kSubBytes, kRawOff = L::kRawOff;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  // the 1024-byte-aligned base, reached by pointer arithmetic on the shared array so that the
+  // compiler keeps the shared address space (shared loads and stores, not generic ones)
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   uint64_t* raw_full = bars;
   uint64_t* raw_empty = raw_full + kRawStages;
@@ -343,6 +356,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     int rs = 0, ss = 0;
     uint32_t rph = 0, sph = 0, n_arr = 0;
     bool ok = true;
+    // byte offsets of this thread's 16-byte code chunk 2q + hf of row r (stored at chunk ^ (r % 8))
+    uint32_t coff[kBK / kSubK];
+#pragma unroll
+    for (int q = 0; q < kBK / kSubK; ++q) coff[q] = r * 128 + (((2 * q + hf) ^ (r & 7)) << 4);
+    // NVFP4: the four E4M3 scales of the row's sub-stage q are one word of scale group q
+    const uint32_t soff = kTileBytes + (r & 31) * 16 + (r >> 5) * 4;
+    uint8_t* const wtile = smem + kWgtOff + r * 128;
     for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
       for (int kb = 0; kb < kblk && ok; ++kb) {
         // every lane waits; the decision is made together, so the warp never diverges
@@ -351,42 +371,60 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
+        // the thread's codes and scales of the whole block go to registers, and the block's
+        // slot is handed back before any of it is decoded
         const uint8_t* raw = smem + kRawOff + rs * kTileBlockBytes;
+        uint4 cq[kBK / kSubK];
+        uint32_t sq[kBK / kSubK];
+#pragma unroll
+        for (int q = 0; q < kBK / kSubK; ++q) {
+          cq[q] = *reinterpret_cast<const uint4*>(raw + coff[q]);
+          // MXFP4: E8M0 scale 2q + hf of the row's eight covers this chunk's 32 codes
+          sq[q] = kMx ? raw[kTileBytes + r * 8 + 2 * q + hf]
+                      : *reinterpret_cast<const uint32_t*>(raw + soff + q * 512);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(raw_empty + rs));
+        if (++rs == kRawStages) { rs = 0; rph ^= 1u; }
+#pragma unroll
         for (int q = 0; q < kBK / kSubK; ++q) {
           if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(sub_empty + ss), sph ^ 1u,
                                                          kWaitLimitNs, p.status))) {
             ok = false;
             break;
           }
-          // the 64 codes of sub-stage q are 16-byte chunks 2q and 2q+1 of the row (stored at
-          // chunk ^ (row % 8)); this warp decodes chunk 2q + hf (32 codes: output chunks
-          // 4hf .. 4hf+3 of the BF16 row); its four scales are one word of scale group q
-          const uint4 c0 = *reinterpret_cast<const uint4*>(raw + r * 128 +
-                                                           (((2 * q + hf) ^ (r & 7)) << 4));
-          // NVFP4: the four E4M3 scales of the sub-stage are one word of scale group q; MXFP4:
-          // its two E8M0 scales are bytes 2q, 2q+1 of the row's eight
-          const uint32_t sw = kMx ? (uint32_t)*reinterpret_cast<const uint16_t*>(
-                                        raw + kTileBytes + r * 8 + 2 * q)
-                                  : *reinterpret_cast<const uint32_t*>(
-                                        raw + kTileBytes + q * 512 + (r & 31) * 16 + (r >> 5) * 4);
-          const uint32_t cw[4] = {c0.x, c0.y, c0.z, c0.w};
-          uint8_t* brow = smem + ss * kSubBytes + kWgtOff + r * 128;
+          // the multipliers of the chunk's values (times 2^-126 after the bit placement):
+          // NVFP4: 16-blocks 2hf (16-byte output chunks 4hf, 4hf+1) and 2hf+1 (4hf+2, 4hf+3), each
+          // times 2^118, so the tile holds the weights times 2^-8 (restored in the epilogue);
+          // MXFP4: 2^126 and the one E8M0 scale of the chunk, applied one after the other
+          uint32_t m0, m1;
+          if constexpr (kMx) {
+            m0 = e8m0_scale_bf16x2(sq[q]);
+            m1 = m0;
+          } else {
+            m0 = e4m3_scale_x2118_bf16x2((sq[q] >> (16 * hf)) & 0xFFu);
+            m1 = e4m3_scale_x2118_bf16x2((sq[q] >> (16 * hf + 8)) & 0xFFu);
+          }
+          const uint32_t cw[4] = {cq[q].x, cq[q].y, cq[q].z, cq[q].w};
+          uint8_t* brow = wtile + ss * kSubBytes;
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {      // 16-byte chunk j of the BF16 row: 8 values
             const int j = 4 * hf + jj;
-            // elements 8j .. 8j+7 use NVFP4 block scale (8j) / 16 = j / 2, MXFP4 block j / 4
-            const uint32_t s2 = kMx ? e8m0_scale_bf16x2((sw >> (8 * (j >> 2))) & 0xFFu)
-                                    : e4m3_scale_bf16x2((sw >> (8 * (j >> 1))) & 0xFFu);
-            uint32_t q[4];
-            e2m1x8_to_bf16x2_scaled_down(cw[jj], q);
-            // (value * 2^-126) * 2^126 is the E2M1 value; times the scale the product has at
-            // most 6 significant bits: each multiplication is exact unless it underflows, as the
-            // FP32 product rounded to BF16 would be
+            const uint32_t m = jj < 2 ? m0 : m1;
+            uint32_t v[4];
+            e2m1x8_to_bf16x2_scaled_down(cw[jj], v);
             uint4 o;
-            o.x = mul_bf16x2(mul_bf16x2(q[0], kBf16x2Pow2_126), s2);
-            o.y = mul_bf16x2(mul_bf16x2(q[1], kBf16x2Pow2_126), s2);
-            o.z = mul_bf16x2(mul_bf16x2(q[2], kBf16x2Pow2_126), s2);
-            o.w = mul_bf16x2(mul_bf16x2(q[3], kBf16x2Pow2_126), s2);
+            if constexpr (kMx) {
+              o.x = mul_bf16x2(mul_bf16x2(v[0], kBf16x2Pow2_126), m);
+              o.y = mul_bf16x2(mul_bf16x2(v[1], kBf16x2Pow2_126), m);
+              o.z = mul_bf16x2(mul_bf16x2(v[2], kBf16x2Pow2_126), m);
+              o.w = mul_bf16x2(mul_bf16x2(v[3], kBf16x2Pow2_126), m);
+            } else {
+              o.x = mul_bf16x2(v[0], m);
+              o.y = mul_bf16x2(v[1], m);
+              o.z = mul_bf16x2(v[2], m);
+              o.w = mul_bf16x2(v[3], m);
+            }
             *reinterpret_cast<uint4*>(brow + ((j ^ (r & 7)) << 4)) = o;
           }
           fence_proxy_async_smem();     // the tensor core reads what these stores wrote
@@ -395,9 +433,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++n_arr;
           if (++ss == kSubStages) { ss = 0; sph ^= 1u; }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(raw_empty + rs));
-        if (++rs == kRawStages) { rs = 0; rph ^= 1u; }
       }
     }
     if (lane == 0) {
@@ -478,8 +513,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p.mode == 0) {
         const bool gated = p.act != kActRelu2;
         const int I = gated ? p.N / 2 : p.N;
-        const float ag = p.w_ts[t.seg * 4 + 0];
-        const float au = p.w_ts[t.seg * 4 + 1];
+        const float ag = p.w_ts[t.seg * 4 + 0] * weight_tile_comp<kMx>();
+        const float au = p.w_ts[t.seg * 4 + 1] * weight_tile_comp<kMx>();
         __nv_bfloat16* hb = reinterpret_cast<__nv_bfloat16*>(p.hb);
         if (gated) {
           // rows 32w .. 32w+15 are the gates and 32w+16 .. 32w+31 the ups of features
@@ -562,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         // lane j < 16 fetches the token and router weight of the tile's row j
-        const float alpha = p.w_ts[t.seg * 4 + 2];
+        const float alpha = p.w_ts[t.seg * 4 + 2] * weight_tile_comp<kMx>();
         int tok = -1;
         float wr = 0.0f;
         if (lane < nrow) {
@@ -604,8 +639,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p.mode == 0) {
         const bool gated = p.act != kActRelu2;
         const int I = gated ? p.N / 2 : p.N;
-        const float ag = p.w_ts[t.seg * 4 + 0];
-        const float au = p.w_ts[t.seg * 4 + 1];
+        const float ag = p.w_ts[t.seg * 4 + 0] * weight_tile_comp<kMx>();
+        const float au = p.w_ts[t.seg * 4 + 1] * weight_tile_comp<kMx>();
         float hk[16];   // W4A8, gated: the first 16 features of a 32-feature MXFP8 block
 #pragma unroll 1
         for (int c = 0; c < kBN / 32; ++c) {
@@ -673,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   packed[4 * i + 3]);
         }
       } else {
-        const float alpha = p.w_ts[t.seg * 4 + 2];
+        const float alpha = p.w_ts[t.seg * 4 + 2] * weight_tile_comp<kMx>();
         int tok = 0;
         float wr = 0.0f;
         bool ok_row = valid;
