@@ -299,16 +299,21 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
+// try_wait with an explicit suspend limit: a thread whose phase is not complete sleeps until the
+// phase completes or kTryWaitSuspendNs pass, instead of polling at the hardware's default
+// interval, so waiting warps leave the issue slots to the ones doing work.
+constexpr uint32_t kTryWaitSuspendNs = 1000000u;
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n"
       ".reg .pred p;\n"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       "selp.u32 %0, 1, 0, p;\n"
       "}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kTryWaitSuspendNs)
       : "memory");
   return ok != 0;
 }
@@ -354,21 +359,18 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 }
 
 // Waits for the phase with the given parity; gives up after `limit_ns` nanoseconds, records
-// MOE_ERR_DEVICE_TIMEOUT in the status word and returns false.  The clock is read only every
-// 1024 polls so that a wait which is about to succeed costs no more than the poll itself.
+// MOE_ERR_DEVICE_TIMEOUT in the status word and returns false.  A wait that succeeds at once costs
+// the poll alone; after that each poll sleeps until the phase completes or the suspend limit
+// passes, and the clock is read between polls.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                                   int32_t* status) {
-  uint64_t t0 = 0;
-  for (uint32_t i = 0;; ++i) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 1023u) == 1023u) {
-      const uint64_t now = global_timer_ns();
-      if (t0 == 0) {
-        t0 = now;
-      } else if (now - t0 > limit_ns) {
-        set_status(status, MOE_ERR_DEVICE_TIMEOUT);
-        return false;
-      }
+    if (global_timer_ns() - t0 > limit_ns) {
+      set_status(status, MOE_ERR_DEVICE_TIMEOUT);
+      return false;
     }
   }
 }
