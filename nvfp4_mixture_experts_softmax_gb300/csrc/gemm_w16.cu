@@ -48,24 +48,26 @@ constexpr int kMmaWarp = 5;
 constexpr int kConvWarp0 = 6;
 constexpr int kConvWarps = 8;   // two per 32-row slice of the tile: half a row each
 constexpr int kThreads = (kConvWarp0 + kConvWarps) * 32;
-constexpr int kSubStages = 4;                 // converted sub-stages (K = 64 each)
 constexpr int kSubK = 64;
 constexpr int kTileBytes16 = 128 * 128;       // 128 rows x 64 BF16
 constexpr uint32_t kTmemCols = 256;           // two 128-column accumulators
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int kMaxSegTable = 1027;            // s_tile + s_seg entries the layout reserves
 
-// Shared memory: kSubStages converted sub-stages (the 128 x 64 BF16 tile of the token rows and
-// the decoded weight tile; swapped: the weight tile and a 16-row token tile), a ring of raw
-// NVFP4 weight blocks as deep as the rest leaves room for (the weight stream's bytes in flight),
-// barriers, the swapped W4A8 amax exchange and the tile tables.
+// Shared memory: kSubStages converted sub-stages of K = 64 (the 128 x 64 BF16 tile of the token
+// rows and the decoded weight tile; swapped: the weight tile and a 16-row token tile), a ring of
+// raw NVFP4 weight blocks, barriers, the swapped W4A8 amax exchange and the tile tables.  The
+// swapped layout's sub-stages are as small as a raw block, and its ring holds eight of them: a
+// converted sub-stage waits for its MMA's completion before the converters may refill it, and
+// four did not cover that round trip.
 template <bool kSwap>
 struct W16Layout {
   static constexpr int kTokBytes = kSwap ? kSubK * kDecodeTileRows * 2 : kTileBytes16;
   static constexpr int kSubBytes = kTileBytes16 + kTokBytes;
   static constexpr int kWgtOff = kSwap ? 0 : kTileBytes16;   // within a sub-stage
   static constexpr int kTokOff = kSwap ? kTileBytes16 : 0;
-  static constexpr int kRawStages = kSwap ? 8 : 4;
+  static constexpr int kSubStages = kSwap ? 10 : 5;
+  static constexpr int kRawStages = kSwap ? 2 : 3;
   static constexpr int kRawOff = kSubStages * kSubBytes;
   static constexpr int kBarOff = kRawOff + kRawStages * kTileBlockBytes;
   static constexpr int kAmaxOff = kBarOff + 512;   // swapped W4A8 GEMM1: [2][kEpiWarps][16] FP32
@@ -219,6 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kBoxBytes = (uint32_t)kSubK * kTR * 2;      // one sub-stage's token box
   constexpr uint32_t kTokOff = L::kTokOff, kWgtOff = L::kWgtOff;
   constexpr int kRawStages = L::kRawStages, kSubBytes = L::kSubBytes, kRawOff = L::kRawOff;
+  constexpr int kSubStages = L::kSubStages;
   extern __shared__ uint8_t smem_raw[];
   // the 1024-byte-aligned base, reached by pointer arithmetic on the shared array so that the
   // compiler keeps the shared address space (shared loads and stores, not generic ones)
