@@ -512,7 +512,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(acc_empty + abuf));
-      const int nrow = min(t.rows, p.out_rows - t.m0);   // valid token columns 0 .. nrow-1
+      // valid token columns 0 .. nrow-1 (none if malformed segment offsets put the tile outside
+      // the expert-ordered rows)
+      const int nrow = t.m0 < 0 ? 0 : min(t.rows, p.out_rows - t.m0);
       if (p.mode == 0) {
         const bool gated = p.act != kActRelu2;
         const int I = gated ? p.N / 2 : p.N;
