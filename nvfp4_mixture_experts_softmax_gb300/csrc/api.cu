@@ -349,9 +349,10 @@ int run_core(const moe_config* cfg, int Hl, int Il, const void* wbuf, const void
                                           &hdr->status, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     const int nseg = E + shared;
-    // decode-sized batches: weights as the MMA's M operand, kDecodeTileRows token rows as its N
+    // decode-sized batches: weights as the MMA's M operand, kDecodeTileRows token rows as its N;
+    // otherwise 256-row token tiles (two 128-row MMA operands sharing each decoded weight tile)
     const bool swap = T <= kDecodeMaxRows;
-    const int tr = swap ? kDecodeTileRows : kBM;
+    const int tr = swap ? kDecodeTileRows : 2 * kBM;
     const int64_t mtiles = ((int64_t)L.Rt + (int64_t)nseg * (tr - 1)) / tr;
     GemmW16Args g{};
     g.a_rows = ws + L.xb_perm;

@@ -50,24 +50,27 @@ constexpr int kConvWarps = 8;   // two per 32-row slice of the tile: half a row 
 constexpr int kThreads = (kConvWarp0 + kConvWarps) * 32;
 constexpr int kSubK = 64;
 constexpr int kTileBytes16 = 128 * 128;       // 128 rows x 64 BF16
-constexpr uint32_t kTmemCols = 256;           // two 128-column accumulators
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int kMaxSegTable = 1027;            // s_tile + s_seg entries the layout reserves
 
-// Shared memory: kSubStages converted sub-stages of K = 64 (the 128 x 64 BF16 tile of the token
-// rows and the decoded weight tile; swapped: the weight tile and a 16-row token tile), a ring of
-// raw NVFP4 weight blocks, barriers, the swapped W4A8 amax exchange and the tile tables.  The
-// swapped layout's sub-stages are as small as a raw block, and its ring holds eight of them: a
-// converted sub-stage waits for its MMA's completion before the converters may refill it, and
-// four did not cover that round trip.
+// Shared memory: kSubStages converted sub-stages of K = 64 (the decoded weight tile and the
+// token rows: a 256-row tile, two 128-row MMA operands sharing the weight tile; swapped, a 16-row
+// tile), a ring of raw NVFP4 weight blocks, barriers, the swapped W4A8 amax exchange and the tile
+// tables.  A converted sub-stage waits for its MMAs' completion before the converters may refill
+// it, and four did not cover that round trip in the swapped layout, whose sub-stages are as small
+// as a raw block: it holds ten.
 template <bool kSwap>
 struct W16Layout {
-  static constexpr int kTokBytes = kSwap ? kSubK * kDecodeTileRows * 2 : kTileBytes16;
+  static constexpr int kTokRows = kSwap ? kDecodeTileRows : 2 * kBM;
+  static constexpr int kTokBytes = kSubK * kTokRows * 2;
   static constexpr int kSubBytes = kTileBytes16 + kTokBytes;
-  static constexpr int kWgtOff = kSwap ? 0 : kTileBytes16;   // within a sub-stage
+  static constexpr int kWgtOff = kSwap ? 0 : kTokBytes;   // within a sub-stage
   static constexpr int kTokOff = kSwap ? kTileBytes16 : 0;
-  static constexpr int kSubStages = kSwap ? 10 : 5;
-  static constexpr int kRawStages = kSwap ? 2 : 3;
+  static constexpr int kSubStages = kSwap ? 10 : 3;
+  static constexpr int kRawStages = 2;
+  // accumulator buffers: 128 rows x (swapped: up to 128 token columns; else two 128-column halves)
+  static constexpr uint32_t kAccCols = kSwap ? kBN : 2 * kBN;
+  static constexpr uint32_t kTmemCols = 2 * kAccCols;
   static constexpr int kRawOff = kSubStages * kSubBytes;
   static constexpr int kBarOff = kRawOff + kRawStages * kTileBlockBytes;
   static constexpr int kAmaxOff = kBarOff + 512;   // swapped W4A8 GEMM1: [2][kEpiWarps][16] FP32
@@ -217,11 +220,12 @@ template <bool kMx, bool kSwap>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_w16_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmW16Args p) {
   using L = W16Layout<kSwap>;
-  constexpr int kTR = kSwap ? kDecodeTileRows : kBM;            // token rows per tile
+  constexpr int kTR = L::kTokRows;                               // token rows per tile
   constexpr uint32_t kBoxBytes = (uint32_t)kSubK * kTR * 2;      // one sub-stage's token box
   constexpr uint32_t kTokOff = L::kTokOff, kWgtOff = L::kWgtOff;
   constexpr int kRawStages = L::kRawStages, kSubBytes = L::kSubBytes, kRawOff = L::kRawOff;
   constexpr int kSubStages = L::kSubStages;
+  constexpr uint32_t kAccCols = L::kAccCols, kTmemCols = L::kTmemCols;
   extern __shared__ uint8_t smem_raw[];
   // the 1024-byte-aligned base, reached by pointer arithmetic on the shared array so that the
   // compiler keeps the shared address space (shared loads and stores, not generic ones)
@@ -272,11 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_a) : "memory");
   griddep_wait();
   griddep_launch();
-  for (int i = threadIdx.x; i <= p.nseg; i += blockDim.x) {
-    if constexpr (!kSwap) s_tile[i] = p.tile_start[i];
-    s_seg[i] = p.seg_off[i];
-  }
-  if constexpr (kSwap) {
+  for (int i = threadIdx.x; i <= p.nseg; i += blockDim.x) s_seg[i] = p.seg_off[i];
+  {
     // tiles of kTR rows per segment: a prefix over ceil(rows / kTR), one warp (lane l takes a
     // run of consecutive segments)
     __syncthreads();
@@ -467,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         acc_phase ^= 1u << abuf;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + abuf * kBN;
+        const uint32_t d_tmem = tmem_base + abuf * kAccCols;
         for (int k = 0; k < nsub; ++k) {
           if (!mbar_wait_bounded(smem_u32(sub_full + ss), sph, kWaitLimitNs, p.status)) {
             ok = false;
@@ -476,9 +477,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint64_t so = (uint64_t)((uint32_t)(ss * kSubBytes) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < kSubK / 16; ++kk)   // K = 16 per MMA: 32 bytes -> 2 units
+          for (int kk = 0; kk < kSubK / 16; ++kk) {   // K = 16 per MMA: 32 bytes -> 2 units
             tc_mma_bf16(d_tmem, dA0 + so + kk * 2, dB0 + so + kk * 2, idesc,
                         (k | kk) != 0 ? 1u : 0u);
+            if constexpr (!kSwap)   // token rows 128-255 (16 KB further) into the second half
+              tc_mma_bf16(d_tmem + kBN, dA0 + so + (kTileBytes16 >> 4) + kk * 2, dB0 + so + kk * 2,
+                          idesc, (k | kk) != 0 ? 1u : 0u);
+          }
           tc_commit(smem_u32(sub_empty + ss));
           if (++ss == kSubStages) { ss = 0; sph ^= 1u; }
         }
@@ -506,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc_phase ^= 1u << abuf;
       tc_fence_after();
       uint32_t v[16];
-      tmem_ld_32x32b_x16(tmem_base + abuf * kBN + ((uint32_t)(warp * 32) << 16), v);
+      tmem_ld_32x32b_x16(tmem_base + abuf * kAccCols + ((uint32_t)(warp * 32) << 16), v);
       tmem_ld_wait();
       // the accumulator is in registers: the buffer goes back before the stores
       tc_fence_before();
@@ -638,106 +643,110 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       acc_phase ^= 1u << abuf;
       tc_fence_after();
-      const int prow = t.m0 + r;
-      const bool valid = r < t.rows && prow >= 0 && prow < p.out_rows;
-      const uint32_t tbase = tmem_base + abuf * kBN + ((uint32_t)(warp * 32) << 16);
-      if (p.mode == 0) {
-        const bool gated = p.act != kActRelu2;
-        const int I = gated ? p.N / 2 : p.N;
-        const float ag = p.w_ts[t.seg * 4 + 0] * weight_tile_comp<kMx>();
-        const float au = p.w_ts[t.seg * 4 + 1] * weight_tile_comp<kMx>();
-        float hk[16];   // W4A8, gated: the first 16 features of a 32-feature MXFP8 block
 #pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tbase + c * 32, v);
-          tmem_ld_wait();
-          if (!valid) continue;
-          if constexpr (kMx) {
-            float h32[32];
+      for (int half = 0; half < 2; ++half) {   // token rows 0-127, then 128-255 of the tile
+        const int prow = t.m0 + half * kBM + r;
+        const bool valid = half * kBM + r < t.rows && prow >= 0 && prow < p.out_rows;
+        const uint32_t tbase =
+            tmem_base + abuf * kAccCols + half * kBN + ((uint32_t)(warp * 32) << 16);
+        if (p.mode == 0) {
+          const bool gated = p.act != kActRelu2;
+          const int I = gated ? p.N / 2 : p.N;
+          const float ag = p.w_ts[t.seg * 4 + 0] * weight_tile_comp<kMx>();
+          const float au = p.w_ts[t.seg * 4 + 1] * weight_tile_comp<kMx>();
+          float hk[16];   // W4A8, gated: the first 16 features of a 32-feature MXFP8 block
+#pragma unroll 1
+          for (int c = 0; c < kBN / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tbase + c * 32, v);
+            tmem_ld_wait();
+            if (!valid) continue;
+            if constexpr (kMx) {
+              float h32[32];
+              if (gated) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                  const float hv = glu_activation(__uint_as_float(v[i]) * ag,
+                                                  __uint_as_float(v[16 + i]) * au, p.act,
+                                                  p.swiglu_limit, p.swiglu_alpha);
+                  if (c & 1) h32[16 + i] = hv;
+                  else hk[i] = hv;
+                }
+                if ((c & 1) == 0) continue;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) h32[i] = hk[i];
+              } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  h32[i] = glu_activation(0.0f, __uint_as_float(v[i]) * au, p.act, p.swiglu_limit,
+                                          p.swiglu_alpha);
+              }
+              const int f0 = gated ? t.nt * (kBN / 2) + (c - 1) * 16 : t.nt * kBN + c * 32;
+              mx8_requant_store(h32, p.hq8 + (size_t)prow * I + f0,
+                                p.hsf8 + (size_t)prow * (I / 32) + f0 / 32,
+                                p.hb + ((size_t)prow * I + f0) * 2);
+              continue;
+            }
+            // gated: (16 gate | 16 up) columns -> 16 features; non-gated: 32 up columns -> 32
+            uint32_t packed[16];
             if (gated) {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const float hv = glu_activation(__uint_as_float(v[i]) * ag,
-                                                __uint_as_float(v[16 + i]) * au, p.act,
+              for (int i = 0; i < 8; ++i) {
+                const float h0 = glu_activation(__uint_as_float(v[2 * i]) * ag,
+                                                __uint_as_float(v[16 + 2 * i]) * au, p.act,
                                                 p.swiglu_limit, p.swiglu_alpha);
-                if (c & 1) h32[16 + i] = hv;
-                else hk[i] = hv;
+                const float h1 = glu_activation(__uint_as_float(v[2 * i + 1]) * ag,
+                                                __uint_as_float(v[17 + 2 * i]) * au, p.act,
+                                                p.swiglu_limit, p.swiglu_alpha);
+                const __nv_bfloat162 b = __floats2bfloat162_rn(h0, h1);
+                packed[i] = *reinterpret_cast<const uint32_t*>(&b);
               }
-              if ((c & 1) == 0) continue;
-#pragma unroll
-              for (int i = 0; i < 16; ++i) h32[i] = hk[i];
             } else {
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
-                h32[i] = glu_activation(0.0f, __uint_as_float(v[i]) * au, p.act, p.swiglu_limit,
-                                        p.swiglu_alpha);
+              for (int i = 0; i < 16; ++i) {
+                const float h0 = glu_activation(0.0f, __uint_as_float(v[2 * i]) * au, p.act,
+                                                p.swiglu_limit, p.swiglu_alpha);
+                const float h1 = glu_activation(0.0f, __uint_as_float(v[2 * i + 1]) * au, p.act,
+                                                p.swiglu_limit, p.swiglu_alpha);
+                const __nv_bfloat162 b = __floats2bfloat162_rn(h0, h1);
+                packed[i] = *reinterpret_cast<const uint32_t*>(&b);
+              }
             }
-            const int f0 = gated ? t.nt * (kBN / 2) + (c - 1) * 16 : t.nt * kBN + c * 32;
-            mx8_requant_store(h32, p.hq8 + (size_t)prow * I + f0,
-                              p.hsf8 + (size_t)prow * (I / 32) + f0 / 32,
-                              p.hb + ((size_t)prow * I + f0) * 2);
-            continue;
+            const int f0 = gated ? t.nt * (kBN / 2) + c * 16 : t.nt * kBN + c * 32;
+            uint4* dst = reinterpret_cast<uint4*>(p.hb + ((size_t)prow * I + f0) * 2);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              if (i < (gated ? 2 : 4))
+                dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                    packed[4 * i + 3]);
           }
-          // gated: (16 gate | 16 up) columns -> 16 features; non-gated: 32 up columns -> 32
-          uint32_t packed[16];
-          if (gated) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float h0 = glu_activation(__uint_as_float(v[2 * i]) * ag,
-                                              __uint_as_float(v[16 + 2 * i]) * au, p.act,
-                                              p.swiglu_limit, p.swiglu_alpha);
-              const float h1 = glu_activation(__uint_as_float(v[2 * i + 1]) * ag,
-                                              __uint_as_float(v[17 + 2 * i]) * au, p.act,
-                                              p.swiglu_limit, p.swiglu_alpha);
-              const __nv_bfloat162 b = __floats2bfloat162_rn(h0, h1);
-              packed[i] = *reinterpret_cast<const uint32_t*>(&b);
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float h0 = glu_activation(0.0f, __uint_as_float(v[2 * i]) * au, p.act,
-                                              p.swiglu_limit, p.swiglu_alpha);
-              const float h1 = glu_activation(0.0f, __uint_as_float(v[2 * i + 1]) * au, p.act,
-                                              p.swiglu_limit, p.swiglu_alpha);
-              const __nv_bfloat162 b = __floats2bfloat162_rn(h0, h1);
-              packed[i] = *reinterpret_cast<const uint32_t*>(&b);
+        } else {
+          const float alpha = p.w_ts[t.seg * 4 + 2] * weight_tile_comp<kMx>();
+          int tok = 0;
+          float wr = 0.0f;
+          bool ok_row = valid;
+          if (valid) {
+            tok = __ldg(p.perm_src + prow);
+            wr = __ldg(p.perm_w + prow);
+            if (tok < 0 || tok >= p.y_rows) {
+              set_status(p.status, MOE_ERR_INVALID_ARG);
+              ok_row = false;
             }
           }
-          const int f0 = gated ? t.nt * (kBN / 2) + c * 16 : t.nt * kBN + c * 32;
-          uint4* dst = reinterpret_cast<uint4*>(p.hb + ((size_t)prow * I + f0) * 2);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            if (i < (gated ? 2 : 4))
-              dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
-                                  packed[4 * i + 3]);
-        }
-      } else {
-        const float alpha = p.w_ts[t.seg * 4 + 2] * weight_tile_comp<kMx>();
-        int tok = 0;
-        float wr = 0.0f;
-        bool ok_row = valid;
-        if (valid) {
-          tok = __ldg(p.perm_src + prow);
-          wr = __ldg(p.perm_w + prow);
-          if (tok < 0 || tok >= p.y_rows) {
-            set_status(p.status, MOE_ERR_INVALID_ARG);
-            ok_row = false;
-          }
-        }
-        float* yrow = p.yacc + (size_t)(ok_row ? tok : 0) * p.N + t.nt * kBN;
+          float* yrow = p.yacc + (size_t)(ok_row ? tok : 0) * p.N + t.nt * kBN;
 #pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tbase + c * 32, v);
-          tmem_ld_wait();
-          if (!ok_row) continue;
+          for (int c = 0; c < kBN / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tbase + c * 32, v);
+            tmem_ld_wait();
+            if (!ok_row) continue;
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            red_add_v4(yrow + c * 32 + 4 * i, (__uint_as_float(v[4 * i]) * alpha) * wr,
-                       (__uint_as_float(v[4 * i + 1]) * alpha) * wr,
-                       (__uint_as_float(v[4 * i + 2]) * alpha) * wr,
-                       (__uint_as_float(v[4 * i + 3]) * alpha) * wr);
+            for (int i = 0; i < 8; ++i)
+              red_add_v4(yrow + c * 32 + 4 * i, (__uint_as_float(v[4 * i]) * alpha) * wr,
+                         (__uint_as_float(v[4 * i + 1]) * alpha) * wr,
+                         (__uint_as_float(v[4 * i + 2]) * alpha) * wr,
+                         (__uint_as_float(v[4 * i + 3]) * alpha) * wr);
+          }
         }
       }
       tc_fence_before();
@@ -804,12 +813,13 @@ cudaError_t launch_grouped_gemm_w16(const GemmW16Args& a, cudaStream_t s) {
   auto encode = encode_fn_w16();
   if (!encode) return cudaErrorNotSupported;
   if (a.N % kBN != 0 || a.K % kBK != 0 || a.nseg < 1) return cudaErrorInvalidValue;
-  // expert-ordered BF16 rows [out_rows, K]; box = 64 elements (128 bytes) x 128 rows (swapped:
-  // kDecodeTileRows rows)
+  // expert-ordered BF16 rows [out_rows, K]; box = 64 elements (128 bytes) x the tile's token rows
+  // (256, or kDecodeTileRows swapped)
   CUtensorMap tmap;
   const cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.out_rows};
   const cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kSubK, (cuuint32_t)(a.swap ? kDecodeTileRows : kBM)};
+  const cuuint32_t box[2] = {(cuuint32_t)kSubK, (cuuint32_t)(a.swap ? W16Layout<true>::kTokRows
+                                                                    : W16Layout<false>::kTokRows)};
   const cuuint32_t estr[2] = {1, 1};
   if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.a_rows), dims,
              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
