@@ -8,25 +8,26 @@
 // decoded BF16 values feed the down projection).  Exact decoding keeps the layer's arithmetic
 // that of its definition: every product of two decoded operands is exact in FP32.
 //
-// Tiles are 128 expert-ordered rows (MMA M) x 128 weight rows (MMA N) on the 5th-generation
-// tensor cores (tcgen05.mma kind::f16, BF16 x BF16 -> FP32 in tensor memory), K in sub-stages of
+// Tiles are 256 expert-ordered token rows x 128 weight rows on the 5th-generation tensor cores
+// (tcgen05.mma kind::f16, BF16 x BF16 -> FP32 in tensor memory): each decoded weight tile is the
+// N = 128 operand of two M = 128 MMAs, one per 128-row half of the token tile, K in sub-stages of
 // 64.  Per K block of 256 the copy warp fetches the expert's packed NVFP4 weight block (18 KB,
 // the layout the FP4 GEMMs read) with one bulk copy into a raw ring, and per sub-stage one 2-D
-// TMA box (64 BF16 x 128 rows, 128-byte swizzle) of the expert-ordered activation rows.  The
+// TMA box (64 BF16 x 256 rows, 128-byte swizzle) of the expert-ordered activation rows.  The
 // converter warps decode the sub-stage's 64 E2M1 codes of each weight row with their block
 // scales into BF16 (e2m1 * scale has at most 6 significant bits and lies in [2^-10, 2688], so it
-// is exact in BF16) by placing the codes' bits into BF16 fields and two exact BF16
-// multiplications, with no per-element float conversion, and store the row into the sub-stage's
-// weight tile in the same 128-byte-swizzled K-major layout; the per-matrix FP32 tensor scale is
-// applied in the epilogue.  Batches of at most 64 tokens swap the operands: the decoded weight tile is the MMA's
+// is exact in BF16) by placing the codes' bits into BF16 fields and exact BF16 multiplications,
+// with no per-element float conversion, and store the row into the sub-stage's weight tile in the
+// same 128-byte-swizzled K-major layout; the per-matrix FP32 tensor scale is applied in the
+// epilogue.  Batches of at most 64 tokens swap the operands: the decoded weight tile is the MMA's
 // M = 128 and tiles of 16 expert-ordered token rows its N, so neither the MMA nor the token copies
-// carry the padding of a 128-row token tile (an active expert averages a few rows there); the
+// carry the padding of a large token tile (an active expert averages a few rows there); the
 // epilogue then holds one weight row per thread and one token per accumulator column.
-// Warps: 0-3 epilogue, 4 copies, 5 tensor-memory allocation + the MMA thread, 6-13
-// converters (two per weight row, each decoding half of the sub-stage's 64 codes: two converter
-// warps per scheduler hide the decode's dependent instruction chains; with one warp per
-// scheduler decoding whole rows the conversion took ~4x the sub-stage's MMA time).  Two
-// 128-column FP32 accumulators let the epilogue overlap the next tile.
+// Warps: 0-3 epilogue, 4 copies, 5 tensor-memory allocation + the MMA thread, 6-13 converters
+// (two per weight row, each decoding half of the sub-stage's 64 codes: two converter warps per
+// scheduler hide the decode's dependent instruction chains; with one warp per scheduler decoding
+// whole rows the conversion took ~4x the sub-stage's MMA time).  Two accumulator buffers (256
+// columns each, 128 swapped) let the epilogue overlap the next tile.
 //   GEMM1 epilogue: g, u (times their tensor scales) -> the activation -> h rounded to BF16
 //                   (row-major [rows, I], expert order: the next GEMM's A operand);
 //   GEMM2 epilogue: (acc * ts_down) * router weight, reduced into the token's FP32 output row.
