@@ -360,7 +360,6 @@ int run_core(const moe_config* cfg, int Hl, int Il, const void* wbuf, const void
     g.b_per_seg = W.w13_per_e;
     g.w_ts = reinterpret_cast<const float*>(wb + W.ts);
     g.seg_off = i32(L.seg_off);
-    g.tile_start = i32(L.tile_start);
     g.nseg = nseg;
     g.N = gemm1_rows(*cfg);
     g.K = H;

@@ -293,15 +293,15 @@ struct GemmArgs {
 };
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s);
 
-// The W4A16 layer (BF16 activations, NVFP4 weights decoded to BF16 in shared memory): one
-// grouped GEMM on kind::f16 tensor cores (gemm_w16.cu), 128 expert-ordered rows x 128 weight rows.
+// The W4A16 / W4A8 layers' grouped GEMM on kind::f16 tensor cores (gemm_w16.cu; weights decoded
+// to BF16 in shared memory): 256 expert-ordered token rows x 128 weight rows per tile, or, swapped,
+// 128 weight rows x 16 token rows.  Its tile table is built in the kernel from seg_off.
 struct GemmW16Args {
   const void* a_rows;         // A operand: BF16 rows [out_rows, K] in expert order
   const uint8_t* b_tiles;     // packed NVFP4 weight blocks (WeightLayout), expert s at s*b_per_seg
   size_t b_per_seg;
   const float* w_ts;          // [nseg][4] tensor scales
   const int32_t* seg_off;     // [nseg+1]
-  const int32_t* tile_start;  // [nseg+1] 128-row tiles
   int nseg;
   int N, K;
   int mode;                   // 0: activation, h to BF16 rows (hb [out_rows, I]); 1: router-
@@ -319,8 +319,8 @@ struct GemmW16Args {
   int out_rows, y_rows, max_items;
   int32_t* status;
   // decode-sized batches: the decoded weights are the MMA's 128-row A operand and tiles of
-  // kDecodeTileRows expert-ordered token rows its N (the tile table is built in the kernel from
-  // seg_off; tile_start is not read); max_items then counts those tiles x N/128
+  // kDecodeTileRows expert-ordered token rows its N; max_items counts the tiles of either layout
+  // x N/128
   int swap;
 };
 cudaError_t launch_grouped_gemm_w16(const GemmW16Args& a, cudaStream_t s);
