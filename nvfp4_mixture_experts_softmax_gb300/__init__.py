@@ -389,7 +389,7 @@ class MoeLayer:
 
     def __init__(self, cfg: MoeConfig, w_gate, w_up, w_down, shared=None, max_tokens=None):
         self.cfg = cfg
-        self.device = w_gate.device
+        self.device = w_up.device          # w_gate is None for non-gated (relu2) experts
         self.wbuf = quantize_weights(cfg, w_gate, w_up, w_down, shared)
         self._ws = None
         self._ws_T = -1
