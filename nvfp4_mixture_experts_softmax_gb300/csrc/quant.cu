@@ -6,6 +6,8 @@
 // Quantization": tensor scale max|x| / (6 * 448); block scales E4M3 over 16 elements, codes E2M1,
 // section "NVFP4 throughout"): ts = amax / 2688, sf = E4M3((block_max / 6) / ts), code =
 // E2M1(x / (decode(sf) * ts)), round to nearest even, IEEE FP32 division (no fast math).
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -705,7 +707,9 @@ cudaError_t launch_act_amax(const void* x, int64_t rows, int64_t cols, float* ts
                             uint32_t* partials, float* zero_buf, int64_t zero_floats,
                             cudaStream_t s, const float* ts_in) {
   const int64_t nvec = ts_in ? 0 : rows * cols / 8;
-  const int g1 = grid_for(ts_in ? zero_floats / 4 : nvec, kThreads * 8, kMaxAmaxBlocks);
+  // sized for the larger of the two jobs: a caller that only zero-fills (rows = 0) still gets a
+  // grid as wide as the fill
+  const int g1 = grid_for(std::max(nvec, zero_floats / 4), kThreads * 8, kMaxAmaxBlocks);
   return launch_pdl(act_amax_kernel, dim3(g1), dim3(kThreads), 0, s,
                     reinterpret_cast<const uint4*>(x), nvec, hdr, partials, ts,
                     reinterpret_cast<float4*>(zero_buf), zero_floats / 4, ts_in);
